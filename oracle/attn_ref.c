@@ -1,0 +1,263 @@
+/*
+ * CPU fp64 oracle for the attention forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may call, link or
+ * load this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline leg use it. It shares no code, header, table or helper with the
+ * CUDA library.
+ *
+ * Sources (the three web pages on FlashAttention):
+ *  - MUSA SDK programming guide, "FlashAttention 优化", section
+ *    "标准 Self-Attention 的问题 / 计算流程": Attention(Q,K,V) =
+ *    softmax(Q K^T / sqrt(d)) V computed as S = Q K^T, P = softmax(S), O = P V.
+ *  - same page, "online softmax / 标准 Softmax 回顾": the three-pass safe
+ *    softmax m = max(S), Z = sum exp(S - m), P = exp(S - m) / Z, and
+ *    "数值稳定性" (subtracting the row maximum).
+ *  - same page, "FlashAttention 完整算法", formula steps 1-4 and the flow
+ *    chart: the tiled recurrence over key blocks (m, l, O updated per block,
+ *    O divided by l at the end).
+ *
+ * Reading taken where the pages are silent: the scale is an argument applied
+ * to the dot product (s = scale * q.k); LSE = m + ln Z in natural log; row
+ * statistics are per row.
+ *
+ * Layouts: Q [BH, Nq, d], K and V [BH, Nk, d], O [BH, Nq, d], LSE [BH, Nq],
+ * all row-major fp64. Build: gcc -O2 (no -ffast-math), libm exp/log.
+ *
+ * ORACLE_MUTANT (compile-time, default 0) plants one deliberate mistake so
+ * the pin tests can show that each such mistake is caught. Mutant builds are
+ * made only by the tests, in a temporary directory.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+typedef struct {
+    const double *Q, *K, *V;
+    double *O, *LSE;
+    long BH, Nq, Nk, d;
+    double scale;
+    long row_begin, row_end; /* flattened (bh, i) rows */
+    /* online model */
+    long block_n;
+    double tau;
+    double *trace_m, *trace_l; /* [BH*Nq, nblocks] or NULL */
+    int ok;
+} job_t;
+
+/* s_j = scale * sum_k q_k * k_jk for one query row against all Nk keys. */
+static void scores_row(const double *q, const double *K, long Nk, long d, double scale, double *s)
+{
+    for (long j = 0; j < Nk; ++j) {
+        const double *kj = K + j * d;
+        double acc = 0.0;
+        for (long c = 0; c < d; ++c) {
+#if ORACLE_MUTANT == 1 /* wrong index: q's components shifted against k's */
+            acc += q[(c + 1) % d] * kj[c];
+#else
+            acc += q[c] * kj[c];
+#endif
+        }
+#if ORACLE_MUTANT == 2 /* scale dropped */
+        s[j] = acc;
+#else
+        s[j] = scale * acc;
+#endif
+    }
+}
+
+/* The three-pass definition for one row: max, normaliser, weighted sum. */
+static void three_pass_row(const double *s, const double *V, long Nk, long d, double *o, double *lse)
+{
+    double m = -INFINITY;
+    for (long j = 0; j < Nk; ++j)
+        if (s[j] > m) m = s[j];
+#if ORACLE_MUTANT == 3 /* max subtraction dropped */
+    m = 0.0;
+#endif
+    double Z = 0.0;
+    for (long j = 0; j < Nk; ++j) {
+#if ORACLE_MUTANT == 4 /* sign error in the exponent */
+        Z += exp(m - s[j]);
+#else
+        Z += exp(s[j] - m);
+#endif
+    }
+    for (long c = 0; c < d; ++c) o[c] = 0.0;
+    for (long j = 0; j < Nk; ++j) {
+#if ORACLE_MUTANT == 4
+        double p = exp(m - s[j]) / Z;
+#else
+        double p = exp(s[j] - m) / Z;
+#endif
+#if ORACLE_MUTANT == 5 /* off-by-one value row */
+        const double *vj = V + ((j + 1) % Nk) * d;
+#else
+        const double *vj = V + j * d;
+#endif
+        for (long c = 0; c < d; ++c) o[c] += p * vj[c];
+    }
+#if ORACLE_MUTANT == 6 /* max term dropped from the logsumexp */
+    *lse = log(Z);
+#else
+    *lse = m + log(Z);
+#endif
+}
+
+static void *three_pass_worker(void *arg)
+{
+    job_t *jb = (job_t *)arg;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(jb->Nk > 0 ? jb->Nk : 1));
+    if (!s) { jb->ok = 0; return NULL; }
+    for (long r = jb->row_begin; r < jb->row_end; ++r) {
+        long bh = r / jb->Nq;
+        const double *q = jb->Q + r * jb->d;
+        const double *K = jb->K + bh * jb->Nk * jb->d;
+        const double *V = jb->V + bh * jb->Nk * jb->d;
+#if ORACLE_MUTANT == 7 /* transposed score matrix: s_ij taken as q_j . k_i */
+        {
+            long i = r % jb->Nq;
+            const double *Qh = jb->Q + bh * jb->Nq * jb->d;
+            for (long j = 0; j < jb->Nk; ++j) {
+                const double *qj = Qh + (j % jb->Nq) * jb->d, *ki = K + (i % jb->Nk) * jb->d;
+                double acc = 0.0;
+                for (long c = 0; c < jb->d; ++c) acc += qj[c] * ki[c];
+                s[j] = jb->scale * acc;
+            }
+        }
+#else
+        scores_row(q, K, jb->Nk, jb->d, jb->scale, s);
+#endif
+        three_pass_row(s, V, jb->Nk, jb->d, jb->O + r * jb->d, jb->LSE + r);
+    }
+    free(s);
+    jb->ok = 1;
+    return NULL;
+}
+
+/*
+ * Online (tiled) model of the same result, one row at a time, in fp64:
+ * keys are taken in blocks of block_n. For each block the block row max is
+ * found, the running max m is replaced by max(m, block max) and the running
+ * denominator l and the unnormalised output o are multiplied by
+ * exp(m_old - m_new) before the block's exp(s - m) terms are added; at the
+ * end o is divided by l (formula steps 3a-3f and 4).
+ *
+ * tau >= 0 makes the replacement lazy: the reference max is only moved when
+ * the block max exceeds it by more than tau (natural-log units) or on the
+ * first block. tau = 0 is the pages' eager update. Because l and o always
+ * share one reference max, the final o / l and m + ln l are the same for
+ * every tau up to rounding.
+ */
+static void *online_worker(void *arg)
+{
+    job_t *jb = (job_t *)arg;
+    long nb = (jb->Nk + jb->block_n - 1) / jb->block_n;
+    double *s = (double *)malloc(sizeof(double) * (size_t)jb->block_n);
+    double *o = (double *)malloc(sizeof(double) * (size_t)jb->d);
+    if (!s || !o) { free(s); free(o); jb->ok = 0; return NULL; }
+    for (long r = jb->row_begin; r < jb->row_end; ++r) {
+        long bh = r / jb->Nq;
+        const double *q = jb->Q + r * jb->d;
+        const double *K = jb->K + bh * jb->Nk * jb->d;
+        const double *V = jb->V + bh * jb->Nk * jb->d;
+        double m = -INFINITY, l = 0.0;
+        for (long c = 0; c < jb->d; ++c) o[c] = 0.0;
+        for (long b = 0; b < nb; ++b) {
+            long j0 = b * jb->block_n;
+            long nj = jb->Nk - j0 < jb->block_n ? jb->Nk - j0 : jb->block_n;
+            scores_row(q, K + j0 * jb->d, nj, jb->d, jb->scale, s);
+            double mb = -INFINITY;
+            for (long j = 0; j < nj; ++j)
+                if (s[j] > mb) mb = s[j];
+            double m_new = mb > m ? mb : m;
+            if (b == 0 || m_new - m > jb->tau) {
+                double alpha = (b == 0) ? 0.0 : exp(m - m_new);
+                l *= alpha;
+                for (long c = 0; c < jb->d; ++c) o[c] *= alpha;
+                m = m_new;
+            }
+            for (long j = 0; j < nj; ++j) {
+                double p = exp(s[j] - m);
+                l += p;
+                const double *vj = V + (j0 + j) * jb->d;
+                for (long c = 0; c < jb->d; ++c) o[c] += p * vj[c];
+            }
+            if (jb->trace_m) {
+                jb->trace_m[r * nb + b] = m;
+                jb->trace_l[r * nb + b] = l;
+            }
+        }
+        for (long c = 0; c < jb->d; ++c) jb->O[r * jb->d + c] = o[c] / l;
+        jb->LSE[r] = m + log(l);
+    }
+    free(s);
+    free(o);
+    jb->ok = 1;
+    return NULL;
+}
+
+static int run_jobs(job_t *proto, void *(*fn)(void *), int nthreads)
+{
+    long rows = proto->BH * proto->Nq;
+    if (rows <= 0) return 0;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if ((long)nthreads > rows) nthreads = (int)rows;
+    job_t jobs[256];
+    pthread_t th[256];
+    int started[256];
+    long per = (rows + nthreads - 1) / nthreads;
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = *proto;
+        jobs[t].row_begin = t * per;
+        jobs[t].row_end = (t + 1) * per < rows ? (t + 1) * per : rows;
+        jobs[t].ok = 0;
+        started[t] = 0;
+        if (jobs[t].row_begin >= jobs[t].row_end) { jobs[t].ok = 1; continue; }
+        if (t > 0 && pthread_create(&th[t], NULL, fn, &jobs[t]) == 0) started[t] = 1;
+    }
+    if (jobs[0].row_begin < jobs[0].row_end) fn(&jobs[0]);
+    for (int t = 1; t < nthreads; ++t) {
+        if (started[t]) pthread_join(th[t], NULL);
+        else if (jobs[t].row_begin < jobs[t].row_end) fn(&jobs[t]); /* thread failed: run inline */
+    }
+    for (int t = 0; t < nthreads; ++t)
+        if (!jobs[t].ok) return -2;
+    return 0;
+}
+
+/* Three-pass definition. Returns 0, or -1 on bad sizes, -2 on allocation failure. */
+int oracle_attn_fp64(const double *Q, const double *K, const double *V, double *O, double *LSE,
+                     long BH, long Nq, long Nk, long d, double scale, int nthreads)
+{
+    if (BH < 0 || Nq < 0 || Nk < 1 || d < 1) return -1;
+    job_t p;
+    memset(&p, 0, sizeof p);
+    p.Q = Q; p.K = K; p.V = V; p.O = O; p.LSE = LSE;
+    p.BH = BH; p.Nq = Nq; p.Nk = Nk; p.d = d; p.scale = scale;
+    return run_jobs(&p, three_pass_worker, nthreads);
+}
+
+/* Online recurrence with key blocks of block_n and lazy threshold tau (natural log).
+ * trace_m / trace_l, if not NULL, receive m and l after every block:
+ * [BH*Nq, ceil(Nk/block_n)]. */
+int oracle_attn_online_fp64(const double *Q, const double *K, const double *V, double *O, double *LSE,
+                            long BH, long Nq, long Nk, long d, double scale, long block_n, double tau,
+                            double *trace_m, double *trace_l, int nthreads)
+{
+    if (BH < 0 || Nq < 0 || Nk < 1 || d < 1 || block_n < 1 || tau < 0) return -1;
+    job_t p;
+    memset(&p, 0, sizeof p);
+    p.Q = Q; p.K = K; p.V = V; p.O = O; p.LSE = LSE;
+    p.BH = BH; p.Nq = Nq; p.Nk = Nk; p.d = d; p.scale = scale;
+    p.block_n = block_n; p.tau = tau; p.trace_m = trace_m; p.trace_l = trace_l;
+    return run_jobs(&p, online_worker, nthreads);
+}
+
+int oracle_mutant_id(void) { return ORACLE_MUTANT; }

@@ -1,0 +1,195 @@
+"""Pins for the CPU oracle: checks against facts fixed by the pages and by mathematics.
+
+Each ``pin_*`` takes an oracle library handle and raises AssertionError when the
+oracle disagrees with something that does not depend on the oracle itself:
+hand-derived worked examples, closed forms, invariants, brute force on tiny
+inputs, and library routines (numpy/scipy) for the textbook special case.
+``tests/test_oracle.py`` runs them against the real oracle, and against
+builds with one planted mistake each, which must fail at least one pin.
+"""
+import itertools
+import math
+
+import numpy as np
+
+import oracle
+from golden_cases import all_cases
+
+RNG = np.random.default_rng(1234)
+
+
+def _attn(lib, q, k, v, scale=None, nthreads=2):
+    return oracle.attn(q, k, v, scale=scale, nthreads=nthreads, lib=lib)
+
+
+def pin_golden(lib):
+    """Hand-derived worked examples (tests/golden)."""
+    for c in all_cases():
+        o, lse = _attn(lib, c["Q"], c["K"], c["V"], scale=c["scale"])
+        np.testing.assert_allclose(o, c["O"], rtol=0, atol=c["tol"], err_msg=c["name"])
+        np.testing.assert_allclose(lse, c["LSE"], rtol=0, atol=c["tol"], err_msg=c["name"])
+
+
+def pin_brute_force(lib):
+    """Tiny inputs against sums of exp of the raw scores (no max shift), exact-summed."""
+    rng = np.random.default_rng(7)
+    for Nq, Nk, d in [(1, 1, 1), (2, 3, 2), (3, 4, 3), (4, 2, 5), (3, 3, 1)]:
+        q, k, v = (rng.standard_normal((n, d)) for n in (Nq, Nk, Nk))
+        scale = 0.7
+        o, lse = _attn(lib, q, k, v, scale=scale)
+        for i in range(Nq):
+            s = [scale * math.fsum(q[i, c] * k[j, c] for c in range(d)) for j in range(Nk)]
+            w = [math.exp(x) for x in s]
+            Z = math.fsum(w)
+            for c in range(d):
+                ref = math.fsum(w[j] * v[j, c] for j in range(Nk)) / Z
+                assert abs(o[i, c] - ref) <= 1e-13 * max(1.0, abs(ref)), (Nq, Nk, d, i, c)
+            assert abs(lse[i] - math.log(Z)) <= 1e-13 * max(1.0, abs(math.log(Z)))
+
+
+def pin_rows_sum_to_one(lib):
+    """With V = identity (Nk = d) the output rows are the softmax rows: >= 0, sum 1."""
+    for N, scale in [(8, 0.5), (33, 0.2), (64, 1.0 / 8)]:
+        q, k = RNG.standard_normal((2, 3, N, N)), RNG.standard_normal((2, 3, N, N))
+        v = np.broadcast_to(np.eye(N), (2, 3, N, N)).copy()
+        p, _ = _attn(lib, q, k, v, scale=scale)
+        assert np.all(p >= 0)
+        np.testing.assert_allclose(p.sum(-1), 1.0, rtol=0, atol=1e-12)
+
+
+def pin_zero_query(lib):
+    """Q = 0: every score is 0, P is uniform, O = column mean of V, LSE = ln Nk."""
+    for Nq, Nk, d in [(5, 7, 3), (4, 64, 16), (1, 129, 8)]:
+        q = np.zeros((Nq, d))
+        k, v = RNG.standard_normal((Nk, d)) * 3, RNG.standard_normal((Nk, d))
+        o, lse = _attn(lib, q, k, v, scale=0.3)
+        np.testing.assert_allclose(o, np.broadcast_to(v.mean(0), o.shape), rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse, math.log(Nk), rtol=0, atol=1e-13)
+
+
+def pin_identical_keys(lib):
+    """All keys equal: P is uniform, O = mean of V, LSE = scale q.k + ln Nk."""
+    Nq, Nk, d, scale = 6, 40, 5, 0.4
+    q = RNG.standard_normal((Nq, d))
+    key = RNG.standard_normal(d)
+    k = np.broadcast_to(key, (Nk, d)).copy()
+    v = RNG.standard_normal((Nk, d))
+    o, lse = _attn(lib, q, k, v, scale=scale)
+    np.testing.assert_allclose(o, np.broadcast_to(v.mean(0), o.shape), rtol=0, atol=1e-13)
+    expect = np.array([scale * math.fsum(q[i] * key) + math.log(Nk) for i in range(Nq)])
+    np.testing.assert_allclose(lse, expect, rtol=0, atol=1e-12)
+
+
+def pin_constant_v_column(lib):
+    """A V column that is constant c passes through as c (convex combination)."""
+    Nq, Nk, d = 9, 23, 4
+    q, k = RNG.standard_normal((Nq, d)) * 2, RNG.standard_normal((Nk, d)) * 2
+    v = RNG.standard_normal((Nk, d))
+    v[:, 2] = -3.25
+    o, _ = _attn(lib, q, k, v, scale=0.9)
+    np.testing.assert_allclose(o[:, 2], -3.25, rtol=1e-14, atol=0)
+
+
+def pin_shift_invariance(lib):
+    """K <- K + 1 w^T adds scale*q.w to a whole score row: O unchanged, LSE += scale*q.w."""
+    B, H, N, d, scale = 2, 2, 31, 6, 0.35
+    q, k, v = (RNG.standard_normal((B, H, N, d)) for _ in range(3))
+    w = RNG.standard_normal(d) * 2
+    o0, l0 = _attn(lib, q, k, v, scale=scale)
+    o1, l1 = _attn(lib, q, k + w, v, scale=scale)
+    np.testing.assert_allclose(o1, o0, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1, l0 + scale * (q @ w), rtol=0, atol=1e-12)
+
+
+def pin_permutation(lib):
+    """Joint K/V row permutation leaves O, LSE unchanged; a Q row permutation permutes them."""
+    N, d = 17, 5
+    q, k, v = (RNG.standard_normal((1, 2, N, d)) for _ in range(3))
+    o0, l0 = _attn(lib, q, k, v, scale=0.5)
+    pk = RNG.permutation(N)
+    o1, l1 = _attn(lib, q, k[:, :, pk], v[:, :, pk], scale=0.5)
+    np.testing.assert_allclose(o1, o0, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l0, rtol=0, atol=1e-13)
+    pq = RNG.permutation(N)
+    o2, l2 = _attn(lib, q[:, :, pq], k, v, scale=0.5)
+    np.testing.assert_allclose(o2, o0[:, :, pq], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l2, l0[:, :, pq], rtol=0, atol=1e-13)
+
+
+def pin_head_independence(lib):
+    """A batched call equals one call per (batch, head)."""
+    B, H, Nq, Nk, d = 2, 3, 7, 11, 4
+    q = RNG.standard_normal((B, H, Nq, d))
+    k, v = RNG.standard_normal((B, H, Nk, d)), RNG.standard_normal((B, H, Nk, d))
+    o, lse = _attn(lib, q, k, v, scale=0.6, nthreads=3)
+    for b, h in itertools.product(range(B), range(H)):
+        o1, l1 = _attn(lib, q[b, h], k[b, h], v[b, h], scale=0.6, nthreads=1)
+        np.testing.assert_array_equal(o[b, h], o1)
+        np.testing.assert_array_equal(lse[b, h], l1)
+
+
+def pin_hard_attention_limit(lib):
+    """Integer scores with a unique row max and scale 60: P is one-hot to < e^-60."""
+    Nq, Nk, d = 6, 9, 3
+    rng = np.random.default_rng(5)
+    while True:
+        q = rng.integers(-3, 4, (Nq, d)).astype(float)
+        k = rng.integers(-3, 4, (Nk, d)).astype(float)
+        s = q @ k.T
+        top = np.sort(s, axis=1)
+        if np.all(top[:, -1] - top[:, -2] >= 1):
+            break
+    v = rng.standard_normal((Nk, d))
+    o, lse = _attn(lib, q, k, v, scale=60.0)
+    np.testing.assert_allclose(o, v[s.argmax(1)], rtol=0, atol=1e-20 + 1e-24)
+    np.testing.assert_allclose(lse, 60.0 * s.max(1), rtol=1e-15, atol=1e-12)
+
+
+def pin_single_key(lib):
+    """Nk = 1: P = 1, O = v, LSE = s."""
+    q, k, v = RNG.standard_normal((5, 4)), RNG.standard_normal((1, 4)), RNG.standard_normal((1, 4))
+    o, lse = _attn(lib, q, k, v, scale=0.25)
+    np.testing.assert_array_equal(o, np.broadcast_to(v[0], o.shape))
+    np.testing.assert_allclose(lse, 0.25 * (q @ k[0]), rtol=0, atol=1e-14)
+
+
+def pin_linearity_in_v(lib):
+    """O is linear in V for fixed Q, K."""
+    Nq, Nk, d = 8, 19, 5
+    q, k = RNG.standard_normal((Nq, d)), RNG.standard_normal((Nk, d))
+    v1, v2 = RNG.standard_normal((Nk, d)), RNG.standard_normal((Nk, d))
+    o1, _ = _attn(lib, q, k, v1, scale=0.5)
+    o2, _ = _attn(lib, q, k, v2, scale=0.5)
+    o3, _ = _attn(lib, q, k, v1 - 2.5 * v2, scale=0.5)
+    np.testing.assert_allclose(o3, o1 - 2.5 * o2, rtol=0, atol=1e-12)
+
+
+def pin_library_reference(lib):
+    """Textbook special case through library routines: scipy softmax/logsumexp of q @ k.T."""
+    from scipy.special import logsumexp, softmax
+    for B, H, Nq, Nk, d in [(1, 2, 37, 53, 16), (2, 1, 64, 64, 64), (1, 1, 130, 257, 8)]:
+        q = RNG.standard_normal((B, H, Nq, d)) * 1.5
+        k, v = RNG.standard_normal((B, H, Nk, d)) * 1.5, RNG.standard_normal((B, H, Nk, d))
+        scale = 1.0 / math.sqrt(d)
+        s = np.einsum("bhid,bhjd->bhij", q, k) * scale
+        o_ref = np.einsum("bhij,bhjd->bhid", softmax(s, axis=-1), v)
+        o, lse = _attn(lib, q, k, v, scale=scale)
+        np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse, logsumexp(s, axis=-1), rtol=0, atol=1e-11)
+
+
+def pin_large_magnitude(lib):
+    """Scores of order +-1000 stay finite and obey the shift rule against a small copy."""
+    Nq, Nk, d = 4, 12, 3
+    q = RNG.standard_normal((Nq, d))
+    k = RNG.standard_normal((Nk, d))
+    v = RNG.standard_normal((Nk, d))
+    w = np.array([300.0, -200.0, 500.0])
+    o0, l0 = _attn(lib, q, k, v, scale=1.0)
+    o1, l1 = _attn(lib, q, k + w, v, scale=1.0)  # scores shift by q.w, several hundred
+    assert np.all(np.isfinite(o1)) and np.all(np.isfinite(l1))
+    np.testing.assert_allclose(o1, o0, rtol=0, atol=1e-10)
+    np.testing.assert_allclose(l1, l0 + q @ w, rtol=1e-14, atol=1e-10)
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
