@@ -1,0 +1,372 @@
+"""Benchmark: attention forward TFLOP/s (4*B*H*N^2*d) on GB300, one JSON line.
+
+A step is one forward pass over the whole workload (one kernel launch).
+Default workload: B=8, H=32, N=4096, d=128, bf16, Q and K ~ N(0, 3^2), V ~ N(0, 1)
+(the largest measured workload; the throughput target applies to N >= 4096, d=128).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gb300|reference]
+
+N > 1 runs one process per GPU under torch.distributed.run: every rank runs
+the full per-GPU workload (independent (batch, head) problems, no collective on
+the data path: weak scaling); the time is the max over ranks.
+
+The `reference` arm times the CPU fp64 oracle (a deliberately slow program) on
+a bounded sample of the same workload; it is a baseline, not a target.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "b8h32n4096d128_bf16_qk3"
+FALLBACK_TFLOPS = 1900.0  # bf16 dense burst measured once on a GB300 (used only if no measured file)
+KERNEL_SOURCES = ["exact_attention_87_gb300/csrc/fa_fwd_f16.cu", "exact_attention_87_gb300/csrc/sm103_ptx.cuh",
+                  "exact_attention_87_gb300/csrc/fa_device_common.cuh"]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return float(m["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)", m
+    except Exception:
+        return FALLBACK_TFLOPS, "fallback", {}
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """dram read+write bytes per launch from the committed ncu summary, if it
+    was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        ent = rec.get(workload)
+        if ent and ent.get("kernel_hash") == kernel_hash():
+            return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock / throttle reasons while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            if self.t:
+                self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable: nvidia-smi gave no samples"]}
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest `value` over all ranks (the job's time is its slowest rank's)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world_size: int, flops_per_rank: float, ms_per_step_max: float) -> float:
+    """Whole-job TFLOP/s under weak scaling: every rank does the full per-GPU
+    workload each step; the step takes as long as the slowest rank."""
+    return world_size * flops_per_rank / (ms_per_step_max * 1e-3) / 1e12
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_oracle_sample(w, q, k, v, seconds: float, max_heads: int | None = None):
+    """Time the oracle on whole heads of the workload until about `seconds` pass.
+    Returns (flops done, wall seconds, threads, description)."""
+    import oracle
+    threads = oracle.default_threads()
+    flops, t_total, heads = 0, 0.0, 0
+    per_head = 4 * w.N * w.N * w.d
+    bh = [(b, h) for b in range(w.B) for h in range(w.H)]
+    for (b, h) in bh:
+        t0 = time.perf_counter()
+        oracle.attn(q[b, h], k[b, h], v[b, h], scale=w.scale, nthreads=threads)
+        t_total += time.perf_counter() - t0
+        flops += per_head
+        heads += 1
+        if t_total >= seconds or (max_heads and heads >= max_heads):
+            break
+    return flops, t_total, threads, f"{heads} of {w.B * w.H} heads (all {w.N} rows each, fp64 three-pass)"
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline budget")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override B (smaller captures of the same workload for profiling; not a bench line)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    import dataclasses
+    from workloads import WORKLOADS, make_inputs
+    w = WORKLOADS[args.workload]
+    if args.batch is not None:
+        w = dataclasses.replace(w, B=args.batch, name=f"{w.name}[B={args.batch}]")
+    ws, rank, local = dist_env()
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype, "sigma_qk": w.sigma_qk,
+           "sigma_v": w.sigma_v, "scale": "1/sqrt(d)", "causal": False,
+           "l2": "inputs larger than L2 (no flush)" if 3 * w.B * w.H * w.N * w.d * 2 > 129e6 else "inputs fit in L2: warm, not flushed"}
+
+    if args.impl == "reference":
+        return run_reference(args, w, cfg, ws, rank)
+
+    import torch
+    import torch.distributed as dist
+    import exact_attention_87_gb300 as fa
+
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fa.build()
+    fa.lib()
+
+    q, k, v = make_inputs(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.attention(qd, kd, vd, scale=w.scale, out=o, lse=lse, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.fa_get_device_status() != fa.FA_OK:
+        raise RuntimeError("device status error after warm-up")
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    with sampler:
+        barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        barrier()
+    ms_total = max_over_ranks(e0.elapsed_time(e1), dev)
+    ms = ms_total / args.steps
+    st = fa.fa_get_device_status()
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status {st} after the timed region")
+    tflops = job_throughput(ws, w.flops, ms)
+
+    # ---- e2e: public API with host buffers, copies inside the timed region ----
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        ho = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+        hl = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            qd.copy_(hq, non_blocking=True)
+            kd.copy_(hk, non_blocking=True)
+            vd.copy_(hv, non_blocking=True)
+            fa.attention(qd, kd, vd, scale=w.scale, out=o, lse=lse, stream=stream)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        n_e2e = max(3, min(args.steps, 10))
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        a1.record(stream)
+        barrier()
+        e_ms = max_over_ranks(a0.elapsed_time(a1), dev) / n_e2e
+        h2d = (hq.numel() + hk.numel() + hv.numel()) * hq.element_size()
+        d2h = ho.numel() * ho.element_size() + hl.numel() * 4
+        e2e = {"value": round(job_throughput(ws, w.flops, e_ms), 2), "unit": "TFLOP/s", "ms_per_step": round(e_ms, 4),
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "path": "pinned host -> cudaMemcpyAsync -> fa_fwd -> cudaMemcpyAsync -> pinned host"}
+
+    if rank != 0:
+        if ws > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    peak, peak_src, _ = peaks()
+    achieved = w.flops / (ms * 1e-3) / 1e12
+    traffic = recorded_traffic(w.name)
+    line = {
+        "metric": "attention fwd TFLOP/s (4*B*H*N^2*d) and % of GB300 dense BF16 tensor peak",
+        "value": round(tflops, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic (seeded, generated on the host)",
+        "config": cfg,
+        "pct_of_peak": round(100.0 * achieved / peak, 2),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                     "kernel": f"fa_fwd_f16_kernel<{w.d},{'bf16' if w.dtype == 'bf16' else 'f16'}>",
+                     "traffic": traffic, "algorithmic_bytes": w.hbm_bytes},
+        "clocks": sampler.summary(),
+        "gpu_launches": args.steps,
+        "e2e": e2e,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        flops, secs, threads, desc = run_oracle_sample(w, q, k, v, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+                                "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_reference(args, w, cfg, ws, rank):
+    """The oracle, as it stands, on host cores: each step is a bounded sample of the workload."""
+    if rank != 0:
+        return
+    from workloads import make_inputs
+    import oracle
+    q, k, v = make_inputs(w)
+    threads = oracle.default_threads()
+    # size one step: whole heads, about 2 s of CPU work each at most, one head at least
+    t0 = time.perf_counter()
+    oracle.attn(q[0, 0, :64], k[0, 0], v[0, 0], scale=w.scale, nthreads=threads)
+    per_row = (time.perf_counter() - t0) / 64
+    rows = int(max(64, min(w.N, 1.5 / max(per_row, 1e-9))))
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+
+    def step(i):
+        b, h = heads[i % len(heads)]
+        oracle.attn(q[b, h, :rows], k[b, h], v[b, h], scale=w.scale, nthreads=threads)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    secs = time.perf_counter() - t0
+    flops = args.steps * 4 * rows * w.N * w.d
+    value = flops / secs / 1e12
+    ms = secs / args.steps * 1e3
+    desc = f"per step {rows} query rows of one (b, h) against all {w.N} keys (fp64 three-pass)"
+    line = {
+        "metric": "attention fwd TFLOP/s (4*B*H*N^2*d) and % of GB300 dense BF16 tensor peak",
+        "impl": "reference", "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)", "config": cfg,
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

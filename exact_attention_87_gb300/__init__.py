@@ -1,0 +1,136 @@
+"""GB300 (sm_103a) FlashAttention forward pass.
+
+Python binding of the C ABI in ``include/fa.h``: argument marshalling only.
+Every step of the computation runs in the library's CUDA kernels; there is no
+CPU fallback. If the compiled library is missing, every call raises.
+
+    import exact_attention_87_gb300 as fa
+    O, LSE = fa.attention(q, k, v)          # q, k, v: [B, H, N, d] CUDA tensors
+
+``fa_fwd`` / ``fa_get_device_status`` / ``fa_strerror`` / ``fa_abi_version``
+are the C entry points under the same names (pointers as Python ints).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from ._build import LIB_PATH, build
+
+FA_F32, FA_F16, FA_BF16 = 0, 1, 2
+FA_OK = 0
+STATUS_NAMES = {
+    0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_DTYPE", 3: "FA_ERR_SHAPE", 4: "FA_ERR_HEADDIM",
+    5: "FA_ERR_ALIGN", 6: "FA_ERR_CUDA", 7: "FA_ERR_DEVICE_TIMEOUT", 8: "FA_ERR_ARCH", 9: "FA_ERR_SCALE",
+}
+for _code, _name in STATUS_NAMES.items():
+    globals()[_name] = _code
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, where: str = "fa_fwd"):
+        self.code = code
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)} ({fa_strerror(code)})")
+
+
+_lib = None
+
+
+def lib(path: str | None = None):
+    """The loaded C library. Raises if it has not been built (no fallback)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: build it with exact_attention_87_gb300._build.build() "
+            "(nvcc for sm_103a); this package has no CPU fallback")
+    L = ctypes.CDLL(path)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    L.fa_fwd.restype = i
+    L.fa_get_device_status.argtypes = [vp]
+    L.fa_get_device_status.restype = i
+    L.fa_strerror.argtypes = [i]
+    L.fa_strerror.restype = ctypes.c_char_p
+    L.fa_abi_version.argtypes = []
+    L.fa_abi_version.restype = i
+    if path == LIB_PATH:
+        _lib = L
+    return L
+
+
+# ---- C entry points, same names ----
+
+def fa_fwd(Q, K, V, O, LSE, B, H, N, d, scale, dtype, stream=None) -> int:
+    return lib().fa_fwd(Q, K, V, O, LSE, B, H, N, d, scale, dtype, stream)
+
+
+def fa_get_device_status(stream=None) -> int:
+    return lib().fa_get_device_status(stream)
+
+
+def fa_strerror(code: int) -> str:
+    try:
+        return lib().fa_strerror(code).decode()
+    except ImportError:
+        return "library not loaded"
+
+
+def fa_abi_version() -> int:
+    return lib().fa_abi_version()
+
+
+# ---- torch convenience wrapper (memory and streams only) ----
+
+def _dtype_code(t):
+    import torch
+    codes = {torch.float32: FA_F32, torch.float16: FA_F16, torch.bfloat16: FA_BF16}
+    if t.dtype not in codes:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return codes[t.dtype]
+
+
+def attention(q, k, v, scale: float | None = None, out=None, lse=None, stream=None):
+    """O, LSE for q, k, v of shape [B, H, N, d] (contiguous CUDA tensors, same dtype).
+
+    Returns O (same dtype as q) and LSE (fp32 [B, H, N], natural log). ``out`` and
+    ``lse`` may be preallocated; ``stream`` defaults to torch's current stream.
+    """
+    import torch
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError(f"q, k, v must share one [B, H, N, d] shape: {q.shape} {k.shape} {v.shape}")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous ([B, H, N, d] row-major)")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor like q")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    with torch.cuda.device(q.device):
+        rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                    B, H, N, d, float(scale), _dtype_code(q), stream)
+    if rc != FA_OK:
+        raise FAError(rc)
+    return out, lse
+
+
+__all__ = ["attention", "fa_fwd", "fa_get_device_status", "fa_strerror", "fa_abi_version", "build", "lib",
+           "FAError", "FA_F32", "FA_F16", "FA_BF16", "FA_OK"]

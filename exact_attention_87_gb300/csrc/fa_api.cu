@@ -1,0 +1,181 @@
+// fa_api.cu — host side of the C ABI declared in include/fa.h: argument
+// validation, per-device checks, TMA descriptor encoding and kernel launch.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+// Device status word of this module: [0] flags (kStatusTimeout), [1] where the
+// first timeout happened. Kernels receive its address as a parameter.
+__device__ unsigned int g_fa_status[2];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool probed = false;
+  bool is_sm103 = false;
+  int num_sms = 0;
+  unsigned int* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+long long g_wait_limit = 0;
+
+long long wait_limit_cycles() {
+  if (g_wait_limit == 0) {
+    long long v = 1ll << 32;  // ~2 s at GB300 clocks
+    if (const char* e = std::getenv("FA_WAIT_LIMIT_CYCLES")) {
+      long long x = std::atoll(e);
+      if (x > 0) v = x;
+    }
+    g_wait_limit = v;
+  }
+  return g_wait_limit;
+}
+
+// Per-device facts, probed once under the lock. Returns FA_OK / FA_ERR_ARCH / FA_ERR_CUDA.
+int device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.probed) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    d.is_sm103 = (major == 10 && minor == 3);
+    d.num_sms = sms;
+    if (d.is_sm103) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_fa_status) != cudaSuccess) return FA_ERR_CUDA;
+      d.status = static_cast<unsigned int*>(p);
+    }
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return FA_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.probed = true;
+  }
+  *out = d;
+  return d.is_sm103 ? FA_OK : FA_ERR_ARCH;
+}
+
+// [B*H, N, d] tensor of 16-bit elements, boxes of 64 (d) x 128 (rows), 128-byte swizzle.
+bool encode_bhnd_16bit(CUtensorMap* map, const void* ptr, int BH, int N, int d, CUtensorMapDataType dt) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int fa_abi_version(void) { return 100; }
+
+const char* fa_strerror(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_NULL: return "a required pointer is NULL";
+    case FA_ERR_DTYPE: return "dtype must be FA_F32, FA_F16 or FA_BF16";
+    case FA_ERR_SHAPE: return "B, H and N must be >= 1 and B*H*N*d must stay below 2^40 elements";
+    case FA_ERR_HEADDIM: return "head dimension d must be 64 or 128";
+    case FA_ERR_ALIGN: return "Q, K, V and O must be 16-byte aligned and LSE 4-byte aligned";
+    case FA_ERR_CUDA: return "a CUDA call failed";
+    case FA_ERR_DEVICE_TIMEOUT: return "a kernel timed out waiting on an internal pipeline barrier";
+    case FA_ERR_ARCH: return "the current device is not sm_103 (GB300)";
+    case FA_ERR_SCALE: return "scale must be finite and > 0";
+    default: return "unknown status";
+  }
+}
+
+int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, float scale,
+           int dtype, void* stream) {
+  if (!Q || !K || !V || !O || !LSE) return FA_ERR_NULL;
+  if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > 0x7fffffffLL || BH * N > (1ll << 40) / d) return FA_ERR_SHAPE;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
+      (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0)
+    return FA_ERR_ALIGN;
+
+  DeviceInfo dev;
+  int st = device_info(&dev);
+  if (st != FA_OK) return st;
+
+  fa::FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = Q;
+  p.k = K;
+  p.v = V;
+  p.o = O;
+  p.lse = LSE;
+  p.status = dev.status;
+  p.wait_limit = wait_limit_cycles();
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.d = d;
+  p.scale = scale;
+  p.num_sms = dev.num_sms;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  cudaError_t e;
+  if (dtype == FA_F32) {
+    e = fa::launch_fwd_f32(p, s);
+  } else {
+    const CUtensorMapDataType dt =
+        dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const int bh = static_cast<int>(BH);
+    if (!encode_bhnd_16bit(&p.tm_q, Q, bh, N, d, dt) || !encode_bhnd_16bit(&p.tm_k, K, bh, N, d, dt) ||
+        !encode_bhnd_16bit(&p.tm_v, V, bh, N, d, dt) || !encode_bhnd_16bit(&p.tm_o, O, bh, N, d, dt))
+      return FA_ERR_CUDA;
+    e = fa::launch_fwd_f16(p, dtype == FA_BF16, s);
+  }
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_get_device_status(void* stream) {
+  DeviceInfo dev;
+  int st = device_info(&dev);
+  if (st != FA_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned int h[2] = {0, 0};
+  if (cudaMemcpyFromSymbol(h, g_fa_status, sizeof(h)) != cudaSuccess) return FA_ERR_CUDA;
+  if (h[0] == 0) return FA_OK;
+  const unsigned int zero[2] = {0, 0};
+  if (cudaMemcpyToSymbol(g_fa_status, zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_ERR_DEVICE_TIMEOUT;
+}
+
+}  // extern "C"

@@ -1,0 +1,470 @@
+// fa_fwd_f16.cu — FlashAttention forward for fp16 / bf16 on sm_103a.
+//
+// Algorithm: the tiled online-softmax recurrence of the MUSA SDK guide
+// ("FlashAttention 优化", "FlashAttention 完整算法", formula steps 1-4 and the
+// flow chart): a Q tile stays resident, K/V tiles stream past it, for each
+// tile S = Q K^T, the running row max m and denominator l are updated, O is
+// rescaled by exp(m_old - m_new) before the new P V is added (the dataflow
+// page, section 2.3, stresses that order), and O is divided by l at the end.
+// The loop order (Q outer, K/V inner, Q loaded once) is the dataflow page's
+// section 2.2; the parallelisation over Q tiles is the guide's FlashAttention-2
+// "sequence parallelism" note.
+//
+// GB300 mapping (one CTA per (batch*head, 256-row Q block), 12 warps):
+//   warp 9      TMA producer: Q0/Q1 once, then K_j and V_j into 2-3 stage rings
+//   warp 8      MMA issuer:   S_i = Q_i K_j^T (SS, into TMEM), O_i += P_i V_j
+//                             (TS: P read from TMEM, V from SMEM); also owns TMEM
+//   warps 0-3   softmax for Q rows 0-127   (thread = row; TMEM lanes = rows)
+//   warps 4-7   softmax for Q rows 128-255
+//   warps 10-11 idle (complete the third warpgroup for the register split)
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [256+d, 256+2d).
+// P_i (16-bit, packed in pairs) overwrites the first 64 columns of S_i.
+// The rescale of O is lazy: the reference max only moves when the tile max
+// exceeds it by more than 8 (log2 units), so P <= 256 and rescales are rare.
+// The epilogue divides by l, rounds to the input type, stages the tile in the
+// (now unused) Q buffer in the TMA 128-byte swizzle layout and TMA-stores it;
+// LSE = ln2 * (m + log2 l) is written per row.
+#include <atomic>
+
+#include "fa_device_common.cuh"
+
+namespace fa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8
+
+template <int D>
+struct Cfg {
+  static constexpr int BM = 128;  // Q rows per sub-tile (= TMEM lanes)
+  static constexpr int BN = 128;  // keys per K/V tile
+  static constexpr int STAGES = (D == 128) ? 2 : 3;
+  static constexpr uint32_t ROW_BYTES = 128;               // one 128-byte swizzle row = 64 elements
+  static constexpr uint32_t Q_SUB_BYTES = BM * D * 2;      // one Q sub-tile
+  static constexpr uint32_t Q_HALF_BYTES = BM * ROW_BYTES; // 64 columns of a Q sub-tile
+  static constexpr uint32_t KV_BYTES = BN * D * 2;         // one K or V tile
+  static constexpr uint32_t KV_HALF_BYTES = BN * ROW_BYTES;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = OFF_Q + 2 * Q_SUB_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;
+  // barriers: q | k_full[S] | k_empty[S] | v_full[S] | v_empty[S] | s_full[2] | p_full[2] | o_done[2] | drain
+  static constexpr int B_Q = 0;
+  static constexpr int B_KF = 1;
+  static constexpr int B_KE = B_KF + STAGES;
+  static constexpr int B_VF = B_KE + STAGES;
+  static constexpr int B_VE = B_VF + STAGES;
+  static constexpr int B_SF = B_VE + STAGES;
+  static constexpr int B_PF = B_SF + 2;
+  static constexpr int B_OD = B_PF + 2;
+  static constexpr int B_DRAIN = B_OD + 2;
+  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O0 = 256, T_O1 = 256 + D;
+  // 3 warpgroups: softmax sub-tile 0, softmax sub-tile 1, and {MMA, TMA, 2 idle} warps.
+  static constexpr int THREADS = 384;
+  static constexpr int WARP_MMA = 8, WARP_TMA = 9;
+  // Register split: launched at LAUNCH_REGS per thread (the compiler's count for
+  // 384 threads, checked on the host before launch), the producer/MMA
+  // warpgroup gives back down to LOW_REGS and each softmax warpgroup grows to
+  // HIGH_REGS: 2*128*HIGH + 128*LOW == 384*LAUNCH exactly.
+  static constexpr int LAUNCH_REGS = 168, HIGH_REGS = 224, LOW_REGS = 56;
+  static_assert(2 * 128 * HIGH_REGS + 128 * LOW_REGS <= THREADS * LAUNCH_REGS, "register split exceeds the pool");
+};
+
+struct Smem {
+  uint32_t base;  // shared-space address, 1024-aligned
+  uint8_t* ptr;   // generic pointer to the same byte
+};
+
+template <int D>
+__device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) {
+  return base + Cfg<D>::OFF_BAR + 8u * i;
+}
+
+// --------------------------------------------------------------------------
+// TMA producer (one thread)
+// --------------------------------------------------------------------------
+template <int D>
+__device__ void producer(const FwdParams& p, uint32_t base, int bh, int row0, bool has1, int nkv,
+                         const WaitCtl& ctl) {
+  using C = Cfg<D>;
+  tma_prefetch_desc(&p.tm_q);
+  tma_prefetch_desc(&p.tm_k);
+  tma_prefetch_desc(&p.tm_v);
+  tma_prefetch_desc(&p.tm_o);
+
+  const uint32_t bq = bar_addr<D>(base, C::B_Q);
+  mbar_arrive_expect_tx(bq, (has1 ? 2u : 1u) * C::Q_SUB_BYTES);
+  for (int sub = 0; sub < (has1 ? 2 : 1); ++sub)
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h)
+      tma_load_3d(base + C::OFF_Q + sub * C::Q_SUB_BYTES + h * C::Q_HALF_BYTES, &p.tm_q, bq, 64 * h,
+                  row0 + 128 * sub, bh);
+
+  // parity of the most recent phase armed on each full barrier (-1: never armed)
+  int k_armed[C::STAGES], v_armed[C::STAGES];
+#pragma unroll
+  for (int s = 0; s < C::STAGES; ++s) k_armed[s] = v_armed[s] = -1;
+
+  bool ok = true;
+  for (int j = 0; j < nkv && ok; ++j) {
+    const int s = j % C::STAGES;
+    const uint32_t par = ((j / C::STAGES) & 1) ^ 1;
+    if (!wait_bar(bar_addr<D>(base, C::B_KE + s), par, ctl, kWhereKEmpty)) { ok = false; break; }
+    const uint32_t kf = bar_addr<D>(base, C::B_KF + s);
+    mbar_arrive_expect_tx(kf, C::KV_BYTES);
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h)
+      tma_load_3d(base + C::OFF_K + s * C::KV_BYTES + h * C::KV_HALF_BYTES, &p.tm_k, kf, 64 * h, j * C::BN, bh);
+#pragma unroll
+    for (int t = 0; t < C::STAGES; ++t)
+      if (t == s) k_armed[t] = (j / C::STAGES) & 1;
+
+    if (!wait_bar(bar_addr<D>(base, C::B_VE + s), par, ctl, kWhereVEmpty)) { ok = false; break; }
+    const uint32_t vf = bar_addr<D>(base, C::B_VF + s);
+    mbar_arrive_expect_tx(vf, C::KV_BYTES);
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h)
+      tma_load_3d(base + C::OFF_V + s * C::KV_BYTES + h * C::KV_HALF_BYTES, &p.tm_v, vf, 64 * h, j * C::BN, bh);
+#pragma unroll
+    for (int t = 0; t < C::STAGES; ++t)
+      if (t == s) v_armed[t] = (j / C::STAGES) & 1;
+  }
+  if (!ok) {
+    // Drain: every copy this thread started must land before the CTA exits.
+    wait_bar_drain(bq, 0, ctl);
+#pragma unroll
+    for (int s = 0; s < C::STAGES; ++s) {
+      if (k_armed[s] >= 0) wait_bar_drain(bar_addr<D>(base, C::B_KF + s), (uint32_t)k_armed[s], ctl);
+      if (v_armed[s] >= 0) wait_bar_drain(bar_addr<D>(base, C::B_VF + s), (uint32_t)v_armed[s], ctl);
+    }
+  }
+}
+
+// --------------------------------------------------------------------------
+// MMA issuer (one thread)
+// --------------------------------------------------------------------------
+template <int D, bool BF16>
+__device__ void mma_issuer(uint32_t base, uint32_t tmem, bool has1, int nkv, const WaitCtl& ctl) {
+  using C = Cfg<D>;
+  constexpr uint32_t fmt = BF16 ? 1u : 0u;
+  // S = Q K^T: A = Q (K-major), B = K tile (K-major), M = 128, N = 128.
+  constexpr uint32_t idesc_qk = make_idesc(fmt, 0, 0, 128, C::BN);
+  // O += P V: A = P from TMEM (K-major), B = V tile, N (= d) contiguous -> MN-major.
+  constexpr uint32_t idesc_pv = make_idesc(fmt, 0, 1, 128, D);
+  const int nsub = has1 ? 2 : 1;
+
+  if (!wait_bar(bar_addr<D>(base, C::B_Q), 0, ctl, kWhereQ)) goto drain;
+  tc_fence_after();
+  for (int j = 0; j < nkv; ++j) {
+    const int s = j % C::STAGES;
+    const uint32_t par = (j / C::STAGES) & 1;
+    if (!wait_bar(bar_addr<D>(base, C::B_KF + s), par, ctl, kWhereKFull)) goto drain;
+    tc_fence_after();
+    const uint32_t kbase = base + C::OFF_K + s * C::KV_BYTES;
+    for (int sub = 0; sub < nsub; ++sub) {
+      if (j > 0) {
+        // P_sub(j-1) lives in the S_sub columns: its P.V must be finished first.
+        if (!wait_bar(bar_addr<D>(base, C::B_OD + sub), (j - 1) & 1, ctl, kWhereODone)) goto drain;
+        tc_fence_after();
+      }
+      const uint32_t d_s = tmem + (sub ? C::T_S1 : C::T_S0);
+      const uint32_t qbase = base + C::OFF_Q + sub * C::Q_SUB_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t koff = (kk & 3) * 32u;  // 16 elements = 32 bytes inside the swizzled row
+        const uint64_t a = smem_desc_sw128(qbase + (kk / 4) * C::Q_HALF_BYTES + koff, 16, 1024);
+        const uint64_t b = smem_desc_sw128(kbase + (kk / 4) * C::KV_HALF_BYTES + koff, 16, 1024);
+        mma_f16_ss(d_s, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+      }
+      tc_commit(bar_addr<D>(base, C::B_SF + sub));
+    }
+    tc_commit(bar_addr<D>(base, C::B_KE + s));
+
+    if (!wait_bar(bar_addr<D>(base, C::B_VF + s), par, ctl, kWhereVFull)) goto drain;
+    tc_fence_after();
+    const uint32_t vbase = base + C::OFF_V + s * C::KV_BYTES;
+    for (int sub = 0; sub < nsub; ++sub) {
+      if (!wait_bar(bar_addr<D>(base, C::B_PF + sub), j & 1, ctl, kWherePFull)) goto drain;
+      tc_fence_after();
+      const uint32_t d_o = tmem + (sub ? C::T_O1 : C::T_O0);
+      const uint32_t a_p = tmem + (sub ? C::T_S1 : C::T_S0);
+#pragma unroll
+      for (int kk = 0; kk < C::BN / 16; ++kk) {
+        // 16 keys = two 8-row swizzle atoms (SBO apart); the two 64-wide halves of d are LBO apart.
+        // With d = 64 there is one half and LBO is unused; 1024 keeps every address inside the tile.
+        constexpr uint32_t lbo = (D == 64) ? 1024u : C::KV_HALF_BYTES;
+        const uint64_t b = smem_desc_sw128(vbase + kk * 16 * C::ROW_BYTES, lbo, 1024);
+        mma_f16_ts(d_o, a_p + kk * 8, b, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+      }
+      tc_commit(bar_addr<D>(base, C::B_OD + sub));
+    }
+    tc_commit(bar_addr<D>(base, C::B_VE + s));
+  }
+drain:
+  // All MMAs issued by this thread complete before the CTA may free TMEM / exit.
+  tc_commit(bar_addr<D>(base, C::B_DRAIN));
+  wait_bar_drain(bar_addr<D>(base, C::B_DRAIN), 0, ctl);
+}
+
+// --------------------------------------------------------------------------
+// Softmax + lazy correction + epilogue (one warpgroup per Q sub-tile)
+// --------------------------------------------------------------------------
+template <int D, bool BF16>
+__device__ void softmax_wg(const FwdParams& p, uint32_t base, uint32_t tmem, int sub, int bh, int row0, int nkv,
+                           const WaitCtl& ctl) {
+  using C = Cfg<D>;
+  const int t = threadIdx.x - sub * 128;  // row within the sub-tile
+  const int lane = threadIdx.x & 31;
+  const uint32_t lane_base = static_cast<uint32_t>(t & ~31) << 16;
+  const uint32_t t_s = tmem + lane_base + (sub ? C::T_S1 : C::T_S0);
+  const uint32_t t_o = tmem + lane_base + (sub ? C::T_O1 : C::T_O0);
+  const uint32_t b_sf = bar_addr<D>(base, C::B_SF + sub);
+  const uint32_t b_pf = bar_addr<D>(base, C::B_PF + sub);
+  const uint32_t b_od = bar_addr<D>(base, C::B_OD + sub);
+  const float c = p.scale * kLog2e;  // scores in log2 units: x = s * c
+
+  float m_ref = -INFINITY;  // reference max (log2 units) shared by l and O
+  float l = 0.f;            // sum of P (fp32) relative to m_ref: gives LSE
+  float l_o = 0.f;          // bf16 only: sum of the rounded P: normalises O
+  bool ok = true;
+
+  for (int j = 0; j < nkv; ++j) {
+    // Wait results are made warp-uniform: TMEM loads/stores below need the whole warp.
+    if (!__all_sync(0xffffffffu, wait_bar(b_sf, j & 1, ctl, kWhereSFull))) { ok = false; break; }
+    tc_fence_after();
+    uint32_t sraw[C::BN / 32][32];
+#pragma unroll
+    for (int q = 0; q < C::BN / 32; ++q) tmem_ld32(t_s + 32 * q, sraw[q]);
+    tmem_ld_wait();
+    float s[C::BN];
+#pragma unroll
+    for (int q = 0; q < C::BN / 32; ++q) {
+      reg_fence(sraw[q]);
+#pragma unroll
+      for (int u = 0; u < 32; ++u) s[32 * q + u] = __uint_as_float(sraw[q][u]);
+    }
+
+    const int valid = p.N - j * C::BN;  // keys of this tile inside the sequence
+    if (valid < C::BN) {
+#pragma unroll
+      for (int u = 0; u < C::BN; ++u)
+        if (u >= valid) s[u] = -INFINITY;
+    }
+    // Row max with 8 independent chains of 3-input max.
+    float mxa[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mxa[i] = fmaxf(s[i], s[i + 8]);
+#pragma unroll
+    for (int u = 16; u < C::BN; u += 16)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mxa[i] = fmax3(mxa[i], s[u + i], s[u + 8 + i]);
+    const float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
+                           fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
+    const float m_new = fmaxf(m_ref, mx * c);
+
+    // Lazy rescale decision (warp-uniform, since TMEM access is per warp): move
+    // the reference max of every row of this warp when any row's tile max
+    // exceeds it by more than the threshold. l is rescaled now; O is rescaled
+    // below, after P is stored but before P is released to the P.V MMA.
+    bool rescale_o = false;
+    float alpha = 1.f;
+    if (j == 0) {
+      m_ref = m_new;  // O is written fresh by the first P.V; l is 0
+    } else if (__any_sync(0xffffffffu, m_new - m_ref > kRescaleThreshold)) {
+      alpha = ex2_approx(m_ref - m_new);  // = exp(m_old - m_new) in natural units
+      m_ref = m_new;
+      l *= alpha;
+      l_o *= alpha;
+      rescale_o = true;
+    }
+
+    // P = 2^(s*c - m_ref), two scores per packed FMA. The exact fp32 sum gives
+    // l (for LSE). For bf16 the P.V product sees P rounded to 8 significant
+    // bits, so O is normalised by the sum of the rounded P (l_o): numerator
+    // and denominator then use the same weights, which keeps |dO| well below
+    // the rounding of a bf16 output even for sharply peaked rows.
+    const float2 c2 = make_float2(c, c);
+    const float2 nm2 = make_float2(-m_ref, -m_ref);
+    float2 se = make_float2(0.f, 0.f), sro = se;  // exact / rounded partial sums
+#pragma unroll
+    for (int q = 0; q < C::BN / 16; ++q) {
+      uint32_t pk[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float2 x = __ffma2_rn(make_float2(s[16 * q + 2 * u], s[16 * q + 2 * u + 1]), c2, nm2);
+        const float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        se = __fadd2_rn(se, pr);
+        pk[u] = pack2<BF16>(pr.x, pr.y);
+        if constexpr (BF16)
+          sro = __fadd2_rn(sro, make_float2(__uint_as_float(pk[u] << 16), __uint_as_float(pk[u] & 0xFFFF0000u)));
+      }
+      tmem_st8(t_s + 8 * q, pk);  // keys [16q, 16q+16) -> packed columns [8q, 8q+8)
+    }
+    l += se.x + se.y;
+    if constexpr (BF16) l_o += sro.x + sro.y;
+    if (rescale_o) {
+      // O_j-1 must be complete (its P.V finished) before it is read and scaled.
+      if (!__all_sync(0xffffffffu, wait_bar(b_od, (j - 1) & 1, ctl, kWhereODone))) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t r[32];
+        tmem_ld32(t_o + 32 * q, r);
+        tmem_ld_wait();
+        reg_fence(r);
+#pragma unroll
+        for (int u = 0; u < 32; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * alpha);
+        tmem_st32(t_o + 32 * q, r);
+      }
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(b_pf);
+  }
+  if (ok) ok = __all_sync(0xffffffffu, wait_bar(b_od, (nkv - 1) & 1, ctl, kWhereODone));
+  // The whole warpgroup agrees before the epilogue, whose named barrier needs all 128 threads.
+  if (!named_bar_and(1 + sub, 128, ok)) return;
+
+  // ---- epilogue: O / l -> dtype -> swizzled staging (Q buffer) -> TMA store; LSE ----
+  tc_fence_after();
+  const float inv_l = 1.0f / (BF16 ? l_o : l);
+  const uint32_t stage = base + C::OFF_Q + sub * C::Q_SUB_BYTES;
+#pragma unroll
+  for (int q = 0; q < D / 32; ++q) {
+    uint32_t r[32];
+    tmem_ld32(t_o + 32 * q, r);
+    tmem_ld_wait();
+    reg_fence(r);
+    uint32_t pk[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      pk[u] = pack2<BF16>(__uint_as_float(r[2 * u]) * inv_l, __uint_as_float(r[2 * u + 1]) * inv_l);
+    const uint32_t half = q / 2;
+    const uint32_t chunk0 = (q & 1) * 4;  // 16-byte chunk within the 128-byte row
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t phys = (chunk0 + u) ^ (static_cast<uint32_t>(t) & 7u);
+      const uint32_t addr = stage + half * C::Q_HALF_BYTES + t * C::ROW_BYTES + phys * 16;
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * u]), "r"(pk[4 * u + 1]),
+                   "r"(pk[4 * u + 2]), "r"(pk[4 * u + 3])
+                   : "memory");
+    }
+  }
+  fence_proxy_async_smem();
+  named_bar_sync(1 + sub, 128);
+  if (t == 0) {
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) tma_store_3d(&p.tm_o, stage + h * C::Q_HALF_BYTES, 64 * h, row0 + 128 * sub, bh);
+    tma_store_commit();
+    tma_store_wait_all();
+  }
+  const int row = row0 + 128 * sub + t;
+  if (row < p.N) p.lse[static_cast<size_t>(bh) * p.N + row] = (m_ref + lg2_approx(l)) * kLn2;
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __grid_constant__ FwdParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem_raw + (base - raw) + C::OFF_MISC);
+
+  const int warp = threadIdx.x >> 5;
+  const int nqb = (p.N + 255) / 256;
+  const int bh = blockIdx.x / nqb;
+  const int row0 = (blockIdx.x % nqb) * 256;
+  const bool has1 = row0 + 128 < p.N;
+  const int nkv = (p.N + C::BN - 1) / C::BN;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_addr<D>(base, C::B_Q), 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar_addr<D>(base, C::B_KF + s), 1);
+      mbar_init(bar_addr<D>(base, C::B_KE + s), 1);
+      mbar_init(bar_addr<D>(base, C::B_VF + s), 1);
+      mbar_init(bar_addr<D>(base, C::B_VE + s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_addr<D>(base, C::B_SF + i), 1);
+      mbar_init(bar_addr<D>(base, C::B_PF + i), 4);  // one arrival per softmax warp
+      mbar_init(bar_addr<D>(base, C::B_OD + i), 1);
+    }
+    mbar_init(bar_addr<D>(base, C::B_DRAIN), 1);
+    misc[1] = 0;
+    mbar_init_fence();
+  }
+  if (warp == C::WARP_MMA) {
+    tmem_alloc(base + C::OFF_MISC, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  WaitCtl ctl{reinterpret_cast<volatile int*>(&misc[1]), p.status, p.wait_limit};
+
+  if (warp >= 8) {
+    warpgroup_reg_dealloc<C::LOW_REGS>();
+    if (warp == C::WARP_TMA) {
+      if ((threadIdx.x & 31) == 0) producer<D>(p, base, bh, row0, has1, nkv, ctl);
+      __syncwarp();
+    } else if (warp == C::WARP_MMA) {
+      if ((threadIdx.x & 31) == 0) mma_issuer<D, BF16>(base, tmem, has1, nkv, ctl);
+      __syncwarp();
+    }
+  } else {
+    warpgroup_reg_alloc<C::HIGH_REGS>();
+    const int sub = warp / 4;
+    if (sub == 0 || has1) softmax_wg<D, BF16>(p, base, tmem, sub, bh, row0, nkv, ctl);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, bool BF16>
+cudaError_t launch(const FwdParams& p, cudaStream_t stream) {
+  using C = Cfg<D>;
+  auto kern = fa_fwd_f16_kernel<D, BF16>;
+  static std::atomic<uint64_t> attr_done{0};  // one bit per device ordinal (< 64)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_done.load() & bit)) {
+    // The warpgroup register split is only valid if the CTA is launched with
+    // exactly LAUNCH_REGS registers per thread; otherwise refuse to launch.
+    cudaFuncAttributes fa_attr;
+    e = cudaFuncGetAttributes(&fa_attr, kern);
+    if (e != cudaSuccess) return e;
+    if (fa_attr.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done.fetch_or(bit);
+  }
+  const long long units = static_cast<long long>(p.B) * p.H * ((p.N + 255) / 256);
+  if (units <= 0 || units > 0x7fffffffLL) return cudaErrorInvalidValue;
+  kern<<<dim3(static_cast<unsigned>(units)), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_f16(const FwdParams& p, bool bf16, cudaStream_t stream) {
+  if (p.d == 128) return bf16 ? launch<128, true>(p, stream) : launch<128, false>(p, stream);
+  if (p.d == 64) return bf16 ? launch<64, true>(p, stream) : launch<64, false>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

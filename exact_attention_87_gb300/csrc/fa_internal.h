@@ -1,0 +1,44 @@
+// fa_internal.h — parameter block and launch entry points shared by the host
+// API (fa_api.cu) and the kernel translation units. Not part of the C ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Bits of the device status word.
+enum : unsigned int {
+  kStatusTimeout = 1u,  // some wait gave up
+};
+// Where a wait gave up (stored in bits 8-15 of the status word, first writer wins).
+enum : unsigned int {
+  kWhereQ = 1, kWhereKEmpty, kWhereVEmpty, kWhereKFull, kWhereVFull, kWhereSFull, kWherePFull,
+  kWhereODone, kWhereDrain, kWhereF32Mma
+};
+
+// Everything a forward kernel needs; passed by value as a __grid_constant__.
+struct alignas(64) FwdParams {
+  CUtensorMap tm_q;  // [B*H, N, d] boxes of 64 x 128 (16-bit path)
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  CUtensorMap tm_o;
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  unsigned int* status;     // device status word of this module on this device
+  long long wait_limit;     // clock64 cycles a barrier wait may spin before giving up
+  int B, H, N, d;
+  float scale;
+  int num_sms;
+};
+
+// Launch the 16-bit (fp16 / bf16) forward kernel for head dimension p.d.
+cudaError_t launch_fwd_f16(const FwdParams& p, bool bf16, cudaStream_t stream);
+// Launch the fp32 (3 x TF32) forward kernel.
+cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);
+
+}  // namespace fa

@@ -1,0 +1,95 @@
+/*
+ * fa.h — C ABI of the GB300 (sm_103a) FlashAttention forward library.
+ *
+ * The operation (MUSA SDK programming guide, "FlashAttention 优化": the
+ * standard attention formula under "计算流程", computed by the tiled
+ * online-softmax algorithm under "FlashAttention 完整算法", formula steps 1-4):
+ *
+ *     for every batch b < B and head h < H, and query row i < N:
+ *         s_ij   = scale * sum_k Q[b,h,i,k] * K[b,h,j,k]          (j < N)
+ *         O[b,h,i,:] = sum_j softmax_j(s_i.) * V[b,h,j,:]
+ *         LSE[b,h,i] = ln sum_j exp(s_ij)
+ *
+ * Non-causal, no mask. S and P are never written to memory. LSE is the
+ * per-row logsumexp that a backward pass by recomputation needs (the Triton
+ * page, "反向传播要不要自己写": keep the row statistics, recompute P).
+ *
+ * Ownership: the caller owns every buffer. The library allocates no device
+ * memory per call; it keeps one process-lifetime device status word per GPU
+ * (a __device__ variable of the module) and nothing else.
+ *
+ * Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).
+ * fa_fwd only enqueues work and never synchronises.
+ *
+ * Devices: sm_103 (GB300) only; other devices get FA_ERR_ARCH.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of Q, K, V and O. */
+typedef enum { FA_F32 = 0, FA_F16 = 1, FA_BF16 = 2 } fa_dtype;
+
+/* Return codes. Every entry point returns one of these. */
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_NULL = 1,           /* a required pointer is NULL                         */
+    FA_ERR_DTYPE = 2,          /* dtype is not one of fa_dtype                       */
+    FA_ERR_SHAPE = 3,          /* B, H or N < 1, or B*H*N*d overflows 2^40 elements  */
+    FA_ERR_HEADDIM = 4,        /* d is not 64 or 128                                 */
+    FA_ERR_ALIGN = 5,          /* a base pointer is not 16-byte aligned              */
+    FA_ERR_CUDA = 6,           /* a CUDA runtime/driver call failed (launch, query)  */
+    FA_ERR_DEVICE_TIMEOUT = 7, /* a kernel gave up waiting on a pipeline barrier     */
+    FA_ERR_ARCH = 8,           /* the current device is not sm_103                   */
+    FA_ERR_SCALE = 9           /* scale is not finite and > 0                        */
+} fa_status;
+
+/*
+ * Forward pass.
+ *
+ * Q, K, V, O: device pointers to [B, H, N, d] row-major contiguous arrays of
+ *             `dtype` (the last index d is contiguous, then N, then H, then B).
+ *             O has the same dtype as Q. O must not alias Q, K or V.
+ * LSE:        device pointer to a [B, H, N] contiguous fp32 array: natural-log
+ *             logsumexp of each scaled score row, ln sum_j exp(scale * q_i.k_j).
+ * d:          64 or 128.
+ * scale:      multiplies q.k before the softmax (1/sqrt(d) is the usual value);
+ *             must be finite and > 0.
+ * dtype:      FA_F32, FA_F16 or FA_BF16. For FA_F16/FA_BF16 both matrix
+ *             products run on the tensor cores with fp32 accumulation and P is
+ *             rounded to `dtype` before P.V; for FA_F32 they run as three
+ *             TF32 products (hi*hi + hi*lo + lo*hi) with fp32 accumulation.
+ * stream:     cudaStream_t to enqueue on.
+ *
+ * Errors: argument errors return before anything is enqueued (FA_ERR_NULL,
+ * FA_ERR_DTYPE, FA_ERR_SHAPE, FA_ERR_HEADDIM, FA_ERR_ALIGN, FA_ERR_SCALE,
+ * FA_ERR_ARCH). A failed launch returns FA_ERR_CUDA. A kernel that times out
+ * on an internal barrier records FA_ERR_DEVICE_TIMEOUT in the device status
+ * word, drains its own asynchronous copies, frees its tensor memory and
+ * returns; read it with fa_get_device_status.
+ */
+int fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
+           int B, int H, int N, int d, float scale, int dtype, void *stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the status word that kernels
+ * of this library on the current device write when they give up on a wait:
+ * FA_OK, FA_ERR_DEVICE_TIMEOUT, or FA_ERR_CUDA if the synchronisation or the
+ * read failed.
+ */
+int fa_get_device_status(void *stream);
+
+/* Static English text for a status code (never NULL). */
+const char *fa_strerror(int status);
+
+/* Library ABI version: 100 * major + minor. */
+int fa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,74 @@
+"""The C ABI: the library builds, loads and exports every entry point that
+include/fa.h declares; argument errors come back as codes before any launch."""
+import os
+import re
+
+import pytest
+
+import exact_attention_87_gb300 as fa
+from exact_attention_87_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return fa.lib()
+
+
+def declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fa_\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    assert "fa_fwd" in names and "fa_get_device_status" in names and "fa_strerror" in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} declared in include/ but not exported"
+
+
+def test_strerror_and_version(L):
+    assert fa.fa_abi_version() >= 100
+    for code in range(0, 10):
+        assert fa.fa_strerror(code) and fa.fa_strerror(code) != "unknown status"
+    assert fa.fa_strerror(12345) == "unknown status"
+
+
+A = 1 << 20  # a 16-byte aligned fake address: validation fails before it is used
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16), fa.FA_ERR_NULL),
+    ((A, A, A, A, 0, 1, 1, 64, 64, 0.125, fa.FA_F16), fa.FA_ERR_NULL),
+    ((A, A, A, A, A, 1, 1, 64, 64, 0.125, 7), fa.FA_ERR_DTYPE),
+    ((A, A, A, A, A, 0, 1, 64, 64, 0.125, fa.FA_F16), fa.FA_ERR_SHAPE),
+    ((A, A, A, A, A, 1, 1, 0, 64, 0.125, fa.FA_F16), fa.FA_ERR_SHAPE),
+    ((A, A, A, A, A, 1, -3, 64, 64, 0.125, fa.FA_F16), fa.FA_ERR_SHAPE),
+    ((A, A, A, A, A, 1, 1, 64, 96, 0.125, fa.FA_F16), fa.FA_ERR_HEADDIM),
+    ((A, A, A, A, A, 1, 1, 64, 256, 0.125, fa.FA_BF16), fa.FA_ERR_HEADDIM),
+    ((A, A, A, A, A, 1, 1, 64, 64, 0.0, fa.FA_F16), fa.FA_ERR_SCALE),
+    ((A, A, A, A, A, 1, 1, 64, 64, float("nan"), fa.FA_F16), fa.FA_ERR_SCALE),
+    ((A, A, A, A, A, 1, 1, 64, 64, -1.0, fa.FA_F16), fa.FA_ERR_SCALE),
+    ((A + 8, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16), fa.FA_ERR_ALIGN),
+    ((A, A, A, A + 2, A, 1, 1, 64, 64, 0.125, fa.FA_BF16), fa.FA_ERR_ALIGN),
+    ((A, A, A, A, A + 2, 1, 1, 64, 64, 0.125, fa.FA_F32), fa.FA_ERR_ALIGN),
+    ((A, A, A, A, A, 65536, 65536, 1 << 20, 128, 0.1, fa.FA_F16), fa.FA_ERR_SHAPE),
+])
+def test_argument_errors_return_before_launch(L, args, code):
+    assert fa.fa_fwd(*args, None) == code
+
+
+def test_missing_library_raises(tmp_path):
+    with pytest.raises(ImportError):
+        fa.lib(str(tmp_path / "nope.so"))

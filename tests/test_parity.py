@@ -1,0 +1,163 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU fp64 oracle.
+
+Small and ragged shapes are compared element by element over every output.
+The five full-size workloads run in the same launch configuration as the
+benchmark and are compared on sampled rows (the oracle computes each sampled
+row against all keys of its head), plus properties that hold at any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_87_gb300 as fa
+import oracle
+from parity_util import compare
+from workloads import WORKLOADS, make_inputs, make_qkv, rising_norm_order
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda_lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fa.build()
+    fa.lib()
+
+
+def run_gpu(q, k, v, scale=None):
+    o, lse = fa.attention(q.cuda(), k.cuda(), v.cuda(), scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    return o.cpu().double().numpy(), lse.cpu().double().numpy()
+
+
+def check(q, k, v, dtype, scale=None, label=""):
+    o, lse = run_gpu(q, k, v, scale)
+    o_ref, lse_ref = oracle.attn(q, k, v, scale=scale)
+    res = compare(o, lse, o_ref, lse_ref, dtype)
+    assert res["ok"], f"{label} {res}"
+    return res
+
+
+SMALL = [
+    # B, H, N, d, dtype, sigma_qk
+    (1, 1, 1, 128, "bf16", 1.0),
+    (1, 1, 63, 128, "f16", 1.0),
+    (1, 2, 128, 128, "bf16", 1.0),
+    (1, 1, 129, 128, "f16", 1.0),
+    (2, 3, 200, 128, "bf16", 3.0),
+    (1, 2, 256, 128, "f16", 1.0),
+    (1, 1, 257, 128, "bf16", 1.0),
+    (2, 2, 383, 128, "f16", 1.0),
+    (1, 3, 700, 128, "bf16", 3.0),
+    (1, 1, 1000, 128, "f16", 2.0),
+    (1, 1, 1, 64, "f16", 1.0),
+    (1, 1, 65, 64, "bf16", 1.0),
+    (2, 2, 300, 64, "bf16", 3.0),
+    (1, 1, 777, 64, "f16", 1.0),
+    (4, 33, 64, 64, "f16", 1.0),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,dtype,sig", SMALL, ids=lambda x: str(x))
+def test_small_shapes(B, H, N, d, dtype, sig):
+    q, k, v = make_qkv(B, H, N, d, dtype, sigma_qk=sig, seed=11, wid=1000 + N + d)
+    check(q, k, v, dtype, label=f"{B}x{H}x{N}x{d} {dtype}")
+
+
+SMALL_F32 = [
+    # B, H, N, d
+    (1, 1, 1, 64),
+    (1, 2, 100, 64),
+    (1, 3, 129, 64),
+    (2, 1, 300, 128),
+    (1, 1, 33, 128),
+    (1, 1, 257, 128),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d", SMALL_F32, ids=lambda x: str(x))
+def test_f32_shapes(B, H, N, d):
+    q, k, v = make_qkv(B, H, N, d, "f32", seed=13, wid=6000 + N + d)
+    check(q, k, v, "f32", label=f"{B}x{H}x{N}x{d} f32")
+
+
+def test_f32_rescale_stress():
+    q, k, v = make_qkv(1, 2, 400, 64, "f32", sigma_qk=3.0, seed=2, wid=6100)
+    k, v = rising_norm_order(k, v)
+    check(q, k, v, "f32")
+
+
+@pytest.mark.parametrize("N", [128, 384])
+@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (64, "f16")])
+def test_single_kv_tile_and_exact_multiples(N, d, dtype):
+    q, k, v = make_qkv(1, 2, N, d, dtype, seed=5, wid=2000 + N)
+    check(q, k, v, dtype)
+
+
+@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (128, "f16"), (64, "bf16")])
+def test_rescale_stress_rising_key_norms(d, dtype):
+    """Keys sorted by rising norm with sigma 3: the row max grows on most tiles."""
+    q, k, v = make_qkv(1, 2, 1024, d, dtype, sigma_qk=3.0, seed=9, wid=3000 + d)
+    k, v = rising_norm_order(k, v)
+    check(q, k, v, dtype)
+
+
+def test_non_default_scale():
+    q, k, v = make_qkv(1, 2, 300, 128, "bf16", seed=3, wid=4000)
+    check(q, k, v, "bf16", scale=0.3)
+
+
+@pytest.mark.parametrize("name", ["b1h1n64d64_f32", "b1h4n512d64_f16"])
+def test_whole_small_workloads(name):
+    """The two small workloads fit the oracle in full: every output is compared."""
+    w = WORKLOADS[name]
+    q, k, v = make_inputs(w)
+    check(q, k, v, w.dtype, label=w.name)
+
+
+def test_deterministic():
+    q, k, v = make_qkv(2, 4, 1000, 128, "bf16", sigma_qk=3.0, seed=1, wid=5000)
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    o1, l1 = fa.attention(qc, kc, vc)
+    o1, l1 = o1.clone(), l1.clone()
+    for _ in range(5):
+        o2, l2 = fa.attention(qc, kc, vc)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def sample_rows(B, H, N, n, seed):
+    rng = np.random.default_rng(seed)
+    rows = set()
+    edge = [0, 1, 127, 128, 255, 256, N - 1, N - 2, N // 2]
+    for t in range(n):
+        b, h = int(rng.integers(B)), int(rng.integers(H))
+        i = edge[t] if t < len(edge) else int(rng.integers(N))
+        if 0 <= i < N:
+            rows.add((b, h, i))
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("name", [n for n in WORKLOADS if WORKLOADS[n].dtype != "f32"])
+def test_full_workload_sampled_rows(name):
+    w = WORKLOADS[name]
+    q, k, v = make_inputs(w)
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    o, lse = fa.attention(qc, kc, vc)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    # properties of every row: finite, O inside the per-column range of its head's V
+    assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())
+    vmin = vc.float().amin(dim=2, keepdim=True)
+    vmax = vc.float().amax(dim=2, keepdim=True)
+    of = o.float()
+    slack = 1e-2 * torch.maximum(vmax.abs(), vmin.abs()) + 1e-3
+    assert bool((of <= vmax + slack).all()) and bool((of >= vmin - slack).all())
+    # sampled rows against the oracle
+    rows = sample_rows(w.B, w.H, w.N, 96, seed=w.wid)
+    o_ref, lse_ref = oracle.attn_rows(q, k, v, rows)
+    oc, lc = o.cpu().double().numpy(), lse.cpu().double().numpy()
+    got_o = np.stack([oc[b, h, i] for b, h, i in rows])
+    got_l = np.array([lc[b, h, i] for b, h, i in rows])
+    res = compare(got_o, got_l, o_ref, lse_ref, w.dtype)
+    assert res["ok"], f"{name} {res}"
