@@ -36,20 +36,26 @@ def _inputs():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(lib_path: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib_path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    if not force and up_to_date():
-        return LIB_PATH
+TESTING_LIB_PATH = os.path.join(HERE, "libfa_gb300_testing.so")
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=None, testing: bool = False) -> str:
+    """Build the product library, or with testing=True the instrumented testing
+    library (-DFA_TESTING: stats/timeline traces and fault injection)."""
+    lib_path = TESTING_LIB_PATH if testing else LIB_PATH
+    if not force and up_to_date(lib_path):
+        return lib_path
     cc = nvcc()
-    objdir = os.path.join(HERE, "_build")
+    objdir = os.path.join(HERE, "_build_testing" if testing else "_build")
     os.makedirs(objdir, exist_ok=True)
-    extra = list(extra_flags or [])
+    extra = list(extra_flags or []) + (["-DFA_TESTING"] if testing else [])
 
     def compile_one(src):
         obj = os.path.join(objdir, os.path.splitext(src)[0] + ".o")
@@ -66,15 +72,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     if verbose:
         for _, log in results:
             print(log)
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, testing="--testing" in sys.argv))

@@ -11,6 +11,9 @@
 #include <cuda_runtime.h>
 
 #include "fa.h"
+#ifdef FA_TESTING
+#include "fa_testing.h"
+#endif
 #include "fa_internal.h"
 
 // Device status word of this module: [0] flags (kStatusTimeout), [1] where the
@@ -116,8 +119,13 @@ const char* fa_strerror(int status) {
   }
 }
 
-int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, float scale,
-           int dtype, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
+             float scale, int dtype, void* stream, int inject, float* stats_trace, unsigned long long* timeline,
+             long long wait_limit) {
   if (!Q || !K || !V || !O || !LSE) return FA_ERR_NULL;
   if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
   if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
@@ -141,7 +149,10 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int
   p.o = O;
   p.lse = LSE;
   p.status = dev.status;
-  p.wait_limit = wait_limit_cycles();
+  p.wait_limit = wait_limit > 0 ? wait_limit : wait_limit_cycles();
+  p.inject = inject;
+  p.stats_trace = stats_trace;
+  p.timeline = timeline;
   p.B = B;
   p.H = H;
   p.N = N;
@@ -164,6 +175,30 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int
   }
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, float scale,
+           int dtype, void* stream) {
+  return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, dtype, stream, 0, nullptr, nullptr, 0);
+}
+
+#ifdef FA_TESTING
+int fa_fwd_testing(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
+                   float scale, int dtype, void* stream, int inject, float* stats_trace,
+                   unsigned long long* timeline, long long wait_limit_cycles) {
+  return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, dtype, stream, inject, stats_trace, timeline,
+                  wait_limit_cycles);
+}
+
+unsigned int fa_testing_last_timeout_where(void) {
+  unsigned int h[2] = {0, 0};
+  if (cudaMemcpyFromSymbol(h, g_fa_status, sizeof(h)) != cudaSuccess) return 0xffffffffu;
+  return h[1];
+}
+#endif
 
 int fa_get_device_status(void* stream) {
   DeviceInfo dev;

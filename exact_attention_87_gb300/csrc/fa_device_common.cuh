@@ -45,4 +45,17 @@ __device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, co
   return wait_bar_slow(bar, parity, ctl, kWhereDrain, false);
 }
 
+// Testing build only: clock64 stamp of pipeline event `ev` for tile `j`.
+#ifdef FA_TESTING
+#define FA_TRACE(p, ev, j)                                                                                 \
+  do {                                                                                                     \
+    if ((p).timeline && blockIdx.x < kTraceCtas && (j) < kTraceTiles)                                     \
+      (p).timeline[(static_cast<size_t>(blockIdx.x) * kTraceEvents + (ev)) * kTraceTiles + (j)] = clock64(); \
+  } while (0)
+#else
+#define FA_TRACE(p, ev, j) \
+  do {                     \
+  } while (0)
+#endif
+
 }  // namespace fa

@@ -124,6 +124,10 @@ __device__ void producer(const FwdParams& p, uint32_t base, int bh, int row0, bo
     for (int t = 0; t < C::STAGES; ++t)
       if (t == s) k_armed[t] = (j / C::STAGES) & 1;
 
+    FA_TRACE(p, kEvKIssued, j);
+#ifdef FA_TESTING
+    if (p.inject == 1 && j == 0) continue;  // fault injection: V_0 is never loaded
+#endif
     if (!wait_bar(bar_addr<D>(base, C::B_VE + s), par, ctl, kWhereVEmpty)) { ok = false; break; }
     const uint32_t vf = bar_addr<D>(base, C::B_VF + s);
     mbar_arrive_expect_tx(vf, C::KV_BYTES);
@@ -133,6 +137,7 @@ __device__ void producer(const FwdParams& p, uint32_t base, int bh, int row0, bo
 #pragma unroll
     for (int t = 0; t < C::STAGES; ++t)
       if (t == s) v_armed[t] = (j / C::STAGES) & 1;
+    FA_TRACE(p, kEvVIssued, j);
   }
   if (!ok) {
     // Drain: every copy this thread started must land before the CTA exits.
@@ -149,7 +154,8 @@ __device__ void producer(const FwdParams& p, uint32_t base, int bh, int row0, bo
 // MMA issuer (one thread)
 // --------------------------------------------------------------------------
 template <int D, bool BF16>
-__device__ void mma_issuer(uint32_t base, uint32_t tmem, bool has1, int nkv, const WaitCtl& ctl) {
+__device__ void mma_issuer(const FwdParams& p, uint32_t base, uint32_t tmem, bool has1, int nkv,
+                           const WaitCtl& ctl) {
   using C = Cfg<D>;
   constexpr uint32_t fmt = BF16 ? 1u : 0u;
   // S = Q K^T: A = Q (K-major), B = K tile (K-major), M = 128, N = 128.
@@ -165,6 +171,7 @@ __device__ void mma_issuer(uint32_t base, uint32_t tmem, bool has1, int nkv, con
     const uint32_t par = (j / C::STAGES) & 1;
     if (!wait_bar(bar_addr<D>(base, C::B_KF + s), par, ctl, kWhereKFull)) goto drain;
     tc_fence_after();
+    FA_TRACE(p, kEvMmaKFull, j);
     const uint32_t kbase = base + C::OFF_K + s * C::KV_BYTES;
     for (int sub = 0; sub < nsub; ++sub) {
       if (j > 0) {
@@ -182,11 +189,13 @@ __device__ void mma_issuer(uint32_t base, uint32_t tmem, bool has1, int nkv, con
         mma_f16_ss(d_s, a, b, idesc_qk, kk > 0 ? 1u : 0u);
       }
       tc_commit(bar_addr<D>(base, C::B_SF + sub));
+      FA_TRACE(p, kEvS0Issued + sub, j);
     }
     tc_commit(bar_addr<D>(base, C::B_KE + s));
 
     if (!wait_bar(bar_addr<D>(base, C::B_VF + s), par, ctl, kWhereVFull)) goto drain;
     tc_fence_after();
+    FA_TRACE(p, kEvMmaVFull, j);
     const uint32_t vbase = base + C::OFF_V + s * C::KV_BYTES;
     for (int sub = 0; sub < nsub; ++sub) {
       if (!wait_bar(bar_addr<D>(base, C::B_PF + sub), j & 1, ctl, kWherePFull)) goto drain;
@@ -202,6 +211,7 @@ __device__ void mma_issuer(uint32_t base, uint32_t tmem, bool has1, int nkv, con
         mma_f16_ts(d_o, a_p + kk * 8, b, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
       }
       tc_commit(bar_addr<D>(base, C::B_OD + sub));
+      FA_TRACE(p, kEvPV0Issued + sub, j);
     }
     tc_commit(bar_addr<D>(base, C::B_VE + s));
   }
@@ -237,6 +247,7 @@ __device__ void softmax_wg(const FwdParams& p, uint32_t base, uint32_t tmem, int
     // Wait results are made warp-uniform: TMEM loads/stores below need the whole warp.
     if (!__all_sync(0xffffffffu, wait_bar(b_sf, j & 1, ctl, kWhereSFull))) { ok = false; break; }
     tc_fence_after();
+    if (t == 0) FA_TRACE(p, kEvSm0SFull + 2 * sub, j);
     uint32_t sraw[C::BN / 32][32];
 #pragma unroll
     for (int q = 0; q < C::BN / 32; ++q) tmem_ld32(t_s + 32 * q, sraw[q]);
@@ -326,6 +337,17 @@ __device__ void softmax_wg(const FwdParams& p, uint32_t base, uint32_t tmem, int
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(b_pf);
+    if (t == 0) FA_TRACE(p, kEvSm0PArrive + 2 * sub, j);
+#ifdef FA_TESTING
+    if (p.stats_trace) {
+      const int row = row0 + 128 * sub + t;
+      if (row < p.N) {
+        float* tr = p.stats_trace + ((static_cast<size_t>(bh) * p.N + row) * nkv + j) * 2;
+        tr[0] = m_ref * kLn2;
+        tr[1] = l;
+      }
+    }
+#endif
   }
   if (ok) ok = __all_sync(0xffffffffu, wait_bar(b_od, (nkv - 1) & 1, ctl, kWhereODone));
   // The whole warpgroup agrees before the epilogue, whose named barrier needs all 128 threads.
@@ -409,6 +431,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
   tc_fence_after();
   const uint32_t tmem = misc[0];
   WaitCtl ctl{reinterpret_cast<volatile int*>(&misc[1]), p.status, p.wait_limit};
+  if (threadIdx.x == 0) FA_TRACE(p, kEvCta, 0);
 
   if (warp >= 8) {
     warpgroup_reg_dealloc<C::LOW_REGS>();
@@ -416,7 +439,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
       if ((threadIdx.x & 31) == 0) producer<D>(p, base, bh, row0, has1, nkv, ctl);
       __syncwarp();
     } else if (warp == C::WARP_MMA) {
-      if ((threadIdx.x & 31) == 0) mma_issuer<D, BF16>(base, tmem, has1, nkv, ctl);
+      if ((threadIdx.x & 31) == 0) mma_issuer<D, BF16>(p, base, tmem, has1, nkv, ctl);
       __syncwarp();
     }
   } else {
@@ -427,6 +450,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) {
+    FA_TRACE(p, kEvCta, 1);
+#ifdef FA_TESTING
+    if (p.timeline && blockIdx.x < kTraceCtas) {
+      uint32_t smid;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+      p.timeline[(static_cast<size_t>(blockIdx.x) * kTraceEvents + kEvCta) * kTraceTiles + 2] = smid;
+    }
+#endif
+  }
   if (warp == C::WARP_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);

@@ -15,8 +15,8 @@
 // Mapping: one CTA per (batch*head, 128-row Q tile), one warpgroup (thread =
 // row = TMEM lane). Q hi/lo stay resident in shared memory; each K/V tile is
 // loaded with coalesced 16-byte loads, split, and written in the 128-byte
-// swizzled layout the MMA descriptors expect; P hi/lo go through shared
-// memory. One thread issues the MMAs; completion is signalled through mbarriers
+// swizzled layout the MMA descriptors expect (V transposed, so that every
+// operand is K-major); P hi/lo go through shared memory. One thread issues the MMAs; completion is signalled through mbarriers
 // by tcgen05.commit. This path targets small, latency-bound fp32 problems.
 #include <atomic>
 
@@ -81,6 +81,27 @@ __device__ __forceinline__ void load_split(const float* __restrict__ g, int row0
   }
 }
 
+// Same for a [N, D] matrix V, stored transposed: element (key j, column n) at
+// row n, K index j - row0, so that V is a K-major B operand ([D rows] x [BN keys]).
+template <int D, int BN>
+__device__ __forceinline__ void load_split_t(const float* __restrict__ g, int row0, int N, uint32_t s_hi,
+                                             uint32_t s_lo) {
+  constexpr int V4_PER_ROW = D / 4;
+  for (int idx = threadIdx.x; idx < BN * V4_PER_ROW; idx += blockDim.x) {
+    const int r = idx / V4_PER_ROW, c4 = idx % V4_PER_ROW;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row0 + r < N) x = __ldg(reinterpret_cast<const float4*>(g + static_cast<size_t>(row0 + r) * D) + c4);
+    const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float h = tf32_hi(xs[e]);
+      const uint32_t off = sw128_off32(c4 * 4 + e, r, D);
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(s_hi + off), "f"(h) : "memory");
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(s_lo + off), "f"(xs[e] - h) : "memory");
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(128, 1) fa_fwd_f32_kernel(const __grid_constant__ FwdParams p) {
   using C = Cfg32<D>;
@@ -122,14 +143,14 @@ __global__ void __launch_bounds__(128, 1) fa_fwd_f32_kernel(const __grid_constan
   const uint32_t t_s = tmem + lane_base + C::T_S, t_o = tmem + lane_base + C::T_O;
 
   constexpr uint32_t idesc_s = make_idesc(2, 0, 0, 128, C::BN);  // tf32, Q and K K-major
-  constexpr uint32_t idesc_o = make_idesc(2, 0, 1, 128, D);      // tf32, P K-major, V MN-major
+  constexpr uint32_t idesc_o = make_idesc(2, 0, 0, 128, D);      // tf32, P and V^T both K-major
   const float c = p.scale * kLog2e;
   float m = -INFINITY, l = 0.f;
   bool ok = true;
 
   for (int j = 0; j < nkv && ok; ++j) {
     load_split<D>(k, j * C::BN, C::BN, p.N, base + C::OFF_KH, base + C::OFF_KL);
-    load_split<D>(v, j * C::BN, C::BN, p.N, base + C::OFF_VH, base + C::OFF_VL);
+    load_split_t<D, C::BN>(v, j * C::BN, p.N, base + C::OFF_VH, base + C::OFF_VL);
     fence_proxy_async_smem();
     __syncthreads();
     if (t == 0) {
@@ -212,13 +233,13 @@ __global__ void __launch_bounds__(128, 1) fa_fwd_f32_kernel(const __grid_constan
       // O += Ph Vh + Ph Vl + Pl Vh; each MMA covers 8 keys.
 #pragma unroll
       for (int kk = 0; kk < C::BN / 8; ++kk) {
-        const uint32_t poff = (kk / 4) * C::BM * 128u + (kk & 3) * 32u;
-        const uint32_t voff = kk * 8u * 128u;  // 8 keys = one swizzle atom along K
-        constexpr uint32_t lbo = C::BN * 128u;  // next 32 columns of d
+        const uint32_t koff = (kk & 3) * 32u;  // 8 keys = 32 bytes inside the swizzled row
+        const uint32_t poff = (kk / 4) * C::BM * 128u + koff;
+        const uint32_t voff = (kk / 4) * D * 128u + koff;
         const uint64_t ph = smem_desc_sw128(base + C::OFF_PH + poff, 16, 1024);
         const uint64_t pl = smem_desc_sw128(base + C::OFF_PL + poff, 16, 1024);
-        const uint64_t vh = smem_desc_sw128(base + C::OFF_VH + voff, lbo, 1024);
-        const uint64_t vl = smem_desc_sw128(base + C::OFF_VL + voff, lbo, 1024);
+        const uint64_t vh = smem_desc_sw128(base + C::OFF_VH + voff, 16, 1024);
+        const uint64_t vl = smem_desc_sw128(base + C::OFF_VL + voff, 16, 1024);
         mma_tf32_ss(tmem + C::T_O, ph, vh, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
         mma_tf32_ss(tmem + C::T_O, ph, vl, idesc_o, 1u);
         mma_tf32_ss(tmem + C::T_O, pl, vh, idesc_o, 1u);

@@ -34,6 +34,17 @@ struct alignas(64) FwdParams {
   int B, H, N, d;
   float scale;
   int num_sms;
+  // Used only by the testing build (-DFA_TESTING); zero / NULL otherwise.
+  int inject;                       // 1: the producer skips the V load of tile 0
+  float* stats_trace;               // [B*H*N, nkv, 2]: (m in natural-log units, l) after each K/V tile
+  unsigned long long* timeline;     // [kTraceCtas, kTraceEvents, kTraceTiles] clock64 stamps
+};
+
+// Timeline trace layout of the testing build.
+constexpr int kTraceCtas = 8, kTraceTiles = 64, kTraceEvents = 16;
+enum : int {
+  kEvS0Issued = 0, kEvS1Issued, kEvPV0Issued, kEvPV1Issued, kEvSm0SFull, kEvSm0PArrive, kEvSm1SFull,
+  kEvSm1PArrive, kEvKIssued, kEvVIssued, kEvMmaKFull, kEvMmaVFull, kEvCta
 };
 
 // Launch the 16-bit (fp16 / bf16) forward kernel for head dimension p.d.

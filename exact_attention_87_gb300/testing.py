@@ -1,0 +1,64 @@
+"""Binding of the TESTING build (libfa_gb300_testing.so, -DFA_TESTING).
+
+Used by the tests only: per-tile running statistics, pipeline timelines and
+fault injection for the bounded barrier waits (see include/fa_testing.h).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+from . import FA_OK, FAError, _dtype_code
+from ._build import TESTING_LIB_PATH, build
+
+TRACE_CTAS, TRACE_EVENTS, TRACE_TILES = 8, 16, 64
+EVENTS = ["S0_issued", "S1_issued", "PV0_issued", "PV1_issued", "sm0_sfull", "sm0_parrive", "sm1_sfull",
+          "sm1_parrive", "K_issued", "V_issued", "mma_kfull", "mma_vfull", "cta"]
+KV_TILE = 128  # keys per K/V tile of the fp16/bf16 kernel (stats_trace has ceil(N / KV_TILE) entries per row)
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build(testing=True)
+        L = ctypes.CDLL(TESTING_LIB_PATH)
+        vp, i, f, ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong
+        L.fa_fwd_testing.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, i, vp, vp, ll]
+        L.fa_fwd_testing.restype = i
+        L.fa_get_device_status.argtypes = [vp]
+        L.fa_get_device_status.restype = i
+        L.fa_testing_last_timeout_where.restype = ctypes.c_uint
+        _lib = L
+    return _lib
+
+
+def attention(q, k, v, scale=None, inject=0, stats=False, timeline=False, wait_limit_cycles=0, check=True):
+    """Like exact_attention_87_gb300.attention, through fa_fwd_testing.
+
+    Returns (O, LSE, stats_trace or None, timeline or None).
+    """
+    import torch
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    nkv = (N + KV_TILE - 1) // KV_TILE
+    st = torch.zeros((B, H, N, nkv, 2), dtype=torch.float32, device=q.device) if stats else None
+    tl = torch.zeros((TRACE_CTAS, TRACE_EVENTS, TRACE_TILES), dtype=torch.int64, device=q.device) if timeline else None
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = lib().fa_fwd_testing(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, d,
+                              float(scale), _dtype_code(q), stream, int(inject),
+                              st.data_ptr() if st is not None else None,
+                              tl.data_ptr() if tl is not None else None, int(wait_limit_cycles))
+    if check and rc != FA_OK:
+        raise FAError(rc, "fa_fwd_testing")
+    return out, lse, st, tl
+
+
+def device_status(stream=None) -> int:
+    return lib().fa_get_device_status(stream)
+
+
+def last_timeout_where() -> int:
+    return lib().fa_testing_last_timeout_where()

@@ -17,11 +17,11 @@ def L():
     return fa.lib()
 
 
-def declared_functions():
+def declared_functions(header=None):
     names = []
     inc = os.path.join(ROOT, "include")
     for f in sorted(os.listdir(inc)):
-        if f.endswith(".h"):
+        if f.endswith(".h") and (header is None or f == header):
             text = open(os.path.join(inc, f)).read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
             names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fa_\w+)\s*\(", text, flags=re.M)
@@ -34,8 +34,25 @@ def test_header_declares_entry_points():
 
 
 def test_library_exports_every_declared_symbol(L):
-    for name in declared_functions():
-        assert hasattr(L, name), f"{name} declared in include/ but not exported"
+    for name in declared_functions("fa.h"):
+        assert hasattr(L, name), f"{name} declared in include/fa.h but not exported"
+
+
+def test_testing_symbols_only_in_testing_library(L):
+    import ctypes
+    testing = ctypes.CDLL(_build.build(testing=True))
+    names = declared_functions("fa_testing.h")
+    assert "fa_fwd_testing" in names
+    for name in names:
+        assert hasattr(testing, name), f"{name} not exported by the testing library"
+        assert not hasattr(L, name), f"{name} leaked into the product library"
+    for name in declared_functions("fa.h"):
+        assert hasattr(testing, name)
+
+
+def test_every_header_is_covered():
+    inc = os.path.join(ROOT, "include")
+    assert sorted(f for f in os.listdir(inc) if f.endswith(".h")) == ["fa.h", "fa_testing.h"]
 
 
 def test_strerror_and_version(L):
