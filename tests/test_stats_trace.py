@@ -40,7 +40,7 @@ def test_running_statistics_match_online_model(N, d, dtype, sig, rising):
     tol = 1e-4 * np.maximum(1.0, np.abs(run_lse_ref))
     assert np.all(np.abs(run_lse_k - run_lse_ref) <= tol), float(np.abs(run_lse_k - run_lse_ref).max())
     eps = 1e-4 * np.maximum(1.0, np.abs(m_eager))
-    assert np.all(np.diff(m_k, axis=-1) >= -eps)                 # never decreases
+    assert np.all(np.diff(m_k, axis=-1) >= -eps[..., 1:])        # never decreases
     assert np.all(m_k <= m_eager + eps)                           # a max of scores seen so far
     assert np.all(m_eager - m_k <= 8 * LN2 + eps)                 # trails by at most the threshold
     # the final tile's statistics give the LSE output
