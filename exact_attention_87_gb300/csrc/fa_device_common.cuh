@@ -39,6 +39,11 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
   return wait_bar_slow(bar, parity, ctl, where, true);
 }
 
+// Whole-warp wait with a warp-uniform outcome.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, const WaitCtl& ctl, unsigned where) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, ctl, where));
+}
+
 // Same, but keeps waiting after another role aborted (used to drain in-flight copies/MMAs).
 __device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
   if (mbar_try_wait(bar, parity)) return true;

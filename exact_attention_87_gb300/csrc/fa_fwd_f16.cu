@@ -71,7 +71,7 @@ struct Cfg {
   // 384 threads, checked on the host before launch), the producer/MMA
   // warpgroup gives back down to LOW_REGS and each softmax warpgroup grows to
   // HIGH_REGS: 2*128*HIGH + 128*LOW == 384*LAUNCH exactly.
-  static constexpr int LAUNCH_REGS = 168, HIGH_REGS = 224, LOW_REGS = 56;
+  static constexpr int LAUNCH_REGS = 168, HIGH_REGS = 216, LOW_REGS = 72;
   static_assert(2 * 128 * HIGH_REGS + 128 * LOW_REGS <= THREADS * LAUNCH_REGS, "register split exceeds the pool");
 };
 
@@ -151,7 +151,7 @@ __device__ void producer(const FwdParams& p, uint32_t base, int bh, int row0, bo
 }
 
 // --------------------------------------------------------------------------
-// MMA issuer (one thread)
+// MMA issuer (one warp, one elected lane issues)
 // --------------------------------------------------------------------------
 template <int D, bool BF16>
 __device__ void mma_issuer(const FwdParams& p, uint32_t base, uint32_t tmem, bool has1, int nkv,
@@ -164,19 +164,19 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t base, uint32_t tmem, boo
   constexpr uint32_t idesc_pv = make_idesc(fmt, 0, 1, 128, D);
   const int nsub = has1 ? 2 : 1;
 
-  if (!wait_bar(bar_addr<D>(base, C::B_Q), 0, ctl, kWhereQ)) goto drain;
+  if (!wait_bar_warp(bar_addr<D>(base, C::B_Q), 0, ctl, kWhereQ)) goto drain;
   tc_fence_after();
   for (int j = 0; j < nkv; ++j) {
     const int s = j % C::STAGES;
     const uint32_t par = (j / C::STAGES) & 1;
-    if (!wait_bar(bar_addr<D>(base, C::B_KF + s), par, ctl, kWhereKFull)) goto drain;
+    if (!wait_bar_warp(bar_addr<D>(base, C::B_KF + s), par, ctl, kWhereKFull)) goto drain;
     tc_fence_after();
     FA_TRACE(p, kEvMmaKFull, j);
     const uint32_t kbase = base + C::OFF_K + s * C::KV_BYTES;
     for (int sub = 0; sub < nsub; ++sub) {
       if (j > 0) {
         // P_sub(j-1) lives in the S_sub columns: its P.V must be finished first.
-        if (!wait_bar(bar_addr<D>(base, C::B_OD + sub), (j - 1) & 1, ctl, kWhereODone)) goto drain;
+        if (!wait_bar_warp(bar_addr<D>(base, C::B_OD + sub), (j - 1) & 1, ctl, kWhereODone)) goto drain;
         tc_fence_after();
       }
       const uint32_t d_s = tmem + (sub ? C::T_S1 : C::T_S0);
@@ -186,19 +186,19 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t base, uint32_t tmem, boo
         const uint32_t koff = (kk & 3) * 32u;  // 16 elements = 32 bytes inside the swizzled row
         const uint64_t a = smem_desc_sw128(qbase + (kk / 4) * C::Q_HALF_BYTES + koff, 16, 1024);
         const uint64_t b = smem_desc_sw128(kbase + (kk / 4) * C::KV_HALF_BYTES + koff, 16, 1024);
-        mma_f16_ss(d_s, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+        mma_f16_ss_elect(d_s, a, b, idesc_qk, kk > 0 ? 1u : 0u);
       }
-      tc_commit(bar_addr<D>(base, C::B_SF + sub));
+      tc_commit_elect(bar_addr<D>(base, C::B_SF + sub));
       FA_TRACE(p, kEvS0Issued + sub, j);
     }
-    tc_commit(bar_addr<D>(base, C::B_KE + s));
+    tc_commit_elect(bar_addr<D>(base, C::B_KE + s));
 
-    if (!wait_bar(bar_addr<D>(base, C::B_VF + s), par, ctl, kWhereVFull)) goto drain;
+    if (!wait_bar_warp(bar_addr<D>(base, C::B_VF + s), par, ctl, kWhereVFull)) goto drain;
     tc_fence_after();
     FA_TRACE(p, kEvMmaVFull, j);
     const uint32_t vbase = base + C::OFF_V + s * C::KV_BYTES;
     for (int sub = 0; sub < nsub; ++sub) {
-      if (!wait_bar(bar_addr<D>(base, C::B_PF + sub), j & 1, ctl, kWherePFull)) goto drain;
+      if (!wait_bar_warp(bar_addr<D>(base, C::B_PF + sub), j & 1, ctl, kWherePFull)) goto drain;
       tc_fence_after();
       const uint32_t d_o = tmem + (sub ? C::T_O1 : C::T_O0);
       const uint32_t a_p = tmem + (sub ? C::T_S1 : C::T_S0);
@@ -208,17 +208,17 @@ __device__ void mma_issuer(const FwdParams& p, uint32_t base, uint32_t tmem, boo
         // With d = 64 there is one half and LBO is unused; 1024 keeps every address inside the tile.
         constexpr uint32_t lbo = (D == 64) ? 1024u : C::KV_HALF_BYTES;
         const uint64_t b = smem_desc_sw128(vbase + kk * 16 * C::ROW_BYTES, lbo, 1024);
-        mma_f16_ts(d_o, a_p + kk * 8, b, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_f16_ts_elect(d_o, a_p + kk * 8, b, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
       }
-      tc_commit(bar_addr<D>(base, C::B_OD + sub));
+      tc_commit_elect(bar_addr<D>(base, C::B_OD + sub));
       FA_TRACE(p, kEvPV0Issued + sub, j);
     }
-    tc_commit(bar_addr<D>(base, C::B_VE + s));
+    tc_commit_elect(bar_addr<D>(base, C::B_VE + s));
   }
 drain:
   // All MMAs issued by this thread complete before the CTA may free TMEM / exit.
-  tc_commit(bar_addr<D>(base, C::B_DRAIN));
-  wait_bar_drain(bar_addr<D>(base, C::B_DRAIN), 0, ctl);
+  tc_commit_elect(bar_addr<D>(base, C::B_DRAIN));
+  __all_sync(0xffffffffu, wait_bar_drain(bar_addr<D>(base, C::B_DRAIN), 0, ctl));
 }
 
 // --------------------------------------------------------------------------
@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
       if ((threadIdx.x & 31) == 0) producer<D>(p, base, bh, row0, has1, nkv, ctl);
       __syncwarp();
     } else if (warp == C::WARP_MMA) {
-      if ((threadIdx.x & 31) == 0) mma_issuer<D, BF16>(p, base, tmem, has1, nkv, ctl);
+      mma_issuer<D, BF16>(p, base, tmem, has1, nkv, ctl);
       __syncwarp();
     }
   } else {

@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(128, 1) fa_fwd_f32_kernel(const __grid_constan
     load_split_t<D, C::BN>(v, j * C::BN, p.N, base + C::OFF_VH, base + C::OFF_VL);
     fence_proxy_async_smem();
     __syncthreads();
-    if (t == 0) {
+    if (warp == 0) {
       tc_fence_after();
       // S = Qh Kh^T + Qh Kl^T + Ql Kh^T; each MMA covers 8 of the d columns.
 #pragma unroll
@@ -164,11 +164,11 @@ __global__ void __launch_bounds__(128, 1) fa_fwd_f32_kernel(const __grid_constan
         const uint64_t ql = smem_desc_sw128(base + C::OFF_QL + qblk + off, 16, 1024);
         const uint64_t kh = smem_desc_sw128(base + C::OFF_KH + kblk + off, 16, 1024);
         const uint64_t kl = smem_desc_sw128(base + C::OFF_KL + kblk + off, 16, 1024);
-        mma_tf32_ss(tmem + C::T_S, qh, kh, idesc_s, kk > 0 ? 1u : 0u);
-        mma_tf32_ss(tmem + C::T_S, qh, kl, idesc_s, 1u);
-        mma_tf32_ss(tmem + C::T_S, ql, kh, idesc_s, 1u);
+        mma_tf32_ss_elect(tmem + C::T_S, qh, kh, idesc_s, kk > 0 ? 1u : 0u);
+        mma_tf32_ss_elect(tmem + C::T_S, qh, kl, idesc_s, 1u);
+        mma_tf32_ss_elect(tmem + C::T_S, ql, kh, idesc_s, 1u);
       }
-      tc_commit(bar_s);
+      tc_commit_elect(bar_s);
     }
     __syncwarp();
     // CTA-uniform outcome: every thread takes the same path through the barriers below.
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(128, 1) fa_fwd_f32_kernel(const __grid_constan
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (t == 0) {
+    if (warp == 0) {
       tc_fence_after();
       // O += Ph Vh + Ph Vl + Pl Vh; each MMA covers 8 keys.
 #pragma unroll
@@ -240,11 +240,11 @@ __global__ void __launch_bounds__(128, 1) fa_fwd_f32_kernel(const __grid_constan
         const uint64_t pl = smem_desc_sw128(base + C::OFF_PL + poff, 16, 1024);
         const uint64_t vh = smem_desc_sw128(base + C::OFF_VH + voff, 16, 1024);
         const uint64_t vl = smem_desc_sw128(base + C::OFF_VL + voff, 16, 1024);
-        mma_tf32_ss(tmem + C::T_O, ph, vh, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_tf32_ss(tmem + C::T_O, ph, vl, idesc_o, 1u);
-        mma_tf32_ss(tmem + C::T_O, pl, vh, idesc_o, 1u);
+        mma_tf32_ss_elect(tmem + C::T_O, ph, vh, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_tf32_ss_elect(tmem + C::T_O, ph, vl, idesc_o, 1u);
+        mma_tf32_ss_elect(tmem + C::T_O, pl, vh, idesc_o, 1u);
       }
-      tc_commit(bar_o);
+      tc_commit_elect(bar_o);
     }
     __syncwarp();
     // Shared K/V/P buffers are reused by the next tile only after this P.V is done.
@@ -271,10 +271,10 @@ __global__ void __launch_bounds__(128, 1) fa_fwd_f32_kernel(const __grid_constan
       }
     }
     if (row < p.N) p.lse[static_cast<size_t>(bh) * p.N + row] = (m + lg2_approx(l)) * kLn2;
-  } else if (t == 0) {
-    // Drain: every MMA this thread issued must finish before TMEM is freed.
-    tc_commit(bar_drain);
-    wait_bar_drain(bar_drain, 0, ctl);
+  } else if (warp == 0) {
+    // Drain: every MMA this warp issued must finish before TMEM is freed.
+    tc_commit_elect(bar_drain);
+    __all_sync(0xffffffffu, wait_bar_drain(bar_drain, 0, ctl));
   }
   tc_fence_before();
   __syncthreads();
