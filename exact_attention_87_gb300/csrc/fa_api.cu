@@ -83,11 +83,12 @@ int device_info(DeviceInfo* out) {
   return d.is_sm103 ? FA_OK : FA_ERR_ARCH;
 }
 
-// [B*H, N, d] tensor of 16-bit elements, boxes of 64 (d) x 128 (rows), 128-byte swizzle.
-bool encode_bhnd_16bit(CUtensorMap* map, const void* ptr, int BH, int N, int d, CUtensorMapDataType dt) {
+// [B*H, N, d] tensor of 16-bit elements, boxes of 64 (d) x `box_rows` rows, 128-byte swizzle.
+bool encode_bhnd_16bit(CUtensorMap* map, const void* ptr, int BH, int N, int d, CUtensorMapDataType dt,
+                       int box_rows) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -168,8 +169,10 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
     const CUtensorMapDataType dt =
         dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const int bh = static_cast<int>(BH);
-    if (!encode_bhnd_16bit(&p.tm_q, Q, bh, N, d, dt) || !encode_bhnd_16bit(&p.tm_k, K, bh, N, d, dt) ||
-        !encode_bhnd_16bit(&p.tm_v, V, bh, N, d, dt) || !encode_bhnd_16bit(&p.tm_o, O, bh, N, d, dt))
+    if (!encode_bhnd_16bit(&p.tm_q, Q, bh, N, d, dt, fa::kF16BlockQ) ||
+        !encode_bhnd_16bit(&p.tm_k, K, bh, N, d, dt, fa::kF16BlockKV) ||
+        !encode_bhnd_16bit(&p.tm_v, V, bh, N, d, dt, fa::kF16BlockKV) ||
+        !encode_bhnd_16bit(&p.tm_o, O, bh, N, d, dt, fa::kF16BlockQ))
       return FA_ERR_CUDA;
     e = fa::launch_fwd_f16(p, dtype == FA_BF16, s);
   }

@@ -12,22 +12,34 @@
 
 namespace fa {
 
+// Everything a bounded wait needs: the CTA's abort flag (a shared-memory
+// address) and the kernel parameters (status word, wait limit). Kept small:
+// once inlined, the parameter reads come from the kernel's parameter space.
 struct WaitCtl {
-  volatile int* abort_flag;  // shared memory, one per CTA
-  unsigned int* status;      // [0] flags, [1] where
-  long long limit;
+  const FwdParams& p;   // the kernel's __grid_constant__ parameters
+  uint32_t abort_addr;  // shared-memory address of the CTA's abort flag
 };
 
+__device__ __forceinline__ int abort_raised(uint32_t addr) {
+  int v;
+  asm volatile("ld.volatile.shared.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+static __device__ __forceinline__ void record_timeout(const FwdParams& p, uint32_t abort_addr, unsigned where) {
+  atomicOr(p.status, kStatusTimeout);
+  atomicCAS(p.status + 1, 0u, where);
+  asm volatile("st.volatile.shared.s32 [%0], %1;" ::"r"(abort_addr), "r"(1) : "memory");
+}
+
 __device__ __forceinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, const WaitCtl& ctl, unsigned where,
-                                           bool honour_abort) {
+                                              bool honour_abort) {
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (honour_abort && *ctl.abort_flag) return false;
-    if (clock64() - t0 > ctl.limit) {
-      atomicOr(ctl.status, kStatusTimeout);
-      atomicCAS(ctl.status + 1, 0u, where);
-      *ctl.abort_flag = 1;
+    if (honour_abort && abort_raised(ctl.abort_addr)) return false;
+    if (clock64() - t0 > ctl.p.wait_limit) {
+      record_timeout(ctl.p, ctl.abort_addr, where);
       return false;
     }
   }

@@ -8,17 +8,25 @@
 // page, section 2.3, stresses that order), and O is divided by l at the end.
 // The loop order (Q outer, K/V inner, Q loaded once) is the dataflow page's
 // section 2.2; the parallelisation over Q tiles is the guide's FlashAttention-2
-// "sequence parallelism" note.
+// "sequence parallelism" note; overlapping the next tile's Q K^T with the
+// current tile's softmax is the guide's FlashAttention-3 pipelining note.
 //
 // GB300 mapping (one CTA per (batch*head, 256-row Q block), 12 warps):
-//   warp 9      TMA producer: Q0/Q1 once, then K_j and V_j into 2-3 stage rings
-//   warp 8      MMA issuer:   S_i = Q_i K_j^T (SS, into TMEM), O_i += P_i V_j
-//                             (TS: P read from TMEM, V from SMEM); also owns TMEM
+//   warp 9      TMA producer: Q0/Q1 once, then K_j and V_j (128 keys each)
+//               into 2-stage (d=128) / 3-stage (d=64) rings
+//   warps 8, 10 MMA warps, one per Q sub-tile i: S_i(j) = Q_i K_j^T (SS, into
+//               TMEM), then O_i += P_i(j) V_j (TS: P read from TMEM, V from
+//               SMEM); one elected lane issues; warp 8 also owns TMEM
 //   warps 0-3   softmax for Q rows 0-127   (thread = row; TMEM lanes = rows)
 //   warps 4-7   softmax for Q rows 128-255
-//   warps 10-11 idle (complete the third warpgroup for the register split)
-// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [256+d, 256+2d).
-// P_i (16-bit, packed in pairs) overwrites the first 64 columns of S_i.
+//   warp 11     idle (completes the third warpgroup for the register split)
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [256+d,256+2d).
+// P_i(j) (16-bit, packed in pairs) overwrites the first 64 columns of S_i, so
+// S_i(j+1) is issued once P_i(j) V_j has completed (the tensor core only
+// orders MMAs on the same accumulator). One MMA warp per sub-tile drives the
+// chain S_i -> softmax_i -> P_i V -> S_i; the two warps pass a turn so that
+// their MMA blocks alternate (ping-pong) and each runs inside the other
+// chain's softmax.
 // The rescale of O is lazy: the reference max only moves when the tile max
 // exceeds it by more than 8 (log2 units), so P <= 256 and rescales are rare.
 // The epilogue divides by l, rounds to the input type, stages the tile in the
@@ -37,8 +45,8 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8
 
 template <int D>
 struct Cfg {
-  static constexpr int BM = 128;  // Q rows per sub-tile (= TMEM lanes)
-  static constexpr int BN = 128;  // keys per K/V tile
+  static constexpr int BM = kF16BlockQ;   // Q rows per sub-tile (= TMEM lanes)
+  static constexpr int BN = kF16BlockKV;  // keys per K/V tile
   static constexpr int STAGES = (D == 128) ? 2 : 3;
   static constexpr uint32_t ROW_BYTES = 128;               // one 128-byte swizzle row = 64 elements
   static constexpr uint32_t Q_SUB_BYTES = BM * D * 2;      // one Q sub-tile
@@ -49,7 +57,8 @@ struct Cfg {
   static constexpr uint32_t OFF_K = OFF_Q + 2 * Q_SUB_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;
-  // barriers: q | k_full[S] | k_empty[S] | v_full[S] | v_empty[S] | s_full[2] | p_full[2] | o_done[2] | drain
+  // barriers: q | k_full[S] | k_empty[S] | v_full[S] | v_empty[S] |
+  //           s_full[2] | p_full[2] | o_done[2] | drain[2] | turn[2]     ([sub])
   static constexpr int B_Q = 0;
   static constexpr int B_KF = 1;
   static constexpr int B_KE = B_KF + STAGES;
@@ -59,26 +68,26 @@ struct Cfg {
   static constexpr int B_PF = B_SF + 2;
   static constexpr int B_OD = B_PF + 2;
   static constexpr int B_DRAIN = B_OD + 2;
-  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr int B_TURN = B_DRAIN + 2;
+  static constexpr int NBAR = B_TURN + 2;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t T_S0 = 0, T_S1 = 128, T_O0 = 256, T_O1 = 256 + D;
-  // 3 warpgroups: softmax sub-tile 0, softmax sub-tile 1, and {MMA, TMA, 2 idle} warps.
+  static constexpr uint32_t T_O0 = 256, T_O1 = 256 + D;
+  // 3 warpgroups: softmax sub-tile 0, softmax sub-tile 1, and {MMA 0, TMA, MMA 1, idle} warps.
   static constexpr int THREADS = 384;
-  static constexpr int WARP_MMA = 8, WARP_TMA = 9;
+  static constexpr int WARP_MMA0 = 8, WARP_TMA = 9, WARP_MMA1 = 10;
   // Register split: launched at LAUNCH_REGS per thread (the compiler's count for
   // 384 threads, checked on the host before launch), the producer/MMA
   // warpgroup gives back down to LOW_REGS and each softmax warpgroup grows to
-  // HIGH_REGS: 2*128*HIGH + 128*LOW == 384*LAUNCH exactly.
+  // HIGH_REGS: 2*128*HIGH + 128*LOW <= 384*LAUNCH.
   static constexpr int LAUNCH_REGS = 168, HIGH_REGS = 216, LOW_REGS = 72;
   static_assert(2 * 128 * HIGH_REGS + 128 * LOW_REGS <= THREADS * LAUNCH_REGS, "register split exceeds the pool");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-struct Smem {
-  uint32_t base;  // shared-space address, 1024-aligned
-  uint8_t* ptr;   // generic pointer to the same byte
-};
+// TMEM column of S_i (and of P_i, which overwrites its first 64 columns).
+__device__ __forceinline__ uint32_t t_s_col(int sub) { return 128u * sub; }
 
 template <int D>
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) {
@@ -89,7 +98,7 @@ __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) {
 // TMA producer (one thread)
 // --------------------------------------------------------------------------
 template <int D>
-__device__ void producer(const FwdParams& p, uint32_t base, int bh, int row0, bool has1, int nkv,
+__device__ __forceinline__ void producer(const FwdParams& p, uint32_t base, int bh, int row0, bool has1, int nkv,
                          const WaitCtl& ctl) {
   using C = Cfg<D>;
   tma_prefetch_desc(&p.tm_q);
@@ -103,15 +112,11 @@ __device__ void producer(const FwdParams& p, uint32_t base, int bh, int row0, bo
 #pragma unroll
     for (int h = 0; h < D / 64; ++h)
       tma_load_3d(base + C::OFF_Q + sub * C::Q_SUB_BYTES + h * C::Q_HALF_BYTES, &p.tm_q, bq, 64 * h,
-                  row0 + 128 * sub, bh);
+                  row0 + C::BM * sub, bh);
 
-  // parity of the most recent phase armed on each full barrier (-1: never armed)
-  int k_armed[C::STAGES], v_armed[C::STAGES];
-#pragma unroll
-  for (int s = 0; s < C::STAGES; ++s) k_armed[s] = v_armed[s] = -1;
-
+  int nk = 0, nv = 0;  // K / V tiles whose loads were issued
   bool ok = true;
-  for (int j = 0; j < nkv && ok; ++j) {
+  for (int j = 0; j < nkv; ++j) {
     const int s = j % C::STAGES;
     const uint32_t par = ((j / C::STAGES) & 1) ^ 1;
     if (!wait_bar(bar_addr<D>(base, C::B_KE + s), par, ctl, kWhereKEmpty)) { ok = false; break; }
@@ -120,10 +125,7 @@ __device__ void producer(const FwdParams& p, uint32_t base, int bh, int row0, bo
 #pragma unroll
     for (int h = 0; h < D / 64; ++h)
       tma_load_3d(base + C::OFF_K + s * C::KV_BYTES + h * C::KV_HALF_BYTES, &p.tm_k, kf, 64 * h, j * C::BN, bh);
-#pragma unroll
-    for (int t = 0; t < C::STAGES; ++t)
-      if (t == s) k_armed[t] = (j / C::STAGES) & 1;
-
+    nk = j + 1;
     FA_TRACE(p, kEvKIssued, j);
 #ifdef FA_TESTING
     if (p.inject == 1 && j == 0) continue;  // fault injection: V_0 is never loaded
@@ -134,108 +136,120 @@ __device__ void producer(const FwdParams& p, uint32_t base, int bh, int row0, bo
 #pragma unroll
     for (int h = 0; h < D / 64; ++h)
       tma_load_3d(base + C::OFF_V + s * C::KV_BYTES + h * C::KV_HALF_BYTES, &p.tm_v, vf, 64 * h, j * C::BN, bh);
-#pragma unroll
-    for (int t = 0; t < C::STAGES; ++t)
-      if (t == s) v_armed[t] = (j / C::STAGES) & 1;
+    nv = j + 1;
     FA_TRACE(p, kEvVIssued, j);
   }
   if (!ok) {
-    // Drain: every copy this thread started must land before the CTA exits.
+    // Drain: every copy this thread started must land before the CTA exits. The
+    // most recent load of each stage is one of the last STAGES tiles issued.
     wait_bar_drain(bq, 0, ctl);
-#pragma unroll
-    for (int s = 0; s < C::STAGES; ++s) {
-      if (k_armed[s] >= 0) wait_bar_drain(bar_addr<D>(base, C::B_KF + s), (uint32_t)k_armed[s], ctl);
-      if (v_armed[s] >= 0) wait_bar_drain(bar_addr<D>(base, C::B_VF + s), (uint32_t)v_armed[s], ctl);
+    for (int t = nk > C::STAGES ? nk - C::STAGES : 0; t < nk; ++t)
+      wait_bar_drain(bar_addr<D>(base, C::B_KF + t % C::STAGES), (t / C::STAGES) & 1, ctl);
+    for (int t = nv > C::STAGES ? nv - C::STAGES : 0; t < nv; ++t) {
+#ifdef FA_TESTING
+      if (p.inject == 1 && t == 0) continue;  // never armed
+#endif
+      wait_bar_drain(bar_addr<D>(base, C::B_VF + t % C::STAGES), (t / C::STAGES) & 1, ctl);
     }
   }
 }
 
 // --------------------------------------------------------------------------
-// MMA issuer (one warp, one elected lane issues)
+// MMA warp of Q sub-tile `sub` (whole warp; one elected lane issues)
 // --------------------------------------------------------------------------
-template <int D, bool BF16>
-__device__ void mma_issuer(const FwdParams& p, uint32_t base, uint32_t tmem, bool has1, int nkv,
-                           const WaitCtl& ctl) {
+// Chain i alternates on the tensor pipe with the other sub-tile's chain in
+// blocks B_i(j) = { P_i(j-1) V_{j-1} ; S_i(j) = Q_i K_j^T }, in the order
+// B_0(0), B_1(0), B_0(1), B_1(1), ... A warp passes the turn (an mbarrier
+// arrival) after issuing its block. Between its blocks each chain runs its
+// softmax, so one chain's block executes inside the other chain's softmax
+// window instead of both chains requesting the pipe at the same time.
+template <int D, bool BF16, int SUB>
+__device__ __forceinline__ void mma_warp(const FwdParams& p, uint32_t base, uint32_t tmem, bool has1, int nkv,
+                                         const WaitCtl& ctl) {
   using C = Cfg<D>;
+  constexpr int sub = SUB;
   constexpr uint32_t fmt = BF16 ? 1u : 0u;
   // S = Q K^T: A = Q (K-major), B = K tile (K-major), M = 128, N = 128.
   constexpr uint32_t idesc_qk = make_idesc(fmt, 0, 0, 128, C::BN);
   // O += P V: A = P from TMEM (K-major), B = V tile, N (= d) contiguous -> MN-major.
   constexpr uint32_t idesc_pv = make_idesc(fmt, 0, 1, 128, D);
-  const int nsub = has1 ? 2 : 1;
+  // 16 keys = two 8-row swizzle atoms (SBO apart); the two 64-wide halves of d are LBO apart.
+  // With d = 64 there is one half and LBO is unused; 1024 keeps every address inside the tile.
+  constexpr uint32_t lbo = (D == 64) ? 1024u : C::KV_HALF_BYTES;
+  const uint32_t d_s = tmem + t_s_col(sub);
+  const uint32_t d_o = tmem + (sub ? C::T_O1 : C::T_O0);
+  const uint32_t qbase = base + C::OFF_Q + sub * C::Q_SUB_BYTES;
+  const uint32_t b_sf = bar_addr<D>(base, C::B_SF + sub), b_pf = bar_addr<D>(base, C::B_PF + sub);
+  const uint32_t b_od = bar_addr<D>(base, C::B_OD + sub), b_drain = bar_addr<D>(base, C::B_DRAIN + sub);
+  const uint32_t my_turn = bar_addr<D>(base, C::B_TURN + sub), next_turn = bar_addr<D>(base, C::B_TURN + (sub ^ 1));
 
   if (!wait_bar_warp(bar_addr<D>(base, C::B_Q), 0, ctl, kWhereQ)) goto drain;
   tc_fence_after();
-  for (int j = 0; j < nkv; ++j) {
-    const int s = j % C::STAGES;
-    const uint32_t par = (j / C::STAGES) & 1;
-    if (!wait_bar_warp(bar_addr<D>(base, C::B_KF + s), par, ctl, kWhereKFull)) goto drain;
-    tc_fence_after();
-    FA_TRACE(p, kEvMmaKFull, j);
-    const uint32_t kbase = base + C::OFF_K + s * C::KV_BYTES;
-    for (int sub = 0; sub < nsub; ++sub) {
-      if (j > 0) {
-        // P_sub(j-1) lives in the S_sub columns: its P.V must be finished first.
-        if (!wait_bar_warp(bar_addr<D>(base, C::B_OD + sub), (j - 1) & 1, ctl, kWhereODone)) goto drain;
-        tc_fence_after();
-      }
-      const uint32_t d_s = tmem + (sub ? C::T_S1 : C::T_S0);
-      const uint32_t qbase = base + C::OFF_Q + sub * C::Q_SUB_BYTES;
+  for (int j = 0; j <= nkv; ++j) {
+    // My block j follows the other chain's block j-1 (sub 0) or block j (sub 1).
+    if (has1 && (sub == 1 || j > 0)) {
+      if (!wait_bar_warp(my_turn, (sub == 1 ? j : j - 1) & 1, ctl, kWhereTurn)) goto drain;
+    }
+    if (j > 0) {
+      // P(j-1) V_{j-1}
+      const int s = (j - 1) % C::STAGES;
+      if (!wait_bar_warp(bar_addr<D>(base, C::B_VF + s), ((j - 1) / C::STAGES) & 1, ctl, kWhereVFull)) goto drain;
+      if (!wait_bar_warp(b_pf, (j - 1) & 1, ctl, kWherePFull)) goto drain;
+      tc_fence_after();
+      if (sub == 0) FA_TRACE(p, kEvMmaVFull, j - 1);
+      const uint64_t v0 = smem_desc_sw128(base + C::OFF_V + s * C::KV_BYTES, lbo, 1024);
+#pragma unroll
+      for (int kk = 0; kk < C::BN / 16; ++kk)
+        mma_f16_ts_elect(d_o, d_s + kk * 8, v0 + ((kk * 16 * C::ROW_BYTES) >> 4), idesc_pv,
+                         (j > 1 || kk > 0) ? 1u : 0u);
+      tc_commit_elect(b_od);
+      tc_commit_elect(bar_addr<D>(base, C::B_VE + s));
+      FA_TRACE(p, kEvPV0Issued + sub, j - 1);
+    }
+    if (j < nkv) {
+      // S(j) = Q K_j^T; P(j-1) lives in the S columns, so its P.V must be finished first.
+      const int s = j % C::STAGES;
+      if (!wait_bar_warp(bar_addr<D>(base, C::B_KF + s), (j / C::STAGES) & 1, ctl, kWhereKFull)) goto drain;
+      if (j > 0 && !wait_bar_warp(b_od, (j - 1) & 1, ctl, kWhereODone)) goto drain;
+      tc_fence_after();
+      if (sub == 0) FA_TRACE(p, kEvMmaKFull, j);
+      // Descriptors of k-step 0; later k-steps advance the 14-bit start-address
+      // field (bytes >> 4), which cannot carry out since shared addresses < 2^18.
+      const uint64_t a0 = smem_desc_sw128(qbase, 16, 1024);
+      const uint64_t b0 = smem_desc_sw128(base + C::OFF_K + s * C::KV_BYTES, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t koff = (kk & 3) * 32u;  // 16 elements = 32 bytes inside the swizzled row
-        const uint64_t a = smem_desc_sw128(qbase + (kk / 4) * C::Q_HALF_BYTES + koff, 16, 1024);
-        const uint64_t b = smem_desc_sw128(kbase + (kk / 4) * C::KV_HALF_BYTES + koff, 16, 1024);
-        mma_f16_ss_elect(d_s, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+        // 16 elements = 32 bytes inside the swizzled row; every 4 k-steps the next 64-column half
+        const uint32_t aoff = ((kk / 4) * C::Q_HALF_BYTES + (kk & 3) * 32u) >> 4;
+        const uint32_t boff = ((kk / 4) * C::KV_HALF_BYTES + (kk & 3) * 32u) >> 4;
+        mma_f16_ss_elect(d_s, a0 + aoff, b0 + boff, idesc_qk, kk > 0 ? 1u : 0u);
       }
-      tc_commit_elect(bar_addr<D>(base, C::B_SF + sub));
+      tc_commit_elect(b_sf);
+      tc_commit_elect(bar_addr<D>(base, C::B_KE + s));  // one of the (nsub) releases of this K stage
       FA_TRACE(p, kEvS0Issued + sub, j);
     }
-    tc_commit_elect(bar_addr<D>(base, C::B_KE + s));
-
-    if (!wait_bar_warp(bar_addr<D>(base, C::B_VF + s), par, ctl, kWhereVFull)) goto drain;
-    tc_fence_after();
-    FA_TRACE(p, kEvMmaVFull, j);
-    const uint32_t vbase = base + C::OFF_V + s * C::KV_BYTES;
-    for (int sub = 0; sub < nsub; ++sub) {
-      if (!wait_bar_warp(bar_addr<D>(base, C::B_PF + sub), j & 1, ctl, kWherePFull)) goto drain;
-      tc_fence_after();
-      const uint32_t d_o = tmem + (sub ? C::T_O1 : C::T_O0);
-      const uint32_t a_p = tmem + (sub ? C::T_S1 : C::T_S0);
-#pragma unroll
-      for (int kk = 0; kk < C::BN / 16; ++kk) {
-        // 16 keys = two 8-row swizzle atoms (SBO apart); the two 64-wide halves of d are LBO apart.
-        // With d = 64 there is one half and LBO is unused; 1024 keeps every address inside the tile.
-        constexpr uint32_t lbo = (D == 64) ? 1024u : C::KV_HALF_BYTES;
-        const uint64_t b = smem_desc_sw128(vbase + kk * 16 * C::ROW_BYTES, lbo, 1024);
-        mma_f16_ts_elect(d_o, a_p + kk * 8, b, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-      }
-      tc_commit_elect(bar_addr<D>(base, C::B_OD + sub));
-      FA_TRACE(p, kEvPV0Issued + sub, j);
+    if (has1) {
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(next_turn);
     }
-    tc_commit_elect(bar_addr<D>(base, C::B_VE + s));
   }
 drain:
-  // All MMAs issued by this thread complete before the CTA may free TMEM / exit.
-  tc_commit_elect(bar_addr<D>(base, C::B_DRAIN));
-  __all_sync(0xffffffffu, wait_bar_drain(bar_addr<D>(base, C::B_DRAIN), 0, ctl));
+  // All MMAs issued by this warp complete before the CTA may free TMEM / exit.
+  tc_commit_elect(b_drain);
+  __all_sync(0xffffffffu, wait_bar_drain(b_drain, 0, ctl));
 }
 
 // --------------------------------------------------------------------------
 // Softmax + lazy correction + epilogue (one warpgroup per Q sub-tile)
 // --------------------------------------------------------------------------
 template <int D, bool BF16>
-__device__ void softmax_wg(const FwdParams& p, uint32_t base, uint32_t tmem, int sub, int bh, int row0, int nkv,
+__device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, uint32_t tmem, int sub, int bh, int row0, int nkv,
                            const WaitCtl& ctl) {
   using C = Cfg<D>;
   const int t = threadIdx.x - sub * 128;  // row within the sub-tile
   const int lane = threadIdx.x & 31;
   const uint32_t lane_base = static_cast<uint32_t>(t & ~31) << 16;
-  const uint32_t t_s = tmem + lane_base + (sub ? C::T_S1 : C::T_S0);
   const uint32_t t_o = tmem + lane_base + (sub ? C::T_O1 : C::T_O0);
-  const uint32_t b_sf = bar_addr<D>(base, C::B_SF + sub);
-  const uint32_t b_pf = bar_addr<D>(base, C::B_PF + sub);
-  const uint32_t b_od = bar_addr<D>(base, C::B_OD + sub);
   const float c = p.scale * kLog2e;  // scores in log2 units: x = s * c
 
   float m_ref = -INFINITY;  // reference max (log2 units) shared by l and O
@@ -243,9 +257,16 @@ __device__ void softmax_wg(const FwdParams& p, uint32_t base, uint32_t tmem, int
   float l_o = 0.f;          // bf16 only: sum of the rounded P: normalises O
   bool ok = true;
 
+  const uint32_t t_s = tmem + lane_base + t_s_col(sub);
+  const uint32_t b_sf = bar_addr<D>(base, C::B_SF + sub), b_pf = bar_addr<D>(base, C::B_PF + sub);
+  const uint32_t b_od = bar_addr<D>(base, C::B_OD + sub);
+
   for (int j = 0; j < nkv; ++j) {
     // Wait results are made warp-uniform: TMEM loads/stores below need the whole warp.
-    if (!__all_sync(0xffffffffu, wait_bar(b_sf, j & 1, ctl, kWhereSFull))) { ok = false; break; }
+    if (!__all_sync(0xffffffffu, wait_bar(b_sf, j & 1, ctl, kWhereSFull))) {
+      ok = false;
+      break;
+    }
     tc_fence_after();
     if (t == 0) FA_TRACE(p, kEvSm0SFull + 2 * sub, j);
     uint32_t sraw[C::BN / 32][32];
@@ -319,8 +340,11 @@ __device__ void softmax_wg(const FwdParams& p, uint32_t base, uint32_t tmem, int
     l += se.x + se.y;
     if constexpr (BF16) l_o += sro.x + sro.y;
     if (rescale_o) {
-      // O_j-1 must be complete (its P.V finished) before it is read and scaled.
-      if (!__all_sync(0xffffffffu, wait_bar(b_od, (j - 1) & 1, ctl, kWhereODone))) { ok = false; break; }
+      // O must be complete up to tile j-1 (its P.V finished) before it is read and scaled.
+      if (!__all_sync(0xffffffffu, wait_bar(b_od, (j - 1) & 1, ctl, kWhereODone))) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {
@@ -340,7 +364,7 @@ __device__ void softmax_wg(const FwdParams& p, uint32_t base, uint32_t tmem, int
     if (t == 0) FA_TRACE(p, kEvSm0PArrive + 2 * sub, j);
 #ifdef FA_TESTING
     if (p.stats_trace) {
-      const int row = row0 + 128 * sub + t;
+      const int row = row0 + C::BM * sub + t;
       if (row < p.N) {
         float* tr = p.stats_trace + ((static_cast<size_t>(bh) * p.N + row) * nkv + j) * 2;
         tr[0] = m_ref * kLn2;
@@ -349,7 +373,9 @@ __device__ void softmax_wg(const FwdParams& p, uint32_t base, uint32_t tmem, int
     }
 #endif
   }
-  if (ok) ok = __all_sync(0xffffffffu, wait_bar(b_od, (nkv - 1) & 1, ctl, kWhereODone));
+  // The last P.V of this sub-tile; its commit also covers every earlier MMA of the warp.
+  if (ok)
+    ok = __all_sync(0xffffffffu, wait_bar(b_od, (nkv - 1) & 1, ctl, kWhereODone));
   // The whole warpgroup agrees before the epilogue, whose named barrier needs all 128 threads.
   if (!named_bar_and(1 + sub, 128, ok)) return;
 
@@ -382,11 +408,12 @@ __device__ void softmax_wg(const FwdParams& p, uint32_t base, uint32_t tmem, int
   named_bar_sync(1 + sub, 128);
   if (t == 0) {
 #pragma unroll
-    for (int h = 0; h < D / 64; ++h) tma_store_3d(&p.tm_o, stage + h * C::Q_HALF_BYTES, 64 * h, row0 + 128 * sub, bh);
+    for (int h = 0; h < D / 64; ++h)
+      tma_store_3d(&p.tm_o, stage + h * C::Q_HALF_BYTES, 64 * h, row0 + C::BM * sub, bh);
     tma_store_commit();
     tma_store_wait_all();
   }
-  const int row = row0 + 128 * sub + t;
+  const int row = row0 + C::BM * sub + t;
   if (row < p.N) p.lse[static_cast<size_t>(bh) * p.N + row] = (m_ref + lg2_approx(l)) * kLn2;
 }
 
@@ -399,30 +426,32 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem_raw + (base - raw) + C::OFF_MISC);
 
   const int warp = threadIdx.x >> 5;
-  const int nqb = (p.N + 255) / 256;
+  const int nqb = (p.N + 2 * C::BM - 1) / (2 * C::BM);
   const int bh = blockIdx.x / nqb;
-  const int row0 = (blockIdx.x % nqb) * 256;
-  const bool has1 = row0 + 128 < p.N;
+  const int row0 = (blockIdx.x % nqb) * 2 * C::BM;
+  const bool has1 = row0 + C::BM < p.N;
   const int nkv = (p.N + C::BN - 1) / C::BN;
 
   if (threadIdx.x == 0) {
     mbar_init(bar_addr<D>(base, C::B_Q), 1);
+    const uint32_t nsub = has1 ? 2u : 1u;  // the stage-empty barriers get one commit per MMA warp
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar_addr<D>(base, C::B_KF + s), 1);
-      mbar_init(bar_addr<D>(base, C::B_KE + s), 1);
+      mbar_init(bar_addr<D>(base, C::B_KE + s), nsub);
       mbar_init(bar_addr<D>(base, C::B_VF + s), 1);
-      mbar_init(bar_addr<D>(base, C::B_VE + s), 1);
+      mbar_init(bar_addr<D>(base, C::B_VE + s), nsub);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_addr<D>(base, C::B_SF + i), 1);
       mbar_init(bar_addr<D>(base, C::B_PF + i), 4);  // one arrival per softmax warp
       mbar_init(bar_addr<D>(base, C::B_OD + i), 1);
+      mbar_init(bar_addr<D>(base, C::B_DRAIN + i), 1);
+      mbar_init(bar_addr<D>(base, C::B_TURN + i), 1);
     }
-    mbar_init(bar_addr<D>(base, C::B_DRAIN), 1);
     misc[1] = 0;
     mbar_init_fence();
   }
-  if (warp == C::WARP_MMA) {
+  if (warp == C::WARP_MMA0) {
     tmem_alloc(base + C::OFF_MISC, C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -430,7 +459,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  WaitCtl ctl{reinterpret_cast<volatile int*>(&misc[1]), p.status, p.wait_limit};
+  const WaitCtl ctl{p, base + C::OFF_MISC + 4};  // misc[1] is the abort flag
   if (threadIdx.x == 0) FA_TRACE(p, kEvCta, 0);
 
   if (warp >= 8) {
@@ -438,8 +467,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
     if (warp == C::WARP_TMA) {
       if ((threadIdx.x & 31) == 0) producer<D>(p, base, bh, row0, has1, nkv, ctl);
       __syncwarp();
-    } else if (warp == C::WARP_MMA) {
-      mma_issuer<D, BF16>(p, base, tmem, has1, nkv, ctl);
+    } else if (warp == C::WARP_MMA0 || (warp == C::WARP_MMA1 && has1)) {
+      if (warp == C::WARP_MMA0)
+        mma_warp<D, BF16, 0>(p, base, tmem, has1, nkv, ctl);
+      else
+        mma_warp<D, BF16, 1>(p, base, tmem, has1, nkv, ctl);
       __syncwarp();
     }
   } else {
@@ -460,7 +492,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
     }
 #endif
   }
-  if (warp == C::WARP_MMA) {
+  if (warp == C::WARP_MMA0) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -486,7 +518,7 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(bit);
   }
-  const long long units = static_cast<long long>(p.B) * p.H * ((p.N + 255) / 256);
+  const long long units = static_cast<long long>(p.B) * p.H * ((p.N + 2 * C::BM - 1) / (2 * C::BM));
   if (units <= 0 || units > 0x7fffffffLL) return cudaErrorInvalidValue;
   kern<<<dim3(static_cast<unsigned>(units)), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();

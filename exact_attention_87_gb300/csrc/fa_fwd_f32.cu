@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(128, 1) fa_fwd_f32_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  WaitCtl ctl{reinterpret_cast<volatile int*>(&misc[1]), p.status, p.wait_limit};
+  const WaitCtl ctl{p, base + C::OFF_MISC + 4};  // misc[1] is the abort flag
   const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
   const uint32_t t_s = tmem + lane_base + C::T_S, t_o = tmem + lane_base + C::T_O;
 

@@ -15,7 +15,7 @@ enum : unsigned int {
 // Where a wait gave up (stored in bits 8-15 of the status word, first writer wins).
 enum : unsigned int {
   kWhereQ = 1, kWhereKEmpty, kWhereVEmpty, kWhereKFull, kWhereVFull, kWhereSFull, kWherePFull,
-  kWhereODone, kWhereDrain, kWhereF32Mma
+  kWhereODone, kWhereDrain, kWhereF32Mma, kWhereTurn
 };
 
 // Everything a forward kernel needs; passed by value as a __grid_constant__.
@@ -39,6 +39,10 @@ struct alignas(64) FwdParams {
   float* stats_trace;               // [B*H*N, nkv, 2]: (m in natural-log units, l) after each K/V tile
   unsigned long long* timeline;     // [kTraceCtas, kTraceEvents, kTraceTiles] clock64 stamps
 };
+
+// Tile sizes of the fp16/bf16 kernel: Q rows per sub-tile (two sub-tiles per
+// CTA) and keys per K/V tile; the host encodes the TMA boxes with them.
+constexpr int kF16BlockQ = 128, kF16BlockKV = 128;
 
 // Timeline trace layout of the testing build.
 constexpr int kTraceCtas = 8, kTraceTiles = 64, kTraceEvents = 16;
