@@ -44,18 +44,24 @@ def up_to_date(lib_path: str = LIB_PATH) -> bool:
 
 
 TESTING_LIB_PATH = os.path.join(HERE, "libfa_gb300_testing.so")
+STRICT_LIB_PATH = os.path.join(HERE, "libfa_gb300_strict.so")
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None, testing: bool = False) -> str:
-    """Build the product library, or with testing=True the instrumented testing
-    library (-DFA_TESTING: stats/timeline traces and fault injection)."""
-    lib_path = TESTING_LIB_PATH if testing else LIB_PATH
+def build(force: bool = False, verbose: bool = False, extra_flags=None, testing: bool = False,
+          strict: bool = False) -> str:
+    """Build the product library; with testing=True the instrumented testing
+    library (-DFA_TESTING: stats/timeline traces and fault injection); with
+    strict=True a variant that waits for each P.V to complete before the next
+    S = Q K^T reuses its tensor-memory columns (-DFA_STRICT_MMA_ORDER), used by
+    the tests to check the default issue order bit for bit."""
+    lib_path = TESTING_LIB_PATH if testing else STRICT_LIB_PATH if strict else LIB_PATH
     if not force and up_to_date(lib_path):
         return lib_path
     cc = nvcc()
-    objdir = os.path.join(HERE, "_build_testing" if testing else "_build")
+    objdir = os.path.join(HERE, "_build_testing" if testing else "_build_strict" if strict else "_build")
     os.makedirs(objdir, exist_ok=True)
-    extra = list(extra_flags or []) + (["-DFA_TESTING"] if testing else [])
+    extra = list(extra_flags or []) + (["-DFA_TESTING"] if testing else []) + \
+        (["-DFA_STRICT_MMA_ORDER"] if strict else [])
 
     def compile_one(src):
         obj = os.path.join(objdir, os.path.splitext(src)[0] + ".o")

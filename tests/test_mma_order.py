@@ -1,0 +1,49 @@
+"""The default MMA issue order against the strictly ordered build, bit for bit.
+
+P_i(j) lives in the tensor-memory columns of S_i, and the default build issues
+S_i(j+1) right behind P_i(j) V_j, relying on one CTA's MMAs executing in issue
+order. The strict build (-DFA_STRICT_MMA_ORDER) instead waits for P_i(j) V_j
+to complete. Both run the same MMAs with the same accumulation order, so their
+outputs must be identical bit for bit; any overwrite of P before it was read
+would show up as a difference.
+"""
+import ctypes
+
+import pytest
+import torch
+
+import exact_attention_87_gb300 as fa
+from exact_attention_87_gb300 import _build
+from workloads import make_qkv
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def strict_lib():
+    L = ctypes.CDLL(_build.build(strict=True))
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    L.fa_fwd.restype = i
+    return L
+
+
+@pytest.mark.parametrize("B,H,N,d,dtype,sig", [
+    (2, 16, 4096, 128, "bf16", 3.0),
+    (1, 8, 8192, 128, "f16", 1.0),
+    (4, 8, 1000, 64, "bf16", 1.0),
+    (3, 5, 777, 128, "f16", 2.0),
+])
+def test_default_order_equals_strict_order(strict_lib, B, H, N, d, dtype, sig):
+    q, k, v = (t.cuda() for t in make_qkv(B, H, N, d, dtype, sigma_qk=sig, seed=21, wid=9000 + N))
+    o1, l1 = fa.attention(q, k, v)
+    o2, l2 = torch.empty_like(o1), torch.empty_like(l1)
+    code = fa.FA_BF16 if dtype == "bf16" else fa.FA_F16
+    stream = torch.cuda.current_stream().cuda_stream
+    for _ in range(3):
+        rc = strict_lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o2.data_ptr(), l2.data_ptr(),
+                               B, H, N, d, 1.0 / d ** 0.5, code, stream)
+        assert rc == fa.FA_OK
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+        o1, l1 = fa.attention(q, k, v)
