@@ -17,6 +17,8 @@ page, sections "计算流程" and "标准 Softmax 回顾"):
 all in fp64 from the already-rounded inputs (fp16/bf16/fp32 upcast exactly).
 ``attn_online`` is the tiled recurrence of the same page's "FlashAttention
 完整算法" formula, in fp64, with an optional lazy-rescale threshold.
+``merge`` combines results computed over disjoint key ranges with the block
+merge of the Triton page (section 2.3), for split-KV.
 """
 from __future__ import annotations
 
@@ -49,6 +51,8 @@ def _bind(path: str):
     lib.oracle_attn_fp64.restype = I
     lib.oracle_attn_online_fp64.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, D, L, D, dp, dp, I]
     lib.oracle_attn_online_fp64.restype = I
+    lib.oracle_merge_fp64.argtypes = [dp, dp, L, L, L, dp, dp]
+    lib.oracle_merge_fp64.restype = I
     lib.oracle_mutant_id.restype = I
     return lib
 
@@ -130,6 +134,26 @@ def attn_online(q, k, v, block_n: int, tau: float = 0.0, scale: float | None = N
     if rc != 0:
         raise RuntimeError(f"oracle_attn_online_fp64 failed ({rc})")
     return (o, lse, tm, tl) if trace else (o, lse)
+
+
+def merge(o_parts, lse_parts, lib=None):
+    """Merge results over disjoint key ranges (block merge of the Triton page, section 2.3).
+
+    o_parts [P, ..., d] (each part's normalised O), lse_parts [P, ...] -> (O, LSE) fp64.
+    """
+    o_parts, lse_parts = _f64(o_parts), _f64(lse_parts)
+    P = o_parts.shape[0]
+    if lse_parts.shape != o_parts.shape[:-1]:
+        raise ValueError(f"bad shapes {o_parts.shape} {lse_parts.shape}")
+    d = o_parts.shape[-1]
+    rows = int(np.prod(o_parts.shape[1:-1])) if o_parts.ndim > 2 else 1
+    o = np.empty(o_parts.shape[1:], dtype=np.float64)
+    lse = np.empty(lse_parts.shape[1:], dtype=np.float64)
+    lib = lib or load()
+    rc = lib.oracle_merge_fp64(_ptr(o_parts), _ptr(lse_parts), P, rows, d, _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise RuntimeError(f"oracle_merge_fp64 failed ({rc})")
+    return o, lse
 
 
 def attn_rows(q, k, v, rows, scale: float | None = None, nthreads: int | None = None):

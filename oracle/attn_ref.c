@@ -260,4 +260,40 @@ int oracle_attn_online_fp64(const double *Q, const double *K, const double *V, d
     return run_jobs(&p, online_worker, nthreads);
 }
 
+/*
+ * Merge of attention results computed over disjoint key ranges (the block
+ * merge of the Triton page, section 2.3): parts are folded in order with the
+ * running triple (m, l, O): for a part with statistics (m_b, l_b) and its
+ * normalised output O_b,
+ *     m_new = max(m, m_b)
+ *     l_new = l e^(m - m_new) + l_b e^(m_b - m_new)
+ *     O_new = (O l e^(m - m_new) + O_b l_b e^(m_b - m_new)) / l_new.
+ * A part's (m_b, l_b) enter only through LSE_b = m_b + ln l_b, so each part is
+ * taken with m_b = LSE_b and l_b = 1. Result: O and LSE = m + ln l.
+ * Layouts: O_parts [nparts, rows, d], LSE_parts [nparts, rows]; O [rows, d], LSE [rows].
+ */
+int oracle_merge_fp64(const double *O_parts, const double *LSE_parts, long nparts, long rows, long d,
+                      double *O, double *LSE)
+{
+    if (nparts < 1 || rows < 0 || d < 1) return -1;
+    for (long r = 0; r < rows; ++r) {
+        double m = -INFINITY, l = 0.0;
+        double *o = O + r * d;
+        for (long c = 0; c < d; ++c) o[c] = 0.0;
+        for (long b = 0; b < nparts; ++b) {
+            const double mb = LSE_parts[b * rows + r], lb = 1.0;
+            const double *ob = O_parts + (b * rows + r) * d;
+            const double m_new = mb > m ? mb : m;
+            const double wa = (m == -INFINITY) ? 0.0 : l * exp(m - m_new);
+            const double wb = lb * exp(mb - m_new);
+            const double l_new = wa + wb;
+            for (long c = 0; c < d; ++c) o[c] = (o[c] * wa + ob[c] * wb) / l_new;
+            m = m_new;
+            l = l_new;
+        }
+        LSE[r] = m + log(l);
+    }
+    return 0;
+}
+
 int oracle_mutant_id(void) { return ORACLE_MUTANT; }

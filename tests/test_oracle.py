@@ -106,3 +106,35 @@ def test_inputs_are_deterministic_and_rounded():
     qk3 = make_qkv(1, 2, 256, 128, "bf16", sigma_qk=3.0, sigma_v=1.0, seed=0, wid=4)
     assert 2.5 < float(qk3[0].float().std()) < 3.5
     assert 0.8 < float(qk3[2].float().std()) < 1.2
+
+
+# ---- block merge (split-KV) ----
+
+@pytest.mark.parametrize("cuts", [[0, 700], [0, 128, 700], [0, 1, 300, 301, 700], [0, 350, 351, 700]])
+def test_merge_of_key_ranges_equals_whole(cuts):
+    """Attention over disjoint key ranges, merged, equals attention over all keys."""
+    q, k, v = make_qkv(2, 2, 700, 32, "f32", sigma_qk=3.0, seed=6, wid=120)
+    o_ref, l_ref = oracle.attn(q, k, v)
+    parts = [oracle.attn(q, k[:, :, a:b], v[:, :, a:b]) for a, b in zip(cuts[:-1], cuts[1:])]
+    o, lse = oracle.merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, l_ref, rtol=0, atol=1e-12)
+
+
+def test_merge_special_cases():
+    rng = np.random.default_rng(3)
+    o1, l1 = rng.standard_normal((5, 4)), rng.standard_normal(5) * 10
+    o, lse = oracle.merge(o1[None], l1[None])            # one part: identity
+    np.testing.assert_array_equal(o, o1)
+    np.testing.assert_allclose(lse, l1, rtol=0, atol=1e-15)
+    o, lse = oracle.merge(np.stack([o1, o1]), np.stack([l1, l1]))   # two equal parts: same O, LSE + ln 2
+    np.testing.assert_allclose(o, o1, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse, l1 + np.log(2.0), rtol=0, atol=1e-14)
+    o2 = rng.standard_normal((5, 4))
+    o, lse = oracle.merge(np.stack([o1, o2]), np.stack([l1, l1 - 800.0]))  # a negligible part
+    np.testing.assert_allclose(o, o1, rtol=0, atol=1e-300 + 1e-15)
+    # order of the parts does not matter
+    oa, la = oracle.merge(np.stack([o1, o2]), np.stack([l1, l1 - 1.0]))
+    ob, lb = oracle.merge(np.stack([o2, o1]), np.stack([l1 - 1.0, l1]))
+    np.testing.assert_allclose(oa, ob, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(la, lb, rtol=0, atol=1e-14)
