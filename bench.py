@@ -185,6 +185,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline budget")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--splits", type=int, default=1,
+                    help="split-KV ranges (0 = automatic; 1 = the plain forward pass)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override B (smaller captures of the same workload for profiling; not a bench line)")
     args = ap.parse_args()
@@ -220,9 +222,16 @@ def main():
     o = torch.empty_like(qd)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    ws_bytes = fa.fa_fwd_splitkv_workspace_size(w.B, w.H, w.N, w.d, args.splits) if args.splits != 1 else 0
+    workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    n_splits = fa.fa_fwd_splitkv_num_splits(w.B, w.H, w.N, w.d) if args.splits == 0 else args.splits
+    if args.splits != 1:
+        cfg["num_splits"] = n_splits
+        cfg["launches_per_step"] = 2 if n_splits > 1 else 1
 
     def step():
-        fa.attention(qd, kd, vd, scale=w.scale, out=o, lse=lse, stream=stream)
+        fa.attention(qd, kd, vd, scale=w.scale, out=o, lse=lse, stream=stream, num_splits=args.splits,
+                     workspace=workspace)
 
     for _ in range(args.warmup):
         step()
@@ -263,7 +272,8 @@ def main():
             qd.copy_(hq, non_blocking=True)
             kd.copy_(hk, non_blocking=True)
             vd.copy_(hv, non_blocking=True)
-            fa.attention(qd, kd, vd, scale=w.scale, out=o, lse=lse, stream=stream)
+            fa.attention(qd, kd, vd, scale=w.scale, out=o, lse=lse, stream=stream, num_splits=args.splits,
+                         workspace=workspace)
             ho.copy_(o, non_blocking=True)
             hl.copy_(lse, non_blocking=True)
 
@@ -314,7 +324,7 @@ def main():
                      "kernel": f"fa_fwd_f16_kernel<{w.d},{'bf16' if w.dtype == 'bf16' else 'f16'}>",
                      "traffic": traffic, "algorithmic_bytes": w.hbm_bytes},
         "clocks": sampler.summary(),
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if args.splits != 1 and n_splits > 1 else 1),
         "e2e": e2e,
     }
     if ws == 1 and not args.no_cpu_baseline:

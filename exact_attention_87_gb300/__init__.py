@@ -23,6 +23,7 @@ FA_OK = 0
 STATUS_NAMES = {
     0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_DTYPE", 3: "FA_ERR_SHAPE", 4: "FA_ERR_HEADDIM",
     5: "FA_ERR_ALIGN", 6: "FA_ERR_CUDA", 7: "FA_ERR_DEVICE_TIMEOUT", 8: "FA_ERR_ARCH", 9: "FA_ERR_SCALE",
+    10: "FA_ERR_WORKSPACE",
 }
 for _code, _name in STATUS_NAMES.items():
     globals()[_name] = _code
@@ -57,6 +58,13 @@ def lib(path: str | None = None):
     L.fa_strerror.restype = ctypes.c_char_p
     L.fa_abi_version.argtypes = []
     L.fa_abi_version.restype = i
+    u64 = ctypes.c_ulonglong
+    L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, u64, vp]
+    L.fa_fwd_splitkv.restype = i
+    L.fa_fwd_splitkv_num_splits.argtypes = [i, i, i, i]
+    L.fa_fwd_splitkv_num_splits.restype = i
+    L.fa_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i]
+    L.fa_fwd_splitkv_workspace_size.restype = u64
     if path == LIB_PATH:
         _lib = L
     return L
@@ -66,6 +74,20 @@ def lib(path: str | None = None):
 
 def fa_fwd(Q, K, V, O, LSE, B, H, N, d, scale, dtype, stream=None) -> int:
     return lib().fa_fwd(Q, K, V, O, LSE, B, H, N, d, scale, dtype, stream)
+
+
+def fa_fwd_splitkv(Q, K, V, O, LSE, B, H, N, d, scale, dtype, num_splits, workspace, workspace_bytes,
+                   stream=None) -> int:
+    return lib().fa_fwd_splitkv(Q, K, V, O, LSE, B, H, N, d, scale, dtype, num_splits, workspace,
+                                workspace_bytes, stream)
+
+
+def fa_fwd_splitkv_num_splits(B, H, N, d) -> int:
+    return lib().fa_fwd_splitkv_num_splits(B, H, N, d)
+
+
+def fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits) -> int:
+    return lib().fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits)
 
 
 def fa_get_device_status(stream=None) -> int:
@@ -93,11 +115,14 @@ def _dtype_code(t):
     return codes[t.dtype]
 
 
-def attention(q, k, v, scale: float | None = None, out=None, lse=None, stream=None):
+def attention(q, k, v, scale: float | None = None, out=None, lse=None, stream=None, num_splits: int = 1,
+              workspace=None):
     """O, LSE for q, k, v of shape [B, H, N, d] (contiguous CUDA tensors, same dtype).
 
     Returns O (same dtype as q) and LSE (fp32 [B, H, N], natural log). ``out`` and
     ``lse`` may be preallocated; ``stream`` defaults to torch's current stream.
+    ``num_splits`` != 1 runs the split-KV path (0 = automatic count); its
+    workspace is allocated with torch unless a CUDA uint8 tensor is given.
     """
     import torch
     if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
@@ -125,12 +150,21 @@ def attention(q, k, v, scale: float | None = None, out=None, lse=None, stream=No
     elif hasattr(stream, "cuda_stream"):
         stream = stream.cuda_stream
     with torch.cuda.device(q.device):
-        rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                    B, H, N, d, float(scale), _dtype_code(q), stream)
+        if num_splits == 1:
+            rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                        B, H, N, d, float(scale), _dtype_code(q), stream)
+        else:
+            need = fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits)
+            if workspace is None:
+                workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+            rc = fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                B, H, N, d, float(scale), _dtype_code(q), num_splits, workspace.data_ptr(),
+                                workspace.numel(), stream)
     if rc != FA_OK:
         raise FAError(rc)
     return out, lse
 
 
-__all__ = ["attention", "fa_fwd", "fa_get_device_status", "fa_strerror", "fa_abi_version", "build", "lib",
+__all__ = ["attention", "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_num_splits", "fa_fwd_splitkv_workspace_size",
+           "fa_get_device_status", "fa_strerror", "fa_abi_version", "build", "lib",
            "FAError", "FA_F32", "FA_F16", "FA_BF16", "FA_OK"]

@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 
 #include <cuda.h>
@@ -116,6 +117,7 @@ const char* fa_strerror(int status) {
     case FA_ERR_DEVICE_TIMEOUT: return "a kernel timed out waiting on an internal pipeline barrier";
     case FA_ERR_ARCH: return "the current device is not sm_103 (GB300)";
     case FA_ERR_SCALE: return "scale must be finite and > 0";
+    case FA_ERR_WORKSPACE: return "split-KV workspace is NULL, not 256-byte aligned or smaller than required";
     default: return "unknown status";
   }
 }
@@ -124,9 +126,48 @@ const char* fa_strerror(int status) {
 
 namespace {
 
+// Split-KV sizing. Work units of the 16-bit kernel are 256 Q rows x (a key
+// range of whole 128-key tiles).
+constexpr int kQBlock = 2 * fa::kF16BlockQ;
+
+long long kv_tiles(int N) { return (static_cast<long long>(N) + fa::kF16BlockKV - 1) / fa::kF16BlockKV; }
+
+// Effective split count: explicit requests are clamped so that every range
+// holds at least one tile; 0 picks the count with the smallest modelled time:
+//   waves(s) * (tiles/s + 1) * t_tile            partial passes (+1 tile of set-up per unit)
+// + (s > 1) * (2 * s * rows * d * 4 bytes / 5 TB/s + 5 us)   the merge pass
+// with t_tile ~ 2 us * d / 128 for one 256-row unit and one 128-key tile on
+// one SM (measured on GB300 at ~2 GHz).
+int effective_splits(int B, int H, int N, int d, int num_splits, int num_sms) {
+  const long long tiles = kv_tiles(N);
+  if (num_splits > 0) return static_cast<int>(std::min<long long>(num_splits, tiles));
+  const long long units = static_cast<long long>(B) * H * ((N + kQBlock - 1) / kQBlock);
+  const double rows = static_cast<double>(B) * H * N;
+  const double t_tile_us = 2.0 * d / 128.0;
+  int best = 1;
+  double best_us = 1e300;
+  for (int s = 1; s <= 16 && s <= tiles; ++s) {
+    const long long per = (tiles + s - 1) / s;
+    if ((tiles + per - 1) / per != s) continue;
+    const double waves = static_cast<double>((units * s + num_sms - 1) / num_sms);
+    double us = waves * (static_cast<double>(per) + 1.0) * t_tile_us;
+    if (s > 1) us += 2.0 * s * rows * d * 4.0 / 5e12 * 1e6 + 5.0;
+    if (us < best_us) { best_us = us; best = s; }
+  }
+  return best;
+}
+
+unsigned long long workspace_bytes_for(int B, int H, int N, int d, int splits) {
+  if (splits <= 1) return 0;
+  const unsigned long long rows = static_cast<unsigned long long>(B) * H * N * splits;
+  const unsigned long long o_bytes = (rows * d * 4 + 255) & ~255ull;
+  return o_bytes + rows * 4;
+}
+
 int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
              float scale, int dtype, void* stream, int inject, float* stats_trace, unsigned long long* timeline,
-             long long wait_limit) {
+             long long wait_limit, int num_splits = 1, void* workspace = nullptr,
+             unsigned long long workspace_bytes = 0) {
   if (!Q || !K || !V || !O || !LSE) return FA_ERR_NULL;
   if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
   if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
@@ -161,6 +202,18 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
   p.scale = scale;
   p.num_sms = dev.num_sms;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int splits = dtype == FA_F32 ? 1 : effective_splits(B, H, N, d, num_splits, dev.num_sms);
+  const long long tiles = kv_tiles(N);
+  p.split_tiles = static_cast<int>((tiles + splits - 1) / splits);
+  p.num_splits = static_cast<int>((tiles + p.split_tiles - 1) / p.split_tiles);
+  if (p.num_splits > 1) {
+    const unsigned long long need = workspace_bytes_for(B, H, N, d, p.num_splits);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
+      return FA_ERR_WORKSPACE;
+    const unsigned long long rows = static_cast<unsigned long long>(B) * H * N * p.num_splits;
+    p.o_part = static_cast<float*>(workspace);
+    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((rows * d * 4 + 255) & ~255ull));
+  }
 
   cudaError_t e;
   if (dtype == FA_F32) {
@@ -175,6 +228,7 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
         !encode_bhnd_16bit(&p.tm_o, O, bh, N, d, dt, fa::kF16BlockQ))
       return FA_ERR_CUDA;
     e = fa::launch_fwd_f16(p, dtype == FA_BF16, s);
+    if (e == cudaSuccess && p.num_splits > 1) e = fa::launch_merge(p, dtype == FA_BF16, s);
   }
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -186,6 +240,36 @@ extern "C" {
 int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, float scale,
            int dtype, void* stream) {
   return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, dtype, stream, 0, nullptr, nullptr, 0);
+}
+
+int fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
+                   float scale, int dtype, int num_splits, void* workspace, unsigned long long workspace_bytes,
+                   void* stream) {
+  if (num_splits < 0) return FA_ERR_SHAPE;
+  return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, dtype, stream, 0, nullptr, nullptr, 0, num_splits, workspace,
+                  workspace_bytes);
+}
+
+int fa_fwd_splitkv_num_splits(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1) return -FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return -FA_ERR_HEADDIM;
+  DeviceInfo dev;
+  const int st = device_info(&dev);
+  if (st != FA_OK) return -st;
+  return effective_splits(B, H, N, d, 0, dev.num_sms);
+}
+
+unsigned long long fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || num_splits < 0) return 0;
+  int splits = num_splits;
+  if (splits == 0) {
+    splits = fa_fwd_splitkv_num_splits(B, H, N, d);
+    if (splits < 1) return 0;
+  }
+  const long long tiles = kv_tiles(N);
+  splits = static_cast<int>(std::min<long long>(splits, tiles));
+  const long long per = (tiles + splits - 1) / splits;
+  return workspace_bytes_for(B, H, N, d, static_cast<int>((tiles + per - 1) / per));
 }
 
 #ifdef FA_TESTING

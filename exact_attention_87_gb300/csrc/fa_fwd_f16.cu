@@ -101,8 +101,8 @@ __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) {
 // TMA producer (one thread)
 // --------------------------------------------------------------------------
 template <int D>
-__device__ __forceinline__ void producer(const FwdParams& p, uint32_t base, int bh, int row0, bool has1, int nkv,
-                         const WaitCtl& ctl) {
+__device__ __forceinline__ void producer(const FwdParams& p, uint32_t base, int bh, int row0, bool has1, int t0,
+                                         int nkv, const WaitCtl& ctl) {
   using C = Cfg<D>;
   tma_prefetch_desc(&p.tm_q);
   tma_prefetch_desc(&p.tm_k);
@@ -127,7 +127,7 @@ __device__ __forceinline__ void producer(const FwdParams& p, uint32_t base, int 
     mbar_arrive_expect_tx(kf, C::KV_BYTES);
 #pragma unroll
     for (int h = 0; h < D / 64; ++h)
-      tma_load_3d(base + C::OFF_K + s * C::KV_BYTES + h * C::KV_HALF_BYTES, &p.tm_k, kf, 64 * h, j * C::BN, bh);
+      tma_load_3d(base + C::OFF_K + s * C::KV_BYTES + h * C::KV_HALF_BYTES, &p.tm_k, kf, 64 * h, (t0 + j) * C::BN, bh);
     nk = j + 1;
     FA_TRACE(p, kEvKIssued, j);
 #ifdef FA_TESTING
@@ -138,7 +138,7 @@ __device__ __forceinline__ void producer(const FwdParams& p, uint32_t base, int 
     mbar_arrive_expect_tx(vf, C::KV_BYTES);
 #pragma unroll
     for (int h = 0; h < D / 64; ++h)
-      tma_load_3d(base + C::OFF_V + s * C::KV_BYTES + h * C::KV_HALF_BYTES, &p.tm_v, vf, 64 * h, j * C::BN, bh);
+      tma_load_3d(base + C::OFF_V + s * C::KV_BYTES + h * C::KV_HALF_BYTES, &p.tm_v, vf, 64 * h, (t0 + j) * C::BN, bh);
     nv = j + 1;
     FA_TRACE(p, kEvVIssued, j);
   }
@@ -251,8 +251,8 @@ drain:
 // Softmax + lazy correction + epilogue (one warpgroup per Q sub-tile)
 // --------------------------------------------------------------------------
 template <int D, bool BF16>
-__device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, uint32_t tmem, int sub, int bh, int row0, int nkv,
-                           const WaitCtl& ctl) {
+__device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, uint32_t tmem, int sub, int bh, int row0,
+                                           int split, int t0, int nkv, const WaitCtl& ctl) {
   using C = Cfg<D>;
   const int t = threadIdx.x - sub * 128;  // row within the sub-tile
   const int lane = threadIdx.x & 31;
@@ -289,7 +289,7 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
       for (int u = 0; u < 32; ++u) s[32 * q + u] = __uint_as_float(sraw[q][u]);
     }
 
-    const int valid = p.N - j * C::BN;  // keys of this tile inside the sequence
+    const int valid = p.N - (t0 + j) * C::BN;  // keys of this tile inside the sequence
     if (valid < C::BN) {
 #pragma unroll
       for (int u = 0; u < C::BN; ++u)
@@ -390,6 +390,27 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
   // ---- epilogue: O / l -> dtype -> swizzled staging (Q buffer) -> TMA store; LSE ----
   tc_fence_after();
   const float inv_l = 1.0f / (BF16 ? l_o : l);
+  if (p.num_splits > 1) {
+    // Split-KV: this key range's normalised O (fp32) and LSE go to the partial buffers.
+    const int row = row0 + C::BM * sub + t;
+    const size_t prow = (static_cast<size_t>(split) * p.B * p.H + bh) * p.N + row;
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) {
+      uint32_t r[32];
+      tmem_ld32(t_o + 32 * q, r);
+      tmem_ld_wait();
+      reg_fence(r);
+      if (row < p.N) {
+        float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D + 32 * q);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          dst[u] = make_float4(__uint_as_float(r[4 * u]) * inv_l, __uint_as_float(r[4 * u + 1]) * inv_l,
+                               __uint_as_float(r[4 * u + 2]) * inv_l, __uint_as_float(r[4 * u + 3]) * inv_l);
+      }
+    }
+    if (row < p.N) p.lse_part[prow] = (m_ref + lg2_approx(l)) * kLn2;
+    return;
+  }
   const uint32_t stage = base + C::OFF_Q + sub * C::Q_SUB_BYTES;
 #pragma unroll
   for (int q = 0; q < D / 32; ++q) {
@@ -434,11 +455,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem_raw + (base - raw) + C::OFF_MISC);
 
   const int warp = threadIdx.x >> 5;
+  // Work unit: (batch*head, 256-row Q block, key range); consecutive units
+  // share a head so its K/V stay in L2 while its Q blocks are processed.
   const int nqb = (p.N + 2 * C::BM - 1) / (2 * C::BM);
-  const int bh = blockIdx.x / nqb;
-  const int row0 = (blockIdx.x % nqb) * 2 * C::BM;
+  const int split = blockIdx.x % p.num_splits;
+  const int qunit = blockIdx.x / p.num_splits;
+  const int bh = qunit / nqb;
+  const int row0 = (qunit % nqb) * 2 * C::BM;
   const bool has1 = row0 + C::BM < p.N;
-  const int nkv = (p.N + C::BN - 1) / C::BN;
+  const int nkv_all = (p.N + C::BN - 1) / C::BN;
+  const int t0 = split * p.split_tiles;                      // first K/V tile of this key range
+  const int nkv = min(nkv_all - t0, p.split_tiles);          // >= 1 (checked on the host)
 
   if (threadIdx.x == 0) {
     mbar_init(bar_addr<D>(base, C::B_Q), 1);
@@ -473,7 +500,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
   if (warp >= 8) {
     warpgroup_reg_dealloc<C::LOW_REGS>();
     if (warp == C::WARP_TMA) {
-      if ((threadIdx.x & 31) == 0) producer<D>(p, base, bh, row0, has1, nkv, ctl);
+      if ((threadIdx.x & 31) == 0) producer<D>(p, base, bh, row0, has1, t0, nkv, ctl);
       __syncwarp();
     } else if (warp == C::WARP_MMA0 || (warp == C::WARP_MMA1 && has1)) {
       if (warp == C::WARP_MMA0)
@@ -485,7 +512,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
   } else {
     warpgroup_reg_alloc<C::HIGH_REGS>();
     const int sub = warp / 4;
-    if (sub == 0 || has1) softmax_wg<D, BF16>(p, base, tmem, sub, bh, row0, nkv, ctl);
+    if (sub == 0 || has1) softmax_wg<D, BF16>(p, base, tmem, sub, bh, row0, split, t0, nkv, ctl);
   }
 
   tc_fence_before();
@@ -526,13 +553,73 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(bit);
   }
-  const long long units = static_cast<long long>(p.B) * p.H * ((p.N + 2 * C::BM - 1) / (2 * C::BM));
+  const long long units =
+      static_cast<long long>(p.B) * p.H * ((p.N + 2 * C::BM - 1) / (2 * C::BM)) * p.num_splits;
   if (units <= 0 || units > 0x7fffffffLL) return cudaErrorInvalidValue;
   kern<<<dim3(static_cast<unsigned>(units)), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 
+// Split-KV merge (block merge of the Triton page, section 2.3, in LSE form):
+// LSE = m + log sum_s exp(LSE_s - m), O = sum_s exp(LSE_s - LSE) O_s.
+// One warp per output row; lane k handles D/32 consecutive columns.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) fa_merge_kernel(const __grid_constant__ FwdParams p) {
+  constexpr int E = D / 32;
+  const long long rows = static_cast<long long>(p.B) * p.H * p.N;
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float m = -INFINITY;
+  for (int s = 0; s < p.num_splits; ++s) m = fmaxf(m, p.lse_part[s * rows + row]);
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float l = 0.f;
+  for (int s = 0; s < p.num_splits; ++s) {
+    const float w = ex2_approx((p.lse_part[s * rows + row] - m) * kLog2e);
+    l += w;
+    const float* src = p.o_part + (s * rows + row) * D + lane * E;
+    if constexpr (E == 4) {
+      const float4 x = *reinterpret_cast<const float4*>(src);
+      acc[0] = fmaf(w, x.x, acc[0]);
+      acc[1] = fmaf(w, x.y, acc[1]);
+      acc[2] = fmaf(w, x.z, acc[2]);
+      acc[3] = fmaf(w, x.w, acc[3]);
+    } else {
+      const float2 x = *reinterpret_cast<const float2*>(src);
+      acc[0] = fmaf(w, x.x, acc[0]);
+      acc[1] = fmaf(w, x.y, acc[1]);
+    }
+  }
+  const float inv = 1.0f / l;
+  uint32_t pk[E / 2];
+#pragma unroll
+  for (int e = 0; e < E / 2; ++e) pk[e] = pack2<BF16>(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+  uint16_t* out = static_cast<uint16_t*>(p.o) + row * D + lane * E;
+  if constexpr (E == 4)
+    *reinterpret_cast<uint2*>(out) = make_uint2(pk[0], pk[1]);
+  else
+    *reinterpret_cast<uint32_t*>(out) = pk[0];
+  if (lane == 0) p.lse[row] = m + lg2_approx(l) * kLn2;
+}
+
+template <int D, bool BF16>
+cudaError_t launch_merge_t(const FwdParams& p, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(p.B) * p.H * p.N;
+  const long long blocks = (rows * 32 + 255) / 256;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  fa_merge_kernel<D, BF16><<<dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_merge(const FwdParams& p, bool bf16, cudaStream_t stream) {
+  if (p.d == 128) return bf16 ? launch_merge_t<128, true>(p, stream) : launch_merge_t<128, false>(p, stream);
+  if (p.d == 64) return bf16 ? launch_merge_t<64, true>(p, stream) : launch_merge_t<64, false>(p, stream);
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_fwd_f16(const FwdParams& p, bool bf16, cudaStream_t stream) {
   if (p.d == 128) return bf16 ? launch<128, true>(p, stream) : launch<128, false>(p, stream);

@@ -34,6 +34,13 @@ struct alignas(64) FwdParams {
   int B, H, N, d;
   float scale;
   int num_sms;
+  // Split-KV: each CTA covers split_tiles K/V tiles of one of num_splits key
+  // ranges and writes its normalised fp32 O and its LSE to o_part / lse_part
+  // ([num_splits, B*H*N, d] and [num_splits, B*H*N]); num_splits == 1: no split.
+  int num_splits;
+  int split_tiles;
+  float* o_part;
+  float* lse_part;
   // Used only by the testing build (-DFA_TESTING); zero / NULL otherwise.
   int inject;                       // 1: the producer skips the V load of tile 0
   float* stats_trace;               // [B*H*N, nkv, 2]: (m in natural-log units, l) after each K/V tile
@@ -53,6 +60,8 @@ enum : int {
 
 // Launch the 16-bit (fp16 / bf16) forward kernel for head dimension p.d.
 cudaError_t launch_fwd_f16(const FwdParams& p, bool bf16, cudaStream_t stream);
+// Merge split-KV partials into O (dtype of the 16-bit path) and LSE.
+cudaError_t launch_merge(const FwdParams& p, bool bf16, cudaStream_t stream);
 // Launch the fp32 (3 x TF32) forward kernel.
 cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);
 

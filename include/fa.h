@@ -44,7 +44,8 @@ typedef enum {
     FA_ERR_CUDA = 6,           /* a CUDA runtime/driver call failed (launch, query)  */
     FA_ERR_DEVICE_TIMEOUT = 7, /* a kernel gave up waiting on a pipeline barrier     */
     FA_ERR_ARCH = 8,           /* the current device is not sm_103                   */
-    FA_ERR_SCALE = 9           /* scale is not finite and > 0                        */
+    FA_ERR_SCALE = 9,          /* scale is not finite and > 0                        */
+    FA_ERR_WORKSPACE = 10      /* split-KV workspace NULL, misaligned or too small   */
 } fa_status;
 
 /*
@@ -73,6 +74,38 @@ typedef enum {
  */
 int fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
            int B, int H, int N, int d, float scale, int dtype, void *stream);
+
+/*
+ * Split-KV forward pass: the same result as fa_fwd, computed by splitting the
+ * keys of every (batch, head) into `num_splits` contiguous ranges (multiples of
+ * 128 keys) that run as separate work units, then merging the per-range
+ * results with the block merge of the Triton page ("FlashAttention + Triton",
+ * section 2.3: m_new = max(m_old, m_block), l and O rescaled by exp(m - m_new)),
+ * written in LSE form: LSE = log sum_r exp(LSE_r), O = sum_r exp(LSE_r - LSE) O_r.
+ * It raises the number of work units when B*H*ceil(N/256) is small against
+ * the number of SMs (long sequences, few heads).
+ *
+ * Arguments up to `dtype` are those of fa_fwd.
+ * num_splits: >= 1 explicit (clamped to ceil(N/128)); 0 = chosen from the
+ *             shape and the device's SM count (fa_fwd_splitkv_num_splits).
+ * workspace:  device memory owned by the caller, 256-byte aligned, at least
+ *             fa_fwd_splitkv_workspace_size(...) bytes; holds the per-range
+ *             fp32 O and LSE. Unused (may be NULL) when the effective split
+ *             count is 1, and for FA_F32 inputs, which always run unsplit.
+ * Errors: those of fa_fwd, plus FA_ERR_WORKSPACE. Two launches are enqueued
+ * on `stream` (partials, then merge); nothing is synchronised.
+ */
+int fa_fwd_splitkv(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                   int B, int H, int N, int d, float scale, int dtype,
+                   int num_splits, void *workspace, unsigned long long workspace_bytes, void *stream);
+
+/* The split count fa_fwd_splitkv uses for num_splits = 0 on the current
+ * device (>= 1), or a negative fa_status on error. */
+int fa_fwd_splitkv_num_splits(int B, int H, int N, int d);
+
+/* Workspace bytes fa_fwd_splitkv needs for this shape and split count
+ * (num_splits = 0: the automatic count); 0 when no workspace is needed. */
+unsigned long long fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits);
 
 /*
  * Synchronises `stream`, then returns and clears the status word that kernels

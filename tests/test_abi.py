@@ -57,7 +57,7 @@ def test_every_header_is_covered():
 
 def test_strerror_and_version(L):
     assert fa.fa_abi_version() >= 100
-    for code in range(0, 10):
+    for code in range(0, 11):
         assert fa.fa_strerror(code) and fa.fa_strerror(code) != "unknown status"
     assert fa.fa_strerror(12345) == "unknown status"
 
@@ -89,3 +89,15 @@ def test_argument_errors_return_before_launch(L, args, code):
 def test_missing_library_raises(tmp_path):
     with pytest.raises(ImportError):
         fa.lib(str(tmp_path / "nope.so"))
+
+
+def test_splitkv_workspace_size_formula(L):
+    assert fa.fa_fwd_splitkv_workspace_size(1, 8, 16384, 128, 1) == 0
+    rows = 1 * 8 * 16384 * 3
+    o_bytes = (rows * 128 * 4 + 255) // 256 * 256
+    assert fa.fa_fwd_splitkv_workspace_size(1, 8, 16384, 128, 3) == o_bytes + rows * 4
+    # requests beyond the number of 128-key tiles are clamped: N = 300 has 3 tiles
+    assert fa.fa_fwd_splitkv_workspace_size(1, 1, 300, 64, 9) == fa.fa_fwd_splitkv_workspace_size(1, 1, 300, 64, 3)
+    assert fa.fa_fwd_splitkv_workspace_size(0, 1, 300, 64, 2) == 0
+    assert fa.fa_fwd_splitkv(0, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, 2, A, 1 << 20, None) == fa.FA_ERR_NULL
+    assert fa.fa_fwd_splitkv(A, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, -1, A, 1 << 20, None) == fa.FA_ERR_SHAPE
