@@ -23,7 +23,7 @@ FA_OK = 0
 STATUS_NAMES = {
     0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_DTYPE", 3: "FA_ERR_SHAPE", 4: "FA_ERR_HEADDIM",
     5: "FA_ERR_ALIGN", 6: "FA_ERR_CUDA", 7: "FA_ERR_DEVICE_TIMEOUT", 8: "FA_ERR_ARCH", 9: "FA_ERR_SCALE",
-    10: "FA_ERR_WORKSPACE",
+    10: "FA_ERR_WORKSPACE", 11: "FA_ERR_SCRATCH_LIMIT",
 }
 for _code, _name in STATUS_NAMES.items():
     globals()[_name] = _code
@@ -61,6 +61,8 @@ def lib(path: str | None = None):
     u64 = ctypes.c_ulonglong
     L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, u64, vp]
     L.fa_fwd_splitkv.restype = i
+    L.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+    L.fa_fwd_splitkv_noalloc.restype = i
     L.fa_fwd_splitkv_num_splits.argtypes = [i, i, i, i]
     L.fa_fwd_splitkv_num_splits.restype = i
     L.fa_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i]
@@ -80,6 +82,12 @@ def fa_fwd_splitkv(Q, K, V, O, LSE, B, H, N, d, scale, dtype, num_splits, worksp
                    stream=None) -> int:
     return lib().fa_fwd_splitkv(Q, K, V, O, LSE, B, H, N, d, scale, dtype, num_splits, workspace,
                                 workspace_bytes, stream)
+
+
+def fa_fwd_splitkv_noalloc(Q, K, V, O, LSE, B, H, N, d, scale, dtype, num_splits, stream=None) -> int:
+    """fa_fwd_splitkv using the library's built-in 32 MiB scratch: for callers
+    that may not allocate device memory (see include/fa.h)."""
+    return lib().fa_fwd_splitkv_noalloc(Q, K, V, O, LSE, B, H, N, d, scale, dtype, num_splits, stream)
 
 
 def fa_fwd_splitkv_num_splits(B, H, N, d) -> int:
@@ -165,6 +173,7 @@ def attention(q, k, v, scale: float | None = None, out=None, lse=None, stream=No
     return out, lse
 
 
-__all__ = ["attention", "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_num_splits", "fa_fwd_splitkv_workspace_size",
+__all__ = ["attention", "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_num_splits",
+           "fa_fwd_splitkv_workspace_size",
            "fa_get_device_status", "fa_strerror", "fa_abi_version", "build", "lib",
            "FAError", "FA_F32", "FA_F16", "FA_BF16", "FA_OK"]

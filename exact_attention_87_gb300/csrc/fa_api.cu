@@ -21,6 +21,11 @@
 // first timeout happened. Kernels receive its address as a parameter.
 __device__ unsigned int g_fa_status[2];
 
+// Built-in scratch of fa_fwd_splitkv_noalloc (split-KV partial O and LSE).
+// Host code must not pass this name to a kernel: it is a host-side stand-in;
+// the device address comes from cudaGetSymbolAddress (noalloc_scratch()).
+static __device__ __align__(256) unsigned char g_fa_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -30,6 +35,7 @@ struct DeviceInfo {
   bool is_sm103 = false;
   int num_sms = 0;
   unsigned int* status = nullptr;
+  void* noalloc_scratch = nullptr;  // device address of g_fa_noalloc_scratch (looked up on first use)
 };
 
 std::mutex g_mu;
@@ -99,6 +105,25 @@ bool encode_bhnd_16bit(CUtensorMap* map, const void* ptr, int BH, int N, int d, 
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Device address of the built-in scratch on the current device, looked up once
+// per device with that device current. Returns FA_OK / FA_ERR_CUDA / FA_ERR_ARCH.
+int noalloc_scratch(void** out) {
+  DeviceInfo dev;
+  const int st = device_info(&dev);
+  if (st != FA_OK) return st;
+  int ord = 0;
+  if (cudaGetDevice(&ord) != cudaSuccess) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[ord];
+  if (!d.noalloc_scratch) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_fa_noalloc_scratch) != cudaSuccess || ptr == nullptr) return FA_ERR_CUDA;
+    d.noalloc_scratch = ptr;
+  }
+  *out = d.noalloc_scratch;
+  return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -118,6 +143,9 @@ const char* fa_strerror(int status) {
     case FA_ERR_ARCH: return "the current device is not sm_103 (GB300)";
     case FA_ERR_SCALE: return "scale must be finite and > 0";
     case FA_ERR_WORKSPACE: return "split-KV workspace is NULL, not 256-byte aligned or smaller than required";
+    case FA_ERR_SCRATCH_LIMIT:
+      return "this shape's split-KV workspace exceeds the library's 32 MiB built-in scratch "
+             "(fa_fwd_splitkv_noalloc); use fa_fwd_splitkv with a caller workspace";
     default: return "unknown status";
   }
 }
@@ -248,6 +276,22 @@ int fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* 
   if (num_splits < 0) return FA_ERR_SHAPE;
   return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, dtype, stream, 0, nullptr, nullptr, 0, num_splits, workspace,
                   workspace_bytes);
+}
+
+int fa_fwd_splitkv_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
+                           int d, float scale, int dtype, int num_splits, void* stream) {
+  if (num_splits < 0) return FA_ERR_SHAPE;
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+  void* scratch = nullptr;
+  const int st = noalloc_scratch(&scratch);
+  if (st != FA_OK) return st;
+  const unsigned long long need =
+      dtype == FA_F32 ? 0ull : fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits);
+  if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
+  return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, dtype, stream, 0, nullptr, nullptr, 0, num_splits, scratch,
+                  FA_NOALLOC_SCRATCH_BYTES);
 }
 
 int fa_fwd_splitkv_num_splits(int B, int H, int N, int d) {

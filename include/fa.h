@@ -45,7 +45,8 @@ typedef enum {
     FA_ERR_DEVICE_TIMEOUT = 7, /* a kernel gave up waiting on a pipeline barrier     */
     FA_ERR_ARCH = 8,           /* the current device is not sm_103                   */
     FA_ERR_SCALE = 9,          /* scale is not finite and > 0                        */
-    FA_ERR_WORKSPACE = 10      /* split-KV workspace NULL, misaligned or too small   */
+    FA_ERR_WORKSPACE = 10,     /* split-KV workspace NULL, misaligned or too small   */
+    FA_ERR_SCRATCH_LIMIT = 11  /* shape needs more than the built-in scratch         */
 } fa_status;
 
 /*
@@ -106,6 +107,35 @@ int fa_fwd_splitkv_num_splits(int B, int H, int N, int d);
 /* Workspace bytes fa_fwd_splitkv needs for this shape and split count
  * (num_splits = 0: the automatic count); 0 when no workspace is needed. */
 unsigned long long fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits);
+
+/*
+ * fa_fwd_splitkv without a caller workspace, for callers that cannot allocate
+ * device memory: code running under an allocation-free policy after start-up
+ * (real-time or safety-certified pipelines, plugins that a host framework
+ * forbids to call cudaMalloc, allocators that must not be re-entered), where a
+ * cudaMalloc/cudaFree would also synchronise the device in the middle of the
+ * work. The pages have no counterpart for it; it is a library addition.
+ *
+ * The per-range partial results live in a scratch array that is part of the
+ * library itself (a __device__ array of FA_NOALLOC_SCRATCH_BYTES = 32 MiB,
+ * present on every GPU that loads the library until the process exits). This
+ * entry point calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Arguments: as fa_fwd_splitkv, without workspace. Shapes whose split-KV
+ * workspace (fa_fwd_splitkv_workspace_size for the effective split count)
+ * exceeds the scratch size return FA_ERR_SCRATCH_LIMIT before anything is
+ * enqueued; with an effective split count of 1 the scratch is not used.
+ * The first call on each device looks up the scratch array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. All calls share the one array and it keeps the
+ * last call's contents; nothing in it needs to start at zero (each call writes
+ * every byte it reads). Calls that can overlap on the GPU (other streams,
+ * other host threads) race on the array: serialise them, e.g. on one stream.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (32ull << 20)
+int fa_fwd_splitkv_noalloc(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                           int B, int H, int N, int d, float scale, int dtype,
+                           int num_splits, void *stream);
 
 /*
  * Synchronises `stream`, then returns and clears the status word that kernels

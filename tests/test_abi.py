@@ -57,7 +57,7 @@ def test_every_header_is_covered():
 
 def test_strerror_and_version(L):
     assert fa.fa_abi_version() >= 100
-    for code in range(0, 11):
+    for code in range(0, 12):
         assert fa.fa_strerror(code) and fa.fa_strerror(code) != "unknown status"
     assert fa.fa_strerror(12345) == "unknown status"
 
