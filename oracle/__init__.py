@@ -51,6 +51,9 @@ def _bind(path: str):
     lib.oracle_attn_fp64.restype = I
     lib.oracle_attn_online_fp64.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, D, L, D, dp, dp, I]
     lib.oracle_attn_online_fp64.restype = I
+    lp = ctypes.POINTER(ctypes.c_long)
+    lib.oracle_attn_masked_fp64.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, L, D, I, lp, I]
+    lib.oracle_attn_masked_fp64.restype = I
     lib.oracle_merge_fp64.argtypes = [dp, dp, L, L, L, dp, dp]
     lib.oracle_merge_fp64.restype = I
     lib.oracle_mutant_id.restype = I
@@ -134,6 +137,35 @@ def attn_online(q, k, v, block_n: int, tau: float = 0.0, scale: float | None = N
     if rc != 0:
         raise RuntimeError(f"oracle_attn_online_fp64 failed ({rc})")
     return (o, lse, tm, tl) if trace else (o, lse)
+
+
+def attn_masked(q, k, v, causal: bool = False, klen=None, scale: float | None = None,
+                nthreads: int | None = None, lib=None):
+    """Masked three-pass attention. q [B,H,Nq,d], k/v [B,H,Nk,d]; klen: None or B ints.
+
+    Row i of batch b attends to keys j < klen[b] and, if causal, j <= i. A row
+    with no allowed key gets O = 0 and LSE = -inf.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if q.ndim != 4:
+        raise ValueError("attn_masked wants [B, H, N, d] arrays")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    o = np.empty(q.shape, dtype=np.float64)
+    lse = np.empty(q.shape[:-1], dtype=np.float64)
+    kl = None
+    if klen is not None:
+        kl = np.ascontiguousarray(np.asarray(klen, dtype=np.int64).reshape(-1))
+        if kl.shape != (B,):
+            raise ValueError("klen must hold one length per batch")
+    lib = lib or load()
+    lp = kl.ctypes.data_as(ctypes.POINTER(ctypes.c_long)) if kl is not None else ctypes.POINTER(ctypes.c_long)()
+    rc = lib.oracle_attn_masked_fp64(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, scale,
+                                     int(bool(causal)), lp, nthreads or default_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_masked_fp64 failed ({rc})")
+    return o, lse
 
 
 def merge(o_parts, lse_parts, lib=None):

@@ -261,6 +261,84 @@ int oracle_attn_online_fp64(const double *Q, const double *K, const double *V, d
 }
 
 /*
+ * Masked definition (causal and/or per-batch key lengths): row i of batch b
+ * attends to the keys j with j < klen[b] (all keys when klen is NULL) and,
+ * if causal, j <= i (query and key positions counted from the start of the
+ * sequence). The three passes run over the allowed keys only. A row with no
+ * allowed key has no softmax (the Triton page, section 5.1, warns that
+ * exp(-inf - (-inf)) is NaN there); its reading here: O = 0, LSE = -inf.
+ * klen: NULL or [B] (B = BH / H).
+ */
+typedef struct {
+    job_t base;
+    int causal;
+    const long *klen;
+    long H;
+} mjob_t;
+
+static void *masked_worker(void *arg)
+{
+    mjob_t *mj = (mjob_t *)arg;
+    job_t *jb = &mj->base;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(jb->Nk > 0 ? jb->Nk : 1));
+    if (!s) { jb->ok = 0; return NULL; }
+    for (long r = jb->row_begin; r < jb->row_end; ++r) {
+        long bh = r / jb->Nq, i = r % jb->Nq, b = bh / mj->H;
+        long nk = mj->klen ? mj->klen[b] : jb->Nk;
+        if (nk > jb->Nk) nk = jb->Nk;
+        if (mj->causal && i + 1 < nk) nk = i + 1;
+        double *o = jb->O + r * jb->d;
+        if (nk <= 0) {
+            for (long c = 0; c < jb->d; ++c) o[c] = 0.0;
+            jb->LSE[r] = -INFINITY;
+            continue;
+        }
+        const double *q = jb->Q + r * jb->d;
+        scores_row(q, jb->K + bh * jb->Nk * jb->d, nk, jb->d, jb->scale, s);
+        three_pass_row(s, jb->V + bh * jb->Nk * jb->d, nk, jb->d, o, jb->LSE + r);
+    }
+    free(s);
+    jb->ok = 1;
+    return NULL;
+}
+
+int oracle_attn_masked_fp64(const double *Q, const double *K, const double *V, double *O, double *LSE,
+                            long B, long H, long Nq, long Nk, long d, double scale, int causal,
+                            const long *klen, int nthreads)
+{
+    if (B < 0 || H < 1 || Nq < 0 || Nk < 1 || d < 1) return -1;
+    long rows = B * H * Nq;
+    if (rows <= 0) return 0;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if ((long)nthreads > rows) nthreads = (int)rows;
+    mjob_t jobs[256];
+    pthread_t th[256];
+    int started[256];
+    long per = (rows + nthreads - 1) / nthreads;
+    for (int t = 0; t < nthreads; ++t) {
+        memset(&jobs[t], 0, sizeof jobs[t]);
+        job_t *p = &jobs[t].base;
+        p->Q = Q; p->K = K; p->V = V; p->O = O; p->LSE = LSE;
+        p->BH = B * H; p->Nq = Nq; p->Nk = Nk; p->d = d; p->scale = scale;
+        p->row_begin = t * per;
+        p->row_end = (t + 1) * per < rows ? (t + 1) * per : rows;
+        jobs[t].causal = causal; jobs[t].klen = klen; jobs[t].H = H;
+        started[t] = 0;
+        if (p->row_begin >= p->row_end) { p->ok = 1; continue; }
+        if (t > 0 && pthread_create(&th[t], NULL, masked_worker, &jobs[t]) == 0) started[t] = 1;
+    }
+    if (jobs[0].base.row_begin < jobs[0].base.row_end) masked_worker(&jobs[0]);
+    for (int t = 1; t < nthreads; ++t) {
+        if (started[t]) pthread_join(th[t], NULL);
+        else if (jobs[t].base.row_begin < jobs[t].base.row_end) masked_worker(&jobs[t]);
+    }
+    for (int t = 0; t < nthreads; ++t)
+        if (!jobs[t].base.ok) return -2;
+    return 0;
+}
+
+/*
  * Merge of attention results computed over disjoint key ranges (the block
  * merge of the Triton page, section 2.3): parts are folded in order with the
  * running triple (m, l, O): for a part with statistics (m_b, l_b) and its

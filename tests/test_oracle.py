@@ -138,3 +138,55 @@ def test_merge_special_cases():
     ob, lb = oracle.merge(np.stack([o2, o1]), np.stack([l1 - 1.0, l1]))
     np.testing.assert_allclose(oa, ob, rtol=0, atol=1e-14)
     np.testing.assert_allclose(la, lb, rtol=0, atol=1e-14)
+
+
+# ---- masks: causal and per-batch key lengths ----
+
+def test_masked_without_masks_is_the_definition():
+    q, k, v = make_qkv(2, 3, 70, 16, "bf16", seed=2, wid=130)
+    o0, l0 = oracle.attn(q, k, v)
+    o1, l1 = oracle.attn_masked(q, k, v)
+    np.testing.assert_array_equal(o1, o0)
+    np.testing.assert_array_equal(l1, l0)
+
+
+def test_causal_rows_are_prefix_attention():
+    """Causal row i equals unmasked attention of q_i over keys 0..i (brute force)."""
+    q, k, v = make_qkv(1, 2, 40, 8, "f32", sigma_qk=2.0, seed=3, wid=131)
+    o, lse = oracle.attn_masked(q, k, v, causal=True)
+    for i in [0, 1, 7, 20, 39]:
+        oi, li = oracle.attn(q[:, :, i:i + 1], k[:, :, : i + 1], v[:, :, : i + 1])
+        np.testing.assert_allclose(o[:, :, i], oi[:, :, 0], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[:, :, i], li[:, :, 0], rtol=0, atol=1e-13)
+    # row 0 sees only key 0: O = v_0, LSE = s_00
+    qd, kd, vd = (t.double().numpy() for t in (q, k, v))
+    np.testing.assert_allclose(o[:, :, 0], vd[:, :, 0], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse[:, :, 0], (qd[:, :, 0] * kd[:, :, 0]).sum(-1) / np.sqrt(8), rtol=0, atol=1e-13)
+    # the last row sees every key
+    o_full, l_full = oracle.attn(q, k, v)
+    np.testing.assert_allclose(o[:, :, -1], o_full[:, :, -1], rtol=0, atol=1e-13)
+
+
+def test_key_lengths_equal_truncated_keys():
+    q, k, v = make_qkv(3, 2, 50, 8, "f32", seed=4, wid=132)
+    klen = [50, 17, 1]
+    o, lse = oracle.attn_masked(q, k, v, klen=klen)
+    for b, n in enumerate(klen):
+        ob, lb = oracle.attn(q[b], k[b, :, :n], v[b, :, :n])
+        np.testing.assert_allclose(o[b], ob, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[b], lb, rtol=0, atol=1e-13)
+    # causal and key lengths together: row i sees keys j < min(i + 1, klen[b])
+    o2, l2 = oracle.attn_masked(q, k, v, causal=True, klen=klen)
+    for b, n in enumerate(klen):
+        for i in [0, 5, 30, 49]:
+            m = min(i + 1, n)
+            oi, li = oracle.attn(q[b, :, i:i + 1], k[b, :, :m], v[b, :, :m])
+            np.testing.assert_allclose(o2[b, :, i], oi[:, 0], rtol=0, atol=1e-13)
+
+
+def test_fully_masked_rows_are_guarded():
+    """No allowed key: O = 0 and LSE = -inf, never NaN."""
+    q, k, v = make_qkv(2, 1, 20, 8, "f32", seed=5, wid=133)
+    o, lse = oracle.attn_masked(q, k, v, klen=[0, 20])
+    assert np.all(o[0] == 0) and np.all(np.isneginf(lse[0]))
+    assert np.all(np.isfinite(o[1])) and np.all(np.isfinite(lse[1]))
