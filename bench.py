@@ -185,6 +185,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline budget")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--causal", action="store_true",
+                    help="causal mask (FLOPs counted for the keys each row sees: 4*d*N*(N+1)/2 per head)")
     ap.add_argument("--splits", type=int, default=1,
                     help="split-KV ranges (0 = automatic; 1 = the plain forward pass)")
     ap.add_argument("--batch", type=int, default=None,
@@ -197,10 +199,14 @@ def main():
     w = WORKLOADS[args.workload]
     if args.batch is not None:
         w = dataclasses.replace(w, B=args.batch, name=f"{w.name}[B={args.batch}]")
+    flops = w.flops if not args.causal else 4 * w.B * w.H * w.d * w.N * (w.N + 1) // 2
     ws, rank, local = dist_env()
     cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype, "sigma_qk": w.sigma_qk,
            "sigma_v": w.sigma_v, "scale": "1/sqrt(d)", "causal": False,
            "l2": "inputs larger than L2 (no flush)" if 3 * w.B * w.H * w.N * w.d * 2 > 129e6 else "inputs fit in L2: warm, not flushed"}
+    if args.causal:
+        cfg["causal"] = True
+        cfg["flops"] = "4*d*N*(N+1)/2 per (b, h)"
 
     if args.impl == "reference":
         return run_reference(args, w, cfg, ws, rank)
@@ -231,7 +237,7 @@ def main():
 
     def step():
         fa.attention(qd, kd, vd, scale=w.scale, out=o, lse=lse, stream=stream, num_splits=args.splits,
-                     workspace=workspace)
+                     workspace=workspace, causal=args.causal)
 
     for _ in range(args.warmup):
         step()
@@ -259,7 +265,7 @@ def main():
     st = fa.fa_get_device_status()
     if st != fa.FA_OK:
         raise RuntimeError(f"device status {st} after the timed region")
-    tflops = job_throughput(ws, w.flops, ms)
+    tflops = job_throughput(ws, flops, ms)
 
     # ---- e2e: public API with host buffers, copies inside the timed region ----
     e2e = None
@@ -273,7 +279,7 @@ def main():
             kd.copy_(hk, non_blocking=True)
             vd.copy_(hv, non_blocking=True)
             fa.attention(qd, kd, vd, scale=w.scale, out=o, lse=lse, stream=stream, num_splits=args.splits,
-                         workspace=workspace)
+                         workspace=workspace, causal=args.causal)
             ho.copy_(o, non_blocking=True)
             hl.copy_(lse, non_blocking=True)
 
@@ -291,7 +297,7 @@ def main():
         e_ms = max_over_ranks(a0.elapsed_time(a1), dev) / n_e2e
         h2d = (hq.numel() + hk.numel() + hv.numel()) * hq.element_size()
         d2h = ho.numel() * ho.element_size() + hl.numel() * 4
-        e2e = {"value": round(job_throughput(ws, w.flops, e_ms), 2), "unit": "TFLOP/s", "ms_per_step": round(e_ms, 4),
+        e2e = {"value": round(job_throughput(ws, flops, e_ms), 2), "unit": "TFLOP/s", "ms_per_step": round(e_ms, 4),
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
                "path": "pinned host -> cudaMemcpyAsync -> fa_fwd -> cudaMemcpyAsync -> pinned host"}
 
@@ -302,7 +308,7 @@ def main():
         return
 
     peak, peak_src, _ = peaks()
-    achieved = w.flops / (ms * 1e-3) / 1e12
+    achieved = flops / (ms * 1e-3) / 1e12
     traffic = recorded_traffic(w.name)
     line = {
         "metric": "attention fwd TFLOP/s (4*B*H*N^2*d) and % of GB300 dense BF16 tensor peak",

@@ -61,6 +61,8 @@ def lib(path: str | None = None):
     u64 = ctypes.c_ulonglong
     L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, u64, vp]
     L.fa_fwd_splitkv.restype = i
+    L.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, vp]
+    L.fa_fwd_ex.restype = i
     L.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
     L.fa_fwd_splitkv_noalloc.restype = i
     L.fa_fwd_splitkv_num_splits.argtypes = [i, i, i, i]
@@ -76,6 +78,10 @@ def lib(path: str | None = None):
 
 def fa_fwd(Q, K, V, O, LSE, B, H, N, d, scale, dtype, stream=None) -> int:
     return lib().fa_fwd(Q, K, V, O, LSE, B, H, N, d, scale, dtype, stream)
+
+
+def fa_fwd_ex(Q, K, V, O, LSE, B, H, N, d, scale, dtype, causal, seqlens_k, stream=None) -> int:
+    return lib().fa_fwd_ex(Q, K, V, O, LSE, B, H, N, d, scale, dtype, causal, seqlens_k, stream)
 
 
 def fa_fwd_splitkv(Q, K, V, O, LSE, B, H, N, d, scale, dtype, num_splits, workspace, workspace_bytes,
@@ -124,13 +130,15 @@ def _dtype_code(t):
 
 
 def attention(q, k, v, scale: float | None = None, out=None, lse=None, stream=None, num_splits: int = 1,
-              workspace=None):
+              workspace=None, causal: bool = False, seqlens_k=None):
     """O, LSE for q, k, v of shape [B, H, N, d] (contiguous CUDA tensors, same dtype).
 
     Returns O (same dtype as q) and LSE (fp32 [B, H, N], natural log). ``out`` and
     ``lse`` may be preallocated; ``stream`` defaults to torch's current stream.
     ``num_splits`` != 1 runs the split-KV path (0 = automatic count); its
     workspace is allocated with torch unless a CUDA uint8 tensor is given.
+    ``causal`` / ``seqlens_k`` (CUDA int32 tensor [B] of key lengths) select the
+    masked pass (not combined with split-KV).
     """
     import torch
     if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
@@ -158,7 +166,17 @@ def attention(q, k, v, scale: float | None = None, out=None, lse=None, stream=No
     elif hasattr(stream, "cuda_stream"):
         stream = stream.cuda_stream
     with torch.cuda.device(q.device):
-        if num_splits == 1:
+        if causal or seqlens_k is not None:
+            if num_splits != 1:
+                raise ValueError("masks are not combined with split-KV")
+            kl = None
+            if seqlens_k is not None:
+                if seqlens_k.dtype != torch.int32 or not seqlens_k.is_cuda or seqlens_k.numel() != B:
+                    raise ValueError("seqlens_k must be a CUDA int32 tensor of B lengths")
+                kl = seqlens_k.contiguous().data_ptr()
+            rc = fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                           B, H, N, d, float(scale), _dtype_code(q), int(bool(causal)), kl, stream)
+        elif num_splits == 1:
             rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                         B, H, N, d, float(scale), _dtype_code(q), stream)
         else:
@@ -173,7 +191,7 @@ def attention(q, k, v, scale: float | None = None, out=None, lse=None, stream=No
     return out, lse
 
 
-__all__ = ["attention", "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_num_splits",
+__all__ = ["attention", "fa_fwd", "fa_fwd_ex", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_num_splits",
            "fa_fwd_splitkv_workspace_size",
            "fa_get_device_status", "fa_strerror", "fa_abi_version", "build", "lib",
            "FAError", "FA_F32", "FA_F16", "FA_BF16", "FA_OK"]

@@ -195,12 +195,13 @@ unsigned long long workspace_bytes_for(int B, int H, int N, int d, int splits) {
 int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
              float scale, int dtype, void* stream, int inject, float* stats_trace, unsigned long long* timeline,
              long long wait_limit, int num_splits = 1, void* workspace = nullptr,
-             unsigned long long workspace_bytes = 0) {
+             unsigned long long workspace_bytes = 0, int causal = 0, const int* klen = nullptr) {
   if (!Q || !K || !V || !O || !LSE) return FA_ERR_NULL;
   if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
   if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
   if (d != 64 && d != 128) return FA_ERR_HEADDIM;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
+  if (causal != 0 && causal != 1) return FA_ERR_SHAPE;
   const long long BH = static_cast<long long>(B) * H;
   if (BH > 0x7fffffffLL || BH * N > (1ll << 40) / d) return FA_ERR_SHAPE;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
@@ -223,6 +224,8 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
   p.inject = inject;
   p.stats_trace = stats_trace;
   p.timeline = timeline;
+  p.causal = causal;
+  p.klen = klen;
   p.B = B;
   p.H = H;
   p.N = N;
@@ -268,6 +271,12 @@ extern "C" {
 int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, float scale,
            int dtype, void* stream) {
   return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, dtype, stream, 0, nullptr, nullptr, 0);
+}
+
+int fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
+              float scale, int dtype, int causal, const int* seqlens_k, void* stream) {
+  return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, dtype, stream, 0, nullptr, nullptr, 0, 1, nullptr, 0, causal,
+                  seqlens_k);
 }
 
 int fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,

@@ -109,6 +109,9 @@ __device__ __forceinline__ void producer(const FwdParams& p, uint32_t base, int 
   tma_prefetch_desc(&p.tm_v);
   tma_prefetch_desc(&p.tm_o);
 
+  // A unit with no key tile (key length 0) loads nothing: its epilogue writes
+  // zeros into the Q buffers, which no copy may land in afterwards.
+  if (nkv == 0) return;
   const uint32_t bq = bar_addr<D>(base, C::B_Q);
   mbar_arrive_expect_tx(bq, (has1 ? 2u : 1u) * C::Q_SUB_BYTES);
   for (int sub = 0; sub < (has1 ? 2 : 1); ++sub)
@@ -168,7 +171,7 @@ __device__ __forceinline__ void producer(const FwdParams& p, uint32_t base, int 
 // window instead of both chains requesting the pipe at the same time.
 template <int D, bool BF16, int SUB>
 __device__ __forceinline__ void mma_warp(const FwdParams& p, uint32_t base, uint32_t tmem, bool has1, int nkv,
-                                         const WaitCtl& ctl) {
+                                         int nkv_other, const WaitCtl& ctl) {
   using C = Cfg<D>;
   constexpr int sub = SUB;
   constexpr uint32_t fmt = BF16 ? 1u : 0u;
@@ -186,12 +189,15 @@ __device__ __forceinline__ void mma_warp(const FwdParams& p, uint32_t base, uint
   const uint32_t b_od = bar_addr<D>(base, C::B_OD + sub), b_drain = bar_addr<D>(base, C::B_DRAIN + sub);
   const uint32_t my_turn = bar_addr<D>(base, C::B_TURN + sub), next_turn = bar_addr<D>(base, C::B_TURN + (sub ^ 1));
 
+  if (nkv == 0) goto drain;  // no key to attend to (key length 0): nothing to issue
   if (!wait_bar_warp(bar_addr<D>(base, C::B_Q), 0, ctl, kWhereQ)) goto drain;
   tc_fence_after();
   for (int j = 0; j <= nkv; ++j) {
-    // My block j follows the other chain's block j-1 (sub 0) or block j (sub 1).
-    if (has1 && (sub == 1 || j > 0)) {
-      if (!wait_bar_warp(my_turn, (sub == 1 ? j : j - 1) & 1, ctl, kWhereTurn)) goto drain;
+    // My block j follows the other chain's block j-1 (sub 0) or block j (sub 1),
+    // as long as the other chain has that block (its tile count can differ).
+    const int other = sub == 1 ? j : j - 1;
+    if (has1 && other >= 0 && other <= nkv_other && nkv_other > 0) {
+      if (!wait_bar_warp(my_turn, other & 1, ctl, kWhereTurn)) goto drain;
     }
     if (j > 0) {
       // P(j-1) V_{j-1}
@@ -252,13 +258,16 @@ drain:
 // --------------------------------------------------------------------------
 template <int D, bool BF16>
 __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, uint32_t tmem, int sub, int bh, int row0,
-                                           int split, int t0, int nkv, const WaitCtl& ctl) {
+                                           int split, int t0, int nkv, int key_end, const WaitCtl& ctl) {
   using C = Cfg<D>;
   const int t = threadIdx.x - sub * 128;  // row within the sub-tile
   const int lane = threadIdx.x & 31;
   const uint32_t lane_base = static_cast<uint32_t>(t & ~31) << 16;
   const uint32_t t_o = tmem + lane_base + (sub ? C::T_O1 : C::T_O0);
   const float c = p.scale * kLog2e;  // scores in log2 units: x = s * c
+  // Keys this row may see: [0, row_end) (all keys up to key_end; causal: up to the row itself).
+  const int my_row = row0 + C::BM * sub + t;
+  const int row_end = p.causal ? min(key_end, my_row + 1) : key_end;
 
   float m_ref = -INFINITY;  // reference max (log2 units) shared by l and O
   float l = 0.f;            // sum of P (fp32) relative to m_ref: gives LSE
@@ -289,7 +298,7 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
       for (int u = 0; u < 32; ++u) s[32 * q + u] = __uint_as_float(sraw[q][u]);
     }
 
-    const int valid = p.N - (t0 + j) * C::BN;  // keys of this tile inside the sequence
+    const int valid = row_end - (t0 + j) * C::BN;  // keys of this tile this row may see
     if (valid < C::BN) {
 #pragma unroll
       for (int u = 0; u < C::BN; ++u)
@@ -382,14 +391,16 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
 #endif
   }
   // The last P.V of this sub-tile; its commit also covers every earlier MMA of the warp.
-  if (ok)
+  if (ok && nkv > 0)
     ok = __all_sync(0xffffffffu, wait_bar(b_od, (nkv - 1) & 1, ctl, kWhereODone));
   // The whole warpgroup agrees before the epilogue, whose named barrier needs all 128 threads.
   if (!named_bar_and(1 + sub, 128, ok)) return;
 
   // ---- epilogue: O / l -> dtype -> swizzled staging (Q buffer) -> TMA store; LSE ----
   tc_fence_after();
-  const float inv_l = 1.0f / (BF16 ? l_o : l);
+  // No key to attend to (key length 0): O = 0, LSE = -inf instead of 0/0.
+  const bool empty = nkv == 0;
+  const float inv_l = empty ? 0.f : 1.0f / (BF16 ? l_o : l);
   if (p.num_splits > 1) {
     // Split-KV: this key range's normalised O (fp32) and LSE go to the partial buffers.
     const int row = row0 + C::BM * sub + t;
@@ -418,6 +429,10 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
     tmem_ld32(t_o + 32 * q, r);
     tmem_ld_wait();
     reg_fence(r);
+    if (empty) {
+#pragma unroll
+      for (int u = 0; u < 32; ++u) r[u] = 0u;  // TMEM O was never written
+    }
     uint32_t pk[16];
 #pragma unroll
     for (int u = 0; u < 16; ++u)
@@ -443,7 +458,7 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
     tma_store_wait_all();
   }
   const int row = row0 + C::BM * sub + t;
-  if (row < p.N) p.lse[static_cast<size_t>(bh) * p.N + row] = (m_ref + lg2_approx(l)) * kLn2;
+  if (row < p.N) p.lse[static_cast<size_t>(bh) * p.N + row] = empty ? -INFINITY : (m_ref + lg2_approx(l)) * kLn2;
 }
 
 template <int D, bool BF16>
@@ -461,11 +476,19 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
   const int split = blockIdx.x % p.num_splits;
   const int qunit = blockIdx.x / p.num_splits;
   const int bh = qunit / nqb;
-  const int row0 = (qunit % nqb) * 2 * C::BM;
+  // Causal: Q blocks later in the sequence see more keys; they are launched first.
+  const int qb = p.causal ? nqb - 1 - qunit % nqb : qunit % nqb;
+  const int row0 = qb * 2 * C::BM;
   const bool has1 = row0 + C::BM < p.N;
-  const int nkv_all = (p.N + C::BN - 1) / C::BN;
+  // Keys this unit may see: [0, key_end); causal limits each sub-tile to its own last row.
+  const int key_end = p.klen ? max(0, min(p.N, p.klen[bh / p.H])) : p.N;
+  const int end0 = p.causal ? min(key_end, row0 + C::BM) : key_end;
+  const int end1 = p.causal ? min(key_end, row0 + 2 * C::BM) : key_end;
   const int t0 = split * p.split_tiles;                      // first K/V tile of this key range
-  const int nkv = min(nkv_all - t0, p.split_tiles);          // >= 1 (checked on the host)
+  // Tiles per sub-tile (masks are not combined with split-KV: then t0 = 0, split_tiles = all tiles).
+  const int nkv0 = min((end0 + C::BN - 1) / C::BN - t0, p.split_tiles);
+  const int nkv1 = has1 ? min((end1 + C::BN - 1) / C::BN - t0, p.split_tiles) : 0;
+  const int nkv = max(nkv0, nkv1);                           // tiles the producer loads
 
   if (threadIdx.x == 0) {
     mbar_init(bar_addr<D>(base, C::B_Q), 1);
@@ -504,15 +527,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
       __syncwarp();
     } else if (warp == C::WARP_MMA0 || (warp == C::WARP_MMA1 && has1)) {
       if (warp == C::WARP_MMA0)
-        mma_warp<D, BF16, 0>(p, base, tmem, has1, nkv, ctl);
+        mma_warp<D, BF16, 0>(p, base, tmem, has1, nkv0, nkv1, ctl);
       else
-        mma_warp<D, BF16, 1>(p, base, tmem, has1, nkv, ctl);
+        mma_warp<D, BF16, 1>(p, base, tmem, has1, nkv1, nkv0, ctl);
       __syncwarp();
     }
   } else {
     warpgroup_reg_alloc<C::HIGH_REGS>();
     const int sub = warp / 4;
-    if (sub == 0 || has1) softmax_wg<D, BF16>(p, base, tmem, sub, bh, row0, split, t0, nkv, ctl);
+    if (sub == 0 || has1)
+      softmax_wg<D, BF16>(p, base, tmem, sub, bh, row0, split, t0, sub ? nkv1 : nkv0, key_end, ctl);
   }
 
   tc_fence_before();

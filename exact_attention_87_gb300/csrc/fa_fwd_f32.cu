@@ -115,7 +115,10 @@ __global__ void __launch_bounds__(128, 1) fa_fwd_f32_kernel(const __grid_constan
   const int nqb = (p.N + C::BM - 1) / C::BM;
   const int bh = blockIdx.x / nqb;
   const int row0 = (blockIdx.x % nqb) * C::BM;
-  const int nkv = (p.N + C::BN - 1) / C::BN;
+  // Keys this tile may see: [0, key_end); causal rows see keys up to themselves.
+  const int key_end = p.klen ? max(0, min(p.N, p.klen[bh / p.H])) : p.N;
+  const int tile_end = p.causal ? min(key_end, row0 + C::BM) : key_end;
+  const int nkv = (tile_end + C::BN - 1) / C::BN;
   const size_t head = static_cast<size_t>(bh) * p.N * D;
   const float* q = static_cast<const float*>(p.q) + head;
   const float* k = static_cast<const float*>(p.k) + head;
@@ -182,7 +185,8 @@ __global__ void __launch_bounds__(128, 1) fa_fwd_f32_kernel(const __grid_constan
     tmem_ld_wait();
 #pragma unroll
     for (int qd = 0; qd < C::BN / 32; ++qd) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&sr[32 * qd]));
-    const int valid = p.N - j * C::BN;
+    const int my_row = row0 + t;
+    const int valid = (p.causal ? min(key_end, my_row + 1) : key_end) - j * C::BN;
     float mx = -INFINITY;
 #pragma unroll
     for (int u = 0; u < C::BN; ++u) {
@@ -253,7 +257,9 @@ __global__ void __launch_bounds__(128, 1) fa_fwd_f32_kernel(const __grid_constan
   }
 
   if (ok) {
-    const float inv_l = 1.0f / l;
+    // No key to attend to (key length 0): O = 0, LSE = -inf instead of 0/0.
+    const bool empty = nkv == 0;
+    const float inv_l = empty ? 0.f : 1.0f / l;
     const int row = row0 + t;
     float* o = static_cast<float*>(p.o) + head;
 #pragma unroll
@@ -262,6 +268,10 @@ __global__ void __launch_bounds__(128, 1) fa_fwd_f32_kernel(const __grid_constan
       tmem_ld32(t_o + 32 * qd, r);
       tmem_ld_wait();
       reg_fence(r);
+      if (empty) {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) r[u] = 0u;  // TMEM O was never written
+      }
       if (row < p.N) {
         float4* dst = reinterpret_cast<float4*>(o + static_cast<size_t>(row) * D + 32 * qd);
 #pragma unroll
@@ -270,7 +280,7 @@ __global__ void __launch_bounds__(128, 1) fa_fwd_f32_kernel(const __grid_constan
                                __uint_as_float(r[4 * u + 2]) * inv_l, __uint_as_float(r[4 * u + 3]) * inv_l);
       }
     }
-    if (row < p.N) p.lse[static_cast<size_t>(bh) * p.N + row] = (m + lg2_approx(l)) * kLn2;
+    if (row < p.N) p.lse[static_cast<size_t>(bh) * p.N + row] = empty ? -INFINITY : (m + lg2_approx(l)) * kLn2;
   } else if (warp == 0) {
     // Drain: every MMA this warp issued must finish before TMEM is freed.
     tc_commit_elect(bar_drain);

@@ -41,6 +41,10 @@ struct alignas(64) FwdParams {
   int split_tiles;
   float* o_part;
   float* lse_part;
+  // Masks: causal (row i sees keys j <= i) and per-batch key lengths
+  // (klen[b]: keys j >= klen[b] masked; NULL = all N keys).
+  int causal;
+  const int* klen;
   // Used only by the testing build (-DFA_TESTING); zero / NULL otherwise.
   int inject;                       // 1: the producer skips the V load of tile 0
   float* stats_trace;               // [B*H*N, nkv, 2]: (m in natural-log units, l) after each K/V tile

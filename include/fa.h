@@ -77,6 +77,23 @@ int fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
            int B, int H, int N, int d, float scale, int dtype, void *stream);
 
 /*
+ * Masked forward pass. The Triton page masks scores with -inf where keys must
+ * not be seen ("FlashAttention + Triton", section 4.3: boundary masks; section
+ * 5.1: padded variable-length batches, where a row can be fully masked).
+ *   causal:    0 or 1. 1: query row i sees keys j <= i only.
+ *   seqlens_k: NULL, or a DEVICE array of B int32 key lengths: row i of batch
+ *              b sees keys j < seqlens_k[b] only (values are clamped to
+ *              [0, N]). Padded keys may hold anything (their scores are
+ *              replaced by -inf); padded values must be finite (they are
+ *              multiplied by zero weights).
+ * A row with no key to see (seqlens_k[b] == 0) gets O = 0 and LSE = -inf.
+ * Other arguments and errors: as fa_fwd (causal outside {0, 1}: FA_ERR_SHAPE).
+ */
+int fa_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE,
+              int B, int H, int N, int d, float scale, int dtype,
+              int causal, const int *seqlens_k, void *stream);
+
+/*
  * Split-KV forward pass: the same result as fa_fwd, computed by splitting the
  * keys of every (batch, head) into `num_splits` contiguous ranges (multiples of
  * 128 keys) that run as separate work units, then merging the per-range

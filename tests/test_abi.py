@@ -101,3 +101,8 @@ def test_splitkv_workspace_size_formula(L):
     assert fa.fa_fwd_splitkv_workspace_size(0, 1, 300, 64, 2) == 0
     assert fa.fa_fwd_splitkv(0, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, 2, A, 1 << 20, None) == fa.FA_ERR_NULL
     assert fa.fa_fwd_splitkv(A, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, -1, A, 1 << 20, None) == fa.FA_ERR_SHAPE
+
+
+def test_masked_entry_point_argument_errors(L):
+    assert fa.fa_fwd_ex(A, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, 2, None, None) == fa.FA_ERR_SHAPE
+    assert fa.fa_fwd_ex(0, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, 1, None, None) == fa.FA_ERR_NULL
