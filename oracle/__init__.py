@@ -18,7 +18,15 @@ all in fp64 from the already-rounded inputs (fp16/bf16/fp32 upcast exactly).
 ``attn_online`` is the tiled recurrence of the same page's "FlashAttention
 完整算法" formula, in fp64, with an optional lazy-rescale threshold.
 ``merge`` combines results computed over disjoint key ranges with the block
-merge of the Triton page (section 2.3), for split-KV.
+merge of the Triton page (section 2.3), for split-KV. ``attn_masked`` is the
+definition restricted to the allowed keys (causal, per-batch key lengths).
+``attn_bwd`` is the backward pass by recomputation (the MUSA guide's fourth
+core principle, the Triton page's sections 2.4 and 4.4): P is rebuilt from Q,
+K and the saved LSE, and the chain rule on the definition gives, with
+D_i = sum_c dO_ic O_ic,
+
+    dV = P^T dO,   dS_ij = P_ij (dO_i . v_j - D_i),
+    dQ = scale dS K,   dK = scale dS^T Q.
 """
 from __future__ import annotations
 
@@ -54,6 +62,8 @@ def _bind(path: str):
     lp = ctypes.POINTER(ctypes.c_long)
     lib.oracle_attn_masked_fp64.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, L, D, I, lp, I]
     lib.oracle_attn_masked_fp64.restype = I
+    lib.oracle_attn_bwd_fp64.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, L, L, L, D, I]
+    lib.oracle_attn_bwd_fp64.restype = I
     lib.oracle_merge_fp64.argtypes = [dp, dp, L, L, L, dp, dp]
     lib.oracle_merge_fp64.restype = I
     lib.oracle_mutant_id.restype = I
@@ -166,6 +176,23 @@ def attn_masked(q, k, v, causal: bool = False, klen=None, scale: float | None = 
     if rc != 0:
         raise RuntimeError(f"oracle_attn_masked_fp64 failed ({rc})")
     return o, lse
+
+
+def attn_bwd(q, k, v, o, do, lse, scale: float | None = None, nthreads: int | None = None, lib=None):
+    """Backward pass by recomputation: (dQ, dK, dV) fp64 for q, k, v, do [..., N, d], with the
+    forward outputs o [..., N, d] and lse [..., N]."""
+    q, k, v, o, do, lse = (_f64(t) for t in (q, k, v, o, do, lse))
+    lead, BH, N, Nk, d = _shapes(q, k, v)
+    if Nk != N or o.shape != q.shape or do.shape != q.shape or lse.shape != q.shape[:-1]:
+        raise ValueError("attn_bwd wants square attention and matching o / do / lse")
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    lib = lib or load()
+    rc = lib.oracle_attn_bwd_fp64(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                                  _ptr(dv), BH, N, d, scale, nthreads or default_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_bwd_fp64 failed ({rc})")
+    return dq, dk, dv
 
 
 def merge(o_parts, lse_parts, lib=None):

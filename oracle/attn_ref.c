@@ -24,6 +24,10 @@
  * Layouts: Q [BH, Nq, d], K and V [BH, Nk, d], O [BH, Nq, d], LSE [BH, Nq],
  * all row-major fp64. Build: gcc -O2 (no -ffast-math), libm exp/log.
  *
+ * oracle_attn_bwd_fp64 is the backward pass (gradients of Q, K, V for a given
+ * dO) written out from the chain rule on the same definition, P recomputed
+ * from the saved LSE.
+ *
  * ORACLE_MUTANT (compile-time, default 0) plants one deliberate mistake so
  * the pin tests can show that each such mistake is caught. Mutant builds are
  * made only by the tests, in a temporary directory.
@@ -335,6 +339,121 @@ int oracle_attn_masked_fp64(const double *Q, const double *K, const double *V, d
     }
     for (int t = 0; t < nthreads; ++t)
         if (!jobs[t].base.ok) return -2;
+    return 0;
+}
+
+/*
+ * Backward pass by recomputation (the MUSA guide's "重计算" principle and the
+ * Triton page, sections 2.4 and 4.4: P is not stored; it is recomputed from
+ * Q, K and the saved row statistics, then the chain rule is applied), for one
+ * (batch, head) slice at a time, by the definitions, in fp64:
+ *     P_ij  = exp(s_ij - LSE_i),  s_ij = scale * q_i . k_j
+ *     D_i   = sum_c dO_ic O_ic
+ *     dV_j  = sum_i P_ij dO_i
+ *     dP_ij = dO_i . v_j
+ *     dS_ij = P_ij (dP_ij - D_i)
+ *     dQ_i  = scale * sum_j dS_ij k_j
+ *     dK_j  = scale * sum_i dS_ij q_i
+ * O and LSE are the forward outputs passed in (from the oracle itself).
+ * Layouts as oracle_attn_fp64 (Nq = Nk = N); dQ/dK/dV like Q/K/V.
+ */
+typedef struct {
+    const double *Q, *K, *V, *O, *dO, *LSE;
+    double *dQ, *dK, *dV;
+    long N, d;
+    double scale;
+    long bh_begin, bh_end;
+    int ok;
+} bjob_t;
+
+static void *bwd_worker(void *arg)
+{
+    bjob_t *jb = (bjob_t *)arg;
+    long N = jb->N, d = jb->d;
+    double *P = (double *)malloc(sizeof(double) * (size_t)N * (size_t)N);
+    double *dS = (double *)malloc(sizeof(double) * (size_t)N * (size_t)N);
+    double *D = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!P || !dS || !D) { free(P); free(dS); free(D); jb->ok = 0; return NULL; }
+    for (long bh = jb->bh_begin; bh < jb->bh_end; ++bh) {
+        const double *Q = jb->Q + bh * N * d, *K = jb->K + bh * N * d, *V = jb->V + bh * N * d;
+        const double *O = jb->O + bh * N * d, *dO = jb->dO + bh * N * d, *L = jb->LSE + bh * N;
+        double *dQ = jb->dQ + bh * N * d, *dK = jb->dK + bh * N * d, *dV = jb->dV + bh * N * d;
+        for (long i = 0; i < N; ++i) {
+            double acc = 0.0;
+            for (long c = 0; c < d; ++c) acc += dO[i * d + c] * O[i * d + c];
+            D[i] = acc;
+            for (long j = 0; j < N; ++j) {
+                double s = 0.0, dp = 0.0;
+                for (long c = 0; c < d; ++c) {
+                    s += Q[i * d + c] * K[j * d + c];
+                    dp += dO[i * d + c] * V[j * d + c];
+                }
+                P[i * N + j] = exp(jb->scale * s - L[i]);
+#if ORACLE_MUTANT == 8 /* the D_i term dropped from dS */
+                dS[i * N + j] = P[i * N + j] * dp;
+#else
+                dS[i * N + j] = P[i * N + j] * (dp - D[i]);
+#endif
+            }
+        }
+        for (long j = 0; j < N; ++j)
+            for (long c = 0; c < d; ++c) {
+                double av = 0.0, ak = 0.0;
+                for (long i = 0; i < N; ++i) {
+#if ORACLE_MUTANT == 10 /* P transposed in dV */
+                    av += P[j * N + i] * dO[i * d + c];
+#else
+                    av += P[i * N + j] * dO[i * d + c];
+#endif
+                    ak += dS[i * N + j] * Q[i * d + c];
+                }
+                dV[j * d + c] = av;
+#if ORACLE_MUTANT == 9 /* scale dropped from dK */
+                dK[j * d + c] = ak;
+#else
+                dK[j * d + c] = jb->scale * ak;
+#endif
+            }
+        for (long i = 0; i < N; ++i)
+            for (long c = 0; c < d; ++c) {
+                double aq = 0.0;
+                for (long j = 0; j < N; ++j) aq += dS[i * N + j] * K[j * d + c];
+                dQ[i * d + c] = jb->scale * aq;
+            }
+    }
+    free(P); free(dS); free(D);
+    jb->ok = 1;
+    return NULL;
+}
+
+int oracle_attn_bwd_fp64(const double *Q, const double *K, const double *V, const double *O, const double *dO,
+                         const double *LSE, double *dQ, double *dK, double *dV, long BH, long N, long d,
+                         double scale, int nthreads)
+{
+    if (BH < 0 || N < 1 || d < 1) return -1;
+    if (BH == 0) return 0;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if ((long)nthreads > BH) nthreads = (int)BH;
+    bjob_t jobs[256];
+    pthread_t th[256];
+    int started[256];
+    long per = (BH + nthreads - 1) / nthreads;
+    for (int t = 0; t < nthreads; ++t) {
+        bjob_t j = {Q, K, V, O, dO, LSE, dQ, dK, dV, N, d, scale, t * per,
+                    (t + 1) * per < BH ? (t + 1) * per : BH, 0};
+        jobs[t] = j;
+        started[t] = 0;
+        if (jobs[t].bh_begin >= jobs[t].bh_end) { jobs[t].ok = 1; continue; }
+        if (t > 0 && pthread_create(&th[t], NULL, bwd_worker, &jobs[t]) == 0) started[t] = 1;
+    }
+    if (jobs[0].bh_begin < jobs[0].bh_end) bwd_worker(&jobs[0]);
+    for (int t = 1; t < nthreads; ++t) {
+        if (started[t]) pthread_join(th[t], NULL);
+        else if (jobs[t].bh_begin < jobs[t].bh_end) bwd_worker(&jobs[t]);
+    }
+    for (int t = 0; t < nthreads; ++t)
+        if (!jobs[t].ok) return -2;
     return 0;
 }
 

@@ -192,4 +192,74 @@ def pin_large_magnitude(lib):
     np.testing.assert_allclose(l1, l0 + q @ w, rtol=1e-14, atol=1e-10)
 
 
+def _bwd(lib, q, k, v, w, scale):
+    """Gradients of L = sum(W * O) from the oracle (dO = W), with the oracle's own O and LSE."""
+    o, lse = _attn(lib, q, k, v, scale=scale)
+    return oracle.attn_bwd(q, k, v, o, w, lse, scale=scale, nthreads=2, lib=lib)
+
+
+def pin_bwd_finite_differences(lib):
+    """Backward pass against central differences of the forward oracle's L = sum(W * O)."""
+    rng = np.random.default_rng(11)
+    B, H, N, d, scale = 1, 2, 9, 5, 0.6
+    q, k, v = (rng.standard_normal((B, H, N, d)) for _ in range(3))
+    w = rng.standard_normal((B, H, N, d))
+    dq, dk, dv = _bwd(lib, q, k, v, w, scale)
+    h = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for idx in [(0, 0, 0, 0), (0, 1, 4, 2), (0, 0, 8, 4), (0, 1, 3, 1), (0, 0, 5, 3)]:
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+            args_m = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+            lp = float((w * _attn(lib, *args_p, scale=scale)[0]).sum())
+            lm = float((w * _attn(lib, *args_m, scale=scale)[0]).sum())
+            assert abs((lp - lm) / (2 * h) - g[idx]) <= 1e-7 * max(1.0, abs(g[idx])), (name, idx)
+
+
+def pin_bwd_invariants(lib):
+    """Rows of P sum to one, so sum_j dV_j = sum_i dO_i; O does not change under
+    K -> K + 1 w^T, so sum_j dK_j = 0; O is linear in V, so V -> 3V leaves dV
+    and triples dQ and dK."""
+    rng = np.random.default_rng(12)
+    q, k, v = (rng.standard_normal((2, 2, 33, 8)) * 1.5 for _ in range(3))
+    w = rng.standard_normal(q.shape)
+    dq, dk, dv = _bwd(lib, q, k, v, w, 0.35)
+    np.testing.assert_allclose(dv.sum(axis=2), w.sum(axis=2), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk.sum(axis=2), 0.0, rtol=0, atol=1e-12)
+    dq2, dk2, dv2 = _bwd(lib, q, k, 3.0 * v, w, 0.35)
+    np.testing.assert_allclose(dv2, dv, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dq2, 3.0 * dq, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dk2, 3.0 * dk, rtol=1e-12, atol=1e-12)
+
+
+def pin_bwd_single_key(lib):
+    """N = 1: O = v whatever q and k are, so dV = dO and dQ = dK = 0."""
+    rng = np.random.default_rng(13)
+    q, k, v, w = (rng.standard_normal((1, 1, 1, 4)) for _ in range(4))
+    dq, dk, dv = _bwd(lib, q, k, v, w, 0.5)
+    np.testing.assert_allclose(dv, w, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(dq, 0.0, atol=1e-15)
+    np.testing.assert_allclose(dk, 0.0, atol=1e-15)
+
+
+def pin_bwd_uniform_attention(lib):
+    """Q = 0: P = 1/N everywhere, so dV_j = mean_i dO_i, and the closed form
+    dQ_i = scale/N * sum_j (dO_i . (v_j - O_i)) k_j with O_i = mean_j v_j."""
+    rng = np.random.default_rng(14)
+    N, d, scale = 7, 3, 0.8
+    q = np.zeros((1, 1, N, d))
+    k, v, w = (rng.standard_normal((1, 1, N, d)) for _ in range(3))
+    dq, dk, dv = _bwd(lib, q, k, v, w, scale)
+    np.testing.assert_allclose(dv[0, 0], np.broadcast_to(w[0, 0].mean(0), (N, d)), rtol=0, atol=1e-14)
+    vbar = v[0, 0].mean(0)
+    for i in range(N):
+        ref = np.zeros(d)
+        for j in range(N):
+            ref += math.fsum(w[0, 0, i] * (v[0, 0, j] - vbar)) * k[0, 0, j]
+        np.testing.assert_allclose(dq[0, 0, i], scale / N * ref, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dk, 0.0 * dk, atol=1e-13)  # q_i = 0 multiplies every term
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

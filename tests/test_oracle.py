@@ -25,6 +25,9 @@ MUTANTS = {
     5: "off-by-one value row",
     6: "max term dropped from LSE",
     7: "transposed score matrix",
+    8: "backward: D term dropped from dS",
+    9: "backward: scale dropped from dK",
+    10: "backward: P transposed in dV",
 }
 
 
@@ -190,3 +193,4 @@ def test_fully_masked_rows_are_guarded():
     o, lse = oracle.attn_masked(q, k, v, klen=[0, 20])
     assert np.all(o[0] == 0) and np.all(np.isneginf(lse[0]))
     assert np.all(np.isfinite(o[1])) and np.all(np.isfinite(lse[1]))
+
