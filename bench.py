@@ -189,6 +189,8 @@ def main():
                     help="causal mask (FLOPs counted for the keys each row sees: 4*d*N*(N+1)/2 per head)")
     ap.add_argument("--splits", type=int, default=1,
                     help="split-KV ranges (0 = automatic; 1 = the plain forward pass)")
+    ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
+                    help="bwd: time the backward pass (fa_bwd: dQ, dK, dV; 10*B*H*N^2*d FLOPs) instead")
     ap.add_argument("--batch", type=int, default=None,
                     help="override B (smaller captures of the same workload for profiling; not a bench line)")
     args = ap.parse_args()
@@ -210,6 +212,8 @@ def main():
 
     if args.impl == "reference":
         return run_reference(args, w, cfg, ws, rank)
+    if args.which == "bwd":
+        return run_backward(args, w, cfg, ws, rank, local)
 
     import torch
     import torch.distributed as dist
@@ -337,6 +341,141 @@ def main():
         flops, secs, threads, desc = run_oracle_sample(w, q, k, v, args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
                                 "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_backward(args, w, cfg, ws, rank, local):
+    """Time the backward pass (fa_bwd: row statistics, main pass, dQ rounding) for
+    the workload, given the forward pass's O and LSE and a seeded dO."""
+    import torch
+    import torch.distributed as dist
+    import exact_attention_87_gb300 as fa
+    from workloads import make_dout, make_inputs
+
+    if args.causal or args.splits != 1:
+        raise SystemExit("--pass bwd takes neither --causal nor --splits")
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fa.build()
+    fa.lib()
+    flops = 10 * w.B * w.H * w.N * w.N * w.d  # five N x N x d products per (b, h)
+    cfg = dict(cfg, pass_="bwd", flops="10*B*H*N^2*d (S, dP, dV, dK, dQ products)")
+    cfg["pass"] = cfg.pop("pass_")
+    q, k, v = make_inputs(w)
+    do = make_dout(w.B, w.H, w.N, w.d, w.dtype, seed=0, wid=w.wid)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    stream = torch.cuda.current_stream(dev)
+    o, lse = fa.attention(qd, kd, vd, scale=w.scale, stream=stream)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    wsp = torch.empty(fa.fa_bwd_workspace_size(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
+
+    def step():
+        fa.attention_backward(qd, kd, vd, o, lse, dod, scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=wsp,
+                              stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.fa_get_device_status() != fa.FA_OK:
+        raise RuntimeError("device status error after warm-up")
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    with sampler:
+        barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1), dev) / args.steps
+    st = fa.fa_get_device_status()
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status {st} after the timed region")
+    tflops = job_throughput(ws, flops, ms)
+
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
+        ho, hl = o.cpu().pin_memory(), lse.cpu().pin_memory()
+        hg = [torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3)]
+        od, ld = torch.empty_like(o), torch.empty_like(lse)
+
+        def e2e_step():
+            for dst, src in ((qd, hq), (kd, hk), (vd, hv), (od, ho), (ld, hl), (dod, hdo)):
+                dst.copy_(src, non_blocking=True)
+            fa.attention_backward(qd, kd, vd, od, ld, dod, scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=wsp,
+                                  stream=stream)
+            for dst, src in zip(hg, (dq, dk, dv)):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        n_e2e = max(3, min(args.steps, 10))
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        a1.record(stream)
+        barrier()
+        e_ms = max_over_ranks(a0.elapsed_time(a1), dev) / n_e2e
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, ho, hl, hdo))
+        d2h = sum(t.numel() * t.element_size() for t in hg)
+        e2e = {"value": round(job_throughput(ws, flops, e_ms), 2), "unit": "TFLOP/s", "ms_per_step": round(e_ms, 4),
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "path": "pinned host -> cudaMemcpyAsync -> fa_bwd -> cudaMemcpyAsync -> pinned host"}
+    if rank != 0:
+        if ws > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+    peak, peak_src, _ = peaks()
+    achieved = flops / (ms * 1e-3) / 1e12
+    es = 2
+    line = {
+        "metric": "attention bwd TFLOP/s (10*B*H*N^2*d) and % of GB300 dense BF16 tensor peak",
+        "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded, generated on the host)", "config": cfg,
+        "pct_of_peak": round(100.0 * achieved / peak, 2),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                     "kernel": "whole step: fa_bwd_pre + fa_bwd_main + fa_bwd_post", "traffic": None,
+                     "algorithmic_bytes": 8 * w.B * w.H * w.N * w.d * es + 4 * w.B * w.H * w.N},
+        "clocks": sampler.summary(),
+        "gpu_launches": 3 * args.steps,
+        "e2e": e2e,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        n = min(w.N, 768)
+        threads = oracle.default_threads()
+        secs, heads = 0.0, 0
+        while secs < args.cpu_seconds and heads < w.B * w.H:
+            b, h = divmod(heads, w.H)
+            sl = (b, h, slice(0, n))
+            oh, lh = oracle.attn(q[sl], k[sl], v[sl], scale=w.scale, nthreads=threads)
+            t0 = time.perf_counter()
+            oracle.attn_bwd(q[sl], k[sl], v[sl], oh, do[sl], lh, scale=w.scale, nthreads=threads)
+            secs += time.perf_counter() - t0
+            heads += 1
+        line["cpu_baseline"] = {"value": round(heads * 10 * n * n * w.d / secs / 1e12, 6), "unit": "TFLOP/s",
+                                "cores": 1, "kind": "oracle", "seconds": round(secs, 2),
+                                "sample": f"{heads} heads truncated to their first {n} queries and keys "
+                                          "(fp64 backward timed; its O, LSE from the forward oracle, untimed; "
+                                          "one head runs on one thread)"}
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.barrier()

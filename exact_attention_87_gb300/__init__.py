@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) FlashAttention forward pass.
+"""GB300 (sm_103a) FlashAttention forward and backward passes.
 
 Python binding of the C ABI in ``include/fa.h``: argument marshalling only.
 Every step of the computation runs in the library's CUDA kernels; there is no
@@ -6,6 +6,7 @@ CPU fallback. If the compiled library is missing, every call raises.
 
     import exact_attention_87_gb300 as fa
     O, LSE = fa.attention(q, k, v)          # q, k, v: [B, H, N, d] CUDA tensors
+    dQ, dK, dV = fa.attention_backward(q, k, v, O, LSE, dO)
 
 ``fa_fwd`` / ``fa_get_device_status`` / ``fa_strerror`` / ``fa_abi_version``
 are the C entry points under the same names (pointers as Python ints).
@@ -23,7 +24,7 @@ FA_OK = 0
 STATUS_NAMES = {
     0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_DTYPE", 3: "FA_ERR_SHAPE", 4: "FA_ERR_HEADDIM",
     5: "FA_ERR_ALIGN", 6: "FA_ERR_CUDA", 7: "FA_ERR_DEVICE_TIMEOUT", 8: "FA_ERR_ARCH", 9: "FA_ERR_SCALE",
-    10: "FA_ERR_WORKSPACE", 11: "FA_ERR_SCRATCH_LIMIT",
+    10: "FA_ERR_WORKSPACE", 11: "FA_ERR_SCRATCH_LIMIT", 12: "FA_ERR_UNSUPPORTED", 13: "FA_ERR_DEVICE_SMEM",
 }
 for _code, _name in STATUS_NAMES.items():
     globals()[_name] = _code
@@ -69,6 +70,10 @@ def lib(path: str | None = None):
     L.fa_fwd_splitkv_num_splits.restype = i
     L.fa_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i]
     L.fa_fwd_splitkv_workspace_size.restype = u64
+    L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, u64, vp]
+    L.fa_bwd.restype = i
+    L.fa_bwd_workspace_size.argtypes = [i, i, i, i]
+    L.fa_bwd_workspace_size.restype = u64
     if path == LIB_PATH:
         _lib = L
     return L
@@ -102,6 +107,16 @@ def fa_fwd_splitkv_num_splits(B, H, N, d) -> int:
 
 def fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits) -> int:
     return lib().fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits)
+
+
+def fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype, workspace, workspace_bytes,
+           stream=None) -> int:
+    return lib().fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype, workspace, workspace_bytes,
+                        stream)
+
+
+def fa_bwd_workspace_size(B, H, N, d) -> int:
+    return lib().fa_bwd_workspace_size(B, H, N, d)
 
 
 def fa_get_device_status(stream=None) -> int:
@@ -191,7 +206,51 @@ def attention(q, k, v, scale: float | None = None, out=None, lse=None, stream=No
     return out, lse
 
 
-__all__ = ["attention", "fa_fwd", "fa_fwd_ex", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_num_splits",
+def attention_backward(q, k, v, o, lse, do, scale: float | None = None, dq=None, dk=None, dv=None, workspace=None,
+                       stream=None):
+    """dQ, dK, dV for the forward pass O, LSE = attention(q, k, v, scale) and the
+    output gradient do (all [B, H, N, d] contiguous CUDA tensors of one 16-bit
+    dtype; lse fp32 [B, H, N]). ``dq``/``dk``/``dv`` may be preallocated; the
+    workspace (fa_bwd_workspace_size bytes) is allocated with torch unless a
+    CUDA uint8 tensor is given; ``stream`` defaults to torch's current stream.
+    """
+    import torch
+    for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{name} must match q in shape and dtype: {tuple(t.shape)} {t.dtype}")
+    if q.dim() != 4:
+        raise ValueError(f"q must be [B, H, N, d]: {tuple(q.shape)}")
+    B, H, N, d = q.shape
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32:
+        raise ValueError("lse must be an fp32 [B, H, N] tensor")
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do), ("lse", lse)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous tensor like q")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    with torch.cuda.device(q.device):
+        need = fa_bwd_workspace_size(B, H, N, d)
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+        rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                    dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, float(scale), _dtype_code(q),
+                    workspace.data_ptr(), workspace.numel(), stream)
+    if rc != FA_OK:
+        raise FAError(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+__all__ = ["attention", "attention_backward", "fa_bwd", "fa_bwd_workspace_size", "fa_fwd", "fa_fwd_ex", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_num_splits",
            "fa_fwd_splitkv_workspace_size",
            "fa_get_device_status", "fa_strerror", "fa_abi_version", "build", "lib",
            "FAError", "FA_F32", "FA_F16", "FA_BF16", "FA_OK"]

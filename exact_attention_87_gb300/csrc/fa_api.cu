@@ -103,6 +103,18 @@ bool encode_bhnd_16bit(CUtensorMap* map, const void* ptr, int BH, int N, int d, 
   return r == CUDA_SUCCESS;
 }
 
+// [B*H, N, d] fp32 tensor, boxes of 32 (d) x 128 rows, 128-byte swizzle (the dQ accumulator).
+bool encode_bhnd_f32_box32(CUtensorMap* map, void* ptr, int BH, int N, int d) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4};
+  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Device address of the built-in scratch on the current device, looked up once
@@ -146,6 +158,8 @@ const char* fa_strerror(int status) {
     case FA_ERR_SCRATCH_LIMIT:
       return "this shape's split-KV workspace exceeds the library's 32 MiB built-in scratch "
              "(fa_fwd_splitkv_noalloc); use fa_fwd_splitkv with a caller workspace";
+    case FA_ERR_UNSUPPORTED: return "this entry point does not take the given dtype (fa_bwd takes FA_F16 or FA_BF16)";
+    case FA_ERR_DEVICE_SMEM: return "a kernel found its dynamic shared memory misaligned and did no work";
     default: return "unknown status";
   }
 }
@@ -325,6 +339,77 @@ unsigned long long fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int
   return workspace_bytes_for(B, H, N, d, static_cast<int>((tiles + per - 1) / per));
 }
 
+namespace {
+
+// fa_bwd workspace: fp32 dQ accumulator [B*H, N, d], then LSE*log2(e) and D
+// per row of the 128-row padded layout [B*H, n_pad], each part 256-byte aligned.
+unsigned long long bwd_part_bytes(unsigned long long n) { return (n + 255) & ~255ull; }
+
+}  // namespace
+
+unsigned long long fa_bwd_workspace_size(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  const unsigned long long bh = static_cast<unsigned long long>(B) * H;
+  const unsigned long long n_pad = static_cast<unsigned long long>(kv_tiles(N)) * fa::kF16BlockKV;
+  return bwd_part_bytes(bh * N * d * 4) + 2 * bwd_part_bytes(bh * n_pad * 4);
+}
+
+int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE, void* dQ,
+           void* dK, void* dV, int B, int H, int N, int d, float scale, int dtype, void* workspace,
+           unsigned long long workspace_bytes, void* stream) {
+  if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return FA_ERR_NULL;
+  if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+  if (dtype == FA_F32) return FA_ERR_UNSUPPORTED;
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > 0x7fffffffLL || BH * N > (1ll << 40) / d) return FA_ERR_SHAPE;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) || !aligned16(dQ) ||
+      !aligned16(dK) || !aligned16(dV) || (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0)
+    return FA_ERR_ALIGN;
+  const unsigned long long need = fa_bwd_workspace_size(B, H, N, d);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
+    return FA_ERR_WORKSPACE;
+
+  DeviceInfo dev;
+  const int st = device_info(&dev);
+  if (st != FA_OK) return st;
+
+  fa::BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.o = O;
+  p.dout = dO;
+  p.lse = LSE;
+  p.dq = dQ;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.d = d;
+  p.scale = scale;
+  p.n_pad = static_cast<int>(kv_tiles(N) * fa::kF16BlockKV);
+  p.status = dev.status;
+  p.wait_limit = wait_limit_cycles();
+  const unsigned long long acc_bytes = bwd_part_bytes(static_cast<unsigned long long>(BH) * N * d * 4);
+  const unsigned long long row_bytes = bwd_part_bytes(static_cast<unsigned long long>(BH) * p.n_pad * 4);
+  p.dq_acc = static_cast<float*>(workspace);
+  p.lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_bytes);
+  p.dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_bytes + row_bytes);
+
+  const CUtensorMapDataType dt = dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const int bh = static_cast<int>(BH);
+  if (!encode_bhnd_16bit(&p.tm_q, Q, bh, N, d, dt, fa::kF16BlockQ) ||
+      !encode_bhnd_16bit(&p.tm_k, K, bh, N, d, dt, fa::kF16BlockKV) ||
+      !encode_bhnd_16bit(&p.tm_v, V, bh, N, d, dt, fa::kF16BlockKV) ||
+      !encode_bhnd_16bit(&p.tm_do, dO, bh, N, d, dt, fa::kF16BlockQ) ||
+      !encode_bhnd_16bit(&p.tm_dk, dK, bh, N, d, dt, fa::kF16BlockKV) ||
+      !encode_bhnd_16bit(&p.tm_dv, dV, bh, N, d, dt, fa::kF16BlockKV) ||
+      !encode_bhnd_f32_box32(&p.tm_dqacc, p.dq_acc, bh, N, d))
+    return FA_ERR_CUDA;
+  const cudaError_t e = fa::launch_bwd_f16(p, dtype == FA_BF16, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 #ifdef FA_TESTING
 int fa_fwd_testing(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
                    float scale, int dtype, void* stream, int inject, float* stats_trace,
@@ -350,7 +435,7 @@ int fa_get_device_status(void* stream) {
   if (h[0] == 0) return FA_OK;
   const unsigned int zero[2] = {0, 0};
   if (cudaMemcpyToSymbol(g_fa_status, zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
-  return FA_ERR_DEVICE_TIMEOUT;
+  return (h[0] & fa::kStatusSmemAlign) ? FA_ERR_DEVICE_SMEM : FA_ERR_DEVICE_TIMEOUT;
 }
 
 }  // extern "C"

@@ -15,10 +15,13 @@ namespace fa {
 // Everything a bounded wait needs: the CTA's abort flag (a shared-memory
 // address) and the kernel parameters (status word, wait limit). Kept small:
 // once inlined, the parameter reads come from the kernel's parameter space.
-struct WaitCtl {
-  const FwdParams& p;   // the kernel's __grid_constant__ parameters
+// P is the kernel's parameter block (FwdParams or BwdParams).
+template <class P>
+struct WaitCtlT {
+  const P& p;           // the kernel's __grid_constant__ parameters
   uint32_t abort_addr;  // shared-memory address of the CTA's abort flag
 };
+using WaitCtl = WaitCtlT<FwdParams>;
 
 __device__ __forceinline__ int abort_raised(uint32_t addr) {
   int v;
@@ -26,13 +29,15 @@ __device__ __forceinline__ int abort_raised(uint32_t addr) {
   return v;
 }
 
-static __device__ __forceinline__ void record_timeout(const FwdParams& p, uint32_t abort_addr, unsigned where) {
+template <class P>
+static __device__ __forceinline__ void record_timeout(const P& p, uint32_t abort_addr, unsigned where) {
   atomicOr(p.status, kStatusTimeout);
   atomicCAS(p.status + 1, 0u, where);
   asm volatile("st.volatile.shared.s32 [%0], %1;" ::"r"(abort_addr), "r"(1) : "memory");
 }
 
-__device__ __forceinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, const WaitCtl& ctl, unsigned where,
+template <class Ctl>
+__device__ __forceinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, const Ctl& ctl, unsigned where,
                                               bool honour_abort) {
   const long long t0 = clock64();
   while (true) {
@@ -46,18 +51,21 @@ __device__ __forceinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, con
 }
 
 // Wait for the phase of parity `parity` of `bar` to complete.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtl& ctl, unsigned where) {
+template <class Ctl>
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& ctl, unsigned where) {
   if (mbar_try_wait(bar, parity)) return true;
   return wait_bar_slow(bar, parity, ctl, where, true);
 }
 
 // Whole-warp wait with a warp-uniform outcome.
-__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, const WaitCtl& ctl, unsigned where) {
+template <class Ctl>
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, const Ctl& ctl, unsigned where) {
   return __all_sync(0xffffffffu, wait_bar(bar, parity, ctl, where));
 }
 
 // Same, but keeps waiting after another role aborted (used to drain in-flight copies/MMAs).
-__device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
+template <class Ctl>
+__device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, const Ctl& ctl) {
   if (mbar_try_wait(bar, parity)) return true;
   return wait_bar_slow(bar, parity, ctl, kWhereDrain, false);
 }

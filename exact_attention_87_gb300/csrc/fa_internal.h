@@ -10,12 +10,17 @@ namespace fa {
 
 // Bits of the device status word.
 enum : unsigned int {
-  kStatusTimeout = 1u,  // some wait gave up
+  kStatusTimeout = 1u,    // some wait gave up
+  kStatusSmemAlign = 2u,  // a kernel found its dynamic shared memory misaligned and did nothing
 };
 // Where a wait gave up (stored in bits 8-15 of the status word, first writer wins).
 enum : unsigned int {
   kWhereQ = 1, kWhereKEmpty, kWhereVEmpty, kWhereKFull, kWhereVFull, kWhereSFull, kWherePFull,
-  kWhereODone, kWhereDrain, kWhereF32Mma, kWhereTurn
+  kWhereODone, kWhereDrain, kWhereF32Mma, kWhereTurn,
+  // backward kernel
+  kWhereBwdKV, kWhereBwdQFull, kWhereBwdQEmpty, kWhereBwdDoFull, kWhereBwdDoEmpty, kWhereBwdSFull,
+  kWhereBwdDpFull, kWhereBwdPFull, kWhereBwdDsFull, kWhereBwdDsEmpty, kWhereBwdDqFull, kWhereBwdDqEmpty,
+  kWhereBwdDone
 };
 
 // Everything a forward kernel needs; passed by value as a __grid_constant__.
@@ -51,6 +56,29 @@ struct alignas(64) FwdParams {
   unsigned long long* timeline;     // [kTraceCtas, kTraceEvents, kTraceTiles] clock64 stamps
 };
 
+// Everything the backward kernels need; passed by value as a __grid_constant__.
+struct alignas(64) BwdParams {
+  CUtensorMap tm_q;      // [B*H, N, d] 16-bit, boxes of 64 x 128 rows
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  CUtensorMap tm_do;
+  CUtensorMap tm_dk;
+  CUtensorMap tm_dv;
+  CUtensorMap tm_dqacc;  // [B*H, N, d] fp32, boxes of 32 x 128 rows (reduce-add target)
+  const void* o;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  float* dq_acc;         // workspace: fp32 dQ accumulator [B*H, N, d]
+  float* lse2;           // workspace: LSE * log2(e) per row, [B*H, n_pad]; +inf on padding rows
+  float* dsum;           // workspace: D_i = sum_c dO_ic O_ic per row, [B*H, n_pad]; 0 on padding rows
+  unsigned int* status;
+  long long wait_limit;
+  int B, H, N, d;
+  int n_pad;             // N rounded up to the 128-row tile
+  float scale;
+};
+
 // Tile sizes of the fp16/bf16 kernel: Q rows per sub-tile (two sub-tiles per
 // CTA) and keys per K/V tile; the host encodes the TMA boxes with them.
 constexpr int kF16BlockQ = 128, kF16BlockKV = 128;
@@ -66,6 +94,9 @@ enum : int {
 cudaError_t launch_fwd_f16(const FwdParams& p, bool bf16, cudaStream_t stream);
 // Merge split-KV partials into O (dtype of the 16-bit path) and LSE.
 cudaError_t launch_merge(const FwdParams& p, bool bf16, cudaStream_t stream);
+// Backward: row statistics (D, LSE * log2 e) and a zeroed dQ accumulator;
+// the main dK/dV/dQ kernel; the dQ accumulator rounded into dQ.
+cudaError_t launch_bwd_f16(const BwdParams& p, bool bf16, cudaStream_t stream);
 // Launch the fp32 (3 x TF32) forward kernel.
 cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);
 

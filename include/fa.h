@@ -46,7 +46,9 @@ typedef enum {
     FA_ERR_ARCH = 8,           /* the current device is not sm_103                   */
     FA_ERR_SCALE = 9,          /* scale is not finite and > 0                        */
     FA_ERR_WORKSPACE = 10,     /* split-KV workspace NULL, misaligned or too small   */
-    FA_ERR_SCRATCH_LIMIT = 11  /* shape needs more than the built-in scratch         */
+    FA_ERR_SCRATCH_LIMIT = 11, /* shape needs more than the built-in scratch         */
+    FA_ERR_UNSUPPORTED = 12,   /* the entry point does not take this dtype           */
+    FA_ERR_DEVICE_SMEM = 13    /* a kernel found its shared memory misaligned        */
 } fa_status;
 
 /*
@@ -155,10 +157,50 @@ int fa_fwd_splitkv_noalloc(const void *Q, const void *K, const void *V, void *O,
                            int num_splits, void *stream);
 
 /*
+ * Backward pass by recomputation (the MUSA guide's fourth core principle,
+ * "重计算（Recompute）换存储"; the Triton page, sections 2.4 and 4.4: the
+ * forward pass keeps only O and the row statistics, the backward pass rebuilds
+ * P from Q, K and them, then applies the chain rule). For every (b, h), with
+ * s_ij = scale * q_i.k_j, P_ij = exp(s_ij - LSE_i) and D_i = sum_c dO_ic O_ic:
+ *
+ *     dV_j = sum_i P_ij dO_i
+ *     dQ_i = scale * sum_j P_ij (dO_i.v_j - D_i) k_j
+ *     dK_j = scale * sum_i P_ij (dO_i.v_j - D_i) q_i
+ *
+ * the gradients of sum(dO * O) for O = softmax(scale Q K^T) V (non-causal, no
+ * mask). P and dS are never written to memory.
+ *
+ * Q, K, V, O, dO: device pointers to [B, H, N, d] contiguous arrays of
+ *             `dtype`; O and LSE are fa_fwd's outputs for these Q, K, V and
+ *             scale (LSE as fa_fwd writes it, [B, H, N] fp32).
+ * dQ, dK, dV: device pointers to [B, H, N, d] arrays of `dtype` that receive
+ *             the gradients; they must not alias any input.
+ * dtype:      FA_F16 or FA_BF16 (FA_F32: FA_ERR_UNSUPPORTED). Products run on
+ *             the tensor cores with fp32 accumulation; P and dS*scale are
+ *             rounded to `dtype` before they enter a product; dQ is
+ *             accumulated in fp32 and rounded once at the end.
+ * workspace:  device memory owned by the caller, 256-byte aligned, at least
+ *             fa_bwd_workspace_size(B, H, N, d) bytes: the fp32 dQ
+ *             accumulator and two fp32 values per row. Its contents need not
+ *             be initialised; they are overwritten.
+ * Other arguments: as fa_fwd.
+ * Errors: those of fa_fwd (checked before anything is enqueued), plus
+ * FA_ERR_WORKSPACE and FA_ERR_UNSUPPORTED. Three launches are enqueued on
+ * `stream` (row statistics, main pass, dQ rounding); nothing is synchronised.
+ */
+int fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *LSE,
+           void *dQ, void *dK, void *dV, int B, int H, int N, int d, float scale, int dtype,
+           void *workspace, unsigned long long workspace_bytes, void *stream);
+
+/* Workspace bytes fa_bwd needs for this shape (0 for invalid arguments). */
+unsigned long long fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
  * Synchronises `stream`, then returns and clears the status word that kernels
  * of this library on the current device write when they give up on a wait:
- * FA_OK, FA_ERR_DEVICE_TIMEOUT, or FA_ERR_CUDA if the synchronisation or the
- * read failed.
+ * FA_OK, FA_ERR_DEVICE_TIMEOUT, FA_ERR_DEVICE_SMEM (a kernel found its shared
+ * memory misaligned and did no work), or FA_ERR_CUDA if the synchronisation or
+ * the read failed.
  */
 int fa_get_device_status(void *stream);
 

@@ -64,6 +64,9 @@ def _bind(path: str):
     lib.oracle_attn_masked_fp64.restype = I
     lib.oracle_attn_bwd_fp64.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, L, L, L, D, I]
     lib.oracle_attn_bwd_fp64.restype = I
+    lp = ctypes.POINTER(ctypes.c_long)
+    lib.oracle_bwd_rows_fp64.argtypes = [dp, dp, dp, dp, dp, dp, L, L, L, D, lp, L, dp, lp, L, dp, dp]
+    lib.oracle_bwd_rows_fp64.restype = I
     lib.oracle_merge_fp64.argtypes = [dp, dp, L, L, L, dp, dp]
     lib.oracle_merge_fp64.restype = I
     lib.oracle_mutant_id.restype = I
@@ -192,6 +195,31 @@ def attn_bwd(q, k, v, o, do, lse, scale: float | None = None, nthreads: int | No
                                   _ptr(dv), BH, N, d, scale, nthreads or default_threads())
     if rc != 0:
         raise RuntimeError(f"oracle_attn_bwd_fp64 failed ({rc})")
+    return dq, dk, dv
+
+
+def attn_bwd_rows(q, k, v, o, do, lse, dq_rows, dkv_rows, scale: float | None = None, lib=None):
+    """Selected rows of the backward pass: dQ at (b, h, i) in ``dq_rows`` and
+    dK, dV at (b, h, j) in ``dkv_rows``; o and lse must be the forward results
+    for every row of the heads named. Returns (dq [n_dq, d], dk, dv [n_dkv, d])."""
+    q, k, v, o, do, lse = (_f64(t) for t in (q, k, v, o, do, lse))
+    B, H, N, d = q.shape
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+
+    def pairs(rows):
+        a = np.array([[b * H + h, i] for b, h, i in rows], dtype=np.int64).reshape(-1, 2)
+        return np.ascontiguousarray(a, dtype=ctypes.c_long)
+
+    a_q, a_kv = pairs(dq_rows), pairs(dkv_rows)
+    dq = np.empty((len(a_q), d))
+    dk, dv = np.empty((len(a_kv), d)), np.empty((len(a_kv), d))
+    lp = ctypes.POINTER(ctypes.c_long)
+    lib = lib or load()
+    rc = lib.oracle_bwd_rows_fp64(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), B * H, N, d, scale,
+                                  a_q.ctypes.data_as(lp), len(a_q), _ptr(dq), a_kv.ctypes.data_as(lp), len(a_kv),
+                                  _ptr(dk), _ptr(dv))
+    if rc != 0:
+        raise RuntimeError(f"oracle_bwd_rows_fp64 failed ({rc})")
     return dq, dk, dv
 
 

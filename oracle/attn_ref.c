@@ -458,6 +458,63 @@ int oracle_attn_bwd_fp64(const double *Q, const double *K, const double *V, cons
 }
 
 /*
+ * Single rows of the backward pass, same definitions and summation orders as
+ * oracle_attn_bwd_fp64: dQ rows given as (bh, i) pairs, dK/dV rows as (bh, j)
+ * pairs. Each row costs O(N d); O and LSE must cover every row of the heads
+ * named. Outputs are [n, d].
+ */
+int oracle_bwd_rows_fp64(const double *Q, const double *K, const double *V, const double *O, const double *dO,
+                         const double *LSE, long BH, long N, long d, double scale, const long *dq_rows, long n_dq,
+                         double *dQ, const long *dkv_rows, long n_dkv, double *dK, double *dV)
+{
+    if (N < 1 || d < 1) return -1;
+    for (long r = 0; r < n_dq; ++r) {
+        long bh = dq_rows[2 * r], i = dq_rows[2 * r + 1];
+        if (bh < 0 || bh >= BH || i < 0 || i >= N) return -1;
+        const double *q = Q + (bh * N + i) * d, *o = O + (bh * N + i) * d, *g = dO + (bh * N + i) * d;
+        double Di = 0.0;
+        for (long c = 0; c < d; ++c) Di += g[c] * o[c];
+        double *out = dQ + r * d;
+        for (long c = 0; c < d; ++c) out[c] = 0.0;
+        for (long j = 0; j < N; ++j) {
+            const double *kj = K + (bh * N + j) * d, *vj = V + (bh * N + j) * d;
+            double sc = 0.0, dp = 0.0;
+            for (long c = 0; c < d; ++c) {
+                sc += q[c] * kj[c];
+                dp += g[c] * vj[c];
+            }
+            double ds = exp(scale * sc - LSE[bh * N + i]) * (dp - Di);
+            for (long c = 0; c < d; ++c) out[c] += ds * kj[c];
+        }
+        for (long c = 0; c < d; ++c) out[c] *= scale;
+    }
+    for (long r = 0; r < n_dkv; ++r) {
+        long bh = dkv_rows[2 * r], j = dkv_rows[2 * r + 1];
+        if (bh < 0 || bh >= BH || j < 0 || j >= N) return -1;
+        const double *kj = K + (bh * N + j) * d, *vj = V + (bh * N + j) * d;
+        double *ok = dK + r * d, *ov = dV + r * d;
+        for (long c = 0; c < d; ++c) ok[c] = ov[c] = 0.0;
+        for (long i = 0; i < N; ++i) {
+            const double *q = Q + (bh * N + i) * d, *o = O + (bh * N + i) * d, *g = dO + (bh * N + i) * d;
+            double Di = 0.0, sc = 0.0, dp = 0.0;
+            for (long c = 0; c < d; ++c) {
+                Di += g[c] * o[c];
+                sc += q[c] * kj[c];
+                dp += g[c] * vj[c];
+            }
+            double pij = exp(scale * sc - LSE[bh * N + i]);
+            double ds = pij * (dp - Di);
+            for (long c = 0; c < d; ++c) {
+                ov[c] += pij * g[c];
+                ok[c] += ds * q[c];
+            }
+        }
+        for (long c = 0; c < d; ++c) ok[c] *= scale;
+    }
+    return 0;
+}
+
+/*
  * Merge of attention results computed over disjoint key ranges (the block
  * merge of the Triton page, section 2.3): parts are folded in order with the
  * running triple (m, l, O): for a part with statistics (m_b, l_b) and its

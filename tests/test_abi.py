@@ -57,7 +57,7 @@ def test_every_header_is_covered():
 
 def test_strerror_and_version(L):
     assert fa.fa_abi_version() >= 100
-    for code in range(0, 12):
+    for code in range(0, 14):
         assert fa.fa_strerror(code) and fa.fa_strerror(code) != "unknown status"
     assert fa.fa_strerror(12345) == "unknown status"
 
@@ -106,3 +106,39 @@ def test_splitkv_workspace_size_formula(L):
 def test_masked_entry_point_argument_errors(L):
     assert fa.fa_fwd_ex(A, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, 2, None, None) == fa.FA_ERR_SHAPE
     assert fa.fa_fwd_ex(0, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, 1, None, None) == fa.FA_ERR_NULL
+
+
+def test_backward_workspace_size_formula(L):
+    def part(n):
+        return (n + 255) // 256 * 256
+    # fp32 dQ accumulator, then two fp32 values per row of the 128-row padded layout
+    assert fa.fa_bwd_workspace_size(2, 3, 300, 64) == part(6 * 300 * 64 * 4) + 2 * part(6 * 384 * 4)
+    assert fa.fa_bwd_workspace_size(8, 32, 4096, 128) == part(256 * 4096 * 128 * 4) + 2 * part(256 * 4096 * 4)
+    assert fa.fa_bwd_workspace_size(1, 1, 1, 96) == 0
+    assert fa.fa_bwd_workspace_size(0, 1, 64, 64) == 0
+
+
+W = 1 << 24  # fake workspace address, 256-byte aligned
+
+
+@pytest.mark.parametrize("change,code", [
+    ({"Q": 0}, fa.FA_ERR_NULL),
+    ({"dO": 0}, fa.FA_ERR_NULL),
+    ({"dV": 0}, fa.FA_ERR_NULL),
+    ({"dtype": 9}, fa.FA_ERR_DTYPE),
+    ({"dtype": fa.FA_F32}, fa.FA_ERR_UNSUPPORTED),
+    ({"N": 0}, fa.FA_ERR_SHAPE),
+    ({"d": 256}, fa.FA_ERR_HEADDIM),
+    ({"scale": float("inf")}, fa.FA_ERR_SCALE),
+    ({"dK": A + 8}, fa.FA_ERR_ALIGN),
+    ({"LSE": A + 2}, fa.FA_ERR_ALIGN),
+    ({"ws": 0}, fa.FA_ERR_WORKSPACE),
+    ({"ws": W + 64}, fa.FA_ERR_WORKSPACE),
+    ({"ws_bytes": 1024}, fa.FA_ERR_WORKSPACE),
+])
+def test_backward_argument_errors_return_before_launch(L, change, code):
+    a = dict(Q=A, K=A, V=A, O=A, dO=A, LSE=A, dQ=A, dK=A, dV=A, B=1, H=2, N=200, d=64, scale=0.125,
+             dtype=fa.FA_BF16, ws=W, ws_bytes=1 << 30)
+    a.update(change)
+    assert fa.fa_bwd(a["Q"], a["K"], a["V"], a["O"], a["dO"], a["LSE"], a["dQ"], a["dK"], a["dV"], a["B"], a["H"],
+                     a["N"], a["d"], a["scale"], a["dtype"], a["ws"], a["ws_bytes"], None) == code

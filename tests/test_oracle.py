@@ -194,3 +194,19 @@ def test_fully_masked_rows_are_guarded():
     assert np.all(o[0] == 0) and np.all(np.isneginf(lse[0]))
     assert np.all(np.isfinite(o[1])) and np.all(np.isfinite(lse[1]))
 
+
+
+def test_backward_rows_match_full_backward(oracle_lib):
+    """The sampled-row backward (used at full sizes) against the full backward."""
+    rng = np.random.default_rng(21)
+    B, H, N, d, scale = 2, 2, 37, 8, 0.4
+    q, k, v, w = (rng.standard_normal((B, H, N, d)) * 1.3 for _ in range(4))
+    o, lse = oracle.attn(q, k, v, scale=scale)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, o, w, lse, scale=scale)
+    rows = [(0, 0, 0), (1, 1, 36), (0, 1, 17), (1, 0, 5)]
+    rq, rk, rv = oracle.attn_bwd_rows(q, k, v, o, w, lse, rows, rows[::-1], scale=scale)
+    for n, (b, h, i) in enumerate(rows):
+        np.testing.assert_allclose(rq[n], dq[b, h, i], rtol=0, atol=1e-14)
+    for n, (b, h, j) in enumerate(rows[::-1]):
+        np.testing.assert_allclose(rk[n], dk[b, h, j], rtol=0, atol=1e-14)
+        np.testing.assert_allclose(rv[n], dv[b, h, j], rtol=0, atol=1e-14)

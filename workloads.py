@@ -7,7 +7,8 @@ any computation.
 
 Recipe (the same bytes go to both sides):
   * one numpy PCG64 stream per tensor: ``default_rng([seed, workload_id, t])``
-    with t = 0, 1, 2 for Q, K, V;
+    with t = 0, 1, 2 for Q, K, V and t = 3 for the output gradient dO of the
+    backward pass;
   * ``standard_normal`` drawn in float32, multiplied by the tensor's sigma;
   * rounded once to the workload dtype with round-to-nearest-even
     (numpy ``astype`` for fp16, torch CPU ``.to(torch.bfloat16)`` for bf16).
@@ -97,6 +98,11 @@ def make_qkv(B, H, N, d, dtype, sigma_qk=1.0, sigma_v=1.0, seed=0, wid=0, Nk=Non
     k = draw((B, H, Nk, d), dtype, sigma_qk, seed, wid, 1)
     v = draw((B, H, Nk, d), dtype, sigma_v, seed, wid, 2)
     return q, k, v
+
+
+def make_dout(B, H, N, d, dtype, seed=0, wid=0, sigma=1.0):
+    """The output gradient dO [B,H,N,d] for the backward pass (stream t = 3)."""
+    return draw((B, H, N, d), dtype, sigma, seed, wid, 3)
 
 
 def make_inputs(w: Workload | str, seed: int = 0):
