@@ -339,24 +339,18 @@ unsigned long long fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int
   return workspace_bytes_for(B, H, N, d, static_cast<int>((tiles + per - 1) / per));
 }
 
+}  // extern "C"
+
 namespace {
 
 // fa_bwd workspace: fp32 dQ accumulator [B*H, N, d], then LSE*log2(e) and D
 // per row of the 128-row padded layout [B*H, n_pad], each part 256-byte aligned.
 unsigned long long bwd_part_bytes(unsigned long long n) { return (n + 255) & ~255ull; }
 
-}  // namespace
-
-unsigned long long fa_bwd_workspace_size(int B, int H, int N, int d) {
-  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
-  const unsigned long long bh = static_cast<unsigned long long>(B) * H;
-  const unsigned long long n_pad = static_cast<unsigned long long>(kv_tiles(N)) * fa::kF16BlockKV;
-  return bwd_part_bytes(bh * N * d * 4) + 2 * bwd_part_bytes(bh * n_pad * 4);
-}
-
-int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE, void* dQ,
-           void* dK, void* dV, int B, int H, int N, int d, float scale, int dtype, void* workspace,
-           unsigned long long workspace_bytes, void* stream) {
+int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE, void* dQ,
+             void* dK, void* dV, int B, int H, int N, int d, float scale, int dtype, void* workspace,
+             unsigned long long workspace_bytes, void* stream, int inject, unsigned long long* timeline,
+             long long wait_limit) {
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return FA_ERR_NULL;
   if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
   if (dtype == FA_F32) return FA_ERR_UNSUPPORTED;
@@ -389,7 +383,9 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const voi
   p.scale = scale;
   p.n_pad = static_cast<int>(kv_tiles(N) * fa::kF16BlockKV);
   p.status = dev.status;
-  p.wait_limit = wait_limit_cycles();
+  p.wait_limit = wait_limit > 0 ? wait_limit : wait_limit_cycles();
+  p.inject = inject;
+  p.timeline = timeline;
   const unsigned long long acc_bytes = bwd_part_bytes(static_cast<unsigned long long>(BH) * N * d * 4);
   const unsigned long long row_bytes = bwd_part_bytes(static_cast<unsigned long long>(BH) * p.n_pad * 4);
   p.dq_acc = static_cast<float*>(workspace);
@@ -409,6 +405,34 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const voi
   const cudaError_t e = fa::launch_bwd_f16(p, dtype == FA_BF16, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
+
+}  // namespace
+
+extern "C" {
+
+unsigned long long fa_bwd_workspace_size(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  const unsigned long long bh = static_cast<unsigned long long>(B) * H;
+  const unsigned long long n_pad = static_cast<unsigned long long>(kv_tiles(N)) * fa::kF16BlockKV;
+  return bwd_part_bytes(bh * N * d * 4) + 2 * bwd_part_bytes(bh * n_pad * 4);
+}
+
+int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE, void* dQ,
+           void* dK, void* dV, int B, int H, int N, int d, float scale, int dtype, void* workspace,
+           unsigned long long workspace_bytes, void* stream) {
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype, workspace, workspace_bytes, stream, 0,
+                  nullptr, 0);
+}
+
+#ifdef FA_TESTING
+int fa_bwd_testing(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                   void* dQ, void* dK, void* dV, int B, int H, int N, int d, float scale, int dtype, void* workspace,
+                   unsigned long long workspace_bytes, void* stream, int inject, unsigned long long* timeline,
+                   long long wait_limit_cycles) {
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype, workspace, workspace_bytes, stream,
+                  inject, timeline, wait_limit_cycles);
+}
+#endif
 
 #ifdef FA_TESTING
 int fa_fwd_testing(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,

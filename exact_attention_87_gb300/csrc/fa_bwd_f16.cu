@@ -21,11 +21,11 @@
 //                accumulator with TMA reduce-add
 //   fa_bwd_post  dQ = accumulator rounded to the input type
 //
-// fa_bwd_main on GB300 (12 warps; TMEM lanes are keys for S^T, dP^T, dV, dK
+// fa_bwd_main on GB300 (16 warps; TMEM lanes are keys for S^T, dP^T, dV, dK
 // and queries for dQ):
-//   warp 8      TMA producer: K_j, V_j once; Q_i (+ its LSE and D rows) into a
+//   warp 12     TMA producer: K_j, V_j once; Q_i (+ its LSE and D rows) into a
 //               2-stage ring; dO_i into a 1-stage (d=128) / 2-stage (d=64) ring
-//   warp 9      MMA warp (one elected lane issues), per Q tile i:
+//   warp 13     MMA warp (one elected lane issues), per Q tile i:
 //                 S^T  = K_j Q_i^T   (SS)           -> TMEM [0,128)
 //                 dP^T = V_j dO_i^T  (SS)           -> TMEM [128,256)
 //                 dV  += P^T dO_i    (TS: P^T from TMEM, dO MN-major)
@@ -38,11 +38,16 @@
 //               written back as 16-bit pairs over S^T columns [0,32) / [64,96)
 //               for the dV product and kept as fp32 P*scale in registers;
 //               dS^T*scale = P*scale (dP^T - D) rounded to 16 bits into their
-//               half of the dS^T tile in SMEM. Then (one thread per query)
-//               columns [0,d/2) / [d/2,d) of dQ_i: TMEM -> registers -> 32-column
-//               fp32 boxes in SMEM (their dS^T half, free once dQ_i is done,
-//               and one more box) -> TMA reduce-add
-//   end         warps 0-3 store dV_j, warps 4-7 store dK_j (TMA, 16-bit)
+//               half of the dS^T tile in SMEM; at the end dV_j / dK_j
+//   warps 8-11  dQ (one thread per query): all d columns of dQ_i from TMEM
+//               into registers (which frees the columns at once), then
+//               32-column fp32 boxes through two SMEM buffers into TMA
+//               reduce-adds on the accumulator. The reduce-adds (64 KB per Q
+//               tile for d=128) drain at the SM's write rate to L2, so they
+//               run beside the other roles instead of in their chain.
+//   warps 14-15 idle (they complete the fourth warpgroup)
+// Registers: launched at 128 per thread; warpgroups 0-2 grow to 160 / 160 /
+// 152 and warpgroup 3 shrinks to 40 (setmaxnreg).
 // TMEM (512 columns): S^T [0,128), dP^T [128,256), dV [256,256+d),
 // dK [256+d,256+2d); dQ_i reuses the dP^T columns for d=128 (dP^T_i is
 // consumed once dS_i is written; dP^T_{i+1} waits for the read-out of dQ_i)
@@ -72,13 +77,13 @@ struct BCfg {
   static constexpr uint32_t HALF = 128 * ROW;       // one 64-column half of a tile
   static constexpr uint32_t DS_BYTES = 128 * 128 * 2;
   static constexpr uint32_t BOX = 128 * 128;        // one fp32 dQ box: 128 rows x 32 columns
-  static constexpr int WG_BOXES = D / 64;           // dQ boxes per softmax warpgroup and Q tile
+  static constexpr int NBOX = D / 32;               // dQ boxes per Q tile
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + TILE;
   static constexpr uint32_t OFF_Q = OFF_V + TILE;
   static constexpr uint32_t OFF_DO = OFF_Q + QST * TILE;
   static constexpr uint32_t OFF_DS = OFF_DO + OST * TILE;
-  static constexpr uint32_t OFF_DQS = OFF_DS + DS_BYTES;   // one extra dQ box per warpgroup
+  static constexpr uint32_t OFF_DQS = OFF_DS + DS_BYTES;   // two dQ staging boxes
   static constexpr uint32_t OFF_ROWS = OFF_DQS + 2 * BOX;  // [QST] x {lse2[128], dsum[128]} fp32
   static constexpr uint32_t ROWS_BYTES = 2 * 128 * 4;
   static constexpr uint32_t OFF_BAR = OFF_ROWS + QST * ROWS_BYTES;
@@ -94,10 +99,12 @@ struct BCfg {
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
   static constexpr uint32_t T_DQ = (D == 128) ? 128 : 384;
-  static constexpr int THREADS = 384;
-  static constexpr int WARP_TMA = 8, WARP_MMA = 9;
+  static constexpr int THREADS = 512;
+  static constexpr int WARP_TMA = 12, WARP_MMA = 13;
+  static constexpr int LAUNCH_REGS = 128, SM_REGS = 160, DQ_REGS = 152, LOW_REGS = 40;
+  static_assert(128 * (2 * SM_REGS + DQ_REGS + LOW_REGS) <= THREADS * LAUNCH_REGS, "register split exceeds the pool");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(OFF_DS % 1024 == 0 && OFF_DQS % 1024 == 0 && OFF_Q % 1024 == 0, "swizzled buffers need 1 KB alignment");
+  static_assert(OFF_DS % 1024 == 0 && OFF_DO % 1024 == 0 && OFF_Q % 1024 == 0, "swizzled buffers need 1 KB alignment");
 };
 
 using BCtl = WaitCtlT<BwdParams>;
@@ -141,6 +148,9 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint32_t base, 
     bulk_load(rows, p.lse2 + row_base + static_cast<size_t>(i) * C::BQ, 512, qf);
     bulk_load(rows + 512, p.dsum + row_base + static_cast<size_t>(i) * C::BQ, 512, qf);
     nqi = i + 1;
+#ifdef FA_TESTING
+    if (p.inject == 1 && i == 0) continue;  // fault injection: dO_0 is never loaded
+#endif
     const int os = i % C::OST;
     if (!wait_bar(bbar<D>(base, C::B_OE + os), ((i / C::OST) & 1) ^ 1, ctl, kWhereBwdDoEmpty)) { ok = false; break; }
     const uint32_t of = bbar<D>(base, C::B_OF + os);
@@ -156,8 +166,12 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint32_t base, 
     wait_bar_drain(bv, 0, ctl);
     for (int t = nqi > C::QST ? nqi - C::QST : 0; t < nqi; ++t)
       wait_bar_drain(bbar<D>(base, C::B_QF + t % C::QST), (t / C::QST) & 1, ctl);
-    for (int t = noi > C::OST ? noi - C::OST : 0; t < noi; ++t)
+    for (int t = noi > C::OST ? noi - C::OST : 0; t < noi; ++t) {
+#ifdef FA_TESTING
+      if (p.inject == 1 && t == 0) continue;  // never armed
+#endif
       wait_bar_drain(bbar<D>(base, C::B_OF + t % C::OST), (t / C::OST) & 1, ctl);
+    }
   }
 }
 
@@ -169,7 +183,7 @@ template <int D>
 __device__ __forceinline__ void mma_kmajor_tiles(uint32_t d_tmem, uint32_t a_base, uint32_t b_base, uint32_t idesc) {
   const uint64_t a0 = smem_desc_sw128(a_base, 16, 1024);
   const uint64_t b0 = smem_desc_sw128(b_base, 16, 1024);
-#pragma unroll
+#pragma unroll 1  // issue-bound anyway; keeps the descriptors out of registers
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = ((kk / 4) * BCfg<D>::HALF + (kk & 3) * 32u) >> 4;
     mma_f16_ss_elect(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
@@ -215,11 +229,12 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, uint32_t base, uint3
     tc_fence_after();
     {
       const uint64_t b0 = smem_desc_sw128(base + C::OFF_DO + os * C::TILE, lbo_d, 1024);
-#pragma unroll
+#pragma unroll 1  // issue-bound anyway; keeps the descriptors out of registers
       for (int kk = 0; kk < C::BQ / 16; ++kk)
         mma_f16_ts_elect(tmem + C::T_DV, tmem + C::T_S + (kk < 4 ? 8 * kk : 64 + 8 * (kk - 4)),
                          b0 + ((kk * 2048u) >> 4), idesc_acc, (i > 0 || kk > 0) ? 1u : 0u);
     }
+    if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDV, i);
     // dP^T_i (tile 0's was issued up front)
     if (i > 0) {
       if constexpr (D == 128) {
@@ -229,6 +244,7 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, uint32_t base, uint3
       tc_fence_after();
       mma_kmajor_tiles<D>(tmem + C::T_DP, base + C::OFF_V, base + C::OFF_DO + os * C::TILE, idesc_st);
       tc_commit_elect(b_dpf);
+      if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDP, i);
     }
     tc_commit_elect(bbar<D>(base, C::B_OE + os));  // dO_i is free once dV_i and dP^T_i are done
     // S^T_{i+1}: overwrites P^T_i, which dV_i (issued before) reads.
@@ -242,13 +258,14 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, uint32_t base, uint3
       tc_fence_after();
       mma_kmajor_tiles<D>(tmem + C::T_S, base + C::OFF_K, base + C::OFF_Q + qn * C::TILE, idesc_st);
       tc_commit_elect(b_sf);
+      if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvS, i);
     }
     // dK += dS^T Q_i and dQ_i = dS K_j, both from the dS^T tile in SMEM.
     if (!wait_bar_warp(b_dsf, i & 1, ctl, kWhereBwdDsFull)) goto drain;
     tc_fence_after();
     {
       const uint64_t b0 = smem_desc_sw128(base + C::OFF_Q + qs * C::TILE, lbo_d, 1024);
-#pragma unroll
+#pragma unroll 1  // issue-bound anyway; keeps the descriptors out of registers
       for (int kk = 0; kk < C::BQ / 16; ++kk) {
         const uint32_t aoff = ((kk / 4) * C::HALF + (kk & 3) * 32u) >> 4;
         mma_f16_ss_elect(tmem + C::T_DK, dk_a0 + aoff, b0 + ((kk * 2048u) >> 4), idesc_acc,
@@ -256,16 +273,18 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, uint32_t base, uint3
       }
     }
     tc_commit_elect(bbar<D>(base, C::B_QE + qs));  // Q_i (and its rows) are free once dK_i is done
+    if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDK, i);
     if constexpr (D == 64) {
       // dQ_{i-1} must have left its TMEM columns.
       if (i > 0 && !wait_bar_warp(b_dqe, (i - 1) & 1, ctl, kWhereBwdDqEmpty)) goto drain;
       tc_fence_after();
     }
-#pragma unroll
+#pragma unroll 1  // issue-bound anyway; keeps the descriptors out of registers
     for (int kk = 0; kk < C::BK / 16; ++kk)
       mma_f16_ss_elect(tmem + C::T_DQ, dq_a0 + ((kk * 2048u) >> 4), dq_b0 + ((kk * 2048u) >> 4), idesc_dq,
                        kk > 0 ? 1u : 0u);
     tc_commit_elect(b_dqf);
+    if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDQ, i);
   }
 drain:
   // One commit after the last MMA: the epilogues wait for it, and every MMA
@@ -311,154 +330,116 @@ __device__ __forceinline__ void store_acc_tile(uint32_t t_acc, uint32_t stage, i
 
 // --------------------------------------------------------------------------
 // Softmax warpgroup W (warps 4W .. 4W+3): queries [64W, 64W+64) of P^T and
-// dS^T, columns [W*D/2, (W+1)*D/2) of dQ; at the end dV (W = 0) or dK (W = 1)
+// dS^T; at the end dV (W = 0) or dK (W = 1)
 // --------------------------------------------------------------------------
 template <int D, bool BF16, int W>
 __device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint32_t base, uint32_t tmem, int bh, int kv0, int nq,
                                             const BCtl& ctl) {
   using C = BCfg<D>;
   constexpr int BAR = 1 + W;  // this warpgroup's named barrier
-  const int t = threadIdx.x - 128 * W;  // key row (P, dS) / query row (dQ) = TMEM lane
+  const int t = threadIdx.x - 128 * W;  // key row = TMEM lane
   const int lane = t & 31;
   const uint32_t lane_base = static_cast<uint32_t>(t & ~31) << 16;
   const uint32_t t_s = tmem + lane_base + C::T_S + 64 * W, t_dp = tmem + lane_base + C::T_DP + 64 * W;
-  const uint32_t t_dq = tmem + lane_base + C::T_DQ + W * (D / 2);
   const float c = p.scale * kLog2eB;
   const bool key_ok = kv0 + t < p.N;  // keys past N (zero-filled rows) get P = 0
   const float2 c2 = make_float2(c, c);
   const float2 sc2 = make_float2(p.scale, p.scale);
   const uint32_t b_sf = bbar<D>(base, C::B_SF), b_dpf = bbar<D>(base, C::B_DPF);
   const uint32_t b_pf = bbar<D>(base, C::B_PF), b_dsf = bbar<D>(base, C::B_DSF);
-  const uint32_t b_dqf = bbar<D>(base, C::B_DQF), b_dqe = bbar<D>(base, C::B_DQE);
+  const uint32_t b_dqf = bbar<D>(base, C::B_DQF);
   const uint32_t ds_half = base + C::OFF_DS + W * C::HALF;  // this warpgroup's half of dS^T
-  const uint32_t dq_extra = base + C::OFF_DQS + W * C::BOX;
   bool ok = true;
   float ps[64];  // P*scale of this thread's key for queries [64W, 64W+64) of the current tile
 
-  // Every wait below is agreed by the whole warpgroup (bar.red.and), so that
-  // all 128 threads reach the named barriers in the same order, or leave together.
-  for (int i = 0; i <= nq; ++i) {
+  // Every wait is agreed by the whole warpgroup (bar.red.and): its epilogue
+  // needs all 128 threads at the same named barriers.
+  for (int i = 0; i < nq; ++i) {
     const uint32_t rows = base + C::OFF_ROWS + (i % C::QST) * C::ROWS_BYTES;  // lse2[128], dsum[128]
-    if (i < nq) {
-      // ---- P_i: S^T columns -> fp32 P (kept, times scale) and 16-bit P^T in TMEM
-      if (!named_bar_and(BAR, 128, wait_bar(b_sf, i & 1, ctl, kWhereBwdSFull))) { ok = false; break; }
-      tc_fence_after();
+    // ---- P_i: S^T columns -> fp32 P (kept, times scale) and 16-bit P^T in TMEM
+    if (!named_bar_and(BAR, 128, wait_bar(b_sf, i & 1, ctl, kWhereBwdSFull))) { ok = false; break; }
+    if (W == 0 && t == 0) FA_TRACE(p, kBvSmS, i);
+    tc_fence_after();
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint32_t r[32];
-        tmem_ld32(t_s + 32 * q, r);
-        tmem_ld_wait();
-        reg_fence(r);
-        uint32_t pk[16];
+    for (int q = 0; q < 2; ++q) {
+      uint32_t r[32];
+      tmem_ld32(t_s + 32 * q, r);
+      tmem_ld_wait();
+      reg_fence(r);
+      uint32_t pk[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          float4 l4;
-          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                       : "=f"(l4.x), "=f"(l4.y), "=f"(l4.z), "=f"(l4.w)
-                       : "r"(rows + (64 * W + 32 * q + 4 * u) * 4));
-          const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1])), c2,
-                                       make_float2(-l4.x, -l4.y));
-          const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])),
-                                       c2, make_float2(-l4.z, -l4.w));
-          float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
-          float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
-          if (!key_ok) p0 = p1 = make_float2(0.f, 0.f);
-          pk[2 * u] = pack2<BF16>(p0.x, p0.y);
-          pk[2 * u + 1] = pack2<BF16>(p1.x, p1.y);
-          const float2 s0 = __fmul2_rn(p0, sc2), s1 = __fmul2_rn(p1, sc2);
-          ps[32 * q + 4 * u] = s0.x;
-          ps[32 * q + 4 * u + 1] = s0.y;
-          ps[32 * q + 4 * u + 2] = s1.x;
-          ps[32 * q + 4 * u + 3] = s1.y;
-        }
-        // Queries [32q, 32q+32) of this half -> packed columns [16q, 16q+16), already read.
-        tmem_st16(t_s + 16 * q, pk);
+      for (int u = 0; u < 8; ++u) {
+        float4 l4;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(l4.x), "=f"(l4.y), "=f"(l4.z), "=f"(l4.w)
+                     : "r"(rows + (64 * W + 32 * q + 4 * u) * 4));
+        const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1])), c2,
+                                     make_float2(-l4.x, -l4.y));
+        const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])),
+                                     c2, make_float2(-l4.z, -l4.w));
+        float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+        float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+        if (!key_ok) p0 = p1 = make_float2(0.f, 0.f);
+        pk[2 * u] = pack2<BF16>(p0.x, p0.y);
+        pk[2 * u + 1] = pack2<BF16>(p1.x, p1.y);
+        const float2 s0 = __fmul2_rn(p0, sc2), s1 = __fmul2_rn(p1, sc2);
+        ps[32 * q + 4 * u] = s0.x;
+        ps[32 * q + 4 * u + 1] = s0.y;
+        ps[32 * q + 4 * u + 2] = s1.x;
+        ps[32 * q + 4 * u + 3] = s1.y;
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_pf);
+      // Queries [32q, 32q+32) of this half -> packed columns [16q, 16q+16), already read.
+      tmem_st16(t_s + 16 * q, pk);
     }
-    if (i > 0) {
-      // ---- dQ_{i-1}: TMEM -> fp32 boxes in SMEM -> TMA reduce-add into the accumulator
-      if (!named_bar_and(BAR, 128, wait_bar(b_dqf, (i - 1) & 1, ctl, kWhereBwdDqFull))) { ok = false; break; }
-      tc_fence_after();
-      // The dS^T half is free: dK_{i-1} and dQ_{i-1}, its last readers, are complete.
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(b_pf);
+    if (t == 0) FA_TRACE(p, W == 0 ? kBvSmP : kBvW1P, i);
+
+    // ---- dS_i: dS^T * scale = P*scale (dP^T - D), 16-bit, into row t of this warpgroup's dS^T half
+    if (!named_bar_and(BAR, 128, wait_bar(b_dpf, i & 1, ctl, kWhereBwdDpFull))) { ok = false; break; }
+    if (W == 0 && t == 0) FA_TRACE(p, kBvSmDp, i);
+    // dS^T_{i-1} is read by dK_{i-1} and dQ_{i-1}; dQ_{i-1} completing covers both
+    // (it is issued before dV_i and dP^T_i, so this wait is normally already over).
+    if (i > 0 && !named_bar_and(BAR, 128, wait_bar(b_dqf, (i - 1) & 1, ctl, kWhereBwdDqFull))) { ok = false; break; }
+    tc_fence_after();
 #pragma unroll
-      for (int b = 0; b < C::WG_BOXES; ++b) {
-        uint32_t r[32];
-        tmem_ld32(t_dq + 32 * b, r);
-        tmem_ld_wait();
-        reg_fence(r);
-        if (b == C::WG_BOXES - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(b_dqe);  // the MMA warp may reuse these TMEM columns
-        }
-        const uint32_t buf = b == 0 ? ds_half : dq_extra;
+    for (int q = 0; q < 2; ++q) {
+      uint32_t r[32];
+      tmem_ld32(t_dp + 32 * q, r);
+      tmem_ld_wait();
+      reg_fence(r);
+      uint32_t pk[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint32_t phys = static_cast<uint32_t>(u) ^ (static_cast<uint32_t>(t) & 7u);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + t * 128u + phys * 16), "r"(r[4 * u]),
-                       "r"(r[4 * u + 1]), "r"(r[4 * u + 2]), "r"(r[4 * u + 3])
-                       : "memory");
-        }
+      for (int u = 0; u < 8; ++u) {
+        float4 d4;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(d4.x), "=f"(d4.y), "=f"(d4.z), "=f"(d4.w)
+                     : "r"(rows + 512 + (64 * W + 32 * q + 4 * u) * 4));
+        const float2 e0 = __fadd2_rn(make_float2(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1])),
+                                     make_float2(-d4.x, -d4.y));
+        const float2 e1 = __fadd2_rn(make_float2(__uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])),
+                                     make_float2(-d4.z, -d4.w));
+        const float2 g0 = __fmul2_rn(e0, make_float2(ps[32 * q + 4 * u], ps[32 * q + 4 * u + 1]));
+        const float2 g1 = __fmul2_rn(e1, make_float2(ps[32 * q + 4 * u + 2], ps[32 * q + 4 * u + 3]));
+        pk[2 * u] = pack2<BF16>(g0.x, g0.y);
+        pk[2 * u + 1] = pack2<BF16>(g1.x, g1.y);
       }
-      fence_proxy_async_smem();
-      named_bar_sync(BAR, 128);
-      if (t == 0) {
 #pragma unroll
-        for (int b = 0; b < C::WG_BOXES; ++b)
-          tma_reduce_add_3d(&p.tm_dqacc, b == 0 ? ds_half : dq_extra, W * (D / 2) + 32 * b, (i - 1) * C::BQ, bh);
-        tma_store_commit();
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t phys = (4 * q + u) ^ (static_cast<uint32_t>(t) & 7u);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ds_half + t * C::ROW + phys * 16),
+                     "r"(pk[4 * u]), "r"(pk[4 * u + 1]), "r"(pk[4 * u + 2]), "r"(pk[4 * u + 3])
+                     : "memory");
       }
     }
-    if (i < nq) {
-      // ---- dS_i: dS^T * scale = P*scale (dP^T - D), 16-bit, into row t of this warpgroup's dS^T half
-      if (!named_bar_and(BAR, 128, wait_bar(b_dpf, i & 1, ctl, kWhereBwdDpFull))) { ok = false; break; }
-      if (i > 0) {
-        // The reduce-adds of dQ_{i-1} read the dS^T half: wait until they have.
-        if (t == 0) bulk_wait_read<0>();
-        named_bar_sync(BAR, 128);
-      }
-      tc_fence_after();
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint32_t r[32];
-        tmem_ld32(t_dp + 32 * q, r);
-        tmem_ld_wait();
-        reg_fence(r);
-        uint32_t pk[16];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          float4 d4;
-          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                       : "=f"(d4.x), "=f"(d4.y), "=f"(d4.z), "=f"(d4.w)
-                       : "r"(rows + 512 + (64 * W + 32 * q + 4 * u) * 4));
-          const float2 e0 = __fadd2_rn(make_float2(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1])),
-                                       make_float2(-d4.x, -d4.y));
-          const float2 e1 = __fadd2_rn(make_float2(__uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])),
-                                       make_float2(-d4.z, -d4.w));
-          const float2 g0 = __fmul2_rn(e0, make_float2(ps[32 * q + 4 * u], ps[32 * q + 4 * u + 1]));
-          const float2 g1 = __fmul2_rn(e1, make_float2(ps[32 * q + 4 * u + 2], ps[32 * q + 4 * u + 3]));
-          pk[2 * u] = pack2<BF16>(g0.x, g0.y);
-          pk[2 * u + 1] = pack2<BF16>(g1.x, g1.y);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t phys = (4 * q + u) ^ (static_cast<uint32_t>(t) & 7u);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ds_half + t * C::ROW + phys * 16),
-                       "r"(pk[4 * u]), "r"(pk[4 * u + 1]), "r"(pk[4 * u + 2]), "r"(pk[4 * u + 3])
-                       : "memory");
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_dsf);
-    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(b_dsf);
+    if (t == 0) FA_TRACE(p, W == 0 ? kBvSmDs : kBvW1Ds, i);
   }
-  if (t == 0) tma_store_wait_all();  // every reduce-add is complete before the CTA exits
   if (ok) ok = wait_bar(bbar<D>(base, C::B_DONE), 0, ctl, kWhereBwdDone);
   if (!named_bar_and(BAR, 128, ok)) return;
   tc_fence_after();
@@ -467,6 +448,58 @@ __device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint32_t base, u
     store_acc_tile<D, BF16>(tmem + lane_base + C::T_DV, base + C::OFF_Q, t, BAR, &p.tm_dv, kv0, bh);
   else
     store_acc_tile<D, BF16>(tmem + lane_base + C::T_DK, base + C::OFF_Q + C::TILE, t, BAR, &p.tm_dk, kv0, bh);
+}
+
+// --------------------------------------------------------------------------
+// dQ warpgroup (warps 8-11): dQ_i -> registers -> fp32 boxes -> TMA reduce-add
+// --------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void bwd_dq(const BwdParams& p, uint32_t base, uint32_t tmem, int bh, int nq,
+                                       const BCtl& ctl) {
+  using C = BCfg<D>;
+  constexpr int BAR = 3;
+  const int t = threadIdx.x - 256;  // query row within the Q tile = TMEM lane
+  const int lane = t & 31;
+  const uint32_t t_dq = tmem + (static_cast<uint32_t>(t & ~31) << 16) + C::T_DQ;
+  const uint32_t b_dqf = bbar<D>(base, C::B_DQF), b_dqe = bbar<D>(base, C::B_DQE);
+  for (int i = 0; i < nq; ++i) {
+    // Agreed by the whole warpgroup: the named barriers below need all 128 threads.
+    if (!named_bar_and(BAR, 128, wait_bar(b_dqf, i & 1, ctl, kWhereBwdDqFull))) break;
+    if (t == 0) FA_TRACE(p, kBvSmDq, i);
+    tc_fence_after();
+    uint32_t r[C::NBOX][32];
+#pragma unroll
+    for (int b = 0; b < C::NBOX; ++b) tmem_ld32(t_dq + 32 * b, r[b]);
+    tmem_ld_wait();
+#pragma unroll
+    for (int b = 0; b < C::NBOX; ++b) reg_fence(r[b]);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(b_dqe);  // the MMA warp may reuse these TMEM columns
+    if (t == 0) FA_TRACE(p, kBvSmDqLoaded, i);
+#pragma unroll
+    for (int b = 0; b < C::NBOX; ++b) {
+      const uint32_t buf = base + C::OFF_DQS + (b & 1) * C::BOX;
+      // The reduce-add that last read this buffer is the one before the most recent.
+      if (t == 0) bulk_wait_read<1>();
+      named_bar_sync(BAR, 128);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t phys = static_cast<uint32_t>(u) ^ (static_cast<uint32_t>(t) & 7u);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + t * 128u + phys * 16), "r"(r[b][4 * u]),
+                     "r"(r[b][4 * u + 1]), "r"(r[b][4 * u + 2]), "r"(r[b][4 * u + 3])
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(BAR, 128);
+      if (t == 0) {
+        tma_reduce_add_3d(&p.tm_dqacc, buf, 32 * b, i * C::BQ, bh);
+        tma_store_commit();
+      }
+    }
+    if (t == 0) FA_TRACE(p, kBvSmRed, i);
+  }
+  if (t == 0) tma_store_wait_all();  // every reduce-add is complete before the CTA exits
 }
 
 template <int D, bool BF16>
@@ -505,7 +538,7 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1) fa_bwd_main_kernel(const 
     mbar_init(bbar<D>(base, C::B_PF), 8);   // one arrival per softmax warp
     mbar_init(bbar<D>(base, C::B_DSF), 8);
     mbar_init(bbar<D>(base, C::B_DQF), 1);
-    mbar_init(bbar<D>(base, C::B_DQE), 8);
+    mbar_init(bbar<D>(base, C::B_DQE), 4);  // one arrival per dQ warp
     mbar_init(bbar<D>(base, C::B_DONE), 1);
     misc[1] = 0;
     mbar_init_fence();
@@ -519,21 +552,31 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1) fa_bwd_main_kernel(const 
   tc_fence_after();
   const uint32_t tmem = misc[0];
   const BCtl ctl{p, base + C::OFF_MISC + 4};
+  if (threadIdx.x == 0) FA_TRACE(p, kBvCta, 0);
 
-  if (warp == C::WARP_TMA) {
-    if ((threadIdx.x & 31) == 0) bwd_producer<D>(p, base, bh, kv0, nq, ctl);
-    __syncwarp();
-  } else if (warp == C::WARP_MMA) {
-    bwd_mma<D, BF16>(p, base, tmem, nq, ctl);
-    __syncwarp();
-  } else if (warp < 4) {
-    bwd_softmax<D, BF16, 0>(p, base, tmem, bh, kv0, nq, ctl);
-  } else if (warp < 8) {
+  if (warp >= 12) {
+    warpgroup_reg_dealloc<C::LOW_REGS>();
+    if (warp == C::WARP_TMA) {
+      if ((threadIdx.x & 31) == 0) bwd_producer<D>(p, base, bh, kv0, nq, ctl);
+      __syncwarp();
+    } else if (warp == C::WARP_MMA) {
+      bwd_mma<D, BF16>(p, base, tmem, nq, ctl);
+      __syncwarp();
+    }
+  } else if (warp >= 8) {
+    warpgroup_reg_alloc<C::DQ_REGS>();
+    bwd_dq<D>(p, base, tmem, bh, nq, ctl);
+  } else if (warp >= 4) {
+    warpgroup_reg_alloc<C::SM_REGS>();
     bwd_softmax<D, BF16, 1>(p, base, tmem, bh, kv0, nq, ctl);
+  } else {
+    warpgroup_reg_alloc<C::SM_REGS>();
+    bwd_softmax<D, BF16, 0>(p, base, tmem, bh, kv0, nq, ctl);
   }
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) FA_TRACE(p, kBvCta, 1);
   if (warp == C::WARP_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -617,6 +660,12 @@ cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(attr_done.load() & bit)) {
+    // The warpgroup register split draws on the registers the CTA is launched
+    // with: it is only valid at exactly LAUNCH_REGS per thread; refuse otherwise.
+    cudaFuncAttributes fa_attr;
+    e = cudaFuncGetAttributes(&fa_attr, kern);
+    if (e != cudaSuccess) return e;
+    if (fa_attr.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(bit);

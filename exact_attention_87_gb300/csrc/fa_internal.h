@@ -77,6 +77,9 @@ struct alignas(64) BwdParams {
   int B, H, N, d;
   int n_pad;             // N rounded up to the 128-row tile
   float scale;
+  // Used only by the testing build (-DFA_TESTING); zero / NULL otherwise.
+  int inject;                    // 1: the producer skips the dO load of Q tile 0
+  unsigned long long* timeline;  // [kTraceCtas, kTraceEvents, kTraceTiles] clock64 stamps
 };
 
 // Tile sizes of the fp16/bf16 kernel: Q rows per sub-tile (two sub-tiles per
@@ -88,6 +91,15 @@ constexpr int kTraceCtas = 8, kTraceTiles = 64, kTraceEvents = 16;
 enum : int {
   kEvS0Issued = 0, kEvS1Issued, kEvPV0Issued, kEvPV1Issued, kEvSm0SFull, kEvSm0PArrive, kEvSm1SFull,
   kEvSm1PArrive, kEvKIssued, kEvVIssued, kEvMmaKFull, kEvMmaVFull, kEvCta
+};
+// Backward kernel events (tile index = Q tile i): MMA issue of dV_i, dP_i,
+// S_{i+1}, dK_i, dQ_i; softmax warpgroup 0 (thread 0): S_i ready, P_i
+// arrived, dQ_i ready, dQ_i reduce-adds issued, dP_i ready, dS_i arrived,
+// dS^T half free (reduce-adds of dQ_{i-1} have read it), dQ_i out of TMEM;
+// warpgroup 1: P_i and dS_i arrived.
+enum : int {
+  kBvDV = 0, kBvDP, kBvS, kBvDK, kBvDQ, kBvSmS, kBvSmP, kBvSmDq, kBvSmRed, kBvSmDp, kBvSmDs, kBvSmDsFree,
+  kBvSmDqLoaded, kBvCta, kBvW1P, kBvW1Ds
 };
 
 // Launch the 16-bit (fp16 / bf16) forward kernel for head dimension p.d.

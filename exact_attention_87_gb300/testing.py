@@ -26,6 +26,11 @@ def lib():
         vp, i, f, ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong
         L.fa_fwd_testing.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, i, vp, vp, ll]
         L.fa_fwd_testing.restype = i
+        u64 = ctypes.c_ulonglong
+        L.fa_bwd_testing.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, u64, vp, i, vp, ll]
+        L.fa_bwd_testing.restype = i
+        L.fa_bwd_workspace_size.argtypes = [i, i, i, i]
+        L.fa_bwd_workspace_size.restype = u64
         L.fa_get_device_status.argtypes = [vp]
         L.fa_get_device_status.restype = i
         L.fa_testing_last_timeout_where.restype = ctypes.c_uint
@@ -54,6 +59,32 @@ def attention(q, k, v, scale=None, inject=0, stats=False, timeline=False, wait_l
     if check and rc != FA_OK:
         raise FAError(rc, "fa_fwd_testing")
     return out, lse, st, tl
+
+
+BWD_EVENTS = ["dV_issued", "dP_issued", "S_next_issued", "dK_issued", "dQ_issued", "sm_S_ready", "sm_P_arrived",
+              "sm_dQ_ready", "sm_dQ_reduce_issued", "sm_dP_ready", "sm_dS_arrived", "sm_dS_half_free", "sm_dQ_loaded",
+              "cta", "wg1_P_arrived", "wg1_dS_arrived"]
+
+
+def attention_backward(q, k, v, o, lse, do, scale=None, inject=0, timeline=False, wait_limit_cycles=0, check=True):
+    """Like exact_attention_87_gb300.attention_backward, through fa_bwd_testing.
+
+    Returns (dQ, dK, dV, timeline or None).
+    """
+    import torch
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(lib().fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=q.device)
+    tl = torch.zeros((TRACE_CTAS, TRACE_EVENTS, TRACE_TILES), dtype=torch.int64, device=q.device) if timeline else None
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = lib().fa_bwd_testing(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                              dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, float(scale), _dtype_code(q),
+                              ws.data_ptr(), ws.numel(), stream, int(inject),
+                              tl.data_ptr() if tl is not None else None, int(wait_limit_cycles))
+    if check and rc != FA_OK:
+        raise FAError(rc, "fa_bwd_testing")
+    return dq, dk, dv, tl
 
 
 def device_status(stream=None) -> int:

@@ -32,6 +32,20 @@ int fa_fwd_testing(const void *Q, const void *K, const void *V, void *O, float *
                    int inject, float *stats_trace, unsigned long long *timeline,
                    long long wait_limit_cycles);
 
+/*
+ * fa_bwd with instrumentation. Arguments up to `stream` are those of fa_bwd.
+ *  inject:       0 = none; 1 = the TMA producer skips the dO load of the first
+ *                Q tile, so the MMA warp's wait on it runs out; the kernel then
+ *                records FA_ERR_DEVICE_TIMEOUT, drains, frees TMEM and exits.
+ *  timeline:     NULL, or a device array [8, 16, 64] of uint64 receiving clock64
+ *                stamps of pipeline events of the first 8 CTAs of the main kernel.
+ *  wait_limit_cycles: > 0 overrides the barrier wait limit for this call.
+ */
+int fa_bwd_testing(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *LSE,
+                   void *dQ, void *dK, void *dV, int B, int H, int N, int d, float scale, int dtype,
+                   void *workspace, unsigned long long workspace_bytes, void *stream,
+                   int inject, unsigned long long *timeline, long long wait_limit_cycles);
+
 /* "Where" code of the first timeout recorded in the status word (0 = none;
  * not cleared by this call). */
 unsigned int fa_testing_last_timeout_where(void);

@@ -33,3 +33,49 @@ def test_injected_missing_tile_times_out_and_recovers():
     o_ref, lse_ref = oracle.attn(q, k, v)
     res = compare(o.cpu().double().numpy(), lse.cpu().double().numpy(), o_ref, lse_ref, "bf16")
     assert res["ok"], res
+
+
+def test_backward_injected_missing_tile_times_out_and_recovers():
+    """The backward kernel: dO of the first Q tile is never loaded."""
+    from exact_attention_87_gb300 import testing
+    from workloads import make_dout
+    q, k, v = (t.cuda() for t in make_qkv(1, 2, 512, 128, "bf16", seed=8, wid=8001))
+    do = make_dout(1, 2, 512, 128, "bf16", seed=8, wid=8001).cuda()
+    o, lse = fa.attention(q, k, v)
+    torch.cuda.synchronize()
+    assert testing.device_status() == 0
+    testing.attention_backward(q, k, v, o, lse, do, inject=1, wait_limit_cycles=20_000_000)
+    torch.cuda.synchronize()
+    assert testing.last_timeout_where() != 0
+    assert testing.device_status() == fa.FA_ERR_DEVICE_TIMEOUT
+    assert testing.device_status() == 0
+    # still usable, and the same result as the product library
+    dq, dk, dv, _ = testing.attention_backward(q, k, v, o, lse, do)
+    ref = fa.attention_backward(q, k, v, o, lse, do)
+    torch.cuda.synchronize()
+    assert testing.device_status() == 0
+    assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
+    assert (dq.float() - ref[0].float()).abs().max().item() <= 1e-2 * ref[0].float().abs().max().item()
+
+
+def test_backward_timeline_respects_dependencies():
+    """clock64 stamps of the testing build: every MMA is issued after the
+    softmax arrival it depends on (same SM clock within one CTA)."""
+    from exact_attention_87_gb300 import testing
+    from workloads import make_dout
+    N = 1024
+    q, k, v = (t.cuda() for t in make_qkv(1, 8, N, 128, "bf16", seed=9, wid=8002))
+    do = make_dout(1, 8, N, 128, "bf16", seed=9, wid=8002).cuda()
+    o, lse = fa.attention(q, k, v)
+    _, _, _, tl = testing.attention_backward(q, k, v, o, lse, do, timeline=True)
+    torch.cuda.synchronize()
+    assert testing.device_status() == 0
+    ev = {n: i for i, n in enumerate(testing.BWD_EVENTS)}
+    t = tl.cpu().numpy().astype("int64")
+    nq = N // 128
+    for c in range(testing.TRACE_CTAS):
+        for i in range(nq):
+            assert t[c, ev["dV_issued"], i] >= t[c, ev["sm_P_arrived"], i] > 0
+            assert t[c, ev["dK_issued"], i] >= t[c, ev["sm_dS_arrived"], i] > 0
+            assert t[c, ev["sm_dQ_ready"], i] >= t[c, ev["dQ_issued"], i] > 0
+            assert t[c, ev["sm_S_ready"], i] > 0 and t[c, ev["sm_dP_ready"], i] > 0
