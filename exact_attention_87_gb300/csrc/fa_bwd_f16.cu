@@ -70,7 +70,7 @@ template <int D>
 struct BCfg {
   static constexpr int BQ = 128;                    // queries per Q tile (MMA N of S^T)
   static constexpr int BK = 128;                    // keys per CTA (TMEM lanes, MMA M)
-  static constexpr int QST = 2;                     // Q (+ LSE, D rows) stages
+  static constexpr int QST = (D == 128) ? 2 : 3;    // Q (+ LSE, D rows) stages
   static constexpr int OST = (D == 128) ? 1 : 2;    // dO stages
   static constexpr uint32_t ROW = 128;              // bytes of one 128-byte swizzle row (64 16-bit elements)
   static constexpr uint32_t TILE = 128 * D * 2;     // a 128-row tile of Q, K, V or dO
@@ -91,8 +91,9 @@ struct BCfg {
   static constexpr int B_QF = 2, B_QE = B_QF + QST;
   static constexpr int B_OF = B_QE + QST, B_OE = B_OF + OST;
   static constexpr int B_SF = B_OE + OST, B_DPF = B_SF + 1, B_PF = B_DPF + 1, B_DSF = B_PF + 1;
-  static constexpr int B_DQF = B_DSF + 1, B_DQE = B_DQF + 1, B_DONE = B_DQE + 1;
-  static constexpr int NBAR = B_DONE + 1;
+  static constexpr int B_DQF = B_DSF + 1, B_DQE = B_DQF + 1, B_DSE = B_DQE + 1, B_DONE = B_DSE + 1;
+  static constexpr int B_PROBE = B_DONE + 1;  // testing build: one commit per product, stamped by warp 14
+  static constexpr int NBAR = B_PROBE + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
   // The dynamic shared memory starts 1 KB-aligned (checked in the kernel): no slack.
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
@@ -101,7 +102,7 @@ struct BCfg {
   static constexpr uint32_t T_DQ = (D == 128) ? 128 : 384;
   static constexpr int THREADS = 512;
   static constexpr int WARP_TMA = 12, WARP_MMA = 13;
-  static constexpr int LAUNCH_REGS = 128, SM_REGS = 160, DQ_REGS = 152, LOW_REGS = 40;
+  static constexpr int LAUNCH_REGS = 128, SM_REGS = 160, DQ_REGS = 144, LOW_REGS = 48;
   static_assert(128 * (2 * SM_REGS + DQ_REGS + LOW_REGS) <= THREADS * LAUNCH_REGS, "register split exceeds the pool");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(OFF_DS % 1024 == 0 && OFF_DO % 1024 == 0 && OFF_Q % 1024 == 0, "swizzled buffers need 1 KB alignment");
@@ -148,6 +149,7 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint32_t base, 
     bulk_load(rows, p.lse2 + row_base + static_cast<size_t>(i) * C::BQ, 512, qf);
     bulk_load(rows + 512, p.dsum + row_base + static_cast<size_t>(i) * C::BQ, 512, qf);
     nqi = i + 1;
+    FA_TRACE(p, kBvQLoad, i);
 #ifdef FA_TESTING
     if (p.inject == 1 && i == 0) continue;  // fault injection: dO_0 is never loaded
 #endif
@@ -159,6 +161,7 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint32_t base, 
     for (int h = 0; h < D / 64; ++h)
       tma_load_3d(base + C::OFF_DO + os * C::TILE + h * C::HALF, &p.tm_do, of, 64 * h, i * C::BQ, bh);
     noi = i + 1;
+    FA_TRACE(p, kBvDOLoad, i);
   }
   if (!ok) {
     // Every copy this thread started must land before the CTA exits.
@@ -178,12 +181,21 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint32_t base, 
 // --------------------------------------------------------------------------
 // MMA warp (whole warp; one elected lane issues)
 // --------------------------------------------------------------------------
+// A descriptor the compiler must treat as computed here: the k-loops below are
+// unrolled (back-to-back MMAs issue at the full rate only from straight-line
+// code), and without this the compiler hoists every k-step's descriptor of all
+// five products out of the Q-tile loop into registers the warp does not have.
+__device__ __forceinline__ uint64_t opaque(uint64_t x) {
+  asm volatile("" : "+l"(x));
+  return x;
+}
+
 // 128 x 128 x D product of two K-major tiles (both 64-column halves, 128-byte swizzle).
 template <int D>
 __device__ __forceinline__ void mma_kmajor_tiles(uint32_t d_tmem, uint32_t a_base, uint32_t b_base, uint32_t idesc) {
-  const uint64_t a0 = smem_desc_sw128(a_base, 16, 1024);
-  const uint64_t b0 = smem_desc_sw128(b_base, 16, 1024);
-#pragma unroll 1  // issue-bound anyway; keeps the descriptors out of registers
+  const uint64_t a0 = opaque(smem_desc_sw128(a_base, 16, 1024));
+  const uint64_t b0 = opaque(smem_desc_sw128(b_base, 16, 1024));
+#pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = ((kk / 4) * BCfg<D>::HALF + (kk & 3) * 32u) >> 4;
     mma_f16_ss_elect(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
@@ -203,95 +215,163 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, uint32_t base, uint3
   const uint32_t b_sf = bbar<D>(base, C::B_SF), b_dpf = bbar<D>(base, C::B_DPF);
   const uint32_t b_pf = bbar<D>(base, C::B_PF), b_dsf = bbar<D>(base, C::B_DSF);
   const uint32_t b_dqf = bbar<D>(base, C::B_DQF), b_dqe = bbar<D>(base, C::B_DQE);
-  const uint32_t b_done = bbar<D>(base, C::B_DONE);
+  const uint32_t b_dse = bbar<D>(base, C::B_DSE), b_done = bbar<D>(base, C::B_DONE);
   const uint64_t dq_a0 = smem_desc_sw128(base + C::OFF_DS, C::HALF, 1024);
   const uint64_t dq_b0 = smem_desc_sw128(base + C::OFF_K, lbo_d, 1024);
   const uint64_t dk_a0 = smem_desc_sw128(base + C::OFF_DS, 16, 1024);
+#ifdef FA_TESTING
+  // Testing build with a timeline: a commit after every product of the loop,
+  // whose completions warp 14 stamps (the probe costs nothing otherwise).
+#define FA_PROBE_COMMIT()                                                         \
+  do {                                                                            \
+    if (p.timeline && blockIdx.x < kTraceCtas) tc_commit_elect(bbar<D>(base, C::B_PROBE)); \
+  } while (0)
+#else
+#define FA_PROBE_COMMIT() \
+  do {                    \
+  } while (0)
+#endif
+
+  // S^T_j = K Q_j^T into the S^T columns, over P^T_{j-1}, whose dV_{j-1} is issued before.
+  auto issue_s = [&](int j) {
+    mma_kmajor_tiles<D>(tmem + C::T_S, base + C::OFF_K, base + C::OFF_Q + (j % C::QST) * C::TILE, idesc_st);
+    tc_commit_elect(b_sf);
+  };
+  // dP^T_j = V dO_j^T
+  auto issue_dp = [&](int j) {
+    mma_kmajor_tiles<D>(tmem + C::T_DP, base + C::OFF_V, base + C::OFF_DO + (j % C::OST) * C::TILE, idesc_st);
+    tc_commit_elect(b_dpf);
+  };
+  // dV += P^T_j dO_j (K = the 128 queries of tile j). P^T of queries 0-63 is
+  // packed in S^T columns [0,32), of queries 64-127 in [64,96). dO_j is free
+  // afterwards (its dP^T_j was issued before).
+  auto issue_dv = [&](int j) {
+    const uint64_t b0 = opaque(smem_desc_sw128(base + C::OFF_DO + (j % C::OST) * C::TILE, lbo_d, 1024));
+#pragma unroll
+    for (int kk = 0; kk < C::BQ / 16; ++kk)
+      mma_f16_ts_elect(tmem + C::T_DV, tmem + C::T_S + (kk < 4 ? 8 * kk : 64 + 8 * (kk - 4)),
+                       b0 + ((kk * 2048u) >> 4), idesc_acc, (j > 0 || kk > 0) ? 1u : 0u);
+    tc_commit_elect(bbar<D>(base, C::B_OE + j % C::OST));
+  };
 
   if (!wait_bar_warp(bbar<D>(base, C::B_K), 0, ctl, kWhereBwdKV)) goto drain;
   if (!wait_bar_warp(bbar<D>(base, C::B_QF), 0, ctl, kWhereBwdQFull)) goto drain;
   tc_fence_after();
-  mma_kmajor_tiles<D>(tmem + C::T_S, base + C::OFF_K, base + C::OFF_Q, idesc_st);
-  tc_commit_elect(b_sf);
+  issue_s(0);
   if (!wait_bar_warp(bbar<D>(base, C::B_V), 0, ctl, kWhereBwdKV)) goto drain;
   if (!wait_bar_warp(bbar<D>(base, C::B_OF), 0, ctl, kWhereBwdDoFull)) goto drain;
   tc_fence_after();
-  mma_kmajor_tiles<D>(tmem + C::T_DP, base + C::OFF_V, base + C::OFF_DO, idesc_st);
-  tc_commit_elect(b_dpf);
-
-  for (int i = 0; i < nq; ++i) {
-    const int qs = i % C::QST, os = i % C::OST;
-    const uint32_t b_of = bbar<D>(base, C::B_OF + os);
-    // dV += P^T dO_i (K = the 128 queries of tile i). P^T of queries 0-63 is
-    // packed in S^T columns [0,32), of queries 64-127 in [64,96).
-    if (!wait_bar_warp(b_pf, i & 1, ctl, kWhereBwdPFull)) goto drain;
-    if (i > 0 && !wait_bar_warp(b_of, (i / C::OST) & 1, ctl, kWhereBwdDoFull)) goto drain;
-    tc_fence_after();
-    {
-      const uint64_t b0 = smem_desc_sw128(base + C::OFF_DO + os * C::TILE, lbo_d, 1024);
-#pragma unroll 1  // issue-bound anyway; keeps the descriptors out of registers
-      for (int kk = 0; kk < C::BQ / 16; ++kk)
-        mma_f16_ts_elect(tmem + C::T_DV, tmem + C::T_S + (kk < 4 ? 8 * kk : 64 + 8 * (kk - 4)),
-                         b0 + ((kk * 2048u) >> 4), idesc_acc, (i > 0 || kk > 0) ? 1u : 0u);
-    }
-    if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDV, i);
-    // dP^T_i (tile 0's was issued up front)
-    if (i > 0) {
-      if constexpr (D == 128) {
-        // dQ_{i-1} occupies the dP^T columns until the softmax warps have read it.
-        if (!wait_bar_warp(b_dqe, (i - 1) & 1, ctl, kWhereBwdDqEmpty)) goto drain;
-      }
-      tc_fence_after();
-      mma_kmajor_tiles<D>(tmem + C::T_DP, base + C::OFF_V, base + C::OFF_DO + os * C::TILE, idesc_st);
-      tc_commit_elect(b_dpf);
-      if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDP, i);
-    }
-    tc_commit_elect(bbar<D>(base, C::B_OE + os));  // dO_i is free once dV_i and dP^T_i are done
-    // S^T_{i+1}: overwrites P^T_i, which dV_i (issued before) reads.
-    if (i + 1 < nq) {
-      const int qn = (i + 1) % C::QST;
+  issue_dp(0);
+  if (!wait_bar_warp(b_pf, 0, ctl, kWhereBwdPFull)) goto drain;
+  tc_fence_after();
+  issue_dv(0);
+  if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDV, 0);
+  if (nq > 1) {
 #ifdef FA_STRICT_MMA_ORDER
-      // dV_i (with dP^T_i) complete before S^T_{i+1} reuses the P^T columns.
-      if (!wait_bar_warp(bbar<D>(base, C::B_OE + os), (i / C::OST) & 1, ctl, kWhereBwdDoEmpty)) goto drain;
+    if (!wait_bar_warp(bbar<D>(base, C::B_OE), 0, ctl, kWhereBwdDoEmpty)) goto drain;
 #endif
-      if (!wait_bar_warp(bbar<D>(base, C::B_QF + qn), ((i + 1) / C::QST) & 1, ctl, kWhereBwdQFull)) goto drain;
-      tc_fence_after();
-      mma_kmajor_tiles<D>(tmem + C::T_S, base + C::OFF_K, base + C::OFF_Q + qn * C::TILE, idesc_st);
-      tc_commit_elect(b_sf);
-      if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvS, i);
-    }
-    // dK += dS^T Q_i and dQ_i = dS K_j, both from the dS^T tile in SMEM.
-    if (!wait_bar_warp(b_dsf, i & 1, ctl, kWhereBwdDsFull)) goto drain;
+    if (!wait_bar_warp(bbar<D>(base, C::B_QF + 1 % C::QST), (1 / C::QST) & 1, ctl, kWhereBwdQFull)) goto drain;
     tc_fence_after();
-    {
-      const uint64_t b0 = smem_desc_sw128(base + C::OFF_Q + qs * C::TILE, lbo_d, 1024);
-#pragma unroll 1  // issue-bound anyway; keeps the descriptors out of registers
-      for (int kk = 0; kk < C::BQ / 16; ++kk) {
-        const uint32_t aoff = ((kk / 4) * C::HALF + (kk & 3) * 32u) >> 4;
-        mma_f16_ss_elect(tmem + C::T_DK, dk_a0 + aoff, b0 + ((kk * 2048u) >> 4), idesc_acc,
-                         (i > 0 || kk > 0) ? 1u : 0u);
-      }
-    }
-    tc_commit_elect(bbar<D>(base, C::B_QE + qs));  // Q_i (and its rows) are free once dK_i is done
-    if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDK, i);
+    issue_s(1);
+  }
+
+  // Block i: dQ_i, dK_i (both need dS_i), dP^T_{i+1} (while dS_i's products run,
+  // so that dS_{i+1} can start as early as possible), dV_{i+1}, S^T_{i+2}.
+  for (int i = 0; i < nq; ++i) {
+    if (!wait_bar_warp(b_dsf, i & 1, ctl, kWhereBwdDsFull)) goto drain;
+    if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDQReady, i);
     if constexpr (D == 64) {
       // dQ_{i-1} must have left its TMEM columns.
       if (i > 0 && !wait_bar_warp(b_dqe, (i - 1) & 1, ctl, kWhereBwdDqEmpty)) goto drain;
-      tc_fence_after();
     }
-#pragma unroll 1  // issue-bound anyway; keeps the descriptors out of registers
-    for (int kk = 0; kk < C::BK / 16; ++kk)
-      mma_f16_ss_elect(tmem + C::T_DQ, dq_a0 + ((kk * 2048u) >> 4), dq_b0 + ((kk * 2048u) >> 4), idesc_dq,
-                       kk > 0 ? 1u : 0u);
+    tc_fence_after();
+    {
+      const uint64_t a0 = opaque(dq_a0), b0 = opaque(dq_b0);
+#pragma unroll
+      for (int kk = 0; kk < C::BK / 16; ++kk)
+        mma_f16_ss_elect(tmem + C::T_DQ, a0 + ((kk * 2048u) >> 4), b0 + ((kk * 2048u) >> 4), idesc_dq,
+                         kk > 0 ? 1u : 0u);
+    }
     tc_commit_elect(b_dqf);
+    FA_PROBE_COMMIT();
     if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDQ, i);
+    {
+      const uint64_t b0 = opaque(smem_desc_sw128(base + C::OFF_Q + (i % C::QST) * C::TILE, lbo_d, 1024));
+      const uint64_t a0 = opaque(dk_a0);
+#pragma unroll
+      for (int kk = 0; kk < C::BQ / 16; ++kk) {
+        const uint32_t aoff = ((kk / 4) * C::HALF + (kk & 3) * 32u) >> 4;
+        mma_f16_ss_elect(tmem + C::T_DK, a0 + aoff, b0 + ((kk * 2048u) >> 4), idesc_acc,
+                         (i > 0 || kk > 0) ? 1u : 0u);
+      }
+    }
+    tc_commit_elect(bbar<D>(base, C::B_QE + i % C::QST));  // Q_i (and its rows) are free once dK_i is done
+    tc_commit_elect(b_dse);                                // so is the dS^T tile (dQ_i was issued before)
+    FA_PROBE_COMMIT();
+    if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDK, i);
+    if (i + 1 < nq) {
+      const int n1 = i + 1;
+      if constexpr (D == 128) {
+        // dQ_i occupies the dP^T columns until the dQ warps have read it.
+        if (!wait_bar_warp(b_dqe, i & 1, ctl, kWhereBwdDqEmpty)) goto drain;
+      }
+      if (!wait_bar_warp(bbar<D>(base, C::B_OF + n1 % C::OST), (n1 / C::OST) & 1, ctl, kWhereBwdDoFull)) goto drain;
+      if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDPReady, n1);
+      tc_fence_after();
+      issue_dp(n1);
+      FA_PROBE_COMMIT();
+      if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDP, n1);
+      if (!wait_bar_warp(b_pf, n1 & 1, ctl, kWhereBwdPFull)) goto drain;
+      if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDVReady, n1);
+      tc_fence_after();
+      issue_dv(n1);
+      FA_PROBE_COMMIT();
+      if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDV, n1);
+    }
+    if (i + 2 < nq) {
+      const int n2 = i + 2;
+#ifdef FA_STRICT_MMA_ORDER
+      // dV_{i+1} complete before S^T_{i+2} reuses the P^T columns.
+      if (!wait_bar_warp(bbar<D>(base, C::B_OE + (i + 1) % C::OST), ((i + 1) / C::OST) & 1, ctl, kWhereBwdDoEmpty))
+        goto drain;
+#endif
+      if (!wait_bar_warp(bbar<D>(base, C::B_QF + n2 % C::QST), (n2 / C::QST) & 1, ctl, kWhereBwdQFull)) goto drain;
+      if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvSReady, n2);
+      tc_fence_after();
+      issue_s(n2);
+      FA_PROBE_COMMIT();
+      if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvS, n2);
+    }
   }
 drain:
   // One commit after the last MMA: the epilogues wait for it, and every MMA
   // completes before the CTA frees TMEM or exits.
   tc_commit_elect(b_done);
   __all_sync(0xffffffffu, wait_bar_drain(b_done, 0, ctl));
+#undef FA_PROBE_COMMIT
 }
+
+#ifdef FA_TESTING
+// Testing build: stamp the completion of every product the MMA warp commits
+// to the probe barrier, in issue order: dQ_i, dK_i, dP_{i+1}, dV_{i+1}, S_{i+2}.
+template <int D>
+__device__ __forceinline__ void bwd_probe(const BwdParams& p, uint32_t base, int nq, const BCtl& ctl) {
+  if (!(p.timeline && blockIdx.x < kTraceCtas)) return;
+  const uint32_t bar = bbar<D>(base, BCfg<D>::B_PROBE);
+  uint32_t phase = 0;
+  for (int i = 0; i < nq; ++i) {
+    const int events[5] = {kBvDoneDQ, kBvDoneDK, kBvDoneDP, kBvDoneDV, kBvDoneS};
+    const int tile[5] = {i, i, i + 1, i + 1, i + 2};
+    const bool made[5] = {true, true, i + 1 < nq, i + 1 < nq, i + 2 < nq};
+    for (int e = 0; e < 5; ++e) {
+      if (!made[e]) continue;
+      if (!wait_bar(bar, phase & 1, ctl, kWhereDrain)) return;
+      ++phase;
+      FA_TRACE(p, events[e], tile[e]);
+    }
+  }
+}
+#endif
 
 // Store a 128 x D fp32 TMEM accumulator (this thread's lane = row t) as a
 // 16-bit tile through the swizzled staging buffer `stage` with TMA.
@@ -347,7 +427,7 @@ __device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint32_t base, u
   const float2 sc2 = make_float2(p.scale, p.scale);
   const uint32_t b_sf = bbar<D>(base, C::B_SF), b_dpf = bbar<D>(base, C::B_DPF);
   const uint32_t b_pf = bbar<D>(base, C::B_PF), b_dsf = bbar<D>(base, C::B_DSF);
-  const uint32_t b_dqf = bbar<D>(base, C::B_DQF);
+  const uint32_t b_dse = bbar<D>(base, C::B_DSE);
   const uint32_t ds_half = base + C::OFF_DS + W * C::HALF;  // this warpgroup's half of dS^T
   bool ok = true;
   float ps[64];  // P*scale of this thread's key for queries [64W, 64W+64) of the current tile
@@ -360,12 +440,15 @@ __device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint32_t base, u
     if (!named_bar_and(BAR, 128, wait_bar(b_sf, i & 1, ctl, kWhereBwdSFull))) { ok = false; break; }
     if (W == 0 && t == 0) FA_TRACE(p, kBvSmS, i);
     tc_fence_after();
+    uint32_t rs[2][32];
+    tmem_ld32(t_s, rs[0]);
+    tmem_ld32(t_s + 32, rs[1]);
+    tmem_ld_wait();
+    reg_fence(rs[0]);
+    reg_fence(rs[1]);
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      uint32_t r[32];
-      tmem_ld32(t_s + 32 * q, r);
-      tmem_ld_wait();
-      reg_fence(r);
+      const uint32_t (&r)[32] = rs[q];
       uint32_t pk[16];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -388,8 +471,9 @@ __device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint32_t base, u
         ps[32 * q + 4 * u + 2] = s1.x;
         ps[32 * q + 4 * u + 3] = s1.y;
       }
-      // Queries [32q, 32q+32) of this half -> packed columns [16q, 16q+16), already read.
+      // Queries [32q, 32q+32) of this half -> packed columns [16q, 16q+16) (both chunks were read above).
       tmem_st16(t_s + 16 * q, pk);
+      if (q == 0 && W == 0 && t == 0) FA_TRACE(p, kBvSmPChunk0, i);
     }
     tmem_st_wait();
     tc_fence_before();
@@ -400,16 +484,20 @@ __device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint32_t base, u
     // ---- dS_i: dS^T * scale = P*scale (dP^T - D), 16-bit, into row t of this warpgroup's dS^T half
     if (!named_bar_and(BAR, 128, wait_bar(b_dpf, i & 1, ctl, kWhereBwdDpFull))) { ok = false; break; }
     if (W == 0 && t == 0) FA_TRACE(p, kBvSmDp, i);
-    // dS^T_{i-1} is read by dK_{i-1} and dQ_{i-1}; dQ_{i-1} completing covers both
-    // (it is issued before dV_i and dP^T_i, so this wait is normally already over).
-    if (i > 0 && !named_bar_and(BAR, 128, wait_bar(b_dqf, (i - 1) & 1, ctl, kWhereBwdDqFull))) { ok = false; break; }
+    // dS^T_{i-1} is read by dQ_{i-1} and dK_{i-1}, issued before dP^T_i: this
+    // wait is normally over by now.
+    if (i > 0 && !named_bar_and(BAR, 128, wait_bar(b_dse, (i - 1) & 1, ctl, kWhereBwdDsEmpty))) { ok = false; break; }
+    if (W == 0 && t == 0) FA_TRACE(p, kBvSmDsWaited, i);
     tc_fence_after();
+    uint32_t rdp[2][32];
+    tmem_ld32(t_dp, rdp[0]);
+    tmem_ld32(t_dp + 32, rdp[1]);
+    tmem_ld_wait();
+    reg_fence(rdp[0]);
+    reg_fence(rdp[1]);
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      uint32_t r[32];
-      tmem_ld32(t_dp + 32 * q, r);
-      tmem_ld_wait();
-      reg_fence(r);
+      const uint32_t (&r)[32] = rdp[q];
       uint32_t pk[16];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -433,6 +521,7 @@ __device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint32_t base, u
                      "r"(pk[4 * u]), "r"(pk[4 * u + 1]), "r"(pk[4 * u + 2]), "r"(pk[4 * u + 3])
                      : "memory");
       }
+      if (W == 0 && t == 0) FA_TRACE(p, q == 0 ? kBvSmDsChunk0 : kBvSmDsChunk1, i);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -539,7 +628,9 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1) fa_bwd_main_kernel(const 
     mbar_init(bbar<D>(base, C::B_DSF), 8);
     mbar_init(bbar<D>(base, C::B_DQF), 1);
     mbar_init(bbar<D>(base, C::B_DQE), 4);  // one arrival per dQ warp
+    mbar_init(bbar<D>(base, C::B_DSE), 1);
     mbar_init(bbar<D>(base, C::B_DONE), 1);
+    mbar_init(bbar<D>(base, C::B_PROBE), 1);
     misc[1] = 0;
     mbar_init_fence();
   }
@@ -563,6 +654,12 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1) fa_bwd_main_kernel(const 
       bwd_mma<D, BF16>(p, base, tmem, nq, ctl);
       __syncwarp();
     }
+#ifdef FA_TESTING
+    else if (warp == C::WARP_MMA + 1) {
+      if ((threadIdx.x & 31) == 0) bwd_probe<D>(p, base, nq, ctl);
+      __syncwarp();
+    }
+#endif
   } else if (warp >= 8) {
     warpgroup_reg_alloc<C::DQ_REGS>();
     bwd_dq<D>(p, base, tmem, bh, nq, ctl);

@@ -87,7 +87,7 @@ struct alignas(64) BwdParams {
 constexpr int kF16BlockQ = 128, kF16BlockKV = 128;
 
 // Timeline trace layout of the testing build.
-constexpr int kTraceCtas = 8, kTraceTiles = 64, kTraceEvents = 16;
+constexpr int kTraceCtas = 8, kTraceTiles = 64, kTraceEvents = 32;
 enum : int {
   kEvS0Issued = 0, kEvS1Issued, kEvPV0Issued, kEvPV1Issued, kEvSm0SFull, kEvSm0PArrive, kEvSm1SFull,
   kEvSm1PArrive, kEvKIssued, kEvVIssued, kEvMmaKFull, kEvMmaVFull, kEvCta
@@ -97,9 +97,13 @@ enum : int {
 // arrived, dQ_i ready, dQ_i reduce-adds issued, dP_i ready, dS_i arrived,
 // dS^T half free (reduce-adds of dQ_{i-1} have read it), dQ_i out of TMEM;
 // warpgroup 1: P_i and dS_i arrived.
+// Then, for the MMA warp, the moment each product's waits are over (before
+// its first MMA), and the producer's issue of the Q_i and dO_i loads.
 enum : int {
   kBvDV = 0, kBvDP, kBvS, kBvDK, kBvDQ, kBvSmS, kBvSmP, kBvSmDq, kBvSmRed, kBvSmDp, kBvSmDs, kBvSmDsFree,
-  kBvSmDqLoaded, kBvCta, kBvW1P, kBvW1Ds
+  kBvSmDqLoaded, kBvCta, kBvW1P, kBvW1Ds, kBvDVReady, kBvDPReady, kBvSReady, kBvDKReady, kBvDQReady, kBvQLoad,
+  kBvDOLoad, kBvSmPChunk0, kBvSmDsWaited, kBvSmDsChunk0, kBvSmDsChunk1, kBvDoneDQ, kBvDoneDK, kBvDoneDP, kBvDoneDV,
+  kBvDoneS
 };
 
 // Launch the 16-bit (fp16 / bf16) forward kernel for head dimension p.d.

@@ -11,7 +11,7 @@ import math
 from . import FA_OK, FAError, _dtype_code
 from ._build import TESTING_LIB_PATH, build
 
-TRACE_CTAS, TRACE_EVENTS, TRACE_TILES = 8, 16, 64
+TRACE_CTAS, TRACE_EVENTS, TRACE_TILES = 8, 32, 64
 EVENTS = ["S0_issued", "S1_issued", "PV0_issued", "PV1_issued", "sm0_sfull", "sm0_parrive", "sm1_sfull",
           "sm1_parrive", "K_issued", "V_issued", "mma_kfull", "mma_vfull", "cta"]
 KV_TILE = 128  # keys per K/V tile of the fp16/bf16 kernel (stats_trace has ceil(N / KV_TILE) entries per row)
@@ -63,7 +63,8 @@ def attention(q, k, v, scale=None, inject=0, stats=False, timeline=False, wait_l
 
 BWD_EVENTS = ["dV_issued", "dP_issued", "S_next_issued", "dK_issued", "dQ_issued", "sm_S_ready", "sm_P_arrived",
               "sm_dQ_ready", "sm_dQ_reduce_issued", "sm_dP_ready", "sm_dS_arrived", "sm_dS_half_free", "sm_dQ_loaded",
-              "cta", "wg1_P_arrived", "wg1_dS_arrived"]
+              "cta", "wg1_P_arrived", "wg1_dS_arrived", "dV_ready", "dP_ready", "S_next_ready", "dK_ready", "dQ_ready",
+              "Q_load_issued", "dO_load_issued"]
 
 
 def attention_backward(q, k, v, o, lse, do, scale=None, inject=0, timeline=False, wait_limit_cycles=0, check=True):

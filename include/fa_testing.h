@@ -23,7 +23,7 @@ extern "C" {
  *  stats_trace:  NULL, or a device array [B*H*N, ceil(N/128), 2] of fp32 that
  *                receives, after every key tile, the row's reference max in
  *                natural-log units and its running denominator (fp16/bf16 only).
- *  timeline:     NULL, or a device array [8, 16, 64] of uint64 receiving clock64
+ *  timeline:     NULL, or a device array [8, 32, 64] of uint64 receiving clock64
  *                stamps of pipeline events of the first 8 CTAs (fp16/bf16 only).
  *  wait_limit_cycles: > 0 overrides the barrier wait limit for this call.
  */
@@ -37,7 +37,7 @@ int fa_fwd_testing(const void *Q, const void *K, const void *V, void *O, float *
  *  inject:       0 = none; 1 = the TMA producer skips the dO load of the first
  *                Q tile, so the MMA warp's wait on it runs out; the kernel then
  *                records FA_ERR_DEVICE_TIMEOUT, drains, frees TMEM and exits.
- *  timeline:     NULL, or a device array [8, 16, 64] of uint64 receiving clock64
+ *  timeline:     NULL, or a device array [8, 32, 64] of uint64 receiving clock64
  *                stamps of pipeline events of the first 8 CTAs of the main kernel.
  *  wait_limit_cycles: > 0 overrides the barrier wait limit for this call.
  */
