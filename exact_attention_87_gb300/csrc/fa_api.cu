@@ -148,7 +148,8 @@ const char* fa_strerror(int status) {
     case FA_ERR_NULL: return "a required pointer is NULL";
     case FA_ERR_DTYPE: return "dtype must be FA_F32, FA_F16 or FA_BF16";
     case FA_ERR_SHAPE: return "B, H and N must be >= 1 and B*H*N*d must stay below 2^40 elements";
-    case FA_ERR_HEADDIM: return "head dimension d must be 64 or 128";
+    case FA_ERR_HEADDIM:
+      return "head dimension d must be 64 or 128 (or 256 for the fp16/bf16 forward pass)";
     case FA_ERR_ALIGN: return "Q, K, V and O must be 16-byte aligned and LSE 4-byte aligned";
     case FA_ERR_CUDA: return "a CUDA call failed";
     case FA_ERR_DEVICE_TIMEOUT: return "a kernel timed out waiting on an internal pipeline barrier";
@@ -213,7 +214,7 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
   if (!Q || !K || !V || !O || !LSE) return FA_ERR_NULL;
   if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
   if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
-  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  if (d != 64 && d != 128 && !(d == 256 && dtype != FA_F32)) return FA_ERR_HEADDIM;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
   if (causal != 0 && causal != 1) return FA_ERR_SHAPE;
   const long long BH = static_cast<long long>(B) * H;
@@ -247,7 +248,8 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
   p.scale = scale;
   p.num_sms = dev.num_sms;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int splits = dtype == FA_F32 ? 1 : effective_splits(B, H, N, d, num_splits, dev.num_sms);
+  // fp32 and d = 256 always run unsplit.
+  const int splits = (dtype == FA_F32 || d == 256) ? 1 : effective_splits(B, H, N, d, num_splits, dev.num_sms);
   const long long tiles = kv_tiles(N);
   p.split_tiles = static_cast<int>((tiles + splits - 1) / splits);
   p.num_splits = static_cast<int>((tiles + p.split_tiles - 1) / p.split_tiles);
@@ -267,13 +269,18 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
     const CUtensorMapDataType dt =
         dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const int bh = static_cast<int>(BH);
+    const int kv_rows = d == 256 ? fa::kD256BlockKV : fa::kF16BlockKV;
     if (!encode_bhnd_16bit(&p.tm_q, Q, bh, N, d, dt, fa::kF16BlockQ) ||
-        !encode_bhnd_16bit(&p.tm_k, K, bh, N, d, dt, fa::kF16BlockKV) ||
-        !encode_bhnd_16bit(&p.tm_v, V, bh, N, d, dt, fa::kF16BlockKV) ||
+        !encode_bhnd_16bit(&p.tm_k, K, bh, N, d, dt, kv_rows) ||
+        !encode_bhnd_16bit(&p.tm_v, V, bh, N, d, dt, kv_rows) ||
         !encode_bhnd_16bit(&p.tm_o, O, bh, N, d, dt, fa::kF16BlockQ))
       return FA_ERR_CUDA;
-    e = fa::launch_fwd_f16(p, dtype == FA_BF16, s);
-    if (e == cudaSuccess && p.num_splits > 1) e = fa::launch_merge(p, dtype == FA_BF16, s);
+    if (d == 256) {
+      e = fa::launch_fwd_d256(p, dtype == FA_BF16, s);
+    } else {
+      e = fa::launch_fwd_f16(p, dtype == FA_BF16, s);
+      if (e == cudaSuccess && p.num_splits > 1) e = fa::launch_merge(p, dtype == FA_BF16, s);
+    }
   }
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -305,13 +312,13 @@ int fa_fwd_splitkv_noalloc(const void* Q, const void* K, const void* V, void* O,
                            int d, float scale, int dtype, int num_splits, void* stream) {
   if (num_splits < 0) return FA_ERR_SHAPE;
   if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
-  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
   if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+  if (d != 64 && d != 128 && !(d == 256 && dtype != FA_F32)) return FA_ERR_HEADDIM;
   void* scratch = nullptr;
   const int st = noalloc_scratch(&scratch);
   if (st != FA_OK) return st;
   const unsigned long long need =
-      dtype == FA_F32 ? 0ull : fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits);
+      (dtype == FA_F32 || d == 256) ? 0ull : fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits);
   if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
   return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, dtype, stream, 0, nullptr, nullptr, 0, num_splits, scratch,
                   FA_NOALLOC_SCRATCH_BYTES);
@@ -319,6 +326,7 @@ int fa_fwd_splitkv_noalloc(const void* Q, const void* K, const void* V, void* O,
 
 int fa_fwd_splitkv_num_splits(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1) return -FA_ERR_SHAPE;
+  if (d == 256) return 1;  // the d = 256 kernel runs unsplit
   if (d != 64 && d != 128) return -FA_ERR_HEADDIM;
   DeviceInfo dev;
   const int st = device_info(&dev);
@@ -327,7 +335,7 @@ int fa_fwd_splitkv_num_splits(int B, int H, int N, int d) {
 }
 
 unsigned long long fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits) {
-  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || num_splits < 0) return 0;
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || num_splits < 0) return 0;  // d = 256: unsplit, none
   int splits = num_splits;
   if (splits == 0) {
     splits = fa_fwd_splitkv_num_splits(B, H, N, d);

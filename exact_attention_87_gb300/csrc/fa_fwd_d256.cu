@@ -1,0 +1,418 @@
+// fa_fwd_d256.cu — FlashAttention forward for fp16 / bf16 with head dimension 256 on sm_103a.
+//
+// Same recurrence as the d = 64 / 128 kernel (MUSA SDK guide, "FlashAttention
+// 优化", "FlashAttention 完整算法" steps 1-4: S = Q K^T per key tile, running
+// row max and denominator, O rescaled by exp(m_old - m_new) before P V is
+// added, O / l at the end), with the tile shape the larger head dimension
+// allows (the dataflow page, section 2.1: the block size follows from the
+// on-chip budget; the MUSA guide's block-size table shrinks B_c as d grows).
+//
+// GB300 mapping (one CTA per (batch*head, 128-row Q tile), 6 warps):
+//   warp 4      TMA producer: Q once (4 column blocks of 64), then K_j and V_j
+//               (64 keys x 256 each) into 2-stage rings
+//   warp 5      MMA warp (one elected lane issues): S_j = Q K_j^T (SS,
+//               128 x 64 x 256) into one of two S buffers, O += P_j V_j (TS,
+//               128 x 256 x 64: P from TMEM, V MN-major). S_{j+2} is issued
+//               right behind P_j V_j, whose P it overwrites (one CTA's MMAs
+//               execute in issue order), so the softmax of tile j runs while
+//               S_{j+1} is on the tensor pipe
+//   warps 0-3   softmax (thread = row = TMEM lane): max, lazy rescale of l and
+//               O, P = 2^(s*c - m) packed to 16 bits over the S columns; then
+//               the epilogue
+// TMEM (512 columns): S0 [0,64), S1 [64,128), O [256,512). With one 128-row
+// Q tile per CTA the 256 fp32 O columns fit; two Q tiles would not.
+// SMEM: Q 64 KB + K ring 2 x 32 KB + V ring 2 x 32 KB.
+#include <atomic>
+
+#include "fa_device_common.cuh"
+
+namespace fa {
+namespace {
+
+constexpr float kLog2e256 = 1.4426950408889634f;
+constexpr float kLn2_256 = 0.6931471805599453f;
+constexpr float kRescaleThreshold256 = 8.0f;  // log2 units: P stays <= 2^8
+
+struct C256 {
+  static constexpr int D = 256;
+  static constexpr int BM = 128;  // Q rows per CTA (TMEM lanes)
+  static constexpr int BN = kD256BlockKV;  // keys per K/V tile
+  static constexpr int STAGES = 2;
+  static constexpr uint32_t ROW = 128;                  // one 128-byte swizzle row = 64 elements
+  static constexpr uint32_t Q_BLOCK = BM * ROW;         // 64 columns of the Q tile (16 KB)
+  static constexpr uint32_t Q_BYTES = 4 * Q_BLOCK;      // 64 KB
+  static constexpr uint32_t KV_BLOCK = BN * ROW;        // 64 columns of a K or V tile (8 KB)
+  static constexpr uint32_t KV_BYTES = 4 * KV_BLOCK;    // 32 KB
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;
+  static constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + STAGES, B_VF = B_KE + STAGES, B_VE = B_VF + STAGES;
+  static constexpr int B_SF = B_VE + STAGES, B_PF = B_SF + 2, B_OD = B_PF + 2, B_DRAIN = B_OD + 1;
+  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t T_O = 256;
+  static constexpr int THREADS = 192;
+  static constexpr int WARP_TMA = 4, WARP_MMA = 5;
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ uint32_t bar256(uint32_t base, int i) { return base + C256::OFF_BAR + 8u * i; }
+__device__ __forceinline__ uint32_t t_s256(int buf) { return 64u * buf; }
+
+// A descriptor the compiler must treat as computed here, so that unrolled
+// k-loops do not make it hoist every k-step's descriptor into registers.
+__device__ __forceinline__ uint64_t opaque256(uint64_t x) {
+  asm volatile("" : "+l"(x));
+  return x;
+}
+
+// --------------------------------------------------------------------------
+// TMA producer (one thread)
+// --------------------------------------------------------------------------
+__device__ __forceinline__ void producer256(const FwdParams& p, uint32_t base, int bh, int row0, int nkv,
+                                            const WaitCtl& ctl) {
+  using C = C256;
+  tma_prefetch_desc(&p.tm_q);
+  tma_prefetch_desc(&p.tm_k);
+  tma_prefetch_desc(&p.tm_v);
+  tma_prefetch_desc(&p.tm_o);
+  if (nkv == 0) return;  // no key to see: the epilogue writes zeros into the Q buffer
+  const uint32_t bq = bar256(base, C::B_Q);
+  mbar_arrive_expect_tx(bq, C::Q_BYTES);
+#pragma unroll
+  for (int h = 0; h < 4; ++h) tma_load_3d(base + C::OFF_Q + h * C::Q_BLOCK, &p.tm_q, bq, 64 * h, row0, bh);
+  int nk = 0, nv = 0;
+  bool ok = true;
+  for (int j = 0; j < nkv; ++j) {
+    const int s = j % C::STAGES;
+    const uint32_t par = ((j / C::STAGES) & 1) ^ 1;
+    if (!wait_bar(bar256(base, C::B_KE + s), par, ctl, kWhereKEmpty)) { ok = false; break; }
+    const uint32_t kf = bar256(base, C::B_KF + s);
+    mbar_arrive_expect_tx(kf, C::KV_BYTES);
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+      tma_load_3d(base + C::OFF_K + s * C::KV_BYTES + h * C::KV_BLOCK, &p.tm_k, kf, 64 * h, j * C::BN, bh);
+    nk = j + 1;
+    if (!wait_bar(bar256(base, C::B_VE + s), par, ctl, kWhereVEmpty)) { ok = false; break; }
+    const uint32_t vf = bar256(base, C::B_VF + s);
+    mbar_arrive_expect_tx(vf, C::KV_BYTES);
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+      tma_load_3d(base + C::OFF_V + s * C::KV_BYTES + h * C::KV_BLOCK, &p.tm_v, vf, 64 * h, j * C::BN, bh);
+    nv = j + 1;
+  }
+  if (!ok) {
+    wait_bar_drain(bq, 0, ctl);
+    for (int t = nk > C::STAGES ? nk - C::STAGES : 0; t < nk; ++t)
+      wait_bar_drain(bar256(base, C::B_KF + t % C::STAGES), (t / C::STAGES) & 1, ctl);
+    for (int t = nv > C::STAGES ? nv - C::STAGES : 0; t < nv; ++t)
+      wait_bar_drain(bar256(base, C::B_VF + t % C::STAGES), (t / C::STAGES) & 1, ctl);
+  }
+}
+
+// --------------------------------------------------------------------------
+// MMA warp (whole warp; one elected lane issues)
+// --------------------------------------------------------------------------
+template <bool BF16>
+__device__ __forceinline__ void mma256(uint32_t base, uint32_t tmem, int nkv, const WaitCtl& ctl) {
+  using C = C256;
+  constexpr uint32_t fmt = BF16 ? 1u : 0u;
+  constexpr uint32_t idesc_qk = make_idesc(fmt, 0, 0, 128, C::BN);  // S: A = Q, B = K tile, both K-major
+  constexpr uint32_t idesc_pv = make_idesc(fmt, 0, 1, 128, C::D);   // O += P V: V MN-major, N = 256
+  const uint32_t b_od = bar256(base, C::B_OD), b_drain = bar256(base, C::B_DRAIN);
+
+  // S_j = Q K_j^T into S buffer j % 2 (16 k-steps over d = 256).
+  auto issue_s = [&](int j) {
+    const int s = j % C::STAGES;
+    const uint64_t a0 = opaque256(smem_desc_sw128(base + C::OFF_Q, 16, 1024));
+    const uint64_t b0 = opaque256(smem_desc_sw128(base + C::OFF_K + s * C::KV_BYTES, 16, 1024));
+#pragma unroll
+    for (int kk = 0; kk < C::D / 16; ++kk) {
+      const uint32_t aoff = ((kk / 4) * C::Q_BLOCK + (kk & 3) * 32u) >> 4;
+      const uint32_t boff = ((kk / 4) * C::KV_BLOCK + (kk & 3) * 32u) >> 4;
+      mma_f16_ss_elect(tmem + t_s256(j & 1), a0 + aoff, b0 + boff, idesc_qk, kk > 0 ? 1u : 0u);
+    }
+    tc_commit_elect(bar256(base, C::B_SF + (j & 1)));
+    tc_commit_elect(bar256(base, C::B_KE + s));
+  };
+
+  if (nkv == 0) goto drain;
+  if (!wait_bar_warp(bar256(base, C::B_Q), 0, ctl, kWhereQ)) goto drain;
+  for (int j = 0; j < nkv && j < 2; ++j) {
+    if (!wait_bar_warp(bar256(base, C::B_KF + j % C::STAGES), (j / C::STAGES) & 1, ctl, kWhereKFull)) goto drain;
+    tc_fence_after();
+    issue_s(j);
+  }
+  for (int j = 0; j < nkv; ++j) {
+    // O += P_j V_j (4 k-steps of 16 keys; the four 64-wide d blocks of V are 8 KB apart)
+    const int s = j % C::STAGES;
+    if (!wait_bar_warp(bar256(base, C::B_VF + s), (j / C::STAGES) & 1, ctl, kWhereVFull)) goto drain;
+    if (!wait_bar_warp(bar256(base, C::B_PF + (j & 1)), (j / 2) & 1, ctl, kWherePFull)) goto drain;
+    tc_fence_after();
+    {
+      const uint64_t b0 = opaque256(smem_desc_sw128(base + C::OFF_V + s * C::KV_BYTES, C::KV_BLOCK, 1024));
+#pragma unroll
+      for (int kk = 0; kk < C::BN / 16; ++kk)
+        mma_f16_ts_elect(tmem + C::T_O, tmem + t_s256(j & 1) + kk * 8, b0 + ((kk * 2048u) >> 4), idesc_pv,
+                         (j > 0 || kk > 0) ? 1u : 0u);
+    }
+    tc_commit_elect(b_od);
+    tc_commit_elect(bar256(base, C::B_VE + s));
+    // S_{j+2} into the columns of P_j, right behind the P_j V_j that reads them.
+    if (j + 2 < nkv) {
+#ifdef FA_STRICT_MMA_ORDER
+      if (!wait_bar_warp(b_od, j & 1, ctl, kWhereODone)) goto drain;
+#endif
+      const int n = j + 2;
+      if (!wait_bar_warp(bar256(base, C::B_KF + n % C::STAGES), (n / C::STAGES) & 1, ctl, kWhereKFull)) goto drain;
+      tc_fence_after();
+      issue_s(n);
+    }
+  }
+drain:
+  tc_commit_elect(b_drain);
+  __all_sync(0xffffffffu, wait_bar_drain(b_drain, 0, ctl));
+}
+
+// --------------------------------------------------------------------------
+// Softmax + lazy correction + epilogue (warps 0-3)
+// --------------------------------------------------------------------------
+template <bool BF16>
+__device__ __forceinline__ void softmax256(const FwdParams& p, uint32_t base, uint32_t tmem, int bh, int row0,
+                                           int nkv, int key_end, const WaitCtl& ctl) {
+  using C = C256;
+  const int t = threadIdx.x;
+  const int lane = t & 31;
+  const uint32_t lane_base = static_cast<uint32_t>(t & ~31) << 16;
+  const uint32_t t_o = tmem + lane_base + C::T_O;
+  const float c = p.scale * kLog2e256;
+  const int my_row = row0 + t;
+  const int row_end = p.causal ? min(key_end, my_row + 1) : key_end;
+  const uint32_t b_od = bar256(base, C::B_OD);
+  float m_ref = -INFINITY, l = 0.f, l_o = 0.f;
+  bool ok = true;
+
+  for (int j = 0; j < nkv; ++j) {
+    const uint32_t t_s = tmem + lane_base + t_s256(j & 1);
+    if (!__all_sync(0xffffffffu, wait_bar(bar256(base, C::B_SF + (j & 1)), (j / 2) & 1, ctl, kWhereSFull))) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    uint32_t sraw[2][32];
+    tmem_ld32(t_s, sraw[0]);
+    tmem_ld32(t_s + 32, sraw[1]);
+    tmem_ld_wait();
+    reg_fence(sraw[0]);
+    reg_fence(sraw[1]);
+    float s[C::BN];
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+      s[u] = __uint_as_float(sraw[0][u]);
+      s[32 + u] = __uint_as_float(sraw[1][u]);
+    }
+    const int valid = row_end - j * C::BN;  // keys of this tile this row may see
+    if (valid < C::BN) {
+#pragma unroll
+      for (int u = 0; u < C::BN; ++u)
+        if (u >= valid) s[u] = -INFINITY;
+    }
+    float mxa[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mxa[i] = fmaxf(s[i], s[i + 8]);
+#pragma unroll
+    for (int u = 16; u < C::BN; u += 16)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mxa[i] = fmax3(mxa[i], s[u + i], s[u + 8 + i]);
+    const float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
+                           fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
+    const float m_new = fmaxf(m_ref, mx * c);
+    bool rescale_o = false;
+    float alpha = 1.f;
+    if (j == 0) {
+      m_ref = m_new;
+    } else if (__any_sync(0xffffffffu, m_new - m_ref > kRescaleThreshold256)) {
+      alpha = ex2_approx(m_ref - m_new);
+      m_ref = m_new;
+      l *= alpha;
+      l_o *= alpha;
+      rescale_o = true;
+    }
+    const float2 c2 = make_float2(c, c);
+    const float2 nm2 = make_float2(-m_ref, -m_ref);
+    float2 se = make_float2(0.f, 0.f), sro = se;
+#pragma unroll
+    for (int q = 0; q < C::BN / 16; ++q) {
+      uint32_t pk[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float2 x = __ffma2_rn(make_float2(s[16 * q + 2 * u], s[16 * q + 2 * u + 1]), c2, nm2);
+        const float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        se = __fadd2_rn(se, pr);
+        pk[u] = pack2<BF16>(pr.x, pr.y);
+        if constexpr (BF16)
+          sro = __fadd2_rn(sro, make_float2(__uint_as_float(pk[u] << 16), __uint_as_float(pk[u] & 0xFFFF0000u)));
+      }
+      tmem_st8(t_s + 8 * q, pk);  // keys [16q, 16q+16) -> packed columns [8q, 8q+8)
+    }
+    l += se.x + se.y;
+    if constexpr (BF16) l_o += sro.x + sro.y;
+    if (rescale_o) {
+      // O complete up to tile j-1 before it is read and scaled.
+      if (!__all_sync(0xffffffffu, wait_bar(b_od, (j - 1) & 1, ctl, kWhereODone))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll 1
+      for (int q = 0; q < C::D / 32; ++q) {
+        uint32_t r[32];
+        tmem_ld32(t_o + 32 * q, r);
+        tmem_ld_wait();
+        reg_fence(r);
+#pragma unroll
+        for (int u = 0; u < 32; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * alpha);
+        tmem_st32(t_o + 32 * q, r);
+      }
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar256(base, C::B_PF + (j & 1)));
+  }
+  if (ok && nkv > 0) ok = __all_sync(0xffffffffu, wait_bar(b_od, (nkv - 1) & 1, ctl, kWhereODone));
+  if (!named_bar_and(1, 128, ok)) return;
+
+  // ---- epilogue: O / l -> dtype -> swizzled staging (Q buffer) -> TMA store; LSE ----
+  tc_fence_after();
+  const bool empty = nkv == 0;
+  const float inv_l = empty ? 0.f : 1.0f / (BF16 ? l_o : l);
+  const uint32_t stage = base + C::OFF_Q;
+#pragma unroll 1
+  for (int q = 0; q < C::D / 32; ++q) {
+    uint32_t r[32];
+    tmem_ld32(t_o + 32 * q, r);
+    tmem_ld_wait();
+    reg_fence(r);
+    if (empty) {
+#pragma unroll
+      for (int u = 0; u < 32; ++u) r[u] = 0u;  // TMEM O was never written
+    }
+    uint32_t pk[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      pk[u] = pack2<BF16>(__uint_as_float(r[2 * u]) * inv_l, __uint_as_float(r[2 * u + 1]) * inv_l);
+    const uint32_t blk = q / 2, chunk0 = (q & 1) * 4;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t phys = (chunk0 + u) ^ (static_cast<uint32_t>(t) & 7u);
+      const uint32_t addr = stage + blk * C::Q_BLOCK + t * C::ROW + phys * 16;
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * u]), "r"(pk[4 * u + 1]),
+                   "r"(pk[4 * u + 2]), "r"(pk[4 * u + 3])
+                   : "memory");
+    }
+  }
+  fence_proxy_async_smem();
+  named_bar_sync(1, 128);
+  if (t == 0) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) tma_store_3d(&p.tm_o, stage + h * C::Q_BLOCK, 64 * h, row0, bh);
+    tma_store_commit();
+    tma_store_wait_all();
+  }
+  if (my_row < p.N)
+    p.lse[static_cast<size_t>(bh) * p.N + my_row] = empty ? -INFINITY : (m_ref + lg2_approx(l)) * kLn2_256;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(C256::THREADS, 1) fa_fwd_d256_kernel(const __grid_constant__ FwdParams p) {
+  using C = C256;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem_raw + (base - raw) + C::OFF_MISC);
+  const int warp = threadIdx.x >> 5;
+  const int nqb = (p.N + C::BM - 1) / C::BM;
+  const int bh = blockIdx.x / nqb;
+  // Causal: Q tiles later in the sequence see more keys; they are launched first.
+  const int qb = p.causal ? nqb - 1 - static_cast<int>(blockIdx.x % nqb) : static_cast<int>(blockIdx.x % nqb);
+  const int row0 = qb * C::BM;
+  const int key_end = p.klen ? max(0, min(p.N, p.klen[bh / p.H])) : p.N;
+  const int end = p.causal ? min(key_end, row0 + C::BM) : key_end;
+  const int nkv = (end + C::BN - 1) / C::BN;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar256(base, C::B_Q), 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar256(base, C::B_KF + s), 1);
+      mbar_init(bar256(base, C::B_KE + s), 1);
+      mbar_init(bar256(base, C::B_VF + s), 1);
+      mbar_init(bar256(base, C::B_VE + s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar256(base, C::B_SF + i), 1);
+      mbar_init(bar256(base, C::B_PF + i), 4);  // one arrival per softmax warp
+    }
+    mbar_init(bar256(base, C::B_OD), 1);
+    mbar_init(bar256(base, C::B_DRAIN), 1);
+    misc[1] = 0;
+    mbar_init_fence();
+  }
+  if (warp == C::WARP_MMA) {
+    tmem_alloc(base + C::OFF_MISC, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const WaitCtl ctl{p, base + C::OFF_MISC + 4};
+
+  if (warp == C::WARP_TMA) {
+    if ((threadIdx.x & 31) == 0) producer256(p, base, bh, row0, nkv, ctl);
+    __syncwarp();
+  } else if (warp == C::WARP_MMA) {
+    mma256<BF16>(base, tmem, nkv, ctl);
+    __syncwarp();
+  } else {
+    softmax256<BF16>(p, base, tmem, bh, row0, nkv, key_end, ctl);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <bool BF16>
+cudaError_t launch256(const FwdParams& p, cudaStream_t stream) {
+  using C = C256;
+  auto kern = fa_fwd_d256_kernel<BF16>;
+  static std::atomic<uint64_t> attr_done{0};  // one bit per device ordinal (< 64)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_done.load() & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done.fetch_or(bit);
+  }
+  const long long units = static_cast<long long>(p.B) * p.H * ((p.N + C::BM - 1) / C::BM);
+  if (units <= 0 || units > 0x7fffffffLL) return cudaErrorInvalidValue;
+  kern<<<dim3(static_cast<unsigned>(units)), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_d256(const FwdParams& p, bool bf16, cudaStream_t stream) {
+  return bf16 ? launch256<true>(p, stream) : launch256<false>(p, stream);
+}
+
+}  // namespace fa

@@ -85,6 +85,8 @@ struct alignas(64) BwdParams {
 // Tile sizes of the fp16/bf16 kernel: Q rows per sub-tile (two sub-tiles per
 // CTA) and keys per K/V tile; the host encodes the TMA boxes with them.
 constexpr int kF16BlockQ = 128, kF16BlockKV = 128;
+// Keys per K/V tile of the d = 256 kernel (its K and V TMA boxes are this many rows).
+constexpr int kD256BlockKV = 64;
 
 // Timeline trace layout of the testing build.
 constexpr int kTraceCtas = 8, kTraceTiles = 64, kTraceEvents = 32;
@@ -113,6 +115,8 @@ cudaError_t launch_merge(const FwdParams& p, bool bf16, cudaStream_t stream);
 // Backward: row statistics (D, LSE * log2 e) and a zeroed dQ accumulator;
 // the main dK/dV/dQ kernel; the dQ accumulator rounded into dQ.
 cudaError_t launch_bwd_f16(const BwdParams& p, bool bf16, cudaStream_t stream);
+// Launch the 16-bit forward kernel for head dimension 256 (no split-KV).
+cudaError_t launch_fwd_d256(const FwdParams& p, bool bf16, cudaStream_t stream);
 // Launch the fp32 (3 x TF32) forward kernel.
 cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);
 

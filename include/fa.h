@@ -39,7 +39,7 @@ typedef enum {
     FA_ERR_NULL = 1,           /* a required pointer is NULL                         */
     FA_ERR_DTYPE = 2,          /* dtype is not one of fa_dtype                       */
     FA_ERR_SHAPE = 3,          /* B, H or N < 1, or B*H*N*d overflows 2^40 elements  */
-    FA_ERR_HEADDIM = 4,        /* d is not 64 or 128                                 */
+    FA_ERR_HEADDIM = 4,        /* d is not 64 or 128 (or 256, 16-bit forward only)   */
     FA_ERR_ALIGN = 5,          /* a base pointer is not 16-byte aligned              */
     FA_ERR_CUDA = 6,           /* a CUDA runtime/driver call failed (launch, query)  */
     FA_ERR_DEVICE_TIMEOUT = 7, /* a kernel gave up waiting on a pipeline barrier     */
@@ -59,7 +59,9 @@ typedef enum {
  *             O has the same dtype as Q. O must not alias Q, K or V.
  * LSE:        device pointer to a [B, H, N] contiguous fp32 array: natural-log
  *             logsumexp of each scaled score row, ln sum_j exp(scale * q_i.k_j).
- * d:          64 or 128.
+ * d:          64 or 128; 256 for FA_F16 / FA_BF16 (a kernel with one 128-row Q
+ *             tile per CTA and 64-key K/V tiles: the MUSA guide's block-size
+ *             table shrinks the key block as d grows).
  * scale:      multiplies q.k before the softmax (1/sqrt(d) is the usual value);
  *             must be finite and > 0.
  * dtype:      FA_F32, FA_F16 or FA_BF16. For FA_F16/FA_BF16 both matrix

@@ -73,7 +73,9 @@ A = 1 << 20  # a 16-byte aligned fake address: validation fails before it is use
     ((A, A, A, A, A, 1, 1, 0, 64, 0.125, fa.FA_F16), fa.FA_ERR_SHAPE),
     ((A, A, A, A, A, 1, -3, 64, 64, 0.125, fa.FA_F16), fa.FA_ERR_SHAPE),
     ((A, A, A, A, A, 1, 1, 64, 96, 0.125, fa.FA_F16), fa.FA_ERR_HEADDIM),
-    ((A, A, A, A, A, 1, 1, 64, 256, 0.125, fa.FA_BF16), fa.FA_ERR_HEADDIM),
+    ((A, A, A, A, A, 1, 1, 64, 256, 0.125, fa.FA_F32), fa.FA_ERR_HEADDIM),
+    ((A, A, A, A, A, 1, 1, 64, 512, 0.125, fa.FA_BF16), fa.FA_ERR_HEADDIM),
+    ((A, A, A, A, A, 1, 1, 64, 192, 0.125, fa.FA_F16), fa.FA_ERR_HEADDIM),
     ((A, A, A, A, A, 1, 1, 64, 64, 0.0, fa.FA_F16), fa.FA_ERR_SCALE),
     ((A, A, A, A, A, 1, 1, 64, 64, float("nan"), fa.FA_F16), fa.FA_ERR_SCALE),
     ((A, A, A, A, A, 1, 1, 64, 64, -1.0, fa.FA_F16), fa.FA_ERR_SCALE),
@@ -142,3 +144,10 @@ def test_backward_argument_errors_return_before_launch(L, change, code):
     a.update(change)
     assert fa.fa_bwd(a["Q"], a["K"], a["V"], a["O"], a["dO"], a["LSE"], a["dQ"], a["dK"], a["dV"], a["B"], a["H"],
                      a["N"], a["d"], a["scale"], a["dtype"], a["ws"], a["ws_bytes"], None) == code
+
+
+def test_d256_split_queries(L):
+    """d = 256 runs unsplit: the automatic split count is 1 and no workspace is needed."""
+    assert fa.fa_fwd_splitkv_num_splits(1, 8, 16384, 256) == 1
+    assert fa.fa_fwd_splitkv_workspace_size(1, 8, 16384, 256, 4) == 0
+    assert fa.fa_bwd_workspace_size(1, 8, 1024, 256) == 0  # the backward takes d = 64 / 128 only

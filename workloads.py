@@ -13,11 +13,13 @@ Recipe (the same bytes go to both sides):
   * rounded once to the workload dtype with round-to-nearest-even
     (numpy ``astype`` for fp16, torch CPU ``.to(torch.bfloat16)`` for bf16).
 
-The five workloads are the shapes, dtypes and value distributions on which the
+The workloads are the shapes, dtypes and value distributions on which the
 method is measured: a tiny fp32 case for single-tile bring-up, a short fp16
 case, a mid-size fp16 case (the worked throughput example on the dataflow page,
 B=8, H=12, L=2048, d=128), a large bf16 case whose Q and K have sigma 3 so that
-row maxima keep jumping between key tiles, and a long-sequence bf16 case.
+row maxima keep jumping between key tiles, a long-sequence bf16 case, and a
+head-dimension-256 bf16 case (the MUSA guide's block-size table goes up to
+d = 256).
 """
 from __future__ import annotations
 
@@ -67,6 +69,7 @@ WORKLOADS = {
         Workload("b8h12n2048d128_f16", 3, 8, 12, 2048, 128, "f16"),
         Workload("b8h32n4096d128_bf16_qk3", 4, 8, 32, 4096, 128, "bf16", sigma_qk=3.0),
         Workload("b1h8n16384d128_bf16", 5, 1, 8, 16384, 128, "bf16"),
+        Workload("b4h16n4096d256_bf16", 6, 4, 16, 4096, 256, "bf16"),
     ]
 }
 WORKLOAD_ORDER = list(WORKLOADS)
