@@ -30,8 +30,14 @@ sys.path.insert(0, ROOT)
 
 DEFAULT_WORKLOAD = "b8h32n4096d128_bf16_qk3"
 FALLBACK_TFLOPS = 1900.0  # bf16 dense burst measured once on a GB300 (used only if no measured file)
-KERNEL_SOURCES = ["exact_attention_87_gb300/csrc/fa_fwd_f16.cu", "exact_attention_87_gb300/csrc/sm103_ptx.cuh",
-                  "exact_attention_87_gb300/csrc/fa_device_common.cuh"]
+COMMON_SOURCES = ["exact_attention_87_gb300/csrc/sm103_ptx.cuh", "exact_attention_87_gb300/csrc/fa_device_common.cuh",
+                  "exact_attention_87_gb300/csrc/fa_internal.h"]
+# The source files of the kernel each timed path spends its time in.
+KERNEL_SOURCES = {
+    "fwd": ["exact_attention_87_gb300/csrc/fa_fwd_f16.cu"] + COMMON_SOURCES,
+    "fwd_d256": ["exact_attention_87_gb300/csrc/fa_fwd_d256.cu"] + COMMON_SOURCES,
+    "bwd": ["exact_attention_87_gb300/csrc/fa_bwd_f16.cu"] + COMMON_SOURCES,
+}
 
 
 def log(*a):
@@ -48,23 +54,23 @@ def peaks():
         return FALLBACK_TFLOPS, "fallback", {}
 
 
-def kernel_hash() -> str:
+def kernel_hash(kind: str = "fwd") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, kind: str = "fwd"):
     """dram read+write bytes per launch from the committed ncu summary, if it
     was taken on the current kernel source; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
-        ent = rec.get(workload)
-        if ent and ent.get("kernel_hash") == kernel_hash():
+        ent = rec.get(workload if kind == "fwd" else f"{workload}:{kind}")
+        if ent and ent.get("kernel_hash") == kernel_hash(kind):
             return float(ent["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -313,7 +319,8 @@ def main():
 
     peak, peak_src, _ = peaks()
     achieved = flops / (ms * 1e-3) / 1e12
-    traffic = recorded_traffic(w.name)
+    kind = "fwd_d256" if w.d == 256 else "fwd"
+    traffic = recorded_traffic(w.name, kind) if not args.causal and args.splits == 1 else None
     line = {
         "metric": "attention fwd TFLOP/s (4*B*H*N^2*d) and % of GB300 dense BF16 tensor peak",
         "value": round(tflops, 2),
@@ -331,7 +338,8 @@ def main():
         "pct_of_peak": round(100.0 * achieved / peak, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                     "kernel": f"fa_fwd_f16_kernel<{w.d},{'bf16' if w.dtype == 'bf16' else 'f16'}>",
+                     "kernel": (f"fa_fwd_d256_kernel<{'bf16' if w.dtype == 'bf16' else 'f16'}>" if w.d == 256 else
+                                f"fa_fwd_f16_kernel<{w.d},{'bf16' if w.dtype == 'bf16' else 'f16'}>"),
                      "traffic": traffic, "algorithmic_bytes": w.hbm_bytes},
         "clocks": sampler.summary(),
         "gpu_launches": args.steps * (2 if args.splits != 1 and n_splits > 1 else 1),
@@ -452,7 +460,8 @@ def run_backward(args, w, cfg, ws, rank, local):
         "pct_of_peak": round(100.0 * achieved / peak, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                     "kernel": "whole step: fa_bwd_pre + fa_bwd_main + fa_bwd_post", "traffic": None,
+                     "kernel": "whole step: fa_bwd_pre + fa_bwd_main + fa_bwd_post",
+                     "traffic": recorded_traffic(w.name, "bwd"),
                      "algorithmic_bytes": 8 * w.B * w.H * w.N * w.d * es + 4 * w.B * w.H * w.N},
         "clocks": sampler.summary(),
         "gpu_launches": 3 * args.steps,
