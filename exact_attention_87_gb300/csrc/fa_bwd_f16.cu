@@ -413,8 +413,8 @@ __device__ __forceinline__ void store_acc_tile(uint32_t t_acc, uint32_t stage, i
 // dS^T; at the end dV (W = 0) or dK (W = 1)
 // --------------------------------------------------------------------------
 template <int D, bool BF16, int W>
-__device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint32_t base, uint32_t tmem, int bh, int kv0, int nq,
-                                            const BCtl& ctl) {
+__device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint8_t* smem, uint32_t base, uint32_t tmem, int bh,
+                                            int kv0, int nq, const BCtl& ctl) {
   using C = BCfg<D>;
   constexpr int BAR = 1 + W;  // this warpgroup's named barrier
   const int t = threadIdx.x - 128 * W;  // key row = TMEM lane
@@ -428,14 +428,17 @@ __device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint32_t base, u
   const uint32_t b_sf = bbar<D>(base, C::B_SF), b_dpf = bbar<D>(base, C::B_DPF);
   const uint32_t b_pf = bbar<D>(base, C::B_PF), b_dsf = bbar<D>(base, C::B_DSF);
   const uint32_t b_dse = bbar<D>(base, C::B_DSE);
-  const uint32_t ds_half = base + C::OFF_DS + W * C::HALF;  // this warpgroup's half of dS^T
+  // Row t of this warpgroup's half of dS^T (128-byte swizzle: 16-byte chunk c sits at c ^ (t & 7)).
+  uint4* ds_row = reinterpret_cast<uint4*>(smem + C::OFF_DS + W * C::HALF + t * C::ROW);
   bool ok = true;
   float ps[64];  // P*scale of this thread's key for queries [64W, 64W+64) of the current tile
 
   // Every wait is agreed by the whole warpgroup (bar.red.and): its epilogue
   // needs all 128 threads at the same named barriers.
   for (int i = 0; i < nq; ++i) {
-    const uint32_t rows = base + C::OFF_ROWS + (i % C::QST) * C::ROWS_BYTES;  // lse2[128], dsum[128]
+    // lse2[128], dsum[128] of Q tile i, read as plain shared-memory loads (the compiler schedules them freely)
+    const float4* lse4 = reinterpret_cast<const float4*>(smem + C::OFF_ROWS + (i % C::QST) * C::ROWS_BYTES) + 16 * W;
+    const float4* dsum4 = lse4 + 32;
     // ---- P_i: S^T columns -> fp32 P (kept, times scale) and 16-bit P^T in TMEM
     if (!named_bar_and(BAR, 128, wait_bar(b_sf, i & 1, ctl, kWhereBwdSFull))) { ok = false; break; }
     if (W == 0 && t == 0) FA_TRACE(p, kBvSmS, i);
@@ -452,10 +455,7 @@ __device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint32_t base, u
       uint32_t pk[16];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        float4 l4;
-        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(l4.x), "=f"(l4.y), "=f"(l4.z), "=f"(l4.w)
-                     : "r"(rows + (64 * W + 32 * q + 4 * u) * 4));
+        const float4 l4 = lse4[8 * q + u];
         const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1])), c2,
                                      make_float2(-l4.x, -l4.y));
         const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])),
@@ -501,10 +501,7 @@ __device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint32_t base, u
       uint32_t pk[16];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        float4 d4;
-        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(d4.x), "=f"(d4.y), "=f"(d4.z), "=f"(d4.w)
-                     : "r"(rows + 512 + (64 * W + 32 * q + 4 * u) * 4));
+        const float4 d4 = dsum4[8 * q + u];
         const float2 e0 = __fadd2_rn(make_float2(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1])),
                                      make_float2(-d4.x, -d4.y));
         const float2 e1 = __fadd2_rn(make_float2(__uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])),
@@ -517,9 +514,7 @@ __device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint32_t base, u
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const uint32_t phys = (4 * q + u) ^ (static_cast<uint32_t>(t) & 7u);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ds_half + t * C::ROW + phys * 16),
-                     "r"(pk[4 * u]), "r"(pk[4 * u + 1]), "r"(pk[4 * u + 2]), "r"(pk[4 * u + 3])
-                     : "memory");
+        ds_row[phys] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
       }
       if (W == 0 && t == 0) FA_TRACE(p, q == 0 ? kBvSmDsChunk0 : kBvSmDsChunk1, i);
     }
@@ -665,10 +660,10 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1) fa_bwd_main_kernel(const 
     bwd_dq<D>(p, base, tmem, bh, nq, ctl);
   } else if (warp >= 4) {
     warpgroup_reg_alloc<C::SM_REGS>();
-    bwd_softmax<D, BF16, 1>(p, base, tmem, bh, kv0, nq, ctl);
+    bwd_softmax<D, BF16, 1>(p, smem_raw, base, tmem, bh, kv0, nq, ctl);
   } else {
     warpgroup_reg_alloc<C::SM_REGS>();
-    bwd_softmax<D, BF16, 0>(p, base, tmem, bh, kv0, nq, ctl);
+    bwd_softmax<D, BF16, 0>(p, smem_raw, base, tmem, bh, kv0, nq, ctl);
   }
 
   tc_fence_before();

@@ -36,17 +36,12 @@ static __device__ __forceinline__ void record_timeout(const P& p, uint32_t abort
   asm volatile("st.volatile.shared.s32 [%0], %1;" ::"r"(abort_addr), "r"(1) : "memory");
 }
 
-// Longest a waiting thread stays suspended per poll of its barrier (it wakes
-// as soon as the phase completes); between polls the abort flag and the wait
-// limit are checked.
-constexpr uint32_t kWaitSleepNs = 20000;
-
 template <class Ctl>
 __device__ __forceinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, const Ctl& ctl, unsigned where,
                                               bool honour_abort) {
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (honour_abort && abort_raised(ctl.abort_addr)) return false;
     if (clock64() - t0 > ctl.p.wait_limit) {
       record_timeout(ctl.p, ctl.abort_addr, where);
