@@ -45,6 +45,11 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8
+#ifdef FA_STRICT_MMA_ORDER
+constexpr bool kOdEveryTile = true;   // every P.V committed to o_done (S waits for it)
+#else
+constexpr bool kOdEveryTile = false;  // only the last P.V of a sub-tile
+#endif
 
 template <int D>
 struct Cfg {
@@ -211,7 +216,10 @@ __device__ __forceinline__ void mma_warp(const FwdParams& p, uint32_t base, uint
       for (int kk = 0; kk < C::BN / 16; ++kk)
         mma_f16_ts_elect(d_o, d_s + kk * 8, v0 + ((kk * 16 * C::ROW_BYTES) >> 4), idesc_pv,
                          (j > 1 || kk > 0) ? 1u : 0u);
-      tc_commit_elect(b_od);
+      // The softmax learns that P(j-1) V_{j-1} is complete from the commit that
+      // follows S(j) (same warp, issued after it); only the last P.V, which no
+      // S follows, is committed on its own (strict order: every P.V is).
+      if (kOdEveryTile || j == nkv) tc_commit_elect(b_od);
       tc_commit_elect(bar_addr<D>(base, C::B_VE + s));
       FA_TRACE(p, kEvPV0Issued + sub, j - 1);
     }
@@ -357,8 +365,11 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
     l += se.x + se.y;
     if constexpr (BF16) l_o += sro.x + sro.y;
     if (rescale_o) {
-      // O must be complete up to tile j-1 (its P.V finished) before it is read and scaled.
-      if (!__all_sync(0xffffffffu, wait_bar(b_od, (j - 1) & 1, ctl, kWhereODone))) {
+      // O must be complete up to tile j-1 (its P.V finished) before it is read
+      // and scaled. P(j-1) V_{j-1} was issued before S(j) by the same warp, so
+      // the S(j) completion waited for above covers it; the strict build
+      // commits and waits for every P.V.
+      if (kOdEveryTile && !__all_sync(0xffffffffu, wait_bar(b_od, (j - 1) & 1, ctl, kWhereODone))) {
         ok = false;
         break;
       }
@@ -392,7 +403,7 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
   }
   // The last P.V of this sub-tile; its commit also covers every earlier MMA of the warp.
   if (ok && nkv > 0)
-    ok = __all_sync(0xffffffffu, wait_bar(b_od, (nkv - 1) & 1, ctl, kWhereODone));
+    ok = __all_sync(0xffffffffu, wait_bar(b_od, kOdEveryTile ? (nkv - 1) & 1 : 0, ctl, kWhereODone));
   // The whole warpgroup agrees before the epilogue, whose named barrier needs all 128 threads.
   if (!named_bar_and(1 + sub, 128, ok)) return;
 
