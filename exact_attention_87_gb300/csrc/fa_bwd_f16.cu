@@ -25,14 +25,16 @@
 // and queries for dQ):
 //   warp 12     TMA producer: K_j, V_j once; Q_i (+ its LSE and D rows) into a
 //               2-stage ring; dO_i into a 1-stage (d=128) / 2-stage (d=64) ring
-//   warp 13     MMA warp (one elected lane issues), per Q tile i:
+//   warps 13-14 MMA warps (one elected lane issues), per Q tile i:
 //                 S^T  = K_j Q_i^T   (SS)           -> TMEM [0,128)
 //                 dP^T = V_j dO_i^T  (SS)           -> TMEM [128,256)
 //                 dV  += P^T dO_i    (TS: P^T from TMEM, dO MN-major)
 //                 dK  += dS^T Q_i    (SS: dS^T from SMEM, Q MN-major)
 //                 dQ_i = dS K_j      (SS: dS^T read MN-major, K MN-major)
-//               issued in blocks  dV_i dP_i S_{i+1} dK_i dQ_i, so that S_{i+1}
-//               runs while dS_i is formed and dV_{i+1} while dQ_i is read out
+//               warp 13 issues dQ_i, dK_i as soon as dS_i is formed; warp 14
+//               issues dP^T_{i+1}, dV_{i+1}, S^T_{i+2}, so that S^T_{i+2} runs
+//               while dS_{i+1} is formed and each warp's waits and commits
+//               overlap the other's MMAs
 //   warps 0-3   queries 0-63 of every Q tile, warps 4-7 queries 64-127 (one
 //   and 4-7     thread per key): P = 2^(s*scale*log2e - LSE*log2e) in fp32,
 //               written back as 16-bit pairs over S^T columns [0,32) / [64,96)
@@ -45,9 +47,9 @@
 //               reduce-adds on the accumulator. The reduce-adds (64 KB per Q
 //               tile for d=128) drain at the SM's write rate to L2, so they
 //               run beside the other roles instead of in their chain.
-//   warps 14-15 idle (they complete the fourth warpgroup)
+//   warp 15     idle (completes the fourth warpgroup)
 // Registers: launched at 128 per thread; warpgroups 0-2 grow to 160 / 160 /
-// 152 and warpgroup 3 shrinks to 40 (setmaxnreg).
+// 144 and warpgroup 3 shrinks to 48 (setmaxnreg).
 // TMEM (512 columns): S^T [0,128), dP^T [128,256), dV [256,256+d),
 // dK [256+d,256+2d); dQ_i reuses the dP^T columns for d=128 (dP^T_i is
 // consumed once dS_i is written; dP^T_{i+1} waits for the read-out of dQ_i)
@@ -92,8 +94,7 @@ struct BCfg {
   static constexpr int B_OF = B_QE + QST, B_OE = B_OF + OST;
   static constexpr int B_SF = B_OE + OST, B_DPF = B_SF + 1, B_PF = B_DPF + 1, B_DSF = B_PF + 1;
   static constexpr int B_DQF = B_DSF + 1, B_DQE = B_DQF + 1, B_DSE = B_DQE + 1, B_DONE = B_DSE + 1;
-  static constexpr int B_PROBE = B_DONE + 1;  // testing build: one commit per product, stamped by warp 14
-  static constexpr int NBAR = B_PROBE + 1;
+  static constexpr int NBAR = B_DONE + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
   // The dynamic shared memory starts 1 KB-aligned (checked in the kernel): no slack.
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
@@ -101,7 +102,7 @@ struct BCfg {
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
   static constexpr uint32_t T_DQ = (D == 128) ? 128 : 384;
   static constexpr int THREADS = 512;
-  static constexpr int WARP_TMA = 12, WARP_MMA = 13;
+  static constexpr int WARP_TMA = 12, WARP_MMA = 13, WARP_MMA_SP = 14;
   static constexpr int LAUNCH_REGS = 128, SM_REGS = 160, DQ_REGS = 144, LOW_REGS = 48;
   static_assert(128 * (2 * SM_REGS + DQ_REGS + LOW_REGS) <= THREADS * LAUNCH_REGS, "register split exceeds the pool");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -202,55 +203,103 @@ __device__ __forceinline__ void mma_kmajor_tiles(uint32_t d_tmem, uint32_t a_bas
   }
 }
 
+// Two MMA warps feed the one tensor pipe, so that the waits and commits of
+// one (each leaves the pipe idle for about a hundred cycles when nothing else
+// is queued: it holds about one MMA) overlap the other's MMAs:
+//   warp 13: dQ_i, dK_i                  (both need dS_i)
+//   warp 14: S^T_0, dP^T_0, dV_0, S^T_1, then dP^T_{i+1}, dV_{i+1}, S^T_{i+2}
+// Each keeps its own products in order (S^T_{i+2} overwrites P^T_{i+1} right
+// behind dV_{i+1} in warp 14); everything between the two warps goes through
+// mbarriers.
 template <int D, bool BF16>
-__device__ __forceinline__ void bwd_mma(const BwdParams& p, uint32_t base, uint32_t tmem, int nq, const BCtl& ctl) {
+struct BwdMma {
   using C = BCfg<D>;
-  constexpr uint32_t fmt = BF16 ? 1u : 0u;
-  constexpr uint32_t idesc_st = make_idesc(fmt, 0, 0, 128, 128);  // S^T, dP^T: M = keys, N = queries
-  constexpr uint32_t idesc_acc = make_idesc(fmt, 0, 1, 128, D);   // dV, dK: B (dO, Q) has d contiguous
-  constexpr uint32_t idesc_dq = make_idesc(fmt, 1, 1, 128, D);    // dQ: A = dS read M-major, B = K
+  static constexpr uint32_t fmt = BF16 ? 1u : 0u;
+  static constexpr uint32_t idesc_st = make_idesc(fmt, 0, 0, 128, 128);  // S^T, dP^T: M = keys, N = queries
+  static constexpr uint32_t idesc_acc = make_idesc(fmt, 0, 1, 128, D);   // dV, dK: B (dO, Q) has d contiguous
+  static constexpr uint32_t idesc_dq = make_idesc(fmt, 1, 1, 128, D);    // dQ: A = dS read M-major, B = K
   // MN-major operands: 16 K-rows = two 8-row swizzle atoms (2048 bytes); the
   // 64-wide MN blocks are LBO apart (a tile's halves; the dS^T halves for A).
-  constexpr uint32_t lbo_d = (D == 64) ? 1024u : C::HALF;
-  const uint32_t b_sf = bbar<D>(base, C::B_SF), b_dpf = bbar<D>(base, C::B_DPF);
-  const uint32_t b_pf = bbar<D>(base, C::B_PF), b_dsf = bbar<D>(base, C::B_DSF);
-  const uint32_t b_dqf = bbar<D>(base, C::B_DQF), b_dqe = bbar<D>(base, C::B_DQE);
+  static constexpr uint32_t lbo_d = (D == 64) ? 1024u : C::HALF;
+};
+
+// Warp 13: the two products that need dS_i.
+template <int D, bool BF16>
+__device__ __forceinline__ void bwd_mma_dsdep(const BwdParams& p, uint32_t base, uint32_t tmem, int nq,
+                                              const BCtl& ctl) {
+  using C = BCfg<D>;
+  using M = BwdMma<D, BF16>;
+  const uint32_t b_dsf = bbar<D>(base, C::B_DSF), b_dqf = bbar<D>(base, C::B_DQF), b_dqe = bbar<D>(base, C::B_DQE);
   const uint32_t b_dse = bbar<D>(base, C::B_DSE), b_done = bbar<D>(base, C::B_DONE);
   const uint64_t dq_a0 = smem_desc_sw128(base + C::OFF_DS, C::HALF, 1024);
-  const uint64_t dq_b0 = smem_desc_sw128(base + C::OFF_K, lbo_d, 1024);
+  const uint64_t dq_b0 = smem_desc_sw128(base + C::OFF_K, M::lbo_d, 1024);
   const uint64_t dk_a0 = smem_desc_sw128(base + C::OFF_DS, 16, 1024);
-#ifdef FA_TESTING
-  // Testing build with a timeline: a commit after every product of the loop,
-  // whose completions warp 14 stamps (the probe costs nothing otherwise).
-#define FA_PROBE_COMMIT()                                                         \
-  do {                                                                            \
-    if (p.timeline && blockIdx.x < kTraceCtas) tc_commit_elect(bbar<D>(base, C::B_PROBE)); \
-  } while (0)
-#else
-#define FA_PROBE_COMMIT() \
-  do {                    \
-  } while (0)
-#endif
+  for (int i = 0; i < nq; ++i) {
+    if (!wait_bar_warp(b_dsf, i & 1, ctl, kWhereBwdDsFull)) break;
+    if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDQReady, i);
+    if constexpr (D == 64) {
+      // dQ_{i-1} must have left its TMEM columns.
+      if (i > 0 && !wait_bar_warp(b_dqe, (i - 1) & 1, ctl, kWhereBwdDqEmpty)) break;
+    }
+    tc_fence_after();
+    {
+      const uint64_t a0 = opaque(dq_a0), b0 = opaque(dq_b0);
+#pragma unroll
+      for (int kk = 0; kk < C::BK / 16; ++kk)
+        mma_f16_ss_elect(tmem + C::T_DQ, a0 + ((kk * 2048u) >> 4), b0 + ((kk * 2048u) >> 4), M::idesc_dq,
+                         kk > 0 ? 1u : 0u);
+    }
+    tc_commit_elect(b_dqf);
+    if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDQ, i);
+    {
+      const uint64_t b0 = opaque(smem_desc_sw128(base + C::OFF_Q + (i % C::QST) * C::TILE, M::lbo_d, 1024));
+      const uint64_t a0 = opaque(dk_a0);
+#pragma unroll
+      for (int kk = 0; kk < C::BQ / 16; ++kk) {
+        const uint32_t aoff = ((kk / 4) * C::HALF + (kk & 3) * 32u) >> 4;
+        mma_f16_ss_elect(tmem + C::T_DK, a0 + aoff, b0 + ((kk * 2048u) >> 4), M::idesc_acc,
+                         (i > 0 || kk > 0) ? 1u : 0u);
+      }
+    }
+    tc_commit_elect(bbar<D>(base, C::B_QE + i % C::QST));  // Q_i (and its rows) are free once dK_i is done
+    tc_commit_elect(b_dse);                                // so is the dS^T tile (dQ_i was issued before)
+    if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDK, i);
+  }
+  // One commit after this warp's last MMA (the barrier counts both MMA warps):
+  // the epilogues wait for it, and every MMA completes before TMEM is freed.
+  tc_commit_elect(b_done);
+  __all_sync(0xffffffffu, wait_bar_drain(b_done, 0, ctl));
+}
+
+// Warp 14: S^T, dP^T and dV.
+template <int D, bool BF16>
+__device__ __forceinline__ void bwd_mma_sp(const BwdParams& p, uint32_t base, uint32_t tmem, int nq,
+                                           const BCtl& ctl) {
+  using C = BCfg<D>;
+  using M = BwdMma<D, BF16>;
+  const uint32_t b_sf = bbar<D>(base, C::B_SF), b_dpf = bbar<D>(base, C::B_DPF);
+  const uint32_t b_pf = bbar<D>(base, C::B_PF), b_dsf = bbar<D>(base, C::B_DSF);
+  const uint32_t b_dqe = bbar<D>(base, C::B_DQE), b_done = bbar<D>(base, C::B_DONE);
 
   // S^T_j = K Q_j^T into the S^T columns, over P^T_{j-1}, whose dV_{j-1} is issued before.
   auto issue_s = [&](int j) {
-    mma_kmajor_tiles<D>(tmem + C::T_S, base + C::OFF_K, base + C::OFF_Q + (j % C::QST) * C::TILE, idesc_st);
+    mma_kmajor_tiles<D>(tmem + C::T_S, base + C::OFF_K, base + C::OFF_Q + (j % C::QST) * C::TILE, M::idesc_st);
     tc_commit_elect(b_sf);
   };
   // dP^T_j = V dO_j^T
   auto issue_dp = [&](int j) {
-    mma_kmajor_tiles<D>(tmem + C::T_DP, base + C::OFF_V, base + C::OFF_DO + (j % C::OST) * C::TILE, idesc_st);
+    mma_kmajor_tiles<D>(tmem + C::T_DP, base + C::OFF_V, base + C::OFF_DO + (j % C::OST) * C::TILE, M::idesc_st);
     tc_commit_elect(b_dpf);
   };
   // dV += P^T_j dO_j (K = the 128 queries of tile j). P^T of queries 0-63 is
   // packed in S^T columns [0,32), of queries 64-127 in [64,96). dO_j is free
   // afterwards (its dP^T_j was issued before).
   auto issue_dv = [&](int j) {
-    const uint64_t b0 = opaque(smem_desc_sw128(base + C::OFF_DO + (j % C::OST) * C::TILE, lbo_d, 1024));
+    const uint64_t b0 = opaque(smem_desc_sw128(base + C::OFF_DO + (j % C::OST) * C::TILE, M::lbo_d, 1024));
 #pragma unroll
     for (int kk = 0; kk < C::BQ / 16; ++kk)
       mma_f16_ts_elect(tmem + C::T_DV, tmem + C::T_S + (kk < 4 ? 8 * kk : 64 + 8 * (kk - 4)),
-                       b0 + ((kk * 2048u) >> 4), idesc_acc, (j > 0 || kk > 0) ? 1u : 0u);
+                       b0 + ((kk * 2048u) >> 4), M::idesc_acc, (j > 0 || kk > 0) ? 1u : 0u);
     tc_commit_elect(bbar<D>(base, C::B_OE + j % C::OST));
   };
 
@@ -274,104 +323,43 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, uint32_t base, uint3
     tc_fence_after();
     issue_s(1);
   }
-
-  // Block i: dQ_i, dK_i (both need dS_i), dP^T_{i+1} (while dS_i's products run,
-  // so that dS_{i+1} can start as early as possible), dV_{i+1}, S^T_{i+2}.
-  for (int i = 0; i < nq; ++i) {
-    if (!wait_bar_warp(b_dsf, i & 1, ctl, kWhereBwdDsFull)) goto drain;
-    if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDQReady, i);
-    if constexpr (D == 64) {
-      // dQ_{i-1} must have left its TMEM columns.
-      if (i > 0 && !wait_bar_warp(b_dqe, (i - 1) & 1, ctl, kWhereBwdDqEmpty)) goto drain;
+  for (int i = 0; i + 1 < nq; ++i) {
+    const int n1 = i + 1;
+    // dP^T_{i+1} overwrites the dP^T columns: the softmax warps must be done with
+    // dP^T_i, and for d = 128 the dQ warps with dQ_i (which implies the former).
+    if constexpr (D == 128) {
+      if (!wait_bar_warp(b_dqe, i & 1, ctl, kWhereBwdDqEmpty)) goto drain;
+    } else {
+      if (!wait_bar_warp(b_dsf, i & 1, ctl, kWhereBwdDsFull)) goto drain;
     }
+    if (!wait_bar_warp(bbar<D>(base, C::B_OF + n1 % C::OST), (n1 / C::OST) & 1, ctl, kWhereBwdDoFull)) goto drain;
+    if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDPReady, n1);
     tc_fence_after();
-    {
-      const uint64_t a0 = opaque(dq_a0), b0 = opaque(dq_b0);
-#pragma unroll
-      for (int kk = 0; kk < C::BK / 16; ++kk)
-        mma_f16_ss_elect(tmem + C::T_DQ, a0 + ((kk * 2048u) >> 4), b0 + ((kk * 2048u) >> 4), idesc_dq,
-                         kk > 0 ? 1u : 0u);
-    }
-    tc_commit_elect(b_dqf);
-    FA_PROBE_COMMIT();
-    if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDQ, i);
-    {
-      const uint64_t b0 = opaque(smem_desc_sw128(base + C::OFF_Q + (i % C::QST) * C::TILE, lbo_d, 1024));
-      const uint64_t a0 = opaque(dk_a0);
-#pragma unroll
-      for (int kk = 0; kk < C::BQ / 16; ++kk) {
-        const uint32_t aoff = ((kk / 4) * C::HALF + (kk & 3) * 32u) >> 4;
-        mma_f16_ss_elect(tmem + C::T_DK, a0 + aoff, b0 + ((kk * 2048u) >> 4), idesc_acc,
-                         (i > 0 || kk > 0) ? 1u : 0u);
-      }
-    }
-    tc_commit_elect(bbar<D>(base, C::B_QE + i % C::QST));  // Q_i (and its rows) are free once dK_i is done
-    tc_commit_elect(b_dse);                                // so is the dS^T tile (dQ_i was issued before)
-    FA_PROBE_COMMIT();
-    if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDK, i);
-    if (i + 1 < nq) {
-      const int n1 = i + 1;
-      if constexpr (D == 128) {
-        // dQ_i occupies the dP^T columns until the dQ warps have read it.
-        if (!wait_bar_warp(b_dqe, i & 1, ctl, kWhereBwdDqEmpty)) goto drain;
-      }
-      if (!wait_bar_warp(bbar<D>(base, C::B_OF + n1 % C::OST), (n1 / C::OST) & 1, ctl, kWhereBwdDoFull)) goto drain;
-      if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDPReady, n1);
-      tc_fence_after();
-      issue_dp(n1);
-      FA_PROBE_COMMIT();
-      if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDP, n1);
-      if (!wait_bar_warp(b_pf, n1 & 1, ctl, kWhereBwdPFull)) goto drain;
-      if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDVReady, n1);
-      tc_fence_after();
-      issue_dv(n1);
-      FA_PROBE_COMMIT();
-      if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDV, n1);
-    }
+    issue_dp(n1);
+    if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDP, n1);
+    if (!wait_bar_warp(b_pf, n1 & 1, ctl, kWhereBwdPFull)) goto drain;
+    if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDVReady, n1);
+    tc_fence_after();
+    issue_dv(n1);
+    if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvDV, n1);
     if (i + 2 < nq) {
       const int n2 = i + 2;
 #ifdef FA_STRICT_MMA_ORDER
       // dV_{i+1} complete before S^T_{i+2} reuses the P^T columns.
-      if (!wait_bar_warp(bbar<D>(base, C::B_OE + (i + 1) % C::OST), ((i + 1) / C::OST) & 1, ctl, kWhereBwdDoEmpty))
+      if (!wait_bar_warp(bbar<D>(base, C::B_OE + n1 % C::OST), (n1 / C::OST) & 1, ctl, kWhereBwdDoEmpty))
         goto drain;
 #endif
       if (!wait_bar_warp(bbar<D>(base, C::B_QF + n2 % C::QST), (n2 / C::QST) & 1, ctl, kWhereBwdQFull)) goto drain;
       if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvSReady, n2);
       tc_fence_after();
       issue_s(n2);
-      FA_PROBE_COMMIT();
       if (threadIdx.x % 32 == 0) FA_TRACE(p, kBvS, n2);
     }
   }
 drain:
-  // One commit after the last MMA: the epilogues wait for it, and every MMA
-  // completes before the CTA frees TMEM or exits.
   tc_commit_elect(b_done);
   __all_sync(0xffffffffu, wait_bar_drain(b_done, 0, ctl));
-#undef FA_PROBE_COMMIT
 }
-
-#ifdef FA_TESTING
-// Testing build: stamp the completion of every product the MMA warp commits
-// to the probe barrier, in issue order: dQ_i, dK_i, dP_{i+1}, dV_{i+1}, S_{i+2}.
-template <int D>
-__device__ __forceinline__ void bwd_probe(const BwdParams& p, uint32_t base, int nq, const BCtl& ctl) {
-  if (!(p.timeline && blockIdx.x < kTraceCtas)) return;
-  const uint32_t bar = bbar<D>(base, BCfg<D>::B_PROBE);
-  uint32_t phase = 0;
-  for (int i = 0; i < nq; ++i) {
-    const int events[5] = {kBvDoneDQ, kBvDoneDK, kBvDoneDP, kBvDoneDV, kBvDoneS};
-    const int tile[5] = {i, i, i + 1, i + 1, i + 2};
-    const bool made[5] = {true, true, i + 1 < nq, i + 1 < nq, i + 2 < nq};
-    for (int e = 0; e < 5; ++e) {
-      if (!made[e]) continue;
-      if (!wait_bar(bar, phase & 1, ctl, kWhereDrain)) return;
-      ++phase;
-      FA_TRACE(p, events[e], tile[e]);
-    }
-  }
-}
-#endif
 
 // Store a 128 x D fp32 TMEM accumulator (this thread's lane = row t) as a
 // 16-bit tile through the swizzled staging buffer `stage` with TMA.
@@ -624,8 +612,7 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1) fa_bwd_main_kernel(const 
     mbar_init(bbar<D>(base, C::B_DQF), 1);
     mbar_init(bbar<D>(base, C::B_DQE), 4);  // one arrival per dQ warp
     mbar_init(bbar<D>(base, C::B_DSE), 1);
-    mbar_init(bbar<D>(base, C::B_DONE), 1);
-    mbar_init(bbar<D>(base, C::B_PROBE), 1);
+    mbar_init(bbar<D>(base, C::B_DONE), 2);  // one commit per MMA warp
     misc[1] = 0;
     mbar_init_fence();
   }
@@ -646,15 +633,12 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1) fa_bwd_main_kernel(const 
       if ((threadIdx.x & 31) == 0) bwd_producer<D>(p, base, bh, kv0, nq, ctl);
       __syncwarp();
     } else if (warp == C::WARP_MMA) {
-      bwd_mma<D, BF16>(p, base, tmem, nq, ctl);
+      bwd_mma_dsdep<D, BF16>(p, base, tmem, nq, ctl);
+      __syncwarp();
+    } else if (warp == C::WARP_MMA_SP) {
+      bwd_mma_sp<D, BF16>(p, base, tmem, nq, ctl);
       __syncwarp();
     }
-#ifdef FA_TESTING
-    else if (warp == C::WARP_MMA + 1) {
-      if ((threadIdx.x & 31) == 0) bwd_probe<D>(p, base, nq, ctl);
-      __syncwarp();
-    }
-#endif
   } else if (warp >= 8) {
     warpgroup_reg_alloc<C::DQ_REGS>();
     bwd_dq<D>(p, base, tmem, bh, nq, ctl);

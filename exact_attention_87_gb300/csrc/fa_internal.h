@@ -104,8 +104,7 @@ enum : int {
 enum : int {
   kBvDV = 0, kBvDP, kBvS, kBvDK, kBvDQ, kBvSmS, kBvSmP, kBvSmDq, kBvSmRed, kBvSmDp, kBvSmDs, kBvSmDsFree,
   kBvSmDqLoaded, kBvCta, kBvW1P, kBvW1Ds, kBvDVReady, kBvDPReady, kBvSReady, kBvDKReady, kBvDQReady, kBvQLoad,
-  kBvDOLoad, kBvSmPChunk0, kBvSmDsWaited, kBvSmDsChunk0, kBvSmDsChunk1, kBvDoneDQ, kBvDoneDK, kBvDoneDP, kBvDoneDV,
-  kBvDoneS
+  kBvDOLoad, kBvSmPChunk0, kBvSmDsWaited, kBvSmDsChunk0, kBvSmDsChunk1
 };
 
 // Launch the 16-bit (fp16 / bf16) forward kernel for head dimension p.d.
