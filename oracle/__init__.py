@@ -67,6 +67,11 @@ def _bind(path: str):
     lp = ctypes.POINTER(ctypes.c_long)
     lib.oracle_bwd_rows_fp64.argtypes = [dp, dp, dp, dp, dp, dp, L, L, L, D, lp, L, dp, lp, L, dp, dp]
     lib.oracle_bwd_rows_fp64.restype = I
+    lib.oracle_attn_bwd_masked_fp64.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, L, L, L, D, I, lp, L, I]
+    lib.oracle_attn_bwd_masked_fp64.restype = I
+    lib.oracle_bwd_rows_masked_fp64.argtypes = [dp, dp, dp, dp, dp, dp, L, L, L, D, I, lp, L, lp, L, dp, lp, L,
+                                                dp, dp]
+    lib.oracle_bwd_rows_masked_fp64.restype = I
     lib.oracle_merge_fp64.argtypes = [dp, dp, L, L, L, dp, dp]
     lib.oracle_merge_fp64.restype = I
     lib.oracle_mutant_id.restype = I
@@ -181,27 +186,51 @@ def attn_masked(q, k, v, causal: bool = False, klen=None, scale: float | None = 
     return o, lse
 
 
-def attn_bwd(q, k, v, o, do, lse, scale: float | None = None, nthreads: int | None = None, lib=None):
+def _klen_arg(klen, B):
+    """(array kept alive, C pointer) for per-batch key lengths; NULL pointer for None."""
+    lp = ctypes.POINTER(ctypes.c_long)
+    if klen is None:
+        return None, lp()
+    kl = np.ascontiguousarray(np.asarray(klen, dtype=np.int64).reshape(-1))
+    if kl.shape != (B,):
+        raise ValueError("klen must hold one length per batch")
+    return kl, kl.ctypes.data_as(lp)
+
+
+def attn_bwd(q, k, v, o, do, lse, scale: float | None = None, nthreads: int | None = None, lib=None,
+             causal: bool = False, klen=None):
     """Backward pass by recomputation: (dQ, dK, dV) fp64 for q, k, v, do [..., N, d], with the
-    forward outputs o [..., N, d] and lse [..., N]."""
+    forward outputs o [..., N, d] and lse [..., N].
+
+    With masks (``causal``; ``klen``: B key lengths, arrays [B, H, N, d]) a
+    masked score is -inf, so its P_ij and dS_ij are exactly 0: masked keys get
+    zero dK, dV and contribute nothing to dQ; a row with no key (LSE = -inf,
+    O = 0) gets dQ = 0."""
     q, k, v, o, do, lse = (_f64(t) for t in (q, k, v, o, do, lse))
     lead, BH, N, Nk, d = _shapes(q, k, v)
     if Nk != N or o.shape != q.shape or do.shape != q.shape or lse.shape != q.shape[:-1]:
         raise ValueError("attn_bwd wants square attention and matching o / do / lse")
+    if klen is not None and q.ndim != 4:
+        raise ValueError("attn_bwd with klen wants [B, H, N, d] arrays")
+    B, H = (q.shape[0], q.shape[1]) if q.ndim == 4 else (BH, 1)
     scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
     dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    kl, klp = _klen_arg(klen, B)
     lib = lib or load()
-    rc = lib.oracle_attn_bwd_fp64(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
-                                  _ptr(dv), BH, N, d, scale, nthreads or default_threads())
+    rc = lib.oracle_attn_bwd_masked_fp64(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                                         _ptr(dk), _ptr(dv), BH, N, d, scale, int(bool(causal)), klp, H,
+                                         nthreads or default_threads())
     if rc != 0:
-        raise RuntimeError(f"oracle_attn_bwd_fp64 failed ({rc})")
+        raise RuntimeError(f"oracle_attn_bwd_masked_fp64 failed ({rc})")
     return dq, dk, dv
 
 
-def attn_bwd_rows(q, k, v, o, do, lse, dq_rows, dkv_rows, scale: float | None = None, lib=None):
+def attn_bwd_rows(q, k, v, o, do, lse, dq_rows, dkv_rows, scale: float | None = None, lib=None,
+                  causal: bool = False, klen=None):
     """Selected rows of the backward pass: dQ at (b, h, i) in ``dq_rows`` and
     dK, dV at (b, h, j) in ``dkv_rows``; o and lse must be the forward results
-    for every row of the heads named. Returns (dq [n_dq, d], dk, dv [n_dkv, d])."""
+    for every row of the heads named. Returns (dq [n_dq, d], dk, dv [n_dkv, d]).
+    ``causal`` and ``klen`` are the masks of ``attn_bwd``."""
     q, k, v, o, do, lse = (_f64(t) for t in (q, k, v, o, do, lse))
     B, H, N, d = q.shape
     scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
@@ -214,12 +243,13 @@ def attn_bwd_rows(q, k, v, o, do, lse, dq_rows, dkv_rows, scale: float | None = 
     dq = np.empty((len(a_q), d))
     dk, dv = np.empty((len(a_kv), d)), np.empty((len(a_kv), d))
     lp = ctypes.POINTER(ctypes.c_long)
+    kl, klp = _klen_arg(klen, B)
     lib = lib or load()
-    rc = lib.oracle_bwd_rows_fp64(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), B * H, N, d, scale,
-                                  a_q.ctypes.data_as(lp), len(a_q), _ptr(dq), a_kv.ctypes.data_as(lp), len(a_kv),
-                                  _ptr(dk), _ptr(dv))
+    rc = lib.oracle_bwd_rows_masked_fp64(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), B * H, N, d,
+                                         scale, int(bool(causal)), klp, H, a_q.ctypes.data_as(lp), len(a_q),
+                                         _ptr(dq), a_kv.ctypes.data_as(lp), len(a_kv), _ptr(dk), _ptr(dv))
     if rc != 0:
-        raise RuntimeError(f"oracle_bwd_rows_fp64 failed ({rc})")
+        raise RuntimeError(f"oracle_bwd_rows_masked_fp64 failed ({rc})")
     return dq, dk, dv
 
 

@@ -26,7 +26,8 @@
  *
  * oracle_attn_bwd_fp64 is the backward pass (gradients of Q, K, V for a given
  * dO) written out from the chain rule on the same definition, P recomputed
- * from the saved LSE.
+ * from the saved LSE; oracle_attn_bwd_masked_fp64 is the same with the causal
+ * and key-length masks.
  *
  * ORACLE_MUTANT (compile-time, default 0) plants one deliberate mistake so
  * the pin tests can show that each such mistake is caught. Mutant builds are
@@ -356,6 +357,10 @@ int oracle_attn_masked_fp64(const double *Q, const double *K, const double *V, d
  *     dK_j  = scale * sum_i dS_ij q_i
  * O and LSE are the forward outputs passed in (from the oracle itself).
  * Layouts as oracle_attn_fp64 (Nq = Nk = N); dQ/dK/dV like Q/K/V.
+ * The masked variant takes the masks of oracle_attn_masked_fp64: a masked
+ * score is -inf, so P_ij = 0 there (set directly, not through exp of the
+ * saved LSE, which is -inf on a row with no key); every sum above then runs
+ * over the allowed (i, j) only.
  */
 typedef struct {
     const double *Q, *K, *V, *O, *dO, *LSE;
@@ -364,6 +369,11 @@ typedef struct {
     double scale;
     long bh_begin, bh_end;
     int ok;
+    /* masks of the masked definition: causal (key j <= query i) and per-batch
+     * key lengths klen[b] (keys j >= klen[b] masked; NULL = none); H heads per batch */
+    int causal;
+    const long *klen;
+    long H;
 } bjob_t;
 
 static void *bwd_worker(void *arg)
@@ -378,6 +388,12 @@ static void *bwd_worker(void *arg)
         const double *Q = jb->Q + bh * N * d, *K = jb->K + bh * N * d, *V = jb->V + bh * N * d;
         const double *O = jb->O + bh * N * d, *dO = jb->dO + bh * N * d, *L = jb->LSE + bh * N;
         double *dQ = jb->dQ + bh * N * d, *dK = jb->dK + bh * N * d, *dV = jb->dV + bh * N * d;
+        long key_end = N;
+        if (jb->klen) {
+            key_end = jb->klen[bh / jb->H];
+            if (key_end < 0) key_end = 0;
+            if (key_end > N) key_end = N;
+        }
         for (long i = 0; i < N; ++i) {
             double acc = 0.0;
             for (long c = 0; c < d; ++c) acc += dO[i * d + c] * O[i * d + c];
@@ -388,7 +404,13 @@ static void *bwd_worker(void *arg)
                     s += Q[i * d + c] * K[j * d + c];
                     dp += dO[i * d + c] * V[j * d + c];
                 }
-                P[i * N + j] = exp(jb->scale * s - L[i]);
+                /* a masked score is -inf: its P is exactly 0 (and a row with no key has no P at all) */
+#if ORACLE_MUTANT == 11 /* backward causal mask off by one: the diagonal key dropped */
+                const int allowed = j < key_end && (!jb->causal || j < i);
+#else
+                const int allowed = j < key_end && (!jb->causal || j <= i);
+#endif
+                P[i * N + j] = allowed ? exp(jb->scale * s - L[i]) : 0.0;
 #if ORACLE_MUTANT == 8 /* the D_i term dropped from dS */
                 dS[i * N + j] = P[i * N + j] * dp;
 #else
@@ -426,9 +448,9 @@ static void *bwd_worker(void *arg)
     return NULL;
 }
 
-int oracle_attn_bwd_fp64(const double *Q, const double *K, const double *V, const double *O, const double *dO,
-                         const double *LSE, double *dQ, double *dK, double *dV, long BH, long N, long d,
-                         double scale, int nthreads)
+int oracle_attn_bwd_masked_fp64(const double *Q, const double *K, const double *V, const double *O,
+                                const double *dO, const double *LSE, double *dQ, double *dK, double *dV, long BH,
+                                long N, long d, double scale, int causal, const long *klen, long H, int nthreads)
 {
     if (BH < 0 || N < 1 || d < 1) return -1;
     if (BH == 0) return 0;
@@ -441,7 +463,7 @@ int oracle_attn_bwd_fp64(const double *Q, const double *K, const double *V, cons
     long per = (BH + nthreads - 1) / nthreads;
     for (int t = 0; t < nthreads; ++t) {
         bjob_t j = {Q, K, V, O, dO, LSE, dQ, dK, dV, N, d, scale, t * per,
-                    (t + 1) * per < BH ? (t + 1) * per : BH, 0};
+                    (t + 1) * per < BH ? (t + 1) * per : BH, 0, causal, klen, H < 1 ? 1 : H};
         jobs[t] = j;
         started[t] = 0;
         if (jobs[t].bh_begin >= jobs[t].bh_end) { jobs[t].ok = 1; continue; }
@@ -457,26 +479,38 @@ int oracle_attn_bwd_fp64(const double *Q, const double *K, const double *V, cons
     return 0;
 }
 
+int oracle_attn_bwd_fp64(const double *Q, const double *K, const double *V, const double *O, const double *dO,
+                         const double *LSE, double *dQ, double *dK, double *dV, long BH, long N, long d,
+                         double scale, int nthreads)
+{
+    return oracle_attn_bwd_masked_fp64(Q, K, V, O, dO, LSE, dQ, dK, dV, BH, N, d, scale, 0, NULL, 1, nthreads);
+}
+
 /*
  * Single rows of the backward pass, same definitions and summation orders as
  * oracle_attn_bwd_fp64: dQ rows given as (bh, i) pairs, dK/dV rows as (bh, j)
  * pairs. Each row costs O(N d); O and LSE must cover every row of the heads
  * named. Outputs are [n, d].
  */
-int oracle_bwd_rows_fp64(const double *Q, const double *K, const double *V, const double *O, const double *dO,
-                         const double *LSE, long BH, long N, long d, double scale, const long *dq_rows, long n_dq,
-                         double *dQ, const long *dkv_rows, long n_dkv, double *dK, double *dV)
+int oracle_bwd_rows_masked_fp64(const double *Q, const double *K, const double *V, const double *O,
+                                const double *dO, const double *LSE, long BH, long N, long d, double scale,
+                                int causal, const long *klen, long H, const long *dq_rows, long n_dq, double *dQ,
+                                const long *dkv_rows, long n_dkv, double *dK, double *dV)
 {
     if (N < 1 || d < 1) return -1;
     for (long r = 0; r < n_dq; ++r) {
         long bh = dq_rows[2 * r], i = dq_rows[2 * r + 1];
         if (bh < 0 || bh >= BH || i < 0 || i >= N) return -1;
         const double *q = Q + (bh * N + i) * d, *o = O + (bh * N + i) * d, *g = dO + (bh * N + i) * d;
+        long key_end = klen ? klen[bh / (H < 1 ? 1 : H)] : N;
+        if (key_end < 0) key_end = 0;
+        if (key_end > N) key_end = N;
+        if (causal && key_end > i + 1) key_end = i + 1;
         double Di = 0.0;
         for (long c = 0; c < d; ++c) Di += g[c] * o[c];
         double *out = dQ + r * d;
         for (long c = 0; c < d; ++c) out[c] = 0.0;
-        for (long j = 0; j < N; ++j) {
+        for (long j = 0; j < key_end; ++j) {
             const double *kj = K + (bh * N + j) * d, *vj = V + (bh * N + j) * d;
             double sc = 0.0, dp = 0.0;
             for (long c = 0; c < d; ++c) {
@@ -494,7 +528,9 @@ int oracle_bwd_rows_fp64(const double *Q, const double *K, const double *V, cons
         const double *kj = K + (bh * N + j) * d, *vj = V + (bh * N + j) * d;
         double *ok = dK + r * d, *ov = dV + r * d;
         for (long c = 0; c < d; ++c) ok[c] = ov[c] = 0.0;
-        for (long i = 0; i < N; ++i) {
+        long key_end = klen ? klen[bh / (H < 1 ? 1 : H)] : N;
+        if (j >= key_end) continue; /* a masked key gets no gradient */
+        for (long i = causal ? j : 0; i < N; ++i) {
             const double *q = Q + (bh * N + i) * d, *o = O + (bh * N + i) * d, *g = dO + (bh * N + i) * d;
             double Di = 0.0, sc = 0.0, dp = 0.0;
             for (long c = 0; c < d; ++c) {
@@ -512,6 +548,14 @@ int oracle_bwd_rows_fp64(const double *Q, const double *K, const double *V, cons
         for (long c = 0; c < d; ++c) ok[c] *= scale;
     }
     return 0;
+}
+
+int oracle_bwd_rows_fp64(const double *Q, const double *K, const double *V, const double *O, const double *dO,
+                         const double *LSE, long BH, long N, long d, double scale, const long *dq_rows, long n_dq,
+                         double *dQ, const long *dkv_rows, long n_dkv, double *dK, double *dV)
+{
+    return oracle_bwd_rows_masked_fp64(Q, K, V, O, dO, LSE, BH, N, d, scale, 0, NULL, 1, dq_rows, n_dq, dQ,
+                                       dkv_rows, n_dkv, dK, dV);
 }
 
 /*

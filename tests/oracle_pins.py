@@ -262,4 +262,55 @@ def pin_bwd_uniform_attention(lib):
     np.testing.assert_allclose(dk, 0.0 * dk, atol=1e-13)  # q_i = 0 multiplies every term
 
 
+def pin_bwd_masked_finite_differences(lib):
+    """Masked backward (causal, key lengths, both, and a batch with no key at
+    all) against central differences of the masked forward's L = sum(W * O)."""
+    rng = np.random.default_rng(15)
+    B, H, N, d, scale = 3, 2, 8, 4, 0.7
+    q, k, v = (rng.standard_normal((B, H, N, d)) for _ in range(3))
+    w = rng.standard_normal((B, H, N, d))
+    h = 1e-6
+    for causal, klen in ((True, None), (False, [8, 5, 0]), (True, [3, 8, 6])):
+        o, lse = oracle.attn_masked(q, k, v, causal=causal, klen=klen, scale=scale, nthreads=2, lib=lib)
+        dq, dk, dv = oracle.attn_bwd(q, k, v, o, w, lse, scale=scale, nthreads=2, lib=lib, causal=causal,
+                                     klen=klen)
+
+        def loss(qq, kk, vv):
+            oo = oracle.attn_masked(qq, kk, vv, causal=causal, klen=klen, scale=scale, nthreads=2, lib=lib)[0]
+            return float((w * oo).sum())
+
+        for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            for idx in [(0, 0, 0, 0), (0, 1, 4, 2), (1, 0, 7, 3), (1, 1, 5, 1), (2, 0, 2, 0), (2, 1, 6, 3),
+                        (1, 0, 4, 2), (0, 0, 7, 1)]:
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                ap = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+                am = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+                fd = (loss(*ap) - loss(*am)) / (2 * h)
+                assert abs(fd - g[idx]) <= 1e-7 * max(1.0, abs(g[idx])), (causal, klen, name, idx)
+
+
+def pin_bwd_masked_structure(lib):
+    """Causal row 0 sees only key 0 (O_0 = v_0), so dQ_0 = 0 and the last key
+    is seen only by the last query; keys at or past a batch's length get zero
+    dK and dV, and a batch with no key gets zero gradients everywhere."""
+    rng = np.random.default_rng(16)
+    B, H, N, d, scale = 2, 2, 10, 3, 0.9
+    q, k, v, w = (rng.standard_normal((B, H, N, d)) for _ in range(4))
+    o, lse = oracle.attn_masked(q, k, v, causal=True, scale=scale, nthreads=2, lib=lib)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, o, w, lse, scale=scale, nthreads=2, lib=lib, causal=True)
+    np.testing.assert_allclose(dq[:, :, 0], 0.0, atol=1e-15)
+    last = N - 1
+    p_last = np.exp(scale * np.einsum("bhc,bhc->bh", q[:, :, last], k[:, :, last]) - lse[:, :, last])
+    np.testing.assert_allclose(dv[:, :, last], p_last[..., None] * w[:, :, last], rtol=1e-12, atol=1e-14)
+    klen = [6, 0]
+    o, lse = oracle.attn_masked(q, k, v, klen=klen, scale=scale, nthreads=2, lib=lib)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, o, w, lse, scale=scale, nthreads=2, lib=lib, klen=klen)
+    assert np.all(dk[0, :, 6:] == 0.0) and np.all(dv[0, :, 6:] == 0.0)
+    assert np.all(dq[1] == 0.0) and np.all(dk[1] == 0.0) and np.all(dv[1] == 0.0)
+    # the unmasked keys obey the unmasked invariant: sum_j dV_j = sum_i dO_i
+    np.testing.assert_allclose(dv[0].sum(axis=1), w[0].sum(axis=1), rtol=0, atol=1e-12)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -28,6 +28,7 @@ MUTANTS = {
     8: "backward: D term dropped from dS",
     9: "backward: scale dropped from dK",
     10: "backward: P transposed in dV",
+    11: "backward: causal mask off by one",
 }
 
 
@@ -205,6 +206,23 @@ def test_backward_rows_match_full_backward(oracle_lib):
     dq, dk, dv = oracle.attn_bwd(q, k, v, o, w, lse, scale=scale)
     rows = [(0, 0, 0), (1, 1, 36), (0, 1, 17), (1, 0, 5)]
     rq, rk, rv = oracle.attn_bwd_rows(q, k, v, o, w, lse, rows, rows[::-1], scale=scale)
+    for n, (b, h, i) in enumerate(rows):
+        np.testing.assert_allclose(rq[n], dq[b, h, i], rtol=0, atol=1e-14)
+    for n, (b, h, j) in enumerate(rows[::-1]):
+        np.testing.assert_allclose(rk[n], dk[b, h, j], rtol=0, atol=1e-14)
+        np.testing.assert_allclose(rv[n], dv[b, h, j], rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal,klen", [(True, None), (False, [30, 0]), (True, [17, 37])])
+def test_masked_backward_rows_match_full_backward(oracle_lib, causal, klen):
+    """The sampled-row backward with masks against the full masked backward."""
+    rng = np.random.default_rng(22)
+    B, H, N, d, scale = 2, 2, 37, 8, 0.4
+    q, k, v, w = (rng.standard_normal((B, H, N, d)) * 1.3 for _ in range(4))
+    o, lse = oracle.attn_masked(q, k, v, causal=causal, klen=klen, scale=scale)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, o, w, lse, scale=scale, causal=causal, klen=klen)
+    rows = [(0, 0, 0), (1, 1, 36), (0, 1, 17), (1, 0, 5), (0, 0, 29), (0, 1, 30), (1, 1, 16)]
+    rq, rk, rv = oracle.attn_bwd_rows(q, k, v, o, w, lse, rows, rows[::-1], scale=scale, causal=causal, klen=klen)
     for n, (b, h, i) in enumerate(rows):
         np.testing.assert_allclose(rq[n], dq[b, h, i], rtol=0, atol=1e-14)
     for n, (b, h, j) in enumerate(rows[::-1]):
