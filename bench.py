@@ -363,8 +363,9 @@ def run_backward(args, w, cfg, ws, rank, local):
     import exact_attention_87_gb300 as fa
     from workloads import make_dout, make_inputs
 
-    if args.causal or args.splits != 1:
-        raise SystemExit("--pass bwd takes neither --causal nor --splits")
+    if args.splits != 1:
+        raise SystemExit("--pass bwd does not take --splits")
+    causal = bool(args.causal)
     if ws > 1:
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
@@ -372,20 +373,24 @@ def run_backward(args, w, cfg, ws, rank, local):
     torch.cuda.set_device(dev)
     fa.build()
     fa.lib()
-    flops = 10 * w.B * w.H * w.N * w.N * w.d  # five N x N x d products per (b, h)
-    cfg = dict(cfg, pass_="bwd", flops="10*B*H*N^2*d (S, dP, dV, dK, dQ products)")
+    if causal:  # the five products over the (query, key) pairs each row sees
+        flops = 10 * w.B * w.H * w.d * w.N * (w.N + 1) // 2
+        cfg = dict(cfg, pass_="bwd", flops="10*B*H*d*N*(N+1)/2 (S, dP, dV, dK, dQ over the causal pairs)")
+    else:
+        flops = 10 * w.B * w.H * w.N * w.N * w.d  # five N x N x d products per (b, h)
+        cfg = dict(cfg, pass_="bwd", flops="10*B*H*N^2*d (S, dP, dV, dK, dQ products)")
     cfg["pass"] = cfg.pop("pass_")
     q, k, v = make_inputs(w)
     do = make_dout(w.B, w.H, w.N, w.d, w.dtype, seed=0, wid=w.wid)
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
     stream = torch.cuda.current_stream(dev)
-    o, lse = fa.attention(qd, kd, vd, scale=w.scale, stream=stream)
+    o, lse = fa.attention(qd, kd, vd, scale=w.scale, stream=stream, causal=causal)
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
     wsp = torch.empty(fa.fa_bwd_workspace_size(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
 
     def step():
         fa.attention_backward(qd, kd, vd, o, lse, dod, scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=wsp,
-                              stream=stream)
+                              stream=stream, causal=causal)
 
     for _ in range(args.warmup):
         step()
@@ -424,7 +429,7 @@ def run_backward(args, w, cfg, ws, rank, local):
             for dst, src in ((qd, hq), (kd, hk), (vd, hv), (od, ho), (ld, hl), (dod, hdo)):
                 dst.copy_(src, non_blocking=True)
             fa.attention_backward(qd, kd, vd, od, ld, dod, scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=wsp,
-                                  stream=stream)
+                                  stream=stream, causal=causal)
             for dst, src in zip(hg, (dq, dk, dv)):
                 dst.copy_(src, non_blocking=True)
 
@@ -443,7 +448,8 @@ def run_backward(args, w, cfg, ws, rank, local):
         d2h = sum(t.numel() * t.element_size() for t in hg)
         e2e = {"value": round(job_throughput(ws, flops, e_ms), 2), "unit": "TFLOP/s", "ms_per_step": round(e_ms, 4),
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
-               "path": "pinned host -> cudaMemcpyAsync -> fa_bwd -> cudaMemcpyAsync -> pinned host"}
+               "path": "pinned host -> cudaMemcpyAsync -> " + ("fa_bwd_ex" if causal else "fa_bwd") +
+                       " -> cudaMemcpyAsync -> pinned host"}
     if rank != 0:
         if ws > 1:
             dist.barrier()
@@ -453,7 +459,8 @@ def run_backward(args, w, cfg, ws, rank, local):
     achieved = flops / (ms * 1e-3) / 1e12
     es = 2
     line = {
-        "metric": "attention bwd TFLOP/s (10*B*H*N^2*d) and % of GB300 dense BF16 tensor peak",
+        "metric": ("attention bwd TFLOP/s (" + ("causal, 10*B*H*d*N*(N+1)/2" if causal else "10*B*H*N^2*d") +
+                   ") and % of GB300 dense BF16 tensor peak"),
         "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded, generated on the host)", "config": cfg,
@@ -461,7 +468,7 @@ def run_backward(args, w, cfg, ws, rank, local):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
                      "kernel": "whole step: fa_bwd_pre + fa_bwd_main + fa_bwd_post",
-                     "traffic": recorded_traffic(w.name, "bwd"),
+                     "traffic": None if causal else recorded_traffic(w.name, "bwd"),
                      "algorithmic_bytes": 8 * w.B * w.H * w.N * w.d * es + 4 * w.B * w.H * w.N},
         "clocks": sampler.summary(),
         "gpu_launches": 3 * args.steps,
@@ -475,12 +482,15 @@ def run_backward(args, w, cfg, ws, rank, local):
         while secs < args.cpu_seconds and heads < w.B * w.H:
             b, h = divmod(heads, w.H)
             sl = (b, h, slice(0, n))
-            oh, lh = oracle.attn(q[sl], k[sl], v[sl], scale=w.scale, nthreads=threads)
+            qs, ks, vs = (t[sl].unsqueeze(0).unsqueeze(0) for t in (q, k, v))
+            dos = do[sl].unsqueeze(0).unsqueeze(0)
+            oh, lh = oracle.attn_masked(qs, ks, vs, causal=causal, scale=w.scale, nthreads=threads)
             t0 = time.perf_counter()
-            oracle.attn_bwd(q[sl], k[sl], v[sl], oh, do[sl], lh, scale=w.scale, nthreads=threads)
+            oracle.attn_bwd(qs, ks, vs, oh, dos, lh, scale=w.scale, nthreads=threads, causal=causal)
             secs += time.perf_counter() - t0
             heads += 1
-        line["cpu_baseline"] = {"value": round(heads * 10 * n * n * w.d / secs / 1e12, 6), "unit": "TFLOP/s",
+        per_head = 10 * w.d * (n * (n + 1) // 2 if causal else n * n)
+        line["cpu_baseline"] = {"value": round(heads * per_head / secs / 1e12, 6), "unit": "TFLOP/s",
                                 "cores": 1, "kind": "oracle", "seconds": round(secs, 2),
                                 "sample": f"{heads} heads truncated to their first {n} queries and keys "
                                           "(fp64 backward timed; its O, LSE from the forward oracle, untimed; "

@@ -72,6 +72,8 @@ def lib(path: str | None = None):
     L.fa_fwd_splitkv_workspace_size.restype = u64
     L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, u64, vp]
     L.fa_bwd.restype = i
+    L.fa_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, vp, u64, vp]
+    L.fa_bwd_ex.restype = i
     L.fa_bwd_workspace_size.argtypes = [i, i, i, i]
     L.fa_bwd_workspace_size.restype = u64
     if path == LIB_PATH:
@@ -113,6 +115,12 @@ def fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype, workspace,
            stream=None) -> int:
     return lib().fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype, workspace, workspace_bytes,
                         stream)
+
+
+def fa_bwd_ex(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype, causal, seqlens_k, workspace,
+              workspace_bytes, stream=None) -> int:
+    return lib().fa_bwd_ex(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype, causal, seqlens_k, workspace,
+                           workspace_bytes, stream)
 
 
 def fa_bwd_workspace_size(B, H, N, d) -> int:
@@ -207,12 +215,14 @@ def attention(q, k, v, scale: float | None = None, out=None, lse=None, stream=No
 
 
 def attention_backward(q, k, v, o, lse, do, scale: float | None = None, dq=None, dk=None, dv=None, workspace=None,
-                       stream=None):
+                       stream=None, causal: bool = False, seqlens_k=None):
     """dQ, dK, dV for the forward pass O, LSE = attention(q, k, v, scale) and the
     output gradient do (all [B, H, N, d] contiguous CUDA tensors of one 16-bit
     dtype; lse fp32 [B, H, N]). ``dq``/``dk``/``dv`` may be preallocated; the
     workspace (fa_bwd_workspace_size bytes) is allocated with torch unless a
     CUDA uint8 tensor is given; ``stream`` defaults to torch's current stream.
+    ``causal`` / ``seqlens_k`` (CUDA int32 tensor [B]) are the masks the
+    forward pass was run with (fa_bwd_ex).
     """
     import torch
     for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
@@ -242,15 +252,28 @@ def attention_backward(q, k, v, o, lse, do, scale: float | None = None, dq=None,
         need = fa_bwd_workspace_size(B, H, N, d)
         if workspace is None:
             workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-        rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
-                    dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, float(scale), _dtype_code(q),
-                    workspace.data_ptr(), workspace.numel(), stream)
+        if causal or seqlens_k is not None:
+            kl = None
+            if seqlens_k is not None:
+                if seqlens_k.dtype != torch.int32 or not seqlens_k.is_cuda or seqlens_k.numel() != B:
+                    raise ValueError("seqlens_k must be a CUDA int32 tensor of B lengths")
+                seqlens_k = seqlens_k.contiguous()
+                kl = seqlens_k.data_ptr()
+            rc = fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                           dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, float(scale), _dtype_code(q),
+                           int(bool(causal)), kl, workspace.data_ptr(), workspace.numel(), stream)
+            name = "fa_bwd_ex"
+        else:
+            rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, float(scale), _dtype_code(q),
+                        workspace.data_ptr(), workspace.numel(), stream)
+            name = "fa_bwd"
     if rc != FA_OK:
-        raise FAError(rc, "fa_bwd")
+        raise FAError(rc, name)
     return dq, dk, dv
 
 
-__all__ = ["attention", "attention_backward", "fa_bwd", "fa_bwd_workspace_size", "fa_fwd", "fa_fwd_ex", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_num_splits",
+__all__ = ["attention", "attention_backward", "fa_bwd", "fa_bwd_ex", "fa_bwd_workspace_size", "fa_fwd", "fa_fwd_ex", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_num_splits",
            "fa_fwd_splitkv_workspace_size",
            "fa_get_device_status", "fa_strerror", "fa_abi_version", "build", "lib",
            "FAError", "FA_F32", "FA_F16", "FA_BF16", "FA_OK"]

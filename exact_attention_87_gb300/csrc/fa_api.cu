@@ -358,8 +358,9 @@ unsigned long long bwd_part_bytes(unsigned long long n) { return (n + 255) & ~25
 int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE, void* dQ,
              void* dK, void* dV, int B, int H, int N, int d, float scale, int dtype, void* workspace,
              unsigned long long workspace_bytes, void* stream, int inject, unsigned long long* timeline,
-             long long wait_limit) {
+             long long wait_limit, int causal, const int* seqlens_k) {
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return FA_ERR_NULL;
+  if (causal != 0 && causal != 1) return FA_ERR_SHAPE;
   if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
   if (dtype == FA_F32) return FA_ERR_UNSUPPORTED;
   if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
@@ -394,6 +395,10 @@ int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const v
   p.wait_limit = wait_limit > 0 ? wait_limit : wait_limit_cycles();
   p.inject = inject;
   p.timeline = timeline;
+  p.causal = causal;
+  p.klen = seqlens_k;
+  p.dk = dK;
+  p.dv = dV;
   const unsigned long long acc_bytes = bwd_part_bytes(static_cast<unsigned long long>(BH) * N * d * 4);
   const unsigned long long row_bytes = bwd_part_bytes(static_cast<unsigned long long>(BH) * p.n_pad * 4);
   p.dq_acc = static_cast<float*>(workspace);
@@ -429,7 +434,14 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const voi
            void* dK, void* dV, int B, int H, int N, int d, float scale, int dtype, void* workspace,
            unsigned long long workspace_bytes, void* stream) {
   return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype, workspace, workspace_bytes, stream, 0,
-                  nullptr, 0);
+                  nullptr, 0, 0, nullptr);
+}
+
+int fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE, void* dQ,
+              void* dK, void* dV, int B, int H, int N, int d, float scale, int dtype, int causal,
+              const int* seqlens_k, void* workspace, unsigned long long workspace_bytes, void* stream) {
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype, workspace, workspace_bytes, stream, 0,
+                  nullptr, 0, causal, seqlens_k);
 }
 
 #ifdef FA_TESTING
@@ -438,7 +450,7 @@ int fa_bwd_testing(const void* Q, const void* K, const void* V, const void* O, c
                    unsigned long long workspace_bytes, void* stream, int inject, unsigned long long* timeline,
                    long long wait_limit_cycles) {
   return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype, workspace, workspace_bytes, stream,
-                  inject, timeline, wait_limit_cycles);
+                  inject, timeline, wait_limit_cycles, 0, nullptr);
 }
 #endif
 

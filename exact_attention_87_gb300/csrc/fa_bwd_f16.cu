@@ -58,6 +58,7 @@
 // one CTA's MMAs execute in issue order (-DFA_STRICT_MMA_ORDER waits for dV_i
 // to complete instead).
 #include <atomic>
+#include <type_traits>
 
 #include <cuda_fp16.h>
 
@@ -120,8 +121,8 @@ __device__ __forceinline__ uint32_t bbar(uint32_t base, int i) {
 // TMA producer (one thread)
 // --------------------------------------------------------------------------
 template <int D>
-__device__ __forceinline__ void bwd_producer(const BwdParams& p, uint32_t base, int bh, int kv0, int nq,
-                                             const BCtl& ctl) {
+__device__ __forceinline__ void bwd_producer(const BwdParams& p, uint32_t base, int bh, int kv0, int q_first,
+                                             int nq, const BCtl& ctl) {
   using C = BCfg<D>;
   tma_prefetch_desc(&p.tm_q);
   tma_prefetch_desc(&p.tm_k);
@@ -145,10 +146,10 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint32_t base, 
     mbar_arrive_expect_tx(qf, C::TILE + C::ROWS_BYTES);
 #pragma unroll
     for (int h = 0; h < D / 64; ++h)
-      tma_load_3d(base + C::OFF_Q + qs * C::TILE + h * C::HALF, &p.tm_q, qf, 64 * h, i * C::BQ, bh);
+      tma_load_3d(base + C::OFF_Q + qs * C::TILE + h * C::HALF, &p.tm_q, qf, 64 * h, (q_first + i) * C::BQ, bh);
     const uint32_t rows = base + C::OFF_ROWS + qs * C::ROWS_BYTES;
-    bulk_load(rows, p.lse2 + row_base + static_cast<size_t>(i) * C::BQ, 512, qf);
-    bulk_load(rows + 512, p.dsum + row_base + static_cast<size_t>(i) * C::BQ, 512, qf);
+    bulk_load(rows, p.lse2 + row_base + static_cast<size_t>(q_first + i) * C::BQ, 512, qf);
+    bulk_load(rows + 512, p.dsum + row_base + static_cast<size_t>(q_first + i) * C::BQ, 512, qf);
     nqi = i + 1;
     FA_TRACE(p, kBvQLoad, i);
 #ifdef FA_TESTING
@@ -160,7 +161,7 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint32_t base, 
     mbar_arrive_expect_tx(of, C::TILE);
 #pragma unroll
     for (int h = 0; h < D / 64; ++h)
-      tma_load_3d(base + C::OFF_DO + os * C::TILE + h * C::HALF, &p.tm_do, of, 64 * h, i * C::BQ, bh);
+      tma_load_3d(base + C::OFF_DO + os * C::TILE + h * C::HALF, &p.tm_do, of, 64 * h, (q_first + i) * C::BQ, bh);
     noi = i + 1;
     FA_TRACE(p, kBvDOLoad, i);
   }
@@ -402,7 +403,7 @@ __device__ __forceinline__ void store_acc_tile(uint32_t t_acc, uint32_t stage, i
 // --------------------------------------------------------------------------
 template <int D, bool BF16, int W>
 __device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint8_t* smem, uint32_t base, uint32_t tmem, int bh,
-                                            int kv0, int nq, const BCtl& ctl) {
+                                            int kv0, int nq, int key_end, const BCtl& ctl) {
   using C = BCfg<D>;
   constexpr int BAR = 1 + W;  // this warpgroup's named barrier
   const int t = threadIdx.x - 128 * W;  // key row = TMEM lane
@@ -410,7 +411,15 @@ __device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint8_t* smem, u
   const uint32_t lane_base = static_cast<uint32_t>(t & ~31) << 16;
   const uint32_t t_s = tmem + lane_base + C::T_S + 64 * W, t_dp = tmem + lane_base + C::T_DP + 64 * W;
   const float c = p.scale * kLog2eB;
-  const bool key_ok = kv0 + t < p.N;  // keys past N (zero-filled rows) get P = 0
+  // Masks. Keys at or past key_end (past N, or past the batch's key length)
+  // get P = 0 in every Q tile; with the causal mask the first Q tile is the
+  // diagonal one (same rows as the keys) and query c of it sees key t only if
+  // c >= t. For this thread: P of query column c (0..63 of this half) is 0
+  // when c < lim. A tile with no masked entry skips the test.
+  const bool key_ok = kv0 + t < key_end;
+  const int lim_diag = key_ok ? t - 64 * W : 64;
+  const int lim_rest = key_ok ? 0 : 64;
+  const bool rest_masked = kv0 + C::BK > key_end;
   const float2 c2 = make_float2(c, c);
   const float2 sc2 = make_float2(p.scale, p.scale);
   const uint32_t b_sf = bbar<D>(base, C::B_SF), b_dpf = bbar<D>(base, C::B_DPF);
@@ -437,32 +446,47 @@ __device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint8_t* smem, u
     tmem_ld_wait();
     reg_fence(rs[0]);
     reg_fence(rs[1]);
+    // Two copies of the P loop: the masked one only for tiles with a masked entry.
+    auto p_phase = [&](auto mask_tag, int lim) {
+      constexpr bool kMasked = decltype(mask_tag)::value;
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const uint32_t (&r)[32] = rs[q];
-      uint32_t pk[16];
+      for (int q = 0; q < 2; ++q) {
+        const uint32_t (&r)[32] = rs[q];
+        uint32_t pk[16];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float4 l4 = lse4[8 * q + u];
-        const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1])), c2,
-                                     make_float2(-l4.x, -l4.y));
-        const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])),
-                                     c2, make_float2(-l4.z, -l4.w));
-        float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
-        float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
-        if (!key_ok) p0 = p1 = make_float2(0.f, 0.f);
-        pk[2 * u] = pack2<BF16>(p0.x, p0.y);
-        pk[2 * u + 1] = pack2<BF16>(p1.x, p1.y);
-        const float2 s0 = __fmul2_rn(p0, sc2), s1 = __fmul2_rn(p1, sc2);
-        ps[32 * q + 4 * u] = s0.x;
-        ps[32 * q + 4 * u + 1] = s0.y;
-        ps[32 * q + 4 * u + 2] = s1.x;
-        ps[32 * q + 4 * u + 3] = s1.y;
+        for (int u = 0; u < 8; ++u) {
+          const float4 l4 = lse4[8 * q + u];
+          const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1])), c2,
+                                       make_float2(-l4.x, -l4.y));
+          const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])),
+                                       c2, make_float2(-l4.z, -l4.w));
+          float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+          float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+          if constexpr (kMasked) {
+            const int c0 = 32 * q + 4 * u;
+            if (c0 < lim) p0.x = 0.f;
+            if (c0 + 1 < lim) p0.y = 0.f;
+            if (c0 + 2 < lim) p1.x = 0.f;
+            if (c0 + 3 < lim) p1.y = 0.f;
+          }
+          pk[2 * u] = pack2<BF16>(p0.x, p0.y);
+          pk[2 * u + 1] = pack2<BF16>(p1.x, p1.y);
+          const float2 s0 = __fmul2_rn(p0, sc2), s1 = __fmul2_rn(p1, sc2);
+          ps[32 * q + 4 * u] = s0.x;
+          ps[32 * q + 4 * u + 1] = s0.y;
+          ps[32 * q + 4 * u + 2] = s1.x;
+          ps[32 * q + 4 * u + 3] = s1.y;
+        }
+        // Queries [32q, 32q+32) of this half -> packed columns [16q, 16q+16) (both chunks were read above).
+        tmem_st16(t_s + 16 * q, pk);
+        if (q == 0 && W == 0 && t == 0) FA_TRACE(p, kBvSmPChunk0, i);
       }
-      // Queries [32q, 32q+32) of this half -> packed columns [16q, 16q+16) (both chunks were read above).
-      tmem_st16(t_s + 16 * q, pk);
-      if (q == 0 && W == 0 && t == 0) FA_TRACE(p, kBvSmPChunk0, i);
-    }
+    };
+    const bool diag = p.causal && i == 0;
+    if (diag || rest_masked)
+      p_phase(std::true_type{}, diag ? lim_diag : lim_rest);
+    else
+      p_phase(std::false_type{}, 0);
     tmem_st_wait();
     tc_fence_before();
     __syncwarp();
@@ -526,8 +550,8 @@ __device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint8_t* smem, u
 // dQ warpgroup (warps 8-11): dQ_i -> registers -> fp32 boxes -> TMA reduce-add
 // --------------------------------------------------------------------------
 template <int D>
-__device__ __forceinline__ void bwd_dq(const BwdParams& p, uint32_t base, uint32_t tmem, int bh, int nq,
-                                       const BCtl& ctl) {
+__device__ __forceinline__ void bwd_dq(const BwdParams& p, uint32_t base, uint32_t tmem, int bh, int q_first,
+                                       int nq, const BCtl& ctl) {
   using C = BCfg<D>;
   constexpr int BAR = 3;
   const int t = threadIdx.x - 256;  // query row within the Q tile = TMEM lane
@@ -565,7 +589,7 @@ __device__ __forceinline__ void bwd_dq(const BwdParams& p, uint32_t base, uint32
       fence_proxy_async_smem();
       named_bar_sync(BAR, 128);
       if (t == 0) {
-        tma_reduce_add_3d(&p.tm_dqacc, buf, 32 * b, i * C::BQ, bh);
+        tma_reduce_add_3d(&p.tm_dqacc, buf, 32 * b, (q_first + i) * C::BQ, bh);
         tma_store_commit();
       }
     }
@@ -592,7 +616,26 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1) fa_bwd_main_kernel(const 
   const int nt = (p.N + C::BK - 1) / C::BK;
   const int bh = blockIdx.x / nt;
   const int kv0 = (blockIdx.x % nt) * C::BK;
-  const int nq = (p.N + C::BQ - 1) / C::BQ;
+  int key_end = p.N;
+  if (p.klen != nullptr) key_end = min(max(p.klen[bh / p.H], 0), p.N);
+  // With the causal mask, Q tiles before the diagonal one (BQ == BK) see none
+  // of these keys; nq counts the Q tiles visited, from q_first on.
+  const int q_first = p.causal ? kv0 / C::BQ : 0;
+  const int nq = kv0 < key_end ? (p.N + C::BQ - 1) / C::BQ - q_first : 0;
+  if (nq == 0) {
+    // Every key of this tile is masked: its dK and dV rows are zero and it
+    // adds nothing to dQ. Nothing has been set up yet.
+    const int rows = min(C::BK, p.N - kv0);
+    const long long first = (static_cast<long long>(bh) * p.N + kv0) * D;  // 16-bit elements
+    const int n16 = rows * D / 8;                                          // 16-byte chunks
+    uint4* dk = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dk) + first);
+    uint4* dv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dv) + first);
+    for (int x = threadIdx.x; x < n16; x += C::THREADS) {
+      dk[x] = make_uint4(0u, 0u, 0u, 0u);
+      dv[x] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    return;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(bbar<D>(base, C::B_K), 1);
@@ -630,7 +673,7 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1) fa_bwd_main_kernel(const 
   if (warp >= 12) {
     warpgroup_reg_dealloc<C::LOW_REGS>();
     if (warp == C::WARP_TMA) {
-      if ((threadIdx.x & 31) == 0) bwd_producer<D>(p, base, bh, kv0, nq, ctl);
+      if ((threadIdx.x & 31) == 0) bwd_producer<D>(p, base, bh, kv0, q_first, nq, ctl);
       __syncwarp();
     } else if (warp == C::WARP_MMA) {
       bwd_mma_dsdep<D, BF16>(p, base, tmem, nq, ctl);
@@ -641,13 +684,13 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1) fa_bwd_main_kernel(const 
     }
   } else if (warp >= 8) {
     warpgroup_reg_alloc<C::DQ_REGS>();
-    bwd_dq<D>(p, base, tmem, bh, nq, ctl);
+    bwd_dq<D>(p, base, tmem, bh, q_first, nq, ctl);
   } else if (warp >= 4) {
     warpgroup_reg_alloc<C::SM_REGS>();
-    bwd_softmax<D, BF16, 1>(p, smem_raw, base, tmem, bh, kv0, nq, ctl);
+    bwd_softmax<D, BF16, 1>(p, smem_raw, base, tmem, bh, kv0, nq, key_end, ctl);
   } else {
     warpgroup_reg_alloc<C::SM_REGS>();
-    bwd_softmax<D, BF16, 0>(p, smem_raw, base, tmem, bh, kv0, nq, ctl);
+    bwd_softmax<D, BF16, 0>(p, smem_raw, base, tmem, bh, kv0, nq, key_end, ctl);
   }
 
   tc_fence_before();
@@ -706,7 +749,9 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __grid_constant__
   for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, G);
   if (in_range && g == 0) {
     p.dsum[prow] = real ? acc : 0.f;
-    p.lse2[prow] = real ? p.lse[bh * p.N + r] * kLog2eB : INFINITY;
+    // A row with no key to see (LSE = -inf, O = 0) gets +inf as well: P = 0, dQ = 0.
+    const float l = real ? p.lse[bh * p.N + r] : -INFINITY;
+    p.lse2[prow] = l > -INFINITY ? l * kLog2eB : INFINITY;
   }
 }
 

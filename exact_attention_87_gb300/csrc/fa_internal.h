@@ -80,6 +80,13 @@ struct alignas(64) BwdParams {
   // Used only by the testing build (-DFA_TESTING); zero / NULL otherwise.
   int inject;                    // 1: the producer skips the dO load of Q tile 0
   unsigned long long* timeline;  // [kTraceCtas, kTraceEvents, kTraceTiles] clock64 stamps
+  // Masks (as FwdParams): causal (row i sees keys j <= i) and per-batch key
+  // lengths (klen[b]: keys j >= klen[b] masked; NULL = all N keys). dK and dV
+  // rows of fully masked key tiles are written as zeros through dk / dv.
+  int causal;
+  const int* klen;
+  void* dk;
+  void* dv;
 };
 
 // Tile sizes of the fp16/bf16 kernel: Q rows per sub-tile (two sub-tiles per

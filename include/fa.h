@@ -198,6 +198,27 @@ int fa_bwd(const void *Q, const void *K, const void *V, const void *O, const voi
 unsigned long long fa_bwd_workspace_size(int B, int H, int N, int d);
 
 /*
+ * Masked backward pass: the gradients of the masked forward pass (fa_fwd_ex)
+ * with the same masks. A masked score is -inf in the forward pass, so its
+ * P_ij and dS_ij are exactly 0 ("FlashAttention + Triton", sections 4.3 and
+ * 5.1, the masks; the backward of section 4.4 then sums over the seen keys
+ * only): keys a row does not see add nothing to its dQ, keys no row sees
+ * (j >= seqlens_k[b]) get dK = dV = 0, and a row with no key to see
+ * (LSE = -inf) gets dQ = 0.
+ *   causal:    0 or 1, as fa_fwd_ex. With 1, key tiles skip the query tiles
+ *              before them, so the pass does about half the work.
+ *   seqlens_k: NULL or a DEVICE array of B int32 key lengths, as fa_fwd_ex
+ *              (clamped to [0, N]). Padded keys and values must be finite:
+ *              both enter products with zero weights.
+ * O and LSE must be the outputs of fa_fwd_ex with the same masks. Other
+ * arguments, workspace and errors: as fa_bwd (causal outside {0, 1}:
+ * FA_ERR_SHAPE).
+ */
+int fa_bwd_ex(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *LSE,
+              void *dQ, void *dK, void *dV, int B, int H, int N, int d, float scale, int dtype, int causal,
+              const int *seqlens_k, void *workspace, unsigned long long workspace_bytes, void *stream);
+
+/*
  * Synchronises `stream`, then returns and clears the status word that kernels
  * of this library on the current device write when they give up on a wait:
  * FA_OK, FA_ERR_DEVICE_TIMEOUT, FA_ERR_DEVICE_SMEM (a kernel found its shared

@@ -108,6 +108,13 @@ def test_splitkv_workspace_size_formula(L):
 def test_masked_entry_point_argument_errors(L):
     assert fa.fa_fwd_ex(A, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, 2, None, None) == fa.FA_ERR_SHAPE
     assert fa.fa_fwd_ex(0, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, 1, None, None) == fa.FA_ERR_NULL
+    ws = fa.fa_bwd_workspace_size(1, 1, 64, 64)
+    args = [A] * 6 + [A] * 3 + [1, 1, 64, 64, 0.125, fa.FA_F16]
+    assert fa.fa_bwd_ex(*args, 2, None, 1 << 24, ws, None) == fa.FA_ERR_SHAPE
+    assert fa.fa_bwd_ex(*args, -1, None, 1 << 24, ws, None) == fa.FA_ERR_SHAPE
+    assert fa.fa_bwd_ex(*([0] + args[1:]), 1, None, 1 << 24, ws, None) == fa.FA_ERR_NULL
+    assert fa.fa_bwd_ex(*args, 1, None, 0, ws, None) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_bwd_ex(*(args[:12] + [256, 0.125, fa.FA_F16]), 1, None, 1 << 24, ws, None) == fa.FA_ERR_HEADDIM
 
 
 def test_backward_workspace_size_formula(L):
