@@ -155,6 +155,67 @@ def job_throughput(world_size: int, flops_per_rank: float, ms_per_step_max: floa
     return world_size * flops_per_rank / (ms_per_step_max * 1e-3) / 1e12
 
 
+L2_BYTES = 129 * 10**6  # GB300 L2
+FLUSH_BYTES = 256 * 2**20  # more than L2: overwriting it evicts every line
+
+
+def l2_policy(input_bytes: int) -> tuple[int, str]:
+    """Bytes to overwrite before every timed step (0: none) and the note for `config`."""
+    if input_bytes > L2_BYTES:
+        return 0, "inputs larger than L2 (no flush)"
+    return FLUSH_BYTES, "L2 flushed before every timed step (256 MiB overwritten outside the timed events)"
+
+
+def timed_steps(step, steps: int, stream, dev, barrier, flush_bytes: int):
+    """Time `steps` calls of `step` with CUDA events on `stream`.
+
+    Returns (total ms, per-step ms). Without a flush the total is one event
+    pair around `steps` back-to-back steps, and the per-step times come from a
+    second pass of `steps` steps with an event pair around each (so the events
+    do not perturb the total). With a flush, a buffer of `flush_bytes` is
+    overwritten before each step, outside that step's events, and the total
+    is the sum of the per-step times of that one pass."""
+    import torch
+
+    def per_step_pass(flush):
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        barrier()
+        for i, (a, b) in enumerate(pairs):
+            if flush is not None:
+                flush.fill_(i & 0xFF)
+            a.record(stream)
+            step()
+            b.record(stream)
+        barrier()
+        return [a.elapsed_time(b) for a, b in pairs]
+
+    if flush_bytes:
+        per = per_step_pass(torch.empty(flush_bytes, dtype=torch.uint8, device=dev))
+        return sum(per), per
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    barrier()
+    total = e0.elapsed_time(e1)
+    return total, per_step_pass(None)
+
+
+def step_distribution(per_ms) -> dict:
+    """Median, 10th and 90th percentile of the per-step times (ms)."""
+    xs = sorted(per_ms)
+
+    def pct(f):
+        i = f * (len(xs) - 1)
+        lo = int(i)
+        hi = min(lo + 1, len(xs) - 1)
+        return xs[lo] + (xs[hi] - xs[lo]) * (i - lo)
+
+    return {"median": round(pct(0.5), 4), "p10": round(pct(0.1), 4), "p90": round(pct(0.9), 4), "n": len(xs)}
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -211,7 +272,10 @@ def main():
     ws, rank, local = dist_env()
     cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype, "sigma_qk": w.sigma_qk,
            "sigma_v": w.sigma_v, "scale": "1/sqrt(d)", "causal": False,
-           "l2": "inputs larger than L2 (no flush)" if 3 * w.B * w.H * w.N * w.d * 2 > 129e6 else "inputs fit in L2: warm, not flushed"}
+           "l2": None}
+    # Inputs of one step: Q, K, V (forward) or Q, K, V, O, dO (backward).
+    es = 4 if w.dtype == "f32" else 2
+    args.flush_bytes, cfg["l2"] = l2_policy((5 if args.which == "bwd" else 3) * w.B * w.H * w.N * w.d * es)
     if args.causal:
         cfg["causal"] = True
         cfg["flops"] = "4*d*N*(N+1)/2 per (b, h)"
@@ -260,17 +324,10 @@ def main():
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     with sampler:
-        barrier()
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
-        barrier()
-    ms_total = max_over_ranks(e0.elapsed_time(e1), dev)
+        local_total, per_step = timed_steps(step, args.steps, stream, dev, barrier, args.flush_bytes)
+    ms_total = max_over_ranks(local_total, dev)
     ms = ms_total / args.steps
     st = fa.fa_get_device_status()
     if st != fa.FA_OK:
@@ -329,6 +386,7 @@ def main():
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms, 4),
+        "ms_per_step_dist": step_distribution(per_step),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -403,16 +461,10 @@ def run_backward(args, w, cfg, ws, rank, local):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     with sampler:
-        barrier()
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
-        barrier()
-    ms = max_over_ranks(e0.elapsed_time(e1), dev) / args.steps
+        local_total, per_step = timed_steps(step, args.steps, stream, dev, barrier, args.flush_bytes)
+    ms = max_over_ranks(local_total, dev) / args.steps
     st = fa.fa_get_device_status()
     if st != fa.FA_OK:
         raise RuntimeError(f"device status {st} after the timed region")
@@ -462,7 +514,8 @@ def run_backward(args, w, cfg, ws, rank, local):
         "metric": ("attention bwd TFLOP/s (" + ("causal, 10*B*H*d*N*(N+1)/2" if causal else "10*B*H*N^2*d") +
                    ") and % of GB300 dense BF16 tensor peak"),
         "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": round(ms, 4), "ms_per_step_dist": step_distribution(per_step), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded, generated on the host)", "config": cfg,
         "pct_of_peak": round(100.0 * achieved / peak, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",

@@ -74,6 +74,10 @@ def lib(path: str | None = None):
     L.fa_bwd.restype = i
     L.fa_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, vp, u64, vp]
     L.fa_bwd_ex.restype = i
+    L.fa_fwd_partial.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    L.fa_fwd_partial.restype = i
+    L.fa_merge.argtypes = [vp, vp, i, vp, vp, i, i, i, i, i, vp]
+    L.fa_merge.restype = i
     L.fa_bwd_workspace_size.argtypes = [i, i, i, i]
     L.fa_bwd_workspace_size.restype = u64
     if path == LIB_PATH:
@@ -115,6 +119,14 @@ def fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype, workspace,
            stream=None) -> int:
     return lib().fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype, workspace, workspace_bytes,
                         stream)
+
+
+def fa_fwd_partial(Q, K, V, O_part, LSE_part, B, H, Nq, Nk, d, scale, dtype, stream=None) -> int:
+    return lib().fa_fwd_partial(Q, K, V, O_part, LSE_part, B, H, Nq, Nk, d, scale, dtype, stream)
+
+
+def fa_merge(O_parts, LSE_parts, num_parts, O, LSE, B, H, N, d, dtype, stream=None) -> int:
+    return lib().fa_merge(O_parts, LSE_parts, num_parts, O, LSE, B, H, N, d, dtype, stream)
 
 
 def fa_bwd_ex(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype, causal, seqlens_k, workspace,
@@ -214,6 +226,77 @@ def attention(q, k, v, scale: float | None = None, out=None, lse=None, stream=No
     return out, lse
 
 
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def attention_partial(q, k, v, scale: float | None = None, o_part=None, lse_part=None, stream=None):
+    """One part of attention over a split key set (fa_fwd_partial): all queries
+    q [B, H, Nq, d] against the keys k, v [B, H, Nk, d] (16-bit, contiguous CUDA
+    tensors). Returns this part's normalised O (fp32 [B, H, Nq, d]) and LSE
+    (fp32 [B, H, Nq]); ``merge_partials`` combines parts. An empty key set
+    (Nk = 0) gives O = 0, LSE = -inf without a launch."""
+    import torch
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape or k.shape[:2] != q.shape[:2] or k.shape[3] != q.shape[3]:
+        raise ValueError(f"q [B, H, Nq, d] and k, v [B, H, Nk, d] expected: {q.shape} {k.shape} {v.shape}")
+    if not (q.dtype == k.dtype == v.dtype) or not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors of one dtype")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o_part = torch.empty((B, H, Nq, d), dtype=torch.float32, device=q.device) if o_part is None else o_part
+    lse_part = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse_part is None else lse_part
+    if o_part.shape != (B, H, Nq, d) or o_part.dtype != torch.float32 or not o_part.is_contiguous():
+        raise ValueError("o_part must be a contiguous fp32 [B, H, Nq, d] tensor")
+    if lse_part.shape != (B, H, Nq) or lse_part.dtype != torch.float32 or not lse_part.is_contiguous():
+        raise ValueError("lse_part must be a contiguous fp32 [B, H, Nq] tensor")
+    if Nk == 0:
+        o_part.zero_()
+        lse_part.fill_(float("-inf"))
+        return o_part, lse_part
+    with torch.cuda.device(q.device):
+        rc = fa_fwd_partial(q.data_ptr(), k.data_ptr(), v.data_ptr(), o_part.data_ptr(), lse_part.data_ptr(),
+                            B, H, Nq, Nk, d, float(scale), _dtype_code(q), _stream_handle(stream, q.device))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_partial")
+    return o_part, lse_part
+
+
+def merge_partials(o_parts, lse_parts, dtype, out=None, lse=None, stream=None):
+    """Merge parts over disjoint key sets (fa_merge): o_parts fp32
+    [P, B, H, N, d], lse_parts fp32 [P, B, H, N] (contiguous CUDA tensors) ->
+    O of ``dtype`` (torch.float16 / torch.bfloat16) [B, H, N, d] and LSE fp32
+    [B, H, N]."""
+    import torch
+    if o_parts.dim() != 5 or lse_parts.shape != o_parts.shape[:4]:
+        raise ValueError(f"o_parts [P, B, H, N, d] and lse_parts [P, B, H, N] expected: {o_parts.shape} {lse_parts.shape}")
+    if o_parts.dtype != torch.float32 or lse_parts.dtype != torch.float32:
+        raise ValueError("parts must be fp32")
+    if not (o_parts.is_cuda and lse_parts.is_cuda and o_parts.is_contiguous() and lse_parts.is_contiguous()):
+        raise ValueError("parts must be contiguous CUDA tensors")
+    P, B, H, N, d = o_parts.shape
+    out = torch.empty((B, H, N, d), dtype=dtype, device=o_parts.device) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=o_parts.device) if lse is None else lse
+    if out.shape != (B, H, N, d) or out.dtype != dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [B, H, N, d] tensor of dtype")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    code = FA_BF16 if dtype == torch.bfloat16 else FA_F16 if dtype == torch.float16 else FA_F32
+    with torch.cuda.device(o_parts.device):
+        rc = fa_merge(o_parts.data_ptr(), lse_parts.data_ptr(), P, out.data_ptr(), lse.data_ptr(), B, H, N, d, code,
+                      _stream_handle(stream, o_parts.device))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_merge")
+    return out, lse
+
+
 def attention_backward(q, k, v, o, lse, do, scale: float | None = None, dq=None, dk=None, dv=None, workspace=None,
                        stream=None, causal: bool = False, seqlens_k=None):
     """dQ, dK, dV for the forward pass O, LSE = attention(q, k, v, scale) and the
@@ -273,7 +356,8 @@ def attention_backward(q, k, v, o, lse, do, scale: float | None = None, dq=None,
     return dq, dk, dv
 
 
-__all__ = ["attention", "attention_backward", "fa_bwd", "fa_bwd_ex", "fa_bwd_workspace_size", "fa_fwd", "fa_fwd_ex", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_num_splits",
+__all__ = ["attention", "attention_backward", "attention_partial", "merge_partials", "fa_fwd_partial", "fa_merge",
+           "fa_bwd", "fa_bwd_ex", "fa_bwd_workspace_size", "fa_fwd", "fa_fwd_ex", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_num_splits",
            "fa_fwd_splitkv_workspace_size",
            "fa_get_device_status", "fa_strerror", "fa_abi_version", "build", "lib",
            "FAError", "FA_F32", "FA_F16", "FA_BF16", "FA_OK"]

@@ -244,6 +244,7 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
   p.B = B;
   p.H = H;
   p.N = N;
+  p.Nk = N;
   p.d = d;
   p.scale = scale;
   p.num_sms = dev.num_sms;
@@ -285,9 +286,99 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// All Nq queries against Nk keys, written as one part of a merge: normalised
+// fp32 O and LSE (the split-KV epilogue of the 16-bit kernel, with K and V of
+// their own length).
+int partial_impl(const void* Q, const void* K, const void* V, float* O_part, float* LSE_part, int B, int H, int Nq,
+                 int Nk, int d, float scale, int dtype, void* stream) {
+  if (!Q || !K || !V || !O_part || !LSE_part) return FA_ERR_NULL;
+  if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+  if (dtype == FA_F32) return FA_ERR_UNSUPPORTED;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > 0x7fffffffLL || BH * std::max(Nq, Nk) > (1ll << 40) / d) return FA_ERR_SHAPE;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O_part) ||
+      (reinterpret_cast<uintptr_t>(LSE_part) & 3u) != 0)
+    return FA_ERR_ALIGN;
+  DeviceInfo dev;
+  const int st = device_info(&dev);
+  if (st != FA_OK) return st;
+
+  fa::FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = Q;
+  p.k = K;
+  p.v = V;
+  p.o_part = O_part;
+  p.lse_part = LSE_part;
+  p.status = dev.status;
+  p.wait_limit = wait_limit_cycles();
+  p.B = B;
+  p.H = H;
+  p.N = Nq;
+  p.Nk = Nk;
+  p.d = d;
+  p.scale = scale;
+  p.num_sms = dev.num_sms;
+  p.num_splits = 1;
+  p.split_tiles = static_cast<int>(kv_tiles(Nk));
+  p.partial = 1;
+  const CUtensorMapDataType dt = dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const int bh = static_cast<int>(BH);
+  if (!encode_bhnd_16bit(&p.tm_q, Q, bh, Nq, d, dt, fa::kF16BlockQ) ||
+      !encode_bhnd_16bit(&p.tm_k, K, bh, Nk, d, dt, fa::kF16BlockKV) ||
+      !encode_bhnd_16bit(&p.tm_v, V, bh, Nk, d, dt, fa::kF16BlockKV))
+    return FA_ERR_CUDA;
+  const cudaError_t e = fa::launch_fwd_f16(p, dtype == FA_BF16, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int merge_impl(const float* O_parts, const float* LSE_parts, int num_parts, void* O, float* LSE, int B, int H, int N,
+               int d, int dtype, void* stream) {
+  if (!O_parts || !LSE_parts || !O || !LSE) return FA_ERR_NULL;
+  if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+  if (dtype == FA_F32) return FA_ERR_UNSUPPORTED;
+  if (B < 1 || H < 1 || N < 1 || num_parts < 1) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  const long long rows = static_cast<long long>(B) * H * N;
+  if (rows * num_parts > (1ll << 40) / d) return FA_ERR_SHAPE;
+  if (!aligned16(O_parts) || !aligned16(O) || (reinterpret_cast<uintptr_t>(LSE_parts) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0)
+    return FA_ERR_ALIGN;
+  DeviceInfo dev;
+  const int st = device_info(&dev);
+  if (st != FA_OK) return st;
+  fa::FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.o_part = const_cast<float*>(O_parts);
+  p.lse_part = const_cast<float*>(LSE_parts);
+  p.num_splits = num_parts;
+  p.o = O;
+  p.lse = LSE;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.Nk = N;
+  p.d = d;
+  const cudaError_t e = fa::launch_merge_guarded(p, dtype == FA_BF16, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
+
+int fa_fwd_partial(const void* Q, const void* K, const void* V, float* O_part, float* LSE_part, int B, int H, int Nq,
+                   int Nk, int d, float scale, int dtype, void* stream) {
+  return partial_impl(Q, K, V, O_part, LSE_part, B, H, Nq, Nk, d, scale, dtype, stream);
+}
+
+int fa_merge(const float* O_parts, const float* LSE_parts, int num_parts, void* O, float* LSE, int B, int H, int N,
+             int d, int dtype, void* stream) {
+  return merge_impl(O_parts, LSE_parts, num_parts, O, LSE, B, H, N, d, dtype, stream);
+}
 
 int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, float scale,
            int dtype, void* stream) {

@@ -412,8 +412,9 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
   // No key to attend to (key length 0): O = 0, LSE = -inf instead of 0/0.
   const bool empty = nkv == 0;
   const float inv_l = empty ? 0.f : 1.0f / (BF16 ? l_o : l);
-  if (p.num_splits > 1) {
-    // Split-KV: this key range's normalised O (fp32) and LSE go to the partial buffers.
+  if (p.num_splits > 1 || p.partial) {
+    // Split-KV (or one part of a merge done elsewhere): this key range's
+    // normalised O (fp32) and LSE go to the partial buffers.
     const int row = row0 + C::BM * sub + t;
     const size_t prow = (static_cast<size_t>(split) * p.B * p.H + bh) * p.N + row;
 #pragma unroll
@@ -492,7 +493,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
   const int row0 = qb * 2 * C::BM;
   const bool has1 = row0 + C::BM < p.N;
   // Keys this unit may see: [0, key_end); causal limits each sub-tile to its own last row.
-  const int key_end = p.klen ? max(0, min(p.N, p.klen[bh / p.H])) : p.N;
+  const int key_end = p.klen ? max(0, min(p.Nk, p.klen[bh / p.H])) : p.Nk;
   const int end0 = p.causal ? min(key_end, row0 + C::BM) : key_end;
   const int end1 = p.causal ? min(key_end, row0 + 2 * C::BM) : key_end;
   const int t0 = split * p.split_tiles;                      // first K/V tile of this key range
@@ -639,6 +640,49 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const __grid_constant__ F
   if (lane == 0) p.lse[row] = m + lg2_approx(l) * kLn2;
 }
 
+// The same merge for rows that may have no key in any part (every part's
+// LSE = -inf): those rows get O = 0 and LSE = -inf.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) fa_merge_guarded_kernel(const __grid_constant__ FwdParams p) {
+  constexpr int E = D / 32;
+  const long long rows = static_cast<long long>(p.B) * p.H * p.N;
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float m = -INFINITY;
+  for (int s = 0; s < p.num_splits; ++s) m = fmaxf(m, p.lse_part[s * rows + row]);
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float l = 0.f;
+  if (m > -INFINITY) {
+    for (int s = 0; s < p.num_splits; ++s) {
+      const float w = ex2_approx((p.lse_part[s * rows + row] - m) * kLog2e);
+      l += w;
+      const float* src = p.o_part + (s * rows + row) * D + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(w, src[e], acc[e]);
+    }
+  }
+  const float inv = l > 0.f ? 1.0f / l : 0.f;
+  uint32_t pk[E / 2];
+#pragma unroll
+  for (int e = 0; e < E / 2; ++e) pk[e] = pack2<BF16>(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+  uint32_t* out = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.o) + row * D + lane * E);
+#pragma unroll
+  for (int e = 0; e < E / 2; ++e) out[e] = pk[e];
+  if (lane == 0) p.lse[row] = m > -INFINITY ? m + lg2_approx(l) * kLn2 : -INFINITY;
+}
+
+template <int D, bool BF16>
+cudaError_t launch_merge_guarded_t(const FwdParams& p, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(p.B) * p.H * p.N;
+  const long long blocks = (rows * 32 + 255) / 256;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  fa_merge_guarded_kernel<D, BF16><<<dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 template <int D, bool BF16>
 cudaError_t launch_merge_t(const FwdParams& p, cudaStream_t stream) {
   const long long rows = static_cast<long long>(p.B) * p.H * p.N;
@@ -653,6 +697,13 @@ cudaError_t launch_merge_t(const FwdParams& p, cudaStream_t stream) {
 cudaError_t launch_merge(const FwdParams& p, bool bf16, cudaStream_t stream) {
   if (p.d == 128) return bf16 ? launch_merge_t<128, true>(p, stream) : launch_merge_t<128, false>(p, stream);
   if (p.d == 64) return bf16 ? launch_merge_t<64, true>(p, stream) : launch_merge_t<64, false>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_merge_guarded(const FwdParams& p, bool bf16, cudaStream_t stream) {
+  if (p.d == 128)
+    return bf16 ? launch_merge_guarded_t<128, true>(p, stream) : launch_merge_guarded_t<128, false>(p, stream);
+  if (p.d == 64) return bf16 ? launch_merge_guarded_t<64, true>(p, stream) : launch_merge_guarded_t<64, false>(p, stream);
   return cudaErrorInvalidValue;
 }
 

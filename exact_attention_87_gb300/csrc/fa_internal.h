@@ -46,6 +46,11 @@ struct alignas(64) FwdParams {
   int split_tiles;
   float* o_part;
   float* lse_part;
+  // Keys: K and V hold Nk rows (Nk = N except for fa_fwd_partial). partial = 1:
+  // the 16-bit kernel writes its normalised fp32 O and LSE to o_part / lse_part
+  // as the one part of a merge done elsewhere (fa_merge).
+  int Nk;
+  int partial;
   // Masks: causal (row i sees keys j <= i) and per-batch key lengths
   // (klen[b]: keys j >= klen[b] masked; NULL = all N keys).
   int causal;
@@ -118,6 +123,9 @@ enum : int {
 cudaError_t launch_fwd_f16(const FwdParams& p, bool bf16, cudaStream_t stream);
 // Merge split-KV partials into O (dtype of the 16-bit path) and LSE.
 cudaError_t launch_merge(const FwdParams& p, bool bf16, cudaStream_t stream);
+// The merge of fa_merge: num_splits parts in o_part / lse_part into o / lse;
+// rows with no key in any part get O = 0, LSE = -inf.
+cudaError_t launch_merge_guarded(const FwdParams& p, bool bf16, cudaStream_t stream);
 // Backward: row statistics (D, LSE * log2 e) and a zeroed dQ accumulator;
 // the main dK/dV/dQ kernel; the dQ accumulator rounded into dQ.
 cudaError_t launch_bwd_f16(const BwdParams& p, bool bf16, cudaStream_t stream);

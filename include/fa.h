@@ -194,6 +194,38 @@ int fa_bwd(const void *Q, const void *K, const void *V, const void *O, const voi
            void *dQ, void *dK, void *dV, int B, int H, int N, int d, float scale, int dtype,
            void *workspace, unsigned long long workspace_bytes, void *stream);
 
+/*
+ * One part of attention over a key set split across parts (devices, for
+ * context parallelism): all Nq queries against these Nk keys. The Triton
+ * page's block merge (section 2.3) combines such parts exactly: each part
+ * keeps its own normalised output and logsumexp, and fa_merge folds them.
+ *   Q:        [B, H, Nq, d] device array, FA_F16 or FA_BF16.
+ *   K, V:     [B, H, Nk, d] device arrays of the same dtype (this part's keys).
+ *   O_part:   [B, H, Nq, d] fp32 device array (caller-owned): this part's
+ *             softmax(scale Q K^T) V over its own keys.
+ *   LSE_part: [B, H, Nq] fp32 device array: this part's row logsumexp.
+ * No mask. Errors: as fa_fwd (FA_F32 -> FA_ERR_UNSUPPORTED; d must be 64 or
+ * 128; Nq, Nk >= 1). One launch on `stream`; nothing is synchronised.
+ */
+int fa_fwd_partial(const void *Q, const void *K, const void *V, float *O_part, float *LSE_part,
+                   int B, int H, int Nq, int Nk, int d, float scale, int dtype, void *stream);
+
+/*
+ * Merge of num_parts results over disjoint key sets (the Triton page, section
+ * 2.3, in LSE form): LSE = m + ln sum_p exp(LSE_p - m) with m = max_p LSE_p,
+ * O = sum_p exp(LSE_p - LSE) O_p, rounded to `dtype` once.
+ *   O_parts:   [num_parts, B, H, N, d] fp32 device array (parts contiguous,
+ *              16-byte aligned), e.g. gathered outputs of fa_fwd_partial.
+ *   LSE_parts: [num_parts, B, H, N] fp32 device array.
+ *   O:         [B, H, N, d] device array of `dtype` (FA_F16 or FA_BF16).
+ *   LSE:       [B, H, N] fp32 device array.
+ * A part with LSE = -inf contributes nothing; a row whose parts are all -inf
+ * gets O = 0 and LSE = -inf. d must be 64 or 128. Errors: as fa_fwd
+ * (FA_F32 -> FA_ERR_UNSUPPORTED). One launch on `stream`.
+ */
+int fa_merge(const float *O_parts, const float *LSE_parts, int num_parts, void *O, float *LSE,
+             int B, int H, int N, int d, int dtype, void *stream);
+
 /* Workspace bytes fa_bwd needs for this shape (0 for invalid arguments). */
 unsigned long long fa_bwd_workspace_size(int B, int H, int N, int d);
 

@@ -117,6 +117,40 @@ def test_masked_entry_point_argument_errors(L):
     assert fa.fa_bwd_ex(*(args[:12] + [256, 0.125, fa.FA_F16]), 1, None, 1 << 24, ws, None) == fa.FA_ERR_HEADDIM
 
 
+def test_partial_and_merge_argument_errors(L):
+    #                 Q  K  V  Op Lp B  H  Nq  Nk  d    scale  dtype
+    ok = [A, A, A, A, A, 1, 1, 64, 64, 64, 0.125, fa.FA_BF16, None]
+    def part(**kw):
+        a = list(ok)
+        for i, name in enumerate(["Q", "K", "V", "Op", "Lp", "B", "H", "Nq", "Nk", "d", "scale", "dtype"]):
+            if name in kw:
+                a[i] = kw[name]
+        return fa.fa_fwd_partial(*a)
+    assert part(Q=0) == fa.FA_ERR_NULL
+    assert part(Lp=0) == fa.FA_ERR_NULL
+    assert part(dtype=fa.FA_F32) == fa.FA_ERR_UNSUPPORTED
+    assert part(dtype=7) == fa.FA_ERR_DTYPE
+    assert part(Nk=0) == fa.FA_ERR_SHAPE
+    assert part(Nq=0) == fa.FA_ERR_SHAPE
+    assert part(d=256) == fa.FA_ERR_HEADDIM
+    assert part(scale=-1.0) == fa.FA_ERR_SCALE
+    assert part(Op=A + 4) == fa.FA_ERR_ALIGN
+    #                Op Lp P  O  L  B  H  N   d   dtype
+    okm = [A, A, 2, A, A, 1, 1, 64, 64, fa.FA_F16, None]
+    def merge(**kw):
+        a = list(okm)
+        for i, name in enumerate(["Op", "Lp", "P", "O", "L", "B", "H", "N", "d", "dtype"]):
+            if name in kw:
+                a[i] = kw[name]
+        return fa.fa_merge(*a)
+    assert merge(Op=0) == fa.FA_ERR_NULL
+    assert merge(P=0) == fa.FA_ERR_SHAPE
+    assert merge(dtype=fa.FA_F32) == fa.FA_ERR_UNSUPPORTED
+    assert merge(d=96) == fa.FA_ERR_HEADDIM
+    assert merge(O=A + 2) == fa.FA_ERR_ALIGN
+    assert merge(L=A + 1) == fa.FA_ERR_ALIGN
+
+
 def test_backward_workspace_size_formula(L):
     def part(n):
         return (n + 255) // 256 * 256
