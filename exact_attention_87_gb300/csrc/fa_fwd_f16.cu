@@ -357,8 +357,15 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
         const float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
         se = __fadd2_rn(se, pr);
         pk[u] = pack2<BF16>(pr.x, pr.y);
-        if constexpr (BF16)
-          sro = __fadd2_rn(sro, make_float2(__uint_as_float(pk[u] << 16), __uint_as_float(pk[u] & 0xFFFF0000u)));
+        if constexpr (BF16) {
+          // The two rounded values added as bf16 operands of mixed-precision
+          // fp32 adds (exact conversion, one add each): cheaper than
+          // unpacking them into fp32 registers first.
+          unsigned short lo16, hi16;
+          asm("mov.b32 {%0, %1}, %2;" : "=h"(lo16), "=h"(hi16) : "r"(pk[u]));
+          asm("add.rn.f32.bf16 %0, %1, %0;" : "+f"(sro.x) : "h"(lo16));
+          asm("add.rn.f32.bf16 %0, %1, %0;" : "+f"(sro.y) : "h"(hi16));
+        }
       }
       tmem_st8(t_s + 8 * q, pk);  // keys [16q, 16q+16) -> packed columns [8q, 8q+8)
     }
