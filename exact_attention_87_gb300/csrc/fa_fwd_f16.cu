@@ -13,7 +13,9 @@
 //
 // GB300 mapping (one CTA per (batch*head, 256-row Q block), 12 warps):
 //   warp 9      TMA producer: Q0/Q1 once, then K_j and V_j (128 keys each)
-//               into 2-stage (d=128) / 3-stage (d=64) rings
+//               into 2-stage (d=128) / 3-stage (d=64) rings; the softmax
+//               warps free a stage once the S product they wait for shows
+//               that its K (and the previous tile's V) have been read
 //   warps 8, 10 MMA warps, one per Q sub-tile i: S_i(j) = Q_i K_j^T (SS, into
 //               TMEM), then O_i += P_i(j) V_j (TS: P read from TMEM, V from
 //               SMEM); one elected lane issues; warp 8 also owns TMEM
@@ -220,7 +222,6 @@ __device__ __forceinline__ void mma_warp(const FwdParams& p, uint32_t base, uint
       // follows S(j) (same warp, issued after it); only the last P.V, which no
       // S follows, is committed on its own (strict order: every P.V is).
       if (kOdEveryTile || j == nkv) tc_commit_elect(b_od);
-      tc_commit_elect(bar_addr<D>(base, C::B_VE + s));
       FA_TRACE(p, kEvPV0Issued + sub, j - 1);
     }
     if (j < nkv) {
@@ -247,7 +248,6 @@ __device__ __forceinline__ void mma_warp(const FwdParams& p, uint32_t base, uint
         mma_f16_ss_elect(d_s, a0 + aoff, b0 + boff, idesc_qk, kk > 0 ? 1u : 0u);
       }
       tc_commit_elect(b_sf);
-      tc_commit_elect(bar_addr<D>(base, C::B_KE + s));  // one of the (nsub) releases of this K stage
       FA_TRACE(p, kEvS0Issued + sub, j);
     }
     if (has1) {
@@ -294,6 +294,15 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
     }
     tc_fence_after();
     if (t == 0) FA_TRACE(p, kEvSm0SFull + 2 * sub, j);
+    if (lane == 0) {
+      // The K/V stages are released from here, not by commits in the MMA
+      // warp's issue stream (a commit right behind a group of MMAs leaves the
+      // tensor pipe idle for ~200 cycles): S(j) is complete, so K_j has been
+      // read, and so has V_{j-1}, since P(j-1) V_{j-1} was issued before S(j)
+      // by the same warp and one commit covers all of its earlier MMAs.
+      mbar_arrive(bar_addr<D>(base, C::B_KE + j % C::STAGES));
+      if (j > 0) mbar_arrive(bar_addr<D>(base, C::B_VE + (j - 1) % C::STAGES));
+    }
     uint32_t sraw[C::BN / 32][32];
 #pragma unroll
     for (int q = 0; q < C::BN / 32; ++q) tmem_ld32(t_s + 32 * q, sraw[q]);
@@ -511,12 +520,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
 
   if (threadIdx.x == 0) {
     mbar_init(bar_addr<D>(base, C::B_Q), 1);
-    const uint32_t nsub = has1 ? 2u : 1u;  // the stage-empty barriers get one commit per MMA warp
+    const uint32_t nsub = has1 ? 2u : 1u;  // the stage-empty barriers get one arrival per softmax warp of each sub-tile
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar_addr<D>(base, C::B_KF + s), 1);
-      mbar_init(bar_addr<D>(base, C::B_KE + s), nsub);
+      mbar_init(bar_addr<D>(base, C::B_KE + s), 4 * nsub);  // one arrival per softmax warp
       mbar_init(bar_addr<D>(base, C::B_VF + s), 1);
-      mbar_init(bar_addr<D>(base, C::B_VE + s), nsub);
+      mbar_init(bar_addr<D>(base, C::B_VE + s), 4 * nsub);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_addr<D>(base, C::B_SF + i), 1);
