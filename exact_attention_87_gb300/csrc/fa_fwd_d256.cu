@@ -48,7 +48,9 @@ struct C256 {
   static constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;
   static constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + STAGES, B_VF = B_KE + STAGES, B_VE = B_VF + STAGES;
-  static constexpr int B_SF = B_VE + STAGES, B_PF = B_SF + 2, B_OD = B_PF + 2, B_DRAIN = B_OD + 1;
+  // B_OD completes once per P.V (the rescale waits for the previous one);
+  // B_OL once, after the last P.V (the epilogue waits for it).
+  static constexpr int B_SF = B_VE + STAGES, B_PF = B_SF + 2, B_OD = B_PF + 2, B_OL = B_OD + 1, B_DRAIN = B_OL + 1;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;  // [0] TMEM base, [1] abort flag
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
@@ -160,6 +162,7 @@ __device__ __forceinline__ void mma256(uint32_t base, uint32_t tmem, int nkv, co
                          (j > 0 || kk > 0) ? 1u : 0u);
     }
     tc_commit_elect(b_od);
+    if (j == nkv - 1) tc_commit_elect(bar256(base, C::B_OL));
     tc_commit_elect(bar256(base, C::B_VE + s));
     // S_{j+2} into the columns of P_j, right behind the P_j V_j that reads them.
     if (j + 2 < nkv) {
@@ -266,7 +269,10 @@ __device__ __forceinline__ void softmax256(const FwdParams& p, uint32_t base, ui
     l += se.x + se.y;
     if constexpr (BF16) l_o += sro.x + sro.y;
     if (rescale_o) {
-      // O complete up to tile j-1 before it is read and scaled.
+      // O complete up to tile j-1 before it is read and scaled. The parity
+      // names one phase: S_j's completion (waited for above) covers
+      // P_{j-2} V (issued before S_j), and P_j V cannot have started, so
+      // B_OD is in phase j-1 or j.
       if (!__all_sync(0xffffffffu, wait_bar(b_od, (j - 1) & 1, ctl, kWhereODone))) {
         ok = false;
         break;
@@ -288,7 +294,10 @@ __device__ __forceinline__ void softmax256(const FwdParams& p, uint32_t base, ui
     __syncwarp();
     if (lane == 0) mbar_arrive(bar256(base, C::B_PF + (j & 1)));
   }
-  if (ok && nkv > 0) ok = __all_sync(0xffffffffu, wait_bar(b_od, (nkv - 1) & 1, ctl, kWhereODone));
+  // The last P.V, through its own barrier: a parity wait on B_OD for its
+  // phase would be ambiguous while an earlier P.V is still running (only
+  // the one before the previous is known complete here, from the last S).
+  if (ok && nkv > 0) ok = __all_sync(0xffffffffu, wait_bar(bar256(base, C::B_OL), 0, ctl, kWhereODone));
   if (!named_bar_and(1, 128, ok)) return;
 
   // ---- epilogue: O / l -> dtype -> swizzled staging (Q buffer) -> TMA store; LSE ----
@@ -362,6 +371,7 @@ __global__ void __launch_bounds__(C256::THREADS, 1) fa_fwd_d256_kernel(const __g
       mbar_init(bar256(base, C::B_PF + i), 4);  // one arrival per softmax warp
     }
     mbar_init(bar256(base, C::B_OD), 1);
+    mbar_init(bar256(base, C::B_OL), 1);
     mbar_init(bar256(base, C::B_DRAIN), 1);
     misc[1] = 0;
     mbar_init_fence();

@@ -300,8 +300,11 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
       // tensor pipe idle for ~200 cycles): S(j) is complete, so K_j has been
       // read, and so has V_{j-1}, since P(j-1) V_{j-1} was issued before S(j)
       // by the same warp and one commit covers all of its earlier MMAs.
-      mbar_arrive(bar_addr<D>(base, C::B_KE + j % C::STAGES));
+      // V first: once the producer sees a K phase complete, every warp's
+      // earlier V arrival has happened, so no warp can arrive for a stage's
+      // next tile while its current phase is still open.
       if (j > 0) mbar_arrive(bar_addr<D>(base, C::B_VE + (j - 1) % C::STAGES));
+      mbar_arrive(bar_addr<D>(base, C::B_KE + j % C::STAGES));
     }
     uint32_t sraw[C::BN / 32][32];
 #pragma unroll
