@@ -302,8 +302,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--causal", action="store_true",
                     help="causal mask (FLOPs counted for the keys each row sees: 4*d*N*(N+1)/2 per head)")
-    ap.add_argument("--splits", type=int, default=1,
-                    help="split-KV ranges (0 = automatic; 1 = the plain forward pass)")
+    ap.add_argument("--splits", type=int, default=0,
+                    help="split-KV ranges (0 = automatic, the default: unsplit unless the cost model finds the "
+                         "wave tail worth splitting; 1 = the plain forward pass)")
     ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
                     help="bwd: time the backward pass (fa_bwd: dQ, dK, dV; 10*B*H*N^2*d FLOPs) instead")
     ap.add_argument("--batch", type=int, default=None,

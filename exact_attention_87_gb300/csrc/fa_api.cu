@@ -181,13 +181,22 @@ long long kv_tiles(int N) { return (static_cast<long long>(N) + fa::kF16BlockKV 
 // + (s > 1) * (2 * s * rows * d * 4 bytes / 5 TB/s + 5 us)   the merge pass
 // with t_tile ~ 2 us * d / 128 for one 256-row unit and one 128-key tile on
 // one SM (measured on GB300 at ~2 GHz).
-int effective_splits(int B, int H, int N, int d, int num_splits, int num_sms) {
+// The tail plan: when the units end in a partial last wave, the full waves
+// run unsplit and only the last wave's units are split (as many ways as fit
+// in one wave), then merged:
+//   W * (tiles + 1) * t_tile + (tiles/s + 1) * t_tile + merge of the tail rows.
+struct SplitPlan {
+  int splits;            // key ranges per split unit (1: unsplit)
+  long long tail_qunit0; // >= 0: units before it unsplit, the rest split; < 0: every unit split alike
+};
+
+SplitPlan split_plan(int B, int H, int N, int d, int num_splits, int num_sms) {
   const long long tiles = kv_tiles(N);
-  if (num_splits > 0) return static_cast<int>(std::min<long long>(num_splits, tiles));
+  if (num_splits > 0) return {static_cast<int>(std::min<long long>(num_splits, tiles)), -1};
   const long long units = static_cast<long long>(B) * H * ((N + kQBlock - 1) / kQBlock);
   const double rows = static_cast<double>(B) * H * N;
   const double t_tile_us = 2.0 * d / 128.0;
-  int best = 1;
+  SplitPlan best{1, -1};
   double best_us = 1e300;
   for (int s = 1; s <= 16 && s <= tiles; ++s) {
     const long long per = (tiles + s - 1) / s;
@@ -195,9 +204,25 @@ int effective_splits(int B, int H, int N, int d, int num_splits, int num_sms) {
     const double waves = static_cast<double>((units * s + num_sms - 1) / num_sms);
     double us = waves * (static_cast<double>(per) + 1.0) * t_tile_us;
     if (s > 1) us += 2.0 * s * rows * d * 4.0 / 5e12 * 1e6 + 5.0;
-    if (us < best_us) { best_us = us; best = s; }
+    if (us < best_us) { best_us = us; best = {s, -1}; }
+  }
+  const long long full = units / num_sms, tail = units - full * num_sms;
+  if (full >= 1 && tail > 0) {
+    const long long s = std::min<long long>({num_sms / tail, tiles, 16});
+    if (s >= 2) {
+      const long long per = (tiles + s - 1) / s;
+      const double tail_rows = static_cast<double>(tail) * kQBlock;
+      const double us = static_cast<double>(full) * (static_cast<double>(tiles) + 1.0) * t_tile_us +
+                        (static_cast<double>(per) + 1.0) * t_tile_us + 2.0 * s * tail_rows * d * 4.0 / 5e12 * 1e6 +
+                        5.0;
+      if (us < best_us) best = {static_cast<int>(s), full * num_sms};
+    }
   }
   return best;
+}
+
+int effective_splits(int B, int H, int N, int d, int num_splits, int num_sms) {
+  return split_plan(B, H, N, d, num_splits, num_sms).splits;
 }
 
 unsigned long long workspace_bytes_for(int B, int H, int N, int d, int splits) {
@@ -250,7 +275,9 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
   p.num_sms = dev.num_sms;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // fp32 and d = 256 always run unsplit.
-  const int splits = (dtype == FA_F32 || d == 256) ? 1 : effective_splits(B, H, N, d, num_splits, dev.num_sms);
+  const SplitPlan plan = (dtype == FA_F32 || d == 256) ? SplitPlan{1, -1}
+                                                        : split_plan(B, H, N, d, num_splits, dev.num_sms);
+  const int splits = plan.splits;
   const long long tiles = kv_tiles(N);
   p.split_tiles = static_cast<int>((tiles + splits - 1) / splits);
   p.num_splits = static_cast<int>((tiles + p.split_tiles - 1) / p.split_tiles);
@@ -278,6 +305,25 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
       return FA_ERR_CUDA;
     if (d == 256) {
       e = fa::launch_fwd_d256(p, dtype == FA_BF16, s);
+    } else if (p.num_splits > 1 && plan.tail_qunit0 > 0) {
+      // Full waves unsplit (O written directly), then the last wave's units
+      // split, then the merge of their rows only.
+      const long long nqb = (N + kQBlock - 1) / kQBlock;
+      const long long qunits = static_cast<long long>(BH) * nqb;
+      fa::FwdParams pm = p;
+      pm.num_splits = 1;
+      pm.split_tiles = static_cast<int>(tiles);
+      pm.qunit0 = 0;
+      pm.qunit_count = static_cast<int>(plan.tail_qunit0);
+      e = fa::launch_fwd_f16(pm, dtype == FA_BF16, s);
+      if (e == cudaSuccess) {
+        fa::FwdParams pt = p;
+        pt.qunit0 = static_cast<int>(plan.tail_qunit0);
+        pt.qunit_count = static_cast<int>(qunits - plan.tail_qunit0);
+        pt.merge_row0 = (plan.tail_qunit0 / nqb) * N + (plan.tail_qunit0 % nqb) * kQBlock;
+        e = fa::launch_fwd_f16(pt, dtype == FA_BF16, s);
+        if (e == cudaSuccess) e = fa::launch_merge(pt, dtype == FA_BF16, s);
+      }
     } else {
       e = fa::launch_fwd_f16(p, dtype == FA_BF16, s);
       if (e == cudaSuccess && p.num_splits > 1) e = fa::launch_merge(p, dtype == FA_BF16, s);

@@ -505,7 +505,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
   // share a head so its K/V stay in L2 while its Q blocks are processed.
   const int nqb = (p.N + 2 * C::BM - 1) / (2 * C::BM);
   const int split = blockIdx.x % p.num_splits;
-  const int qunit = blockIdx.x / p.num_splits;
+  const int qunit = p.qunit0 + blockIdx.x / p.num_splits;
   const int bh = qunit / nqb;
   // Causal: Q blocks later in the sequence see more keys; they are launched first.
   const int qb = p.causal ? nqb - 1 - qunit % nqb : qunit % nqb;
@@ -608,8 +608,10 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(bit);
   }
-  const long long units =
-      static_cast<long long>(p.B) * p.H * ((p.N + 2 * C::BM - 1) / (2 * C::BM)) * p.num_splits;
+  const long long all_qunits = static_cast<long long>(p.B) * p.H * ((p.N + 2 * C::BM - 1) / (2 * C::BM));
+  const long long qunits = p.qunit_count > 0 ? p.qunit_count : all_qunits;
+  if (p.qunit0 < 0 || p.qunit0 + qunits > all_qunits) return cudaErrorInvalidValue;
+  const long long units = qunits * p.num_splits;
   if (units <= 0 || units > 0x7fffffffLL) return cudaErrorInvalidValue;
   kern<<<dim3(static_cast<unsigned>(units)), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
@@ -622,7 +624,7 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_merge_kernel(const __grid_constant__ FwdParams p) {
   constexpr int E = D / 32;
   const long long rows = static_cast<long long>(p.B) * p.H * p.N;
-  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long row = p.merge_row0 + ((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   float m = -INFINITY;
@@ -704,7 +706,8 @@ cudaError_t launch_merge_guarded_t(const FwdParams& p, cudaStream_t stream) {
 
 template <int D, bool BF16>
 cudaError_t launch_merge_t(const FwdParams& p, cudaStream_t stream) {
-  const long long rows = static_cast<long long>(p.B) * p.H * p.N;
+  const long long rows = static_cast<long long>(p.B) * p.H * p.N - p.merge_row0;
+  if (rows <= 0 || p.merge_row0 < 0) return cudaErrorInvalidValue;
   const long long blocks = (rows * 32 + 255) / 256;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   fa_merge_kernel<D, BF16><<<dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream>>>(p);

@@ -51,6 +51,14 @@ struct alignas(64) FwdParams {
   // as the one part of a merge done elsewhere (fa_merge).
   int Nk;
   int partial;
+  // Work units of this launch of the 16-bit kernel: Q blocks [qunit0,
+  // qunit0 + qunit_count) of the B*H*ceil(N/256) in (b*h, block) order, each
+  // split num_splits ways (qunit_count = 0: all of them). The split-KV merge
+  // covers rows [merge_row0, B*H*N). The wave tail of a launch is split this
+  // way: full waves unsplit, the last partial wave's units split.
+  int qunit0;
+  int qunit_count;
+  long long merge_row0;
   // Masks: causal (row i sees keys j <= i) and per-batch key lengths
   // (klen[b]: keys j >= klen[b] masked; NULL = all N keys).
   int causal;

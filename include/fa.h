@@ -109,7 +109,12 @@ int fa_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE,
  *
  * Arguments up to `dtype` are those of fa_fwd.
  * num_splits: >= 1 explicit (clamped to ceil(N/128)); 0 = chosen from the
- *             shape and the device's SM count (fa_fwd_splitkv_num_splits).
+ *             shape and the device's SM count (fa_fwd_splitkv_num_splits)
+ *             by a cost model, which can also pick the tail plan: when the
+ *             B*H*ceil(N/256) work units end in a partial last wave of SMs,
+ *             the full waves run unsplit and only the last wave's units are
+ *             split (as many ways as fit in one wave) and merged; that is
+ *             three launches (full waves, split tail, merge of its rows).
  * workspace:  device memory owned by the caller, 256-byte aligned, at least
  *             fa_fwd_splitkv_workspace_size(...) bytes; holds the per-range
  *             fp32 O and LSE. Unused (may be NULL) when the effective split

@@ -65,3 +65,31 @@ def test_splitkv_workspace_errors():
     # a split count of 1 needs no workspace
     assert fa.fa_fwd_splitkv(*args[:-1], 1, None, 0, None) == fa.FA_OK
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("B,H,N,d,dtype", [
+    (1, 4, 10240, 128, "bf16"),   # one full wave of units, the 12 left over split 12 ways
+    (1, 2, 20000, 128, "f16"),    # N not a multiple of 256: the last Q block of a head is partial
+    (8, 12, 2048, 128, "f16"),    # 768 units: 5 full waves, 28 split 5 ways
+])
+def test_splitkv_tail_plan(B, H, N, d, dtype):
+    """num_splits = 0 on shapes whose units end in a partial last wave: the
+    full waves run unsplit, the last wave's units split and merged. Rows of
+    the first and last heads (both sides of the split) against the oracle."""
+    assert fa.fa_fwd_splitkv_num_splits(B, H, N, d) >= 2
+    q, k, v = make_qkv(B, H, N, d, dtype, sigma_qk=1.5, seed=31, wid=11500 + N)
+    o, lse = fa.attention(q.cuda(), k.cuda(), v.cuda(), num_splits=0)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    rng = np.random.default_rng(N)
+    heads = [(0, 0), (B - 1, H - 1)] + ([(B - 1, H - 2)] if H > 1 else [])
+    rows = []
+    for b, h in heads:
+        for i in sorted({0, 255, 256, N - 1, N // 2, *rng.integers(0, N, 8).tolist()}):
+            rows.append((b, h, i))
+    o_ref, lse_ref = oracle.attn_rows(q, k, v, rows)
+    oc, lc = o.cpu().double().numpy(), lse.cpu().double().numpy()
+    res = compare(np.stack([oc[b, h, i] for b, h, i in rows]), np.array([lc[b, h, i] for b, h, i in rows]),
+                  o_ref, lse_ref, dtype)
+    assert res["ok"], res
+    assert np.all(np.isfinite(oc)) and np.all(np.isfinite(lc))
