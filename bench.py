@@ -302,15 +302,22 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--causal", action="store_true",
                     help="causal mask (FLOPs counted for the keys each row sees: 4*d*N*(N+1)/2 per head)")
-    ap.add_argument("--splits", type=int, default=0,
-                    help="split-KV ranges (0 = automatic, the default: unsplit unless the cost model finds the "
-                         "wave tail worth splitting; 1 = the plain forward pass)")
+    ap.add_argument("--splits", type=int, default=None,
+                    help="forward split-KV ranges (0 = automatic, the default: unsplit unless the cost model finds "
+                         "the wave tail worth splitting; 1 = the plain forward pass); masked and backward runs "
+                         "are unsplit")
     ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
                     help="bwd: time the backward pass (fa_bwd: dQ, dK, dV; 10*B*H*N^2*d FLOPs) instead")
     ap.add_argument("--batch", type=int, default=None,
                     help="override B (smaller captures of the same workload for profiling; not a bench line)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.which == "bwd" and args.splits not in (None, 1):
+        raise SystemExit("--pass bwd does not take --splits")
+    if args.splits is None:
+        args.splits = 1 if (args.causal or args.which == "bwd") else 0
+    if args.causal and args.splits != 1:
+        raise SystemExit("masks are not combined with split-KV: --causal takes --splits 1")
 
     import dataclasses
     from workloads import WORKLOADS, make_inputs
@@ -353,10 +360,17 @@ def main():
     stream = torch.cuda.current_stream(dev)
     ws_bytes = fa.fa_fwd_splitkv_workspace_size(w.B, w.H, w.N, w.d, args.splits) if args.splits != 1 else 0
     workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
-    n_splits = fa.fa_fwd_splitkv_num_splits(w.B, w.H, w.N, w.d) if args.splits == 0 else args.splits
-    if args.splits != 1:
-        cfg["num_splits"] = n_splits
-        cfg["launches_per_step"] = 2 if n_splits > 1 else 1
+    # The plan the library runs: 1 launch (unsplit), 2 (every unit split, merge) or 3 (split wave tail).
+    n_launch = 1
+    if args.splits != 1 and not args.causal and w.dtype != "f32" and w.d != 256:
+        n_launch = fa.fa_fwd_splitkv_launches(w.B, w.H, w.N, w.d, args.splits)
+        if n_launch < 1:
+            raise RuntimeError(f"fa_fwd_splitkv_launches failed ({n_launch})")
+        n_splits = fa.fa_fwd_splitkv_num_splits(w.B, w.H, w.N, w.d) if args.splits == 0 else args.splits
+        cfg["num_splits"] = n_splits if n_launch > 1 else 1
+        cfg["launches_per_step"] = n_launch
+        if n_launch == 3:
+            cfg["split_plan"] = "tail: full waves unsplit, the last wave's units split, their rows merged"
 
     def step():
         fa.attention(qd, kd, vd, scale=w.scale, out=o, lse=lse, stream=stream, num_splits=args.splits,
@@ -417,7 +431,7 @@ def main():
     peak, peak_src, _ = peaks()
     achieved = flops / (ms * 1e-3) / 1e12
     kind = "fwd_d256" if w.d == 256 else "fwd"
-    traffic = recorded_traffic(w.name, kind) if not args.causal and args.splits == 1 else None
+    traffic = recorded_traffic(w.name, kind) if not args.causal and n_launch == 1 else None
     line = {
         "metric": "attention fwd TFLOP/s (4*B*H*N^2*d) and % of GB300 dense BF16 tensor peak",
         "value": round(tflops, 2),
@@ -440,7 +454,7 @@ def main():
                                 f"fa_fwd_f16_kernel<{w.d},{'bf16' if w.dtype == 'bf16' else 'f16'}>"),
                      "traffic": traffic, "algorithmic_bytes": w.hbm_bytes},
         "clocks": sampler.summary(),
-        "gpu_launches": args.steps * (2 if args.splits != 1 and n_splits > 1 else 1),
+        "gpu_launches": args.steps * n_launch,
         "e2e": e2e,
     }
     if ws == 1 and not args.no_cpu_baseline:
@@ -461,8 +475,6 @@ def run_backward(args, w, cfg, ws, rank, local):
     import exact_attention_87_gb300 as fa
     from workloads import make_dout, make_inputs
 
-    if args.splits != 1:
-        raise SystemExit("--pass bwd does not take --splits")
     causal = bool(args.causal)
     if ws > 1:
         torch.cuda.set_device(local)

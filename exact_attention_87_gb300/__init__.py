@@ -74,6 +74,8 @@ def lib(path: str | None = None):
     L.fa_bwd.restype = i
     L.fa_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, vp, u64, vp]
     L.fa_bwd_ex.restype = i
+    L.fa_fwd_splitkv_launches.argtypes = [i, i, i, i, i]
+    L.fa_fwd_splitkv_launches.restype = i
     L.fa_fwd_partial.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
     L.fa_fwd_partial.restype = i
     L.fa_merge.argtypes = [vp, vp, i, vp, vp, i, i, i, i, i, vp]
@@ -119,6 +121,10 @@ def fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype, workspace,
            stream=None) -> int:
     return lib().fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype, workspace, workspace_bytes,
                         stream)
+
+
+def fa_fwd_splitkv_launches(B, H, N, d, num_splits) -> int:
+    return lib().fa_fwd_splitkv_launches(B, H, N, d, num_splits)
 
 
 def fa_fwd_partial(Q, K, V, O_part, LSE_part, B, H, Nq, Nk, d, scale, dtype, stream=None) -> int:
@@ -357,6 +363,7 @@ def attention_backward(q, k, v, o, lse, do, scale: float | None = None, dq=None,
 
 
 __all__ = ["attention", "attention_backward", "attention_partial", "merge_partials", "fa_fwd_partial", "fa_merge",
+           "fa_fwd_splitkv_launches",
            "fa_bwd", "fa_bwd_ex", "fa_bwd_workspace_size", "fa_fwd", "fa_fwd_ex", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_num_splits",
            "fa_fwd_splitkv_workspace_size",
            "fa_get_device_status", "fa_strerror", "fa_abi_version", "build", "lib",

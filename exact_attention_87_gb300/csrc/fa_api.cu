@@ -461,6 +461,20 @@ int fa_fwd_splitkv_noalloc(const void* Q, const void* K, const void* V, void* O,
                   FA_NOALLOC_SCRATCH_BYTES);
 }
 
+int fa_fwd_splitkv_launches(int B, int H, int N, int d, int num_splits) {
+  if (B < 1 || H < 1 || N < 1 || num_splits < 0) return -FA_ERR_SHAPE;
+  if (d == 256) return 1;
+  if (d != 64 && d != 128) return -FA_ERR_HEADDIM;
+  DeviceInfo dev;
+  const int st = device_info(&dev);
+  if (st != FA_OK) return -st;
+  const SplitPlan plan = split_plan(B, H, N, d, num_splits, dev.num_sms);
+  const long long tiles = kv_tiles(N);
+  const long long per = (tiles + plan.splits - 1) / plan.splits;
+  if ((tiles + per - 1) / per <= 1) return 1;
+  return plan.tail_qunit0 > 0 ? 3 : 2;
+}
+
 int fa_fwd_splitkv_num_splits(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1) return -FA_ERR_SHAPE;
   if (d == 256) return 1;  // the d = 256 kernel runs unsplit

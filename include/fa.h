@@ -130,6 +130,12 @@ int fa_fwd_splitkv(const void *Q, const void *K, const void *V, void *O, float *
  * device (>= 1), or a negative fa_status on error. */
 int fa_fwd_splitkv_num_splits(int B, int H, int N, int d);
 
+/* Kernel launches fa_fwd_splitkv enqueues for this shape and split count on
+ * the current device, for FA_F16 / FA_BF16 inputs: 1 (unsplit), 2 (every
+ * unit split, then the merge) or 3 (the tail plan: full waves, the split
+ * tail, the merge of its rows); a negative fa_status on error. */
+int fa_fwd_splitkv_launches(int B, int H, int N, int d, int num_splits);
+
 /* Workspace bytes fa_fwd_splitkv needs for this shape and split count
  * (num_splits = 0: the automatic count); 0 when no workspace is needed. */
 unsigned long long fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits);

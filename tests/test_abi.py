@@ -105,6 +105,13 @@ def test_splitkv_workspace_size_formula(L):
     assert fa.fa_fwd_splitkv(A, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, -1, A, 1 << 20, None) == fa.FA_ERR_SHAPE
 
 
+def test_splitkv_launch_count_argument_errors(L):
+    assert fa.fa_fwd_splitkv_launches(0, 1, 64, 64, 0) == -fa.FA_ERR_SHAPE
+    assert fa.fa_fwd_splitkv_launches(1, 1, 64, 64, -1) == -fa.FA_ERR_SHAPE
+    assert fa.fa_fwd_splitkv_launches(1, 1, 64, 96, 0) == -fa.FA_ERR_HEADDIM
+    assert fa.fa_fwd_splitkv_launches(1, 1, 64, 256, 0) == 1  # the d = 256 kernel runs unsplit
+
+
 def test_masked_entry_point_argument_errors(L):
     assert fa.fa_fwd_ex(A, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, 2, None, None) == fa.FA_ERR_SHAPE
     assert fa.fa_fwd_ex(0, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, 1, None, None) == fa.FA_ERR_NULL

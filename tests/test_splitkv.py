@@ -77,6 +77,7 @@ def test_splitkv_tail_plan(B, H, N, d, dtype):
     full waves run unsplit, the last wave's units split and merged. Rows of
     the first and last heads (both sides of the split) against the oracle."""
     assert fa.fa_fwd_splitkv_num_splits(B, H, N, d) >= 2
+    assert fa.fa_fwd_splitkv_launches(B, H, N, d, 0) == 3
     q, k, v = make_qkv(B, H, N, d, dtype, sigma_qk=1.5, seed=31, wid=11500 + N)
     o, lse = fa.attention(q.cuda(), k.cuda(), v.cuda(), num_splits=0)
     torch.cuda.synchronize()
