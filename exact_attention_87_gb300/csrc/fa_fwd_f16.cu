@@ -13,9 +13,10 @@
 //
 // GB300 mapping (one CTA per (batch*head, 256-row Q block), 12 warps):
 //   warp 9      TMA producer: Q0/Q1 once, then K_j and V_j (128 keys each)
-//               into 2-stage (d=128) / 3-stage (d=64) rings; the softmax
-//               warps free a stage once the S product they wait for shows
-//               that its K (and the previous tile's V) have been read
+//               into 2-stage (d=128) / 3-stage (d=64) rings; for d=128 the
+//               softmax warps free a stage once the S product they wait for
+//               shows that its K (and the previous tile's V) have been read,
+//               for d=64 commits behind the MMAs do
 //   warps 8, 10 MMA warps, one per Q sub-tile i: S_i(j) = Q_i K_j^T (SS, into
 //               TMEM), then O_i += P_i(j) V_j (TS: P read from TMEM, V from
 //               SMEM); one elected lane issues; warp 8 also owns TMEM
@@ -58,6 +59,10 @@ struct Cfg {
   static constexpr int BM = kF16BlockQ;   // Q rows per sub-tile (= TMEM lanes)
   static constexpr int BN = kF16BlockKV;  // keys per K/V tile
   static constexpr int STAGES = (D == 128) ? 2 : 3;
+  // Who frees the K/V stages: the softmax warps (d = 128: keeps commits out
+  // of the MMA issue stream, whose blocks are long) or commits behind the MMAs
+  // (d = 64: short blocks, and the softmax is the longer part of the chain).
+  static constexpr bool SOFTMAX_FREES_STAGES = (D == 128);
   static constexpr uint32_t ROW_BYTES = 128;               // one 128-byte swizzle row = 64 elements
   static constexpr uint32_t Q_SUB_BYTES = BM * D * 2;      // one Q sub-tile
   static constexpr uint32_t Q_HALF_BYTES = BM * ROW_BYTES; // 64 columns of a Q sub-tile
@@ -222,6 +227,7 @@ __device__ __forceinline__ void mma_warp(const FwdParams& p, uint32_t base, uint
       // follows S(j) (same warp, issued after it); only the last P.V, which no
       // S follows, is committed on its own (strict order: every P.V is).
       if (kOdEveryTile || j == nkv) tc_commit_elect(b_od);
+      if constexpr (!C::SOFTMAX_FREES_STAGES) tc_commit_elect(bar_addr<D>(base, C::B_VE + s));
       FA_TRACE(p, kEvPV0Issued + sub, j - 1);
     }
     if (j < nkv) {
@@ -248,6 +254,7 @@ __device__ __forceinline__ void mma_warp(const FwdParams& p, uint32_t base, uint
         mma_f16_ss_elect(d_s, a0 + aoff, b0 + boff, idesc_qk, kk > 0 ? 1u : 0u);
       }
       tc_commit_elect(b_sf);
+      if constexpr (!C::SOFTMAX_FREES_STAGES) tc_commit_elect(bar_addr<D>(base, C::B_KE + s));
       FA_TRACE(p, kEvS0Issued + sub, j);
     }
     if (has1) {
@@ -294,7 +301,7 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
     }
     tc_fence_after();
     if (t == 0) FA_TRACE(p, kEvSm0SFull + 2 * sub, j);
-    if (lane == 0) {
+    if (C::SOFTMAX_FREES_STAGES && lane == 0) {
       // The K/V stages are released from here, not by commits in the MMA
       // warp's issue stream (a commit right behind a group of MMAs leaves the
       // tensor pipe idle for ~200 cycles): S(j) is complete, so K_j has been
@@ -523,12 +530,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
 
   if (threadIdx.x == 0) {
     mbar_init(bar_addr<D>(base, C::B_Q), 1);
-    const uint32_t nsub = has1 ? 2u : 1u;  // the stage-empty barriers get one arrival per softmax warp of each sub-tile
+    const uint32_t nsub = has1 ? 2u : 1u;  // the stage-empty barriers get releases from each sub-tile
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar_addr<D>(base, C::B_KF + s), 1);
-      mbar_init(bar_addr<D>(base, C::B_KE + s), 4 * nsub);  // one arrival per softmax warp
+      // one arrival per softmax warp (d = 128) or one commit per MMA warp (d = 64)
+      mbar_init(bar_addr<D>(base, C::B_KE + s), C::SOFTMAX_FREES_STAGES ? 4 * nsub : nsub);
       mbar_init(bar_addr<D>(base, C::B_VF + s), 1);
-      mbar_init(bar_addr<D>(base, C::B_VE + s), 4 * nsub);
+      mbar_init(bar_addr<D>(base, C::B_VE + s), C::SOFTMAX_FREES_STAGES ? 4 * nsub : nsub);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_addr<D>(base, C::B_SF + i), 1);
