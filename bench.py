@@ -467,6 +467,15 @@ def main():
         dist.destroy_process_group()
 
 
+def bwd_config(cfg, causal: bool) -> dict:
+    """The `config` of a backward line (both arms)."""
+    cfg = dict(cfg)
+    cfg["pass"] = "bwd"
+    cfg["flops"] = ("10*B*H*d*N*(N+1)/2 (S, dP, dV, dK, dQ over the causal pairs)" if causal
+                    else "10*B*H*N^2*d (S, dP, dV, dK, dQ products)")
+    return cfg
+
+
 def run_backward(args, w, cfg, ws, rank, local):
     """Time the backward pass (fa_bwd: row statistics, main pass, dQ rounding) for
     the workload, given the forward pass's O and LSE and a seeded dO."""
@@ -485,11 +494,9 @@ def run_backward(args, w, cfg, ws, rank, local):
     fa.lib()
     if causal:  # the five products over the (query, key) pairs each row sees
         flops = 10 * w.B * w.H * w.d * w.N * (w.N + 1) // 2
-        cfg = dict(cfg, pass_="bwd", flops="10*B*H*d*N*(N+1)/2 (S, dP, dV, dK, dQ over the causal pairs)")
     else:
         flops = 10 * w.B * w.H * w.N * w.N * w.d  # five N x N x d products per (b, h)
-        cfg = dict(cfg, pass_="bwd", flops="10*B*H*N^2*d (S, dP, dV, dK, dQ products)")
-    cfg["pass"] = cfg.pop("pass_")
+    cfg = bwd_config(cfg, causal)
     q, k, v = make_inputs(w)
     do = make_dout(w.B, w.H, w.N, w.d, w.dtype, seed=0, wid=w.wid)
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
@@ -602,36 +609,68 @@ def run_backward(args, w, cfg, ws, rank, local):
 
 
 def run_reference(args, w, cfg, ws, rank):
-    """The oracle, as it stands, on host cores: each step is a bounded sample of the workload."""
+    """The oracle, as it stands, on host cores: each step is a bounded sample of the workload
+    (forward: query rows of one head against all its keys; backward: one head truncated to its
+    first n tokens, the oracle backward timed)."""
     if rank != 0:
         return
-    from workloads import make_inputs
+    from workloads import make_dout, make_inputs
     import oracle
     q, k, v = make_inputs(w)
     threads = oracle.default_threads()
-    # size one step: whole heads, about 2 s of CPU work each at most, one head at least
-    t0 = time.perf_counter()
-    oracle.attn(q[0, 0, :64], k[0, 0], v[0, 0], scale=w.scale, nthreads=threads)
-    per_row = (time.perf_counter() - t0) / 64
-    rows = int(max(64, min(w.N, 1.5 / max(per_row, 1e-9))))
     heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    causal = bool(args.causal)
+    if args.which == "bwd":
+        do = make_dout(w.B, w.H, w.N, w.d, w.dtype, seed=0, wid=w.wid)
+        n = min(w.N, 512)
 
-    def step(i):
-        b, h = heads[i % len(heads)]
-        oracle.attn(q[b, h, :rows], k[b, h], v[b, h], scale=w.scale, nthreads=threads)
+        def sl(t, b, h):
+            return t[b, h, :n].unsqueeze(0).unsqueeze(0)
+
+        def step(i):
+            b, h = heads[i % len(heads)]
+            qs, ks, vs, ds = (sl(t, b, h) for t in (q, k, v, do))
+            o, lse = oracle.attn_masked(qs, ks, vs, causal=causal, scale=w.scale, nthreads=threads)
+            t0 = time.perf_counter()
+            oracle.attn_bwd(qs, ks, vs, o, ds, lse, scale=w.scale, nthreads=threads, causal=causal)
+            return time.perf_counter() - t0
+
+        flops_per_step = 10 * w.d * (n * (n + 1) // 2 if causal else n * n)
+        cfg = bwd_config(cfg, causal)
+        metric = ("attention bwd TFLOP/s (" + ("causal, 10*B*H*d*N*(N+1)/2" if causal else "10*B*H*N^2*d") +
+                  ") and % of GB300 dense BF16 tensor peak")
+        desc = f"per step one (b, h) truncated to its first {n} tokens (fp64 backward timed; its O, LSE untimed)"
+    else:
+        # size one step: whole key sets, about 1.5 s of CPU work each at most, 64 query rows at least
+        t0 = time.perf_counter()
+        oracle.attn(q[0, 0, :64], k[0, 0], v[0, 0], scale=w.scale, nthreads=threads)
+        per_row = (time.perf_counter() - t0) / 64
+        rows = int(max(64, min(w.N, 1.5 / max(per_row, 1e-9))))
+
+        def step(i):
+            b, h = heads[i % len(heads)]
+            t0 = time.perf_counter()
+            if causal:
+                # the first `rows` queries see keys 0..row: the causal rows of the head
+                oracle.attn_masked(q[b, h, :rows].unsqueeze(0).unsqueeze(0), k[b, h, :rows].unsqueeze(0).unsqueeze(0),
+                                   v[b, h, :rows].unsqueeze(0).unsqueeze(0), causal=True, scale=w.scale,
+                                   nthreads=threads)
+            else:
+                oracle.attn(q[b, h, :rows], k[b, h], v[b, h], scale=w.scale, nthreads=threads)
+            return time.perf_counter() - t0
+
+        flops_per_step = 4 * w.d * (rows * (rows + 1) // 2 if causal else rows * w.N)
+        metric = "attention fwd TFLOP/s (4*B*H*N^2*d) and % of GB300 dense BF16 tensor peak"
+        desc = (f"per step the first {rows} query rows of one (b, h) against " +
+                ("the keys each sees (causal)" if causal else f"all {w.N} keys") + " (fp64 three-pass)")
 
     for i in range(args.warmup):
         step(i)
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        step(args.warmup + i)
-    secs = time.perf_counter() - t0
-    flops = args.steps * 4 * rows * w.N * w.d
-    value = flops / secs / 1e12
+    secs = sum(step(args.warmup + i) for i in range(args.steps))
+    value = args.steps * flops_per_step / secs / 1e12
     ms = secs / args.steps * 1e3
-    desc = f"per step {rows} query rows of one (b, h) against all {w.N} keys (fp64 three-pass)"
     line = {
-        "metric": "attention fwd TFLOP/s (4*B*H*N^2*d) and % of GB300 dense BF16 tensor peak",
+        "metric": metric,
         "impl": "reference", "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)", "config": cfg,
