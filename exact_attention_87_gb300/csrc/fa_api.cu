@@ -225,11 +225,20 @@ int effective_splits(int B, int H, int N, int d, int num_splits, int num_sms) {
   return split_plan(B, H, N, d, num_splits, num_sms).splits;
 }
 
-unsigned long long workspace_bytes_for(int B, int H, int N, int d, int splits) {
+// Partial O and LSE of `splits` key ranges over the rows from row0 on (the
+// rows of the split units: all rows, or those of the wave tail).
+unsigned long long workspace_bytes_for(int B, int H, int N, int d, int splits, long long row0 = 0) {
   if (splits <= 1) return 0;
-  const unsigned long long rows = static_cast<unsigned long long>(B) * H * N * splits;
+  const unsigned long long rows = (static_cast<unsigned long long>(B) * H * N - row0) * splits;
   const unsigned long long o_bytes = (rows * d * 4 + 255) & ~255ull;
   return o_bytes + rows * 4;
+}
+
+// First row of the split units of a plan (0 unless only the wave tail is split).
+long long plan_row0(const SplitPlan& plan, int N) {
+  if (plan.tail_qunit0 <= 0) return 0;
+  const long long nqb = (N + kQBlock - 1) / kQBlock;
+  return (plan.tail_qunit0 / nqb) * N + (plan.tail_qunit0 % nqb) * kQBlock;
 }
 
 int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
@@ -281,11 +290,12 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
   const long long tiles = kv_tiles(N);
   p.split_tiles = static_cast<int>((tiles + splits - 1) / splits);
   p.num_splits = static_cast<int>((tiles + p.split_tiles - 1) / p.split_tiles);
+  const long long row0 = (p.num_splits > 1) ? plan_row0(plan, N) : 0;
   if (p.num_splits > 1) {
-    const unsigned long long need = workspace_bytes_for(B, H, N, d, p.num_splits);
+    const unsigned long long need = workspace_bytes_for(B, H, N, d, p.num_splits, row0);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
       return FA_ERR_WORKSPACE;
-    const unsigned long long rows = static_cast<unsigned long long>(B) * H * N * p.num_splits;
+    const unsigned long long rows = (static_cast<unsigned long long>(B) * H * N - row0) * p.num_splits;
     p.o_part = static_cast<float*>(workspace);
     p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((rows * d * 4 + 255) & ~255ull));
   }
@@ -320,7 +330,7 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
         fa::FwdParams pt = p;
         pt.qunit0 = static_cast<int>(plan.tail_qunit0);
         pt.qunit_count = static_cast<int>(qunits - plan.tail_qunit0);
-        pt.merge_row0 = (plan.tail_qunit0 / nqb) * N + (plan.tail_qunit0 % nqb) * kQBlock;
+        pt.merge_row0 = row0;
         e = fa::launch_fwd_f16(pt, dtype == FA_BF16, s);
         if (e == cudaSuccess) e = fa::launch_merge(pt, dtype == FA_BF16, s);
       }
@@ -487,15 +497,17 @@ int fa_fwd_splitkv_num_splits(int B, int H, int N, int d) {
 
 unsigned long long fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits) {
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || num_splits < 0) return 0;  // d = 256: unsplit, none
-  int splits = num_splits;
-  if (splits == 0) {
-    splits = fa_fwd_splitkv_num_splits(B, H, N, d);
-    if (splits < 1) return 0;
+  SplitPlan plan{num_splits, -1};
+  if (num_splits == 0) {
+    DeviceInfo dev;
+    if (device_info(&dev) != FA_OK) return 0;
+    plan = split_plan(B, H, N, d, 0, dev.num_sms);
   }
   const long long tiles = kv_tiles(N);
-  splits = static_cast<int>(std::min<long long>(splits, tiles));
+  const long long splits = std::min<long long>(plan.splits, tiles);
   const long long per = (tiles + splits - 1) / splits;
-  return workspace_bytes_for(B, H, N, d, static_cast<int>((tiles + per - 1) / per));
+  const int eff = static_cast<int>((tiles + per - 1) / per);
+  return workspace_bytes_for(B, H, N, d, eff, eff > 1 ? plan_row0(plan, N) : 0);
 }
 
 }  // extern "C"

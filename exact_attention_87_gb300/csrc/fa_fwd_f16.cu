@@ -442,7 +442,10 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
     // Split-KV (or one part of a merge done elsewhere): this key range's
     // normalised O (fp32) and LSE go to the partial buffers.
     const int row = row0 + C::BM * sub + t;
-    const size_t prow = (static_cast<size_t>(split) * p.B * p.H + bh) * p.N + row;
+    // Partial rows are numbered from merge_row0 (the first row of the split
+    // units; 0 unless only the wave tail is split), one span per key range.
+    const size_t span = static_cast<size_t>(p.B) * p.H * p.N - p.merge_row0;
+    const size_t prow = static_cast<size_t>(split) * span + (static_cast<size_t>(bh) * p.N + row - p.merge_row0);
 #pragma unroll
     for (int q = 0; q < D / 32; ++q) {
       uint32_t r[32];
@@ -635,16 +638,18 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const __grid_constant__ F
   const long long row = p.merge_row0 + ((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
+  // partial rows numbered from merge_row0, one span per key range (as the split epilogue writes them)
+  const long long span = rows - p.merge_row0, prow = row - p.merge_row0;
   float m = -INFINITY;
-  for (int s = 0; s < p.num_splits; ++s) m = fmaxf(m, p.lse_part[s * rows + row]);
+  for (int s = 0; s < p.num_splits; ++s) m = fmaxf(m, p.lse_part[s * span + prow]);
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   float l = 0.f;
   for (int s = 0; s < p.num_splits; ++s) {
-    const float w = ex2_approx((p.lse_part[s * rows + row] - m) * kLog2e);
+    const float w = ex2_approx((p.lse_part[s * span + prow] - m) * kLog2e);
     l += w;
-    const float* src = p.o_part + (s * rows + row) * D + lane * E;
+    const float* src = p.o_part + (s * span + prow) * D + lane * E;
     if constexpr (E == 4) {
       const float4 x = *reinterpret_cast<const float4*>(src);
       acc[0] = fmaf(w, x.x, acc[0]);

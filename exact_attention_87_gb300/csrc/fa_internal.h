@@ -41,7 +41,8 @@ struct alignas(64) FwdParams {
   int num_sms;
   // Split-KV: each CTA covers split_tiles K/V tiles of one of num_splits key
   // ranges and writes its normalised fp32 O and its LSE to o_part / lse_part
-  // ([num_splits, B*H*N, d] and [num_splits, B*H*N]); num_splits == 1: no split.
+  // ([num_splits, R, d] and [num_splits, R] over the R = B*H*N - merge_row0
+  // rows from merge_row0 on); num_splits == 1: no split.
   int num_splits;
   int split_tiles;
   float* o_part;

@@ -117,10 +117,12 @@ int fa_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE,
  *             three launches (full waves, split tail, merge of its rows).
  * workspace:  device memory owned by the caller, 256-byte aligned, at least
  *             fa_fwd_splitkv_workspace_size(...) bytes; holds the per-range
- *             fp32 O and LSE. Unused (may be NULL) when the effective split
- *             count is 1, and for FA_F32 inputs, which always run unsplit.
- * Errors: those of fa_fwd, plus FA_ERR_WORKSPACE. Two launches are enqueued
- * on `stream` (partials, then merge); nothing is synchronised.
+ *             fp32 O and LSE of the split rows only (all B*H*N rows, or under
+ *             the tail plan the rows of the last wave's units). Unused (may be
+ *             NULL) when the effective split count is 1, and for FA_F32
+ *             inputs, which always run unsplit.
+ * Errors: those of fa_fwd, plus FA_ERR_WORKSPACE. Two or three launches are
+ * enqueued on `stream` (fa_fwd_splitkv_launches); nothing is synchronised.
  */
 int fa_fwd_splitkv(const void *Q, const void *K, const void *V, void *O, float *LSE,
                    int B, int H, int N, int d, float scale, int dtype,
@@ -136,8 +138,9 @@ int fa_fwd_splitkv_num_splits(int B, int H, int N, int d);
  * tail, the merge of its rows); a negative fa_status on error. */
 int fa_fwd_splitkv_launches(int B, int H, int N, int d, int num_splits);
 
-/* Workspace bytes fa_fwd_splitkv needs for this shape and split count
- * (num_splits = 0: the automatic count); 0 when no workspace is needed. */
+/* Workspace bytes fa_fwd_splitkv needs for this shape and split count on the
+ * current device (num_splits = 0: the automatic plan, which depends on the
+ * SM count); 0 when no workspace is needed or on error. */
 unsigned long long fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits);
 
 /*

@@ -94,3 +94,30 @@ def test_splitkv_tail_plan(B, H, N, d, dtype):
                   o_ref, lse_ref, dtype)
     assert res["ok"], res
     assert np.all(np.isfinite(oc)) and np.all(np.isfinite(lc))
+
+
+def test_splitkv_tail_plan_workspace_covers_only_the_tail_rows():
+    """Under the tail plan the partial buffers hold the split rows only: the
+    workspace is smaller than the one every row split alike would need, a
+    byte less is refused, and the launches write nothing past its end."""
+    B, H, N, d = 1, 4, 10240, 128
+    assert fa.fa_fwd_splitkv_launches(B, H, N, d, 0) == 3
+    splits = fa.fa_fwd_splitkv_num_splits(B, H, N, d)
+    need = fa.fa_fwd_splitkv_workspace_size(B, H, N, d, 0)
+    assert 0 < need < fa.fa_fwd_splitkv_workspace_size(B, H, N, d, splits)
+    q, k, v = make_qkv(B, H, N, d, "bf16", sigma_qk=1.5, seed=32, wid=11600)
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    o, lse = torch.empty_like(qc), torch.empty((B, H, N), device="cuda")
+    ws = torch.full((need + 65536,), 0x5A, dtype=torch.uint8, device="cuda")
+    args = (qc.data_ptr(), kc.data_ptr(), vc.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, d ** -0.5,
+            fa.FA_BF16, 0)
+    assert fa.fa_fwd_splitkv(*args, ws.data_ptr(), need - 1, None) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_fwd_splitkv(*args, ws.data_ptr(), need, None) == fa.FA_OK
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    assert bool((ws[need:] == 0x5A).all())
+    o_ref, lse_ref = fa.attention(qc, kc, vc, num_splits=1)
+    torch.cuda.synchronize()
+    # the same rows as the unsplit pass up to the merge's rounding
+    assert float((o.float() - o_ref.float()).abs().max()) <= 1e-2
+    assert float((lse - lse_ref).abs().max()) <= 1e-4 * max(1.0, float(lse_ref.abs().max()))

@@ -68,3 +68,20 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     rc = fa.fa_fwd_splitkv_noalloc(a, a, a, a, a, B, H, N, d, d ** -0.5, fa.FA_BF16, splits, None)
     assert rc == fa.FA_ERR_SCRATCH_LIMIT
     assert "scratch" in fa.fa_strerror(rc)
+
+
+def test_noalloc_runs_the_automatic_plan_on_the_long_sequence_workload():
+    """B=1, H=8, N=16384, d=128 with the automatic plan: the tail plan's
+    partial buffers (the last wave's rows only) fit the built-in scratch, and
+    the result equals the workspace entry point's bit for bit."""
+    fa.build()
+    B, H, N, d = 1, 8, 16384, 128
+    need = fa.fa_fwd_splitkv_workspace_size(B, H, N, d, 0)
+    assert need <= (32 << 20)
+    q, k, v = (t.cuda() for t in make_qkv(B, H, N, d, "bf16", sigma_qk=1.0, seed=33, wid=12500))
+    o_ref, l_ref = _run_with_workspace(q, k, v, 0)
+    o, l = _run_noalloc(q, k, v, 0)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    assert torch.equal(o, o_ref) and torch.equal(l, l_ref)
+    assert bool(torch.isfinite(o).all())
