@@ -16,8 +16,9 @@
 //               right behind P_j V_j, whose P it overwrites (one CTA's MMAs
 //               execute in issue order), so the softmax of tile j runs while
 //               S_{j+1} is on the tensor pipe
-//   warps 0-3   softmax (thread = row = TMEM lane): max, lazy rescale of l and
-//               O, P = 2^(s*c - m) packed to 16 bits over the S columns; then
+//   warps 0-3   softmax (thread = row = TMEM lane): frees K_j's stage once S_j
+//               is complete, max, lazy rescale of l and O, P = 2^(s*c - m)
+//               packed to 16 bits over the S columns; then
 //               the epilogue
 // TMEM (512 columns): S0 [0,64), S1 [64,128), O [256,512). With one 128-row
 // Q tile per CTA the 256 fp32 O columns fit; two Q tiles would not.
@@ -138,7 +139,6 @@ __device__ __forceinline__ void mma256(uint32_t base, uint32_t tmem, int nkv, co
       mma_f16_ss_elect(tmem + t_s256(j & 1), a0 + aoff, b0 + boff, idesc_qk, kk > 0 ? 1u : 0u);
     }
     tc_commit_elect(bar256(base, C::B_SF + (j & 1)));
-    tc_commit_elect(bar256(base, C::B_KE + s));
   };
 
   if (nkv == 0) goto drain;
@@ -205,6 +205,10 @@ __device__ __forceinline__ void softmax256(const FwdParams& p, uint32_t base, ui
       break;
     }
     tc_fence_after();
+    // S_j is complete, so K_j has been read: the softmax warps free its stage
+    // (an arrival here instead of a commit behind the S MMAs, which would
+    // keep the tensor pipe idle while it is processed).
+    if (lane == 0) mbar_arrive(bar256(base, C::B_KE + j % C::STAGES));
     uint32_t sraw[2][32];
     tmem_ld32(t_s, sraw[0]);
     tmem_ld32(t_s + 32, sraw[1]);
@@ -362,7 +366,7 @@ __global__ void __launch_bounds__(C256::THREADS, 1) fa_fwd_d256_kernel(const __g
     mbar_init(bar256(base, C::B_Q), 1);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar256(base, C::B_KF + s), 1);
-      mbar_init(bar256(base, C::B_KE + s), 1);
+      mbar_init(bar256(base, C::B_KE + s), 4);  // one arrival per softmax warp
       mbar_init(bar256(base, C::B_VF + s), 1);
       mbar_init(bar256(base, C::B_VE + s), 1);
     }
