@@ -76,6 +76,10 @@ def lib(path: str | None = None):
     L.fa_bwd_ex.restype = i
     L.fa_fwd_splitkv_launches.argtypes = [i, i, i, i, i]
     L.fa_fwd_splitkv_launches.restype = i
+    L.fa_fwd_splitkv_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int),
+                                      ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_int),
+                                      ctypes.POINTER(ctypes.c_ulonglong)]
+    L.fa_fwd_splitkv_plan.restype = i
     L.fa_fwd_partial.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
     L.fa_fwd_partial.restype = i
     L.fa_merge.argtypes = [vp, vp, i, vp, vp, i, i, i, i, i, vp]
@@ -125,6 +129,17 @@ def fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype, workspace,
 
 def fa_fwd_splitkv_launches(B, H, N, d, num_splits) -> int:
     return lib().fa_fwd_splitkv_launches(B, H, N, d, num_splits)
+
+
+def fa_fwd_splitkv_plan(B, H, N, d, num_splits, num_sms) -> tuple[int, dict | None]:
+    """(status, plan) with plan = {splits, first_split_unit, launches,
+    workspace_bytes} for a device with num_sms SMs (host arithmetic only)."""
+    s, f, n, w = ctypes.c_int(), ctypes.c_longlong(), ctypes.c_int(), ctypes.c_ulonglong()
+    rc = lib().fa_fwd_splitkv_plan(B, H, N, d, num_splits, num_sms, ctypes.byref(s), ctypes.byref(f),
+                                   ctypes.byref(n), ctypes.byref(w))
+    if rc != FA_OK:
+        return rc, None
+    return rc, {"splits": s.value, "first_split_unit": f.value, "launches": n.value, "workspace_bytes": w.value}
 
 
 def fa_fwd_partial(Q, K, V, O_part, LSE_part, B, H, Nq, Nk, d, scale, dtype, stream=None) -> int:

@@ -221,10 +221,6 @@ SplitPlan split_plan(int B, int H, int N, int d, int num_splits, int num_sms) {
   return best;
 }
 
-int effective_splits(int B, int H, int N, int d, int num_splits, int num_sms) {
-  return split_plan(B, H, N, d, num_splits, num_sms).splits;
-}
-
 // Partial O and LSE of `splits` key ranges over the rows from row0 on (the
 // rows of the split units: all rows, or those of the wave tail).
 unsigned long long workspace_bytes_for(int B, int H, int N, int d, int splits, long long row0 = 0) {
@@ -239,6 +235,29 @@ long long plan_row0(const SplitPlan& plan, int N) {
   if (plan.tail_qunit0 <= 0) return 0;
   const long long nqb = (N + kQBlock - 1) / kQBlock;
   return (plan.tail_qunit0 / nqb) * N + (plan.tail_qunit0 % nqb) * kQBlock;
+}
+
+// What a 16-bit split-KV pass does for a shape on a device with num_sms SMs:
+// the key ranges per split unit after clamping to whole tiles, the first
+// split unit, the launches and the workspace. Host arithmetic only.
+struct PlanSummary {
+  int splits;              // key ranges of each split unit (1: nothing is split)
+  long long first_split;   // first split work unit (all units: nothing is split)
+  int launches;            // 1, 2 or 3
+  unsigned long long workspace;
+};
+
+PlanSummary summarize_plan(int B, int H, int N, int d, int num_splits, int num_sms) {
+  const long long units = static_cast<long long>(B) * H * ((N + kQBlock - 1) / kQBlock);
+  if (d == 256) return {1, units, 1, 0};  // the d = 256 kernel runs unsplit
+  const SplitPlan plan = split_plan(B, H, N, d, num_splits, num_sms);
+  const long long tiles = kv_tiles(N);
+  const long long per = (tiles + plan.splits - 1) / plan.splits;
+  const int eff = static_cast<int>((tiles + per - 1) / per);
+  if (eff <= 1) return {1, units, 1, 0};
+  const bool tail = plan.tail_qunit0 > 0;
+  return {eff, tail ? plan.tail_qunit0 : 0, tail ? 3 : 2,
+          workspace_bytes_for(B, H, N, d, eff, tail ? plan_row0(plan, N) : 0)};
 }
 
 int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
@@ -478,11 +497,21 @@ int fa_fwd_splitkv_launches(int B, int H, int N, int d, int num_splits) {
   DeviceInfo dev;
   const int st = device_info(&dev);
   if (st != FA_OK) return -st;
-  const SplitPlan plan = split_plan(B, H, N, d, num_splits, dev.num_sms);
-  const long long tiles = kv_tiles(N);
-  const long long per = (tiles + plan.splits - 1) / plan.splits;
-  if ((tiles + per - 1) / per <= 1) return 1;
-  return plan.tail_qunit0 > 0 ? 3 : 2;
+  return summarize_plan(B, H, N, d, num_splits, dev.num_sms).launches;
+}
+
+int fa_fwd_splitkv_plan(int B, int H, int N, int d, int num_splits, int num_sms, int* splits,
+                        long long* first_split_unit, int* launches, unsigned long long* workspace_bytes) {
+  if (!splits || !first_split_unit || !launches || !workspace_bytes) return FA_ERR_NULL;
+  if (B < 1 || H < 1 || N < 1 || num_splits < 0 || num_sms < 1) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_HEADDIM;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL) return FA_ERR_SHAPE;
+  const PlanSummary ps = summarize_plan(B, H, N, d, num_splits, num_sms);
+  *splits = ps.splits;
+  *first_split_unit = ps.first_split;
+  *launches = ps.launches;
+  *workspace_bytes = ps.workspace;
+  return FA_OK;
 }
 
 int fa_fwd_splitkv_num_splits(int B, int H, int N, int d) {
@@ -492,22 +521,18 @@ int fa_fwd_splitkv_num_splits(int B, int H, int N, int d) {
   DeviceInfo dev;
   const int st = device_info(&dev);
   if (st != FA_OK) return -st;
-  return effective_splits(B, H, N, d, 0, dev.num_sms);
+  return summarize_plan(B, H, N, d, 0, dev.num_sms).splits;
 }
 
 unsigned long long fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits) {
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || num_splits < 0) return 0;  // d = 256: unsplit, none
-  SplitPlan plan{num_splits, -1};
+  int num_sms = 1;  // an explicit split count does not depend on the device
   if (num_splits == 0) {
     DeviceInfo dev;
     if (device_info(&dev) != FA_OK) return 0;
-    plan = split_plan(B, H, N, d, 0, dev.num_sms);
+    num_sms = dev.num_sms;
   }
-  const long long tiles = kv_tiles(N);
-  const long long splits = std::min<long long>(plan.splits, tiles);
-  const long long per = (tiles + splits - 1) / splits;
-  const int eff = static_cast<int>((tiles + per - 1) / per);
-  return workspace_bytes_for(B, H, N, d, eff, eff > 1 ? plan_row0(plan, N) : 0);
+  return summarize_plan(B, H, N, d, num_splits, num_sms).workspace;
 }
 
 }  // extern "C"

@@ -138,6 +138,30 @@ int fa_fwd_splitkv_num_splits(int B, int H, int N, int d);
  * tail, the merge of its rows); a negative fa_status on error. */
 int fa_fwd_splitkv_launches(int B, int H, int N, int d, int num_splits);
 
+/*
+ * The split-KV plan fa_fwd_splitkv follows for FA_F16 / FA_BF16 inputs of
+ * this shape on a device with `num_sms` SMs, computed on the host (no device
+ * is touched; a caller can size workspaces for a device it has not opened).
+ * With num_sms = the current device's SM count it agrees with
+ * fa_fwd_splitkv_num_splits, fa_fwd_splitkv_launches and
+ * fa_fwd_splitkv_workspace_size.
+ *
+ * Work units are the B*H*ceil(N/256) (batch*head, 256-row Q block) pairs.
+ * Outputs (all written on success):
+ *   splits           key ranges of each split unit after clamping to whole
+ *                    128-key tiles (1: nothing is split);
+ *   first_split_unit index of the first split unit: 0 when every unit is
+ *                    split, B*H*ceil(N/256) when none is, in between under the
+ *                    tail plan (the units of the last, partial wave of SMs);
+ *   launches         kernel launches enqueued: 1, 2 or 3;
+ *   workspace_bytes  the workspace fa_fwd_splitkv needs (0: none).
+ * Errors: FA_ERR_NULL (an output pointer is NULL), FA_ERR_SHAPE (B, H, N or
+ * num_sms < 1, num_splits < 0, B*H >= 2^31), FA_ERR_HEADDIM (d not 64, 128 or
+ * 256; d = 256 always runs unsplit).
+ */
+int fa_fwd_splitkv_plan(int B, int H, int N, int d, int num_splits, int num_sms, int *splits,
+                        long long *first_split_unit, int *launches, unsigned long long *workspace_bytes);
+
 /* Workspace bytes fa_fwd_splitkv needs for this shape and split count on the
  * current device (num_splits = 0: the automatic plan, which depends on the
  * SM count); 0 when no workspace is needed or on error. */

@@ -199,3 +199,92 @@ def test_d256_split_queries(L):
     assert fa.fa_fwd_splitkv_num_splits(1, 8, 16384, 256) == 1
     assert fa.fa_fwd_splitkv_workspace_size(1, 8, 16384, 256, 4) == 0
     assert fa.fa_bwd_workspace_size(1, 8, 1024, 256) == 0  # the backward takes d = 64 / 128 only
+
+
+def _partials_bytes(rows, d):
+    """Workspace of fp32 O partials (256-byte aligned) followed by fp32 LSE partials."""
+    return (rows * d * 4 + 255) // 256 * 256 + rows * 4
+
+
+def _tail_expectation(B, H, N, d, num_sms):
+    """The wave-tail plan written out: the full waves of 256-row Q blocks run
+    unsplit, the units of the last partial wave are split as many ways as fit
+    in one wave (at most 16, at most one range per 128-key tile), and only
+    their rows need partial buffers."""
+    nqb = -(-N // 256)
+    units = B * H * nqb
+    full, tail = divmod(units, num_sms)
+    tiles = -(-N // 128)
+    s = min(num_sms // tail, tiles, 16)
+    per = -(-tiles // s)
+    s = -(-tiles // per)
+    first = full * num_sms
+    row0 = (first // nqb) * N + (first % nqb) * 256
+    return s, first, _partials_bytes(s * (B * H * N - row0), d)
+
+
+@pytest.mark.parametrize("B,H,N,d,num_sms", [
+    (1, 8, 16384, 128, 152),   # 512 units: 3 full waves, 56 left split 2 ways
+    (1, 8, 16384, 128, 148),   # 68 left, split 2 ways
+    (8, 12, 2048, 128, 152),   # 768 units: 5 full waves, 8 left split 16 ways
+    (1, 4, 10240, 128, 152),   # 160 units: 1 full wave, 8 left split 16 ways
+])
+def test_splitkv_plan_tail_on_the_host(L, B, H, N, d, num_sms):
+    rc, p = fa.fa_fwd_splitkv_plan(B, H, N, d, 0, num_sms)
+    assert rc == fa.FA_OK
+    s, first, ws = _tail_expectation(B, H, N, d, num_sms)
+    assert p == {"splits": s, "first_split_unit": first, "launches": 3, "workspace_bytes": ws}
+
+
+def test_splitkv_plan_uniform_and_unsplit_on_the_host(L):
+    # explicit counts split every unit alike: workspace for every row
+    rc, p = fa.fa_fwd_splitkv_plan(1, 8, 16384, 128, 3, 152)
+    assert rc == fa.FA_OK and p == {"splits": 3, "first_split_unit": 0, "launches": 2,
+                                    "workspace_bytes": _partials_bytes(3 * 8 * 16384, 128)}
+    assert fa.fa_fwd_splitkv_workspace_size(1, 8, 16384, 128, 3) == p["workspace_bytes"]
+    # clamped to whole 128-key tiles: N = 300 has 3
+    rc, p = fa.fa_fwd_splitkv_plan(1, 1, 300, 64, 9, 152)
+    assert p == {"splits": 3, "first_split_unit": 0, "launches": 2, "workspace_bytes": _partials_bytes(900, 64)}
+    # 4096 units on 152 SMs: the last wave is nearly full (144 units), no split pays
+    rc, p = fa.fa_fwd_splitkv_plan(8, 32, 4096, 128, 0, 152)
+    assert p == {"splits": 1, "first_split_unit": 4096, "launches": 1, "workspace_bytes": 0}
+    # d = 256 always runs unsplit; an explicit count of 1 too
+    for args in [(4, 16, 4096, 256, 0, 152), (4, 16, 4096, 256, 8, 152), (2, 2, 1000, 128, 1, 152)]:
+        rc, p = fa.fa_fwd_splitkv_plan(*args)
+        units = args[0] * args[1] * -(-args[2] // 256)
+        assert rc == fa.FA_OK and p == {"splits": 1, "first_split_unit": units, "launches": 1, "workspace_bytes": 0}
+
+
+def test_splitkv_plan_invariants_over_shapes(L):
+    """Over a sweep of shapes and SM counts: three launches exactly when some
+    but not all units are split, and the workspace covers exactly the split
+    units' rows, one span per key range."""
+    for B, H, N in [(1, 1, 64), (1, 2, 1000), (2, 3, 4097), (1, 8, 16384), (3, 5, 777), (16, 16, 512), (1, 1, 65536)]:
+        for d in (64, 128):
+            for num_sms in (1, 7, 132, 148, 152, 1000):
+                for ns in (0, 1, 2, 5):
+                    rc, p = fa.fa_fwd_splitkv_plan(B, H, N, d, ns, num_sms)
+                    assert rc == fa.FA_OK
+                    nqb = -(-N // 256)
+                    units = B * H * nqb
+                    first, s = p["first_split_unit"], p["splits"]
+                    if s == 1:
+                        assert first == units and p["launches"] == 1 and p["workspace_bytes"] == 0
+                        continue
+                    assert 1 < s <= max(ns, 16) and s <= -(-N // 128)
+                    assert p["launches"] == (3 if 0 < first < units else 2)
+                    assert ns == 0 or first == 0
+                    row0 = (first // nqb) * N + (first % nqb) * 256
+                    assert p["workspace_bytes"] == _partials_bytes(s * (B * H * N - row0), d)
+
+
+def test_splitkv_plan_argument_errors(L):
+    import ctypes
+    assert fa.fa_fwd_splitkv_plan(1, 1, 64, 64, 0, 0)[0] == fa.FA_ERR_SHAPE
+    assert fa.fa_fwd_splitkv_plan(0, 1, 64, 64, 0, 152)[0] == fa.FA_ERR_SHAPE
+    assert fa.fa_fwd_splitkv_plan(1, 1, 64, 64, -1, 152)[0] == fa.FA_ERR_SHAPE
+    assert fa.fa_fwd_splitkv_plan(1, 1, 64, 96, 0, 152)[0] == fa.FA_ERR_HEADDIM
+    assert fa.fa_fwd_splitkv_plan(65536, 65536, 64, 64, 0, 152)[0] == fa.FA_ERR_SHAPE
+    assert L.fa_fwd_splitkv_plan(1, 1, 64, 64, 0, 152, None, None, None, None) == fa.FA_ERR_NULL
+    s = ctypes.c_int()
+    assert L.fa_fwd_splitkv_plan(1, 1, 64, 64, 0, 152, ctypes.byref(s), None, None, None) == fa.FA_ERR_NULL

@@ -121,3 +121,19 @@ def test_splitkv_tail_plan_workspace_covers_only_the_tail_rows():
     # the same rows as the unsplit pass up to the merge's rounding
     assert float((o.float() - o_ref.float()).abs().max()) <= 1e-2
     assert float((lse - lse_ref).abs().max()) <= 1e-4 * max(1.0, float(lse_ref.abs().max()))
+
+
+def test_splitkv_plan_matches_the_device_queries():
+    """fa_fwd_splitkv_plan with this device's SM count agrees with the queries
+    that read the device: split count, launches, workspace."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for B, H, N, d in [(1, 8, 16384, 128), (8, 32, 4096, 128), (8, 12, 2048, 128), (1, 4, 10240, 128),
+                       (2, 2, 1000, 64), (4, 16, 4096, 256), (1, 1, 1280, 64)]:
+        for ns in (0, 1, 3):
+            rc, p = fa.fa_fwd_splitkv_plan(B, H, N, d, ns, sms)
+            assert rc == fa.FA_OK
+            assert p["launches"] == fa.fa_fwd_splitkv_launches(B, H, N, d, ns)
+            if d != 256:
+                assert p["workspace_bytes"] == fa.fa_fwd_splitkv_workspace_size(B, H, N, d, ns)
+            if ns == 0:
+                assert p["splits"] == fa.fa_fwd_splitkv_num_splits(B, H, N, d)
