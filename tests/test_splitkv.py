@@ -68,9 +68,9 @@ def test_splitkv_workspace_errors():
 
 
 @pytest.mark.parametrize("B,H,N,d,dtype", [
-    (1, 4, 10240, 128, "bf16"),   # one full wave of units, the 12 left over split 12 ways
+    (1, 4, 10240, 128, "bf16"),   # 160 units: on 152 SMs one full wave, the 8 left over split 16 ways
     (1, 2, 20000, 128, "f16"),    # N not a multiple of 256: the last Q block of a head is partial
-    (8, 12, 2048, 128, "f16"),    # 768 units: 5 full waves, 28 split 5 ways
+    (8, 12, 2048, 128, "f16"),    # 768 units: on 152 SMs 5 full waves, the 8 left over split 16 ways
 ])
 def test_splitkv_tail_plan(B, H, N, d, dtype):
     """num_splits = 0 on shapes whose units end in a partial last wave: the
