@@ -1,0 +1,307 @@
+"""A model check of the 16-bit forward kernel's barrier protocol (CPU).
+
+The roles of one CTA of `fa_fwd_f16_kernel` are written here as generators
+that follow the kernel's waits, arrivals, commits and issues in program
+order: the TMA producer, the MMA warp of each Q sub-tile (turns, P·V then S),
+and the four softmax warps of each sub-tile. The tensor pipe executes the
+CTA's MMAs in issue order; a commit fires once every MMA its warp issued
+before it has completed; TMA copies land at any later time. A random
+scheduler interleaves all of it, thousands of times per configuration.
+
+Checked on every run:
+  * no deadlock (some role can always make progress until all are done);
+  * parity waits never alias: a wait for phase k of a barrier succeeds only
+    when exactly k+1 phases have completed (a barrier one phase behind would
+    satisfy the parity too, and two ahead would never release it);
+  * the data dependencies the barriers stand for: S_i(j) runs on a landed
+    K_j and after P_i(j-1)·V has read the columns it overwrites; P_i(j)·V
+    runs on a landed V_j after all four softmax warps wrote P_i(j); the
+    softmax reads S_i(j) after it completed, rescales O only with every
+    earlier P·V complete and none later started, and writes P only after the
+    previous P·V read those columns; a K or V stage is reloaded only after
+    every MMA reading its previous tile has completed; the epilogue reads O
+    after the last P·V.
+
+Configurations: d = 128 (2-stage rings, stages freed by softmax-warp
+arrivals) and d = 64 (3-stage rings, stages freed by commits), the default
+order (P·V completion taken from the following S's commit) and the strict
+order (every P·V committed and waited for), tile counts of both sub-tiles
+equal, causal (one more tile for the second sub-tile), a single sub-tile,
+and no key tile at all.
+"""
+import random
+
+import pytest
+
+
+class Bar:
+    def __init__(self, count):
+        self.count, self.pending, self.done = count, 0, 0  # done = completed phases
+
+    def arrive(self, n=1):
+        for _ in range(n):
+            self.pending += 1
+            assert self.pending <= self.count
+            if self.pending == self.count:
+                self.pending, self.done = 0, self.done + 1
+
+
+class Model:
+    def __init__(self, nkv0, nkv1, has1, stages, softmax_frees, strict, rng):
+        self.rng = rng
+        self.ST, self.SFREE, self.STRICT = stages, softmax_frees, strict
+        self.nk = [nkv0, nkv1 if has1 else 0]
+        self.has1 = has1
+        self.nkv = max(self.nk)
+        nsub = 2 if has1 else 1
+        rel = 4 * nsub if softmax_frees else nsub
+        self.bars = {"QF": Bar(1)}
+        for s in range(stages):
+            self.bars.update({f"KF{s}": Bar(1), f"KE{s}": Bar(rel), f"VF{s}": Bar(1), f"VE{s}": Bar(rel)})
+        for i in range(2):
+            self.bars.update({f"SF{i}": Bar(1), f"PF{i}": Bar(4), f"OD{i}": Bar(1), f"DR{i}": Bar(1),
+                              f"T{i}": Bar(1)})
+        self.kstage = [None] * stages   # tile landed in each K stage (None: empty or loading)
+        self.vstage = [None] * stages
+        self.landing = []               # (kind, stage, tile, bar) copies in flight
+        self.pipe = []                  # MMAs issued, not yet complete: (warp, kind, sub, j)
+        self.issued = {0: 0, 1: 0}      # MMAs issued per warp
+        self.completed_by = {0: 0, 1: 0}
+        self.commits = []               # (warp, count of its MMAs to wait for, bar)
+        self.mma_done = set()           # ("S"|"PV", sub, j) completed
+        self.mma_started = set()
+        self.p_written = {}             # (sub, j) -> softmax warps that wrote P
+        self.rescaled = {}              # (sub, j) -> softmax warps that rescaled O at tile j
+        self.release_v = True           # softmax warps free V stages (planted-mistake switch)
+
+    # -- barrier waits: runnable only when the parity says so; then no aliasing allowed
+    def can_wait(self, name, k):
+        return (self.bars[name].done & 1) != (k & 1)
+
+    def check_wait(self, name, k):
+        assert self.bars[name].done == k + 1, f"wait on {name} for phase {k} saw {self.bars[name].done} done"
+
+    # ---------------------------------------------------------------- roles
+    def producer(self):
+        if self.nkv == 0:
+            return
+        self.landing.append(("Q", 0, 0, "QF"))
+        for j in range(self.nkv):
+            s = j % self.ST
+            yield ("wait", f"KE{s}", j // self.ST - 1)
+            # the stage's previous tile j-ST must have been read by every S
+            if j >= self.ST:
+                for i in range(2 if self.has1 else 1):
+                    if j - self.ST < self.nk[i]:
+                        assert ("S", i, j - self.ST) in self.mma_done, f"K stage {s} reloaded before S{i}({j - self.ST})"
+            self.kstage[s] = None
+            self.landing.append(("K", s, j, f"KF{s}"))
+            yield ("step",)
+            yield ("wait", f"VE{s}", j // self.ST - 1)
+            if j >= self.ST:
+                for i in range(2 if self.has1 else 1):
+                    if j - self.ST < self.nk[i]:
+                        assert ("PV", i, j - self.ST) in self.mma_done, f"V stage {s} reloaded before PV{i}({j - self.ST})"
+            self.vstage[s] = None
+            self.landing.append(("V", s, j, f"VF{s}"))
+            yield ("step",)
+
+    def mma(self, sub):
+        nkv, nko = self.nk[sub], self.nk[sub ^ 1]
+        if nkv > 0:
+            yield ("wait", "QF", 0)
+            for j in range(nkv + 1):
+                other = j if sub == 1 else j - 1
+                if self.has1 and 0 <= other <= nko and nko > 0:
+                    yield ("wait", f"T{sub}", other)
+                if j > 0:
+                    s = (j - 1) % self.ST
+                    yield ("wait", f"VF{s}", (j - 1) // self.ST)
+                    yield ("wait", f"PF{sub}", j - 1)
+                    self.issue(sub, "PV", j - 1)
+                    if self.STRICT or j == nkv:
+                        self.commit(sub, f"OD{sub}")
+                    if not self.SFREE:
+                        self.commit(sub, f"VE{s}")
+                    yield ("step",)
+                if j < nkv:
+                    s = j % self.ST
+                    yield ("wait", f"KF{s}", j // self.ST)
+                    if self.STRICT and j > 0:
+                        yield ("wait", f"OD{sub}", j - 1)
+                    self.issue(sub, "S", j)
+                    self.commit(sub, f"SF{sub}")
+                    if not self.SFREE:
+                        self.commit(sub, f"KE{s}")
+                    yield ("step",)
+                if self.has1:
+                    self.bars[f"T{sub ^ 1}"].arrive()
+                    yield ("step",)
+        self.commit(sub, f"DR{sub}")
+        yield ("wait", f"DR{sub}", 0)
+
+    def softmax(self, sub, w):
+        nkv = self.nk[sub]
+        for j in range(nkv):
+            yield ("wait", f"SF{sub}", j)
+            if self.SFREE:
+                if j > 0 and self.release_v:
+                    self.bars[f"VE{(j - 1) % self.ST}"].arrive()
+                self.bars[f"KE{j % self.ST}"].arrive()
+            assert ("S", sub, j) in self.mma_done
+            yield ("step",)
+            if j > 0 and self.rng.random() < 0.3:   # a rescale of O at tile j
+                if self.STRICT:
+                    yield ("wait", f"OD{sub}", j - 1)
+                assert ("PV", sub, j - 1) in self.mma_done, "O rescaled while an earlier P.V may run"
+                assert ("PV", sub, j) not in self.mma_started
+                self.rescaled.setdefault((sub, j), set()).add(w)
+            # P overwrites S columns that P(j-1).V read
+            assert j == 0 or ("PV", sub, j - 1) in self.mma_done
+            self.p_written.setdefault((sub, j), set()).add(w)
+            self.bars[f"PF{sub}"].arrive()
+            yield ("step",)
+        if nkv > 0:
+            yield ("wait", f"OD{sub}", nkv - 1 if self.STRICT else 0)
+            for j in range(nkv):
+                assert ("PV", sub, j) in self.mma_done, "epilogue read O before the last P.V"
+
+    # ---------------------------------------------------------------- async agents
+    def issue(self, warp, kind, j):
+        self.issued[warp] += 1
+        self.pipe.append((warp, kind, warp, j))
+
+    def commit(self, warp, bar):
+        self.commits.append((warp, self.issued[warp], bar))
+
+    def execute_head(self):
+        warp, kind, sub, j = self.pipe.pop(0)
+        self.mma_started.add((kind, sub, j))
+        if kind == "S":
+            assert self.kstage[j % self.ST] == j, f"S{sub}({j}) on a K stage without K_{j}"
+            assert j == 0 or ("PV", sub, j - 1) in self.mma_done, "S overwrote P before P.V read it"
+        else:
+            assert self.vstage[j % self.ST] == j, f"PV{sub}({j}) on a V stage without V_{j}"
+            assert self.p_written.get((sub, j)) == {0, 1, 2, 3}, "P.V before every softmax warp wrote P"
+        self.mma_done.add((kind, sub, j))
+        self.completed_by[warp] += 1
+
+    def events(self):
+        ev = []
+        if self.pipe:
+            ev.append(("pipe",))
+        for n, c in enumerate(self.commits):
+            if self.completed_by[c[0]] >= c[1]:
+                ev.append(("commit", n))
+        for n in range(len(self.landing)):
+            ev.append(("land", n))
+        return ev
+
+    def fire(self, e):
+        if e[0] == "pipe":
+            self.execute_head()
+        elif e[0] == "commit":
+            _, _, bar = self.commits.pop(e[1])
+            self.bars[bar].arrive()
+        else:
+            kind, s, j, bar = self.landing.pop(e[1])
+            if kind == "K":
+                self.kstage[s] = j
+            elif kind == "V":
+                self.vstage[s] = j
+            self.bars[bar].arrive()
+
+    # ---------------------------------------------------------------- scheduler
+    def run(self):
+        roles = [self.producer(), self.mma(0)]
+        roles += [self.softmax(0, w) for w in range(4)]
+        if self.has1:
+            roles += [self.mma(1)] + [self.softmax(1, w) for w in range(4)]
+        state = {n: None for n in range(len(roles))}  # pending request of each live role
+        live = set(range(len(roles)))
+
+        def advance(n):
+            try:
+                state[n] = next(roles[n])
+            except StopIteration:
+                live.discard(n)
+                state[n] = None
+
+        for n in list(live):
+            advance(n)
+        for _ in range(200000):
+            if not live and not self.pipe and not self.commits and not self.landing:
+                return
+            choices = []
+            for n in live:
+                req = state[n]
+                if req[0] == "step" or self.can_wait(req[1], req[2]):
+                    choices.append(("role", n))
+            choices += self.events()
+            assert choices, f"deadlock: {[state[n] for n in live]}"
+            c = self.rng.choice(choices)
+            if c[0] == "role":
+                req = state[c[1]]
+                if req[0] == "wait":
+                    self.check_wait(req[1], req[2])
+                advance(c[1])
+            else:
+                self.fire(c)
+        raise AssertionError("did not finish")
+
+
+CASES = [(1, 1, True), (2, 2, True), (5, 5, True), (3, 4, True), (1, 2, True), (4, 0, False), (0, 0, True),
+         (0, 0, False)]
+
+
+@pytest.mark.parametrize("stages,softmax_frees", [(2, True), (3, False)], ids=["d128", "d64"])
+@pytest.mark.parametrize("strict", [False, True], ids=["default", "strict"])
+@pytest.mark.parametrize("nkv0,nkv1,has1", CASES)
+def test_forward_barrier_protocol(stages, softmax_frees, strict, nkv0, nkv1, has1):
+    rng = random.Random(hash((stages, strict, nkv0, nkv1, has1)) & 0xFFFFFFFF)
+    for _ in range(300):
+        Model(nkv0, nkv1, has1, stages, softmax_frees, strict, rng).run()
+
+
+def test_model_catches_a_missing_stage_release():
+    """Planted mistake in the model: softmax warps that never free the V
+    stage. The producer then waits on a phase that cannot complete."""
+    m = Model(4, 4, True, 2, True, False, random.Random(1))
+    m.release_v = False
+    with pytest.raises(AssertionError, match="deadlock"):
+        m.run()
+
+
+def test_model_catches_a_parity_wait_that_skips_a_phase():
+    """Planted mistake in the model: a softmax warp that waits for S-full
+    only on odd tiles can observe the barrier two phases late, which the
+    parity alone does not reveal."""
+    class SkipWait(Model):
+        def softmax(self, sub, w):
+            for req in Model.softmax(self, sub, w):
+                if req[0] == "wait" and req[1] == f"SF{sub}" and req[2] % 2 == 0 and req[2] > 0:
+                    continue
+                yield req
+    with pytest.raises(AssertionError):
+        for seed in range(50):
+            SkipWait(6, 6, True, 2, True, False, random.Random(seed)).run()
+
+
+def test_model_catches_a_stage_freed_too_early():
+    """Planted mistake in the model: softmax warps that free V_j's stage as
+    soon as S_j is complete (instead of V_{j-1}'s), before P_j·V_j has read
+    it. The producer then reloads a V stage that an MMA still needs."""
+    class EarlyV(Model):
+        def softmax(self, sub, w):
+            for j in range(self.nk[sub]):
+                yield ("wait", f"SF{sub}", j)
+                self.bars[f"VE{j % self.ST}"].arrive()
+                self.bars[f"KE{j % self.ST}"].arrive()
+                yield ("step",)
+                self.p_written.setdefault((sub, j), set()).add(w)
+                self.bars[f"PF{sub}"].arrive()
+                yield ("step",)
+            if self.nk[sub] > 0:
+                yield ("wait", f"OD{sub}", 0)
+    with pytest.raises(AssertionError, match="reloaded before"):
+        EarlyV(6, 6, True, 2, True, False, random.Random(3)).run()
