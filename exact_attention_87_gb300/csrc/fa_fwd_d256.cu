@@ -272,15 +272,21 @@ __device__ __forceinline__ void softmax256(const FwdParams& p, uint32_t base, ui
     }
     l += se.x + se.y;
     if constexpr (BF16) l_o += sro.x + sro.y;
-    if (rescale_o) {
-      // O complete up to tile j-1 before it is read and scaled. The parity
-      // names one phase: S_j's completion (waited for above) covers
-      // P_{j-2} V (issued before S_j), and P_j V cannot have started, so
-      // B_OD is in phase j-1 or j.
+    if (j > 0) {
+      // P_{j-1} V complete, which a rescale of O needs. The wait is made at
+      // every tile, not only before a rescale, so that each phase of B_OD is
+      // waited for in turn and the parity always names phase j-1: P_j V
+      // cannot start before this warp's P-full arrival, and the previous wait
+      // saw phase j-2 complete. (S_j's completion implies that P_{j-2} V is
+      // complete, but not that the commit's arrival on B_OD has landed: commits
+      // on different barriers may land in any order.) P_{j-1} V normally
+      // completes while this tile's softmax runs.
       if (!__all_sync(0xffffffffu, wait_bar(b_od, (j - 1) & 1, ctl, kWhereODone))) {
         ok = false;
         break;
       }
+    }
+    if (rescale_o) {
       tc_fence_after();
 #pragma unroll 1
       for (int q = 0; q < C::D / 32; ++q) {

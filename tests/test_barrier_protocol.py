@@ -212,11 +212,15 @@ class Model:
             self.bars[bar].arrive()
 
     # ---------------------------------------------------------------- scheduler
-    def run(self):
+    def roles(self):
         roles = [self.producer(), self.mma(0)]
         roles += [self.softmax(0, w) for w in range(4)]
         if self.has1:
             roles += [self.mma(1)] + [self.softmax(1, w) for w in range(4)]
+        return roles
+
+    def run(self):
+        roles = self.roles()
         state = {n: None for n in range(len(roles))}  # pending request of each live role
         live = set(range(len(roles)))
 
@@ -305,3 +309,113 @@ def test_model_catches_a_stage_freed_too_early():
                 yield ("wait", f"OD{sub}", 0)
     with pytest.raises(AssertionError, match="reloaded before"):
         EarlyV(6, 6, True, 2, True, False, random.Random(3)).run()
+
+
+class D256Model(Model):
+    """`fa_fwd_d256_kernel`: one 128-row Q tile, 64-key K/V tiles in 2-stage
+    rings, two S buffers (S_{j+2} issued right behind P_j·V into the columns
+    of P_j), K stages freed by the four softmax warps once S_j is complete, V
+    stages by a commit behind each P·V, a per-P·V barrier (OD) for rescales
+    and a barrier committed once after the last P·V (OL) for the epilogue."""
+
+    def __init__(self, nkv, strict, rng):
+        super().__init__(nkv, 0, False, 2, True, strict, rng)
+        self.bars["OL"] = Bar(1)
+        for s in range(2):
+            self.bars[f"KE{s}"] = Bar(4)
+            self.bars[f"VE{s}"] = Bar(1)
+        self.bars["PF0"], self.bars["PF1"] = Bar(4), Bar(4)
+
+    def roles(self):
+        return [self.producer(), self.mma256()] + [self.softmax256(w) for w in range(4)]
+
+    def mma256(self):
+        nkv = self.nkv
+        if nkv > 0:
+            yield ("wait", "QF", 0)
+            for j in range(min(nkv, 2)):
+                yield ("wait", f"KF{j % 2}", j // 2)
+                self.issue(0, "S", j)
+                self.commit(0, f"SF{j & 1}")
+                yield ("step",)
+            for j in range(nkv):
+                s = j % 2
+                yield ("wait", f"VF{s}", j // 2)
+                yield ("wait", f"PF{j & 1}", j // 2)
+                self.issue(0, "PV", j)
+                self.commit(0, "OD0")
+                if j == nkv - 1:
+                    self.commit(0, "OL")
+                self.commit(0, f"VE{s}")
+                yield ("step",)
+                if j + 2 < nkv:
+                    if self.STRICT:
+                        yield ("wait", "OD0", j)
+                    n = j + 2
+                    yield ("wait", f"KF{n % 2}", n // 2)
+                    self.issue(0, "S", n)
+                    self.commit(0, f"SF{n & 1}")
+                    yield ("step",)
+        self.commit(0, "DR0")
+        yield ("wait", "DR0", 0)
+
+    def softmax256(self, w):
+        nkv = self.nkv
+        for j in range(nkv):
+            yield ("wait", f"SF{j & 1}", j // 2)
+            self.bars[f"KE{j % 2}"].arrive()
+            assert ("S", 0, j) in self.mma_done
+            yield ("step",)
+            # P_j overwrites the buffer of S_j, whose previous P (P_{j-2}) P_{j-2}.V read
+            assert j < 2 or ("PV", 0, j - 2) in self.mma_done
+            self.p_written.setdefault((0, j), set()).add(w)
+            if j > 0:
+                # every phase of the per-P.V barrier is waited for in turn (not
+                # only before a rescale), so its parity names one phase
+                # whatever the order in which commits on different barriers land
+                yield ("wait", "OD0", j - 1)
+                if self.rng.random() < 0.3:   # a rescale of O at tile j
+                    assert ("PV", 0, j - 1) in self.mma_done, "O rescaled while an earlier P.V may run"
+                    assert ("PV", 0, j) not in self.mma_started
+            self.bars[f"PF{j & 1}"].arrive()
+            yield ("step",)
+        if nkv > 0:
+            yield ("wait", "OL", 0)
+            for j in range(nkv):
+                assert ("PV", 0, j) in self.mma_done, "epilogue read O before the last P.V"
+
+    def execute_head(self):
+        warp, kind, sub, j = self.pipe.pop(0)
+        self.mma_started.add((kind, sub, j))
+        if kind == "S":
+            assert self.kstage[j % 2] == j, f"S({j}) on a K stage without K_{j}"
+            assert j < 2 or ("PV", 0, j - 2) in self.mma_done, "S overwrote P before P.V read it"
+        else:
+            assert self.vstage[j % 2] == j, f"PV({j}) on a V stage without V_{j}"
+            assert self.p_written.get((0, j)) == {0, 1, 2, 3}, "P.V before every softmax warp wrote P"
+        self.mma_done.add((kind, sub, j))
+        self.completed_by[warp] += 1
+
+
+@pytest.mark.parametrize("strict", [False, True], ids=["default", "strict"])
+@pytest.mark.parametrize("nkv", [0, 1, 2, 3, 7])
+def test_d256_barrier_protocol(strict, nkv):
+    rng = random.Random(1000 + 10 * nkv + strict)
+    for _ in range(300):
+        D256Model(nkv, strict, rng).run()
+
+
+def test_model_catches_a_rescale_wait_that_relies_on_commit_order():
+    """The d = 256 softmax used to wait on the per-P.V barrier only before a
+    rescale, trusting that S_j's completion implies the arrival for the P.V
+    issued before it. Commits on different barriers may land in any order, and
+    then that parity can name a phase two behind."""
+    class OnlyOnRescale(D256Model):
+        def softmax256(self, w):
+            for req in D256Model.softmax256(self, w):
+                if req[0] == "wait" and req[1] == "OD0" and self.rng.random() < 0.7:
+                    continue   # no rescale at this tile: the old code did not wait
+                yield req
+    with pytest.raises(AssertionError):
+        for seed in range(200):
+            OnlyOnRescale(7, False, random.Random(seed)).run()
