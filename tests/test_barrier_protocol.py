@@ -1,4 +1,8 @@
-"""A model check of the 16-bit forward kernel's barrier protocol (CPU).
+"""A model check of the kernels' barrier protocols (CPU).
+
+The d = 64 / 128 forward kernel is modelled in full below; `D256Model` and
+`BwdModel` at the end do the same for the d = 256 forward and the backward
+kernels.
 
 The roles of one CTA of `fa_fwd_f16_kernel` are written here as generators
 that follow the kernel's waits, arrivals, commits and issues in program
@@ -419,3 +423,206 @@ def test_model_catches_a_rescale_wait_that_relies_on_commit_order():
     with pytest.raises(AssertionError):
         for seed in range(200):
             OnlyOnRescale(7, False, random.Random(seed)).run()
+
+
+class BwdModel(Model):
+    """`fa_bwd_main_kernel`: the TMA producer (K, V once; Q_i with its rows
+    in a QST-stage ring, dO_i in an OST-stage ring), MMA warp A (dQ_i, dK_i
+    once dS_i is formed), MMA warp B (S^T_0, dP^T_0, dV_0, S^T_1, then per
+    tile dP^T_{i+1}, dV_{i+1}, S^T_{i+2}), eight softmax warps (P_i over the
+    S^T columns, then dS_i into shared memory) and four dQ warps (dQ_i out of
+    TMEM). For d = 128 dQ_i reuses the dP^T columns; for d = 64 it has its own."""
+
+    def __init__(self, nq, d, strict, rng):
+        self.rng, self.STRICT, self.nq, self.d = rng, strict, nq, d
+        self.QST, self.OST = (2, 1) if d == 128 else (3, 2)
+        self.bars = {"K": Bar(1), "V": Bar(1), "SF": Bar(1), "DPF": Bar(1), "PF": Bar(8), "DSF": Bar(8),
+                     "DQF": Bar(1), "DQE": Bar(4), "DSE": Bar(1), "DONE": Bar(2)}
+        for s in range(self.QST):
+            self.bars.update({f"QF{s}": Bar(1), f"QE{s}": Bar(1)})
+        for s in range(self.OST):
+            self.bars.update({f"OF{s}": Bar(1), f"OE{s}": Bar(1)})
+        self.qstage, self.ostage = [None] * self.QST, [None] * self.OST
+        self.kv = set()
+        self.landing, self.pipe, self.commits = [], [], []
+        self.issued = {0: 0, 1: 0}
+        self.completed_by = {0: 0, 1: 0}
+        self.mma_done, self.mma_started = set(), set()
+        self.count = {}  # (event, i) -> number of warps that did it
+
+    def bump(self, ev, i):
+        self.count[(ev, i)] = self.count.get((ev, i), 0) + 1
+
+    def roles(self):
+        return ([self.producer(), self.mma_a(), self.mma_b()] + [self.softmax_bwd(w) for w in range(8)]
+                + [self.dq_warp(w) for w in range(4)])
+
+    def producer(self):
+        self.landing += [("K", 0, 0, "K"), ("V", 0, 0, "V")]
+        for i in range(self.nq):
+            qs, os_ = i % self.QST, i % self.OST
+            yield ("wait", f"QE{qs}", i // self.QST - 1)
+            if i >= self.QST:  # readers of Q_{i-QST} and its rows: S^T, dK, the softmax's P and dS phases
+                assert {("S", i - self.QST), ("DK", i - self.QST)} <= self.mma_done, "Q stage reloaded early"
+                assert self.count.get(("ds", i - self.QST), 0) == 8, "Q rows reloaded before the softmax used them"
+            self.qstage[qs] = None
+            self.landing.append(("Q", qs, i, f"QF{qs}"))
+            yield ("step",)
+            yield ("wait", f"OE{os_}", i // self.OST - 1)
+            if i >= self.OST:
+                assert {("DP", i - self.OST), ("DV", i - self.OST)} <= self.mma_done, "dO stage reloaded early"
+            self.ostage[os_] = None
+            self.landing.append(("O", os_, i, f"OF{os_}"))
+            yield ("step",)
+
+    def mma_a(self):
+        for i in range(self.nq):
+            yield ("wait", "DSF", i)
+            if self.d == 64 and i > 0:
+                yield ("wait", "DQE", i - 1)
+            self.issue(0, "DQ", i)
+            self.commit(0, "DQF")
+            self.issue(0, "DK", i)
+            self.commit(0, f"QE{i % self.QST}")
+            self.commit(0, "DSE")
+            yield ("step",)
+        self.commit(0, "DONE")
+        yield ("wait", "DONE", 0)
+
+    def mma_b(self):
+        nq = self.nq
+        yield ("wait", "K", 0)
+        yield ("wait", "QF0", 0)
+        self.issue(1, "S", 0)
+        self.commit(1, "SF")
+        yield ("wait", "V", 0)
+        yield ("wait", "OF0", 0)
+        self.issue(1, "DP", 0)
+        self.commit(1, "DPF")
+        yield ("wait", "PF", 0)
+        self.issue(1, "DV", 0)
+        self.commit(1, "OE0")
+        yield ("step",)
+        if nq > 1:
+            if self.STRICT:
+                yield ("wait", "OE0", 0)
+            yield ("wait", f"QF{1 % self.QST}", 1 // self.QST)
+            self.issue(1, "S", 1)
+            self.commit(1, "SF")
+            yield ("step",)
+        for i in range(nq - 1):
+            n1 = i + 1
+            yield ("wait", "DQE", i) if self.d == 128 else ("wait", "DSF", i)
+            yield ("wait", f"OF{n1 % self.OST}", n1 // self.OST)
+            self.issue(1, "DP", n1)
+            self.commit(1, "DPF")
+            yield ("wait", "PF", n1)
+            self.issue(1, "DV", n1)
+            self.commit(1, f"OE{n1 % self.OST}")
+            yield ("step",)
+            if i + 2 < nq:
+                n2 = i + 2
+                if self.STRICT:
+                    yield ("wait", f"OE{n1 % self.OST}", n1 // self.OST)
+                yield ("wait", f"QF{n2 % self.QST}", n2 // self.QST)
+                self.issue(1, "S", n2)
+                self.commit(1, "SF")
+                yield ("step",)
+        self.commit(1, "DONE")
+        yield ("wait", "DONE", 0)
+
+    def softmax_bwd(self, w):
+        for i in range(self.nq):
+            yield ("wait", "SF", i)
+            assert ("S", i) in self.mma_done and self.qstage[i % self.QST] == i
+            # P^T_i over the S^T columns that dV_{i-1} read
+            assert i == 0 or ("DV", i - 1) in self.mma_done
+            self.bump("p", i)
+            self.bars["PF"].arrive()
+            yield ("step",)
+            yield ("wait", "DPF", i)
+            if i > 0:
+                yield ("wait", "DSE", i - 1)
+                assert {("DQ", i - 1), ("DK", i - 1)} <= self.mma_done, "dS overwritten while an MMA reads it"
+            assert ("DP", i) in self.mma_done
+            self.bump("ds", i)
+            self.bars["DSF"].arrive()
+            yield ("step",)
+        yield ("wait", "DONE", 0)
+        for i in range(self.nq):
+            assert {("DV", i), ("DK", i)} <= self.mma_done, "epilogue read dV / dK before the last MMA"
+
+    def dq_warp(self, w):
+        for i in range(self.nq):
+            yield ("wait", "DQF", i)
+            assert ("DQ", i) in self.mma_done
+            self.bump("dqread", i)
+            self.bars["DQE"].arrive()
+            yield ("step",)
+
+    def issue(self, warp, kind, i):
+        self.issued[warp] += 1
+        self.pipe.append((warp, kind, 0, i))
+
+    def execute_head(self):
+        warp, kind, _, i = self.pipe.pop(0)
+        self.mma_started.add((kind, i))
+        c = self.count.get
+        if kind == "S":
+            assert "K" in self.kv and self.qstage[i % self.QST] == i
+            if i > 0:  # over P^T_{i-1}: dV_{i-1} read it, every softmax warp wrote it
+                assert ("DV", i - 1) in self.mma_done and c(("p", i - 1), 0) == 8
+        elif kind == "DP":
+            assert "V" in self.kv and self.ostage[i % self.OST] == i
+            if i > 0:  # over dP^T_{i-1} (and, for d = 128, dQ_{i-1})
+                assert c(("ds", i - 1), 0) == 8, "dP^T overwritten before the softmax read it"
+                if self.d == 128:
+                    assert c(("dqread", i - 1), 0) == 4, "dP^T overwrote dQ before it was read out"
+        elif kind == "DV":
+            assert c(("p", i), 0) == 8 and self.ostage[i % self.OST] == i
+        elif kind == "DQ":
+            assert c(("ds", i), 0) == 8, "dQ before dS was formed"
+            if self.d == 64 and i > 0:
+                assert c(("dqread", i - 1), 0) == 4, "dQ overwrote the previous dQ before it was read out"
+            if self.d == 128:   # into the dP^T columns: the softmax read dP^T_i (it formed dS_i)
+                assert ("DP", i) in self.mma_done
+        elif kind == "DK":
+            assert c(("ds", i), 0) == 8 and self.qstage[i % self.QST] == i
+        self.mma_done.add((kind, i))
+        self.completed_by[warp] += 1
+
+    def fire(self, e):
+        if e[0] == "land":
+            kind, s, i, bar = self.landing.pop(e[1])
+            if kind in ("K", "V"):
+                self.kv.add(kind)
+            elif kind == "Q":
+                self.qstage[s] = i
+            else:
+                self.ostage[s] = i
+            self.bars[bar].arrive()
+        else:
+            Model.fire(self, e)
+
+
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("strict", [False, True], ids=["default", "strict"])
+@pytest.mark.parametrize("nq", [1, 2, 3, 6])
+def test_backward_barrier_protocol(d, strict, nq):
+    rng = random.Random(2000 + 10 * nq + d + strict)
+    for _ in range(200):
+        BwdModel(nq, d, strict, rng).run()
+
+
+def test_model_catches_dp_overwriting_dq():
+    """Planted mistake in the model: for d = 128, warp B issuing dP^T_{i+1}
+    without waiting for the dQ warps to read dQ_i out of the same columns."""
+    class NoDqWait(BwdModel):
+        def mma_b(self):
+            for req in BwdModel.mma_b(self):
+                if req[0] == "wait" and req[1] == "DQE":
+                    continue
+                yield req
+    with pytest.raises(AssertionError, match="dQ before it was read out"):
+        for seed in range(100):
+            NoDqWait(6, 128, False, random.Random(seed)).run()
