@@ -267,7 +267,7 @@ CASES = [(1, 1, True), (2, 2, True), (5, 5, True), (3, 4, True), (1, 2, True), (
 @pytest.mark.parametrize("nkv0,nkv1,has1", CASES)
 def test_forward_barrier_protocol(stages, softmax_frees, strict, nkv0, nkv1, has1):
     rng = random.Random(hash((stages, strict, nkv0, nkv1, has1)) & 0xFFFFFFFF)
-    for _ in range(300):
+    for _ in range(500):
         Model(nkv0, nkv1, has1, stages, softmax_frees, strict, rng).run()
 
 
@@ -610,7 +610,7 @@ class BwdModel(Model):
 @pytest.mark.parametrize("nq", [1, 2, 3, 6])
 def test_backward_barrier_protocol(d, strict, nq):
     rng = random.Random(2000 + 10 * nq + d + strict)
-    for _ in range(200):
+    for _ in range(400):
         BwdModel(nq, d, strict, rng).run()
 
 

@@ -1,0 +1,66 @@
+"""Split-KV partial buffers: the row indexing of the split epilogue and of
+the merge, restated from the kernels' index expressions and checked on the
+CPU against the workspace the host plans (`fa_fwd_splitkv_plan`).
+
+Work unit u covers Q block u % nqb of head u // nqb (256 rows). Under a plan
+whose split units start at unit `first`, their rows start at
+row0 = (first // nqb) * N + (first % nqb) * 256, and the epilogue of key
+range s writes row r (< N) of head bh to partial row
+s * (B*H*N - row0) + (bh * N + r - row0). The merge reads, for every output
+row from row0 on, the same index for each s. The check: over every split
+unit, every key range and every row, the partial rows written are exactly
+[0, splits * (B*H*N - row0)), each once, inside the planned workspace, and
+they are the rows the merge reads.
+"""
+import numpy as np
+import pytest
+
+import exact_attention_87_gb300 as fa
+from exact_attention_87_gb300 import _build
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return fa.lib()
+
+
+def _written(B, H, N, first, splits):
+    nqb = -(-N // 256)
+    units = B * H * nqb
+    row0 = (first // nqb) * N + (first % nqb) * 256
+    span = B * H * N - row0
+    idx = []
+    for u in range(first, units):
+        bh, qb = divmod(u, nqb)
+        rows = np.arange(qb * 256, min(qb * 256 + 256, N))
+        for s in range(splits):
+            idx.append(s * span + (bh * N + rows - row0))
+    return np.concatenate(idx) if idx else np.zeros(0, dtype=np.int64), row0, span
+
+
+@pytest.mark.parametrize("B,H,N,d,num_sms", [
+    (1, 8, 16384, 128, 152), (1, 8, 16384, 128, 148), (8, 12, 2048, 128, 152), (1, 4, 10240, 128, 152),
+    (1, 2, 20000, 128, 152), (3, 5, 1000, 64, 7), (2, 3, 4097, 64, 13), (1, 1, 300, 64, 1),
+])
+@pytest.mark.parametrize("num_splits", [0, 2, 5])
+def test_partial_rows_tile_the_planned_workspace(L, B, H, N, d, num_sms, num_splits):
+    rc, p = fa.fa_fwd_splitkv_plan(B, H, N, d, num_splits, num_sms)
+    assert rc == fa.FA_OK
+    if p["splits"] == 1:
+        assert p["workspace_bytes"] == 0
+        return
+    idx, row0, span = _written(B, H, N, p["first_split_unit"], p["splits"])
+    # every partial row exactly once, no gap, no overlap
+    assert len(idx) == p["splits"] * span
+    assert np.array_equal(np.sort(idx), np.arange(p["splits"] * span))
+    # inside the planned workspace: fp32 O rows (256-byte aligned block) then fp32 LSE rows
+    o_bytes = (p["splits"] * span * d * 4 + 255) // 256 * 256
+    assert o_bytes + p["splits"] * span * 4 == p["workspace_bytes"]
+    # the merge reads row r >= row0 of range s at s * span + (r - row0): the same set
+    merge = np.concatenate([s * span + np.arange(span) for s in range(p["splits"])])
+    assert np.array_equal(np.sort(merge), np.sort(idx))
+    # and the merged rows are exactly the split units' rows
+    nqb = -(-N // 256)
+    first = p["first_split_unit"]
+    assert row0 == (first // nqb) * N + (first % nqb) * 256 and span == B * H * N - row0
