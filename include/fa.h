@@ -108,7 +108,9 @@ int fa_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE,
  * the number of SMs (long sequences, few heads).
  *
  * Arguments up to `dtype` are those of fa_fwd.
- * num_splits: >= 1 explicit (clamped to ceil(N/128)); 0 = chosen from the
+ * num_splits: >= 1 explicit (ranges of whole 128-key tiles, so at most
+ *             ceil(N/128); a count that does not divide the tiles evenly
+ *             gives ceil(tiles / ceil(tiles / num_splits)) ranges); 0 = chosen from the
  *             shape and the device's SM count (fa_fwd_splitkv_num_splits)
  *             by a cost model, which can also pick the tail plan: when the
  *             B*H*ceil(N/256) work units end in a partial last wave of SMs,
@@ -128,8 +130,10 @@ int fa_fwd_splitkv(const void *Q, const void *K, const void *V, void *O, float *
                    int B, int H, int N, int d, float scale, int dtype,
                    int num_splits, void *workspace, unsigned long long workspace_bytes, void *stream);
 
-/* The split count fa_fwd_splitkv uses for num_splits = 0 on the current
- * device (>= 1), or a negative fa_status on error. */
+/* The effective split count fa_fwd_splitkv uses for num_splits = 0 on the
+ * current device (>= 1: key ranges of each split unit after clamping to whole
+ * 128-key tiles; 1 = unsplit), or a negative fa_status on error. Under the
+ * tail plan only the units of the last wave are split this many ways. */
 int fa_fwd_splitkv_num_splits(int B, int H, int N, int d);
 
 /* Kernel launches fa_fwd_splitkv enqueues for this shape and split count on
