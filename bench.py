@@ -30,11 +30,14 @@ sys.path.insert(0, ROOT)
 
 DEFAULT_WORKLOAD = "b8h32n4096d128_bf16_qk3"
 FALLBACK_TFLOPS = 1900.0  # bf16 dense burst measured once on a GB300 (used only if no measured file)
+FALLBACK_SUSTAINED_TFLOPS = 1700.0  # the same measurement held for seconds under the power cap
+DATASHEET_TFLOPS = 2250.0  # GB300 dense bf16/fp16 tensor peak per GPU, nominal (without 2:4 sparsity)
 COMMON_SOURCES = ["exact_attention_87_gb300/csrc/sm103_ptx.cuh", "exact_attention_87_gb300/csrc/fa_device_common.cuh",
                   "exact_attention_87_gb300/csrc/fa_internal.h"]
 # The source files of the kernel each timed path spends its time in.
 KERNEL_SOURCES = {
     "fwd": ["exact_attention_87_gb300/csrc/fa_fwd_f16.cu"] + COMMON_SOURCES,
+    "fwd_d128": ["exact_attention_87_gb300/csrc/fa_fwd_d128.cu"] + COMMON_SOURCES,
     "fwd_d256": ["exact_attention_87_gb300/csrc/fa_fwd_d256.cu"] + COMMON_SOURCES,
     "bwd": ["exact_attention_87_gb300/csrc/fa_bwd_f16.cu"] + COMMON_SOURCES,
 }
@@ -52,6 +55,37 @@ def peaks():
         return float(m["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)", m
     except Exception:
         return FALLBACK_TFLOPS, "fallback", {}
+
+
+def sustained_peak(m: dict):
+    """The bf16 dense rate held for seconds under the power cap, and its source."""
+    try:
+        return float(m["bf16_tflops_sustained"]), "measured (MEASURED_PEAKS.json bf16_tflops_sustained)"
+    except Exception:
+        return FALLBACK_SUSTAINED_TFLOPS, "fallback"
+
+
+def sustained_leg(step, flops_per_step: float, stream, dev, barrier, seconds: float, ms_hint: float) -> dict:
+    """The same step back to back for about `seconds` (one event pair around
+    all of them), with the SM clock sampled throughout: how the kernel holds
+    up once the GPU settles at its power cap."""
+    import torch
+    n = max(10, int(seconds * 1e3 / max(ms_hint, 1e-3)))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    with sampler:
+        barrier()
+        e0.record(stream)
+        for _ in range(n):
+            step()
+        e1.record(stream)
+        barrier()
+    ms = e0.elapsed_time(e1) / n
+    value = flops_per_step / (ms * 1e-3) / 1e12
+    peak, src = sustained_peak(peaks()[2])
+    return {"seconds": round(ms * n / 1e3, 3), "steps": n, "value": round(value, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "peak": peak, "peak_source": src, "frac": round(value / peak, 4),
+            "clocks": sampler.summary()}
 
 
 def kernel_hash(kind: str = "fwd") -> str:
@@ -272,23 +306,81 @@ def dist_env():
     return ws, rank, local
 
 
-def run_oracle_sample(w, q, k, v, seconds: float, max_heads: int | None = None):
+def run_oracle_sample(w, q, k, v, seconds: float, max_heads: int | None = None, causal: bool = False):
     """Time the oracle on whole heads of the workload until about `seconds` pass.
-    Returns (flops done, wall seconds, threads, description)."""
+    Returns (flops done, wall seconds, threads, description, results) where
+    results holds each timed head's (b, h, O_ref, LSE_ref)."""
     import oracle
     threads = oracle.default_threads()
-    flops, t_total, heads = 0, 0.0, 0
-    per_head = 4 * w.N * w.N * w.d
-    bh = [(b, h) for b in range(w.B) for h in range(w.H)]
-    for (b, h) in bh:
+    flops, t_total, heads, results = 0, 0.0, 0, []
+    per_head = 4 * w.d * (w.N * (w.N + 1) // 2 if causal else w.N * w.N)
+    # heads spread over the batch: every (b, h) in a fixed shuffled order
+    order = [(b, h) for b in range(w.B) for h in range(w.H)]
+    order = [order[(i * 7919) % len(order)] for i in range(len(order))] if len(order) % 7919 else order
+    for (b, h) in order:
         t0 = time.perf_counter()
-        oracle.attn(q[b, h], k[b, h], v[b, h], scale=w.scale, nthreads=threads)
+        if causal:
+            o_ref, l_ref = oracle.attn_masked(q[b, h][None, None], k[b, h][None, None], v[b, h][None, None],
+                                              causal=True, scale=w.scale, nthreads=threads)
+            o_ref, l_ref = o_ref[0, 0], l_ref[0, 0]
+        else:
+            o_ref, l_ref = oracle.attn(q[b, h], k[b, h], v[b, h], scale=w.scale, nthreads=threads)
         t_total += time.perf_counter() - t0
+        results.append((b, h, o_ref, l_ref))
         flops += per_head
         heads += 1
         if t_total >= seconds or (max_heads and heads >= max_heads):
             break
-    return flops, t_total, threads, f"{heads} of {w.B * w.H} heads (all {w.N} rows each, fp64 three-pass)"
+    desc = (f"{heads} of {w.B * w.H} heads (all {w.N} rows each, fp64 three-pass" +
+            (", causal)" if causal else ")"))
+    return flops, t_total, threads, desc, results
+
+
+def bf16_rounding_excess(o, o_ref):
+    """Distance from o_ref to the interval of reals that round to the bf16
+    value o (0 when o is the rounding of o_ref itself)."""
+    import numpy as np
+    y = np.asarray(o, dtype=np.float64)
+    a = np.abs(y)
+    m, e = np.frexp(a)
+    ulp = np.ldexp(1.0, e - 8)
+    away, toward = ulp / 2, np.where(m == 0.5, ulp / 4, ulp / 2)
+    lo = np.where(a == 0, 0.0, np.where(y >= 0, y - toward, y - away))
+    hi = np.where(a == 0, 0.0, np.where(y >= 0, y + away, y + toward))
+    return np.maximum(0.0, np.maximum(lo - o_ref, o_ref - hi))
+
+
+def parity_figures(o, lse, results, dtype: str) -> dict:
+    """The timed output against the oracle on the CPU-baseline leg's heads:
+    max |err|, the bf16 error beyond the rounding of the stored output,
+    cosine over those heads and the smallest per-head cosine, max |dLSE|, and
+    whether the gates hold (fp16: max |err| <= 1e-2; bf16: error beyond the
+    rounding <= 1e-2; both: cosine >= 0.999, |dLSE| <= 1e-4 max(1, |LSE|))."""
+    import numpy as np
+    max_abs = max_ex = lse_max = 0.0
+    dot = n1 = n2 = 0.0
+    min_cos, lse_ok = 2.0, True
+    for b, h, o_ref, l_ref in results:
+        ob = o[b, h].float().cpu().double().numpy()
+        lb = lse[b, h].cpu().double().numpy()
+        max_abs = max(max_abs, float(np.abs(ob - o_ref).max()))
+        if dtype == "bf16":
+            max_ex = max(max_ex, float(bf16_rounding_excess(ob, o_ref).max()))
+        le = np.abs(lb - l_ref)
+        lse_max = max(lse_max, float(le.max()))
+        lse_ok = lse_ok and bool(np.all(le <= 1e-4 * np.maximum(1.0, np.abs(l_ref))))
+        hd, h1, h2 = float((ob * o_ref).sum()), float((ob * ob).sum()), float((o_ref * o_ref).sum())
+        min_cos = min(min_cos, hd / (h1 * h2) ** 0.5)
+        dot, n1, n2 = dot + hd, n1 + h1, n2 + h2
+    cos = dot / (n1 * n2) ** 0.5
+    o_metric = max_ex if dtype == "bf16" else max_abs
+    res = {"heads": len(results), "max_abs": round(max_abs, 6), "cos": round(cos, 9),
+           "min_head_cos": round(min_cos, 9), "lse_max_abs": float(f"{lse_max:.3e}")}
+    if dtype == "bf16":
+        res["max_excess_over_rounding"] = round(max_ex, 6)
+    res["ok"] = bool(o_metric <= 1e-2 and cos >= 0.999 and min_cos >= 0.999 and lse_ok)
+    res["checked"] = "the output of the last timed step, every element of the heads the CPU baseline computed"
+    return res
 
 
 def main():
@@ -299,16 +391,22 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline budget")
+    ap.add_argument("--sustained-seconds", type=float, default=2.0,
+                    help="length of the sustained leg (0: skip it)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--causal", action="store_true",
                     help="causal mask (FLOPs counted for the keys each row sees: 4*d*N*(N+1)/2 per head)")
     ap.add_argument("--splits", type=int, default=None,
                     help="forward split-KV ranges (0 = automatic, the default: unsplit unless the cost model finds "
-                         "the wave tail worth splitting; 1 = the plain forward pass); masked and backward runs "
-                         "are unsplit")
+                         "the wave tail worth splitting; 1 = the plain forward pass); causal runs default to 1, "
+                         "backward runs are unsplit")
     ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
                     help="bwd: time the backward pass (fa_bwd: dQ, dK, dV; 10*B*H*N^2*d FLOPs) instead")
+    ap.add_argument("--shard", default="none", choices=["none", "heads"],
+                    help="heads: one problem split across the ranks in contiguous blocks of its B*H (batch, head) "
+                         "problems (strong scaling, no collective); none: every rank runs the whole workload "
+                         "(weak scaling)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override B (smaller captures of the same workload for profiling; not a bench line)")
     args = ap.parse_args()
@@ -317,8 +415,6 @@ def main():
         raise SystemExit("--pass bwd does not take --splits")
     if args.splits is None:
         args.splits = 1 if (args.causal or args.which == "bwd") else 0
-    if args.causal and args.splits != 1:
-        raise SystemExit("masks are not combined with split-KV: --causal takes --splits 1")
 
     import dataclasses
     from workloads import WORKLOADS, make_inputs
@@ -355,6 +451,17 @@ def main():
     fa.lib()
 
     q, k, v = make_inputs(w)
+    job_flops = flops
+    if args.shard == "heads":
+        # This rank's contiguous block of the B*H problems of the one workload.
+        from exact_attention_87_gb300.head_parallel import head_bounds, head_slice
+        lo, hi = head_bounds(w.B, w.H, ws, rank)
+        if hi <= lo:
+            raise SystemExit("--shard heads needs at least one (batch, head) problem per rank")
+        q, k, v = (head_slice(t, lo, hi).contiguous() for t in (q, k, v))
+        w = dataclasses.replace(w, B=1, H=hi - lo)
+        flops = flops * (hi - lo) // (cfg["B"] * cfg["H"])
+        cfg["parallelism"] = f"heads: rank r runs problems head_bounds(B, H, {ws}, r) (no collective)"
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     o = torch.empty_like(qd)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
@@ -363,7 +470,7 @@ def main():
     workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     # The plan the library runs: 1 launch (unsplit), 2 (every unit split, merge) or 3 (split wave tail).
     n_launch = 1
-    if args.splits != 1 and not args.causal and w.dtype != "f32" and w.d != 256:
+    if args.splits != 1 and w.dtype != "f32" and w.d != 256:
         n_launch = fa.fa_fwd_splitkv_launches(w.B, w.H, w.N, w.d, args.splits)
         if n_launch < 1:
             raise RuntimeError(f"fa_fwd_splitkv_launches failed ({n_launch})")
@@ -396,7 +503,13 @@ def main():
     st = fa.fa_get_device_status()
     if st != fa.FA_OK:
         raise RuntimeError(f"device status {st} after the timed region")
-    tflops = job_throughput(ws, flops, ms)
+    # weak: every rank ran the whole workload; strong (--shard heads): the
+    # ranks shared one workload, the job's FLOPs over the slowest rank's time
+    tflops = job_throughput(ws, flops, ms) if args.shard == "none" else job_flops / (ms * 1e-3) / 1e12
+    # The timed steps' output, kept for the parity figures (the e2e leg below reuses the buffers).
+    o_timed, lse_timed = o.clone(), lse.clone()
+    sustained = (sustained_leg(step, flops, stream, dev, barrier, args.sustained_seconds, ms)
+                 if args.sustained_seconds > 0 else None)
 
     # ---- e2e: public API with host buffers, copies inside the timed region ----
     e2e = None
@@ -431,7 +544,7 @@ def main():
 
     peak, peak_src, _ = peaks()
     achieved = flops / (ms * 1e-3) / 1e12
-    kind = "fwd_d256" if w.d == 256 else "fwd"
+    kind = "fwd_d256" if w.d == 256 else "fwd_d128" if w.d == 128 else "fwd"
     traffic = recorded_traffic(w.name, kind) if not args.causal and n_launch == 1 else None
     line = {
         "metric": "attention fwd TFLOP/s (4*B*H*N^2*d) and % of GB300 dense BF16 tensor peak",
@@ -443,29 +556,43 @@ def main():
         "ms_per_step": round(ms, 4),
         "ms_per_step_dist": step_distribution(per_step),
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "weak" if args.shard == "none" else "strong",
         "vs_baseline": None,
         "dtype": w.dtype,
         "data": "synthetic (seeded, generated on the host)",
         "config": cfg,
-        "pct_of_peak": round(100.0 * achieved / peak, 2),
+        "pct_of_measured_peak": round(100.0 * achieved / peak, 2),
+        "pct_of_datasheet_peak": round(100.0 * achieved / DATASHEET_TFLOPS, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                     "kernel": (f"fa_fwd_d256_kernel<{'bf16' if w.dtype == 'bf16' else 'f16'}>" if w.d == 256 else
-                                f"fa_fwd_f16_kernel<{w.d},{'bf16' if w.dtype == 'bf16' else 'f16'}>"),
+                     "kernel": fwd_kernel_name(w),
                      "traffic": traffic, "algorithmic_bytes": w.hbm_bytes},
         "clocks": sampler.summary(),
+        "sustained": sustained,
         "gpu_launches": args.steps * n_launch,
         "e2e": e2e,
     }
     if ws == 1 and not args.no_cpu_baseline:
-        flops, secs, threads, desc = run_oracle_sample(w, q, k, v, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+        flops_s, secs, threads, desc, results = run_oracle_sample(w, q, k, v, args.cpu_seconds, causal=args.causal)
+        line["cpu_baseline"] = {"value": round(flops_s / secs / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
                                 "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+        line["parity"] = parity_figures(o_timed, lse_timed, results, w.dtype)
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def fwd_kernel_name(w) -> str:
+    """The forward kernel a workload's step spends its time in."""
+    t = "bf16" if w.dtype == "bf16" else "f16"
+    if w.dtype == "f32":
+        return f"fa_fwd_f32_kernel<{w.d}>"
+    if w.d == 256:
+        return f"fa_fwd_d256_kernel<{t}>"
+    if w.d == 128:
+        return f"fa_fwd_d128_kernel<{t}>"
+    return f"fa_fwd_f16_kernel<{w.d},{t}>"
 
 
 def bwd_config(cfg, causal: bool) -> dict:
@@ -572,7 +699,8 @@ def run_backward(args, w, cfg, ws, rank, local):
         "ms_per_step": round(ms, 4), "ms_per_step_dist": step_distribution(per_step), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded, generated on the host)", "config": cfg,
-        "pct_of_peak": round(100.0 * achieved / peak, 2),
+        "pct_of_measured_peak": round(100.0 * achieved / peak, 2),
+        "pct_of_datasheet_peak": round(100.0 * achieved / DATASHEET_TFLOPS, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
                      "kernel": "whole step: fa_bwd_pre + fa_bwd_main + fa_bwd_post",

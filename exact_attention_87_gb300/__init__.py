@@ -50,7 +50,7 @@ def lib(path: str | None = None):
             f"{path} is missing: build it with exact_attention_87_gb300._build.build() "
             "(nvcc for sm_103a); this package has no CPU fallback")
     L = ctypes.CDLL(path)
-    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    vp, i, f, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_ulonglong
     L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     L.fa_fwd.restype = i
     L.fa_get_device_status.argtypes = [vp]
@@ -59,11 +59,12 @@ def lib(path: str | None = None):
     L.fa_strerror.restype = ctypes.c_char_p
     L.fa_abi_version.argtypes = []
     L.fa_abi_version.restype = i
-    u64 = ctypes.c_ulonglong
     L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, u64, vp]
     L.fa_fwd_splitkv.restype = i
     L.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, vp]
     L.fa_fwd_ex.restype = i
+    L.fa_fwd_splitkv_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, i, vp, u64, vp]
+    L.fa_fwd_splitkv_ex.restype = i
     L.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
     L.fa_fwd_splitkv_noalloc.restype = i
     L.fa_fwd_splitkv_num_splits.argtypes = [i, i, i, i]
@@ -105,6 +106,12 @@ def fa_fwd_splitkv(Q, K, V, O, LSE, B, H, N, d, scale, dtype, num_splits, worksp
                    stream=None) -> int:
     return lib().fa_fwd_splitkv(Q, K, V, O, LSE, B, H, N, d, scale, dtype, num_splits, workspace,
                                 workspace_bytes, stream)
+
+
+def fa_fwd_splitkv_ex(Q, K, V, O, LSE, B, H, N, d, scale, dtype, causal, seqlens_k, num_splits, workspace,
+                      workspace_bytes, stream=None) -> int:
+    return lib().fa_fwd_splitkv_ex(Q, K, V, O, LSE, B, H, N, d, scale, dtype, causal, seqlens_k, num_splits,
+                                   workspace, workspace_bytes, stream)
 
 
 def fa_fwd_splitkv_noalloc(Q, K, V, O, LSE, B, H, N, d, scale, dtype, num_splits, stream=None) -> int:
@@ -194,7 +201,7 @@ def attention(q, k, v, scale: float | None = None, out=None, lse=None, stream=No
     ``num_splits`` != 1 runs the split-KV path (0 = automatic count); its
     workspace is allocated with torch unless a CUDA uint8 tensor is given.
     ``causal`` / ``seqlens_k`` (CUDA int32 tensor [B] of key lengths) select the
-    masked pass (not combined with split-KV).
+    masked pass, unsplit or (``num_splits`` != 1) split.
     """
     import torch
     if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
@@ -222,16 +229,23 @@ def attention(q, k, v, scale: float | None = None, out=None, lse=None, stream=No
     elif hasattr(stream, "cuda_stream"):
         stream = stream.cuda_stream
     with torch.cuda.device(q.device):
-        if causal or seqlens_k is not None:
-            if num_splits != 1:
-                raise ValueError("masks are not combined with split-KV")
-            kl = None
-            if seqlens_k is not None:
-                if seqlens_k.dtype != torch.int32 or not seqlens_k.is_cuda or seqlens_k.numel() != B:
-                    raise ValueError("seqlens_k must be a CUDA int32 tensor of B lengths")
-                kl = seqlens_k.contiguous().data_ptr()
+        masked = causal or seqlens_k is not None
+        kl = None
+        if seqlens_k is not None:
+            if seqlens_k.dtype != torch.int32 or not seqlens_k.is_cuda or seqlens_k.numel() != B:
+                raise ValueError("seqlens_k must be a CUDA int32 tensor of B lengths")
+            seqlens_k = seqlens_k.contiguous()
+            kl = seqlens_k.data_ptr()
+        if masked and num_splits == 1:
             rc = fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                            B, H, N, d, float(scale), _dtype_code(q), int(bool(causal)), kl, stream)
+        elif masked:
+            need = fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits)
+            if workspace is None:
+                workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+            rc = fa_fwd_splitkv_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                   B, H, N, d, float(scale), _dtype_code(q), int(bool(causal)), kl, num_splits,
+                                   workspace.data_ptr(), workspace.numel(), stream)
         elif num_splits == 1:
             rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                         B, H, N, d, float(scale), _dtype_code(q), stream)
@@ -379,7 +393,7 @@ def attention_backward(q, k, v, o, lse, do, scale: float | None = None, dq=None,
 
 __all__ = ["attention", "attention_backward", "attention_partial", "merge_partials", "fa_fwd_partial", "fa_merge",
            "fa_fwd_splitkv_launches",
-           "fa_bwd", "fa_bwd_ex", "fa_bwd_workspace_size", "fa_fwd", "fa_fwd_ex", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_num_splits",
+           "fa_bwd", "fa_bwd_ex", "fa_bwd_workspace_size", "fa_fwd", "fa_fwd_ex", "fa_fwd_splitkv", "fa_fwd_splitkv_ex", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_num_splits",
            "fa_fwd_splitkv_workspace_size",
            "fa_get_device_status", "fa_strerror", "fa_abi_version", "build", "lib",
            "FAError", "FA_F32", "FA_F16", "FA_BF16", "FA_OK"]

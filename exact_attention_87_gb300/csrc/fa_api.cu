@@ -5,6 +5,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include <cuda.h>
@@ -42,6 +43,22 @@ std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 long long g_wait_limit = 0;
+
+#ifdef FA_TESTING
+// Testing build: when set, the entry points return FA_OK after every argument
+// and device check, before anything is enqueued (so that argument-error tests
+// can pass placeholder addresses: a check that regressed then shows up as a
+// wrong status, never as a launch on memory that does not exist).
+std::atomic<int> g_dry_run{0};
+#define FA_DRY_RUN_RETURN() \
+  do {                      \
+    if (g_dry_run.load()) return FA_OK; \
+  } while (0)
+#else
+#define FA_DRY_RUN_RETURN() \
+  do {                      \
+  } while (0)
+#endif
 
 long long wait_limit_cycles() {
   if (g_wait_limit == 0) {
@@ -260,10 +277,11 @@ PlanSummary summarize_plan(int B, int H, int N, int d, int num_splits, int num_s
           workspace_bytes_for(B, H, N, d, eff, tail ? plan_row0(plan, N) : 0)};
 }
 
-int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
-             float scale, int dtype, void* stream, int inject, float* stats_trace, unsigned long long* timeline,
-             long long wait_limit, int num_splits = 1, void* workspace = nullptr,
-             unsigned long long workspace_bytes = 0, int causal = 0, const int* klen = nullptr) {
+// Argument checks of the forward entry points, in the order their status
+// codes are documented: pointers, dtype, shape, head dimension, scale, mask
+// flag, size limits, alignment. Nothing here touches a device.
+int validate_fwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, int B, int H, int N,
+                 int d, float scale, int dtype, int causal) {
   if (!Q || !K || !V || !O || !LSE) return FA_ERR_NULL;
   if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
   if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
@@ -275,6 +293,22 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
       (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0)
     return FA_ERR_ALIGN;
+  return FA_OK;
+}
+
+int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
+             float scale, int dtype, void* stream, int inject, float* stats_trace, unsigned long long* timeline,
+             long long wait_limit, int num_splits = 1, void* workspace = nullptr,
+             unsigned long long workspace_bytes = 0, int causal = 0, const int* klen = nullptr,
+             float rescale_tau = fa::kRescaleThresholdLog2, float* o_f32 = nullptr) {
+  // o_f32 (testing build only): O is written as normalised fp32, before the
+  // rounding to the input type, to o_f32 instead of O (O may then be NULL).
+  const int vst = validate_fwd(Q, K, V, O ? O : o_f32, LSE, B, H, N, d, scale, dtype, causal);
+  if (vst != FA_OK) return vst;
+  const long long BH = static_cast<long long>(B) * H;
+  if (o_f32 && !aligned16(o_f32)) return FA_ERR_ALIGN;
+  if (o_f32 && (dtype == FA_F32 || d == 256 || num_splits != 1 || causal || klen)) return FA_ERR_UNSUPPORTED;
+  if (!(rescale_tau >= 0.f) || !(rescale_tau <= 64.f)) return FA_ERR_SCALE;
 
   DeviceInfo dev;
   int st = device_info(&dev);
@@ -301,6 +335,7 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
   p.d = d;
   p.scale = scale;
   p.num_sms = dev.num_sms;
+  p.rescale_tau = rescale_tau;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // fp32 and d = 256 always run unsplit.
   const SplitPlan plan = (dtype == FA_F32 || d == 256) ? SplitPlan{1, -1}
@@ -318,7 +353,14 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
     p.o_part = static_cast<float*>(workspace);
     p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((rows * d * 4 + 255) & ~255ull));
   }
+  if (o_f32) {
+    // The one-part epilogue writes [B*H*N, d] fp32 rows and the LSE (natural log).
+    p.partial = 1;
+    p.o_part = o_f32;
+    p.lse_part = LSE;
+  }
 
+  FA_DRY_RUN_RETURN();
   cudaError_t e;
   if (dtype == FA_F32) {
     e = fa::launch_fwd_f32(p, s);
@@ -326,11 +368,11 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
     const CUtensorMapDataType dt =
         dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const int bh = static_cast<int>(BH);
-    const int kv_rows = d == 256 ? fa::kD256BlockKV : fa::kF16BlockKV;
+    const int kv_rows = fa::fwd_kv_box_rows(d);
     if (!encode_bhnd_16bit(&p.tm_q, Q, bh, N, d, dt, fa::kF16BlockQ) ||
         !encode_bhnd_16bit(&p.tm_k, K, bh, N, d, dt, kv_rows) ||
         !encode_bhnd_16bit(&p.tm_v, V, bh, N, d, dt, kv_rows) ||
-        !encode_bhnd_16bit(&p.tm_o, O, bh, N, d, dt, fa::kF16BlockQ))
+        (O && !encode_bhnd_16bit(&p.tm_o, O, bh, N, d, dt, fa::kF16BlockQ)))
       return FA_ERR_CUDA;
     if (d == 256) {
       e = fa::launch_fwd_d256(p, dtype == FA_BF16, s);
@@ -397,15 +439,17 @@ int partial_impl(const void* Q, const void* K, const void* V, float* O_part, flo
   p.d = d;
   p.scale = scale;
   p.num_sms = dev.num_sms;
+  p.rescale_tau = fa::kRescaleThresholdLog2;
   p.num_splits = 1;
   p.split_tiles = static_cast<int>(kv_tiles(Nk));
   p.partial = 1;
   const CUtensorMapDataType dt = dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const int bh = static_cast<int>(BH);
   if (!encode_bhnd_16bit(&p.tm_q, Q, bh, Nq, d, dt, fa::kF16BlockQ) ||
-      !encode_bhnd_16bit(&p.tm_k, K, bh, Nk, d, dt, fa::kF16BlockKV) ||
-      !encode_bhnd_16bit(&p.tm_v, V, bh, Nk, d, dt, fa::kF16BlockKV))
+      !encode_bhnd_16bit(&p.tm_k, K, bh, Nk, d, dt, fa::fwd_kv_box_rows(d)) ||
+      !encode_bhnd_16bit(&p.tm_v, V, bh, Nk, d, dt, fa::fwd_kv_box_rows(d)))
     return FA_ERR_CUDA;
+  FA_DRY_RUN_RETURN();
   const cudaError_t e = fa::launch_fwd_f16(p, dtype == FA_BF16, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -437,7 +481,8 @@ int merge_impl(const float* O_parts, const float* LSE_parts, int num_parts, void
   p.N = N;
   p.Nk = N;
   p.d = d;
-  const cudaError_t e = fa::launch_merge_guarded(p, dtype == FA_BF16, static_cast<cudaStream_t>(stream));
+  FA_DRY_RUN_RETURN();
+  const cudaError_t e = fa::launch_merge(p, dtype == FA_BF16, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -474,12 +519,21 @@ int fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* 
                   workspace_bytes);
 }
 
+int fa_fwd_splitkv_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
+                      float scale, int dtype, int causal, const int* seqlens_k, int num_splits, void* workspace,
+                      unsigned long long workspace_bytes, void* stream) {
+  if (num_splits < 0) return FA_ERR_SHAPE;
+  return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, dtype, stream, 0, nullptr, nullptr, 0, num_splits, workspace,
+                  workspace_bytes, causal, seqlens_k);
+}
+
 int fa_fwd_splitkv_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
                            int d, float scale, int dtype, int num_splits, void* stream) {
+  // Every argument check of fa_fwd_splitkv first (same codes, same order);
+  // only then the device lookup of the scratch and the size limit.
+  const int vst = validate_fwd(Q, K, V, O, LSE, B, H, N, d, scale, dtype, 0);
+  if (vst != FA_OK) return vst;
   if (num_splits < 0) return FA_ERR_SHAPE;
-  if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
-  if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
-  if (d != 64 && d != 128 && !(d == 256 && dtype != FA_F32)) return FA_ERR_HEADDIM;
   void* scratch = nullptr;
   const int st = noalloc_scratch(&scratch);
   if (st != FA_OK) return st;
@@ -603,6 +657,7 @@ int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const v
       !encode_bhnd_16bit(&p.tm_dv, dV, bh, N, d, dt, fa::kF16BlockKV) ||
       !encode_bhnd_f32_box32(&p.tm_dqacc, p.dq_acc, bh, N, d))
     return FA_ERR_CUDA;
+  FA_DRY_RUN_RETURN();
   const cudaError_t e = fa::launch_bwd_f16(p, dtype == FA_BF16, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -649,6 +704,16 @@ int fa_fwd_testing(const void* Q, const void* K, const void* V, void* O, float* 
   return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, dtype, stream, inject, stats_trace, timeline,
                   wait_limit_cycles);
 }
+
+int fa_fwd_debug(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
+                 float scale, int dtype, void* stream, float* O_f32, float rescale_threshold_log2,
+                 float* stats_trace) {
+  const float tau = rescale_threshold_log2 < 0.f ? fa::kRescaleThresholdLog2 : rescale_threshold_log2;
+  return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, dtype, stream, 0, stats_trace, nullptr, 0, 1, nullptr, 0, 0,
+                  nullptr, tau, O_f32);
+}
+
+void fa_testing_set_dry_run(int on) { g_dry_run.store(on ? 1 : 0); }
 
 unsigned int fa_testing_last_timeout_where(void) {
   unsigned int h[2] = {0, 0};

@@ -165,8 +165,11 @@ __device__ __forceinline__ void bwd_producer(const BwdParams& p, uint32_t base, 
     noi = i + 1;
     FA_TRACE(p, kBvDOLoad, i);
   }
-  if (!ok) {
-    // Every copy this thread started must land before the CTA exits.
+  // Drain, always (the loop ended, this thread's wait gave up, or another role
+  // may abort later): every copy this thread started must land before the CTA
+  // exits. Cheap when nothing failed: the consumers need these copies anyway.
+  (void)ok;
+  {
     wait_bar_drain(bk, 0, ctl);
     wait_bar_drain(bv, 0, ctl);
     for (int t = nqi > C::QST ? nqi - C::QST : 0; t < nqi; ++t)

@@ -70,6 +70,21 @@ __device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, co
   return wait_bar_slow(bar, parity, ctl, kWhereDrain, false);
 }
 
+// The lazy-rescale threshold in log2 units: the reference max of a row moves
+// only when P taken against it would exceed 2^threshold (the d = 64 and 256
+// kernels test the tile max against it, the d = 128 kernel the tile's sum of
+// P), so P <= 2^threshold (fits fp16 and bf16). The testing build takes it
+// from the parameters, so that 0 (rescale whenever the max grows, the
+// dataflow page's section 2.3) can be run against the oracle too.
+__device__ __forceinline__ float rescale_threshold(const FwdParams& p) {
+#ifdef FA_TESTING
+  return p.rescale_tau;
+#else
+  (void)p;
+  return kRescaleThresholdLog2;
+#endif
+}
+
 // Testing build only: clock64 stamp of pipeline event `ev` for tile `j`.
 #ifdef FA_TESTING
 #define FA_TRACE(p, ev, j)                                                                                 \

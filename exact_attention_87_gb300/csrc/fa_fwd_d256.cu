@@ -32,7 +32,6 @@ namespace {
 
 constexpr float kLog2e256 = 1.4426950408889634f;
 constexpr float kLn2_256 = 0.6931471805599453f;
-constexpr float kRescaleThreshold256 = 8.0f;  // log2 units: P stays <= 2^8
 
 struct C256 {
   static constexpr int D = 256;
@@ -107,7 +106,11 @@ __device__ __forceinline__ void producer256(const FwdParams& p, uint32_t base, i
       tma_load_3d(base + C::OFF_V + s * C::KV_BYTES + h * C::KV_BLOCK, &p.tm_v, vf, 64 * h, j * C::BN, bh);
     nv = j + 1;
   }
-  if (!ok) {
+  // Drain, always (the loop ended, this thread's wait gave up, or another role
+  // may abort later): every copy this thread started must land before the CTA
+  // exits. Cheap when nothing failed: the consumers need these copies anyway.
+  (void)ok;
+  {
     wait_bar_drain(bq, 0, ctl);
     for (int t = nk > C::STAGES ? nk - C::STAGES : 0; t < nk; ++t)
       wait_bar_drain(bar256(base, C::B_KF + t % C::STAGES), (t / C::STAGES) & 1, ctl);
@@ -195,6 +198,7 @@ __device__ __forceinline__ void softmax256(const FwdParams& p, uint32_t base, ui
   const int my_row = row0 + t;
   const int row_end = p.causal ? min(key_end, my_row + 1) : key_end;
   const uint32_t b_od = bar256(base, C::B_OD);
+  const float tau = rescale_threshold(p);
   float m_ref = -INFINITY, l = 0.f, l_o = 0.f;
   bool ok = true;
 
@@ -241,7 +245,7 @@ __device__ __forceinline__ void softmax256(const FwdParams& p, uint32_t base, ui
     float alpha = 1.f;
     if (j == 0) {
       m_ref = m_new;
-    } else if (__any_sync(0xffffffffu, m_new - m_ref > kRescaleThreshold256)) {
+    } else if (__any_sync(0xffffffffu, m_new - m_ref > tau)) {
       alpha = ex2_approx(m_ref - m_new);
       m_ref = m_new;
       l *= alpha;

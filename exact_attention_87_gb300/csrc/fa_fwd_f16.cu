@@ -34,7 +34,8 @@
 // the two warps pass a turn so that their MMA blocks alternate (ping-pong) and
 // each runs inside the other chain's softmax.
 // The rescale of O is lazy: the reference max only moves when the tile max
-// exceeds it by more than 8 (log2 units), so P <= 256 and rescales are rare.
+// exceeds it by more than the threshold (15 in log2 units), so P <= 2^15 and
+// rescales are rare.
 // The epilogue divides by l, rounds to the input type, stages the tile in the
 // (now unused) Q buffer in the TMA 128-byte swizzle layout and TMA-stores it;
 // LSE = ln2 * (m + log2 l) is written per row.
@@ -47,7 +48,6 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8
 #ifdef FA_STRICT_MMA_ORDER
 constexpr bool kOdEveryTile = true;   // every P.V committed to o_done (S waits for it)
 #else
@@ -157,9 +157,14 @@ __device__ __forceinline__ void producer(const FwdParams& p, uint32_t base, int 
     nv = j + 1;
     FA_TRACE(p, kEvVIssued, j);
   }
-  if (!ok) {
-    // Drain: every copy this thread started must land before the CTA exits. The
-    // most recent load of each stage is one of the last STAGES tiles issued.
+  // Drain: every copy this thread started must land before the CTA exits,
+  // whether the loop ended normally, this thread's own wait gave up, or
+  // another role aborts later (its waits give up only after the last loads
+  // were issued). The most recent load of each stage is one of the last
+  // STAGES tiles issued. Cheap when nothing failed: the consumers need these
+  // copies anyway, so they land before the CTA could finish.
+  (void)ok;
+  {
     wait_bar_drain(bq, 0, ctl);
     for (int t = nk > C::STAGES ? nk - C::STAGES : 0; t < nk; ++t)
       wait_bar_drain(bar_addr<D>(base, C::B_KF + t % C::STAGES), (t / C::STAGES) & 1, ctl);
@@ -284,6 +289,7 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
   const int my_row = row0 + C::BM * sub + t;
   const int row_end = p.causal ? min(key_end, my_row + 1) : key_end;
 
+  const float tau = rescale_threshold(p);
   float m_ref = -INFINITY;  // reference max (log2 units) shared by l and O
   float l = 0.f;            // sum of P (fp32) relative to m_ref: gives LSE
   float l_o = 0.f;          // bf16 only: sum of the rounded P: normalises O
@@ -351,8 +357,10 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
     float alpha = 1.f;
     if (j == 0) {
       m_ref = m_new;  // O is written fresh by the first P.V; l is 0
-    } else if (__any_sync(0xffffffffu, m_new - m_ref > kRescaleThreshold)) {
-      alpha = ex2_approx(m_ref - m_new);  // = exp(m_old - m_new) in natural units
+    } else if (__any_sync(0xffffffffu, m_new - m_ref > tau)) {
+      // = exp(m_old - m_new) in natural units; 0 for a row that saw no key
+      // yet (its l and O are 0), never exp2(-inf + inf)
+      alpha = m_ref > -INFINITY ? ex2_approx(m_ref - m_new) : 0.f;
       m_ref = m_new;
       l *= alpha;
       l_o *= alpha;
@@ -364,8 +372,12 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
     // bits, so O is normalised by the sum of the rounded P (l_o): numerator
     // and denominator then use the same weights, which keeps |dO| well below
     // the rounding of a bf16 output even for sharply peaked rows.
+    // A row that has seen no key yet (every score so far masked: possible in
+    // a key range of a split under the causal mask) keeps m_ref = -inf; its
+    // P are computed against 0 so that they are 0, not exp2(-inf + inf).
+    const float m_use = m_ref > -INFINITY ? m_ref : 0.f;
     const float2 c2 = make_float2(c, c);
-    const float2 nm2 = make_float2(-m_ref, -m_ref);
+    const float2 nm2 = make_float2(-m_use, -m_use);
     float2 se = make_float2(0.f, 0.f), sro = se;  // exact / rounded partial sums
 #pragma unroll
     for (int q = 0; q < C::BN / 16; ++q) {
@@ -435,8 +447,9 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
 
   // ---- epilogue: O / l -> dtype -> swizzled staging (Q buffer) -> TMA store; LSE ----
   tc_fence_after();
-  // No key to attend to (key length 0): O = 0, LSE = -inf instead of 0/0.
-  const bool empty = nkv == 0;
+  // No key to attend to (key length 0, or under the causal mask no key of
+  // this split's range for this row): O = 0, LSE = -inf instead of 0/0.
+  const bool empty = nkv == 0 || !(l > 0.f);
   const float inv_l = empty ? 0.f : 1.0f / (BF16 ? l_o : l);
   if (p.num_splits > 1 || p.partial) {
     // Split-KV (or one part of a merge done elsewhere): this key range's
@@ -452,6 +465,10 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
       tmem_ld32(t_o + 32 * q, r);
       tmem_ld_wait();
       reg_fence(r);
+      if (empty) {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) r[u] = 0u;  // no key in this range: O_part = 0, LSE_part = -inf
+      }
       if (row < p.N) {
         float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D + 32 * q);
 #pragma unroll
@@ -460,7 +477,7 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
                                __uint_as_float(r[4 * u + 2]) * inv_l, __uint_as_float(r[4 * u + 3]) * inv_l);
       }
     }
-    if (row < p.N) p.lse_part[prow] = (m_ref + lg2_approx(l)) * kLn2;
+    if (row < p.N) p.lse_part[prow] = empty ? -INFINITY : (m_ref + lg2_approx(l)) * kLn2;
     return;
   }
   const uint32_t stage = base + C::OFF_Q + sub * C::Q_SUB_BYTES;
@@ -517,8 +534,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
   const int split = blockIdx.x % p.num_splits;
   const int qunit = p.qunit0 + blockIdx.x / p.num_splits;
   const int bh = qunit / nqb;
-  // Causal: Q blocks later in the sequence see more keys; they are launched first.
-  const int qb = p.causal ? nqb - 1 - qunit % nqb : qunit % nqb;
+  // Causal, one launch over every unit unsplit: Q blocks later in the
+  // sequence see more keys; they are launched first. Split launches keep the
+  // natural order, in which the units of the split-KV tail plan (the last
+  // ones) hold the last rows: its merge and partial buffers cover the rows
+  // from merge_row0 on.
+  const bool heavy_first = p.causal && p.num_splits == 1 && p.qunit_count == 0;
+  const int qb = heavy_first ? nqb - 1 - qunit % nqb : qunit % nqb;
   const int row0 = qb * 2 * C::BM;
   const bool has1 = row0 + C::BM < p.N;
   // Keys this unit may see: [0, key_end); causal limits each sub-tile to its own last row.
@@ -526,9 +548,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
   const int end0 = p.causal ? min(key_end, row0 + C::BM) : key_end;
   const int end1 = p.causal ? min(key_end, row0 + 2 * C::BM) : key_end;
   const int t0 = split * p.split_tiles;                      // first K/V tile of this key range
-  // Tiles per sub-tile (masks are not combined with split-KV: then t0 = 0, split_tiles = all tiles).
-  const int nkv0 = min((end0 + C::BN - 1) / C::BN - t0, p.split_tiles);
-  const int nkv1 = has1 ? min((end1 + C::BN - 1) / C::BN - t0, p.split_tiles) : 0;
+  // Tiles per sub-tile in this key range (none when its keys end before the range starts).
+  const int nkv0 = max(0, min((end0 + C::BN - 1) / C::BN - t0, p.split_tiles));
+  const int nkv1 = has1 ? max(0, min((end1 + C::BN - 1) / C::BN - t0, p.split_tiles)) : 0;
   const int nkv = max(nkv0, nkv1);                           // tiles the producer loads
 
   if (threadIdx.x == 0) {
@@ -629,8 +651,14 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream) {
 }
 
 // Split-KV merge (block merge of the Triton page, section 2.3, in LSE form):
-// LSE = m + log sum_s exp(LSE_s - m), O = sum_s exp(LSE_s - LSE) O_s.
-// One warp per output row; lane k handles D/32 consecutive columns.
+// LSE = m + log sum_s exp(LSE_s - m), O = sum_s exp(LSE_s - LSE) O_s, with
+// m the largest LSE_s. Rows [merge_row0, B*H*N): their parts are numbered
+// from merge_row0, one span per part (as the split epilogue writes them). A
+// part that saw no key has LSE_s = -inf and O_s = 0 and adds nothing; a row
+// that no part saw (every LSE_s = -inf: masked by the key lengths or the
+// causal mask) gets O = 0 and LSE = -inf instead of 0/0 (the guard of the
+// Triton page, section 5.1). One warp per output row; lane k handles D/32
+// consecutive columns.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_merge_kernel(const __grid_constant__ FwdParams p) {
   constexpr int E = D / 32;
@@ -638,7 +666,6 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const __grid_constant__ F
   const long long row = p.merge_row0 + ((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
-  // partial rows numbered from merge_row0, one span per key range (as the split epilogue writes them)
   const long long span = rows - p.merge_row0, prow = row - p.merge_row0;
   float m = -INFINITY;
   for (int s = 0; s < p.num_splits; ++s) m = fmaxf(m, p.lse_part[s * span + prow]);
@@ -646,23 +673,25 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const __grid_constant__ F
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   float l = 0.f;
-  for (int s = 0; s < p.num_splits; ++s) {
-    const float w = ex2_approx((p.lse_part[s * span + prow] - m) * kLog2e);
-    l += w;
-    const float* src = p.o_part + (s * span + prow) * D + lane * E;
-    if constexpr (E == 4) {
-      const float4 x = *reinterpret_cast<const float4*>(src);
-      acc[0] = fmaf(w, x.x, acc[0]);
-      acc[1] = fmaf(w, x.y, acc[1]);
-      acc[2] = fmaf(w, x.z, acc[2]);
-      acc[3] = fmaf(w, x.w, acc[3]);
-    } else {
-      const float2 x = *reinterpret_cast<const float2*>(src);
-      acc[0] = fmaf(w, x.x, acc[0]);
-      acc[1] = fmaf(w, x.y, acc[1]);
+  if (m > -INFINITY) {
+    for (int s = 0; s < p.num_splits; ++s) {
+      const float w = ex2_approx((p.lse_part[s * span + prow] - m) * kLog2e);
+      l += w;
+      const float* src = p.o_part + (s * span + prow) * D + lane * E;
+      if constexpr (E == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        acc[0] = fmaf(w, x.x, acc[0]);
+        acc[1] = fmaf(w, x.y, acc[1]);
+        acc[2] = fmaf(w, x.z, acc[2]);
+        acc[3] = fmaf(w, x.w, acc[3]);
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        acc[0] = fmaf(w, x.x, acc[0]);
+        acc[1] = fmaf(w, x.y, acc[1]);
+      }
     }
   }
-  const float inv = 1.0f / l;
+  const float inv = l > 0.f ? 1.0f / l : 0.f;
   uint32_t pk[E / 2];
 #pragma unroll
   for (int e = 0; e < E / 2; ++e) pk[e] = pack2<BF16>(acc[2 * e] * inv, acc[2 * e + 1] * inv);
@@ -671,50 +700,7 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const __grid_constant__ F
     *reinterpret_cast<uint2*>(out) = make_uint2(pk[0], pk[1]);
   else
     *reinterpret_cast<uint32_t*>(out) = pk[0];
-  if (lane == 0) p.lse[row] = m + lg2_approx(l) * kLn2;
-}
-
-// The same merge for rows that may have no key in any part (every part's
-// LSE = -inf): those rows get O = 0 and LSE = -inf.
-template <int D, bool BF16>
-__global__ void __launch_bounds__(256) fa_merge_guarded_kernel(const __grid_constant__ FwdParams p) {
-  constexpr int E = D / 32;
-  const long long rows = static_cast<long long>(p.B) * p.H * p.N;
-  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  float m = -INFINITY;
-  for (int s = 0; s < p.num_splits; ++s) m = fmaxf(m, p.lse_part[s * rows + row]);
-  float acc[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  float l = 0.f;
-  if (m > -INFINITY) {
-    for (int s = 0; s < p.num_splits; ++s) {
-      const float w = ex2_approx((p.lse_part[s * rows + row] - m) * kLog2e);
-      l += w;
-      const float* src = p.o_part + (s * rows + row) * D + lane * E;
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = fmaf(w, src[e], acc[e]);
-    }
-  }
-  const float inv = l > 0.f ? 1.0f / l : 0.f;
-  uint32_t pk[E / 2];
-#pragma unroll
-  for (int e = 0; e < E / 2; ++e) pk[e] = pack2<BF16>(acc[2 * e] * inv, acc[2 * e + 1] * inv);
-  uint32_t* out = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.o) + row * D + lane * E);
-#pragma unroll
-  for (int e = 0; e < E / 2; ++e) out[e] = pk[e];
   if (lane == 0) p.lse[row] = m > -INFINITY ? m + lg2_approx(l) * kLn2 : -INFINITY;
-}
-
-template <int D, bool BF16>
-cudaError_t launch_merge_guarded_t(const FwdParams& p, cudaStream_t stream) {
-  const long long rows = static_cast<long long>(p.B) * p.H * p.N;
-  const long long blocks = (rows * 32 + 255) / 256;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  fa_merge_guarded_kernel<D, BF16><<<dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream>>>(p);
-  return cudaGetLastError();
 }
 
 template <int D, bool BF16>
@@ -735,15 +721,8 @@ cudaError_t launch_merge(const FwdParams& p, bool bf16, cudaStream_t stream) {
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_merge_guarded(const FwdParams& p, bool bf16, cudaStream_t stream) {
-  if (p.d == 128)
-    return bf16 ? launch_merge_guarded_t<128, true>(p, stream) : launch_merge_guarded_t<128, false>(p, stream);
-  if (p.d == 64) return bf16 ? launch_merge_guarded_t<64, true>(p, stream) : launch_merge_guarded_t<64, false>(p, stream);
-  return cudaErrorInvalidValue;
-}
-
 cudaError_t launch_fwd_f16(const FwdParams& p, bool bf16, cudaStream_t stream) {
-  if (p.d == 128) return bf16 ? launch<128, true>(p, stream) : launch<128, false>(p, stream);
+  if (p.d == 128) return launch_fwd_d128(p, bf16, stream);
   if (p.d == 64) return bf16 ? launch<64, true>(p, stream) : launch<64, false>(p, stream);
   return cudaErrorInvalidValue;
 }

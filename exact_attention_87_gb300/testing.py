@@ -13,17 +13,29 @@ from ._build import TESTING_LIB_PATH, build
 
 TRACE_CTAS, TRACE_EVENTS, TRACE_TILES = 8, 32, 64
 EVENTS = ["S0_issued", "S1_issued", "PV0_issued", "PV1_issued", "sm0_sfull", "sm0_parrive", "sm1_sfull",
-          "sm1_parrive", "K_issued", "V_issued", "mma_kfull", "mma_vfull", "cta"]
-KV_TILE = 128  # keys per K/V tile of the fp16/bf16 kernel (stats_trace has ceil(N / KV_TILE) entries per row)
+          "sm1_parrive", "K_issued", "V_issued", "mma_kfull", "mma_vfull", "cta",
+          "sm0_loaded", "sm0_voted", "sm0_pdone", "sm0_stored", "sm1_loaded", "sm1_voted", "sm1_pdone", "sm1_stored"]
+def kv_tile(d: int) -> int:
+    """Keys per K/V tile of the 16-bit forward kernel for head dimension d
+    (stats_trace has ceil(N / kv_tile(d)) entries per row): 128 for d = 64,
+    64 for d = 128 and 256."""
+    return 128 if d == 64 else 64
 _lib = None
 
 
 def lib():
+    """The testing library, with the product entry points bound as in the
+    package plus the testing ones."""
     global _lib
     if _lib is None:
         build(testing=True)
-        L = ctypes.CDLL(TESTING_LIB_PATH)
+        from . import lib as _product_binding
+        L = _product_binding(TESTING_LIB_PATH)
         vp, i, f, ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong
+        L.fa_fwd_debug.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, f, vp]
+        L.fa_fwd_debug.restype = i
+        L.fa_testing_set_dry_run.argtypes = [i]
+        L.fa_testing_set_dry_run.restype = None
         L.fa_fwd_testing.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, i, vp, vp, ll]
         L.fa_fwd_testing.restype = i
         u64 = ctypes.c_ulonglong
@@ -48,7 +60,7 @@ def attention(q, k, v, scale=None, inject=0, stats=False, timeline=False, wait_l
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     out = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    nkv = (N + KV_TILE - 1) // KV_TILE
+    nkv = (N + kv_tile(d) - 1) // kv_tile(d)
     st = torch.zeros((B, H, N, nkv, 2), dtype=torch.float32, device=q.device) if stats else None
     tl = torch.zeros((TRACE_CTAS, TRACE_EVENTS, TRACE_TILES), dtype=torch.int64, device=q.device) if timeline else None
     stream = torch.cuda.current_stream(q.device).cuda_stream
@@ -59,6 +71,43 @@ def attention(q, k, v, scale=None, inject=0, stats=False, timeline=False, wait_l
     if check and rc != FA_OK:
         raise FAError(rc, "fa_fwd_testing")
     return out, lse, st, tl
+
+
+def attention_debug(q, k, v, scale=None, out_f32=False, tau=-1.0, stats=False, check=True):
+    """The forward pass through fa_fwd_debug: with out_f32 the output is the
+    fp32 O before rounding to the input type; tau is the lazy-rescale
+    threshold in log2 units (< 0: the built-in 8; 0: rescale whenever a row's
+    max grows). Returns (O, LSE, stats_trace or None)."""
+    import torch
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if out_f32:
+        out16, out32 = None, torch.empty((B, H, N, d), dtype=torch.float32, device=q.device)
+    else:
+        out16, out32 = torch.empty_like(q), None
+    tile = kv_tile(d)
+    st = torch.zeros((B, H, N, (N + tile - 1) // tile, 2), dtype=torch.float32, device=q.device) if stats else None
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = lib().fa_fwd_debug(q.data_ptr(), k.data_ptr(), v.data_ptr(), out16.data_ptr() if out16 is not None else None,
+                            lse.data_ptr(), B, H, N, d, float(scale), _dtype_code(q), stream,
+                            out32.data_ptr() if out32 is not None else None, float(tau),
+                            st.data_ptr() if st is not None else None)
+    if check and rc != FA_OK:
+        raise FAError(rc, "fa_fwd_debug")
+    return (out32 if out_f32 else out16), lse, st
+
+
+class dry_run:
+    """Context: the testing library's entry points stop after their argument
+    and device checks and enqueue nothing."""
+
+    def __enter__(self):
+        lib().fa_testing_set_dry_run(1)
+        return lib()
+
+    def __exit__(self, *exc):
+        lib().fa_testing_set_dry_run(0)
 
 
 BWD_EVENTS = ["dV_issued", "dP_issued", "S_next_issued", "dK_issued", "dQ_issued", "sm_S_ready", "sm_P_arrived",

@@ -130,6 +130,24 @@ int fa_fwd_splitkv(const void *Q, const void *K, const void *V, void *O, float *
                    int B, int H, int N, int d, float scale, int dtype,
                    int num_splits, void *workspace, unsigned long long workspace_bytes, void *stream);
 
+/*
+ * Masked split-KV forward pass: fa_fwd_ex's masks with fa_fwd_splitkv's key
+ * ranges. This is the padded variable-length batch of the Triton page
+ * ("FlashAttention + Triton", section 5.1), typically few heads with long
+ * sequences, where splitting the keys gives the SMs enough work units. Each
+ * (unit, key range) sees the keys of its range that the masks leave it; a
+ * range it sees none of contributes O = 0, LSE = -inf and the merge ignores
+ * it; a row that no range sees (seqlens_k[b] == 0) gets O = 0, LSE = -inf.
+ *   causal, seqlens_k: as fa_fwd_ex (seqlens_k: NULL or a device int32 [B]).
+ *   num_splits, workspace, workspace_bytes: as fa_fwd_splitkv; the plan and
+ *              the workspace size do not depend on the masks
+ *              (fa_fwd_splitkv_workspace_size applies).
+ * Errors: those of fa_fwd_ex and fa_fwd_splitkv.
+ */
+int fa_fwd_splitkv_ex(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                      int B, int H, int N, int d, float scale, int dtype, int causal, const int *seqlens_k,
+                      int num_splits, void *workspace, unsigned long long workspace_bytes, void *stream);
+
 /* The effective split count fa_fwd_splitkv uses for num_splits = 0 on the
  * current device (>= 1: key ranges of each split unit after clamping to whole
  * 128-key tiles; 1 = unsplit), or a negative fa_status on error. Under the

@@ -46,6 +46,36 @@ int fa_bwd_testing(const void *Q, const void *K, const void *V, const void *O, c
                    void *workspace, unsigned long long workspace_bytes, void *stream,
                    int inject, unsigned long long *timeline, long long wait_limit_cycles);
 
+/*
+ * fa_fwd with the two test-only controls the parity gates need. Arguments up
+ * to `stream` are those of fa_fwd (fp16/bf16 only for the first control).
+ *  O_f32:  NULL, or a device fp32 array [B,H,N,d] (16-byte aligned) that
+ *          receives O normalised by l but NOT rounded to the input type; O is
+ *          then not written and may be NULL. This isolates the fp32
+ *          accumulation (S, P.V, l) from the rounding of the stored output,
+ *          which for bf16 outputs of |O| ~ 4 alone exceeds 1e-2 (the accuracy
+ *          threshold of the dataflow page, section 4.1). d = 64 or 128 only;
+ *          otherwise FA_ERR_UNSUPPORTED.
+ *  rescale_threshold_log2: the lazy-rescale threshold in log2 units; < 0
+ *          takes the built-in 8; 0 rescales O whenever a row's max grows
+ *          (the dataflow page, section 2.3). Must lie in [0, 64] otherwise
+ *          (FA_ERR_SCALE). Ignored by fp32 inputs, whose rescale is eager.
+ *  stats_trace: as in fa_fwd_testing (NULL for none).
+ * Errors: those of fa_fwd, returned before any launch.
+ */
+int fa_fwd_debug(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                 int B, int H, int N, int d, float scale, int dtype, void *stream,
+                 float *O_f32, float rescale_threshold_log2, float *stats_trace);
+
+/*
+ * on != 0: every entry point of this library returns FA_OK after its argument
+ * and device checks, before anything is enqueued (0 restores normal calls).
+ * Lets argument-error tests pass placeholder addresses safely: a validation
+ * check that regressed shows up as FA_OK instead of the expected error code,
+ * never as a kernel launched on memory that does not exist.
+ */
+void fa_testing_set_dry_run(int on);
+
 /* "Where" code of the first timeout recorded in the status word (0 = none;
  * not cleared by this call). */
 unsigned int fa_testing_last_timeout_where(void);

@@ -1,5 +1,11 @@
 """The C ABI: the library builds, loads and exports every entry point that
-include/fa.h declares; argument errors come back as codes before any launch."""
+include/fa.h declares; argument errors come back as codes before any launch.
+
+The argument-error tests pass placeholder addresses. They call the testing
+build of the library (same host code, compiled with -DFA_TESTING) with its
+dry-run switch on, under which a call that gets past every check returns
+FA_OK without enqueuing anything: a check that regressed shows up as a wrong
+status code, never as a kernel launched on memory that does not exist."""
 import os
 import re
 
@@ -62,7 +68,17 @@ def test_strerror_and_version(L):
     assert fa.fa_strerror(12345) == "unknown status"
 
 
-A = 1 << 20  # a 16-byte aligned fake address: validation fails before it is used
+A = 1 << 20  # a 16-byte aligned placeholder address (dry runs only: never dereferenced)
+
+
+@pytest.fixture(scope="module")
+def D():
+    """The testing library with dry runs on (same entry points and argument types)."""
+    from exact_attention_87_gb300 import testing
+    lib = testing.lib()
+    lib.fa_testing_set_dry_run(1)
+    yield lib
+    lib.fa_testing_set_dry_run(0)
 
 
 @pytest.mark.parametrize("args,code", [
@@ -84,8 +100,8 @@ A = 1 << 20  # a 16-byte aligned fake address: validation fails before it is use
     ((A, A, A, A, A + 2, 1, 1, 64, 64, 0.125, fa.FA_F32), fa.FA_ERR_ALIGN),
     ((A, A, A, A, A, 65536, 65536, 1 << 20, 128, 0.1, fa.FA_F16), fa.FA_ERR_SHAPE),
 ])
-def test_argument_errors_return_before_launch(L, args, code):
-    assert fa.fa_fwd(*args, None) == code
+def test_argument_errors_return_before_launch(D, args, code):
+    assert D.fa_fwd(*args, None) == code
 
 
 def test_missing_library_raises(tmp_path):
@@ -93,7 +109,7 @@ def test_missing_library_raises(tmp_path):
         fa.lib(str(tmp_path / "nope.so"))
 
 
-def test_splitkv_workspace_size_formula(L):
+def test_splitkv_workspace_size_formula(L, D):
     assert fa.fa_fwd_splitkv_workspace_size(1, 8, 16384, 128, 1) == 0
     rows = 1 * 8 * 16384 * 3
     o_bytes = (rows * 128 * 4 + 255) // 256 * 256
@@ -101,8 +117,15 @@ def test_splitkv_workspace_size_formula(L):
     # requests beyond the number of 128-key tiles are clamped: N = 300 has 3 tiles
     assert fa.fa_fwd_splitkv_workspace_size(1, 1, 300, 64, 9) == fa.fa_fwd_splitkv_workspace_size(1, 1, 300, 64, 3)
     assert fa.fa_fwd_splitkv_workspace_size(0, 1, 300, 64, 2) == 0
-    assert fa.fa_fwd_splitkv(0, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, 2, A, 1 << 20, None) == fa.FA_ERR_NULL
-    assert fa.fa_fwd_splitkv(A, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, -1, A, 1 << 20, None) == fa.FA_ERR_SHAPE
+    assert D.fa_fwd_splitkv(0, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, 2, A, 1 << 20, None) == fa.FA_ERR_NULL
+    assert D.fa_fwd_splitkv(A, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, -1, A, 1 << 20, None) == fa.FA_ERR_SHAPE
+    # the allocation-free variant checks every argument before it looks at its scratch
+    big = (1, 64, 16384, 128, 0.088, fa.FA_BF16, 4)
+    assert D.fa_fwd_splitkv_noalloc(0, A, A, A, A, *big, None) == fa.FA_ERR_NULL
+    assert D.fa_fwd_splitkv_noalloc(A, A, A, A + 2, A, *big, None) == fa.FA_ERR_ALIGN
+    assert D.fa_fwd_splitkv_noalloc(A, A, A, A, A, 1, 64, 16384, 96, 0.088, fa.FA_BF16, 4, None) == \
+        fa.FA_ERR_HEADDIM
+    assert D.fa_fwd_splitkv_noalloc(A, A, A, A, A, 1, 64, 16384, 128, -1.0, fa.FA_BF16, 4, None) == fa.FA_ERR_SCALE
 
 
 def test_splitkv_launch_count_argument_errors(L):
@@ -112,19 +135,19 @@ def test_splitkv_launch_count_argument_errors(L):
     assert fa.fa_fwd_splitkv_launches(1, 1, 64, 256, 0) == 1  # the d = 256 kernel runs unsplit
 
 
-def test_masked_entry_point_argument_errors(L):
-    assert fa.fa_fwd_ex(A, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, 2, None, None) == fa.FA_ERR_SHAPE
-    assert fa.fa_fwd_ex(0, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, 1, None, None) == fa.FA_ERR_NULL
+def test_masked_entry_point_argument_errors(D):
+    assert D.fa_fwd_ex(A, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, 2, None, None) == fa.FA_ERR_SHAPE
+    assert D.fa_fwd_ex(0, A, A, A, A, 1, 1, 64, 64, 0.125, fa.FA_F16, 1, None, None) == fa.FA_ERR_NULL
     ws = fa.fa_bwd_workspace_size(1, 1, 64, 64)
     args = [A] * 6 + [A] * 3 + [1, 1, 64, 64, 0.125, fa.FA_F16]
-    assert fa.fa_bwd_ex(*args, 2, None, 1 << 24, ws, None) == fa.FA_ERR_SHAPE
-    assert fa.fa_bwd_ex(*args, -1, None, 1 << 24, ws, None) == fa.FA_ERR_SHAPE
-    assert fa.fa_bwd_ex(*([0] + args[1:]), 1, None, 1 << 24, ws, None) == fa.FA_ERR_NULL
-    assert fa.fa_bwd_ex(*args, 1, None, 0, ws, None) == fa.FA_ERR_WORKSPACE
-    assert fa.fa_bwd_ex(*(args[:12] + [256, 0.125, fa.FA_F16]), 1, None, 1 << 24, ws, None) == fa.FA_ERR_HEADDIM
+    assert D.fa_bwd_ex(*args, 2, None, 1 << 24, ws, None) == fa.FA_ERR_SHAPE
+    assert D.fa_bwd_ex(*args, -1, None, 1 << 24, ws, None) == fa.FA_ERR_SHAPE
+    assert D.fa_bwd_ex(*([0] + args[1:]), 1, None, 1 << 24, ws, None) == fa.FA_ERR_NULL
+    assert D.fa_bwd_ex(*args, 1, None, 0, ws, None) == fa.FA_ERR_WORKSPACE
+    assert D.fa_bwd_ex(*(args[:12] + [256, 0.125, fa.FA_F16]), 1, None, 1 << 24, ws, None) == fa.FA_ERR_HEADDIM
 
 
-def test_partial_and_merge_argument_errors(L):
+def test_partial_and_merge_argument_errors(D):
     #                 Q  K  V  Op Lp B  H  Nq  Nk  d    scale  dtype
     ok = [A, A, A, A, A, 1, 1, 64, 64, 64, 0.125, fa.FA_BF16, None]
     def part(**kw):
@@ -132,7 +155,7 @@ def test_partial_and_merge_argument_errors(L):
         for i, name in enumerate(["Q", "K", "V", "Op", "Lp", "B", "H", "Nq", "Nk", "d", "scale", "dtype"]):
             if name in kw:
                 a[i] = kw[name]
-        return fa.fa_fwd_partial(*a)
+        return D.fa_fwd_partial(*a)
     assert part(Q=0) == fa.FA_ERR_NULL
     assert part(Lp=0) == fa.FA_ERR_NULL
     assert part(dtype=fa.FA_F32) == fa.FA_ERR_UNSUPPORTED
@@ -149,7 +172,7 @@ def test_partial_and_merge_argument_errors(L):
         for i, name in enumerate(["Op", "Lp", "P", "O", "L", "B", "H", "N", "d", "dtype"]):
             if name in kw:
                 a[i] = kw[name]
-        return fa.fa_merge(*a)
+        return D.fa_merge(*a)
     assert merge(Op=0) == fa.FA_ERR_NULL
     assert merge(P=0) == fa.FA_ERR_SHAPE
     assert merge(dtype=fa.FA_F32) == fa.FA_ERR_UNSUPPORTED
@@ -168,7 +191,7 @@ def test_backward_workspace_size_formula(L):
     assert fa.fa_bwd_workspace_size(0, 1, 64, 64) == 0
 
 
-W = 1 << 24  # fake workspace address, 256-byte aligned
+W = 1 << 24  # placeholder workspace address, 256-byte aligned (dry runs only)
 
 
 @pytest.mark.parametrize("change,code", [
@@ -186,11 +209,11 @@ W = 1 << 24  # fake workspace address, 256-byte aligned
     ({"ws": W + 64}, fa.FA_ERR_WORKSPACE),
     ({"ws_bytes": 1024}, fa.FA_ERR_WORKSPACE),
 ])
-def test_backward_argument_errors_return_before_launch(L, change, code):
+def test_backward_argument_errors_return_before_launch(D, change, code):
     a = dict(Q=A, K=A, V=A, O=A, dO=A, LSE=A, dQ=A, dK=A, dV=A, B=1, H=2, N=200, d=64, scale=0.125,
              dtype=fa.FA_BF16, ws=W, ws_bytes=1 << 30)
     a.update(change)
-    assert fa.fa_bwd(a["Q"], a["K"], a["V"], a["O"], a["dO"], a["LSE"], a["dQ"], a["dK"], a["dV"], a["B"], a["H"],
+    assert D.fa_bwd(a["Q"], a["K"], a["V"], a["O"], a["dO"], a["LSE"], a["dQ"], a["dK"], a["dV"], a["B"], a["H"],
                      a["N"], a["d"], a["scale"], a["dtype"], a["ws"], a["ws_bytes"], None) == code
 
 

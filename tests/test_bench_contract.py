@@ -49,3 +49,17 @@ def test_gpu_arm_line(args):
     dist = d["ms_per_step_dist"]
     assert dist["n"] == 4 and dist["p10"] <= dist["median"] <= dist["p90"]
     assert d["config"]["l2"]
+
+
+@pytest.mark.gpu
+def test_gpu_arm_line_parity_and_sustained_leg():
+    """The forward line carries the parity figures of the timed output on the
+    heads the CPU baseline computed, and the seconds-long sustained leg."""
+    d = run_bench("--workload", "b8h12n2048d128_f16", "--steps", "4", "--warmup", "3", "--no-e2e",
+                  "--cpu-seconds", "2", "--sustained-seconds", "0.5")
+    p = d["parity"]
+    assert p["ok"] and p["heads"] >= 1 and p["cos"] >= 0.999 and p["max_abs"] <= 1e-2
+    s = d["sustained"]
+    assert s["steps"] >= 10 and s["value"] > 0 and abs(s["value"] / s["peak"] - s["frac"]) < 1e-3
+    assert {"sm_mhz", "reasons"} <= set(s["clocks"])
+    assert 0 < d["pct_of_measured_peak"] and 0 < d["pct_of_datasheet_peak"] < d["pct_of_measured_peak"]

@@ -12,16 +12,16 @@ from workloads import make_qkv
 pytestmark = pytest.mark.gpu
 
 
-def run(q, k, v, causal, klen):
+def run(q, k, v, causal, klen, num_splits=1):
     kl = torch.tensor(klen, dtype=torch.int32, device="cuda") if klen is not None else None
-    o, lse = fa.attention(q.cuda(), k.cuda(), v.cuda(), causal=causal, seqlens_k=kl)
+    o, lse = fa.attention(q.cuda(), k.cuda(), v.cuda(), causal=causal, seqlens_k=kl, num_splits=num_splits)
     torch.cuda.synchronize()
     assert fa.fa_get_device_status() == fa.FA_OK
     return o.cpu().double().numpy(), lse.cpu().double().numpy()
 
 
-def check(q, k, v, dtype, causal=False, klen=None):
-    o, lse = run(q, k, v, causal, klen)
+def check(q, k, v, dtype, causal=False, klen=None, num_splits=1):
+    o, lse = run(q, k, v, causal, klen, num_splits)
     o_ref, lse_ref = oracle.attn_masked(q, k, v, causal=causal, klen=klen)
     empty = np.isneginf(lse_ref)
     assert np.all(o[empty] == 0) and np.all(np.isneginf(lse[empty]))
@@ -70,3 +70,30 @@ def test_padded_keys_need_not_be_finite():
     o, lse = run(q, k2, v2, False, klen)
     res = compare(o, lse, o_ref, lse_ref, "bf16")
     assert res["ok"], res
+
+
+@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (64, "f16")])
+@pytest.mark.parametrize("splits", [2, 3, 0])
+@pytest.mark.parametrize("causal,klen", [(True, None), (False, [700, 1, 129, 256, 0]),
+                                         (True, [600, 300, 77, 0, 700])], ids=["causal", "lengths", "both"])
+def test_masks_with_split_kv(d, dtype, splits, causal, klen):
+    """fa_fwd_splitkv_ex: key ranges that a row's masks leave empty contribute
+    nothing, rows with no key anywhere get O = 0 and LSE = -inf."""
+    B, H, N = 5, 2, 700
+    q, k, v = make_qkv(B, H, N, d, dtype, sigma_qk=2.0, seed=44, wid=13400 + d + splits)
+    check(q, k, v, dtype, causal=causal, klen=klen, num_splits=splits)
+
+
+@pytest.mark.parametrize("splits", [0, 3])
+@pytest.mark.parametrize("causal", [False, True])
+def test_padded_long_sequence_batch_split(causal, splits):
+    """The padded variable-length batch with few heads and long sequences
+    (the Triton page, section 5.1): B=4 H=1 N=4096 with key lengths 4096,
+    3000, 0 and 2500 (64 work units on 152 SMs, which the automatic plan
+    splits), split automatically and three ways."""
+    B, H, N, d = 4, 1, 4096, 128
+    klen = [4096, 3000, 0, 2500]
+    q, k, v = make_qkv(B, H, N, d, "bf16", sigma_qk=1.5, seed=45, wid=13500 + causal)
+    if splits == 0:
+        assert fa.fa_fwd_splitkv_num_splits(B, H, N, d) > 1
+    check(q, k, v, "bf16", causal=causal, klen=klen, num_splits=splits)

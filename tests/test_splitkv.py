@@ -35,19 +35,18 @@ def test_splitkv_parity(B, H, N, d, dtype, sig, splits):
     assert res["ok"], res
 
 
-def test_splitkv_long_sequence_workload():
+def test_splitkv_long_sequence_workload_uniform_split_whole():
+    """B=1 H=8 N=16384 with every unit split four ways (two launches: the
+    partial pass and the merge), every output against the oracle."""
+    from whole_parity import compare_whole, oracle_full
     w = WORKLOADS["b1h8n16384d128_bf16"]
     q, k, v = make_inputs(w)
-    splits = fa.fa_fwd_splitkv_num_splits(w.B, w.H, w.N, w.d)
-    assert splits >= 1
-    o, lse = fa.attention(q.cuda(), k.cuda(), v.cuda(), num_splits=0)
+    assert fa.fa_fwd_splitkv_launches(w.B, w.H, w.N, w.d, 4) == 2
+    o, lse = fa.attention(q.cuda(), k.cuda(), v.cuda(), num_splits=4)
     torch.cuda.synchronize()
     assert fa.fa_get_device_status() == fa.FA_OK
-    rows = sample_rows(w.B, w.H, w.N, 64, seed=5)
-    o_ref, lse_ref = oracle.attn_rows(q, k, v, rows)
-    oc, lc = o.cpu().double().numpy(), lse.cpu().double().numpy()
-    res = compare(np.stack([oc[b, h, i] for b, h, i in rows]), np.array([lc[b, h, i] for b, h, i in rows]),
-                  o_ref, lse_ref, w.dtype)
+    o_ref, lse_ref, _ = oracle_full(w, q, k, v)
+    res = compare_whole(o, lse, o_ref, lse_ref, "bf16", label=f"{w.name} uniform 4-way split")
     assert res["ok"], res
 
 

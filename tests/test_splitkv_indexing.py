@@ -25,14 +25,23 @@ def L():
     return fa.lib()
 
 
-def _written(B, H, N, first, splits):
+def _qblock(u, nqb, causal, num_splits, qunit_count):
+    """The Q block of work unit u, restated from the kernels: under the causal
+    mask a launch over every unit unsplit takes the heavy (late) blocks
+    first; every split launch keeps the natural order."""
+    heavy_first = causal and num_splits == 1 and qunit_count == 0
+    return nqb - 1 - u % nqb if heavy_first else u % nqb
+
+
+def _written(B, H, N, first, splits, causal=False):
     nqb = -(-N // 256)
     units = B * H * nqb
     row0 = (first // nqb) * N + (first % nqb) * 256
     span = B * H * N - row0
     idx = []
     for u in range(first, units):
-        bh, qb = divmod(u, nqb)
+        bh = u // nqb
+        qb = _qblock(u, nqb, causal, splits, units - first)
         rows = np.arange(qb * 256, min(qb * 256 + 256, N))
         for s in range(splits):
             idx.append(s * span + (bh * N + rows - row0))
@@ -44,13 +53,17 @@ def _written(B, H, N, first, splits):
     (1, 2, 20000, 128, 152), (3, 5, 1000, 64, 7), (2, 3, 4097, 64, 13), (1, 1, 300, 64, 1),
 ])
 @pytest.mark.parametrize("num_splits", [0, 2, 5])
-def test_partial_rows_tile_the_planned_workspace(L, B, H, N, d, num_sms, num_splits):
+@pytest.mark.parametrize("causal", [False, True])
+def test_partial_rows_tile_the_planned_workspace(L, B, H, N, d, num_sms, num_splits, causal):
+    """Also under the causal mask (fa_fwd_splitkv_ex), whose plan is the
+    unmasked one: the split launches keep the natural unit order, so the tail
+    plan's units still hold exactly the rows from row0 on."""
     rc, p = fa.fa_fwd_splitkv_plan(B, H, N, d, num_splits, num_sms)
     assert rc == fa.FA_OK
     if p["splits"] == 1:
         assert p["workspace_bytes"] == 0
         return
-    idx, row0, span = _written(B, H, N, p["first_split_unit"], p["splits"])
+    idx, row0, span = _written(B, H, N, p["first_split_unit"], p["splits"], causal)
     # every partial row exactly once, no gap, no overlap
     assert len(idx) == p["splits"] * span
     assert np.array_equal(np.sort(idx), np.arange(p["splits"] * span))
@@ -64,3 +77,20 @@ def test_partial_rows_tile_the_planned_workspace(L, B, H, N, d, num_sms, num_spl
     nqb = -(-N // 256)
     first = p["first_split_unit"]
     assert row0 == (first // nqb) * N + (first % nqb) * 256 and span == B * H * N - row0
+
+
+def test_heavy_first_order_would_break_the_tail_plan():
+    """Planted mistake: the causal heavy-first order applied to the split
+    tail launch too. Its units would then write rows before row0, outside
+    the partial buffers (negative partial rows)."""
+    B, H, N, num_sms = 1, 8, 16384, 152
+    rc, p = fa.fa_fwd_splitkv_plan(B, H, N, 128, 0, num_sms)
+    assert rc == fa.FA_OK and 0 < p["first_split_unit"]
+    nqb = -(-N // 256)
+    first = p["first_split_unit"]
+    row0 = (first // nqb) * N + (first % nqb) * 256
+    bad = []
+    for u in range(first, B * H * nqb):
+        bh, qb = u // nqb, nqb - 1 - u % nqb   # reversed
+        bad.append(bh * N + qb * 256 - row0)
+    assert min(bad) < 0

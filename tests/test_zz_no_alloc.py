@@ -61,13 +61,25 @@ def test_noalloc_matches_workspace_entry_point_twice(B, H, N, d, dtype, splits):
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
+    """A shape whose split-KV partials exceed the built-in scratch is refused
+    with FA_ERR_SCRATCH_LIMIT, on real buffers of that shape (4 x 256 MiB), so
+    that a regression of the size check could only compute, never touch
+    memory that does not exist; a NULL pointer with the same shape is refused
+    with FA_ERR_NULL, before the scratch is looked at."""
     fa.build()
     B, H, N, d, splits = 1, 64, 16384, 128, 4
     assert fa.fa_fwd_splitkv_workspace_size(B, H, N, d, splits) > (32 << 20)
-    a = 1 << 20  # never dereferenced: the size check comes first
-    rc = fa.fa_fwd_splitkv_noalloc(a, a, a, a, a, B, H, N, d, d ** -0.5, fa.FA_BF16, splits, None)
+    q = torch.zeros((B, H, N, d), dtype=torch.bfloat16, device="cuda")
+    k, v, o = torch.zeros_like(q), torch.zeros_like(q), torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr())
+    rc = fa.fa_fwd_splitkv_noalloc(*ptrs, B, H, N, d, d ** -0.5, fa.FA_BF16, splits, None)
     assert rc == fa.FA_ERR_SCRATCH_LIMIT
     assert "scratch" in fa.fa_strerror(rc)
+    rc = fa.fa_fwd_splitkv_noalloc(0, *ptrs[1:], B, H, N, d, d ** -0.5, fa.FA_BF16, splits, None)
+    assert rc == fa.FA_ERR_NULL
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
 
 
 def test_noalloc_runs_the_automatic_plan_on_the_long_sequence_workload():
