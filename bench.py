@@ -37,7 +37,6 @@ COMMON_SOURCES = ["exact_attention_87_gb300/csrc/sm103_ptx.cuh", "exact_attentio
 # The source files of the kernel each timed path spends its time in.
 KERNEL_SOURCES = {
     "fwd": ["exact_attention_87_gb300/csrc/fa_fwd_f16.cu"] + COMMON_SOURCES,
-    "fwd_d128": ["exact_attention_87_gb300/csrc/fa_fwd_d128.cu"] + COMMON_SOURCES,
     "fwd_d256": ["exact_attention_87_gb300/csrc/fa_fwd_d256.cu"] + COMMON_SOURCES,
     "bwd": ["exact_attention_87_gb300/csrc/fa_bwd_f16.cu"] + COMMON_SOURCES,
 }
@@ -544,7 +543,7 @@ def main():
 
     peak, peak_src, _ = peaks()
     achieved = flops / (ms * 1e-3) / 1e12
-    kind = "fwd_d256" if w.d == 256 else "fwd_d128" if w.d == 128 else "fwd"
+    kind = "fwd_d256" if w.d == 256 else "fwd"
     traffic = recorded_traffic(w.name, kind) if not args.causal and n_launch == 1 else None
     line = {
         "metric": "attention fwd TFLOP/s (4*B*H*N^2*d) and % of GB300 dense BF16 tensor peak",
@@ -590,8 +589,6 @@ def fwd_kernel_name(w) -> str:
         return f"fa_fwd_f32_kernel<{w.d}>"
     if w.d == 256:
         return f"fa_fwd_d256_kernel<{t}>"
-    if w.d == 128:
-        return f"fa_fwd_d128_kernel<{t}>"
     return f"fa_fwd_f16_kernel<{w.d},{t}>"
 
 

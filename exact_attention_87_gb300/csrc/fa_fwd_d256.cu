@@ -213,12 +213,16 @@ __device__ __forceinline__ void softmax256(const FwdParams& p, uint32_t base, ui
     // (an arrival here instead of a commit behind the S MMAs, which would
     // keep the tensor pipe idle while it is processed).
     if (lane == 0) mbar_arrive(bar256(base, C::B_KE + j % C::STAGES));
+    // S in registers, with each half's row max from the same load (the TMEM
+    // load with a max reduction of sm_103a).
     uint32_t sraw[2][32];
-    tmem_ld32(t_s, sraw[0]);
-    tmem_ld32(t_s + 32, sraw[1]);
+    float mx_lo, mx_hi;
+    tmem_ld32_max(t_s, sraw[0], mx_lo);
+    tmem_ld32_max(t_s + 32, sraw[1], mx_hi);
     tmem_ld_wait();
     reg_fence(sraw[0]);
     reg_fence(sraw[1]);
+    asm volatile("" : "+f"(mx_lo), "+f"(mx_hi));  // valid only after the wait, like sraw
     float s[C::BN];
 #pragma unroll
     for (int u = 0; u < 32; ++u) {
@@ -226,20 +230,22 @@ __device__ __forceinline__ void softmax256(const FwdParams& p, uint32_t base, ui
       s[32 + u] = __uint_as_float(sraw[1][u]);
     }
     const int valid = row_end - j * C::BN;  // keys of this tile this row may see
+    float mx = fmaxf(mx_lo, mx_hi);
     if (valid < C::BN) {
+      // Masked keys become -inf and the max is taken over the rest (the
+      // loads' max includes them).
 #pragma unroll
       for (int u = 0; u < C::BN; ++u)
         if (u >= valid) s[u] = -INFINITY;
+      float mxa[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mxa[i] = fmaxf(s[i], s[i + 8]);
+#pragma unroll
+      for (int u = 16; u < C::BN; u += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mxa[i] = fmax3(mxa[i], s[u + i], s[u + 8 + i]);
+      mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])), fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
     }
-    float mxa[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) mxa[i] = fmaxf(s[i], s[i + 8]);
-#pragma unroll
-    for (int u = 16; u < C::BN; u += 16)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mxa[i] = fmax3(mxa[i], s[u + i], s[u + 8 + i]);
-    const float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
-                           fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
     const float m_new = fmaxf(m_ref, mx * c);
     bool rescale_o = false;
     float alpha = 1.f;

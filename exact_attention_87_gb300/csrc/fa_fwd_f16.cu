@@ -33,9 +33,12 @@
 // One MMA warp per sub-tile drives the chain S_i -> softmax_i -> P_i V -> S_i;
 // the two warps pass a turn so that their MMA blocks alternate (ping-pong) and
 // each runs inside the other chain's softmax.
-// The rescale of O is lazy: the reference max only moves when the tile max
-// exceeds it by more than the threshold (15 in log2 units), so P <= 2^15 and
-// rescales are rare.
+// Each tile's row max comes with the TMEM load of its scores (sm_103a's
+// tcgen05.ld with a max reduction), so no max tree over the scores stands
+// between the load and the exponentials; tiles with masked keys take the max
+// in registers after masking. The rescale of O is lazy: the reference max
+// only moves when the tile max exceeds it by more than the threshold (15 in
+// log2 units), so P <= 2^15 and rescales are rare.
 // The epilogue divides by l, rounds to the input type, stages the tile in the
 // (now unused) Q buffer in the TMA 128-byte swizzle layout and TMA-stores it;
 // LSE = ln2 * (m + log2 l) is written per row.
@@ -319,34 +322,41 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
       if (j > 0) mbar_arrive(bar_addr<D>(base, C::B_VE + (j - 1) % C::STAGES));
       mbar_arrive(bar_addr<D>(base, C::B_KE + j % C::STAGES));
     }
+    // S in registers, with each 32-column block's row max from the same load
+    // (the TMEM load with a max reduction of sm_103a).
     uint32_t sraw[C::BN / 32][32];
+    float mxq[C::BN / 32];
 #pragma unroll
-    for (int q = 0; q < C::BN / 32; ++q) tmem_ld32(t_s + 32 * q, sraw[q]);
+    for (int q = 0; q < C::BN / 32; ++q) tmem_ld32_max(t_s + 32 * q, sraw[q], mxq[q]);
     tmem_ld_wait();
     float s[C::BN];
 #pragma unroll
     for (int q = 0; q < C::BN / 32; ++q) {
       reg_fence(sraw[q]);
+      asm volatile("" : "+f"(mxq[q]));  // valid only after the wait, like sraw
 #pragma unroll
       for (int u = 0; u < 32; ++u) s[32 * q + u] = __uint_as_float(sraw[q][u]);
     }
 
     const int valid = row_end - (t0 + j) * C::BN;  // keys of this tile this row may see
+    float mx = mxq[0];
+#pragma unroll
+    for (int q = 1; q < C::BN / 32; ++q) mx = fmaxf(mx, mxq[q]);
     if (valid < C::BN) {
+      // Masked keys (the ragged end, the diagonal, a key length) become -inf
+      // and the max is taken over the rest: the loads' max includes them.
 #pragma unroll
       for (int u = 0; u < C::BN; ++u)
         if (u >= valid) s[u] = -INFINITY;
+      float mxa[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mxa[i] = fmaxf(s[i], s[i + 8]);
+#pragma unroll
+      for (int u = 16; u < C::BN; u += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mxa[i] = fmax3(mxa[i], s[u + i], s[u + 8 + i]);
+      mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])), fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
     }
-    // Row max with 8 independent chains of 3-input max.
-    float mxa[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) mxa[i] = fmaxf(s[i], s[i + 8]);
-#pragma unroll
-    for (int u = 16; u < C::BN; u += 16)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mxa[i] = fmax3(mxa[i], s[u + i], s[u + 8 + i]);
-    const float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
-                           fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
     const float m_new = fmaxf(m_ref, mx * c);
 
     // Lazy rescale decision (warp-uniform, since TMEM access is per warp): move
@@ -722,7 +732,7 @@ cudaError_t launch_merge(const FwdParams& p, bool bf16, cudaStream_t stream) {
 }
 
 cudaError_t launch_fwd_f16(const FwdParams& p, bool bf16, cudaStream_t stream) {
-  if (p.d == 128) return launch_fwd_d128(p, bf16, stream);
+  if (p.d == 128) return bf16 ? launch<128, true>(p, stream) : launch<128, false>(p, stream);
   if (p.d == 64) return bf16 ? launch<64, true>(p, stream) : launch<64, false>(p, stream);
   return cudaErrorInvalidValue;
 }

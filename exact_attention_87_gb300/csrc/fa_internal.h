@@ -113,21 +113,17 @@ constexpr float kRescaleThresholdLog2 = 15.0f;
 // Tile sizes of the fp16/bf16 kernel: Q rows per sub-tile (two sub-tiles per
 // CTA) and keys per K/V tile; the host encodes the TMA boxes with them.
 constexpr int kF16BlockQ = 128, kF16BlockKV = 128;
-// Keys per K/V tile of the d = 128 and d = 256 kernels (their K and V TMA
-// boxes are this many rows); the d = 64 kernel takes kF16BlockKV.
-constexpr int kD128BlockKV = 64;
+// Keys per K/V tile of the d = 256 kernel (its K and V TMA boxes are this
+// many rows); the d = 64 / 128 kernel takes kF16BlockKV.
 constexpr int kD256BlockKV = 64;
 // Rows of the K and V TMA boxes of the 16-bit forward kernel for head dimension d.
-constexpr int fwd_kv_box_rows(int d) { return d == 64 ? kF16BlockKV : d == 128 ? kD128BlockKV : kD256BlockKV; }
+constexpr int fwd_kv_box_rows(int d) { return d == 256 ? kD256BlockKV : kF16BlockKV; }
 
 // Timeline trace layout of the testing build.
 constexpr int kTraceCtas = 8, kTraceTiles = 64, kTraceEvents = 32;
 enum : int {
   kEvS0Issued = 0, kEvS1Issued, kEvPV0Issued, kEvPV1Issued, kEvSm0SFull, kEvSm0PArrive, kEvSm1SFull,
-  kEvSm1PArrive, kEvKIssued, kEvVIssued, kEvMmaKFull, kEvMmaVFull, kEvCta,
-  // phases inside a softmax tile (thread 0 of each sub-tile; +4 for sub-tile 1):
-  // S in registers, rescale decided, P computed and stored (issued), P stores complete
-  kEvSm0Loaded, kEvSm0Voted, kEvSm0PDone, kEvSm0Stored
+  kEvSm1PArrive, kEvKIssued, kEvVIssued, kEvMmaKFull, kEvMmaVFull, kEvCta
 };
 // Backward kernel events (tile index = Q tile i): MMA issue of dV_i, dP_i,
 // S_{i+1}, dK_i, dQ_i; softmax warpgroup 0 (thread 0): S_i ready, P_i
@@ -144,8 +140,6 @@ enum : int {
 
 // Launch the 16-bit (fp16 / bf16) forward kernel for head dimension p.d (64 or 128).
 cudaError_t launch_fwd_f16(const FwdParams& p, bool bf16, cudaStream_t stream);
-// The head-dimension-128 kernel (64-key tiles, two S buffers per Q sub-tile).
-cudaError_t launch_fwd_d128(const FwdParams& p, bool bf16, cudaStream_t stream);
 // Merge num_splits parts in o_part / lse_part (rows from merge_row0 on) into
 // O (dtype of the 16-bit path) and LSE; rows with no key in any part get
 // O = 0, LSE = -inf. Serves split-KV and fa_merge alike.

@@ -17,9 +17,9 @@ EVENTS = ["S0_issued", "S1_issued", "PV0_issued", "PV1_issued", "sm0_sfull", "sm
           "sm0_loaded", "sm0_voted", "sm0_pdone", "sm0_stored", "sm1_loaded", "sm1_voted", "sm1_pdone", "sm1_stored"]
 def kv_tile(d: int) -> int:
     """Keys per K/V tile of the 16-bit forward kernel for head dimension d
-    (stats_trace has ceil(N / kv_tile(d)) entries per row): 128 for d = 64,
-    64 for d = 128 and 256."""
-    return 128 if d == 64 else 64
+    (stats_trace has ceil(N / kv_tile(d)) entries per row): 128 for d = 64
+    and 128, 64 for d = 256."""
+    return 64 if d == 256 else 128
 _lib = None
 
 

@@ -315,202 +315,6 @@ def test_model_catches_a_stage_freed_too_early():
         EarlyV(6, 6, True, 2, True, False, random.Random(3)).run()
 
 
-class D128Model(Model):
-    """`fa_fwd_d128_kernel`: two 128-row Q sub-tiles, 64-key K/V tiles in a
-    KST-stage K ring and a VST-stage V ring, two S buffers per sub-tile
-    (S_i(j+2) issued right behind P_i(j)·V into the columns of P_i(j)), both
-    rings freed by arrivals of the softmax warps once S_i(j) is complete (K_j,
-    and V_{j-2}, whose P·V precedes S_i(j) in that sub-tile's issue stream).
-    A rescale at tile j waits for S_i(j+1) (issued after P_i(j-1)·V), and then
-    does not wait for it again at tile j+1; at the last tile it waits for a
-    barrier committed once after P_i(nkv-2)·V (OP). The epilogue waits for a
-    barrier committed once after the last P·V (OL). The strict build commits
-    every P·V (PVD) and the MMA warp waits for it before S_i(j+2)."""
-
-    def __init__(self, nkv0, nkv1, has1, strict, rng, kst=4, vst=6):
-        super().__init__(nkv0, nkv1, has1, 1, True, strict, rng)
-        self.KST, self.VST = kst, vst   # the kernel's rings: 4 K stages, 6 V stages
-        nsub = 2 if has1 else 1
-        self.bars = {"QF": Bar(1)}
-        for s in range(self.KST):
-            self.bars.update({f"KF{s}": Bar(1), f"KE{s}": Bar(4 * nsub)})
-        for s in range(self.VST):
-            self.bars.update({f"VF{s}": Bar(1), f"VE{s}": Bar(4 * nsub)})
-        for i in range(2):
-            for b in range(2):
-                self.bars.update({f"SF{i}{b}": Bar(1), f"PF{i}{b}": Bar(4)})
-            self.bars.update({f"OP{i}": Bar(1), f"OL{i}": Bar(1), f"PVD{i}": Bar(1), f"DR{i}": Bar(1)})
-        self.kstage, self.vstage = [None] * self.KST, [None] * self.VST
-        self.v_release_lag = 2    # planted-mistake switch: V_{j-lag} freed at tile j
-        self.rescale_waits_next_s = True   # planted-mistake switch
-
-    def roles(self):
-        roles = [self.producer128(), self.mma128(0)] + [self.softmax128(0, w) for w in range(4)]
-        if self.has1:
-            roles += [self.mma128(1)] + [self.softmax128(1, w) for w in range(4)]
-        return roles
-
-    def producer128(self):
-        if self.nkv == 0:
-            return
-        self.landing.append(("Q", 0, 0, "QF"))
-        subs = range(2 if self.has1 else 1)
-        for j in range(self.nkv):
-            ks, vs = j % self.KST, j % self.VST
-            yield ("wait", f"KE{ks}", j // self.KST - 1)
-            if j >= self.KST:
-                for i in subs:
-                    if j - self.KST < self.nk[i]:
-                        assert ("S", i, j - self.KST) in self.mma_done, f"K stage {ks} reloaded before S{i}"
-            self.kstage[ks] = None
-            self.landing.append(("K", ks, j, f"KF{ks}"))
-            yield ("step",)
-            yield ("wait", f"VE{vs}", j // self.VST - 1)
-            if j >= self.VST:
-                for i in subs:
-                    if j - self.VST < self.nk[i]:
-                        assert ("PV", i, j - self.VST) in self.mma_done, f"V stage {vs} reloaded before PV{i}"
-            self.vstage[vs] = None
-            self.landing.append(("V", vs, j, f"VF{vs}"))
-            yield ("step",)
-
-    def mma128(self, sub):
-        nkv = self.nk[sub]
-        if nkv > 0:
-            yield ("wait", "QF", 0)
-            for j in range(min(nkv, 2)):
-                yield ("wait", f"KF{j % self.KST}", j // self.KST)
-                self.issue(sub, "S", j)
-                self.commit(sub, f"SF{sub}{j & 1}")
-                yield ("step",)
-            for j in range(nkv):
-                yield ("wait", f"VF{j % self.VST}", j // self.VST)
-                yield ("wait", f"PF{sub}{j & 1}", j >> 1)
-                self.issue(sub, "PV", j)
-                if self.STRICT:
-                    self.commit(sub, f"PVD{sub}")
-                if j == nkv - 2:
-                    self.commit(sub, f"OP{sub}")
-                if j == nkv - 1:
-                    self.commit(sub, f"OL{sub}")
-                yield ("step",)
-                if j + 2 < nkv:
-                    if self.STRICT:
-                        yield ("wait", f"PVD{sub}", j)
-                    n = j + 2
-                    yield ("wait", f"KF{n % self.KST}", n // self.KST)
-                    self.issue(sub, "S", n)
-                    self.commit(sub, f"SF{sub}{n & 1}")
-                    yield ("step",)
-        self.commit(sub, f"DR{sub}")
-        yield ("wait", f"DR{sub}", 0)
-
-    def softmax128(self, sub, w):
-        nkv, lag = self.nk[sub], self.v_release_lag
-        s_waited = False
-        for j in range(nkv):
-            b = j & 1
-            if not s_waited:
-                yield ("wait", f"SF{sub}{b}", j >> 1)
-            s_waited = False
-            if j >= lag:
-                self.bars[f"VE{(j - lag) % self.VST}"].arrive()
-            self.bars[f"KE{j % self.KST}"].arrive()
-            assert ("S", sub, j) in self.mma_done
-            yield ("step",)
-            # P_i(j) overwrites the buffer of S_i(j), whose previous P (P_i(j-2)) P_i(j-2)·V read
-            assert j < 2 or ("PV", sub, j - 2) in self.mma_done, "P written over P(j-2) before its P.V"
-            self.p_written.setdefault((sub, j), set()).add(w)
-            if j > 0 and self.rng.random() < 0.3:   # a rescale of O at tile j (this warp's vote)
-                if self.rescale_waits_next_s:
-                    if j + 1 < nkv:
-                        yield ("wait", f"SF{sub}{b ^ 1}", (j + 1) >> 1)
-                        s_waited = True
-                    else:
-                        yield ("wait", f"OP{sub}", 0)
-                assert ("PV", sub, j - 1) in self.mma_done, "O rescaled while an earlier P.V may run"
-                assert ("PV", sub, j) not in self.mma_started
-            self.bars[f"PF{sub}{b}"].arrive()
-            yield ("step",)
-        if nkv > 0:
-            yield ("wait", f"OL{sub}", 0)
-            for j in range(nkv):
-                assert ("PV", sub, j) in self.mma_done, "epilogue read O before the last P.V"
-
-    def execute_head(self):
-        warp, kind, sub, j = self.pipe.pop(0)
-        self.mma_started.add((kind, sub, j))
-        if kind == "S":
-            assert self.kstage[j % self.KST] == j, f"S{sub}({j}) on a K stage without K_{j}"
-            assert j < 2 or ("PV", sub, j - 2) in self.mma_done, "S overwrote P before P.V read it"
-        else:
-            assert self.vstage[j % self.VST] == j, f"PV{sub}({j}) on a V stage without V_{j}"
-            assert self.p_written.get((sub, j)) == {0, 1, 2, 3}, "P.V before every softmax warp wrote P"
-        self.mma_done.add((kind, sub, j))
-        self.completed_by[warp] += 1
-
-
-# (nkv0, nkv1, has1): equal counts, the causal shape (sub-tile 1 sees two
-# more 64-key tiles), a single sub-tile, no key tile
-CASES128 = [(1, 1, True), (2, 2, True), (3, 3, True), (8, 8, True), (13, 13, True), (2, 4, True), (7, 9, True),
-            (6, 0, False), (1, 0, False), (0, 0, True), (0, 0, False)]
-
-
-@pytest.mark.parametrize("kst,vst", [(4, 6), (2, 4), (3, 4), (4, 4), (2, 2), (3, 3)], ids=lambda x: str(x))
-@pytest.mark.parametrize("strict", [False, True], ids=["default", "strict"])
-@pytest.mark.parametrize("nkv0,nkv1,has1", CASES128)
-def test_d128_barrier_protocol(strict, nkv0, nkv1, has1, kst, vst):
-    """The kernel's rings (4 K, 6 V stages) and tighter ones, so that either
-    ring can be the one the producer waits on. With the causal mask the
-    second sub-tile runs two tiles past the first, which never frees the V
-    stages of its last two tiles: the V ring then needs at least 4 stages
-    (the kernel asserts it; see the next test), so smaller V rings are run
-    on equal tile counts only."""
-    if vst < 4 and nkv1 > nkv0:
-        pytest.skip("a V ring under 4 stages is only valid for equal tile counts")
-    rng = random.Random(3000 + 100 * nkv0 + 10 * nkv1 + 2 * has1 + strict + 7 * kst + 13 * vst)
-    for _ in range(200):
-        D128Model(nkv0, nkv1, has1, strict, rng, kst, vst).run()
-
-
-def test_d128_model_causal_needs_four_v_stages():
-    """Why the kernel requires V_STAGES >= 4: under the causal mask the first
-    sub-tile's last V release is for V_{nkv0-3}, and the producer, loading up
-    to V_{nkv0+1}, must not need a stage freed later than that."""
-    with pytest.raises(AssertionError, match="deadlock"):
-        for seed in range(100):
-            D128Model(7, 9, True, False, random.Random(seed), 4, 3).run()
-
-
-def test_d128_model_catches_a_rescale_that_trusts_only_its_own_s():
-    """Planted mistake: a rescale at tile j that takes S_i(j)'s completion as
-    proof that P_i(j-1)·V is complete. With S_i(j+1) issued before it, that
-    P·V can still be running."""
-    class NoRescaleWait(D128Model):
-        def __init__(self, *a):
-            super().__init__(*a)
-            self.rescale_waits_next_s = False
-    with pytest.raises(AssertionError, match="O rescaled while an earlier P.V may run"):
-        for seed in range(200):
-            NoRescaleWait(8, 8, True, False, random.Random(seed)).run()
-
-
-@pytest.mark.parametrize("lag", [0, 1])
-def test_d128_model_catches_v_freed_early(lag):
-    """Planted mistake: V_{j-lag} freed at tile j (lag 0 or 1), when only
-    P_i(j-2)·V is known to be complete. On a V ring the producer waits on
-    (3 stages here) it can then reload a V stage under a P·V. (With the
-    kernel's 4 K and 6 V stages the K ring holds the producer back far enough
-    that these releases would happen to be harmless.)"""
-    class EarlyV(D128Model):
-        def __init__(self, *a):
-            super().__init__(*a, kst=4, vst=3)
-            self.v_release_lag = lag
-    with pytest.raises(AssertionError, match="reloaded before|without V_"):
-        for seed in range(300):
-            EarlyV(13, 13, True, False, random.Random(seed)).run()
-
-
 class D256Model(Model):
     """`fa_fwd_d256_kernel`: one 128-row Q tile, 64-key K/V tiles in 2-stage
     rings, two S buffers (S_{j+2} issued right behind P_j·V into the columns
