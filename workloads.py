@@ -19,7 +19,8 @@ case, a mid-size fp16 case (the worked throughput example on the dataflow page,
 B=8, H=12, L=2048, d=128), a large bf16 case whose Q and K have sigma 3 so that
 row maxima keep jumping between key tiles, a long-sequence bf16 case, and a
 head-dimension-256 bf16 case (the MUSA guide's block-size table goes up to
-d = 256).
+d = 256), and the 4096-token shape at head dimension 64 (bf16 and fp16), where
+the softmax is twice the share of the work.
 """
 from __future__ import annotations
 
@@ -70,6 +71,8 @@ WORKLOADS = {
         Workload("b8h32n4096d128_bf16_qk3", 4, 8, 32, 4096, 128, "bf16", sigma_qk=3.0),
         Workload("b1h8n16384d128_bf16", 5, 1, 8, 16384, 128, "bf16"),
         Workload("b4h16n4096d256_bf16", 6, 4, 16, 4096, 256, "bf16"),
+        Workload("b8h32n4096d64_bf16", 7, 8, 32, 4096, 64, "bf16"),
+        Workload("b8h32n4096d64_f16", 8, 8, 32, 4096, 64, "f16"),
     ]
 }
 WORKLOAD_ORDER = list(WORKLOADS)
