@@ -469,7 +469,7 @@ def main():
     workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     # The plan the library runs: 1 launch (unsplit), 2 (every unit split, merge) or 3 (split wave tail).
     n_launch = 1
-    if args.splits != 1 and w.dtype != "f32" and w.d != 256:
+    if args.splits != 1 and w.dtype != "f32":
         n_launch = fa.fa_fwd_splitkv_launches(w.B, w.H, w.N, w.d, args.splits)
         if n_launch < 1:
             raise RuntimeError(f"fa_fwd_splitkv_launches failed ({n_launch})")

@@ -186,33 +186,50 @@ const char* fa_strerror(int status) {
 
 namespace {
 
-// Split-KV sizing. Work units of the 16-bit kernel are 256 Q rows x (a key
-// range of whole 128-key tiles).
-constexpr int kQBlock = 2 * fa::kF16BlockQ;
-
-long long kv_tiles(int N) { return (static_cast<long long>(N) + fa::kF16BlockKV - 1) / fa::kF16BlockKV; }
+// Split-KV sizing. Work units of the 16-bit forward kernels are
+// fa::fwd_q_block(d) Q rows (256, or 128 at d = 256) x (a key range of whole
+// K/V tiles of fa::fwd_kv_box_rows(d) keys: 128, or 64 at d = 256).
+long long kv_tiles(int N, int d) {
+  const int t = fa::fwd_kv_box_rows(d);
+  return (static_cast<long long>(N) + t - 1) / t;
+}
+long long q_blocks(int N, int d) {
+  const int q = fa::fwd_q_block(d);
+  return (static_cast<long long>(N) + q - 1) / q;
+}
+// 128-row tiles of the backward kernels.
+long long bwd_tiles(int N) { return (static_cast<long long>(N) + fa::kF16BlockKV - 1) / fa::kF16BlockKV; }
 
 // Effective split count: explicit requests are clamped so that every range
 // holds at least one tile; 0 picks the count with the smallest modelled time:
 //   waves(s) * (tiles/s + 1) * t_tile            partial passes (+1 tile of set-up per unit)
 // + (s > 1) * (2 * s * rows * d * 4 bytes / 5 TB/s + 5 us)   the merge pass
 // with t_tile ~ 2 us * d / 128 for one 256-row unit and one 128-key tile on
-// one SM (measured on GB300 at ~2 GHz).
+// one SM (measured on GB300 at ~2 GHz), scaled by the unit's rows x keys for
+// the d = 256 kernel's 128-row units and 64-key tiles (1 us).
 // The tail plan: when the units end in a partial last wave, the full waves
 // run unsplit and only the last wave's units are split (as many ways as fit
 // in one wave), then merged:
-//   W * (tiles + 1) * t_tile + (tiles/s + 1) * t_tile + merge of the tail rows.
+//   W * (tiles + 1) * t_tile + (tiles/s + 1) * t_tile + merge of the tail rows
+//   + 20 us
+// The last term is the launch boundary: the split tail starts only once
+// every CTA of the full waves has finished, whereas unsplit tail units start
+// as SMs free up. Measured on GB300: with the tail split, B=1 H=8 N=16384
+// d=128 runs 8 % faster than unsplit (uniform 2-way splits 1 % slower), B=8
+// H=12 N=2048 d=128 within 1 %, and B=4 H=16 N=4096 d=256 (13.5 waves) 1 %
+// slower; the term makes the last two run unsplit.
 struct SplitPlan {
   int splits;            // key ranges per split unit (1: unsplit)
   long long tail_qunit0; // >= 0: units before it unsplit, the rest split; < 0: every unit split alike
 };
 
 SplitPlan split_plan(int B, int H, int N, int d, int num_splits, int num_sms) {
-  const long long tiles = kv_tiles(N);
+  const long long tiles = kv_tiles(N, d);
   if (num_splits > 0) return {static_cast<int>(std::min<long long>(num_splits, tiles)), -1};
-  const long long units = static_cast<long long>(B) * H * ((N + kQBlock - 1) / kQBlock);
+  const long long units = static_cast<long long>(B) * H * q_blocks(N, d);
   const double rows = static_cast<double>(B) * H * N;
-  const double t_tile_us = 2.0 * d / 128.0;
+  const double t_tile_us =
+      2.0 * d / 128.0 * (fa::fwd_q_block(d) * fa::fwd_kv_box_rows(d)) / (2.0 * fa::kF16BlockQ * fa::kF16BlockKV);
   SplitPlan best{1, -1};
   double best_us = 1e300;
   for (int s = 1; s <= 16 && s <= tiles; ++s) {
@@ -228,10 +245,10 @@ SplitPlan split_plan(int B, int H, int N, int d, int num_splits, int num_sms) {
     const long long s = std::min<long long>({num_sms / tail, tiles, 16});
     if (s >= 2) {
       const long long per = (tiles + s - 1) / s;
-      const double tail_rows = static_cast<double>(tail) * kQBlock;
+      const double tail_rows = static_cast<double>(tail) * fa::fwd_q_block(d);
       const double us = static_cast<double>(full) * (static_cast<double>(tiles) + 1.0) * t_tile_us +
                         (static_cast<double>(per) + 1.0) * t_tile_us + 2.0 * s * tail_rows * d * 4.0 / 5e12 * 1e6 +
-                        5.0;
+                        5.0 + 20.0;
       if (us < best_us) best = {static_cast<int>(s), full * num_sms};
     }
   }
@@ -248,10 +265,10 @@ unsigned long long workspace_bytes_for(int B, int H, int N, int d, int splits, l
 }
 
 // First row of the split units of a plan (0 unless only the wave tail is split).
-long long plan_row0(const SplitPlan& plan, int N) {
+long long plan_row0(const SplitPlan& plan, int N, int d) {
   if (plan.tail_qunit0 <= 0) return 0;
-  const long long nqb = (N + kQBlock - 1) / kQBlock;
-  return (plan.tail_qunit0 / nqb) * N + (plan.tail_qunit0 % nqb) * kQBlock;
+  const long long nqb = q_blocks(N, d);
+  return (plan.tail_qunit0 / nqb) * N + (plan.tail_qunit0 % nqb) * fa::fwd_q_block(d);
 }
 
 // What a 16-bit split-KV pass does for a shape on a device with num_sms SMs:
@@ -265,16 +282,20 @@ struct PlanSummary {
 };
 
 PlanSummary summarize_plan(int B, int H, int N, int d, int num_splits, int num_sms) {
-  const long long units = static_cast<long long>(B) * H * ((N + kQBlock - 1) / kQBlock);
-  if (d == 256) return {1, units, 1, 0};  // the d = 256 kernel runs unsplit
+  const long long units = static_cast<long long>(B) * H * q_blocks(N, d);
   const SplitPlan plan = split_plan(B, H, N, d, num_splits, num_sms);
-  const long long tiles = kv_tiles(N);
+  const long long tiles = kv_tiles(N, d);
   const long long per = (tiles + plan.splits - 1) / plan.splits;
   const int eff = static_cast<int>((tiles + per - 1) / per);
   if (eff <= 1) return {1, units, 1, 0};
   const bool tail = plan.tail_qunit0 > 0;
   return {eff, tail ? plan.tail_qunit0 : 0, tail ? 3 : 2,
-          workspace_bytes_for(B, H, N, d, eff, tail ? plan_row0(plan, N) : 0)};
+          workspace_bytes_for(B, H, N, d, eff, tail ? plan_row0(plan, N, d) : 0)};
+}
+
+// The 16-bit forward kernel for the head dimension p.d.
+cudaError_t launch_fwd16(const fa::FwdParams& p, bool bf16, cudaStream_t s) {
+  return p.d == 256 ? fa::launch_fwd_d256(p, bf16, s) : fa::launch_fwd_f16(p, bf16, s);
 }
 
 // Argument checks of the forward entry points, in the order their status
@@ -307,7 +328,7 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
   if (vst != FA_OK) return vst;
   const long long BH = static_cast<long long>(B) * H;
   if (o_f32 && !aligned16(o_f32)) return FA_ERR_ALIGN;
-  if (o_f32 && (dtype == FA_F32 || d == 256 || num_splits != 1 || causal || klen)) return FA_ERR_UNSUPPORTED;
+  if (o_f32 && (dtype == FA_F32 || num_splits != 1 || causal || klen)) return FA_ERR_UNSUPPORTED;
   if (!(rescale_tau >= 0.f) || !(rescale_tau <= 64.f)) return FA_ERR_SCALE;
 
   DeviceInfo dev;
@@ -337,14 +358,13 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
   p.num_sms = dev.num_sms;
   p.rescale_tau = rescale_tau;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // fp32 and d = 256 always run unsplit.
-  const SplitPlan plan = (dtype == FA_F32 || d == 256) ? SplitPlan{1, -1}
-                                                        : split_plan(B, H, N, d, num_splits, dev.num_sms);
+  // fp32 always runs unsplit.
+  const SplitPlan plan = dtype == FA_F32 ? SplitPlan{1, -1} : split_plan(B, H, N, d, num_splits, dev.num_sms);
   const int splits = plan.splits;
-  const long long tiles = kv_tiles(N);
+  const long long tiles = kv_tiles(N, d);
   p.split_tiles = static_cast<int>((tiles + splits - 1) / splits);
   p.num_splits = static_cast<int>((tiles + p.split_tiles - 1) / p.split_tiles);
-  const long long row0 = (p.num_splits > 1) ? plan_row0(plan, N) : 0;
+  const long long row0 = (p.num_splits > 1) ? plan_row0(plan, N, d) : 0;
   if (p.num_splits > 1) {
     const unsigned long long need = workspace_bytes_for(B, H, N, d, p.num_splits, row0);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
@@ -374,30 +394,28 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
         !encode_bhnd_16bit(&p.tm_v, V, bh, N, d, dt, kv_rows) ||
         (O && !encode_bhnd_16bit(&p.tm_o, O, bh, N, d, dt, fa::kF16BlockQ)))
       return FA_ERR_CUDA;
-    if (d == 256) {
-      e = fa::launch_fwd_d256(p, dtype == FA_BF16, s);
-    } else if (p.num_splits > 1 && plan.tail_qunit0 > 0) {
+    const bool bf16 = dtype == FA_BF16;
+    if (p.num_splits > 1 && plan.tail_qunit0 > 0) {
       // Full waves unsplit (O written directly), then the last wave's units
       // split, then the merge of their rows only.
-      const long long nqb = (N + kQBlock - 1) / kQBlock;
-      const long long qunits = static_cast<long long>(BH) * nqb;
+      const long long qunits = static_cast<long long>(BH) * q_blocks(N, d);
       fa::FwdParams pm = p;
       pm.num_splits = 1;
       pm.split_tiles = static_cast<int>(tiles);
       pm.qunit0 = 0;
       pm.qunit_count = static_cast<int>(plan.tail_qunit0);
-      e = fa::launch_fwd_f16(pm, dtype == FA_BF16, s);
+      e = launch_fwd16(pm, bf16, s);
       if (e == cudaSuccess) {
         fa::FwdParams pt = p;
         pt.qunit0 = static_cast<int>(plan.tail_qunit0);
         pt.qunit_count = static_cast<int>(qunits - plan.tail_qunit0);
         pt.merge_row0 = row0;
-        e = fa::launch_fwd_f16(pt, dtype == FA_BF16, s);
-        if (e == cudaSuccess) e = fa::launch_merge(pt, dtype == FA_BF16, s);
+        e = launch_fwd16(pt, bf16, s);
+        if (e == cudaSuccess) e = fa::launch_merge(pt, bf16, s);
       }
     } else {
-      e = fa::launch_fwd_f16(p, dtype == FA_BF16, s);
-      if (e == cudaSuccess && p.num_splits > 1) e = fa::launch_merge(p, dtype == FA_BF16, s);
+      e = launch_fwd16(p, bf16, s);
+      if (e == cudaSuccess && p.num_splits > 1) e = fa::launch_merge(p, bf16, s);
     }
   }
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -412,7 +430,7 @@ int partial_impl(const void* Q, const void* K, const void* V, float* O_part, flo
   if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
   if (dtype == FA_F32) return FA_ERR_UNSUPPORTED;
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_SHAPE;
-  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_HEADDIM;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
   const long long BH = static_cast<long long>(B) * H;
   if (BH > 0x7fffffffLL || BH * std::max(Nq, Nk) > (1ll << 40) / d) return FA_ERR_SHAPE;
@@ -441,7 +459,7 @@ int partial_impl(const void* Q, const void* K, const void* V, float* O_part, flo
   p.num_sms = dev.num_sms;
   p.rescale_tau = fa::kRescaleThresholdLog2;
   p.num_splits = 1;
-  p.split_tiles = static_cast<int>(kv_tiles(Nk));
+  p.split_tiles = static_cast<int>(kv_tiles(Nk, d));
   p.partial = 1;
   const CUtensorMapDataType dt = dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const int bh = static_cast<int>(BH);
@@ -450,7 +468,7 @@ int partial_impl(const void* Q, const void* K, const void* V, float* O_part, flo
       !encode_bhnd_16bit(&p.tm_v, V, bh, Nk, d, dt, fa::fwd_kv_box_rows(d)))
     return FA_ERR_CUDA;
   FA_DRY_RUN_RETURN();
-  const cudaError_t e = fa::launch_fwd_f16(p, dtype == FA_BF16, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_fwd16(p, dtype == FA_BF16, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -460,7 +478,7 @@ int merge_impl(const float* O_parts, const float* LSE_parts, int num_parts, void
   if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
   if (dtype == FA_F32) return FA_ERR_UNSUPPORTED;
   if (B < 1 || H < 1 || N < 1 || num_parts < 1) return FA_ERR_SHAPE;
-  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_HEADDIM;
   const long long rows = static_cast<long long>(B) * H * N;
   if (rows * num_parts > (1ll << 40) / d) return FA_ERR_SHAPE;
   if (!aligned16(O_parts) || !aligned16(O) || (reinterpret_cast<uintptr_t>(LSE_parts) & 3u) != 0 ||
@@ -537,8 +555,7 @@ int fa_fwd_splitkv_noalloc(const void* Q, const void* K, const void* V, void* O,
   void* scratch = nullptr;
   const int st = noalloc_scratch(&scratch);
   if (st != FA_OK) return st;
-  const unsigned long long need =
-      (dtype == FA_F32 || d == 256) ? 0ull : fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits);
+  const unsigned long long need = dtype == FA_F32 ? 0ull : fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits);
   if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
   return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, dtype, stream, 0, nullptr, nullptr, 0, num_splits, scratch,
                   FA_NOALLOC_SCRATCH_BYTES);
@@ -546,8 +563,7 @@ int fa_fwd_splitkv_noalloc(const void* Q, const void* K, const void* V, void* O,
 
 int fa_fwd_splitkv_launches(int B, int H, int N, int d, int num_splits) {
   if (B < 1 || H < 1 || N < 1 || num_splits < 0) return -FA_ERR_SHAPE;
-  if (d == 256) return 1;
-  if (d != 64 && d != 128) return -FA_ERR_HEADDIM;
+  if (d != 64 && d != 128 && d != 256) return -FA_ERR_HEADDIM;
   DeviceInfo dev;
   const int st = device_info(&dev);
   if (st != FA_OK) return -st;
@@ -570,8 +586,7 @@ int fa_fwd_splitkv_plan(int B, int H, int N, int d, int num_splits, int num_sms,
 
 int fa_fwd_splitkv_num_splits(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1) return -FA_ERR_SHAPE;
-  if (d == 256) return 1;  // the d = 256 kernel runs unsplit
-  if (d != 64 && d != 128) return -FA_ERR_HEADDIM;
+  if (d != 64 && d != 128 && d != 256) return -FA_ERR_HEADDIM;
   DeviceInfo dev;
   const int st = device_info(&dev);
   if (st != FA_OK) return -st;
@@ -579,7 +594,7 @@ int fa_fwd_splitkv_num_splits(int B, int H, int N, int d) {
 }
 
 unsigned long long fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits) {
-  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || num_splits < 0) return 0;  // d = 256: unsplit, none
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128 && d != 256) || num_splits < 0) return 0;
   int num_sms = 1;  // an explicit split count does not depend on the device
   if (num_splits == 0) {
     DeviceInfo dev;
@@ -632,7 +647,7 @@ int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const v
   p.N = N;
   p.d = d;
   p.scale = scale;
-  p.n_pad = static_cast<int>(kv_tiles(N) * fa::kF16BlockKV);
+  p.n_pad = static_cast<int>(bwd_tiles(N) * fa::kF16BlockKV);
   p.status = dev.status;
   p.wait_limit = wait_limit > 0 ? wait_limit : wait_limit_cycles();
   p.inject = inject;
@@ -669,7 +684,7 @@ extern "C" {
 unsigned long long fa_bwd_workspace_size(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
   const unsigned long long bh = static_cast<unsigned long long>(B) * H;
-  const unsigned long long n_pad = static_cast<unsigned long long>(kv_tiles(N)) * fa::kF16BlockKV;
+  const unsigned long long n_pad = static_cast<unsigned long long>(bwd_tiles(N)) * fa::kF16BlockKV;
   return bwd_part_bytes(bh * N * d * 4) + 2 * bwd_part_bytes(bh * n_pad * 4);
 }
 

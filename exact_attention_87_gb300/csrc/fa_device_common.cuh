@@ -71,9 +71,9 @@ __device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, co
 }
 
 // The lazy-rescale threshold in log2 units: the reference max of a row moves
-// only when P taken against it would exceed 2^threshold (the d = 64 and 256
-// kernels test the tile max against it, the d = 128 kernel the tile's sum of
-// P), so P <= 2^threshold (fits fp16 and bf16). The testing build takes it
+// only when P taken against it would exceed 2^threshold (the kernels test
+// each tile's max against it), so P <= 2^threshold (fits fp16 and bf16). The
+// testing build takes it
 // from the parameters, so that 0 (rescale whenever the max grows, the
 // dataflow page's section 2.3) can be run against the oracle too.
 __device__ __forceinline__ float rescale_threshold(const FwdParams& p) {

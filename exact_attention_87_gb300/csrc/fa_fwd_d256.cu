@@ -7,7 +7,7 @@
 // allows (the dataflow page, section 2.1: the block size follows from the
 // on-chip budget; the MUSA guide's block-size table shrinks B_c as d grows).
 //
-// GB300 mapping (one CTA per (batch*head, 128-row Q tile), 6 warps):
+// GB300 mapping (one CTA per (batch*head, 128-row Q tile, key range), 6 warps):
 //   warp 4      TMA producer: Q once (4 column blocks of 64), then K_j and V_j
 //               (64 keys x 256 each) into 2-stage rings
 //   warp 5      MMA warp (one elected lane issues): S_j = Q K_j^T (SS,
@@ -19,7 +19,8 @@
 //   warps 0-3   softmax (thread = row = TMEM lane): frees K_j's stage once S_j
 //               is complete, max, lazy rescale of l and O, P = 2^(s*c - m)
 //               packed to 16 bits over the S columns; then
-//               the epilogue
+//               the epilogue (O / l through a TMA store, or under split-KV
+//               this key range's fp32 O / l and LSE to the partial buffers)
 // TMEM (512 columns): S0 [0,64), S1 [64,128), O [256,512). With one 128-row
 // Q tile per CTA the 256 fp32 O columns fit; two Q tiles would not.
 // SMEM: Q 64 KB + K ring 2 x 32 KB + V ring 2 x 32 KB.
@@ -74,7 +75,7 @@ __device__ __forceinline__ uint64_t opaque256(uint64_t x) {
 // --------------------------------------------------------------------------
 // TMA producer (one thread)
 // --------------------------------------------------------------------------
-__device__ __forceinline__ void producer256(const FwdParams& p, uint32_t base, int bh, int row0, int nkv,
+__device__ __forceinline__ void producer256(const FwdParams& p, uint32_t base, int bh, int row0, int t0, int nkv,
                                             const WaitCtl& ctl) {
   using C = C256;
   tma_prefetch_desc(&p.tm_q);
@@ -96,14 +97,14 @@ __device__ __forceinline__ void producer256(const FwdParams& p, uint32_t base, i
     mbar_arrive_expect_tx(kf, C::KV_BYTES);
 #pragma unroll
     for (int h = 0; h < 4; ++h)
-      tma_load_3d(base + C::OFF_K + s * C::KV_BYTES + h * C::KV_BLOCK, &p.tm_k, kf, 64 * h, j * C::BN, bh);
+      tma_load_3d(base + C::OFF_K + s * C::KV_BYTES + h * C::KV_BLOCK, &p.tm_k, kf, 64 * h, (t0 + j) * C::BN, bh);
     nk = j + 1;
     if (!wait_bar(bar256(base, C::B_VE + s), par, ctl, kWhereVEmpty)) { ok = false; break; }
     const uint32_t vf = bar256(base, C::B_VF + s);
     mbar_arrive_expect_tx(vf, C::KV_BYTES);
 #pragma unroll
     for (int h = 0; h < 4; ++h)
-      tma_load_3d(base + C::OFF_V + s * C::KV_BYTES + h * C::KV_BLOCK, &p.tm_v, vf, 64 * h, j * C::BN, bh);
+      tma_load_3d(base + C::OFF_V + s * C::KV_BYTES + h * C::KV_BLOCK, &p.tm_v, vf, 64 * h, (t0 + j) * C::BN, bh);
     nv = j + 1;
   }
   // Drain, always (the loop ended, this thread's wait gave up, or another role
@@ -188,7 +189,7 @@ drain:
 // --------------------------------------------------------------------------
 template <bool BF16>
 __device__ __forceinline__ void softmax256(const FwdParams& p, uint32_t base, uint32_t tmem, int bh, int row0,
-                                           int nkv, int key_end, const WaitCtl& ctl) {
+                                           int split, int t0, int nkv, int key_end, const WaitCtl& ctl) {
   using C = C256;
   const int t = threadIdx.x;
   const int lane = t & 31;
@@ -229,7 +230,7 @@ __device__ __forceinline__ void softmax256(const FwdParams& p, uint32_t base, ui
       s[u] = __uint_as_float(sraw[0][u]);
       s[32 + u] = __uint_as_float(sraw[1][u]);
     }
-    const int valid = row_end - j * C::BN;  // keys of this tile this row may see
+    const int valid = row_end - (t0 + j) * C::BN;  // keys of this tile this row may see
     float mx = fmaxf(mx_lo, mx_hi);
     if (valid < C::BN) {
       // Masked keys become -inf and the max is taken over the rest (the
@@ -252,14 +253,19 @@ __device__ __forceinline__ void softmax256(const FwdParams& p, uint32_t base, ui
     if (j == 0) {
       m_ref = m_new;
     } else if (__any_sync(0xffffffffu, m_new - m_ref > tau)) {
-      alpha = ex2_approx(m_ref - m_new);
+      // 0 for a row that saw no key yet (its l and O are 0), never exp2(-inf + inf)
+      alpha = m_ref > -INFINITY ? ex2_approx(m_ref - m_new) : 0.f;
       m_ref = m_new;
       l *= alpha;
       l_o *= alpha;
       rescale_o = true;
     }
+    // A row that has seen no key yet (every score so far masked: possible in a
+    // key range of a split under the causal mask) keeps m_ref = -inf; its P
+    // are taken against 0 so that they are 0, not exp2(-inf + inf).
+    const float m_use = m_ref > -INFINITY ? m_ref : 0.f;
     const float2 c2 = make_float2(c, c);
-    const float2 nm2 = make_float2(-m_ref, -m_ref);
+    const float2 nm2 = make_float2(-m_use, -m_use);
     float2 se = make_float2(0.f, 0.f), sro = se;
 #pragma unroll
     for (int q = 0; q < C::BN / 16; ++q) {
@@ -322,8 +328,37 @@ __device__ __forceinline__ void softmax256(const FwdParams& p, uint32_t base, ui
 
   // ---- epilogue: O / l -> dtype -> swizzled staging (Q buffer) -> TMA store; LSE ----
   tc_fence_after();
-  const bool empty = nkv == 0;
+  // No key to attend to (key length 0, or under the causal mask no key of
+  // this split's range for this row): O = 0, LSE = -inf instead of 0/0.
+  const bool empty = nkv == 0 || !(l > 0.f);
   const float inv_l = empty ? 0.f : 1.0f / (BF16 ? l_o : l);
+  if (p.num_splits > 1 || p.partial) {
+    // Split-KV (or one part of a merge done elsewhere): this key range's
+    // normalised O (fp32) and LSE go to the partial buffers, rows numbered
+    // from merge_row0, one span of rows per key range.
+    const size_t span = static_cast<size_t>(p.B) * p.H * p.N - p.merge_row0;
+    const size_t prow = static_cast<size_t>(split) * span + (static_cast<size_t>(bh) * p.N + my_row - p.merge_row0);
+#pragma unroll 1
+    for (int q = 0; q < C::D / 32; ++q) {
+      uint32_t r[32];
+      tmem_ld32(t_o + 32 * q, r);
+      tmem_ld_wait();
+      reg_fence(r);
+      if (empty) {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) r[u] = 0u;  // no key in this range: O_part = 0, LSE_part = -inf
+      }
+      if (my_row < p.N) {
+        float4* dst = reinterpret_cast<float4*>(p.o_part + prow * C::D + 32 * q);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          dst[u] = make_float4(__uint_as_float(r[4 * u]) * inv_l, __uint_as_float(r[4 * u + 1]) * inv_l,
+                               __uint_as_float(r[4 * u + 2]) * inv_l, __uint_as_float(r[4 * u + 3]) * inv_l);
+      }
+    }
+    if (my_row < p.N) p.lse_part[prow] = empty ? -INFINITY : (m_ref + lg2_approx(l)) * kLn2_256;
+    return;
+  }
   const uint32_t stage = base + C::OFF_Q;
 #pragma unroll 1
   for (int q = 0; q < C::D / 32; ++q) {
@@ -369,14 +404,26 @@ __global__ void __launch_bounds__(C256::THREADS, 1) fa_fwd_d256_kernel(const __g
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem_raw + (base - raw) + C::OFF_MISC);
   const int warp = threadIdx.x >> 5;
+  // Work unit: (batch*head, 128-row Q tile, key range); consecutive units
+  // share a head so its K/V stay in L2 while its Q tiles are processed.
   const int nqb = (p.N + C::BM - 1) / C::BM;
-  const int bh = blockIdx.x / nqb;
-  // Causal: Q tiles later in the sequence see more keys; they are launched first.
-  const int qb = p.causal ? nqb - 1 - static_cast<int>(blockIdx.x % nqb) : static_cast<int>(blockIdx.x % nqb);
+  const int split = blockIdx.x % p.num_splits;
+  const int qunit = p.qunit0 + blockIdx.x / p.num_splits;
+  const int bh = qunit / nqb;
+  // Causal, one launch over every unit unsplit: Q tiles later in the sequence
+  // see more keys; they are launched first. Split launches keep the natural
+  // order, in which the units of the split-KV tail plan (the last ones) hold
+  // the last rows: its merge and partial buffers cover the rows from
+  // merge_row0 on.
+  const bool heavy_first = p.causal && p.num_splits == 1 && p.qunit_count == 0;
+  const int qb = heavy_first ? nqb - 1 - qunit % nqb : qunit % nqb;
   const int row0 = qb * C::BM;
-  const int key_end = p.klen ? max(0, min(p.N, p.klen[bh / p.H])) : p.N;
+  // Keys this unit may see: [0, key_end); causal limits the tile to its own last row.
+  const int key_end = p.klen ? max(0, min(p.Nk, p.klen[bh / p.H])) : p.Nk;
   const int end = p.causal ? min(key_end, row0 + C::BM) : key_end;
-  const int nkv = (end + C::BN - 1) / C::BN;
+  const int t0 = split * p.split_tiles;  // first K/V tile of this key range
+  // Tiles in this key range (none when the unit's keys end before the range starts).
+  const int nkv = max(0, min((end + C::BN - 1) / C::BN - t0, p.split_tiles));
 
   if (threadIdx.x == 0) {
     mbar_init(bar256(base, C::B_Q), 1);
@@ -407,13 +454,13 @@ __global__ void __launch_bounds__(C256::THREADS, 1) fa_fwd_d256_kernel(const __g
   const WaitCtl ctl{p, base + C::OFF_MISC + 4};
 
   if (warp == C::WARP_TMA) {
-    if ((threadIdx.x & 31) == 0) producer256(p, base, bh, row0, nkv, ctl);
+    if ((threadIdx.x & 31) == 0) producer256(p, base, bh, row0, t0, nkv, ctl);
     __syncwarp();
   } else if (warp == C::WARP_MMA) {
     mma256<BF16>(base, tmem, nkv, ctl);
     __syncwarp();
   } else {
-    softmax256<BF16>(p, base, tmem, bh, row0, nkv, key_end, ctl);
+    softmax256<BF16>(p, base, tmem, bh, row0, split, t0, nkv, key_end, ctl);
   }
 
   tc_fence_before();
@@ -438,7 +485,10 @@ cudaError_t launch256(const FwdParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(bit);
   }
-  const long long units = static_cast<long long>(p.B) * p.H * ((p.N + C::BM - 1) / C::BM);
+  const long long all_qunits = static_cast<long long>(p.B) * p.H * ((p.N + C::BM - 1) / C::BM);
+  const long long qunits = p.qunit_count > 0 ? p.qunit_count : all_qunits;
+  if (p.qunit0 < 0 || p.qunit0 + qunits > all_qunits) return cudaErrorInvalidValue;
+  const long long units = qunits * p.num_splits;
   if (units <= 0 || units > 0x7fffffffLL) return cudaErrorInvalidValue;
   kern<<<dim3(static_cast<unsigned>(units)), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();

@@ -688,7 +688,18 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const __grid_constant__ F
       const float w = ex2_approx((p.lse_part[s * span + prow] - m) * kLog2e);
       l += w;
       const float* src = p.o_part + (s * span + prow) * D + lane * E;
-      if constexpr (E == 4) {
+      if constexpr (E == 8) {
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        const float4 y = *reinterpret_cast<const float4*>(src + 4);
+        acc[0] = fmaf(w, x.x, acc[0]);
+        acc[1] = fmaf(w, x.y, acc[1]);
+        acc[2] = fmaf(w, x.z, acc[2]);
+        acc[3] = fmaf(w, x.w, acc[3]);
+        acc[4] = fmaf(w, y.x, acc[4]);
+        acc[5] = fmaf(w, y.y, acc[5]);
+        acc[6] = fmaf(w, y.z, acc[6]);
+        acc[7] = fmaf(w, y.w, acc[7]);
+      } else if constexpr (E == 4) {
         const float4 x = *reinterpret_cast<const float4*>(src);
         acc[0] = fmaf(w, x.x, acc[0]);
         acc[1] = fmaf(w, x.y, acc[1]);
@@ -706,7 +717,9 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const __grid_constant__ F
 #pragma unroll
   for (int e = 0; e < E / 2; ++e) pk[e] = pack2<BF16>(acc[2 * e] * inv, acc[2 * e + 1] * inv);
   uint16_t* out = static_cast<uint16_t*>(p.o) + row * D + lane * E;
-  if constexpr (E == 4)
+  if constexpr (E == 8)
+    *reinterpret_cast<uint4*>(out) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  else if constexpr (E == 4)
     *reinterpret_cast<uint2*>(out) = make_uint2(pk[0], pk[1]);
   else
     *reinterpret_cast<uint32_t*>(out) = pk[0];
@@ -726,6 +739,7 @@ cudaError_t launch_merge_t(const FwdParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_merge(const FwdParams& p, bool bf16, cudaStream_t stream) {
+  if (p.d == 256) return bf16 ? launch_merge_t<256, true>(p, stream) : launch_merge_t<256, false>(p, stream);
   if (p.d == 128) return bf16 ? launch_merge_t<128, true>(p, stream) : launch_merge_t<128, false>(p, stream);
   if (p.d == 64) return bf16 ? launch_merge_t<64, true>(p, stream) : launch_merge_t<64, false>(p, stream);
   return cudaErrorInvalidValue;

@@ -53,8 +53,8 @@ struct alignas(64) FwdParams {
   int Nk;
   int partial;
   // Work units of this launch of the 16-bit kernel: Q blocks [qunit0,
-  // qunit0 + qunit_count) of the B*H*ceil(N/256) in (b*h, block) order, each
-  // split num_splits ways (qunit_count = 0: all of them). The split-KV merge
+  // qunit0 + qunit_count) of the B*H*ceil(N/q) in (b*h, block) order (q =
+  // fwd_q_block(d)), each split num_splits ways (qunit_count = 0: all of them). The split-KV merge
   // covers rows [merge_row0, B*H*N). The wave tail of a launch is split this
   // way: full waves unsplit, the last partial wave's units split.
   int qunit0;
@@ -68,7 +68,7 @@ struct alignas(64) FwdParams {
   int inject;                       // 1: the producer skips the V load of tile 0
   float* stats_trace;               // [B*H*N, nkv, 2]: (m in natural-log units, l) after each K/V tile
   unsigned long long* timeline;     // [kTraceCtas, kTraceEvents, kTraceTiles] clock64 stamps
-  float rescale_tau;                // lazy-rescale threshold (log2 units); the product build uses 8
+  float rescale_tau;                // lazy-rescale threshold (log2 units); the product build uses 15
 };
 
 // Everything the backward kernels need; passed by value as a __grid_constant__.
@@ -113,11 +113,14 @@ constexpr float kRescaleThresholdLog2 = 15.0f;
 // Tile sizes of the fp16/bf16 kernel: Q rows per sub-tile (two sub-tiles per
 // CTA) and keys per K/V tile; the host encodes the TMA boxes with them.
 constexpr int kF16BlockQ = 128, kF16BlockKV = 128;
-// Keys per K/V tile of the d = 256 kernel (its K and V TMA boxes are this
-// many rows); the d = 64 / 128 kernel takes kF16BlockKV.
-constexpr int kD256BlockKV = 64;
+// Tile sizes of the d = 256 kernel: Q rows per CTA (one Q tile) and keys per
+// K/V tile (its K and V TMA boxes are this many rows).
+constexpr int kD256BlockQ = 128, kD256BlockKV = 64;
 // Rows of the K and V TMA boxes of the 16-bit forward kernel for head dimension d.
 constexpr int fwd_kv_box_rows(int d) { return d == 256 ? kD256BlockKV : kF16BlockKV; }
+// Q rows of one work unit of the 16-bit forward kernel for head dimension d
+// (two 128-row sub-tiles for d = 64 / 128, one 128-row tile for d = 256).
+constexpr int fwd_q_block(int d) { return d == 256 ? kD256BlockQ : 2 * kF16BlockQ; }
 
 // Timeline trace layout of the testing build.
 constexpr int kTraceCtas = 8, kTraceTiles = 64, kTraceEvents = 32;
@@ -141,13 +144,16 @@ enum : int {
 // Launch the 16-bit (fp16 / bf16) forward kernel for head dimension p.d (64 or 128).
 cudaError_t launch_fwd_f16(const FwdParams& p, bool bf16, cudaStream_t stream);
 // Merge num_splits parts in o_part / lse_part (rows from merge_row0 on) into
-// O (dtype of the 16-bit path) and LSE; rows with no key in any part get
-// O = 0, LSE = -inf. Serves split-KV and fa_merge alike.
+// O (dtype of the 16-bit path, head dimension 64, 128 or 256) and LSE; rows
+// with no key in any part get O = 0, LSE = -inf. Serves split-KV and fa_merge
+// alike.
 cudaError_t launch_merge(const FwdParams& p, bool bf16, cudaStream_t stream);
 // Backward: row statistics (D, LSE * log2 e) and a zeroed dQ accumulator;
 // the main dK/dV/dQ kernel; the dQ accumulator rounded into dQ.
 cudaError_t launch_bwd_f16(const BwdParams& p, bool bf16, cudaStream_t stream);
-// Launch the 16-bit forward kernel for head dimension 256 (no split-KV).
+// Launch the 16-bit forward kernel for head dimension 256 (same parameter
+// block and work-unit scheme as launch_fwd_f16, with 128-row Q tiles and
+// 64-key K/V tiles).
 cudaError_t launch_fwd_d256(const FwdParams& p, bool bf16, cudaStream_t stream);
 // Launch the fp32 (3 x TF32) forward kernel.
 cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);

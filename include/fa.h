@@ -99,21 +99,23 @@ int fa_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE,
 
 /*
  * Split-KV forward pass: the same result as fa_fwd, computed by splitting the
- * keys of every (batch, head) into `num_splits` contiguous ranges (multiples of
- * 128 keys) that run as separate work units, then merging the per-range
+ * keys of every (batch, head) into `num_splits` contiguous ranges (whole K/V
+ * tiles: multiples of 128 keys, of 64 at d = 256) that run as separate work
+ * units, then merging the per-range
  * results with the block merge of the Triton page ("FlashAttention + Triton",
  * section 2.3: m_new = max(m_old, m_block), l and O rescaled by exp(m - m_new)),
  * written in LSE form: LSE = log sum_r exp(LSE_r), O = sum_r exp(LSE_r - LSE) O_r.
- * It raises the number of work units when B*H*ceil(N/256) is small against
- * the number of SMs (long sequences, few heads).
+ * It raises the number of work units when B*H*ceil(N/q) (q = 256 Q rows per
+ * unit; 128 at d = 256) is small against the number of SMs (long sequences,
+ * few heads).
  *
  * Arguments up to `dtype` are those of fa_fwd.
- * num_splits: >= 1 explicit (ranges of whole 128-key tiles, so at most
- *             ceil(N/128); a count that does not divide the tiles evenly
+ * num_splits: >= 1 explicit (ranges of whole K/V tiles, so at most
+ *             ceil(N/128), ceil(N/64) at d = 256; a count that does not divide the tiles evenly
  *             gives ceil(tiles / ceil(tiles / num_splits)) ranges); 0 = chosen from the
  *             shape and the device's SM count (fa_fwd_splitkv_num_splits)
  *             by a cost model, which can also pick the tail plan: when the
- *             B*H*ceil(N/256) work units end in a partial last wave of SMs,
+ *             B*H*ceil(N/q) work units end in a partial last wave of SMs,
  *             the full waves run unsplit and only the last wave's units are
  *             split (as many ways as fit in one wave) and merged; that is
  *             three launches (full waves, split tail, merge of its rows).
@@ -150,7 +152,7 @@ int fa_fwd_splitkv_ex(const void *Q, const void *K, const void *V, void *O, floa
 
 /* The effective split count fa_fwd_splitkv uses for num_splits = 0 on the
  * current device (>= 1: key ranges of each split unit after clamping to whole
- * 128-key tiles; 1 = unsplit), or a negative fa_status on error. Under the
+ * K/V tiles; 1 = unsplit), or a negative fa_status on error. Under the
  * tail plan only the units of the last wave are split this many ways. */
 int fa_fwd_splitkv_num_splits(int B, int H, int N, int d);
 
@@ -168,18 +170,19 @@ int fa_fwd_splitkv_launches(int B, int H, int N, int d, int num_splits);
  * fa_fwd_splitkv_num_splits, fa_fwd_splitkv_launches and
  * fa_fwd_splitkv_workspace_size.
  *
- * Work units are the B*H*ceil(N/256) (batch*head, 256-row Q block) pairs.
+ * Work units are the B*H*ceil(N/q) (batch*head, q-row Q block) pairs, q = 256
+ * (128 at d = 256); K/V tiles hold 128 keys (64 at d = 256).
  * Outputs (all written on success):
  *   splits           key ranges of each split unit after clamping to whole
- *                    128-key tiles (1: nothing is split);
+ *                    K/V tiles (1: nothing is split);
  *   first_split_unit index of the first split unit: 0 when every unit is
- *                    split, B*H*ceil(N/256) when none is, in between under the
+ *                    split, B*H*ceil(N/q) when none is, in between under the
  *                    tail plan (the units of the last, partial wave of SMs);
  *   launches         kernel launches enqueued: 1, 2 or 3;
  *   workspace_bytes  the workspace fa_fwd_splitkv needs (0: none).
  * Errors: FA_ERR_NULL (an output pointer is NULL), FA_ERR_SHAPE (B, H, N or
  * num_sms < 1, num_splits < 0, B*H >= 2^31), FA_ERR_HEADDIM (d not 64, 128 or
- * 256; d = 256 always runs unsplit).
+ * 256).
  */
 int fa_fwd_splitkv_plan(int B, int H, int N, int d, int num_splits, int num_sms, int *splits,
                         long long *first_split_unit, int *launches, unsigned long long *workspace_bytes);
@@ -264,8 +267,8 @@ int fa_bwd(const void *Q, const void *K, const void *V, const void *O, const voi
  *   O_part:   [B, H, Nq, d] fp32 device array (caller-owned): this part's
  *             softmax(scale Q K^T) V over its own keys.
  *   LSE_part: [B, H, Nq] fp32 device array: this part's row logsumexp.
- * No mask. Errors: as fa_fwd (FA_F32 -> FA_ERR_UNSUPPORTED; d must be 64 or
- * 128; Nq, Nk >= 1). One launch on `stream`; nothing is synchronised.
+ * No mask. Errors: as fa_fwd (FA_F32 -> FA_ERR_UNSUPPORTED; d must be 64, 128
+ * or 256; Nq, Nk >= 1). One launch on `stream`; nothing is synchronised.
  */
 int fa_fwd_partial(const void *Q, const void *K, const void *V, float *O_part, float *LSE_part,
                    int B, int H, int Nq, int Nk, int d, float scale, int dtype, void *stream);
@@ -280,7 +283,7 @@ int fa_fwd_partial(const void *Q, const void *K, const void *V, float *O_part, f
  *   O:         [B, H, N, d] device array of `dtype` (FA_F16 or FA_BF16).
  *   LSE:       [B, H, N] fp32 device array.
  * A part with LSE = -inf contributes nothing; a row whose parts are all -inf
- * gets O = 0 and LSE = -inf. d must be 64 or 128. Errors: as fa_fwd
+ * gets O = 0 and LSE = -inf. d must be 64, 128 or 256. Errors: as fa_fwd
  * (FA_F32 -> FA_ERR_UNSUPPORTED). One launch on `stream`.
  */
 int fa_merge(const float *O_parts, const float *LSE_parts, int num_parts, void *O, float *LSE,

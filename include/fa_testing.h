@@ -54,10 +54,10 @@ int fa_bwd_testing(const void *Q, const void *K, const void *V, const void *O, c
  *          then not written and may be NULL. This isolates the fp32
  *          accumulation (S, P.V, l) from the rounding of the stored output,
  *          which for bf16 outputs of |O| ~ 4 alone exceeds 1e-2 (the accuracy
- *          threshold of the dataflow page, section 4.1). d = 64 or 128 only;
- *          otherwise FA_ERR_UNSUPPORTED.
+ *          threshold of the dataflow page, section 4.1). fp16/bf16 and no
+ *          mask, unsplit; otherwise FA_ERR_UNSUPPORTED.
  *  rescale_threshold_log2: the lazy-rescale threshold in log2 units; < 0
- *          takes the built-in 8; 0 rescales O whenever a row's max grows
+ *          takes the built-in 15; 0 rescales O whenever a row's max grows
  *          (the dataflow page, section 2.3). Must lie in [0, 64] otherwise
  *          (FA_ERR_SCALE). Ignored by fp32 inputs, whose rescale is eager.
  *  stats_trace: as in fa_fwd_testing (NULL for none).

@@ -132,7 +132,6 @@ def test_splitkv_launch_count_argument_errors(L):
     assert fa.fa_fwd_splitkv_launches(0, 1, 64, 64, 0) == -fa.FA_ERR_SHAPE
     assert fa.fa_fwd_splitkv_launches(1, 1, 64, 64, -1) == -fa.FA_ERR_SHAPE
     assert fa.fa_fwd_splitkv_launches(1, 1, 64, 96, 0) == -fa.FA_ERR_HEADDIM
-    assert fa.fa_fwd_splitkv_launches(1, 1, 64, 256, 0) == 1  # the d = 256 kernel runs unsplit
 
 
 def test_masked_entry_point_argument_errors(D):
@@ -162,7 +161,7 @@ def test_partial_and_merge_argument_errors(D):
     assert part(dtype=7) == fa.FA_ERR_DTYPE
     assert part(Nk=0) == fa.FA_ERR_SHAPE
     assert part(Nq=0) == fa.FA_ERR_SHAPE
-    assert part(d=256) == fa.FA_ERR_HEADDIM
+    assert part(d=96) == fa.FA_ERR_HEADDIM
     assert part(scale=-1.0) == fa.FA_ERR_SCALE
     assert part(Op=A + 4) == fa.FA_ERR_ALIGN
     #                Op Lp P  O  L  B  H  N   d   dtype
@@ -218,10 +217,12 @@ def test_backward_argument_errors_return_before_launch(D, change, code):
 
 
 def test_d256_split_queries(L):
-    """d = 256 runs unsplit: the automatic split count is 1 and no workspace is needed."""
-    assert fa.fa_fwd_splitkv_num_splits(1, 8, 16384, 256) == 1
-    assert fa.fa_fwd_splitkv_workspace_size(1, 8, 16384, 256, 4) == 0
-    assert fa.fa_bwd_workspace_size(1, 8, 1024, 256) == 0  # the backward takes d = 64 / 128 only
+    """d = 256 splits over 64-key tiles (128-row Q tiles): an explicit count
+    needs partial rows for every row; the backward takes d = 64 / 128 only."""
+    assert fa.fa_fwd_splitkv_workspace_size(1, 8, 16384, 256, 4) == _partials_bytes(4 * 8 * 16384, 256)
+    # N = 300 has 5 tiles of 64 keys: a request for 9 ranges gets 5
+    assert fa.fa_fwd_splitkv_workspace_size(1, 1, 300, 256, 9) == _partials_bytes(5 * 300, 256)
+    assert fa.fa_bwd_workspace_size(1, 8, 1024, 256) == 0
 
 
 def _partials_bytes(rows, d):
@@ -229,28 +230,34 @@ def _partials_bytes(rows, d):
     return (rows * d * 4 + 255) // 256 * 256 + rows * 4
 
 
+def _unit_shape(d):
+    """(Q rows per work unit, keys per K/V tile) of the 16-bit forward kernels."""
+    return (128, 64) if d == 256 else (256, 128)
+
+
 def _tail_expectation(B, H, N, d, num_sms):
-    """The wave-tail plan written out: the full waves of 256-row Q blocks run
-    unsplit, the units of the last partial wave are split as many ways as fit
-    in one wave (at most 16, at most one range per 128-key tile), and only
-    their rows need partial buffers."""
-    nqb = -(-N // 256)
+    """The wave-tail plan written out: the full waves of Q blocks run unsplit,
+    the units of the last partial wave are split as many ways as fit in one
+    wave (at most 16, at most one range per K/V tile), and only their rows
+    need partial buffers."""
+    qr, kt = _unit_shape(d)
+    nqb = -(-N // qr)
     units = B * H * nqb
     full, tail = divmod(units, num_sms)
-    tiles = -(-N // 128)
+    tiles = -(-N // kt)
     s = min(num_sms // tail, tiles, 16)
     per = -(-tiles // s)
     s = -(-tiles // per)
     first = full * num_sms
-    row0 = (first // nqb) * N + (first % nqb) * 256
+    row0 = (first // nqb) * N + (first % nqb) * qr
     return s, first, _partials_bytes(s * (B * H * N - row0), d)
 
 
 @pytest.mark.parametrize("B,H,N,d,num_sms", [
     (1, 8, 16384, 128, 152),   # 512 units: 3 full waves, 56 left split 2 ways
     (1, 8, 16384, 128, 148),   # 68 left, split 2 ways
-    (8, 12, 2048, 128, 152),   # 768 units: 5 full waves, 8 left split 16 ways
     (1, 4, 10240, 128, 152),   # 160 units: 1 full wave, 8 left split 16 ways
+    (1, 4, 16384, 256, 152),   # d = 256: 512 units of 128 rows, 3 full waves, 56 left split 2 ways
 ])
 def test_splitkv_plan_tail_on_the_host(L, B, H, N, d, num_sms):
     rc, p = fa.fa_fwd_splitkv_plan(B, H, N, d, 0, num_sms)
@@ -271,10 +278,21 @@ def test_splitkv_plan_uniform_and_unsplit_on_the_host(L):
     # 4096 units on 152 SMs: the last wave is nearly full (144 units), no split pays
     rc, p = fa.fa_fwd_splitkv_plan(8, 32, 4096, 128, 0, 152)
     assert p == {"splits": 1, "first_split_unit": 4096, "launches": 1, "workspace_bytes": 0}
-    # d = 256 always runs unsplit; an explicit count of 1 too
-    for args in [(4, 16, 4096, 256, 0, 152), (4, 16, 4096, 256, 8, 152), (2, 2, 1000, 128, 1, 152)]:
+    # a short last wave whose split saves less than the launch boundary costs:
+    # d = 256, B=4 H=16 N=4096 (2048 units, 13.5 waves) and d = 128, B=8 H=12
+    # N=2048 (768 units, 5.05 waves)
+    rc, p = fa.fa_fwd_splitkv_plan(4, 16, 4096, 256, 0, 152)
+    assert p == {"splits": 1, "first_split_unit": 2048, "launches": 1, "workspace_bytes": 0}
+    rc, p = fa.fa_fwd_splitkv_plan(8, 12, 2048, 128, 0, 152)
+    assert p == {"splits": 1, "first_split_unit": 768, "launches": 1, "workspace_bytes": 0}
+    # d = 256: explicit counts over 64-key tiles
+    rc, p = fa.fa_fwd_splitkv_plan(4, 16, 4096, 256, 8, 152)
+    assert p == {"splits": 8, "first_split_unit": 0, "launches": 2,
+                 "workspace_bytes": _partials_bytes(8 * 64 * 4096, 256)}
+    # an explicit count of 1 never splits
+    for args in [(2, 2, 1000, 128, 1, 152), (2, 2, 1000, 256, 1, 152)]:
         rc, p = fa.fa_fwd_splitkv_plan(*args)
-        units = args[0] * args[1] * -(-args[2] // 256)
+        units = args[0] * args[1] * -(-args[2] // _unit_shape(args[3])[0])
         assert rc == fa.FA_OK and p == {"splits": 1, "first_split_unit": units, "launches": 1, "workspace_bytes": 0}
 
 
@@ -283,21 +301,22 @@ def test_splitkv_plan_invariants_over_shapes(L):
     but not all units are split, and the workspace covers exactly the split
     units' rows, one span per key range."""
     for B, H, N in [(1, 1, 64), (1, 2, 1000), (2, 3, 4097), (1, 8, 16384), (3, 5, 777), (16, 16, 512), (1, 1, 65536)]:
-        for d in (64, 128):
+        for d in (64, 128, 256):
+            qr, kt = _unit_shape(d)
             for num_sms in (1, 7, 132, 148, 152, 1000):
                 for ns in (0, 1, 2, 5):
                     rc, p = fa.fa_fwd_splitkv_plan(B, H, N, d, ns, num_sms)
                     assert rc == fa.FA_OK
-                    nqb = -(-N // 256)
+                    nqb = -(-N // qr)
                     units = B * H * nqb
                     first, s = p["first_split_unit"], p["splits"]
                     if s == 1:
                         assert first == units and p["launches"] == 1 and p["workspace_bytes"] == 0
                         continue
-                    assert 1 < s <= max(ns, 16) and s <= -(-N // 128)
+                    assert 1 < s <= max(ns, 16) and s <= -(-N // kt)
                     assert p["launches"] == (3 if 0 < first < units else 2)
                     assert ns == 0 or first == 0
-                    row0 = (first // nqb) * N + (first % nqb) * 256
+                    row0 = (first // nqb) * N + (first % nqb) * qr
                     assert p["workspace_bytes"] == _partials_bytes(s * (B * H * N - row0), d)
 
 

@@ -104,6 +104,8 @@ def _gpu():
     (2, 1, 1000, 700, 64, "f16", 1.0),
     (1, 3, 64, 1, 128, "f16", 1.0),
     (1, 1, 257, 2048, 128, "bf16", 2.0),
+    (1, 2, 300, 129, 256, "bf16", 3.0),
+    (2, 1, 200, 1000, 256, "f16", 1.0),
 ])
 def test_partial_against_oracle_on_one_key_shard(B, H, Nq, Nk, d, dtype, sig):
     """Normalised fp32 O of one part: max error 1e-2, cosine 0.999 (P is
@@ -130,6 +132,7 @@ def test_partial_against_oracle_on_one_key_shard(B, H, Nq, Nk, d, dtype, sig):
     (2, 2, 777, 64, "f16", 1.0, 3),
     (1, 1, 4096, 128, "bf16", 3.0, 4),
     (1, 2, 130, 128, "f16", 1.0, 5),   # shards of 26 keys
+    (1, 2, 1000, 256, "bf16", 3.0, 3),
 ])
 def test_shards_merged_equal_attention_over_all_keys(B, H, N, d, dtype, sig, parts):
     from parity_util import compare

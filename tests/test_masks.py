@@ -72,7 +72,7 @@ def test_padded_keys_need_not_be_finite():
     assert res["ok"], res
 
 
-@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (64, "f16")])
+@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (64, "f16"), (256, "bf16")])
 @pytest.mark.parametrize("splits", [2, 3, 0])
 @pytest.mark.parametrize("causal,klen", [(True, None), (False, [700, 1, 129, 256, 0]),
                                          (True, [600, 300, 77, 0, 700])], ids=["causal", "lengths", "both"])

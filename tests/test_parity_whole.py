@@ -63,9 +63,10 @@ def test_whole_workload_bench_launch_configuration(name):
     assert res["ok"], res
 
 
-@pytest.mark.parametrize("name", ["b8h12n2048d128_f16", "b1h8n16384d128_bf16"])
+@pytest.mark.parametrize("name", ["b8h12n2048d128_f16", "b1h8n16384d128_bf16", "b4h16n4096d256_bf16"])
 def test_whole_workload_unsplit(name):
-    """The same workloads as one unsplit launch (their automatic plan splits the wave tail)."""
+    """The same workloads as one unsplit launch (the long-sequence workload's
+    automatic plan splits the wave tail)."""
     w, (q, k, v), (qd, kd, vd) = inputs(name)
     o, lse = run_product(qd, kd, vd, w, 1)
     o_ref, lse_ref, _ = oracle_full(w, q, k, v)
@@ -73,7 +74,8 @@ def test_whole_workload_unsplit(name):
     assert res["ok"], res
 
 
-@pytest.mark.parametrize("name", ["b8h32n4096d128_bf16_qk3", "b1h8n16384d128_bf16", "b8h12n2048d128_f16"])
+@pytest.mark.parametrize("name", ["b8h32n4096d128_bf16_qk3", "b1h8n16384d128_bf16", "b8h12n2048d128_f16",
+                                  "b4h16n4096d256_bf16"])
 def test_whole_fp32_output_strict_gate(name):
     """O written as fp32 before the rounding to the input type (testing build):
     the raw 1e-2 threshold holds for the accumulation itself, with no

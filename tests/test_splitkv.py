@@ -22,6 +22,10 @@ pytestmark = pytest.mark.gpu
     (2, 1, 2048, 64, "bf16", 1.0, 5),
     (1, 1, 300, 64, "f16", 2.0, 9),      # clamped to 3 ranges, the last one ragged
     (1, 2, 4096, 128, "bf16", 3.0, 0),   # automatic count
+    (1, 2, 1000, 256, "bf16", 3.0, 2),   # d = 256: 128-row Q tiles, 64-key tiles
+    (2, 1, 1111, 256, "f16", 1.0, 4),
+    (1, 1, 300, 256, "bf16", 2.0, 9),    # 5 tiles of 64 keys: clamped to 5 ranges, the last one ragged
+    (1, 3, 2048, 256, "bf16", 3.0, 0),   # automatic count (24 units on 152 SMs: split)
 ])
 def test_splitkv_parity(B, H, N, d, dtype, sig, splits):
     q, k, v = make_qkv(B, H, N, d, dtype, sigma_qk=sig, seed=17, wid=11000 + N + splits)
@@ -69,7 +73,7 @@ def test_splitkv_workspace_errors():
 @pytest.mark.parametrize("B,H,N,d,dtype", [
     (1, 4, 10240, 128, "bf16"),   # 160 units: on 152 SMs one full wave, the 8 left over split 16 ways
     (1, 2, 20000, 128, "f16"),    # N not a multiple of 256: the last Q block of a head is partial
-    (8, 12, 2048, 128, "f16"),    # 768 units: on 152 SMs 5 full waves, the 8 left over split 16 ways
+    (1, 4, 16384, 256, "bf16"),   # d = 256: 512 units of 128 rows, 3 full waves, the 56 left split 2 ways
 ])
 def test_splitkv_tail_plan(B, H, N, d, dtype):
     """num_splits = 0 on shapes whose units end in a partial last wave: the
@@ -132,7 +136,6 @@ def test_splitkv_plan_matches_the_device_queries():
             rc, p = fa.fa_fwd_splitkv_plan(B, H, N, d, ns, sms)
             assert rc == fa.FA_OK
             assert p["launches"] == fa.fa_fwd_splitkv_launches(B, H, N, d, ns)
-            if d != 256:
-                assert p["workspace_bytes"] == fa.fa_fwd_splitkv_workspace_size(B, H, N, d, ns)
+            assert p["workspace_bytes"] == fa.fa_fwd_splitkv_workspace_size(B, H, N, d, ns)
             if ns == 0:
                 assert p["splits"] == fa.fa_fwd_splitkv_num_splits(B, H, N, d)

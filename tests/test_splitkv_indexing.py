@@ -2,9 +2,10 @@
 the merge, restated from the kernels' index expressions and checked on the
 CPU against the workspace the host plans (`fa_fwd_splitkv_plan`).
 
-Work unit u covers Q block u % nqb of head u // nqb (256 rows). Under a plan
-whose split units start at unit `first`, their rows start at
-row0 = (first // nqb) * N + (first % nqb) * 256, and the epilogue of key
+Work unit u covers Q block u % nqb of head u // nqb (q = 256 rows; 128 at
+head dimension 256). Under a plan whose split units start at unit `first`,
+their rows start at row0 = (first // nqb) * N + (first % nqb) * q, and the
+epilogue of key
 range s writes row r (< N) of head bh to partial row
 s * (B*H*N - row0) + (bh * N + r - row0). The merge reads, for every output
 row from row0 on, the same index for each s. The check: over every split
@@ -33,16 +34,22 @@ def _qblock(u, nqb, causal, num_splits, qunit_count):
     return nqb - 1 - u % nqb if heavy_first else u % nqb
 
 
-def _written(B, H, N, first, splits, causal=False):
-    nqb = -(-N // 256)
+def _qrows(d):
+    """Q rows of one work unit: two 128-row sub-tiles, or one tile at d = 256."""
+    return 128 if d == 256 else 256
+
+
+def _written(B, H, N, first, splits, causal=False, d=128):
+    q = _qrows(d)
+    nqb = -(-N // q)
     units = B * H * nqb
-    row0 = (first // nqb) * N + (first % nqb) * 256
+    row0 = (first // nqb) * N + (first % nqb) * q
     span = B * H * N - row0
     idx = []
     for u in range(first, units):
         bh = u // nqb
         qb = _qblock(u, nqb, causal, splits, units - first)
-        rows = np.arange(qb * 256, min(qb * 256 + 256, N))
+        rows = np.arange(qb * q, min(qb * q + q, N))
         for s in range(splits):
             idx.append(s * span + (bh * N + rows - row0))
     return np.concatenate(idx) if idx else np.zeros(0, dtype=np.int64), row0, span
@@ -51,6 +58,7 @@ def _written(B, H, N, first, splits, causal=False):
 @pytest.mark.parametrize("B,H,N,d,num_sms", [
     (1, 8, 16384, 128, 152), (1, 8, 16384, 128, 148), (8, 12, 2048, 128, 152), (1, 4, 10240, 128, 152),
     (1, 2, 20000, 128, 152), (3, 5, 1000, 64, 7), (2, 3, 4097, 64, 13), (1, 1, 300, 64, 1),
+    (4, 16, 4096, 256, 152), (1, 4, 16384, 256, 152), (2, 3, 1000, 256, 7), (1, 1, 300, 256, 1),
 ])
 @pytest.mark.parametrize("num_splits", [0, 2, 5])
 @pytest.mark.parametrize("causal", [False, True])
@@ -63,7 +71,7 @@ def test_partial_rows_tile_the_planned_workspace(L, B, H, N, d, num_sms, num_spl
     if p["splits"] == 1:
         assert p["workspace_bytes"] == 0
         return
-    idx, row0, span = _written(B, H, N, p["first_split_unit"], p["splits"], causal)
+    idx, row0, span = _written(B, H, N, p["first_split_unit"], p["splits"], causal, d)
     # every partial row exactly once, no gap, no overlap
     assert len(idx) == p["splits"] * span
     assert np.array_equal(np.sort(idx), np.arange(p["splits"] * span))
@@ -74,9 +82,10 @@ def test_partial_rows_tile_the_planned_workspace(L, B, H, N, d, num_sms, num_spl
     merge = np.concatenate([s * span + np.arange(span) for s in range(p["splits"])])
     assert np.array_equal(np.sort(merge), np.sort(idx))
     # and the merged rows are exactly the split units' rows
-    nqb = -(-N // 256)
+    q = _qrows(d)
+    nqb = -(-N // q)
     first = p["first_split_unit"]
-    assert row0 == (first // nqb) * N + (first % nqb) * 256 and span == B * H * N - row0
+    assert row0 == (first // nqb) * N + (first % nqb) * q and span == B * H * N - row0
 
 
 def test_heavy_first_order_would_break_the_tail_plan():
