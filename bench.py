@@ -39,6 +39,8 @@ KERNEL_SOURCES = {
     "fwd": ["exact_attention_87_gb300/csrc/fa_fwd_f16.cu"] + COMMON_SOURCES,
     "fwd_d256": ["exact_attention_87_gb300/csrc/fa_fwd_d256.cu"] + COMMON_SOURCES,
     "bwd": ["exact_attention_87_gb300/csrc/fa_bwd_f16.cu"] + COMMON_SOURCES,
+    "bwd_d256": ["exact_attention_87_gb300/csrc/fa_bwd_f16.cu", "exact_attention_87_gb300/csrc/fa_bwd_d256.cu"]
+    + COMMON_SOURCES,
 }
 
 
@@ -700,11 +702,12 @@ def run_backward(args, w, cfg, ws, rank, local):
         "pct_of_datasheet_peak": round(100.0 * achieved / DATASHEET_TFLOPS, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                     "kernel": "whole step: fa_bwd_pre + fa_bwd_main + fa_bwd_post",
-                     "traffic": None if causal else recorded_traffic(w.name, "bwd"),
+                     "kernel": ("whole step: fa_bwd_pre + fa_bwd_dv256 + fa_bwd_dkdq256 + fa_bwd_post" if w.d == 256
+                                else "whole step: fa_bwd_pre + fa_bwd_main + fa_bwd_post"),
+                     "traffic": None if causal else recorded_traffic(w.name, "bwd_d256" if w.d == 256 else "bwd"),
                      "algorithmic_bytes": 8 * w.B * w.H * w.N * w.d * es + 4 * w.B * w.H * w.N},
         "clocks": sampler.summary(),
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (4 if w.d == 256 else 3) * args.steps,
         "e2e": e2e,
     }
     if ws == 1 and not args.no_cpu_baseline:

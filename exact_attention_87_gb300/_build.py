@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
-SOURCES = ["fa_api.cu", "fa_fwd_f16.cu", "fa_fwd_f32.cu", "fa_fwd_d256.cu", "fa_bwd_f16.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd_f16.cu", "fa_fwd_f32.cu", "fa_fwd_d256.cu", "fa_bwd_f16.cu", "fa_bwd_d256.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-diag-suppress", "1160",
          "-I", INCLUDE, "-I", CSRC]

@@ -621,7 +621,7 @@ int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const v
   if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
   if (dtype == FA_F32) return FA_ERR_UNSUPPORTED;
   if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
-  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_HEADDIM;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
   const long long BH = static_cast<long long>(B) * H;
   if (BH > 0x7fffffffLL || BH * N > (1ll << 40) / d) return FA_ERR_SHAPE;
@@ -664,10 +664,12 @@ int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const v
 
   const CUtensorMapDataType dt = dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const int bh = static_cast<int>(BH);
-  if (!encode_bhnd_16bit(&p.tm_q, Q, bh, N, d, dt, fa::kF16BlockQ) ||
+  // Q tiles of the backward: 128 rows (64 at d = 256); key tiles: 128 rows.
+  const int q_rows = d == 256 ? 64 : fa::kF16BlockQ;
+  if (!encode_bhnd_16bit(&p.tm_q, Q, bh, N, d, dt, q_rows) ||
       !encode_bhnd_16bit(&p.tm_k, K, bh, N, d, dt, fa::kF16BlockKV) ||
       !encode_bhnd_16bit(&p.tm_v, V, bh, N, d, dt, fa::kF16BlockKV) ||
-      !encode_bhnd_16bit(&p.tm_do, dO, bh, N, d, dt, fa::kF16BlockQ) ||
+      !encode_bhnd_16bit(&p.tm_do, dO, bh, N, d, dt, q_rows) ||
       !encode_bhnd_16bit(&p.tm_dk, dK, bh, N, d, dt, fa::kF16BlockKV) ||
       !encode_bhnd_16bit(&p.tm_dv, dV, bh, N, d, dt, fa::kF16BlockKV) ||
       !encode_bhnd_f32_box32(&p.tm_dqacc, p.dq_acc, bh, N, d))
@@ -682,7 +684,7 @@ int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const v
 extern "C" {
 
 unsigned long long fa_bwd_workspace_size(int B, int H, int N, int d) {
-  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128 && d != 256)) return 0;
   const unsigned long long bh = static_cast<unsigned long long>(B) * H;
   const unsigned long long n_pad = static_cast<unsigned long long>(bwd_tiles(N)) * fa::kF16BlockKV;
   return bwd_part_bytes(bh * N * d * 4) + 2 * bwd_part_bytes(bh * n_pad * 4);

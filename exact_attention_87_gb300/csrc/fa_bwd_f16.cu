@@ -810,9 +810,28 @@ cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// d = 256: the same row statistics and dQ rounding around the two main
+// kernels of fa_bwd_d256.cu.
+template <bool BF16>
+cudaError_t launch_bwd_d256_t(const BwdParams& p, cudaStream_t stream) {
+  const long long bh = static_cast<long long>(p.B) * p.H;
+  const long long pre_threads = bh * p.n_pad * (256 / 8);
+  const long long post_threads = bh * p.N * 256 / 8;
+  if ((pre_threads + 255) / 256 > 0x7fffffffLL || (post_threads + 255) / 256 > 0x7fffffffLL)
+    return cudaErrorInvalidValue;
+  fa_bwd_pre_kernel<256, BF16><<<dim3(static_cast<unsigned>((pre_threads + 255) / 256)), dim3(256), 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_bwd_main_d256(p, BF16, stream);
+  if (e != cudaSuccess) return e;
+  fa_bwd_post_kernel<BF16><<<dim3(static_cast<unsigned>((post_threads + 255) / 256)), dim3(256), 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_f16(const BwdParams& p, bool bf16, cudaStream_t stream) {
+  if (p.d == 256) return bf16 ? launch_bwd_d256_t<true>(p, stream) : launch_bwd_d256_t<false>(p, stream);
   if (p.d == 128) return bf16 ? launch_bwd_t<128, true>(p, stream) : launch_bwd_t<128, false>(p, stream);
   if (p.d == 64) return bf16 ? launch_bwd_t<64, true>(p, stream) : launch_bwd_t<64, false>(p, stream);
   return cudaErrorInvalidValue;

@@ -150,7 +150,11 @@ cudaError_t launch_fwd_f16(const FwdParams& p, bool bf16, cudaStream_t stream);
 cudaError_t launch_merge(const FwdParams& p, bool bf16, cudaStream_t stream);
 // Backward: row statistics (D, LSE * log2 e) and a zeroed dQ accumulator;
 // the main dK/dV/dQ kernel; the dQ accumulator rounded into dQ.
+// Head dimension 64, 128 or 256 (the last through launch_bwd_main_d256).
 cudaError_t launch_bwd_f16(const BwdParams& p, bool bf16, cudaStream_t stream);
+// The two main kernels of the d = 256 backward (dV; then dK and the dQ
+// contributions), between the row statistics and the dQ rounding.
+cudaError_t launch_bwd_main_d256(const BwdParams& p, bool bf16, cudaStream_t stream);
 // Launch the 16-bit forward kernel for head dimension 256 (same parameter
 // block and work-unit scheme as launch_fwd_f16, with 128-row Q tiles and
 // 64-key K/V tiles).

@@ -39,7 +39,7 @@ typedef enum {
     FA_ERR_NULL = 1,           /* a required pointer is NULL                         */
     FA_ERR_DTYPE = 2,          /* dtype is not one of fa_dtype                       */
     FA_ERR_SHAPE = 3,          /* B, H or N < 1, or B*H*N*d overflows 2^40 elements  */
-    FA_ERR_HEADDIM = 4,        /* d is not 64 or 128 (or 256, 16-bit forward only)   */
+    FA_ERR_HEADDIM = 4,        /* d is not 64 or 128 (or 256, 16-bit types only)     */
     FA_ERR_ALIGN = 5,          /* a base pointer is not 16-byte aligned              */
     FA_ERR_CUDA = 6,           /* a CUDA runtime/driver call failed (launch, query)  */
     FA_ERR_DEVICE_TIMEOUT = 7, /* a kernel gave up waiting on a pipeline barrier     */
@@ -244,6 +244,10 @@ int fa_fwd_splitkv_noalloc(const void *Q, const void *K, const void *V, void *O,
  *             the tensor cores with fp32 accumulation; P and dS*scale are
  *             rounded to `dtype` before they enter a product; dQ is
  *             accumulated in fp32 and rounded once at the end.
+ * d:          64, 128 or 256. At d = 256 the pass runs two main kernels (dV,
+ *             then dK with the dQ contributions: dK and dV do not fit the
+ *             tensor memory together) with 64-row Q tiles; S^T is computed
+ *             in both.
  * workspace:  device memory owned by the caller, 256-byte aligned, at least
  *             fa_bwd_workspace_size(B, H, N, d) bytes: the fp32 dQ
  *             accumulator and two fp32 values per row. Its contents need not
@@ -251,7 +255,8 @@ int fa_fwd_splitkv_noalloc(const void *Q, const void *K, const void *V, void *O,
  * Other arguments: as fa_fwd.
  * Errors: those of fa_fwd (checked before anything is enqueued), plus
  * FA_ERR_WORKSPACE and FA_ERR_UNSUPPORTED. Three launches are enqueued on
- * `stream` (row statistics, main pass, dQ rounding); nothing is synchronised.
+ * `stream` (row statistics, main pass, dQ rounding; four at d = 256);
+ * nothing is synchronised.
  */
 int fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *LSE,
            void *dQ, void *dK, void *dV, int B, int H, int N, int d, float scale, int dtype,

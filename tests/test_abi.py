@@ -143,7 +143,7 @@ def test_masked_entry_point_argument_errors(D):
     assert D.fa_bwd_ex(*args, -1, None, 1 << 24, ws, None) == fa.FA_ERR_SHAPE
     assert D.fa_bwd_ex(*([0] + args[1:]), 1, None, 1 << 24, ws, None) == fa.FA_ERR_NULL
     assert D.fa_bwd_ex(*args, 1, None, 0, ws, None) == fa.FA_ERR_WORKSPACE
-    assert D.fa_bwd_ex(*(args[:12] + [256, 0.125, fa.FA_F16]), 1, None, 1 << 24, ws, None) == fa.FA_ERR_HEADDIM
+    assert D.fa_bwd_ex(*(args[:12] + [96, 0.125, fa.FA_F16]), 1, None, 1 << 24, ws, None) == fa.FA_ERR_HEADDIM
 
 
 def test_partial_and_merge_argument_errors(D):
@@ -200,7 +200,7 @@ W = 1 << 24  # placeholder workspace address, 256-byte aligned (dry runs only)
     ({"dtype": 9}, fa.FA_ERR_DTYPE),
     ({"dtype": fa.FA_F32}, fa.FA_ERR_UNSUPPORTED),
     ({"N": 0}, fa.FA_ERR_SHAPE),
-    ({"d": 256}, fa.FA_ERR_HEADDIM),
+    ({"d": 96}, fa.FA_ERR_HEADDIM),
     ({"scale": float("inf")}, fa.FA_ERR_SCALE),
     ({"dK": A + 8}, fa.FA_ERR_ALIGN),
     ({"LSE": A + 2}, fa.FA_ERR_ALIGN),
@@ -218,11 +218,13 @@ def test_backward_argument_errors_return_before_launch(D, change, code):
 
 def test_d256_split_queries(L):
     """d = 256 splits over 64-key tiles (128-row Q tiles): an explicit count
-    needs partial rows for every row; the backward takes d = 64 / 128 only."""
+    needs partial rows for every row."""
     assert fa.fa_fwd_splitkv_workspace_size(1, 8, 16384, 256, 4) == _partials_bytes(4 * 8 * 16384, 256)
     # N = 300 has 5 tiles of 64 keys: a request for 9 ranges gets 5
     assert fa.fa_fwd_splitkv_workspace_size(1, 1, 300, 256, 9) == _partials_bytes(5 * 300, 256)
-    assert fa.fa_bwd_workspace_size(1, 8, 1024, 256) == 0
+    # the backward at d = 256: fp32 dQ accumulator and two rows of statistics
+    assert fa.fa_bwd_workspace_size(1, 8, 1000, 256) == \
+        (8 * 1000 * 256 * 4 + 255) // 256 * 256 + 2 * ((8 * 1024 * 4 + 255) // 256 * 256)
 
 
 def _partials_bytes(rows, d):

@@ -83,6 +83,13 @@ SMALL = [
     (1, 2, 640, 128, "bf16", 3.0),
     (1, 1, 1000, 64, "bf16", 2.0),
     (3, 5, 64, 64, "f16", 1.0),
+    # d = 256: two main kernels, 64-row Q tiles
+    (1, 1, 1, 256, "bf16", 1.0),
+    (1, 2, 128, 256, "bf16", 1.0),
+    (1, 1, 129, 256, "f16", 1.0),
+    (2, 2, 300, 256, "bf16", 2.0),
+    (1, 2, 640, 256, "bf16", 3.0),
+    (2, 1, 1000, 256, "f16", 1.0),
 ]
 
 
@@ -91,21 +98,23 @@ def test_backward_small_shapes(B, H, N, d, dtype, sig):
     check(B, H, N, d, dtype, sig, wid=8000 + N + d)
 
 
-@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (64, "f16")])
+@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (64, "f16"), (256, "bf16")])
 def test_backward_rising_key_norms(d, dtype):
     """sigma 3 with keys sorted by norm: sharply peaked rows, P near 0 and 1."""
     check(1, 2, 768, d, dtype, 3.0, wid=8100 + d, order=True)
 
 
-def test_backward_non_default_scale():
-    check(1, 2, 300, 128, "bf16", 1.0, wid=8200, scale=0.3)
+@pytest.mark.parametrize("d", [128, 256])
+def test_backward_non_default_scale(d):
+    check(1, 2, 300, d, "bf16", 1.0, wid=8200, scale=0.3)
 
 
-def test_backward_deterministic():
+@pytest.mark.parametrize("d", [128, 256])
+def test_backward_deterministic(d):
     """dK and dV are written once per key tile; dQ is a sum of fp32 reduce-adds
     over key tiles, whose order can vary: it must agree to fp32 rounding."""
-    q, k, v = (t.cuda() for t in make_qkv(1, 4, 700, 128, "bf16", sigma_qk=2.0, seed=1, wid=8300))
-    do = make_dout(1, 4, 700, 128, "bf16", seed=1, wid=8300).cuda()
+    q, k, v = (t.cuda() for t in make_qkv(1, 4, 700, d, "bf16", sigma_qk=2.0, seed=1, wid=8300))
+    do = make_dout(1, 4, 700, d, "bf16", seed=1, wid=8300).cuda()
     o, lse = fa.attention(q, k, v)
     ref = [t.clone() for t in fa.attention_backward(q, k, v, o, lse, do)]
     for _ in range(3):
@@ -164,3 +173,33 @@ def test_backward_full_workload_sampled():
         gate(gq, rq, f"dQ head {b},{h}")
         gate(gk, rk, f"dK head {b},{h}")
         gate(gv, rv, f"dV head {b},{h}")
+
+
+def test_backward_d256_workload_sampled():
+    """The head-dimension-256 workload (B=4, H=16, N=4096, bf16): sampled rows
+    of two heads against the oracle, sum identities for every head."""
+    w = WORKLOADS["b4h16n4096d256_bf16"]
+    q, k, v = make_inputs(w)
+    do = make_dout(w.B, w.H, w.N, w.d, w.dtype, seed=0, wid=w.wid)
+    qc, kc, vc, dc = (t.cuda() for t in (q, k, v, do))
+    o, lse = fa.attention(qc, kc, vc)
+    dq, dk, dv = fa.attention_backward(qc, kc, vc, o, lse, dc)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    for t in (dq, dk, dv):
+        assert bool(torch.isfinite(t).all())
+    sv = dv.double().sum(dim=2)
+    assert (sv - dc.double().sum(dim=2)).abs().max().item() <= 1e-2 * dv.double().abs().sum(dim=2).max().item()
+    sk = dk.double().sum(dim=2)
+    assert sk.abs().max().item() <= 1e-2 * dk.double().abs().sum(dim=2).max().item()
+    rng = np.random.default_rng(w.wid)
+    for b, h in [(0, 0), (3, 15)]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        qh, kh, vh, dh = (t[sl] for t in (q, k, v, do))
+        oh, lh = oracle.attn(qh, kh, vh)
+        idx = sorted({0, 1, 63, 64, 127, 128, w.N - 1, *rng.integers(0, w.N, 25).tolist()})
+        rows = [(0, 0, i) for i in idx]
+        rq, rk, rv = oracle.attn_bwd_rows(qh, kh, vh, oh, dh, lh, rows, rows)
+        gate(dq[b, h, idx].cpu().double().numpy(), rq, f"dQ head {b},{h}")
+        gate(dk[b, h, idx].cpu().double().numpy(), rk, f"dK head {b},{h}")
+        gate(dv[b, h, idx].cpu().double().numpy(), rv, f"dV head {b},{h}")

@@ -85,6 +85,9 @@ CAUSAL = [
     (2, 2, 383, 128, "f16", 1.0),
     (1, 2, 640, 128, "bf16", 3.0),
     (1, 1, 1000, 64, "bf16", 2.0),
+    (1, 1, 65, 256, "bf16", 1.0),
+    (2, 2, 300, 256, "bf16", 2.0),
+    (1, 1, 640, 256, "f16", 1.0),
 ]
 
 
@@ -100,6 +103,8 @@ KLEN = [
     (2, 3, 513, 128, "bf16", False, [1000, -4]),
     (3, 2, 300, 128, "f16", True, [300, 200, 0]),
     (2, 2, 640, 64, "bf16", True, [257, 640]),
+    (3, 2, 300, 256, "bf16", False, [300, 64, 0]),
+    (2, 2, 333, 256, "f16", True, [200, 333]),
 ]
 
 
