@@ -626,3 +626,254 @@ def test_model_catches_dp_overwriting_dq():
     with pytest.raises(AssertionError, match="dQ before it was read out"):
         for seed in range(100):
             NoDqWait(6, 128, False, random.Random(seed)).run()
+
+
+class Bwd256DvModel(BwdModel):
+    """`fa_bwd_dv256_kernel`: the producer (K once; Q_i with its LSE row and
+    dO_i in 2-stage rings, Q stages freed by the four softmax warps once they
+    have read the LSE row), the MMA warp (S^T_0, S^T_1, then dV_i and S^T_{i+2}
+    into the buffer of P^T_i right behind it) and four softmax warps (P^T_i
+    over S buffer i % 2)."""
+
+    def __init__(self, nq, strict, rng):
+        BwdModel.__init__(self, nq, 128, strict, rng)
+        self.QST = self.OST = 2
+        self.qstage, self.ostage = [None] * 2, [None] * 2
+        self.bars = {"K": Bar(1), "DONE": Bar(1), "DR": Bar(1)}
+        for s in range(2):
+            self.bars.update({f"QF{s}": Bar(1), f"QE{s}": Bar(4), f"OF{s}": Bar(1), f"OE{s}": Bar(1),
+                              f"SF{s}": Bar(1), f"PF{s}": Bar(4)})
+
+    def roles(self):
+        return [self.producer(), self.mma()] + [self.softmax(w) for w in range(4)]
+
+    def producer(self):
+        self.landing.append(("K", 0, 0, "K"))
+        for i in range(self.nq):
+            s = i % 2
+            yield ("wait", f"QE{s}", i // 2 - 1)
+            if i >= 2:
+                assert ("S", i - 2) in self.mma_done and self.count.get(("p", i - 2), 0) == 4, "Q stage reloaded early"
+            self.qstage[s] = None
+            self.landing.append(("Q", s, i, f"QF{s}"))
+            yield ("step",)
+            yield ("wait", f"OE{s}", i // 2 - 1)
+            if i >= 2:
+                assert ("DV", i - 2) in self.mma_done, "dO stage reloaded early"
+            self.ostage[s] = None
+            self.landing.append(("O", s, i, f"OF{s}"))
+            yield ("step",)
+
+    def mma(self):
+        nq = self.nq
+        if nq > 0:
+            yield ("wait", "K", 0)
+            for i in range(min(nq, 2)):
+                yield ("wait", f"QF{i % 2}", i // 2)
+                self.issue(0, "S", i)
+                self.commit(0, f"SF{i & 1}")
+                yield ("step",)
+            for i in range(nq):
+                s = i % 2
+                yield ("wait", f"OF{s}", i // 2)
+                yield ("wait", f"PF{i & 1}", i // 2)
+                self.issue(0, "DV", i)
+                self.commit(0, f"OE{s}")
+                if i == nq - 1:
+                    self.commit(0, "DONE")
+                yield ("step",)
+                if i + 2 < nq:
+                    n = i + 2
+                    if self.STRICT:
+                        yield ("wait", f"OE{s}", i // 2)
+                    yield ("wait", f"QF{n % 2}", n // 2)
+                    self.issue(0, "S", n)
+                    self.commit(0, f"SF{n & 1}")
+                    yield ("step",)
+        self.commit(0, "DR")
+        yield ("wait", "DR", 0)
+
+    def softmax(self, w):
+        for i in range(self.nq):
+            yield ("wait", f"SF{i & 1}", i // 2)
+            assert ("S", i) in self.mma_done and self.qstage[i % 2] == i
+            # P^T_i over the buffer whose P^T_{i-2} dV_{i-2} read
+            assert i < 2 or ("DV", i - 2) in self.mma_done
+            self.bump("p", i)
+            self.bars[f"PF{i & 1}"].arrive()
+            self.bars[f"QE{i % 2}"].arrive()
+            yield ("step",)
+        if self.nq > 0:
+            yield ("wait", "DONE", 0)
+            for i in range(self.nq):
+                assert ("DV", i) in self.mma_done, "epilogue read dV before the last MMA"
+
+    def execute_head(self):
+        warp, kind, _, i = self.pipe.pop(0)
+        self.mma_started.add((kind, i))
+        if kind == "S":
+            assert "K" in self.kv and self.qstage[i % 2] == i
+            if i >= 2:  # over P^T_{i-2}: dV_{i-2} read it, every softmax warp wrote it
+                assert ("DV", i - 2) in self.mma_done and self.count.get(("p", i - 2), 0) == 4, \
+                    "S^T overwrote P^T before dV read it"
+        else:
+            assert self.count.get(("p", i), 0) == 4 and self.ostage[i % 2] == i, "dV before P^T or dO"
+        self.mma_done.add((kind, i))
+        self.completed_by[warp] += 1
+
+
+class Bwd256DkdqModel(BwdModel):
+    """`fa_bwd_dkdq256_kernel`: the producer (K, V once; dO_i and Q_i with its
+    rows, one stage each), the MMA warp (dP^T_0, then per tile S^T_i,
+    dP^T_{i+1} once the softmax has read dP^T_i, dK_i and dQ^T_i once dS_i is
+    written), four softmax warps (S^T_i and dP^T_i into registers, dS^T_i into
+    shared memory) and four dQ warps (dQ^T_i out of TMEM)."""
+
+    def __init__(self, nq, rng):
+        BwdModel.__init__(self, nq, 128, False, rng)
+        self.qstage, self.ostage = [None], [None]
+        self.bars = {n: Bar(1) for n in ["K", "V", "QF", "QE", "OF", "OE", "SF", "DPF", "DSE", "DQF", "DONE", "DR"]}
+        self.bars.update({"SC": Bar(4), "DSF": Bar(4), "DQE": Bar(4)})
+
+    def roles(self):
+        return ([self.producer(), self.mma()] + [self.softmax(w) for w in range(4)]
+                + [self.dq_warp(w) for w in range(4)])
+
+    def producer(self):
+        self.landing += [("K", 0, 0, "K"), ("V", 0, 0, "V")]
+        for i in range(self.nq):
+            yield ("wait", "OE", i - 1)
+            assert i == 0 or ("DP", i - 1) in self.mma_done, "dO reloaded early"
+            self.ostage[0] = None
+            self.landing.append(("O", 0, i, "OF"))
+            yield ("step",)
+            yield ("wait", "QE", i - 1)
+            if i > 0:
+                assert {("S", i - 1), ("DK", i - 1)} <= self.mma_done, "Q reloaded early"
+                assert self.count.get(("ds", i - 1), 0) == 4, "Q rows reloaded before the softmax used them"
+            self.qstage[0] = None
+            self.landing.append(("Q", 0, i, "QF"))
+            yield ("step",)
+
+    def mma(self):
+        nq = self.nq
+        if nq > 0:
+            yield ("wait", "V", 0)
+            yield ("wait", "OF", 0)
+            self.issue(0, "DP", 0)
+            self.commit(0, "DPF")
+            self.commit(0, "OE")
+            yield ("wait", "K", 0)
+            for i in range(nq):
+                yield ("wait", "QF", i)
+                self.issue(0, "S", i)
+                self.commit(0, "SF")
+                yield ("wait", "SC", i)
+                if i + 1 < nq:
+                    yield ("wait", "OF", i + 1)
+                    self.issue(0, "DP", i + 1)
+                    self.commit(0, "DPF")
+                    self.commit(0, "OE")
+                yield ("wait", "DSF", i)
+                self.issue(0, "DK", i)
+                self.commit(0, "QE")
+                if i > 0:
+                    yield ("wait", "DQE", i - 1)
+                self.issue(0, "DQ", i)
+                self.commit(0, "DQF")
+                self.commit(0, "DSE")
+                yield ("step",)
+            self.commit(0, "DONE")
+        self.commit(0, "DR")
+        yield ("wait", "DR", 0)
+
+    def softmax(self, w):
+        for i in range(self.nq):
+            yield ("wait", "SF", i)
+            assert ("S", i) in self.mma_done
+            yield ("wait", "DPF", i)
+            assert ("DP", i) in self.mma_done
+            self.bump("sc", i)
+            self.bars["SC"].arrive()
+            yield ("step",)
+            if i > 0:
+                yield ("wait", "DSE", i - 1)
+                assert {("DQ", i - 1), ("DK", i - 1)} <= self.mma_done, "dS overwritten while an MMA reads it"
+            self.bump("ds", i)
+            self.bars["DSF"].arrive()
+            yield ("step",)
+        if self.nq > 0:
+            yield ("wait", "DONE", 0)
+            for i in range(self.nq):
+                assert {("DK", i), ("DQ", i)} <= self.mma_done, "epilogue read dK before the last MMA"
+
+    def dq_warp(self, w):
+        for i in range(self.nq):
+            yield ("wait", "DQF", i)
+            assert ("DQ", i) in self.mma_done
+            self.bump("dqread", i)
+            self.bars["DQE"].arrive()
+            yield ("step",)
+
+    def execute_head(self):
+        warp, kind, _, i = self.pipe.pop(0)
+        self.mma_started.add((kind, i))
+        c = self.count.get
+        if kind == "DP":
+            assert "V" in self.kv and self.ostage[0] == i
+            assert i == 0 or c(("sc", i - 1), 0) == 4, "dP^T overwritten before the softmax read it"
+        elif kind == "S":
+            assert "K" in self.kv and self.qstage[0] == i
+            assert i == 0 or c(("sc", i - 1), 0) == 4, "S^T overwritten before the softmax read it"
+        elif kind == "DK":
+            assert c(("ds", i), 0) == 4 and self.qstage[0] == i and "K" in self.kv
+        else:
+            assert c(("ds", i), 0) == 4, "dQ^T before dS was formed"
+            assert i == 0 or c(("dqread", i - 1), 0) == 4, "dQ^T overwrote the previous one before it was read out"
+        self.mma_done.add((kind, i))
+        self.completed_by[warp] += 1
+
+
+@pytest.mark.parametrize("strict", [False, True], ids=["default", "strict"])
+@pytest.mark.parametrize("nq", [0, 1, 2, 3, 7])
+def test_backward_d256_dv_barrier_protocol(strict, nq):
+    rng = random.Random(3000 + 10 * nq + strict)
+    for _ in range(400):
+        Bwd256DvModel(nq, strict, rng).run()
+
+
+@pytest.mark.parametrize("nq", [0, 1, 2, 3, 7])
+def test_backward_d256_dkdq_barrier_protocol(nq):
+    rng = random.Random(4000 + nq)
+    for _ in range(400):
+        Bwd256DkdqModel(nq, rng).run()
+
+
+def test_model_catches_dq_overwrite_in_the_d256_dkdq_kernel():
+    """Planted mistake: dQ^T_i issued without waiting for the dQ warps to read
+    dQ^T_{i-1} out of the same columns."""
+    class NoDqeWait(Bwd256DkdqModel):
+        def mma(self):
+            for req in Bwd256DkdqModel.mma(self):
+                if req[0] == "wait" and req[1] == "DQE":
+                    continue
+                yield req
+    with pytest.raises(AssertionError, match="before it was read out"):
+        for seed in range(200):
+            NoDqeWait(6, random.Random(seed)).run()
+
+
+def test_model_catches_s_issued_before_dv_in_the_d256_dv_kernel():
+    """Planted mistake: S^T_{i+2} issued before dV_i, whose P^T it overwrites."""
+    class SBeforeDv(Bwd256DvModel):
+        def issue(self, warp, kind, i):
+            Bwd256DvModel.issue(self, warp, kind, i)
+            if kind == "S" and i >= 2:
+                # move S^T_i in front of dV_{i-2} while that is still queued
+                for n, (_, k, _, j) in enumerate(self.pipe[:-1]):
+                    if (k, j) == ("DV", i - 2):
+                        self.pipe.insert(n, self.pipe.pop())
+                        break
+    with pytest.raises(AssertionError, match="overwrote P"):
+        for seed in range(300):
+            SBeforeDv(7, False, random.Random(seed)).run()

@@ -53,6 +53,7 @@ def test_default_order_equals_strict_order(strict_lib, B, H, N, d, dtype, sig):
     (1, 16, 2048, 128, "bf16", 3.0),
     (2, 4, 1000, 64, "f16", 1.0),
     (1, 3, 777, 128, "f16", 2.0),
+    (1, 4, 1000, 256, "bf16", 2.0),   # the d = 256 dV kernel issues S^T_{i+2} behind dV_i
 ])
 def test_backward_default_order_equals_strict_order(strict_lib, B, H, N, d, dtype, sig):
     """The backward kernel issues S^T_{i+2} behind dV_{i+1}, whose P^T it
