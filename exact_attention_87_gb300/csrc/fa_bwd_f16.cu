@@ -433,14 +433,17 @@ __device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint8_t* smem, u
   bool ok = true;
   float ps[64];  // P*scale of this thread's key for queries [64W, 64W+64) of the current tile
 
-  // Every wait is agreed by the whole warpgroup (bar.red.and): its epilogue
-  // needs all 128 threads at the same named barriers.
+  // Each wait is agreed by the warp (its TMEM accesses are per warp), not by
+  // the warpgroup: a warp that gives up leaves the loop, the others give up
+  // too once the abort flag is raised (the MMA warps then wait in vain for its
+  // arrivals), and all four meet once, at the agreement before the epilogue,
+  // whose named barriers need all 128 threads.
   for (int i = 0; i < nq; ++i) {
     // lse2[128], dsum[128] of Q tile i, read as plain shared-memory loads (the compiler schedules them freely)
     const float4* lse4 = reinterpret_cast<const float4*>(smem + C::OFF_ROWS + (i % C::QST) * C::ROWS_BYTES) + 16 * W;
     const float4* dsum4 = lse4 + 32;
     // ---- P_i: S^T columns -> fp32 P (kept, times scale) and 16-bit P^T in TMEM
-    if (!named_bar_and(BAR, 128, wait_bar(b_sf, i & 1, ctl, kWhereBwdSFull))) { ok = false; break; }
+    if (!__all_sync(0xffffffffu, wait_bar(b_sf, i & 1, ctl, kWhereBwdSFull))) { ok = false; break; }
     if (W == 0 && t == 0) FA_TRACE(p, kBvSmS, i);
     tc_fence_after();
     uint32_t rs[2][32];
@@ -497,11 +500,11 @@ __device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint8_t* smem, u
     if (t == 0) FA_TRACE(p, W == 0 ? kBvSmP : kBvW1P, i);
 
     // ---- dS_i: dS^T * scale = P*scale (dP^T - D), 16-bit, into row t of this warpgroup's dS^T half
-    if (!named_bar_and(BAR, 128, wait_bar(b_dpf, i & 1, ctl, kWhereBwdDpFull))) { ok = false; break; }
+    if (!__all_sync(0xffffffffu, wait_bar(b_dpf, i & 1, ctl, kWhereBwdDpFull))) { ok = false; break; }
     if (W == 0 && t == 0) FA_TRACE(p, kBvSmDp, i);
     // dS^T_{i-1} is read by dQ_{i-1} and dK_{i-1}, issued before dP^T_i: this
     // wait is normally over by now.
-    if (i > 0 && !named_bar_and(BAR, 128, wait_bar(b_dse, (i - 1) & 1, ctl, kWhereBwdDsEmpty))) { ok = false; break; }
+    if (i > 0 && !__all_sync(0xffffffffu, wait_bar(b_dse, (i - 1) & 1, ctl, kWhereBwdDsEmpty))) { ok = false; break; }
     if (W == 0 && t == 0) FA_TRACE(p, kBvSmDsWaited, i);
     tc_fence_after();
     uint32_t rdp[2][32];
