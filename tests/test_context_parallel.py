@@ -1,8 +1,9 @@
 """Context parallelism: keys split across ranks, parts merged after one exchange.
 
-CPU tests (gloo, world size 2 and 3) check the exchange logic: rank order,
-shapes, an empty key shard, and that every rank ends with attention over the
-whole key set. The kernels cannot run there, so the part and merge steps are
+CPU tests (gloo, world size 2 and 3) check the exchange logic of both
+exchanges (all-gather of the parts; all-to-all of row blocks, then a gather of
+the merged blocks): rank order, shapes, an empty key shard, a rank with no
+rows, and that every rank ends with attention over the whole key set. The kernels cannot run there, so the part and merge steps are
 the oracle's (``partial=`` / ``merge=`` of context_parallel_attention).
 GPU tests check the kernels themselves: fa_fwd_partial against the oracle on
 one key shard, shards merged by fa_merge against attention over all keys, and
@@ -174,8 +175,53 @@ def test_merge_of_empty_parts():
     assert np.all(o[0, 1, 7] == 0.0) and lse[0, 1, 7] == -np.inf
 
 
+def _worker_a2a(rank, world, port, B, H, N, out):
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import torch.distributed as dist
+    from exact_attention_87_gb300.context_parallel import context_parallel_attention, shard_bounds
+    from workloads import make_qkv
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    q, k, v = make_qkv(B, H, N, 16, "f16", sigma_qk=2.0, seed=4, wid=12500 + N)
+    lo, hi = shard_bounds(N, world, rank)
+    kw = dict(scale=0.3, exchange="all_to_all", partial=_oracle_partial, merge=_oracle_merge, o_dtype=torch.float64)
+    kl, vl = k[:, :, lo:hi].contiguous(), v[:, :, lo:hi].contiguous()
+    rlo, rhi, o_r, l_r = context_parallel_attention(q, kl, vl, gather=False, **kw)
+    o, lse = context_parallel_attention(q, kl, vl, gather=True, **kw)
+    out[rank] = (rlo, rhi, o_r.numpy(), l_r.numpy(), o.numpy(), lse.numpy())
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,B,H,N", [(2, 2, 3, 37), (3, 1, 2, 5), (3, 1, 1, 2)])
+def test_all_to_all_exchange_on_cpu_ranks(world, B, H, N):
+    """The memory-bounded exchange: each rank merges its block of the B*H*N
+    rows from every part, then the merged blocks are gathered. (3, 1, 1, 2):
+    two rows on three ranks, so one rank merges none (and one holds no key)."""
+    from exact_attention_87_gb300.context_parallel import shard_bounds
+    port = _free_port()
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_worker_a2a, args=(world, port, B, H, N, out), nprocs=world, join=True)
+    q, k, v = make_qkv(B, H, N, 16, "f16", sigma_qk=2.0, seed=4, wid=12500 + N)
+    o_ref, lse_ref = oracle.attn(q, k, v, scale=0.3)
+    rows_o, rows_l = o_ref.reshape(-1, 16), lse_ref.reshape(-1)
+    covered = []
+    for r in range(world):
+        rlo, rhi, o_r, l_r, o, lse = out[r]
+        assert (rlo, rhi) == shard_bounds(B * H * N, world, r)
+        np.testing.assert_allclose(o_r, rows_o[rlo:rhi], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(l_r, rows_l[rlo:rhi], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+        covered += list(range(rlo, rhi))
+    assert covered == list(range(B * H * N))
+
+
 @pytest.mark.gpu
-def test_context_parallel_through_a_one_rank_nccl_group():
+@pytest.mark.parametrize("exchange", ["all_gather", "all_to_all"])
+def test_context_parallel_through_a_one_rank_nccl_group(exchange):
     import datetime
     import torch.distributed as dist
     from parity_util import compare
@@ -185,7 +231,7 @@ def test_context_parallel_through_a_one_rank_nccl_group():
     dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{_free_port()}", rank=0, world_size=1,
                             timeout=datetime.timedelta(seconds=120))
     try:
-        o, lse = context_parallel_attention(q.cuda(), k.cuda(), v.cuda())
+        o, lse = context_parallel_attention(q.cuda(), k.cuda(), v.cuda(), exchange=exchange)
         torch.cuda.synchronize()
     finally:
         dist.destroy_process_group()
