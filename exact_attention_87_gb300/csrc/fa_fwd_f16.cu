@@ -17,9 +17,10 @@
 //               softmax warps free a stage once the S product they wait for
 //               shows that its K (and the previous tile's V) have been read,
 //               for d=64 commits behind the MMAs do
-//   warps 8, 10 MMA warps, one per Q sub-tile i: S_i(j) = Q_i K_j^T (SS, into
-//               TMEM), then O_i += P_i(j) V_j (TS: P read from TMEM, V from
-//               SMEM); one elected lane issues; warp 8 also owns TMEM
+//   warps 8, 10 MMA warps, one per Q sub-tile i (d=128; at d=64 warp 8
+//               issues for both): S_i(j) = Q_i K_j^T (SS, into TMEM), then
+//               O_i += P_i(j) V_j (TS: P read from TMEM, V from SMEM); one
+//               elected lane issues; warp 8 also owns TMEM
 //   warps 0-3   softmax for Q rows 0-127   (thread = row; TMEM lanes = rows)
 //   warps 4-7   softmax for Q rows 128-255
 //   warp 11     idle (completes the third warpgroup for the register split)
@@ -32,7 +33,8 @@
 // -DFA_STRICT_MMA_ORDER waits for P_i(j) V_j to complete instead).
 // One MMA warp per sub-tile drives the chain S_i -> softmax_i -> P_i V -> S_i;
 // the two warps pass a turn so that their MMA blocks alternate (ping-pong) and
-// each runs inside the other chain's softmax.
+// each runs inside the other chain's softmax (d=64: one warp issues the blocks
+// of both chains in that order).
 // Each tile's row max comes with the TMEM load of its scores (sm_103a's
 // tcgen05.ld with a max reduction), so no max tree over the scores stands
 // between the load and the exponentials; tiles with masked keys take the max
@@ -181,17 +183,13 @@ __device__ __forceinline__ void producer(const FwdParams& p, uint32_t base, int 
 }
 
 // --------------------------------------------------------------------------
-// MMA warp of Q sub-tile `sub` (whole warp; one elected lane issues)
+// MMA issue (whole warp; one elected lane issues)
 // --------------------------------------------------------------------------
-// Chain i alternates on the tensor pipe with the other sub-tile's chain in
-// blocks B_i(j) = { P_i(j-1) V_{j-1} ; S_i(j) = Q_i K_j^T }, in the order
-// B_0(0), B_1(0), B_0(1), B_1(1), ... A warp passes the turn (an mbarrier
-// arrival) after issuing its block. Between its blocks each chain runs its
-// softmax, so one chain's block executes inside the other chain's softmax
-// window instead of both chains requesting the pipe at the same time.
+// Block j of sub-tile SUB's chain: P(j-1) V_{j-1}, then S(j) = Q K_j^T.
+// Returns false when a wait gave up.
 template <int D, bool BF16, int SUB>
-__device__ __forceinline__ void mma_warp(const FwdParams& p, uint32_t base, uint32_t tmem, bool has1, int nkv,
-                                         int nkv_other, const WaitCtl& ctl) {
+__device__ __forceinline__ bool mma_block(const FwdParams& p, uint32_t base, uint32_t tmem, int j, int nkv,
+                                          const WaitCtl& ctl) {
   using C = Cfg<D>;
   constexpr int sub = SUB;
   constexpr uint32_t fmt = BF16 ? 1u : 0u;
@@ -206,7 +204,69 @@ __device__ __forceinline__ void mma_warp(const FwdParams& p, uint32_t base, uint
   const uint32_t d_o = tmem + (sub ? C::T_O1 : C::T_O0);
   const uint32_t qbase = base + C::OFF_Q + sub * C::Q_SUB_BYTES;
   const uint32_t b_sf = bar_addr<D>(base, C::B_SF + sub), b_pf = bar_addr<D>(base, C::B_PF + sub);
-  const uint32_t b_od = bar_addr<D>(base, C::B_OD + sub), b_drain = bar_addr<D>(base, C::B_DRAIN + sub);
+  const uint32_t b_od = bar_addr<D>(base, C::B_OD + sub);
+  if (j > 0) {
+    // P(j-1) V_{j-1}
+    const int s = (j - 1) % C::STAGES;
+    if (!wait_bar_warp(bar_addr<D>(base, C::B_VF + s), ((j - 1) / C::STAGES) & 1, ctl, kWhereVFull)) return false;
+    if (!wait_bar_warp(b_pf, (j - 1) & 1, ctl, kWherePFull)) return false;
+    tc_fence_after();
+    if (sub == 0) FA_TRACE(p, kEvMmaVFull, j - 1);
+    const uint64_t v0 = smem_desc_sw128(base + C::OFF_V + s * C::KV_BYTES, lbo, 1024);
+#pragma unroll
+    for (int kk = 0; kk < C::BN / 16; ++kk)
+      mma_f16_ts_elect(d_o, d_s + kk * 8, v0 + ((kk * 16 * C::ROW_BYTES) >> 4), idesc_pv,
+                       (j > 1 || kk > 0) ? 1u : 0u);
+    // The softmax learns that P(j-1) V_{j-1} is complete from the commit that
+    // follows S(j) (same warp, issued after it); only the last P.V, which no
+    // S follows, is committed on its own (strict order: every P.V is).
+    if (kOdEveryTile || j == nkv) tc_commit_elect(b_od);
+    if constexpr (!C::SOFTMAX_FREES_STAGES) tc_commit_elect(bar_addr<D>(base, C::B_VE + s));
+    FA_TRACE(p, kEvPV0Issued + sub, j - 1);
+  }
+  if (j < nkv) {
+    // S(j) = Q K_j^T. P(j-1) lives in the S columns: S(j) must not overwrite
+    // them before P(j-1) V_{j-1} has read them. By default S(j) is issued right
+    // behind that P.V (same warp, same tensor pipe, executed in issue order);
+    // FA_STRICT_MMA_ORDER waits for the P.V to complete first.
+    const int s = j % C::STAGES;
+    if (!wait_bar_warp(bar_addr<D>(base, C::B_KF + s), (j / C::STAGES) & 1, ctl, kWhereKFull)) return false;
+#ifdef FA_STRICT_MMA_ORDER
+    if (j > 0 && !wait_bar_warp(b_od, (j - 1) & 1, ctl, kWhereODone)) return false;
+#endif
+    tc_fence_after();
+    if (sub == 0) FA_TRACE(p, kEvMmaKFull, j);
+    // Descriptors of k-step 0; later k-steps advance the 14-bit start-address
+    // field (bytes >> 4), which cannot carry out since shared addresses < 2^18.
+    const uint64_t a0 = smem_desc_sw128(qbase, 16, 1024);
+    const uint64_t b0 = smem_desc_sw128(base + C::OFF_K + s * C::KV_BYTES, 16, 1024);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      // 16 elements = 32 bytes inside the swizzled row; every 4 k-steps the next 64-column half
+      const uint32_t aoff = ((kk / 4) * C::Q_HALF_BYTES + (kk & 3) * 32u) >> 4;
+      const uint32_t boff = ((kk / 4) * C::KV_HALF_BYTES + (kk & 3) * 32u) >> 4;
+      mma_f16_ss_elect(d_s, a0 + aoff, b0 + boff, idesc_qk, kk > 0 ? 1u : 0u);
+    }
+    tc_commit_elect(b_sf);
+    if constexpr (!C::SOFTMAX_FREES_STAGES) tc_commit_elect(bar_addr<D>(base, C::B_KE + s));
+    FA_TRACE(p, kEvS0Issued + sub, j);
+  }
+  return true;
+}
+
+// d = 128: one MMA warp per Q sub-tile. Chain i alternates on the tensor pipe
+// with the other sub-tile's chain in blocks B_i(j) = { P_i(j-1) V_{j-1} ;
+// S_i(j) = Q_i K_j^T }, in the order B_0(0), B_1(0), B_0(1), B_1(1), ... A warp
+// passes the turn (an mbarrier arrival) after issuing its block. Between its
+// blocks each chain runs its softmax, so one chain's block executes inside the
+// other chain's softmax window instead of both chains requesting the pipe at
+// the same time.
+template <int D, bool BF16, int SUB>
+__device__ __forceinline__ void mma_warp(const FwdParams& p, uint32_t base, uint32_t tmem, bool has1, int nkv,
+                                         int nkv_other, const WaitCtl& ctl) {
+  using C = Cfg<D>;
+  constexpr int sub = SUB;
+  const uint32_t b_drain = bar_addr<D>(base, C::B_DRAIN + sub);
   const uint32_t my_turn = bar_addr<D>(base, C::B_TURN + sub), next_turn = bar_addr<D>(base, C::B_TURN + (sub ^ 1));
 
   if (nkv == 0) goto drain;  // no key to attend to (key length 0): nothing to issue
@@ -219,58 +279,34 @@ __device__ __forceinline__ void mma_warp(const FwdParams& p, uint32_t base, uint
     if (has1 && other >= 0 && other <= nkv_other && nkv_other > 0) {
       if (!wait_bar_warp(my_turn, other & 1, ctl, kWhereTurn)) goto drain;
     }
-    if (j > 0) {
-      // P(j-1) V_{j-1}
-      const int s = (j - 1) % C::STAGES;
-      if (!wait_bar_warp(bar_addr<D>(base, C::B_VF + s), ((j - 1) / C::STAGES) & 1, ctl, kWhereVFull)) goto drain;
-      if (!wait_bar_warp(b_pf, (j - 1) & 1, ctl, kWherePFull)) goto drain;
-      tc_fence_after();
-      if (sub == 0) FA_TRACE(p, kEvMmaVFull, j - 1);
-      const uint64_t v0 = smem_desc_sw128(base + C::OFF_V + s * C::KV_BYTES, lbo, 1024);
-#pragma unroll
-      for (int kk = 0; kk < C::BN / 16; ++kk)
-        mma_f16_ts_elect(d_o, d_s + kk * 8, v0 + ((kk * 16 * C::ROW_BYTES) >> 4), idesc_pv,
-                         (j > 1 || kk > 0) ? 1u : 0u);
-      // The softmax learns that P(j-1) V_{j-1} is complete from the commit that
-      // follows S(j) (same warp, issued after it); only the last P.V, which no
-      // S follows, is committed on its own (strict order: every P.V is).
-      if (kOdEveryTile || j == nkv) tc_commit_elect(b_od);
-      if constexpr (!C::SOFTMAX_FREES_STAGES) tc_commit_elect(bar_addr<D>(base, C::B_VE + s));
-      FA_TRACE(p, kEvPV0Issued + sub, j - 1);
-    }
-    if (j < nkv) {
-      // S(j) = Q K_j^T. P(j-1) lives in the S columns: S(j) must not overwrite
-      // them before P(j-1) V_{j-1} has read them. By default S(j) is issued right
-      // behind that P.V (same warp, same tensor pipe, executed in issue order);
-      // FA_STRICT_MMA_ORDER waits for the P.V to complete first.
-      const int s = j % C::STAGES;
-      if (!wait_bar_warp(bar_addr<D>(base, C::B_KF + s), (j / C::STAGES) & 1, ctl, kWhereKFull)) goto drain;
-#ifdef FA_STRICT_MMA_ORDER
-      if (j > 0 && !wait_bar_warp(b_od, (j - 1) & 1, ctl, kWhereODone)) goto drain;
-#endif
-      tc_fence_after();
-      if (sub == 0) FA_TRACE(p, kEvMmaKFull, j);
-      // Descriptors of k-step 0; later k-steps advance the 14-bit start-address
-      // field (bytes >> 4), which cannot carry out since shared addresses < 2^18.
-      const uint64_t a0 = smem_desc_sw128(qbase, 16, 1024);
-      const uint64_t b0 = smem_desc_sw128(base + C::OFF_K + s * C::KV_BYTES, 16, 1024);
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        // 16 elements = 32 bytes inside the swizzled row; every 4 k-steps the next 64-column half
-        const uint32_t aoff = ((kk / 4) * C::Q_HALF_BYTES + (kk & 3) * 32u) >> 4;
-        const uint32_t boff = ((kk / 4) * C::KV_HALF_BYTES + (kk & 3) * 32u) >> 4;
-        mma_f16_ss_elect(d_s, a0 + aoff, b0 + boff, idesc_qk, kk > 0 ? 1u : 0u);
-      }
-      tc_commit_elect(b_sf);
-      if constexpr (!C::SOFTMAX_FREES_STAGES) tc_commit_elect(bar_addr<D>(base, C::B_KE + s));
-      FA_TRACE(p, kEvS0Issued + sub, j);
-    }
+    if (!mma_block<D, BF16, SUB>(p, base, tmem, j, nkv, ctl)) goto drain;
     if (has1) {
       __syncwarp();
       if ((threadIdx.x & 31) == 0) mbar_arrive(next_turn);
     }
   }
 drain:
+  // All MMAs issued by this warp complete before the CTA may free TMEM / exit.
+  tc_commit_elect(b_drain);
+  __all_sync(0xffffffffu, wait_bar_drain(b_drain, 0, ctl));
+}
+
+// d = 64: one MMA warp issues both chains' blocks in the same order
+// (B_0(0), B_1(0), B_0(1), ...) by program order instead of turns: the blocks
+// are short there and the turn handoff between two warps cost more than the
+// second warp's overlap of waits and commits gained.
+template <int D, bool BF16>
+__device__ __forceinline__ void mma_both(const FwdParams& p, uint32_t base, uint32_t tmem, bool has1, int nkv0,
+                                         int nkv1, const WaitCtl& ctl) {
+  const uint32_t b_drain = bar_addr<D>(base, Cfg<D>::B_DRAIN);
+  const int n = max(nkv0, nkv1);
+  if (n > 0 && wait_bar_warp(bar_addr<D>(base, Cfg<D>::B_Q), 0, ctl, kWhereQ)) {
+    tc_fence_after();
+    for (int j = 0; j <= n; ++j) {
+      if (nkv0 > 0 && j <= nkv0 && !mma_block<D, BF16, 0>(p, base, tmem, j, nkv0, ctl)) break;
+      if (has1 && nkv1 > 0 && j <= nkv1 && !mma_block<D, BF16, 1>(p, base, tmem, j, nkv1, ctl)) break;
+    }
+  }
   // All MMAs issued by this warp complete before the CTA may free TMEM / exit.
   tc_commit_elect(b_drain);
   __all_sync(0xffffffffu, wait_bar_drain(b_drain, 0, ctl));
@@ -599,7 +635,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
     if (warp == C::WARP_TMA) {
       if ((threadIdx.x & 31) == 0) producer<D>(p, base, bh, row0, has1, t0, nkv, ctl);
       __syncwarp();
-    } else if (warp == C::WARP_MMA0 || (warp == C::WARP_MMA1 && has1)) {
+    } else if (D == 64 && warp == C::WARP_MMA0) {
+      mma_both<D, BF16>(p, base, tmem, has1, nkv0, nkv1, ctl);
+      __syncwarp();
+    } else if (D != 64 && (warp == C::WARP_MMA0 || (warp == C::WARP_MMA1 && has1))) {
       if (warp == C::WARP_MMA0)
         mma_warp<D, BF16, 0>(p, base, tmem, has1, nkv0, nkv1, ctl);
       else

@@ -877,3 +877,73 @@ def test_model_catches_s_issued_before_dv_in_the_d256_dv_kernel():
     with pytest.raises(AssertionError, match="overwrote P"):
         for seed in range(300):
             SBeforeDv(7, False, random.Random(seed)).run()
+
+
+class OneWarpModel(Model):
+    """The d = 64 kernel: one MMA warp issues both chains' blocks in the turn
+    order B_0(0), B_1(0), B_0(1), ... by program order (no turn barriers); the
+    rest as in Model with commit-freed stages."""
+
+    def roles(self):
+        roles = [self.producer(), self.mma_both()]
+        roles += [self.softmax(0, w) for w in range(4)]
+        if self.has1:
+            roles += [self.softmax(1, w) for w in range(4)]
+        return roles
+
+    def block(self, sub, j):
+        nkv = self.nk[sub]
+        sv, sk = (j - 1) % self.ST, j % self.ST
+        if j > 0:
+            yield ("wait", f"VF{sv}", (j - 1) // self.ST)
+            yield ("wait", f"PF{sub}", j - 1)
+            self.issue(sub, "PV", j - 1)
+            if self.STRICT or j == nkv:
+                self.commit(sub, f"OD{sub}")
+            if not self.SFREE:
+                self.commit(sub, f"VE{sv}")
+            yield ("step",)
+        if j < nkv:
+            yield ("wait", f"KF{sk}", j // self.ST)
+            if self.STRICT and j > 0:
+                yield ("wait", f"OD{sub}", j - 1)
+            self.issue(sub, "S", j)
+            self.commit(sub, f"SF{sub}")
+            if not self.SFREE:
+                self.commit(sub, f"KE{sk}")
+            yield ("step",)
+
+    def mma_both(self):
+        n = max(self.nk)
+        if n > 0:
+            yield ("wait", "QF", 0)
+            for j in range(n + 1):
+                for sub in (0, 1):
+                    if self.nk[sub] > 0 and j <= self.nk[sub]:
+                        yield from self.block(sub, j)
+        for sub in (0, 1):
+            self.commit(sub, f"DR{sub}")
+            yield ("wait", f"DR{sub}", 0)
+
+    def issue(self, warp, kind, j):
+        # one warp issues for both chains: one issue stream, in order
+        self.issued[0] += 1
+        self.pipe.append((0, kind, warp, j))
+
+    def commit(self, warp, bar):
+        self.commits.append((0, self.issued[0], bar))
+
+    def execute_head(self):
+        _, kind, sub, j = self.pipe.pop(0)
+        self.pipe.insert(0, (sub, kind, sub, j))
+        Model.execute_head(self)
+        self.completed_by[sub] -= 1
+        self.completed_by[0] += 1
+
+
+@pytest.mark.parametrize("strict", [False, True], ids=["default", "strict"])
+@pytest.mark.parametrize("nkv0,nkv1,has1", CASES)
+def test_forward_d64_one_mma_warp_protocol(strict, nkv0, nkv1, has1):
+    rng = random.Random(hash(("one", strict, nkv0, nkv1, has1)) & 0xFFFFFFFF)
+    for _ in range(400):
+        OneWarpModel(nkv0, nkv1, has1, 3, False, strict, rng).run()
