@@ -99,6 +99,9 @@ __device__ __forceinline__ void producer256(const FwdParams& p, uint32_t base, i
     for (int h = 0; h < 4; ++h)
       tma_load_3d(base + C::OFF_K + s * C::KV_BYTES + h * C::KV_BLOCK, &p.tm_k, kf, 64 * h, (t0 + j) * C::BN, bh);
     nk = j + 1;
+#ifdef FA_TESTING
+    if (p.inject == 1 && j == 0) continue;  // fault injection: V_0 is never loaded
+#endif
     if (!wait_bar(bar256(base, C::B_VE + s), par, ctl, kWhereVEmpty)) { ok = false; break; }
     const uint32_t vf = bar256(base, C::B_VF + s);
     mbar_arrive_expect_tx(vf, C::KV_BYTES);
@@ -115,8 +118,12 @@ __device__ __forceinline__ void producer256(const FwdParams& p, uint32_t base, i
     wait_bar_drain(bq, 0, ctl);
     for (int t = nk > C::STAGES ? nk - C::STAGES : 0; t < nk; ++t)
       wait_bar_drain(bar256(base, C::B_KF + t % C::STAGES), (t / C::STAGES) & 1, ctl);
-    for (int t = nv > C::STAGES ? nv - C::STAGES : 0; t < nv; ++t)
+    for (int t = nv > C::STAGES ? nv - C::STAGES : 0; t < nv; ++t) {
+#ifdef FA_TESTING
+      if (p.inject == 1 && t == 0) continue;  // never armed
+#endif
       wait_bar_drain(bar256(base, C::B_VF + t % C::STAGES), (t / C::STAGES) & 1, ctl);
+    }
   }
 }
 

@@ -1,7 +1,7 @@
 """Bounded waits: a barrier that is never completed makes the kernel give up,
 report FA_ERR_DEVICE_TIMEOUT through the status word, drain its own work and
 exit; the context stays usable. The failure is injected on the producer side
-(one V tile is never loaded): no GPU fault, trap or endless loop is involved,
+(one V or dO tile is never loaded): no GPU fault, trap or endless loop is involved,
 and every wait has a short limit (2e7 cycles, about 10 ms).
 """
 import pytest
@@ -15,9 +15,10 @@ from workloads import make_qkv
 pytestmark = pytest.mark.gpu
 
 
-def test_injected_missing_tile_times_out_and_recovers():
+@pytest.mark.parametrize("d", [128, 256])
+def test_injected_missing_tile_times_out_and_recovers(d):
     from exact_attention_87_gb300 import testing
-    q, k, v = make_qkv(1, 2, 512, 128, "bf16", seed=8, wid=8000)
+    q, k, v = make_qkv(1, 2, 512, d, "bf16", seed=8, wid=8000)
     qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
     assert testing.device_status() == 0
     testing.attention(qc, kc, vc, inject=1, wait_limit_cycles=20_000_000)
@@ -35,12 +36,14 @@ def test_injected_missing_tile_times_out_and_recovers():
     assert res["ok"], res
 
 
-def test_backward_injected_missing_tile_times_out_and_recovers():
-    """The backward kernel: dO of the first Q tile is never loaded."""
+@pytest.mark.parametrize("d", [128, 256])
+def test_backward_injected_missing_tile_times_out_and_recovers(d):
+    """The backward kernel (at d = 256 the dK/dQ kernel): dO of the first Q
+    tile is never loaded."""
     from exact_attention_87_gb300 import testing
     from workloads import make_dout
-    q, k, v = (t.cuda() for t in make_qkv(1, 2, 512, 128, "bf16", seed=8, wid=8001))
-    do = make_dout(1, 2, 512, 128, "bf16", seed=8, wid=8001).cuda()
+    q, k, v = (t.cuda() for t in make_qkv(1, 2, 512, d, "bf16", seed=8, wid=8001))
+    do = make_dout(1, 2, 512, d, "bf16", seed=8, wid=8001).cuda()
     o, lse = fa.attention(q, k, v)
     torch.cuda.synchronize()
     assert testing.device_status() == 0
