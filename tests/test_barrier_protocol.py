@@ -947,3 +947,190 @@ def test_forward_d64_one_mma_warp_protocol(strict, nkv0, nkv1, has1):
     rng = random.Random(hash(("one", strict, nkv0, nkv1, has1)) & 0xFFFFFFFF)
     for _ in range(400):
         OneWarpModel(nkv0, nkv1, has1, 3, False, strict, rng).run()
+
+
+class PersistModel(BwdModel):
+    """The persistent form of the d = 128 forward kernel: one CTA walks a list
+    of units (nkv0, nkv1); the producer (Q per unit once the previous unit's
+    last S products of both sub-tiles completed; K/V tiles in a 2-stage ring
+    numbered across units), one MMA warp (both chains' blocks in turn order;
+    a unit's first P.V of sub-tile i waits until the previous unit's epilogue
+    read O_i), four softmax warps per sub-tile (stage releases per tile, the
+    tiles only the other sub-tile uses released once they have landed, the
+    last V released after the unit's last P.V, the Q-free arrival after the
+    last S, the O-free arrival after the epilogue read O)."""
+
+    ST = 2
+
+    def __init__(self, units, rng):
+        BwdModel.__init__(self, 1, 128, False, rng)
+        self.units = units
+        self.bars = {"Q": Bar(1), "QE": Bar(8), "DR": Bar(1)}
+        for s in range(self.ST):
+            self.bars.update({f"KF{s}": Bar(1), f"KE{s}": Bar(8), f"VF{s}": Bar(1), f"VE{s}": Bar(8)})
+        for i in range(2):
+            self.bars.update({f"SF{i}": Bar(1), f"PF{i}": Bar(4), f"OD{i}": Bar(1), f"OF{i}": Bar(4)})
+        self.kst, self.vst, self.qunit = [None] * self.ST, [None] * self.ST, None
+        self.o_read = set()  # (sub, unit) epilogues that read O
+
+    def base(self, k):
+        return sum(max(a, b) for a, b in self.units[:k])
+
+    def pending(self):
+        """MMAs issued and not yet complete, as (kind, key)."""
+        return [(kind, key) for _, kind, _, key in self.pipe]
+
+    def roles(self):
+        return [self.producer(), self.mma()] + [self.softmax(sub, w) for sub in (0, 1) for w in range(4)]
+
+    def producer(self):
+        g = 0
+        for k, (n0, n1) in enumerate(self.units):
+            nkv = max(n0, n1)
+            if k > 0:
+                yield ("wait", "QE", k - 1)
+                p0, p1 = self.units[k - 1]
+                b = self.base(k - 1)
+                assert all(("S", (i, k - 1, j, b + j)) in self.mma_done for i, n in ((0, p0), (1, p1))
+                           for j in range(n)), "Q reloaded before the last S read it"
+            self.qunit = None
+            self.landing.append(("Q", 0, k, "Q"))
+            yield ("step",)
+            for j in range(nkv):
+                gg = g + j
+                s = gg % self.ST
+                yield ("wait", f"KE{s}", gg // self.ST - 1)
+                if gg >= self.ST:
+                    old_t = gg - self.ST
+                    assert not any(x[0] == "S" and x[1][3] == old_t for x in self.pending()), \
+                        "K stage reloaded while an S product may read it"
+                self.kst[s] = None
+                self.landing.append(("K", s, gg, f"KF{s}"))
+                yield ("step",)
+                yield ("wait", f"VE{s}", gg // self.ST - 1)
+                if gg >= self.ST:
+                    old_t = gg - self.ST
+                    assert not any(x[0] == "PV" and x[1][3] == old_t for x in self.pending()), \
+                        "V stage reloaded while a P.V may read it"
+                self.vst[s] = None
+                self.landing.append(("V", s, gg, f"VF{s}"))
+                yield ("step",)
+            g += nkv
+
+    def mma(self):
+        g, gp = 0, [0, 0]
+        for k, (n0, n1) in enumerate(self.units):
+            nkv = max(n0, n1)
+            yield ("wait", "Q", k)
+            for j in range(nkv + 1):
+                for sub, n in ((0, n0), (1, n1)):
+                    if j > n:
+                        continue
+                    if j == 1 and k > 0:
+                        yield ("wait", f"OF{sub}", k - 1)
+                    if j > 0:
+                        gg = g + j - 1
+                        yield ("wait", f"VF{gg % self.ST}", gg // self.ST)
+                        yield ("wait", f"PF{sub}", gp[sub] + j - 1)
+                        self.issue(0, "PV", (sub, k, j - 1, gg))
+                        if j == n:
+                            self.commit(0, f"OD{sub}")
+                        yield ("step",)
+                    if j < n:
+                        gg = g + j
+                        yield ("wait", f"KF{gg % self.ST}", gg // self.ST)
+                        self.issue(0, "S", (sub, k, j, gg))
+                        self.commit(0, f"SF{sub}")
+                        yield ("step",)
+            g += nkv
+            gp[0] += n0
+            gp[1] += n1
+        self.commit(0, "DR")
+        yield ("wait", "DR", 0)
+
+    def softmax(self, sub, w):
+        g, gs = 0, 0
+        for k, (n0, n1) in enumerate(self.units):
+            nkv, n = max(n0, n1), (n1 if sub else n0)
+            for j in range(n):
+                yield ("wait", f"SF{sub}", gs + j)
+                assert ("S", (sub, k, j, g + j)) in self.mma_done
+                if j > 0:
+                    self.bars[f"VE{(g + j - 1) % self.ST}"].arrive()
+                self.bars[f"KE{(g + j) % self.ST}"].arrive()
+                self.bump(("p", sub, k), j)
+                self.bars[f"PF{sub}"].arrive()
+                if j == n - 1:
+                    self.bars["QE"].arrive()
+                yield ("step",)
+            for jj in range(n, nkv):
+                gg = g + jj
+                yield ("wait", f"KF{gg % self.ST}", gg // self.ST)
+                yield ("wait", f"VF{gg % self.ST}", gg // self.ST)
+                self.bars[f"VE{gg % self.ST}"].arrive()
+                self.bars[f"KE{gg % self.ST}"].arrive()
+                yield ("step",)
+            yield ("wait", f"OD{sub}", k)
+            assert all(("PV", (sub, k, j, g + j)) in self.mma_done for j in range(n)), "epilogue before the last P.V"
+            self.bars[f"VE{(g + n - 1) % self.ST}"].arrive()
+            self.o_read.add((sub, k))
+            self.bars[f"OF{sub}"].arrive()
+            yield ("step",)
+            g += nkv
+            gs += n
+
+    def execute_head(self):
+        warp, kind, _, key = self.pipe.pop(0)
+        sub, k, j, gg = key
+        self.mma_started.add((kind, key))
+        if kind == "S":
+            assert self.qunit == k, "S on a Q buffer without this unit's Q"
+            assert self.kst[gg % self.ST] == gg, "S on a K stage without its tile"
+            # S overwrites the P columns that the previous P.V of this sub-tile read
+            prev = [x for x in self.mma_started if x[0] == "PV" and x[1][0] == sub]
+            assert all(x in self.mma_done for x in prev), "S overwrote P before P.V read it"
+        else:
+            assert self.vst[gg % self.ST] == gg, "P.V on a V stage without its tile"
+            assert self.count.get((("p", sub, k), j), 0) == 4, "P.V before every softmax warp wrote P"
+            if j == 0 and k > 0:
+                assert (sub, k - 1) in self.o_read, "P.V overwrote O before the epilogue read it"
+        self.mma_done.add((kind, key))
+        self.completed_by[warp] += 1
+
+    def fire(self, e):
+        if e[0] == "land":
+            kind, s, x, bar = self.landing.pop(e[1])
+            if kind == "K":
+                self.kst[s] = x
+            elif kind == "V":
+                self.vst[s] = x
+            else:
+                self.qunit = x
+            self.bars[bar].arrive()
+        else:
+            Model.fire(self, e)
+
+
+@pytest.mark.parametrize("units", [
+    [(3, 3)], [(2, 2), (2, 2), (2, 2)], [(1, 2), (4, 5), (2, 3)], [(5, 6), (1, 2)], [(1, 1), (1, 1), (1, 1), (1, 1)],
+    [(3, 4), (3, 4), (1, 2), (6, 7)],
+], ids=lambda u: "-".join(f"{a}.{b}" for a, b in u))
+def test_forward_persistent_barrier_protocol(units):
+    rng = random.Random(hash(tuple(units)) & 0xFFFFFFFF)
+    for _ in range(400):
+        PersistModel(units, rng).run()
+
+
+def test_model_catches_an_early_release_of_an_unused_tile():
+    """Planted mistake: the sub-tile that does not use a unit's last tile
+    releases its stage at once instead of after the tile landed; its arrivals
+    can then complete the stage's previous phase early."""
+    class EarlyRelease(PersistModel):
+        def softmax(self, sub, w):
+            for req in PersistModel.softmax(self, sub, w):
+                if req[0] == "wait" and req[1][:2] in ("KF", "VF") and self.rng.random() < 0.9:
+                    continue
+                yield req
+    with pytest.raises(AssertionError):
+        for seed in range(300):
+            EarlyRelease([(1, 2), (4, 5), (2, 3), (3, 4)], random.Random(seed)).run()
