@@ -566,7 +566,7 @@ def main():
         "pct_of_datasheet_peak": round(100.0 * achieved / DATASHEET_TFLOPS, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                     "kernel": fwd_kernel_name(w),
+                     "kernel": fwd_kernel_name(w, args.causal, n_launch),
                      "traffic": traffic, "algorithmic_bytes": w.hbm_bytes},
         "clocks": sampler.summary(),
         "sustained": sustained,
@@ -584,13 +584,17 @@ def main():
         dist.destroy_process_group()
 
 
-def fwd_kernel_name(w) -> str:
-    """The forward kernel a workload's step spends its time in."""
+def fwd_kernel_name(w, causal: bool = False, launches: int = 1) -> str:
+    """The forward kernel a workload's step spends its time in: at d = 128 one
+    unsplit launch takes the persistent form when N is a multiple of 256
+    (512 with the causal mask)."""
     t = "bf16" if w.dtype == "bf16" else "f16"
     if w.dtype == "f32":
         return f"fa_fwd_f32_kernel<{w.d}>"
     if w.d == 256:
         return f"fa_fwd_d256_kernel<{t}>"
+    if w.d == 128 and launches == 1 and w.N % (512 if causal else 256) == 0:
+        return f"fa_fwd_persist_kernel<{w.d},{t}>"
     return f"fa_fwd_f16_kernel<{w.d},{t}>"
 
 
