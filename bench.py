@@ -471,6 +471,7 @@ def main():
     workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     # The plan the library runs: 1 launch (unsplit), 2 (every unit split, merge) or 3 (split wave tail).
     n_launch = 1
+    streamed = False
     if args.splits != 1 and w.dtype != "f32":
         n_launch = fa.fa_fwd_splitkv_launches(w.B, w.H, w.N, w.d, args.splits)
         if n_launch < 1:
@@ -480,6 +481,14 @@ def main():
         cfg["launches_per_step"] = n_launch
         if n_launch == 3:
             cfg["split_plan"] = "tail: full waves unsplit, the last wave's units split, their rows merged"
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        rc, sp = fa.fa_fwd_stream_plan(w.B, w.H, w.N, w.d, sms)
+        if args.splits == 0 and not args.causal and rc == fa.FA_OK and sp["ctas"] > 0:
+            cfg["num_splits"] = 1
+            cfg["split_plan"] = (f"streamed tail: units 0..{sp['unit0'] - 1} whole on the persistent kernel, "
+                                 f"the {sp['tiles']} K/V tiles of the rest cut into {sp['ctas']} ranges "
+                                 f"(one per SM), cut units merged (at most {n_splits} pieces)")
+            streamed = True
 
     def step():
         fa.attention(qd, kd, vd, scale=w.scale, out=o, lse=lse, stream=stream, num_splits=args.splits,
@@ -566,7 +575,7 @@ def main():
         "pct_of_datasheet_peak": round(100.0 * achieved / DATASHEET_TFLOPS, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                     "kernel": fwd_kernel_name(w, args.causal, n_launch),
+                     "kernel": fwd_kernel_name(w, args.causal, n_launch, streamed),
                      "traffic": traffic, "algorithmic_bytes": w.hbm_bytes},
         "clocks": sampler.summary(),
         "sustained": sustained,
@@ -584,16 +593,16 @@ def main():
         dist.destroy_process_group()
 
 
-def fwd_kernel_name(w, causal: bool = False, launches: int = 1) -> str:
+def fwd_kernel_name(w, causal: bool = False, launches: int = 1, streamed: bool = False) -> str:
     """The forward kernel a workload's step spends its time in: at d = 128 one
     unsplit launch takes the persistent form when N is a multiple of 256
-    (512 with the causal mask)."""
+    (512 with the causal mask), and so does the streamed tail."""
     t = "bf16" if w.dtype == "bf16" else "f16"
     if w.dtype == "f32":
         return f"fa_fwd_f32_kernel<{w.d}>"
     if w.d == 256:
         return f"fa_fwd_d256_kernel<{t}>"
-    if w.d == 128 and launches == 1 and w.N % (512 if causal else 256) == 0:
+    if w.d == 128 and (streamed or (launches == 1 and w.N % (512 if causal else 256) == 0)):
         return f"fa_fwd_persist_kernel<{w.d},{t}>"
     return f"fa_fwd_f16_kernel<{w.d},{t}>"
 

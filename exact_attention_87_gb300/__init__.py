@@ -81,6 +81,9 @@ def lib(path: str | None = None):
                                       ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_int),
                                       ctypes.POINTER(ctypes.c_ulonglong)]
     L.fa_fwd_splitkv_plan.restype = i
+    ip = ctypes.POINTER(ctypes.c_int)
+    L.fa_fwd_stream_plan.argtypes = [i, i, i, i, i, ip, ip, ip]
+    L.fa_fwd_stream_plan.restype = i
     L.fa_fwd_partial.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
     L.fa_fwd_partial.restype = i
     L.fa_merge.argtypes = [vp, vp, i, vp, vp, i, i, i, i, i, vp]
@@ -147,6 +150,17 @@ def fa_fwd_splitkv_plan(B, H, N, d, num_splits, num_sms) -> tuple[int, dict | No
     if rc != FA_OK:
         return rc, None
     return rc, {"splits": s.value, "first_split_unit": f.value, "launches": n.value, "workspace_bytes": w.value}
+
+
+def fa_fwd_stream_plan(B, H, N, d, num_sms) -> tuple[int, dict | None]:
+    """(status, plan) with plan = {unit0, tiles, ctas}: the streamed tail of the
+    automatic plan for unmasked 16-bit inputs on a device with num_sms SMs
+    (ctas = 0: not streamed; host arithmetic only)."""
+    u, t, c = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    rc = lib().fa_fwd_stream_plan(B, H, N, d, num_sms, ctypes.byref(u), ctypes.byref(t), ctypes.byref(c))
+    if rc != FA_OK:
+        return rc, None
+    return rc, {"unit0": u.value, "tiles": t.value, "ctas": c.value}
 
 
 def fa_fwd_partial(Q, K, V, O_part, LSE_part, B, H, Nq, Nk, d, scale, dtype, stream=None) -> int:
@@ -392,7 +406,7 @@ def attention_backward(q, k, v, o, lse, do, scale: float | None = None, dq=None,
 
 
 __all__ = ["attention", "attention_backward", "attention_partial", "merge_partials", "fa_fwd_partial", "fa_merge",
-           "fa_fwd_splitkv_launches",
+           "fa_fwd_splitkv_launches", "fa_fwd_splitkv_plan", "fa_fwd_stream_plan",
            "fa_bwd", "fa_bwd_ex", "fa_bwd_workspace_size", "fa_fwd", "fa_fwd_ex", "fa_fwd_splitkv", "fa_fwd_splitkv_ex", "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_num_splits",
            "fa_fwd_splitkv_workspace_size",
            "fa_get_device_status", "fa_strerror", "fa_abi_version", "build", "lib",

@@ -271,6 +271,86 @@ long long plan_row0(const SplitPlan& plan, int N, int d) {
   return (plan.tail_qunit0 / nqb) * N + (plan.tail_qunit0 % nqb) * fa::fwd_q_block(d);
 }
 
+// Streamed tail of the persistent d = 128 forward (unmasked, N a multiple of
+// 256; see fa::FwdParams::st_ctas): the full rounds of num_sms units run
+// whole, the K/V tiles of the units left over are cut into one contiguous
+// range per CTA, and the units a range boundary cuts are merged afterwards.
+// Modelled time, in tiles of one 256-row unit and one 128-key tile on one SM
+// (t_p ~ 1.63 us on GB300 in the persistent kernel):
+//   whole units only:  ceil(units / num_sms) * n
+//   streamed tail:     R * n + ceil(tail tiles / ctas) + 1
+//                      + (3 us + 2 * partial bytes / 4 TB/s) / t_p   (the merge)
+// with R full rounds, n tiles per unit and `ctas` CTAs sharing the tail
+// (num_sms / k for k = 1..8, at most kStreamMaxCtas so that the part slots
+// fit the library's 32 MiB scratch). The tail is streamed only when that
+// saves at least two tiles. On B=8 H=12 N=2048 (768 units, 5.05 rounds)
+// it takes 2-tile ranges on 64 CTAs; on B=8 H=32 N=4096 (26.9 rounds) it
+// does not pay.
+struct StreamPlan {
+  int unit0 = 0;            // first tail unit (R * num_sms)
+  int tiles = 0;            // K/V tiles of the tail
+  int ctas = 0;             // CTAs sharing the tail (0: no streamed tail)
+  int max_pieces = 0;       // most pieces one unit is cut into
+};
+constexpr int kStreamRows = 2 * fa::kF16BlockQ;  // rows of a unit (and of a part slot)
+constexpr unsigned long long stream_slot_bytes(int d) {
+  return static_cast<unsigned long long>(kStreamRows) * (4ull * d + 4);
+}
+constexpr int kStreamMaxCtas = static_cast<int>(FA_NOALLOC_SCRATCH_BYTES / (2 * (stream_slot_bytes(128) + 512)));
+
+unsigned long long stream_workspace_bytes(int ctas, int d) {
+  if (ctas <= 0) return 0;
+  const unsigned long long rows = 2ull * ctas * kStreamRows;
+  return ((rows * d * 4 + 255) & ~255ull) + rows * 4;
+}
+
+StreamPlan stream_plan(int B, int H, int N, int d, int num_sms) {
+  StreamPlan best;
+  if (d != 128 || N % kStreamRows != 0 || num_sms < 1) return best;
+  const long long units = static_cast<long long>(B) * H * (N / kStreamRows);
+  const int n = N / fa::kF16BlockKV;
+  const long long R = units / num_sms, tail = units - R * num_sms;
+  if (tail == 0 || units > 0x7fffffffLL) return best;
+  const double t_p = 1.63;
+  const long long T = tail * n;
+  // 32-bit range arithmetic on the device
+  if (T * num_sms >= (1ll << 31)) return best;
+  double best_t = static_cast<double>(R + 1) * n - 2.0;
+  int last = 0;
+  for (int k = 1; k <= 8; ++k) {
+    const int ctas = std::min((num_sms + k - 1) / k, kStreamMaxCtas);
+    if (ctas == last || ctas < 1) continue;
+    last = ctas;
+    long long partial = 0;  // pieces written as parts: a range's first and last, when they cut a unit
+    for (int c = 0; c < ctas; ++c) {
+      const int a = fa::st_begin(static_cast<int>(T), ctas, c), b = fa::st_begin(static_cast<int>(T), ctas, c + 1);
+      if (a == b) continue;
+      fa::StPiece pc;
+      fa::st_piece(static_cast<int>(T), ctas, n, c, 0, pc);
+      if (pc.slot >= 0) ++partial;
+      if (b > (a / n + 1) * n && b % n != 0) ++partial;
+    }
+    const double t = static_cast<double>(R) * n + static_cast<double>((T + ctas - 1) / ctas) + 1.0 +
+                     (3.0 + 2.0 * partial * stream_slot_bytes(d) / 4e12 * 1e6) / t_p;
+    if (t < best_t) {
+      best_t = t;
+      best.unit0 = static_cast<int>(R * num_sms);
+      best.tiles = static_cast<int>(T);
+      best.ctas = ctas;
+    }
+  }
+  if (best.ctas > 0) {
+    for (int i = 0; i < tail; ++i) {
+      int c_lo, c_hi, pieces = 0;
+      fa::st_unit_ctas(best.tiles, best.ctas, n, i, c_lo, c_hi);
+      for (int c = c_lo; c <= c_hi; ++c)
+        if (fa::st_begin(best.tiles, best.ctas, c) != fa::st_begin(best.tiles, best.ctas, c + 1)) ++pieces;
+      best.max_pieces = std::max(best.max_pieces, pieces);
+    }
+  }
+  return best;
+}
+
 // What a 16-bit split-KV pass does for a shape on a device with num_sms SMs:
 // the key ranges per split unit after clamping to whole tiles, the first
 // split unit, the launches and the workspace. Host arithmetic only.
@@ -281,7 +361,7 @@ struct PlanSummary {
   unsigned long long workspace;
 };
 
-PlanSummary summarize_plan(int B, int H, int N, int d, int num_splits, int num_sms) {
+PlanSummary summarize_classic(int B, int H, int N, int d, int num_splits, int num_sms) {
   const long long units = static_cast<long long>(B) * H * q_blocks(N, d);
   const SplitPlan plan = split_plan(B, H, N, d, num_splits, num_sms);
   const long long tiles = kv_tiles(N, d);
@@ -291,6 +371,19 @@ PlanSummary summarize_plan(int B, int H, int N, int d, int num_splits, int num_s
   const bool tail = plan.tail_qunit0 > 0;
   return {eff, tail ? plan.tail_qunit0 : 0, tail ? 3 : 2,
           workspace_bytes_for(B, H, N, d, eff, tail ? plan_row0(plan, N, d) : 0)};
+}
+
+// The automatic count of an unmasked 16-bit call with d = 128 and N a
+// multiple of 256 takes the streamed tail when it pays (2 launches: the
+// persistent pass and the merge of the cut units; splits = the most pieces
+// of one unit). Calls with masks take the key-range plan of the same
+// arguments, so the workspace covers both.
+PlanSummary summarize_plan(int B, int H, int N, int d, int num_splits, int num_sms) {
+  const PlanSummary classic = summarize_classic(B, H, N, d, num_splits, num_sms);
+  if (num_splits != 0) return classic;
+  const StreamPlan sp = stream_plan(B, H, N, d, num_sms);
+  if (sp.ctas == 0) return classic;
+  return {sp.max_pieces, sp.unit0, 2, std::max(classic.workspace, stream_workspace_bytes(sp.ctas, d))};
 }
 
 // The 16-bit forward kernel for the head dimension p.d.
@@ -358,6 +451,36 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
   p.num_sms = dev.num_sms;
   p.rescale_tau = rescale_tau;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The automatic count of an unmasked 16-bit call may stream the persistent
+  // kernel's last units instead of splitting key ranges.
+  if (dtype != FA_F32 && num_splits == 0 && !causal && !klen && !o_f32 && inject == 0 && !stats_trace && !timeline) {
+    const StreamPlan sp = stream_plan(B, H, N, d, dev.num_sms);
+    if (sp.ctas > 0) {
+      const unsigned long long need_all = summarize_plan(B, H, N, d, 0, dev.num_sms).workspace;
+      if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need_all)
+        return FA_ERR_WORKSPACE;
+      const unsigned long long rows = 2ull * sp.ctas * kStreamRows;
+      p.num_splits = 1;
+      p.split_tiles = static_cast<int>(kv_tiles(N, d));
+      p.st_unit0 = sp.unit0;
+      p.st_tiles = sp.tiles;
+      p.st_ctas = sp.ctas;
+      p.o_part = static_cast<float*>(workspace);
+      p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((rows * d * 4 + 255) & ~255ull));
+      FA_DRY_RUN_RETURN();
+      const CUtensorMapDataType dt =
+          dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+      const int bh = static_cast<int>(BH);
+      if (!encode_bhnd_16bit(&p.tm_q, Q, bh, N, d, dt, fa::kF16BlockQ) ||
+          !encode_bhnd_16bit(&p.tm_k, K, bh, N, d, dt, fa::kF16BlockKV) ||
+          !encode_bhnd_16bit(&p.tm_v, V, bh, N, d, dt, fa::kF16BlockKV) ||
+          !encode_bhnd_16bit(&p.tm_o, O, bh, N, d, dt, fa::kF16BlockQ))
+        return FA_ERR_CUDA;
+      if (!fa::fwd_persist_eligible(p)) return FA_ERR_CUDA;
+      const cudaError_t e = fa::launch_fwd_f16(p, dtype == FA_BF16, s);
+      return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    }
+  }
   // fp32 always runs unsplit.
   const SplitPlan plan = dtype == FA_F32 ? SplitPlan{1, -1} : split_plan(B, H, N, d, num_splits, dev.num_sms);
   const int splits = plan.splits;
@@ -584,6 +707,18 @@ int fa_fwd_splitkv_plan(int B, int H, int N, int d, int num_splits, int num_sms,
   return FA_OK;
 }
 
+int fa_fwd_stream_plan(int B, int H, int N, int d, int num_sms, int* unit0, int* tiles, int* ctas) {
+  if (!unit0 || !tiles || !ctas) return FA_ERR_NULL;
+  if (B < 1 || H < 1 || N < 1 || num_sms < 1) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_HEADDIM;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL) return FA_ERR_SHAPE;
+  const StreamPlan sp = stream_plan(B, H, N, d, num_sms);
+  *unit0 = sp.unit0;
+  *tiles = sp.tiles;
+  *ctas = sp.ctas;
+  return FA_OK;
+}
+
 int fa_fwd_splitkv_num_splits(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1) return -FA_ERR_SHAPE;
   if (d != 64 && d != 128 && d != 256) return -FA_ERR_HEADDIM;
@@ -731,6 +866,23 @@ int fa_fwd_debug(const void* Q, const void* K, const void* V, void* O, float* LS
 }
 
 void fa_testing_set_dry_run(int on) { g_dry_run.store(on ? 1 : 0); }
+
+int fa_testing_stream_piece(int tiles, int ctas, int n, int c, int q, int* out) {
+  if (!out || tiles < 1 || ctas < 1 || n < 1 || static_cast<long long>(tiles) * ctas >= (1ll << 31)) return -1;
+  if (q < 0) {
+    if (c < 0 || static_cast<long long>(c) * n >= tiles) return -1;
+    fa::st_unit_ctas(tiles, ctas, n, c, out[0], out[1]);
+    return 1;
+  }
+  if (c < 0 || c >= ctas) return -1;
+  fa::StPiece pc;
+  if (!fa::st_piece(tiles, ctas, n, c, q, pc)) return 0;
+  out[0] = pc.i;
+  out[1] = pc.t0;
+  out[2] = pc.t1;
+  out[3] = pc.slot;
+  return 1;
+}
 
 unsigned int fa_testing_last_timeout_where(void) {
   unsigned int h[2] = {0, 0};

@@ -721,39 +721,59 @@ __device__ __forceinline__ uint32_t xbar_addr(uint32_t base, int i) {
   return base + PCfg<D>::OFF_XBAR + 8u * i;
 }
 
-// The k-th unit of this CTA (units: the total), or -1 past its last.
-// Unmasked: units blockIdx.x + k G. Causal: pairs of units, pair
-// blockIdx.x + (k / 2) G, unit k % 2 of it.
-__device__ __forceinline__ int persist_unit_index(bool causal, int units, int k) {
-  const int G = gridDim.x;
-  const int u = causal ? 2 * (static_cast<int>(blockIdx.x) + (k / 2) * G) + (k & 1)
-                       : static_cast<int>(blockIdx.x) + k * G;
-  return u < units ? u : -1;
-}
-
-// Work unit u of the persistent form: head, first Q row, tiles per sub-tile.
-// Units are numbered head by head, so that the CTAs working at the same time
-// share few heads (their K/V stay in L2). Causal: unit 2i of a head is its
-// Q block nqb-1-i and unit 2i+1 its Q block i, so that the units a CTA takes
-// in pairs (2m, 2m+1) all add up to the same work; units are then handed out
-// in pairs (CTA c takes pairs c, c+G, ...).
-struct PUnit {
-  int bh, row0, nkv0, nkv1;
+// Work item k of this CTA: a whole unit or, in the streamed tail, one piece
+// of a unit (tiles [t0, t0 + nkv1) of its K/V sequence). Units are numbered
+// head by head, so that the CTAs working at the same time share few heads
+// (their K/V stay in L2). Unmasked: whole units blockIdx.x + k G (G CTAs)
+// before the tail, then this CTA's tail pieces. Causal (no tail): unit 2i of
+// a head is its Q block nqb-1-i and unit 2i+1 its Q block i, so that the
+// pairs (2m, 2m+1) all add up to the same work; CTA c takes pairs c, c+G, ...
+// slot: < 0 for a whole unit (O written out), else the part slot of a piece.
+struct PItem {
+  int bh, row0, t0, nkv0, nkv1, slot;
 };
 template <int D>
-__device__ __forceinline__ PUnit persist_unit(const FwdParams& p, int u) {
+__device__ __forceinline__ bool persist_item(const FwdParams& p, int units, int k, PItem& it) {
   using C = Cfg<D>;
   const int nqb = p.N / (2 * C::BM);
-  PUnit U;
-  U.bh = u / nqb;
-  const int w = u % nqb;
+  const int n = p.N / C::BN;  // K/V tiles of a whole unit (sub-tile 1 under the causal mask)
+  const int G = gridDim.x, c = blockIdx.x;
+  int u;
+  it.t0 = 0;
+  it.slot = -1;
+  int t1 = n;
+  if (p.causal) {
+    const long long uu = 2ll * (c + (k / 2) * static_cast<long long>(G)) + (k & 1);
+    if (uu >= units) return false;
+    u = static_cast<int>(uu);
+  } else {
+    const int whole = p.st_ctas > 0 ? p.st_unit0 : units;  // units handed out whole
+    const long long uu = c + static_cast<long long>(k) * G;
+    if (uu < whole) {
+      u = static_cast<int>(uu);
+    } else {
+      if (c >= p.st_ctas) return false;
+      const int rounds = c < whole ? (whole - c + G - 1) / G : 0;
+      StPiece pc;
+      if (!st_piece(p.st_tiles, p.st_ctas, n, c, k - rounds, pc)) return false;
+      u = p.st_unit0 + pc.i;
+      it.t0 = pc.t0;
+      t1 = pc.t1;
+      it.slot = pc.slot;
+    }
+  }
+  it.bh = u / nqb;
+  const int w = u - it.bh * nqb;
   const int qb = p.causal ? ((w & 1) ? w / 2 : nqb - 1 - w / 2) : w;
-  U.row0 = qb * 2 * C::BM;
-  const int end0 = p.causal ? U.row0 + C::BM : p.N;
-  const int end1 = p.causal ? U.row0 + 2 * C::BM : p.N;
-  U.nkv0 = (end0 + C::BN - 1) / C::BN;
-  U.nkv1 = (end1 + C::BN - 1) / C::BN;
-  return U;
+  it.row0 = qb * 2 * C::BM;
+  if (p.causal) {
+    // Tiles per sub-tile: up to the diagonal tile of its last row.
+    it.nkv0 = (it.row0 + C::BM + C::BN - 1) / C::BN;
+    it.nkv1 = (it.row0 + 2 * C::BM + C::BN - 1) / C::BN;
+  } else {
+    it.nkv0 = it.nkv1 = t1 - it.t0;
+  }
+  return true;
 }
 
 // TMA producer (one thread).
@@ -768,15 +788,13 @@ __device__ __forceinline__ void persist_producer(const FwdParams& p, uint32_t ba
   int nq = 0, g = 0;  // units whose Q was loaded; K/V tiles of the units before this one
   int gk = 0, gv = 0; // K and V loads issued (positions in the ring sequence)
   for (int kk = 0;; ++kk) {
-    const int u = persist_unit_index(p.causal, units, kk);
-    if (u < 0) break;
-    const PUnit U = persist_unit<D>(p, u);
+    PItem U;
+    if (!persist_item<D>(p, units, kk, U)) break;
     const int nkv = max(U.nkv0, U.nkv1);
-    // The next unit's Q rows into L2 while this unit runs (its load, later, then hits L2).
+    // The next item's Q rows into L2 while this one runs (its load, later, then hits L2).
     {
-      const int un = persist_unit_index(p.causal, units, kk + 1);
-      if (un >= 0) {
-        const PUnit N2 = persist_unit<D>(p, un);
+      PItem N2;
+      if (persist_item<D>(p, units, kk + 1, N2)) {
         const uint16_t* qn = static_cast<const uint16_t*>(p.q) + (static_cast<size_t>(N2.bh) * p.N + N2.row0) * D;
         l2_prefetch_bulk(qn, 2u * C::Q_SUB_BYTES);
       }
@@ -799,14 +817,16 @@ __device__ __forceinline__ void persist_producer(const FwdParams& p, uint32_t ba
       mbar_arrive_expect_tx(kf, C::KV_BYTES);
 #pragma unroll
       for (int h = 0; h < D / 64; ++h)
-        tma_load_3d(base + C::OFF_K + s * C::KV_BYTES + h * C::KV_HALF_BYTES, &p.tm_k, kf, 64 * h, j * C::BN, U.bh);
+        tma_load_3d(base + C::OFF_K + s * C::KV_BYTES + h * C::KV_HALF_BYTES, &p.tm_k, kf, 64 * h,
+                    (U.t0 + j) * C::BN, U.bh);
       gk = gg + 1;
       if (!wait_bar(bar_addr<D>(base, C::B_VE + s), par, ctl, kWhereVEmpty)) { ok = false; break; }
       const uint32_t vf = bar_addr<D>(base, C::B_VF + s);
       mbar_arrive_expect_tx(vf, C::KV_BYTES);
 #pragma unroll
       for (int h = 0; h < D / 64; ++h)
-        tma_load_3d(base + C::OFF_V + s * C::KV_BYTES + h * C::KV_HALF_BYTES, &p.tm_v, vf, 64 * h, j * C::BN, U.bh);
+        tma_load_3d(base + C::OFF_V + s * C::KV_BYTES + h * C::KV_HALF_BYTES, &p.tm_v, vf, 64 * h,
+                    (U.t0 + j) * C::BN, U.bh);
       gv = gg + 1;
     }
     if (!ok) break;
@@ -830,9 +850,8 @@ __device__ __forceinline__ void persist_mma(const FwdParams& p, uint32_t base, u
   const uint32_t b_drain = bar_addr<D>(base, C::B_DRAIN);
   int k = 0, g = 0, gp0 = 0, gp1 = 0;  // units, K/V tiles, P products of sub-tile 0 and 1 so far
   for (;; ++k) {
-    const int u = persist_unit_index(p.causal, units, k);
-    if (u < 0) break;
-    const PUnit U = persist_unit<D>(p, u);
+    PItem U;
+    if (!persist_item<D>(p, units, k, U)) break;
     const int nkv = max(U.nkv0, U.nkv1);
     if (!wait_bar_warp(bar_addr<D>(base, C::B_Q), k & 1, ctl, kWhereQ)) break;
     tc_fence_after();
@@ -879,17 +898,16 @@ __device__ __forceinline__ void persist_softmax(const FwdParams& p, uint32_t bas
   const float tau = rescale_threshold(p);
   int k = 0, g = 0, gs = 0;  // units, K/V tiles, S products of this sub-tile so far
   for (;; ++k) {
-    const int u = persist_unit_index(p.causal, units, k);
-    if (u < 0) break;
-    const PUnit U = persist_unit<D>(p, u);
+    PItem U;
+    if (!persist_item<D>(p, units, k, U)) break;
     const int nkv = max(U.nkv0, U.nkv1), nkv_s = sub ? U.nkv1 : U.nkv0;
     const int my_row = U.row0 + C::BM * sub + t;
     const int row_end = p.causal ? min(p.N, my_row + 1) : p.N;
     float m_ref = -INFINITY, l = 0.f, l_o = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv_s; ++j) {
-      if (!softmax_tile<D, BF16>(p, base, sub, t, lane, t_s, t_o, c, tau, row_end - j * C::BN, j, g + j, gs + j,
-                                 m_ref, l, l_o, ctl)) {
+      if (!softmax_tile<D, BF16>(p, base, sub, t, lane, t_s, t_o, c, tau, row_end - (U.t0 + j) * C::BN, j, g + j,
+                                 gs + j, m_ref, l, l_o, ctl)) {
         ok = false;
         break;
       }
@@ -915,8 +933,36 @@ __device__ __forceinline__ void persist_softmax(const FwdParams& p, uint32_t bas
     // The whole warpgroup agrees before the epilogue, whose named barriers need all 128 threads.
     if (!named_bar_and(1 + sub, 128, ok)) break;
 
-    // ---- epilogue: O / l -> dtype -> staging (64 columns at a time) -> TMA store; LSE ----
     tc_fence_after();
+    if (U.slot >= 0) {
+      // ---- a piece of a tail unit: its normalised fp32 O and LSE to its slot ----
+      const bool empty = !(l > 0.f);
+      const float inv_l = empty ? 0.f : 1.0f / (BF16 ? l_o : l);
+      const size_t prow = static_cast<size_t>(U.slot) * (2 * C::BM) + C::BM * sub + t;
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t r[32];
+        tmem_ld32(t_o + 32 * q, r);
+        tmem_ld_wait();
+        reg_fence(r);
+        if (q == D / 32 - 1) {
+          // O_sub has been read: the next item's first P.V may overwrite it.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(xbar_addr<D>(base, PCfg<D>::X_OF + sub));
+        }
+        float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D + 32 * q);
+#pragma unroll
+        for (int u2 = 0; u2 < 8; ++u2)
+          dst[u2] = make_float4(__uint_as_float(r[4 * u2]) * inv_l, __uint_as_float(r[4 * u2 + 1]) * inv_l,
+                                __uint_as_float(r[4 * u2 + 2]) * inv_l, __uint_as_float(r[4 * u2 + 3]) * inv_l);
+      }
+      p.lse_part[prow] = empty ? -INFINITY : (m_ref + lg2_approx(l)) * kLn2;
+      g += nkv;
+      gs += nkv_s;
+      continue;
+    }
+    // ---- epilogue: O / l -> dtype -> staging (64 columns at a time) -> TMA store; LSE ----
     uint32_t pk[D / 2];
     {
       const bool empty = !(l > 0.f);
@@ -1031,6 +1077,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_persist_kernel(cons
 // testing build's traces. On GB300 it measured +1.4 % on B=8 H=32 N=4096,
 // +5 % causal and +5 % on B=8 H=12 N=2048 (bit-identical results). The
 // strict-order build keeps one CTA per unit.
+// A streamed tail (st_ctas > 0) takes the same conditions, unmasked only,
+// with its slots in o_part / lse_part and at most one range per CTA.
 template <int D>
 bool persist_eligible(const FwdParams& p) {
 #ifdef FA_STRICT_MMA_ORDER
@@ -1038,11 +1086,78 @@ bool persist_eligible(const FwdParams& p) {
   return false;
 #else
   if (D != 128) return false;
+  if (p.st_ctas > 0) {
+    const long long units = static_cast<long long>(p.B) * p.H * (p.N / (2 * Cfg<D>::BM));
+    if (p.causal || p.o_part == nullptr || p.lse_part == nullptr || p.st_ctas > p.num_sms || p.st_unit0 < 0 ||
+        p.st_unit0 >= units || p.st_unit0 % p.num_sms != 0 ||
+        static_cast<long long>(p.st_tiles) != (units - p.st_unit0) * (p.N / Cfg<D>::BN) ||
+        static_cast<long long>(p.st_tiles) * p.st_ctas >= (1ll << 31))
+      return false;
+  }
   return p.num_splits == 1 && p.qunit0 == 0 && p.qunit_count == 0 && !p.partial && p.klen == nullptr &&
          p.Nk == p.N && p.N % (p.causal ? 4 * Cfg<D>::BM : 2 * Cfg<D>::BM) == 0 && p.stats_trace == nullptr &&
          p.timeline == nullptr &&
          p.inject == 0;
 #endif
+}
+
+// Merge of the streamed tail's pieces: for each row of a tail unit cut into
+// pieces, LSE = m + log sum_s exp(LSE_s - m) and O = sum_s exp(LSE_s - LSE)
+// O_s over its pieces s (the block merge of the Triton page, section 2.3, in
+// LSE form; m the largest LSE_s). Units that one CTA computed whole are
+// skipped: their O and LSE are already written. One warp per row.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) fa_merge_stream_kernel(const __grid_constant__ FwdParams p) {
+  constexpr int E = D / 32;
+  constexpr int ROWS = 2 * Cfg<D>::BM;  // rows of a unit
+  const int n = p.N / Cfg<D>::BN;
+  const int i = blockIdx.x / (ROWS / 8);  // tail unit; 8 warps per block, ROWS / 8 blocks per unit
+  const int r = (blockIdx.x % (ROWS / 8)) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  int c_lo, c_hi;
+  st_unit_ctas(p.st_tiles, p.st_ctas, n, i, c_lo, c_hi);
+  if (c_lo == c_hi) return;
+  const int x = i * n;
+  float m = -INFINITY;
+  for (int cc = c_lo; cc <= c_hi; ++cc) {
+    const int a = st_begin(p.st_tiles, p.st_ctas, cc);
+    if (a == st_begin(p.st_tiles, p.st_ctas, cc + 1)) continue;  // an empty range
+    const int slot = 2 * cc + (a >= x ? 0 : 1);
+    m = fmaxf(m, p.lse_part[static_cast<size_t>(slot) * ROWS + r]);
+  }
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float l = 0.f;
+  if (m > -INFINITY) {
+    for (int cc = c_lo; cc <= c_hi; ++cc) {
+      const int a = st_begin(p.st_tiles, p.st_ctas, cc);
+      if (a == st_begin(p.st_tiles, p.st_ctas, cc + 1)) continue;
+      const size_t prow = static_cast<size_t>(2 * cc + (a >= x ? 0 : 1)) * ROWS + r;
+      const float w = ex2_approx((p.lse_part[prow] - m) * kLog2e);
+      l += w;
+      const float4* src = reinterpret_cast<const float4*>(p.o_part + prow * D + lane * E);
+#pragma unroll
+      for (int e = 0; e < E / 4; ++e) {
+        const float4 v = src[e];
+        acc[4 * e] = fmaf(w, v.x, acc[4 * e]);
+        acc[4 * e + 1] = fmaf(w, v.y, acc[4 * e + 1]);
+        acc[4 * e + 2] = fmaf(w, v.z, acc[4 * e + 2]);
+        acc[4 * e + 3] = fmaf(w, v.w, acc[4 * e + 3]);
+      }
+    }
+  }
+  const float inv = l > 0.f ? 1.0f / l : 0.f;
+  uint32_t pk[E / 2];
+#pragma unroll
+  for (int e = 0; e < E / 2; ++e) pk[e] = pack2<BF16>(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+  const int nqb = p.N / ROWS;
+  const int u = p.st_unit0 + i;
+  const long long row = static_cast<long long>(u / nqb) * p.N + (u % nqb) * ROWS + r;
+  uint16_t* out = static_cast<uint16_t*>(p.o) + row * D + lane * E;
+  static_assert(E == 4, "one 8-byte store per lane");
+  *reinterpret_cast<uint2*>(out) = make_uint2(pk[0], pk[1]);
+  if (lane == 0) p.lse[row] = m > -INFINITY ? m + lg2_approx(l) * kLn2 : -INFINITY;
 }
 
 template <int D, bool BF16>
@@ -1066,6 +1181,7 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream) {
     attr_done.fetch_or(bit);
   }
   const long long all_qunits = static_cast<long long>(p.B) * p.H * ((p.N + 2 * C::BM - 1) / (2 * C::BM));
+  if (p.st_ctas > 0 && !persist_eligible<D>(p)) return cudaErrorInvalidValue;
   if constexpr (D == 128) {
     if (persist_eligible<D>(p)) {
       auto pk = fa_fwd_persist_kernel<D, BF16>;
@@ -1081,8 +1197,14 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream) {
       }
       if (all_qunits <= 0 || all_qunits > 0x7fffffffLL) return cudaErrorInvalidValue;
       const long long work = p.causal ? (all_qunits + 1) / 2 : all_qunits;  // causal: pairs of units
-      const long long ctas = std::min<long long>(work, p.num_sms > 0 ? p.num_sms : 1);
+      // With a streamed tail every SM takes part (the whole units fill rounds of num_sms).
+      const long long ctas = p.st_ctas > 0 ? p.num_sms : std::min<long long>(work, p.num_sms > 0 ? p.num_sms : 1);
       pk<<<dim3(static_cast<unsigned>(ctas)), dim3(C::THREADS), PCfg<D>::SMEM_BYTES, stream>>>(p);
+      e = cudaGetLastError();
+      if (e != cudaSuccess || p.st_ctas == 0) return e;
+      const long long blocks = (all_qunits - p.st_unit0) * (2 * C::BM / 8);
+      if (blocks <= 0 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+      fa_merge_stream_kernel<D, BF16><<<dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream>>>(p);
       return cudaGetLastError();
     }
   }
@@ -1178,6 +1300,8 @@ cudaError_t launch_merge(const FwdParams& p, bool bf16, cudaStream_t stream) {
   if (p.d == 64) return bf16 ? launch_merge_t<64, true>(p, stream) : launch_merge_t<64, false>(p, stream);
   return cudaErrorInvalidValue;
 }
+
+bool fwd_persist_eligible(const FwdParams& p) { return p.d == 128 && persist_eligible<128>(p); }
 
 cudaError_t launch_fwd_f16(const FwdParams& p, bool bf16, cudaStream_t stream) {
   if (p.d == 128) return bf16 ? launch<128, true>(p, stream) : launch<128, false>(p, stream);

@@ -64,6 +64,16 @@ struct alignas(64) FwdParams {
   // (klen[b]: keys j >= klen[b] masked; NULL = all N keys).
   int causal;
   const int* klen;
+  // Streamed tail of the persistent d = 128 form (st_ctas > 0; unmasked, no
+  // split): units before st_unit0 are handed out whole, round by round; the
+  // K/V tiles of units [st_unit0, units) are laid end to end (st_tiles in
+  // all) and CTA c < st_ctas takes the range [st_begin(c), st_begin(c + 1)).
+  // Units a range boundary cuts are computed in pieces: normalised fp32 O
+  // and LSE of each piece go to a slot of o_part / lse_part ([2 st_ctas, 256,
+  // d] and [2 st_ctas, 256]) and a merge pass combines them.
+  int st_unit0;
+  int st_tiles;
+  int st_ctas;
   // Used only by the testing build (-DFA_TESTING); zero / NULL otherwise.
   int inject;                       // 1: the producer skips the V load of tile 0
   float* stats_trace;               // [B*H*N, nkv, 2]: (m in natural-log units, l) after each K/V tile
@@ -122,6 +132,38 @@ constexpr int fwd_kv_box_rows(int d) { return d == 256 ? kD256BlockKV : kF16Bloc
 // (two 128-row sub-tiles for d = 64 / 128, one 128-row tile for d = 256).
 constexpr int fwd_q_block(int d) { return d == 256 ? kD256BlockQ : 2 * kF16BlockQ; }
 
+// Streamed tail (see FwdParams::st_ctas): first tail tile of CTA c's range
+// (c = ctas: the end of the last range). Ranges are as equal as whole tiles
+// allow; some are empty when the tail has fewer tiles than CTAs. 32-bit
+// arithmetic: the host streams a tail only when tiles * ctas < 2^31.
+__host__ __device__ inline int st_begin(int tiles, int ctas, int c) { return c * tiles / ctas; }
+// One piece of CTA c's range: its q-th (0: the one holding the range's first
+// tile), in tail unit i (counted from st_unit0), tiles [t0, t1) of the n in a
+// unit; slot < 0 when the piece is the whole unit (written out directly),
+// else 2c for the range's first piece and 2c + 1 for its last.
+struct StPiece {
+  int i, t0, t1, slot;
+};
+__host__ __device__ inline bool st_piece(int tiles, int ctas, int n, int c, int q, StPiece& pc) {
+  const int a = st_begin(tiles, ctas, c), b = st_begin(tiles, ctas, c + 1);
+  const int x = q == 0 ? a : (a / n + q) * n;
+  if (q < 0 || x >= b) return false;
+  pc.i = x / n;
+  pc.t0 = x - pc.i * n;
+  pc.t1 = b - x < n - pc.t0 ? pc.t0 + (b - x) : n;
+  pc.slot = (pc.t0 == 0 && pc.t1 == n) ? -1 : 2 * c + (q == 0 ? 0 : 1);
+  return true;
+}
+// The CTAs whose ranges hold tiles of tail unit i: c_lo .. c_hi (one CTA: the
+// unit is whole in it). A CTA c in between with an empty range has no piece;
+// the others' pieces sit in slot 2c when the range starts inside the unit,
+// 2c + 1 when it started in an earlier one.
+__host__ __device__ inline void st_unit_ctas(int tiles, int ctas, int n, int i, int& c_lo, int& c_hi) {
+  const int x = i * n, e = x + n;
+  c_lo = ((x + 1) * ctas - 1) / tiles;
+  c_hi = (e * ctas - 1) / tiles;
+}
+
 // Timeline trace layout of the testing build.
 constexpr int kTraceCtas = 8, kTraceTiles = 64, kTraceEvents = 32;
 enum : int {
@@ -148,6 +190,9 @@ cudaError_t launch_fwd_f16(const FwdParams& p, bool bf16, cudaStream_t stream);
 // with no key in any part get O = 0, LSE = -inf. Serves split-KV and fa_merge
 // alike.
 cudaError_t launch_merge(const FwdParams& p, bool bf16, cudaStream_t stream);
+// Whether the persistent d = 128 forward takes this launch (also the
+// condition for a streamed tail, st_ctas > 0).
+bool fwd_persist_eligible(const FwdParams& p);
 // Backward: row statistics (D, LSE * log2 e) and a zeroed dQ accumulator;
 // the main dK/dV/dQ kernel; the dQ accumulator rounded into dQ.
 // Head dimension 64, 128 or 256 (the last through launch_bwd_main_d256).

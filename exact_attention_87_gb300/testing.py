@@ -46,6 +46,8 @@ def lib():
         L.fa_get_device_status.argtypes = [vp]
         L.fa_get_device_status.restype = i
         L.fa_testing_last_timeout_where.restype = ctypes.c_uint
+        L.fa_testing_stream_piece.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]
+        L.fa_testing_stream_piece.restype = i
         _lib = L
     return _lib
 
@@ -143,3 +145,11 @@ def device_status(stream=None) -> int:
 
 def last_timeout_where() -> int:
     return lib().fa_testing_last_timeout_where()
+
+
+def stream_piece(tiles: int, ctas: int, n: int, c: int, q: int):
+    """fa_testing_stream_piece: (rc, values) with values the 4 outputs (q >= 0:
+    unit, first tile, end tile, slot) or the 2 of q = -1 (c_lo, c_hi)."""
+    out = (ctypes.c_int * 4)()
+    rc = lib().fa_testing_stream_piece(tiles, ctas, n, c, q, out)
+    return rc, list(out[:4] if q >= 0 else out[:2])

@@ -119,12 +119,23 @@ int fa_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE,
  *             the full waves run unsplit and only the last wave's units are
  *             split (as many ways as fit in one wave) and merged; that is
  *             three launches (full waves, split tail, merge of its rows).
+ *             For unmasked d = 128 inputs with N a multiple of 256 the
+ *             automatic count may instead stream the tail: the persistent
+ *             kernel runs the full rounds of Q blocks whole and cuts the K/V
+ *             tiles of the units left over into one contiguous range per
+ *             SM; units a range boundary cuts are computed in pieces and
+ *             merged (two launches; fa_fwd_stream_plan).
  * workspace:  device memory owned by the caller, 256-byte aligned, at least
  *             fa_fwd_splitkv_workspace_size(...) bytes; holds the per-range
  *             fp32 O and LSE of the split rows only (all B*H*N rows, or under
  *             the tail plan the rows of the last wave's units). Unused (may be
  *             NULL) when the effective split count is 1, and for FA_F32
- *             inputs, which always run unsplit.
+ *             inputs, which always run unsplit. Under the streamed tail it
+ *             holds the pieces' fp32 O and LSE (two 256-row slots per SM
+ *             that shares the tail); its size is then the larger of that
+ *             and what the key-range plan of the same arguments needs, so
+ *             that masked calls (fa_fwd_splitkv_ex, which always take the
+ *             key-range plan) fit the same workspace.
  * Errors: those of fa_fwd, plus FA_ERR_WORKSPACE. Two or three launches are
  * enqueued on `stream` (fa_fwd_splitkv_launches); nothing is synchronised.
  */
@@ -174,11 +185,14 @@ int fa_fwd_splitkv_launches(int B, int H, int N, int d, int num_splits);
  * (128 at d = 256); K/V tiles hold 128 keys (64 at d = 256).
  * Outputs (all written on success):
  *   splits           key ranges of each split unit after clamping to whole
- *                    K/V tiles (1: nothing is split);
+ *                    K/V tiles (1: nothing is split); under the streamed
+ *                    tail the most pieces one unit is cut into;
  *   first_split_unit index of the first split unit: 0 when every unit is
  *                    split, B*H*ceil(N/q) when none is, in between under the
- *                    tail plan (the units of the last, partial wave of SMs);
- *   launches         kernel launches enqueued: 1, 2 or 3;
+ *                    tail plan (the units of the last, partial wave of SMs)
+ *                    and the streamed tail (its first unit);
+ *   launches         kernel launches enqueued: 1, 2 or 3 (the streamed
+ *                    tail: 2);
  *   workspace_bytes  the workspace fa_fwd_splitkv needs (0: none).
  * Errors: FA_ERR_NULL (an output pointer is NULL), FA_ERR_SHAPE (B, H, N or
  * num_sms < 1, num_splits < 0, B*H >= 2^31), FA_ERR_HEADDIM (d not 64, 128 or
@@ -186,6 +200,27 @@ int fa_fwd_splitkv_launches(int B, int H, int N, int d, int num_splits);
  */
 int fa_fwd_splitkv_plan(int B, int H, int N, int d, int num_splits, int num_sms, int *splits,
                         long long *first_split_unit, int *launches, unsigned long long *workspace_bytes);
+
+/*
+ * The streamed tail of fa_fwd_splitkv's automatic plan (num_splits = 0) for
+ * unmasked FA_F16 / FA_BF16 inputs of this shape on a device with `num_sms`
+ * SMs, computed on the host. The persistent d = 128 kernel hands out Q blocks
+ * (units of 256 rows of one (b, h), numbered head by head) whole in rounds of
+ * num_sms until `unit0`; the `tiles` K/V tiles (128 keys) of units unit0 ..
+ * B*H*N/256 - 1, laid end to end, are then cut into `ctas` contiguous ranges,
+ * range c = [floor(c * tiles / ctas), floor((c + 1) * tiles / ctas)) taken by
+ * SM c. A unit that a range boundary cuts is computed in pieces, each written
+ * as normalised fp32 O and LSE, and a merge pass combines them (the block
+ * merge in LSE form, as fa_fwd_splitkv). The tail is streamed when the cost
+ * model expects it to shorten the pass: the units then end in a partial last
+ * round (B*H*N/256 not a multiple of num_sms) long enough to pay for the merge.
+ * Outputs (all written on success): ctas = 0 when the plan does not stream
+ * the tail (other d, N not a multiple of 256, or it does not pay; unit0 =
+ * tiles = 0 then); else 1 <= ctas <= num_sms, unit0 a multiple of num_sms.
+ * Errors: FA_ERR_NULL (an output pointer is NULL), FA_ERR_SHAPE (B, H, N or
+ * num_sms < 1, B*H >= 2^31), FA_ERR_HEADDIM (d not 64, 128 or 256).
+ */
+int fa_fwd_stream_plan(int B, int H, int N, int d, int num_sms, int *unit0, int *tiles, int *ctas);
 
 /* Workspace bytes fa_fwd_splitkv needs for this shape and split count on the
  * current device (num_splits = 0: the automatic plan, which depends on the

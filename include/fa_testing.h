@@ -80,6 +80,19 @@ void fa_testing_set_dry_run(int on);
  * not cleared by this call). */
 unsigned int fa_testing_last_timeout_where(void);
 
+/*
+ * The streamed tail's partition as the persistent kernel walks it (host
+ * copy of the device arithmetic, see fa_fwd_stream_plan): piece q (0 = the
+ * one holding the range's first tile) of range c among `ctas` over `tiles`
+ * tail tiles of n tiles per unit. Returns 1 and out[0..3] = (tail unit,
+ * first tile, end tile, part slot; slot -1 = whole unit), or 0 when the
+ * range has no piece q. With q = -1 it returns 1 and out[0..1] = (c_lo,
+ * c_hi), the ranges that hold tiles of tail unit c (the merge's view).
+ * Requires tiles >= 1, 1 <= ctas, tiles * ctas < 2^31, n >= 1; returns -1
+ * for arguments outside that (out untouched).
+ */
+int fa_testing_stream_piece(int tiles, int ctas, int n, int c, int q, int *out);
+
 #ifdef __cplusplus
 }
 #endif

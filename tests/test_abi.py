@@ -256,9 +256,9 @@ def _tail_expectation(B, H, N, d, num_sms):
 
 
 @pytest.mark.parametrize("B,H,N,d,num_sms", [
-    (1, 8, 16384, 128, 152),   # 512 units: 3 full waves, 56 left split 2 ways
-    (1, 8, 16384, 128, 148),   # 68 left, split 2 ways
-    (1, 4, 10240, 128, 152),   # 160 units: 1 full wave, 8 left split 16 ways
+    (1, 8, 16000, 128, 152),   # 504 units (N not a multiple of 256): 3 full waves, 48 left split 3 ways
+    (1, 8, 16000, 128, 148),   # 60 left, split 2 ways
+    (1, 4, 10000, 128, 152),   # 160 units: 1 full wave, 8 left split 16 ways
     (1, 4, 16384, 256, 152),   # d = 256: 512 units of 128 rows, 3 full waves, 56 left split 2 ways
 ])
 def test_splitkv_plan_tail_on_the_host(L, B, H, N, d, num_sms):
@@ -281,11 +281,11 @@ def test_splitkv_plan_uniform_and_unsplit_on_the_host(L):
     rc, p = fa.fa_fwd_splitkv_plan(8, 32, 4096, 128, 0, 152)
     assert p == {"splits": 1, "first_split_unit": 4096, "launches": 1, "workspace_bytes": 0}
     # a short last wave whose split saves less than the launch boundary costs:
-    # d = 256, B=4 H=16 N=4096 (2048 units, 13.5 waves) and d = 128, B=8 H=12
-    # N=2048 (768 units, 5.05 waves)
+    # d = 256, B=4 H=16 N=4096 (2048 units, 13.5 waves); d = 128, B=8 H=12
+    # N=2000 (N not a multiple of 256: no streamed tail; 768 units, 5.05 waves)
     rc, p = fa.fa_fwd_splitkv_plan(4, 16, 4096, 256, 0, 152)
     assert p == {"splits": 1, "first_split_unit": 2048, "launches": 1, "workspace_bytes": 0}
-    rc, p = fa.fa_fwd_splitkv_plan(8, 12, 2048, 128, 0, 152)
+    rc, p = fa.fa_fwd_splitkv_plan(8, 12, 2000, 128, 0, 152)
     assert p == {"splits": 1, "first_split_unit": 768, "launches": 1, "workspace_bytes": 0}
     # d = 256: explicit counts over 64-key tiles
     rc, p = fa.fa_fwd_splitkv_plan(4, 16, 4096, 256, 8, 152)
@@ -312,6 +312,13 @@ def test_splitkv_plan_invariants_over_shapes(L):
                     nqb = -(-N // qr)
                     units = B * H * nqb
                     first, s = p["first_split_unit"], p["splits"]
+                    rc, sp = fa.fa_fwd_stream_plan(B, H, N, d, num_sms)
+                    assert rc == fa.FA_OK
+                    if ns == 0 and sp["ctas"] > 0:
+                        # the streamed tail (its own tests check the partition)
+                        assert d == 128 and N % 256 == 0 and first == sp["unit0"] and p["launches"] == 2
+                        assert p["workspace_bytes"] >= 2 * sp["ctas"] * 256 * (4 * d + 4)
+                        continue
                     if s == 1:
                         assert first == units and p["launches"] == 1 and p["workspace_bytes"] == 0
                         continue

@@ -1114,6 +1114,8 @@ class PersistModel(BwdModel):
 @pytest.mark.parametrize("units", [
     [(3, 3)], [(2, 2), (2, 2), (2, 2)], [(1, 2), (4, 5), (2, 3)], [(5, 6), (1, 2)], [(1, 1), (1, 1), (1, 1), (1, 1)],
     [(3, 4), (3, 4), (1, 2), (6, 7)],
+    # the streamed tail: whole units, then pieces of a few tiles (equal on both sub-tiles)
+    [(4, 4), (4, 4), (1, 1), (2, 2)], [(3, 3), (1, 1)],
 ], ids=lambda u: "-".join(f"{a}.{b}" for a, b in u))
 def test_forward_persistent_barrier_protocol(units):
     rng = random.Random(hash(tuple(units)) & 0xFFFFFFFF)

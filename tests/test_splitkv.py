@@ -71,7 +71,7 @@ def test_splitkv_workspace_errors():
 
 
 @pytest.mark.parametrize("B,H,N,d,dtype", [
-    (1, 4, 10240, 128, "bf16"),   # 160 units: on 152 SMs one full wave, the 8 left over split 16 ways
+    (1, 4, 10000, 128, "bf16"),   # 160 units: on 152 SMs one full wave, the 8 left over split 16 ways
     (1, 2, 20000, 128, "f16"),    # N not a multiple of 256: the last Q block of a head is partial
     (1, 4, 16384, 256, "bf16"),   # d = 256: 512 units of 128 rows, 3 full waves, the 56 left split 2 ways
 ])
@@ -103,7 +103,7 @@ def test_splitkv_tail_plan_workspace_covers_only_the_tail_rows():
     """Under the tail plan the partial buffers hold the split rows only: the
     workspace is smaller than the one every row split alike would need, a
     byte less is refused, and the launches write nothing past its end."""
-    B, H, N, d = 1, 4, 10240, 128
+    B, H, N, d = 1, 4, 10000, 128
     assert fa.fa_fwd_splitkv_launches(B, H, N, d, 0) == 3
     splits = fa.fa_fwd_splitkv_num_splits(B, H, N, d)
     need = fa.fa_fwd_splitkv_workspace_size(B, H, N, d, 0)
@@ -139,3 +139,82 @@ def test_splitkv_plan_matches_the_device_queries():
             assert p["workspace_bytes"] == fa.fa_fwd_splitkv_workspace_size(B, H, N, d, ns)
             if ns == 0:
                 assert p["splits"] == fa.fa_fwd_splitkv_num_splits(B, H, N, d)
+
+
+def _stream_plan_here(B, H, N):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rc, sp = fa.fa_fwd_stream_plan(B, H, N, 128, sms)
+    assert rc == fa.FA_OK
+    if sp["ctas"] == 0:
+        pytest.skip(f"the plan does not stream this shape's tail on {sms} SMs")
+    return sp
+
+
+@pytest.mark.parametrize("B,H,N,dtype,sig", [
+    (1, 20, 2048, "bf16", 3.0),   # 160 units: one full round, 8 units (128 tiles) over 76 CTAs, up to 10 pieces
+    (3, 7, 2048, "f16", 1.0),     # 168 units: one full round, 16 units (256 tiles) over 76 CTAs
+    (1, 2, 4096, "bf16", 2.0),    # 32 units: no full round, every unit streamed over 126 CTAs
+])
+def test_stream_tail_parity(B, H, N, dtype, sig):
+    """The streamed tail of the automatic plan (persistent kernel: full rounds
+    of whole units, then the left-over units' K/V tiles cut into one range
+    per CTA, the cut units merged): every output against the oracle, and
+    the rows of the whole units bit-identical to the unsplit pass, which
+    computes them with the same code."""
+    sp = _stream_plan_here(B, H, N)
+    q, k, v = make_qkv(B, H, N, 128, dtype, sigma_qk=sig, seed=41, wid=12000 + N + H)
+    if sig > 1:
+        k, v = rising_norm_order(k, v)
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    o, lse = fa.attention(qc, kc, vc, num_splits=0)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    o_ref, lse_ref = oracle.attn(q, k, v)
+    res = compare(o.cpu().double().numpy(), lse.cpu().double().numpy(), o_ref, lse_ref, dtype)
+    assert res["ok"], res
+    o1, lse1 = fa.attention(qc, kc, vc, num_splits=1)
+    torch.cuda.synchronize()
+    rows = sp["unit0"] * 256  # units are numbered head by head, 256 rows each
+    assert torch.equal(o.view(-1, 128)[:rows], o1.view(-1, 128)[:rows])
+    assert torch.equal(lse.view(-1)[:rows], lse1.view(-1)[:rows])
+
+
+def test_stream_tail_workspace_bound():
+    """The streamed path needs exactly the reported workspace: a byte less is
+    refused, and nothing is written past its end."""
+    B, H, N, d = 1, 20, 2048, 128
+    _stream_plan_here(B, H, N)
+    need = fa.fa_fwd_splitkv_workspace_size(B, H, N, d, 0)
+    q, k, v = make_qkv(B, H, N, d, "bf16", sigma_qk=1.0, seed=42, wid=12100)
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    o, lse = torch.empty_like(qc), torch.empty((B, H, N), device="cuda")
+    ws = torch.full((need + 65536,), 0x5A, dtype=torch.uint8, device="cuda")
+    args = (qc.data_ptr(), kc.data_ptr(), vc.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, d ** -0.5,
+            fa.FA_BF16, 0)
+    assert fa.fa_fwd_splitkv(*args, ws.data_ptr(), need - 1, None) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_fwd_splitkv(*args, ws.data_ptr(), need, None) == fa.FA_OK
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    assert bool((ws[need:] == 0x5A).all())
+    o1, lse1 = fa.attention(qc, kc, vc, num_splits=1)
+    torch.cuda.synchronize()
+    assert float((o.float() - o1.float()).abs().max()) <= 1e-2
+    assert float((lse - lse1).abs().max()) <= 1e-4 * max(1.0, float(lse1.abs().max()))
+
+
+def test_stream_tail_noalloc_matches_workspace_call():
+    """fa_fwd_splitkv_noalloc takes the streamed tail through the built-in
+    scratch: bit-identical to the caller-workspace call, twice in a row."""
+    B, H, N, d = 3, 7, 2048, 128
+    _stream_plan_here(B, H, N)
+    q, k, v = make_qkv(B, H, N, d, "f16", sigma_qk=1.0, seed=43, wid=12200)
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    o_ref, lse_ref = fa.attention(qc, kc, vc, num_splits=0)
+    for _ in range(2):
+        o, lse = torch.empty_like(qc), torch.empty((B, H, N), device="cuda")
+        rc = fa.fa_fwd_splitkv_noalloc(qc.data_ptr(), kc.data_ptr(), vc.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                       B, H, N, d, d ** -0.5, fa.FA_F16, 0)
+        assert rc == fa.FA_OK
+        torch.cuda.synchronize()
+        assert fa.fa_get_device_status() == fa.FA_OK
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
