@@ -272,20 +272,22 @@ long long plan_row0(const SplitPlan& plan, int N, int d) {
 }
 
 // Streamed tail of the persistent d = 128 forward (unmasked, N a multiple of
-// 256; see fa::FwdParams::st_ctas): the full rounds of num_sms units run
-// whole, the K/V tiles of the units left over are cut into one contiguous
-// range per CTA, and the units a range boundary cuts are merged afterwards.
-// Modelled time, in tiles of one 256-row unit and one 128-key tile on one SM
+// 256 and at most 4096, where the persistent form runs; see
+// fa::FwdParams::st_ctas): the full rounds of num_sms units run whole, the
+// K/V tiles of the units left over are cut into one contiguous range per
+// CTA, and the units a range boundary cuts are merged afterwards. Modelled
+// time, in tiles of one 256-row unit and one 128-key tile on one SM
 // (t_p ~ 1.63 us on GB300 in the persistent kernel):
 //   whole units only:  ceil(units / num_sms) * n
-//   streamed tail:     R * n + ceil(tail tiles / ctas) + 1
+//   streamed tail:     1.04 * (R * n + ceil(tail tiles / ctas) + 1)
 //                      + (3 us + 2 * partial bytes / 4 TB/s) / t_p   (the merge)
 // with R full rounds, n tiles per unit and `ctas` CTAs sharing the tail
 // (num_sms / k for k = 1..8, at most kStreamMaxCtas so that the part slots
-// fit the library's 32 MiB scratch). The tail is streamed only when that
-// saves at least two tiles. On B=8 H=12 N=2048 (768 units, 5.05 rounds)
-// it takes 2-tile ranges on 64 CTAs; on B=8 H=32 N=4096 (26.9 rounds) it
-// does not pay.
+// fit the library's 32 MiB scratch); 1.04: the tile rate of the kernel
+// instantiation that carries the tail's code (measured 2-5 % below the one
+// without). The tail is streamed only when that saves at least two tiles.
+// On B=8 H=12 N=2048 (768 units, 5.05 rounds) it takes 2-tile ranges on 76
+// CTAs; on B=8 H=32 N=4096 (26.9 rounds) it does not pay.
 struct StreamPlan {
   int unit0 = 0;            // first tail unit (R * num_sms)
   int tiles = 0;            // K/V tiles of the tail
@@ -306,7 +308,7 @@ unsigned long long stream_workspace_bytes(int ctas, int d) {
 
 StreamPlan stream_plan(int B, int H, int N, int d, int num_sms) {
   StreamPlan best;
-  if (d != 128 || N % kStreamRows != 0 || num_sms < 1) return best;
+  if (d != 128 || N % kStreamRows != 0 || N > 4096 || num_sms < 1) return best;
   const long long units = static_cast<long long>(B) * H * (N / kStreamRows);
   const int n = N / fa::kF16BlockKV;
   const long long R = units / num_sms, tail = units - R * num_sms;
@@ -330,7 +332,7 @@ StreamPlan stream_plan(int B, int H, int N, int d, int num_sms) {
       if (pc.slot >= 0) ++partial;
       if (b > (a / n + 1) * n && b % n != 0) ++partial;
     }
-    const double t = static_cast<double>(R) * n + static_cast<double>((T + ctas - 1) / ctas) + 1.0 +
+    const double t = 1.04 * (static_cast<double>(R) * n + static_cast<double>((T + ctas - 1) / ctas) + 1.0) +
                      (3.0 + 2.0 * partial * stream_slot_bytes(d) / 4e12 * 1e6) / t_p;
     if (t < best_t) {
       best_t = t;

@@ -732,7 +732,7 @@ __device__ __forceinline__ uint32_t xbar_addr(uint32_t base, int i) {
 struct PItem {
   int bh, row0, t0, nkv0, nkv1, slot;
 };
-template <int D>
+template <int D, bool STREAM>
 __device__ __forceinline__ bool persist_item(const FwdParams& p, int units, int k, PItem& it) {
   using C = Cfg<D>;
   const int nqb = p.N / (2 * C::BM);
@@ -747,10 +747,12 @@ __device__ __forceinline__ bool persist_item(const FwdParams& p, int units, int 
     if (uu >= units) return false;
     u = static_cast<int>(uu);
   } else {
-    const int whole = p.st_ctas > 0 ? p.st_unit0 : units;  // units handed out whole
+    const int whole = STREAM ? p.st_unit0 : units;  // units handed out whole
     const long long uu = c + static_cast<long long>(k) * G;
     if (uu < whole) {
       u = static_cast<int>(uu);
+    } else if (!STREAM) {
+      return false;
     } else {
       if (c >= p.st_ctas) return false;
       const int rounds = c < whole ? (whole - c + G - 1) / G : 0;
@@ -777,7 +779,7 @@ __device__ __forceinline__ bool persist_item(const FwdParams& p, int units, int 
 }
 
 // TMA producer (one thread).
-template <int D>
+template <int D, bool STREAM>
 __device__ __forceinline__ void persist_producer(const FwdParams& p, uint32_t base, int units, const WaitCtl& ctl) {
   using C = Cfg<D>;
   tma_prefetch_desc(&p.tm_q);
@@ -789,12 +791,12 @@ __device__ __forceinline__ void persist_producer(const FwdParams& p, uint32_t ba
   int gk = 0, gv = 0; // K and V loads issued (positions in the ring sequence)
   for (int kk = 0;; ++kk) {
     PItem U;
-    if (!persist_item<D>(p, units, kk, U)) break;
+    if (!persist_item<D, STREAM>(p, units, kk, U)) break;
     const int nkv = max(U.nkv0, U.nkv1);
     // The next item's Q rows into L2 while this one runs (its load, later, then hits L2).
     {
       PItem N2;
-      if (persist_item<D>(p, units, kk + 1, N2)) {
+      if (persist_item<D, STREAM>(p, units, kk + 1, N2)) {
         const uint16_t* qn = static_cast<const uint16_t*>(p.q) + (static_cast<size_t>(N2.bh) * p.N + N2.row0) * D;
         l2_prefetch_bulk(qn, 2u * C::Q_SUB_BYTES);
       }
@@ -843,7 +845,7 @@ __device__ __forceinline__ void persist_producer(const FwdParams& p, uint32_t ba
 
 // MMA warp (whole warp; one elected lane issues): both chains' blocks of each
 // unit in turn order, with positions counted across units.
-template <int D, bool BF16>
+template <int D, bool BF16, bool STREAM>
 __device__ __forceinline__ void persist_mma(const FwdParams& p, uint32_t base, uint32_t tmem, int units,
                                             const WaitCtl& ctl) {
   using C = Cfg<D>;
@@ -851,7 +853,7 @@ __device__ __forceinline__ void persist_mma(const FwdParams& p, uint32_t base, u
   int k = 0, g = 0, gp0 = 0, gp1 = 0;  // units, K/V tiles, P products of sub-tile 0 and 1 so far
   for (;; ++k) {
     PItem U;
-    if (!persist_item<D>(p, units, k, U)) break;
+    if (!persist_item<D, STREAM>(p, units, k, U)) break;
     const int nkv = max(U.nkv0, U.nkv1);
     if (!wait_bar_warp(bar_addr<D>(base, C::B_Q), k & 1, ctl, kWhereQ)) break;
     tc_fence_after();
@@ -883,7 +885,7 @@ __device__ __forceinline__ void persist_mma(const FwdParams& p, uint32_t base, u
 
 // Softmax warpgroup of sub-tile `sub`: the tiles of each unit, then its
 // epilogue (O / l through this sub-tile's staging buffer and TMA stores; LSE).
-template <int D, bool BF16>
+template <int D, bool BF16, bool STREAM>
 __device__ __forceinline__ void persist_softmax(const FwdParams& p, uint32_t base, uint32_t tmem, int sub, int units,
                                                 const WaitCtl& ctl) {
   using C = Cfg<D>;
@@ -899,7 +901,7 @@ __device__ __forceinline__ void persist_softmax(const FwdParams& p, uint32_t bas
   int k = 0, g = 0, gs = 0;  // units, K/V tiles, S products of this sub-tile so far
   for (;; ++k) {
     PItem U;
-    if (!persist_item<D>(p, units, k, U)) break;
+    if (!persist_item<D, STREAM>(p, units, k, U)) break;
     const int nkv = max(U.nkv0, U.nkv1), nkv_s = sub ? U.nkv1 : U.nkv0;
     const int my_row = U.row0 + C::BM * sub + t;
     const int row_end = p.causal ? min(p.N, my_row + 1) : p.N;
@@ -934,7 +936,7 @@ __device__ __forceinline__ void persist_softmax(const FwdParams& p, uint32_t bas
     if (!named_bar_and(1 + sub, 128, ok)) break;
 
     tc_fence_after();
-    if (U.slot >= 0) {
+    if (STREAM && U.slot >= 0) {
       // ---- a piece of a tail unit: its normalised fp32 O and LSE to its slot ----
       const bool empty = !(l > 0.f);
       const float inv_l = empty ? 0.f : 1.0f / (BF16 ? l_o : l);
@@ -1010,7 +1012,7 @@ __device__ __forceinline__ void persist_softmax(const FwdParams& p, uint32_t bas
   if (t == 0) tma_store_wait_all();  // every store has completed before the CTA exits
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool STREAM>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_persist_kernel(const __grid_constant__ FwdParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -1052,15 +1054,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_persist_kernel(cons
   if (warp >= 8) {
     warpgroup_reg_dealloc<C::LOW_REGS>();
     if (warp == C::WARP_TMA) {
-      if ((threadIdx.x & 31) == 0) persist_producer<D>(p, base, units, ctl);
+      if ((threadIdx.x & 31) == 0) persist_producer<D, STREAM>(p, base, units, ctl);
       __syncwarp();
     } else if (warp == C::WARP_MMA0) {
-      persist_mma<D, BF16>(p, base, tmem, units, ctl);
+      persist_mma<D, BF16, STREAM>(p, base, tmem, units, ctl);
       __syncwarp();
     }
   } else {
     warpgroup_reg_alloc<C::HIGH_REGS>();
-    persist_softmax<D, BF16>(p, base, tmem, warp / 4, units, ctl);
+    persist_softmax<D, BF16, STREAM>(p, base, tmem, warp / 4, units, ctl);
   }
 
   tc_fence_before();
@@ -1073,12 +1075,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_persist_kernel(cons
 
 // Whether a launch takes the persistent form: d = 128, one launch over all
 // units with the whole key range (no split-KV, no key lengths), N a multiple
-// of 256 (of 512 with the causal mask, whose units go in pairs), none of the
-// testing build's traces. On GB300 it measured +1.4 % on B=8 H=32 N=4096,
-// +5 % causal and +5 % on B=8 H=12 N=2048 (bit-identical results). The
-// strict-order build keeps one CTA per unit.
+// of 256 (of 512 with the causal mask, whose units go in pairs) and at most
+// kPersistMaxN, none of the testing build's traces. On GB300 it measured
+// +2 to +5 % on B=8 H=32 N=4096 and +4 to +5 % on B=8 H=12 N=2048 against one
+// CTA per unit (bit-identical results), but -6 % on B=1 H=8 N=16384: its
+// tile rate is a few per cent lower (one MMA warp, runtime ring positions,
+// the larger shared-memory footprint), which longer units do not win back
+// from the CTA starts and ends it saves. The strict-order build keeps one
+// CTA per unit.
 // A streamed tail (st_ctas > 0) takes the same conditions, unmasked only,
 // with its slots in o_part / lse_part and at most one range per CTA.
+constexpr int kPersistMaxN = 4096;
 template <int D>
 bool persist_eligible(const FwdParams& p) {
 #ifdef FA_STRICT_MMA_ORDER
@@ -1088,14 +1095,16 @@ bool persist_eligible(const FwdParams& p) {
   if (D != 128) return false;
   if (p.st_ctas > 0) {
     const long long units = static_cast<long long>(p.B) * p.H * (p.N / (2 * Cfg<D>::BM));
-    if (p.causal || p.o_part == nullptr || p.lse_part == nullptr || p.st_ctas > p.num_sms || p.st_unit0 < 0 ||
+    if (p.causal || p.o_part == nullptr || p.lse_part == nullptr || p.st_ctas > p.num_sms || p.st_ctas > 128 ||
+        p.st_unit0 < 0 ||
         p.st_unit0 >= units || p.st_unit0 % p.num_sms != 0 ||
         static_cast<long long>(p.st_tiles) != (units - p.st_unit0) * (p.N / Cfg<D>::BN) ||
         static_cast<long long>(p.st_tiles) * p.st_ctas >= (1ll << 31))
       return false;
   }
   return p.num_splits == 1 && p.qunit0 == 0 && p.qunit_count == 0 && !p.partial && p.klen == nullptr &&
-         p.Nk == p.N && p.N % (p.causal ? 4 * Cfg<D>::BM : 2 * Cfg<D>::BM) == 0 && p.stats_trace == nullptr &&
+         p.Nk == p.N && p.N % (p.causal ? 4 * Cfg<D>::BM : 2 * Cfg<D>::BM) == 0 && p.N <= kPersistMaxN &&
+         p.stats_trace == nullptr &&
          p.timeline == nullptr &&
          p.inject == 0;
 #endif
@@ -1105,59 +1114,90 @@ bool persist_eligible(const FwdParams& p) {
 // pieces, LSE = m + log sum_s exp(LSE_s - m) and O = sum_s exp(LSE_s - LSE)
 // O_s over its pieces s (the block merge of the Triton page, section 2.3, in
 // LSE form; m the largest LSE_s). Units that one CTA computed whole are
-// skipped: their O and LSE are already written. One warp per row.
+// skipped: their O and LSE are already written. One CTA per tail unit: the
+// unit's part slots are listed once in shared memory, then each warp takes
+// rows; a row's LSE_s are read one per lane and reduced across the warp, its
+// O_s rows (lane = 4 columns) four at a time. Launched as a programmatic
+// dependent of the persistent kernel: its launch overlaps that kernel's end
+// and it waits for the kernel's writes before reading them.
+constexpr int kMergeMaxPieces = 128;  // a unit has at most one piece per CTA sharing the tail (<= 126)
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_merge_stream_kernel(const __grid_constant__ FwdParams p) {
   constexpr int E = D / 32;
+  static_assert(E == 4, "one float4 of O per lane and piece");
   constexpr int ROWS = 2 * Cfg<D>::BM;  // rows of a unit
+  __shared__ int slots[kMergeMaxPieces];
+  __shared__ int npieces;
   const int n = p.N / Cfg<D>::BN;
-  const int i = blockIdx.x / (ROWS / 8);  // tail unit; 8 warps per block, ROWS / 8 blocks per unit
-  const int r = (blockIdx.x % (ROWS / 8)) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  int c_lo, c_hi;
-  st_unit_ctas(p.st_tiles, p.st_ctas, n, i, c_lo, c_hi);
-  if (c_lo == c_hi) return;
-  const int x = i * n;
-  float m = -INFINITY;
-  for (int cc = c_lo; cc <= c_hi; ++cc) {
-    const int a = st_begin(p.st_tiles, p.st_ctas, cc);
-    if (a == st_begin(p.st_tiles, p.st_ctas, cc + 1)) continue;  // an empty range
-    const int slot = 2 * cc + (a >= x ? 0 : 1);
-    m = fmaxf(m, p.lse_part[static_cast<size_t>(slot) * ROWS + r]);
-  }
-  float acc[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  float l = 0.f;
-  if (m > -INFINITY) {
-    for (int cc = c_lo; cc <= c_hi; ++cc) {
-      const int a = st_begin(p.st_tiles, p.st_ctas, cc);
-      if (a == st_begin(p.st_tiles, p.st_ctas, cc + 1)) continue;
-      const size_t prow = static_cast<size_t>(2 * cc + (a >= x ? 0 : 1)) * ROWS + r;
-      const float w = ex2_approx((p.lse_part[prow] - m) * kLog2e);
-      l += w;
-      const float4* src = reinterpret_cast<const float4*>(p.o_part + prow * D + lane * E);
-#pragma unroll
-      for (int e = 0; e < E / 4; ++e) {
-        const float4 v = src[e];
-        acc[4 * e] = fmaf(w, v.x, acc[4 * e]);
-        acc[4 * e + 1] = fmaf(w, v.y, acc[4 * e + 1]);
-        acc[4 * e + 2] = fmaf(w, v.z, acc[4 * e + 2]);
-        acc[4 * e + 3] = fmaf(w, v.w, acc[4 * e + 3]);
+  const int i = blockIdx.x;  // tail unit
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    int c_lo, c_hi, np = 0;
+    st_unit_ctas(p.st_tiles, p.st_ctas, n, i, c_lo, c_hi);
+    if (c_lo != c_hi) {
+      const int x = i * n;
+      for (int cc = c_lo; cc <= c_hi && np < kMergeMaxPieces; ++cc) {
+        const int a = st_begin(p.st_tiles, p.st_ctas, cc);
+        if (a == st_begin(p.st_tiles, p.st_ctas, cc + 1)) continue;  // an empty range
+        slots[np++] = 2 * cc + (a >= x ? 0 : 1);
       }
     }
+    npieces = np;
   }
-  const float inv = l > 0.f ? 1.0f / l : 0.f;
-  uint32_t pk[E / 2];
-#pragma unroll
-  for (int e = 0; e < E / 2; ++e) pk[e] = pack2<BF16>(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+  __syncthreads();
+  const int np = npieces;
+  if (np == 0) return;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the persistent kernel's parts are written
   const int nqb = p.N / ROWS;
   const int u = p.st_unit0 + i;
-  const long long row = static_cast<long long>(u / nqb) * p.N + (u % nqb) * ROWS + r;
-  uint16_t* out = static_cast<uint16_t*>(p.o) + row * D + lane * E;
-  static_assert(E == 4, "one 8-byte store per lane");
-  *reinterpret_cast<uint2*>(out) = make_uint2(pk[0], pk[1]);
-  if (lane == 0) p.lse[row] = m > -INFINITY ? m + lg2_approx(l) * kLn2 : -INFINITY;
+  const long long row_base = static_cast<long long>(u / nqb) * p.N + (u % nqb) * ROWS;
+  for (int r = warp; r < ROWS; r += 8) {
+    // the largest LSE_s, then each piece's weight w_s = exp(LSE_s - m) and their sum
+    float m = -INFINITY;
+    for (int s0 = lane; s0 < np; s0 += 32) m = fmaxf(m, p.lse_part[static_cast<size_t>(slots[s0]) * ROWS + r]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float acc[E] = {0.f, 0.f, 0.f, 0.f};
+    float l = 0.f;
+    if (m > -INFINITY) {
+      for (int s0 = 0; s0 < np; s0 += 32) {
+        const int cnt = min(32, np - s0);
+        const float w_mine =
+            lane < cnt ? ex2_approx((p.lse_part[static_cast<size_t>(slots[s0 + lane]) * ROWS + r] - m) * kLog2e) : 0.f;
+        l += w_mine;
+        int s = 0;
+        for (; s + 4 <= cnt; s += 4) {
+          float4 v[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            v[q] = reinterpret_cast<const float4*>(p.o_part + (static_cast<size_t>(slots[s0 + s + q]) * ROWS + r) * D)[lane];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float w = __shfl_sync(0xffffffffu, w_mine, s + q);
+            acc[0] = fmaf(w, v[q].x, acc[0]);
+            acc[1] = fmaf(w, v[q].y, acc[1]);
+            acc[2] = fmaf(w, v[q].z, acc[2]);
+            acc[3] = fmaf(w, v[q].w, acc[3]);
+          }
+        }
+        for (; s < cnt; ++s) {
+          const float4 v = reinterpret_cast<const float4*>(p.o_part + (static_cast<size_t>(slots[s0 + s]) * ROWS + r) * D)[lane];
+          const float w = __shfl_sync(0xffffffffu, w_mine, s);
+          acc[0] = fmaf(w, v.x, acc[0]);
+          acc[1] = fmaf(w, v.y, acc[1]);
+          acc[2] = fmaf(w, v.z, acc[2]);
+          acc[3] = fmaf(w, v.w, acc[3]);
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+    }
+    const float inv = l > 0.f ? 1.0f / l : 0.f;
+    const long long row = row_base + r;
+    uint16_t* out = static_cast<uint16_t*>(p.o) + row * D + lane * E;
+    *reinterpret_cast<uint2*>(out) = make_uint2(pack2<BF16>(acc[0] * inv, acc[1] * inv), pack2<BF16>(acc[2] * inv, acc[3] * inv));
+    if (lane == 0) p.lse[row] = m > -INFINITY ? m + lg2_approx(l) * kLn2 : -INFINITY;
+  }
 }
 
 template <int D, bool BF16>
@@ -1184,16 +1224,20 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream) {
   if (p.st_ctas > 0 && !persist_eligible<D>(p)) return cudaErrorInvalidValue;
   if constexpr (D == 128) {
     if (persist_eligible<D>(p)) {
-      auto pk = fa_fwd_persist_kernel<D, BF16>;
-      static std::atomic<uint64_t> pattr{0};
-      if (!(pattr.load() & bit)) {
+      // Two instantiations: without the streamed tail the kernel carries none
+      // of its code (its item walk and part epilogue cost 2-5 % of the tile
+      // rate when present, measured on GB300).
+      const bool stream_tail = p.st_ctas > 0;
+      auto pk = stream_tail ? fa_fwd_persist_kernel<D, BF16, true> : fa_fwd_persist_kernel<D, BF16, false>;
+      static std::atomic<uint64_t> pattr[2] = {0, 0};
+      if (!(pattr[stream_tail].load() & bit)) {
         cudaFuncAttributes pa;
         e = cudaFuncGetAttributes(&pa, pk);
         if (e != cudaSuccess) return e;
         if (pa.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
         e = cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, PCfg<D>::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        pattr.fetch_or(bit);
+        pattr[stream_tail].fetch_or(bit);
       }
       if (all_qunits <= 0 || all_qunits > 0x7fffffffLL) return cudaErrorInvalidValue;
       const long long work = p.causal ? (all_qunits + 1) / 2 : all_qunits;  // causal: pairs of units
@@ -1202,10 +1246,21 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream) {
       pk<<<dim3(static_cast<unsigned>(ctas)), dim3(C::THREADS), PCfg<D>::SMEM_BYTES, stream>>>(p);
       e = cudaGetLastError();
       if (e != cudaSuccess || p.st_ctas == 0) return e;
-      const long long blocks = (all_qunits - p.st_unit0) * (2 * C::BM / 8);
+      const long long blocks = all_qunits - p.st_unit0;  // one per tail unit
       if (blocks <= 0 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-      fa_merge_stream_kernel<D, BF16><<<dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream>>>(p);
-      return cudaGetLastError();
+      // A programmatic dependent launch: the merge grid is set up while the
+      // persistent kernel finishes and waits (griddepcontrol.wait) for its writes.
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+      cfg.blockDim = dim3(256);
+      cfg.dynamicSmemBytes = 0;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      return cudaLaunchKernelEx(&cfg, fa_merge_stream_kernel<D, BF16>, p);
     }
   }
   const long long qunits = p.qunit_count > 0 ? p.qunit_count : all_qunits;

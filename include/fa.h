@@ -119,8 +119,8 @@ int fa_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE,
  *             the full waves run unsplit and only the last wave's units are
  *             split (as many ways as fit in one wave) and merged; that is
  *             three launches (full waves, split tail, merge of its rows).
- *             For unmasked d = 128 inputs with N a multiple of 256 the
- *             automatic count may instead stream the tail: the persistent
+ *             For unmasked d = 128 inputs with N a multiple of 256 and at
+ *             most 4096 the automatic count may instead stream the tail: the persistent
  *             kernel runs the full rounds of Q blocks whole and cuts the K/V
  *             tiles of the units left over into one contiguous range per
  *             SM; units a range boundary cuts are computed in pieces and
@@ -215,8 +215,8 @@ int fa_fwd_splitkv_plan(int B, int H, int N, int d, int num_splits, int num_sms,
  * model expects it to shorten the pass: the units then end in a partial last
  * round (B*H*N/256 not a multiple of num_sms) long enough to pay for the merge.
  * Outputs (all written on success): ctas = 0 when the plan does not stream
- * the tail (other d, N not a multiple of 256, or it does not pay; unit0 =
- * tiles = 0 then); else 1 <= ctas <= num_sms, unit0 a multiple of num_sms.
+ * the tail (other d, N not a multiple of 256 or above 4096, or it does not
+ * pay; unit0 = tiles = 0 then); else 1 <= ctas <= num_sms, unit0 a multiple of num_sms.
  * Errors: FA_ERR_NULL (an output pointer is NULL), FA_ERR_SHAPE (B, H, N or
  * num_sms < 1, B*H >= 2^31), FA_ERR_HEADDIM (d not 64, 128 or 256).
  */

@@ -1123,6 +1123,114 @@ def test_forward_persistent_barrier_protocol(units):
         PersistModel(units, rng).run()
 
 
+class PersistTwoWarpModel(PersistModel):
+    """The persistent form with one MMA warp per sub-tile whose blocks
+    alternate by turns, as in the one-unit kernel: sub-tile 0's block j >= 1
+    waits for sub-tile 1's block j-1, its first block of a unit for
+    sub-tile 1's last block of the previous unit; sub-tile 1's block j waits
+    for sub-tile 0's block j while sub-tile 0 has one; a warp passes the turn
+    only for a block the other waits for. Turn phases are counted across
+    units, so a turn barrier holding two arrivals would show up as an
+    aliased parity wait."""
+
+    def __init__(self, units, rng):
+        PersistModel.__init__(self, units, rng)
+        self.bars.update({"T0": Bar(1), "T1": Bar(1), "DR0": Bar(1), "DR1": Bar(1)})
+
+    def roles(self):
+        return ([self.producer(), self.mma_warp(0), self.mma_warp(1)]
+                + [self.softmax(sub, w) for sub in (0, 1) for w in range(4)])
+
+    def mma_warp(self, sub):
+        g, gp, nt = 0, 0, 0
+        for k, (n0, n1) in enumerate(self.units):
+            nkv = max(n0, n1)
+            n_me, n_other = (n1, n0) if sub else (n0, n1)
+            yield ("wait", "Q", k)
+            for j in range(n_me + 1):
+                if (j > 0 or k > 0) if sub == 0 else (j <= n_other):
+                    yield ("wait", f"T{sub}", nt)
+                    nt += 1
+                if j == 1 and k > 0:
+                    yield ("wait", f"OF{sub}", k - 1)
+                if j > 0:
+                    gg = g + j - 1
+                    yield ("wait", f"VF{gg % self.ST}", gg // self.ST)
+                    yield ("wait", f"PF{sub}", gp + j - 1)
+                    self.issue(sub, "PV", (sub, k, j - 1, gg))
+                    if j == n_me:
+                        self.commit(sub, f"OD{sub}")
+                    yield ("step",)
+                if j < n_me:
+                    gg = g + j
+                    yield ("wait", f"KF{gg % self.ST}", gg // self.ST)
+                    self.issue(sub, "S", (sub, k, j, gg))
+                    self.commit(sub, f"SF{sub}")
+                    yield ("step",)
+                if sub == 0 or j < n_other or j == n_me:
+                    self.bars[f"T{sub ^ 1}"].arrive()
+                    yield ("step",)
+            g += nkv
+            gp += n_me
+        self.commit(sub, f"DR{sub}")
+        yield ("wait", f"DR{sub}", 0)
+
+
+@pytest.mark.parametrize("units", [
+    [(3, 3)], [(2, 2), (2, 2), (2, 2)], [(1, 2), (4, 5), (2, 3)], [(5, 6), (1, 2)], [(1, 1), (1, 1), (1, 1), (1, 1)],
+    [(3, 4), (3, 4), (1, 2), (6, 7)], [(4, 4), (4, 4), (1, 1), (2, 2)], [(3, 3), (1, 1)], [(1, 2), (1, 2), (1, 2)],
+], ids=lambda u: "-".join(f"{a}.{b}" for a, b in u))
+def test_forward_persistent_two_mma_warps_barrier_protocol(units):
+    rng = random.Random(hash(tuple(units)) & 0xFFFFFFFF)
+    for _ in range(400):
+        PersistTwoWarpModel(units, rng).run()
+
+
+def test_model_catches_a_turn_passed_for_every_block():
+    """Planted mistake: sub-tile 1 passes the turn after every block, also
+    the one sub-tile 0 does not wait for (a unit whose sub-tile 1 has one
+    tile more); the extra arrival completes a turn phase early and a later
+    parity wait aliases."""
+    class EveryPass(PersistTwoWarpModel):
+        def mma_warp(self, sub):
+            if sub == 0:
+                yield from PersistTwoWarpModel.mma_warp(self, 0)
+                return
+            units = self.units
+            g, gp, nt = 0, 0, 0
+            for k, (n0, n1) in enumerate(units):
+                yield ("wait", "Q", k)
+                for j in range(n1 + 1):
+                    if j <= n0:
+                        yield ("wait", "T1", nt)
+                        nt += 1
+                    if j == 1 and k > 0:
+                        yield ("wait", "OF1", k - 1)
+                    if j > 0:
+                        gg = g + j - 1
+                        yield ("wait", f"VF{gg % self.ST}", gg // self.ST)
+                        yield ("wait", "PF1", gp + j - 1)
+                        self.issue(1, "PV", (1, k, j - 1, gg))
+                        if j == n1:
+                            self.commit(1, "OD1")
+                        yield ("step",)
+                    if j < n1:
+                        gg = g + j
+                        yield ("wait", f"KF{gg % self.ST}", gg // self.ST)
+                        self.issue(1, "S", (1, k, j, gg))
+                        self.commit(1, "SF1")
+                        yield ("step",)
+                    self.bars["T0"].arrive()
+                    yield ("step",)
+                g += max(n0, n1)
+                gp += n1
+            self.commit(1, "DR1")
+            yield ("wait", "DR1", 0)
+    with pytest.raises(AssertionError):
+        for seed in range(300):
+            EveryPass([(1, 2), (4, 5), (2, 3), (3, 4)], random.Random(seed)).run()
+
+
 def test_model_catches_an_early_release_of_an_unused_tile():
     """Planted mistake: the sub-tile that does not use a unit's last tile
     releases its stage at once instead of after the tile landed; its arrivals

@@ -110,9 +110,8 @@ def unit_pieces(T, G, n):
 
 @pytest.mark.parametrize("B,H,N,num_sms", [
     (8, 12, 2048, 152),    # 768 units: 5 full rounds, 8 units (128 tiles) streamed
-    (8, 12, 2048, 148),
-    (1, 8, 16384, 152),    # 512 units: 3 full rounds, 56 units of 128 tiles streamed
     (1, 20, 2048, 152),    # 160 units: 1 full round, 8 left
+    (3, 7, 2048, 152),     # 168 units: 1 full round, 16 left
     (1, 2, 4096, 152),     # 32 units: no full round, all streamed
 ])
 def test_stream_plan_on_the_host(B, H, N, num_sms):
@@ -139,6 +138,8 @@ def test_stream_plan_on_the_host(B, H, N, num_sms):
     (8, 12, 2048, 64, 152),    # d = 64 has no persistent form
     (4, 16, 4096, 256, 152),   # nor d = 256
     (2, 3, 4096, 128, 152),    # 96 units of 32 tiles: the merge of ~220 pieces costs more than it saves
+    (8, 12, 2048, 128, 148),   # 768 units on 148 SMs: 5.19 rounds, the 28 left over fill enough of the last
+    (1, 8, 16384, 128, 152),   # N > 4096: one CTA per unit (the key-range tail plan)
 ])
 def test_stream_plan_declines(B, H, N, d, num_sms):
     rc, sp = fa.fa_fwd_stream_plan(B, H, N, d, num_sms)
