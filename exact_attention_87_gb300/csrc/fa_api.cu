@@ -211,13 +211,14 @@ long long bwd_tiles(int N) { return (static_cast<long long>(N) + fa::kF16BlockKV
 // run unsplit and only the last wave's units are split (as many ways as fit
 // in one wave), then merged:
 //   W * (tiles + 1) * t_tile + (tiles/s + 1) * t_tile + merge of the tail rows
-//   + 20 us
-// The last term is the launch boundary: the split tail starts only once
-// every CTA of the full waves has finished, whereas unsplit tail units start
-// as SMs free up. Measured on GB300: with the tail split, B=1 H=8 N=16384
-// d=128 runs 8 % faster than unsplit (uniform 2-way splits 1 % slower), B=8
-// H=12 N=2048 d=128 within 1 %, and B=4 H=16 N=4096 d=256 (13.5 waves) 1 %
-// slower; the term makes the last two run unsplit.
+//   + b
+// The last term is the launch boundary. The split tail is a programmatic
+// dependent launch (its CTAs start as the full waves' CTAs finish); b = 5 us
+// for d <= 128, and 20 us at d = 256, the boundary measured before the tail
+// was launched that way (no measurement of d = 256 with it yet). Measured on
+// GB300 with b = 20 us: with the tail split, B=1 H=8 N=16384 d=128 runs 8 %
+// faster than unsplit (uniform 2-way splits 1 % slower) and B=4 H=16 N=4096
+// d=256 (13.5 waves) 1 % slower (unsplit there).
 struct SplitPlan {
   int splits;            // key ranges per split unit (1: unsplit)
   long long tail_qunit0; // >= 0: units before it unsplit, the rest split; < 0: every unit split alike
@@ -248,7 +249,7 @@ SplitPlan split_plan(int B, int H, int N, int d, int num_splits, int num_sms) {
       const double tail_rows = static_cast<double>(tail) * fa::fwd_q_block(d);
       const double us = static_cast<double>(full) * (static_cast<double>(tiles) + 1.0) * t_tile_us +
                         (static_cast<double>(per) + 1.0) * t_tile_us + 2.0 * s * tail_rows * d * 4.0 / 5e12 * 1e6 +
-                        5.0 + 20.0;
+                        5.0 + (d == 256 ? 20.0 : 5.0);
       if (us < best_us) best = {static_cast<int>(s), full * num_sms};
     }
   }
@@ -535,6 +536,9 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
         pt.qunit0 = static_cast<int>(plan.tail_qunit0);
         pt.qunit_count = static_cast<int>(qunits - plan.tail_qunit0);
         pt.merge_row0 = row0;
+        // The tail's CTAs start as the full waves' CTAs finish instead of at
+        // the end of the first launch (they read none of its results).
+        pt.launch_pdl = 1;
         e = launch_fwd16(pt, bf16, s);
         if (e == cudaSuccess) e = fa::launch_merge(pt, bf16, s);
       }

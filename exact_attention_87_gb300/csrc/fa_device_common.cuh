@@ -85,6 +85,25 @@ __device__ __forceinline__ float rescale_threshold(const FwdParams& p) {
 #endif
 }
 
+// Host side: launch `kern` as a programmatic dependent of the previous kernel
+// in `stream` (it may start while that kernel's last CTAs still run; it
+// must itself wait, griddepcontrol.wait, before it reads that kernel's
+// results or, reading none, before it completes).
+template <class Kern, class... Args>
+inline cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, const Args&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Testing build only: clock64 stamp of pipeline event `ev` for tile `j`.
 #ifdef FA_TESTING
 #define FA_TRACE(p, ev, j)                                                                                 \

@@ -459,6 +459,9 @@ __global__ void __launch_bounds__(C256::THREADS, 1) fa_fwd_d256_kernel(const __g
   tc_fence_after();
   const uint32_t tmem = misc[0];
   const WaitCtl ctl{p, base + C::OFF_MISC + 4};
+  // A split tail launched behind this kernel (a programmatic dependent that
+  // reads none of its results) may start its CTAs as this kernel's finish.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
 
   if (warp == C::WARP_TMA) {
     if ((threadIdx.x & 31) == 0) producer256(p, base, bh, row0, t0, nkv, ctl);
@@ -476,6 +479,9 @@ __global__ void __launch_bounds__(C256::THREADS, 1) fa_fwd_d256_kernel(const __g
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+  // Launched as a programmatic dependent (the split tail after the full
+  // waves): finish only after the kernel before it (no-op otherwise).
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <bool BF16>
@@ -497,6 +503,7 @@ cudaError_t launch256(const FwdParams& p, cudaStream_t stream) {
   if (p.qunit0 < 0 || p.qunit0 + qunits > all_qunits) return cudaErrorInvalidValue;
   const long long units = qunits * p.num_splits;
   if (units <= 0 || units > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (p.launch_pdl) return launch_pdl(kern, dim3(static_cast<unsigned>(units)), dim3(C::THREADS), C::SMEM_BYTES, stream, p);
   kern<<<dim3(static_cast<unsigned>(units)), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }

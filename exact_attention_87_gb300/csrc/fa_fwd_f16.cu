@@ -648,6 +648,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
   tc_fence_after();
   const uint32_t tmem = misc[0];
   const WaitCtl ctl{p, base + C::OFF_MISC + 4};  // misc[1] is the abort flag
+  // A split tail launched behind this kernel (a programmatic dependent that
+  // reads none of its results) may start its CTAs as this kernel's finish.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
   if (threadIdx.x == 0) FA_TRACE(p, kEvCta, 0);
 
   if (warp >= 8) {
@@ -688,6 +691,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+  // Launched as a programmatic dependent (the split tail after the full
+  // rounds): finish only after the kernel before it (no-op otherwise).
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ==========================================================================
@@ -1020,7 +1026,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_persist_kernel(cons
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem_raw + (base - raw) + C::OFF_MISC);
   const int warp = threadIdx.x >> 5;
-  const int units = p.B * p.H * (p.N / (2 * C::BM));
+  // Units 0 .. units-1: all of them, or the full rounds before a split tail.
+  const int units = p.qunit_count > 0 ? p.qunit_count : p.B * p.H * (p.N / (2 * C::BM));
 
   if (threadIdx.x == 0) {
     mbar_init(bar_addr<D>(base, C::B_Q), 1);
@@ -1050,6 +1057,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_persist_kernel(cons
   tc_fence_after();
   const uint32_t tmem = misc[0];
   const WaitCtl ctl{p, base + C::OFF_MISC + 4};
+  // A split tail launched behind this kernel (a programmatic dependent that
+  // reads none of its results) may start its CTAs as this kernel's finish.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
 
   if (warp >= 8) {
     warpgroup_reg_dealloc<C::LOW_REGS>();
@@ -1102,7 +1112,10 @@ bool persist_eligible(const FwdParams& p) {
         static_cast<long long>(p.st_tiles) * p.st_ctas >= (1ll << 31))
       return false;
   }
-  return p.num_splits == 1 && p.qunit0 == 0 && p.qunit_count == 0 && !p.partial && p.klen == nullptr &&
+  // A launch over the first qunit_count units only (the full rounds before a
+  // split tail) takes it too, unmasked: its units are then numbered in order.
+  if (p.qunit_count > 0 && (p.causal || p.st_ctas > 0)) return false;
+  return p.num_splits == 1 && p.qunit0 == 0 && !p.partial && p.klen == nullptr &&
          p.Nk == p.N && p.N % (p.causal ? 4 * Cfg<D>::BM : 2 * Cfg<D>::BM) == 0 && p.N <= kPersistMaxN &&
          p.stats_trace == nullptr &&
          p.timeline == nullptr &&
@@ -1114,90 +1127,98 @@ bool persist_eligible(const FwdParams& p) {
 // pieces, LSE = m + log sum_s exp(LSE_s - m) and O = sum_s exp(LSE_s - LSE)
 // O_s over its pieces s (the block merge of the Triton page, section 2.3, in
 // LSE form; m the largest LSE_s). Units that one CTA computed whole are
-// skipped: their O and LSE are already written. One CTA per tail unit: the
-// unit's part slots are listed once in shared memory, then each warp takes
-// rows; a row's LSE_s are read one per lane and reduced across the warp, its
-// O_s rows (lane = 4 columns) four at a time. Launched as a programmatic
-// dependent of the persistent kernel: its launch overlaps that kernel's end
-// and it waits for the kernel's writes before reading them.
+// skipped: their O and LSE are already written. A CTA takes 8 rows of a tail
+// unit (one per warp): its first warp lists the unit's part slots in shared
+// memory (one candidate range per lane), then each warp reads its row's part
+// LSEs one per lane, reduces them across the warp and adds the O rows four at
+// a time. Launched as a programmatic dependent of the persistent kernel: it
+// lists the slots while that kernel finishes and waits for its writes before
+// reading them.
 constexpr int kMergeMaxPieces = 128;  // a unit has at most one piece per CTA sharing the tail (<= 126)
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_merge_stream_kernel(const __grid_constant__ FwdParams p) {
   constexpr int E = D / 32;
   static_assert(E == 4, "one float4 of O per lane and piece");
   constexpr int ROWS = 2 * Cfg<D>::BM;  // rows of a unit
+  constexpr int BLOCKS_PER_UNIT = ROWS / 8;
   __shared__ int slots[kMergeMaxPieces];
   __shared__ int npieces;
   const int n = p.N / Cfg<D>::BN;
-  const int i = blockIdx.x;  // tail unit
+  const int i = blockIdx.x / BLOCKS_PER_UNIT;  // tail unit
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    int c_lo, c_hi, np = 0;
-    st_unit_ctas(p.st_tiles, p.st_ctas, n, i, c_lo, c_hi);
-    if (c_lo != c_hi) {
-      const int x = i * n;
-      for (int cc = c_lo; cc <= c_hi && np < kMergeMaxPieces; ++cc) {
+  const int r = (blockIdx.x % BLOCKS_PER_UNIT) * 8 + warp;  // this warp's row of the unit
+  int c_lo, c_hi;
+  st_unit_ctas(p.st_tiles, p.st_ctas, n, i, c_lo, c_hi);
+  if (c_lo == c_hi) return;  // whole in one range: written directly
+  if (warp == 0) {
+    const int x = i * n;
+    int np = 0;
+    for (int c0 = c_lo; c0 <= c_hi; c0 += 32) {
+      const int cc = c0 + lane;
+      bool has = false;
+      int slot = 0;
+      if (cc <= c_hi) {
         const int a = st_begin(p.st_tiles, p.st_ctas, cc);
-        if (a == st_begin(p.st_tiles, p.st_ctas, cc + 1)) continue;  // an empty range
-        slots[np++] = 2 * cc + (a >= x ? 0 : 1);
+        has = a != st_begin(p.st_tiles, p.st_ctas, cc + 1);  // an empty range holds no piece
+        slot = 2 * cc + (a >= x ? 0 : 1);
       }
+      const unsigned m = __ballot_sync(0xffffffffu, has);
+      const int at = np + __popc(m & ((1u << lane) - 1u));
+      if (has && at < kMergeMaxPieces) slots[at] = slot;
+      np += __popc(m);
     }
-    npieces = np;
+    if (lane == 0) npieces = min(np, kMergeMaxPieces);
   }
   __syncthreads();
   const int np = npieces;
-  if (np == 0) return;
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the persistent kernel's parts are written
-  const int nqb = p.N / ROWS;
-  const int u = p.st_unit0 + i;
-  const long long row_base = static_cast<long long>(u / nqb) * p.N + (u % nqb) * ROWS;
-  for (int r = warp; r < ROWS; r += 8) {
-    // the largest LSE_s, then each piece's weight w_s = exp(LSE_s - m) and their sum
-    float m = -INFINITY;
-    for (int s0 = lane; s0 < np; s0 += 32) m = fmaxf(m, p.lse_part[static_cast<size_t>(slots[s0]) * ROWS + r]);
+  // the largest LSE_s, then each piece's weight w_s = exp(LSE_s - m) and their sum
+  float m = -INFINITY;
+  for (int s0 = lane; s0 < np; s0 += 32) m = fmaxf(m, p.lse_part[static_cast<size_t>(slots[s0]) * ROWS + r]);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    float acc[E] = {0.f, 0.f, 0.f, 0.f};
-    float l = 0.f;
-    if (m > -INFINITY) {
-      for (int s0 = 0; s0 < np; s0 += 32) {
-        const int cnt = min(32, np - s0);
-        const float w_mine =
-            lane < cnt ? ex2_approx((p.lse_part[static_cast<size_t>(slots[s0 + lane]) * ROWS + r] - m) * kLog2e) : 0.f;
-        l += w_mine;
-        int s = 0;
-        for (; s + 4 <= cnt; s += 4) {
-          float4 v[4];
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  float acc[E] = {0.f, 0.f, 0.f, 0.f};
+  float l = 0.f;
+  if (m > -INFINITY) {
+    for (int s0 = 0; s0 < np; s0 += 32) {
+      const int cnt = min(32, np - s0);
+      const float w_mine =
+          lane < cnt ? ex2_approx((p.lse_part[static_cast<size_t>(slots[s0 + lane]) * ROWS + r] - m) * kLog2e) : 0.f;
+      l += w_mine;
+      int s = 0;
+      for (; s + 4 <= cnt; s += 4) {
+        float4 v[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            v[q] = reinterpret_cast<const float4*>(p.o_part + (static_cast<size_t>(slots[s0 + s + q]) * ROWS + r) * D)[lane];
+        for (int q = 0; q < 4; ++q)
+          v[q] = reinterpret_cast<const float4*>(p.o_part + (static_cast<size_t>(slots[s0 + s + q]) * ROWS + r) * D)[lane];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float w = __shfl_sync(0xffffffffu, w_mine, s + q);
-            acc[0] = fmaf(w, v[q].x, acc[0]);
-            acc[1] = fmaf(w, v[q].y, acc[1]);
-            acc[2] = fmaf(w, v[q].z, acc[2]);
-            acc[3] = fmaf(w, v[q].w, acc[3]);
-          }
-        }
-        for (; s < cnt; ++s) {
-          const float4 v = reinterpret_cast<const float4*>(p.o_part + (static_cast<size_t>(slots[s0 + s]) * ROWS + r) * D)[lane];
-          const float w = __shfl_sync(0xffffffffu, w_mine, s);
-          acc[0] = fmaf(w, v.x, acc[0]);
-          acc[1] = fmaf(w, v.y, acc[1]);
-          acc[2] = fmaf(w, v.z, acc[2]);
-          acc[3] = fmaf(w, v.w, acc[3]);
+        for (int q = 0; q < 4; ++q) {
+          const float w = __shfl_sync(0xffffffffu, w_mine, s + q);
+          acc[0] = fmaf(w, v[q].x, acc[0]);
+          acc[1] = fmaf(w, v[q].y, acc[1]);
+          acc[2] = fmaf(w, v[q].z, acc[2]);
+          acc[3] = fmaf(w, v[q].w, acc[3]);
         }
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+      for (; s < cnt; ++s) {
+        const float4 v = reinterpret_cast<const float4*>(p.o_part + (static_cast<size_t>(slots[s0 + s]) * ROWS + r) * D)[lane];
+        const float w = __shfl_sync(0xffffffffu, w_mine, s);
+        acc[0] = fmaf(w, v.x, acc[0]);
+        acc[1] = fmaf(w, v.y, acc[1]);
+        acc[2] = fmaf(w, v.z, acc[2]);
+        acc[3] = fmaf(w, v.w, acc[3]);
+      }
     }
-    const float inv = l > 0.f ? 1.0f / l : 0.f;
-    const long long row = row_base + r;
-    uint16_t* out = static_cast<uint16_t*>(p.o) + row * D + lane * E;
-    *reinterpret_cast<uint2*>(out) = make_uint2(pack2<BF16>(acc[0] * inv, acc[1] * inv), pack2<BF16>(acc[2] * inv, acc[3] * inv));
-    if (lane == 0) p.lse[row] = m > -INFINITY ? m + lg2_approx(l) * kLn2 : -INFINITY;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
   }
+  const float inv = l > 0.f ? 1.0f / l : 0.f;
+  const int nqb = p.N / ROWS;
+  const int u = p.st_unit0 + i;
+  const long long row = static_cast<long long>(u / nqb) * p.N + (u % nqb) * ROWS + r;
+  uint16_t* out = static_cast<uint16_t*>(p.o) + row * D + lane * E;
+  *reinterpret_cast<uint2*>(out) = make_uint2(pack2<BF16>(acc[0] * inv, acc[1] * inv), pack2<BF16>(acc[2] * inv, acc[3] * inv));
+  if (lane == 0) p.lse[row] = m > -INFINITY ? m + lg2_approx(l) * kLn2 : -INFINITY;
 }
 
 template <int D, bool BF16>
@@ -1239,34 +1260,26 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         pattr[stream_tail].fetch_or(bit);
       }
-      if (all_qunits <= 0 || all_qunits > 0x7fffffffLL) return cudaErrorInvalidValue;
-      const long long work = p.causal ? (all_qunits + 1) / 2 : all_qunits;  // causal: pairs of units
+      if (all_qunits <= 0 || all_qunits > 0x7fffffffLL || p.qunit_count > all_qunits) return cudaErrorInvalidValue;
+      const long long units = p.qunit_count > 0 ? p.qunit_count : all_qunits;
+      const long long work = p.causal ? (units + 1) / 2 : units;  // causal: pairs of units
       // With a streamed tail every SM takes part (the whole units fill rounds of num_sms).
       const long long ctas = p.st_ctas > 0 ? p.num_sms : std::min<long long>(work, p.num_sms > 0 ? p.num_sms : 1);
       pk<<<dim3(static_cast<unsigned>(ctas)), dim3(C::THREADS), PCfg<D>::SMEM_BYTES, stream>>>(p);
       e = cudaGetLastError();
       if (e != cudaSuccess || p.st_ctas == 0) return e;
-      const long long blocks = all_qunits - p.st_unit0;  // one per tail unit
+      const long long blocks = (all_qunits - p.st_unit0) * (2 * C::BM / 8);  // 8 rows of a tail unit each
       if (blocks <= 0 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
       // A programmatic dependent launch: the merge grid is set up while the
       // persistent kernel finishes and waits (griddepcontrol.wait) for its writes.
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-      cfg.blockDim = dim3(256);
-      cfg.dynamicSmemBytes = 0;
-      cfg.stream = stream;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-      attr[0].val.programmaticStreamSerializationAllowed = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      return cudaLaunchKernelEx(&cfg, fa_merge_stream_kernel<D, BF16>, p);
+      return launch_pdl(fa_merge_stream_kernel<D, BF16>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
     }
   }
   const long long qunits = p.qunit_count > 0 ? p.qunit_count : all_qunits;
   if (p.qunit0 < 0 || p.qunit0 + qunits > all_qunits) return cudaErrorInvalidValue;
   const long long units = qunits * p.num_splits;
   if (units <= 0 || units > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (p.launch_pdl) return launch_pdl(kern, dim3(static_cast<unsigned>(units)), dim3(C::THREADS), C::SMEM_BYTES, stream, p);
   kern<<<dim3(static_cast<unsigned>(units)), dim3(C::THREADS), C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }

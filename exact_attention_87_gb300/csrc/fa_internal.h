@@ -74,6 +74,12 @@ struct alignas(64) FwdParams {
   int st_unit0;
   int st_tiles;
   int st_ctas;
+  // Host side only: launch this kernel as a programmatic dependent of the
+  // previous kernel in the stream (it may start while that kernel's last
+  // CTAs run; it reads none of its results, and its CTAs wait for that
+  // kernel's completion before they exit, so that the stream's order of
+  // completion is kept).
+  int launch_pdl;
   // Used only by the testing build (-DFA_TESTING); zero / NULL otherwise.
   int inject;                       // 1: the producer skips the V load of tile 0
   float* stats_trace;               // [B*H*N, nkv, 2]: (m in natural-log units, l) after each K/V tile

@@ -259,6 +259,7 @@ def _tail_expectation(B, H, N, d, num_sms):
     (1, 8, 16000, 128, 152),   # 504 units (N not a multiple of 256): 3 full waves, 48 left split 3 ways
     (1, 8, 16000, 128, 148),   # 60 left, split 2 ways
     (1, 4, 10000, 128, 152),   # 160 units: 1 full wave, 8 left split 16 ways
+    (8, 12, 2000, 128, 152),   # 768 units (N not a multiple of 256: no streamed tail): 5 full waves, 8 left
     (1, 4, 16384, 256, 152),   # d = 256: 512 units of 128 rows, 3 full waves, 56 left split 2 ways
 ])
 def test_splitkv_plan_tail_on_the_host(L, B, H, N, d, num_sms):
@@ -281,12 +282,9 @@ def test_splitkv_plan_uniform_and_unsplit_on_the_host(L):
     rc, p = fa.fa_fwd_splitkv_plan(8, 32, 4096, 128, 0, 152)
     assert p == {"splits": 1, "first_split_unit": 4096, "launches": 1, "workspace_bytes": 0}
     # a short last wave whose split saves less than the launch boundary costs:
-    # d = 256, B=4 H=16 N=4096 (2048 units, 13.5 waves); d = 128, B=8 H=12
-    # N=2000 (N not a multiple of 256: no streamed tail; 768 units, 5.05 waves)
+    # d = 256, B=4 H=16 N=4096 (2048 units, 13.5 waves)
     rc, p = fa.fa_fwd_splitkv_plan(4, 16, 4096, 256, 0, 152)
     assert p == {"splits": 1, "first_split_unit": 2048, "launches": 1, "workspace_bytes": 0}
-    rc, p = fa.fa_fwd_splitkv_plan(8, 12, 2000, 128, 0, 152)
-    assert p == {"splits": 1, "first_split_unit": 768, "launches": 1, "workspace_bytes": 0}
     # d = 256: explicit counts over 64-key tiles
     rc, p = fa.fa_fwd_splitkv_plan(4, 16, 4096, 256, 8, 152)
     assert p == {"splits": 8, "first_split_unit": 0, "launches": 2,
