@@ -738,7 +738,7 @@ __device__ __forceinline__ uint32_t xbar_addr(uint32_t base, int i) {
 struct PItem {
   int bh, row0, t0, nkv0, nkv1, slot;
 };
-template <int D, bool STREAM>
+template <int D, bool STREAM, bool CAUSAL>
 __device__ __forceinline__ bool persist_item(const FwdParams& p, int units, int k, PItem& it) {
   using C = Cfg<D>;
   const int nqb = p.N / (2 * C::BM);
@@ -748,7 +748,7 @@ __device__ __forceinline__ bool persist_item(const FwdParams& p, int units, int 
   it.t0 = 0;
   it.slot = -1;
   int t1 = n;
-  if (p.causal) {
+  if (CAUSAL) {
     const long long uu = 2ll * (c + (k / 2) * static_cast<long long>(G)) + (k & 1);
     if (uu >= units) return false;
     u = static_cast<int>(uu);
@@ -772,9 +772,9 @@ __device__ __forceinline__ bool persist_item(const FwdParams& p, int units, int 
   }
   it.bh = u / nqb;
   const int w = u - it.bh * nqb;
-  const int qb = p.causal ? ((w & 1) ? w / 2 : nqb - 1 - w / 2) : w;
+  const int qb = CAUSAL ? ((w & 1) ? w / 2 : nqb - 1 - w / 2) : w;
   it.row0 = qb * 2 * C::BM;
-  if (p.causal) {
+  if (CAUSAL) {
     // Tiles per sub-tile: up to the diagonal tile of its last row.
     it.nkv0 = (it.row0 + C::BM + C::BN - 1) / C::BN;
     it.nkv1 = (it.row0 + 2 * C::BM + C::BN - 1) / C::BN;
@@ -785,7 +785,7 @@ __device__ __forceinline__ bool persist_item(const FwdParams& p, int units, int 
 }
 
 // TMA producer (one thread).
-template <int D, bool STREAM>
+template <int D, bool STREAM, bool CAUSAL>
 __device__ __forceinline__ void persist_producer(const FwdParams& p, uint32_t base, int units, const WaitCtl& ctl) {
   using C = Cfg<D>;
   tma_prefetch_desc(&p.tm_q);
@@ -797,12 +797,12 @@ __device__ __forceinline__ void persist_producer(const FwdParams& p, uint32_t ba
   int gk = 0, gv = 0; // K and V loads issued (positions in the ring sequence)
   for (int kk = 0;; ++kk) {
     PItem U;
-    if (!persist_item<D, STREAM>(p, units, kk, U)) break;
+    if (!persist_item<D, STREAM, CAUSAL>(p, units, kk, U)) break;
     const int nkv = max(U.nkv0, U.nkv1);
     // The next item's Q rows into L2 while this one runs (its load, later, then hits L2).
     {
       PItem N2;
-      if (persist_item<D, STREAM>(p, units, kk + 1, N2)) {
+      if (persist_item<D, STREAM, CAUSAL>(p, units, kk + 1, N2)) {
         const uint16_t* qn = static_cast<const uint16_t*>(p.q) + (static_cast<size_t>(N2.bh) * p.N + N2.row0) * D;
         l2_prefetch_bulk(qn, 2u * C::Q_SUB_BYTES);
       }
@@ -851,7 +851,7 @@ __device__ __forceinline__ void persist_producer(const FwdParams& p, uint32_t ba
 
 // MMA warp (whole warp; one elected lane issues): both chains' blocks of each
 // unit in turn order, with positions counted across units.
-template <int D, bool BF16, bool STREAM>
+template <int D, bool BF16, bool STREAM, bool CAUSAL>
 __device__ __forceinline__ void persist_mma(const FwdParams& p, uint32_t base, uint32_t tmem, int units,
                                             const WaitCtl& ctl) {
   using C = Cfg<D>;
@@ -859,7 +859,7 @@ __device__ __forceinline__ void persist_mma(const FwdParams& p, uint32_t base, u
   int k = 0, g = 0, gp0 = 0, gp1 = 0;  // units, K/V tiles, P products of sub-tile 0 and 1 so far
   for (;; ++k) {
     PItem U;
-    if (!persist_item<D, STREAM>(p, units, k, U)) break;
+    if (!persist_item<D, STREAM, CAUSAL>(p, units, k, U)) break;
     const int nkv = max(U.nkv0, U.nkv1);
     if (!wait_bar_warp(bar_addr<D>(base, C::B_Q), k & 1, ctl, kWhereQ)) break;
     tc_fence_after();
@@ -891,7 +891,7 @@ __device__ __forceinline__ void persist_mma(const FwdParams& p, uint32_t base, u
 
 // Softmax warpgroup of sub-tile `sub`: the tiles of each unit, then its
 // epilogue (O / l through this sub-tile's staging buffer and TMA stores; LSE).
-template <int D, bool BF16, bool STREAM>
+template <int D, bool BF16, bool STREAM, bool CAUSAL>
 __device__ __forceinline__ void persist_softmax(const FwdParams& p, uint32_t base, uint32_t tmem, int sub, int units,
                                                 const WaitCtl& ctl) {
   using C = Cfg<D>;
@@ -907,15 +907,18 @@ __device__ __forceinline__ void persist_softmax(const FwdParams& p, uint32_t bas
   int k = 0, g = 0, gs = 0;  // units, K/V tiles, S products of this sub-tile so far
   for (;; ++k) {
     PItem U;
-    if (!persist_item<D, STREAM>(p, units, k, U)) break;
+    if (!persist_item<D, STREAM, CAUSAL>(p, units, k, U)) break;
     const int nkv = max(U.nkv0, U.nkv1), nkv_s = sub ? U.nkv1 : U.nkv0;
     const int my_row = U.row0 + C::BM * sub + t;
-    const int row_end = p.causal ? min(p.N, my_row + 1) : p.N;
+    const int row_end = CAUSAL ? min(p.N, my_row + 1) : p.N;
     float m_ref = -INFINITY, l = 0.f, l_o = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv_s; ++j) {
-      if (!softmax_tile<D, BF16>(p, base, sub, t, lane, t_s, t_o, c, tau, row_end - (U.t0 + j) * C::BN, j, g + j,
-                                 gs + j, m_ref, l, l_o, ctl)) {
+      // Unmasked (N a multiple of 256): every key of every tile is valid, and
+      // the masked path of the tile is compiled out.
+      const int valid = CAUSAL ? row_end - (U.t0 + j) * C::BN : C::BN;
+      if (!softmax_tile<D, BF16>(p, base, sub, t, lane, t_s, t_o, c, tau, valid, j, g + j, gs + j, m_ref, l, l_o,
+                                 ctl)) {
         ok = false;
         break;
       }
@@ -925,7 +928,7 @@ __device__ __forceinline__ void persist_softmax(const FwdParams& p, uint32_t bas
     // Tiles of this unit only the other sub-tile uses: count this sub-tile's
     // stage releases once they have landed (their stage's previous phase is
     // then complete, so the arrivals cannot fall into it).
-    for (int jj = nkv_s; ok && jj < nkv; ++jj) {
+    for (int jj = nkv_s; CAUSAL && ok && jj < nkv; ++jj) {
       const int gg = g + jj, s = gg % C::STAGES;
       const uint32_t par = (gg / C::STAGES) & 1;
       ok = __all_sync(0xffffffffu, wait_bar(bar_addr<D>(base, C::B_KF + s), par, ctl, kWhereKFull) &&
@@ -1018,7 +1021,7 @@ __device__ __forceinline__ void persist_softmax(const FwdParams& p, uint32_t bas
   if (t == 0) tma_store_wait_all();  // every store has completed before the CTA exits
 }
 
-template <int D, bool BF16, bool STREAM>
+template <int D, bool BF16, bool STREAM, bool CAUSAL>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_persist_kernel(const __grid_constant__ FwdParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -1064,15 +1067,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_persist_kernel(cons
   if (warp >= 8) {
     warpgroup_reg_dealloc<C::LOW_REGS>();
     if (warp == C::WARP_TMA) {
-      if ((threadIdx.x & 31) == 0) persist_producer<D, STREAM>(p, base, units, ctl);
+      if ((threadIdx.x & 31) == 0) persist_producer<D, STREAM, CAUSAL>(p, base, units, ctl);
       __syncwarp();
     } else if (warp == C::WARP_MMA0) {
-      persist_mma<D, BF16, STREAM>(p, base, tmem, units, ctl);
+      persist_mma<D, BF16, STREAM, CAUSAL>(p, base, tmem, units, ctl);
       __syncwarp();
     }
   } else {
     warpgroup_reg_alloc<C::HIGH_REGS>();
-    persist_softmax<D, BF16, STREAM>(p, base, tmem, warp / 4, units, ctl);
+    persist_softmax<D, BF16, STREAM, CAUSAL>(p, base, tmem, warp / 4, units, ctl);
   }
 
   tc_fence_before();
@@ -1245,20 +1248,22 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream) {
   if (p.st_ctas > 0 && !persist_eligible<D>(p)) return cudaErrorInvalidValue;
   if constexpr (D == 128) {
     if (persist_eligible<D>(p)) {
-      // Two instantiations: without the streamed tail the kernel carries none
-      // of its code (its item walk and part epilogue cost 2-5 % of the tile
-      // rate when present, measured on GB300).
-      const bool stream_tail = p.st_ctas > 0;
-      auto pk = stream_tail ? fa_fwd_persist_kernel<D, BF16, true> : fa_fwd_persist_kernel<D, BF16, false>;
-      static std::atomic<uint64_t> pattr[2] = {0, 0};
-      if (!(pattr[stream_tail].load() & bit)) {
+      // Three instantiations: unmasked, causal, unmasked with the streamed
+      // tail. Each carries only its own code: the tail's item walk and part
+      // epilogue cost 2-5 % of the tile rate when present (measured on GB300).
+      const int variant = p.st_ctas > 0 ? 2 : p.causal ? 1 : 0;
+      auto pk = variant == 2   ? fa_fwd_persist_kernel<D, BF16, true, false>
+                : variant == 1 ? fa_fwd_persist_kernel<D, BF16, false, true>
+                               : fa_fwd_persist_kernel<D, BF16, false, false>;
+      static std::atomic<uint64_t> pattr[3] = {0, 0, 0};
+      if (!(pattr[variant].load() & bit)) {
         cudaFuncAttributes pa;
         e = cudaFuncGetAttributes(&pa, pk);
         if (e != cudaSuccess) return e;
         if (pa.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
         e = cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, PCfg<D>::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        pattr[stream_tail].fetch_or(bit);
+        pattr[variant].fetch_or(bit);
       }
       if (all_qunits <= 0 || all_qunits > 0x7fffffffLL || p.qunit_count > all_qunits) return cudaErrorInvalidValue;
       const long long units = p.qunit_count > 0 ? p.qunit_count : all_qunits;
