@@ -466,7 +466,9 @@ __device__ __forceinline__ bool softmax_tile(const FwdParams& p, uint32_t base, 
 // --------------------------------------------------------------------------
 // Softmax + lazy correction + epilogue (one warpgroup per Q sub-tile)
 // --------------------------------------------------------------------------
-template <int D, bool BF16>
+// FULL: no key of any tile is masked (no causal mask, no key lengths, a
+// multiple of 128 keys), so the masked path of the tile is compiled out.
+template <int D, bool BF16, bool FULL>
 __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, uint32_t tmem, int sub, int bh, int row0,
                                            int split, int t0, int nkv, int key_end, const WaitCtl& ctl) {
   using C = Cfg<D>;
@@ -489,8 +491,8 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
   const uint32_t b_od = bar_addr<D>(base, C::B_OD + sub);
 
   for (int j = 0; j < nkv; ++j) {
-    if (!softmax_tile<D, BF16>(p, base, sub, t, lane, t_s, t_o, c, tau, row_end - (t0 + j) * C::BN, j, j, j, m_ref, l,
-                               l_o, ctl)) {
+    const int valid = FULL ? C::BN : row_end - (t0 + j) * C::BN;
+    if (!softmax_tile<D, BF16>(p, base, sub, t, lane, t_s, t_o, c, tau, valid, j, j, j, m_ref, l, l_o, ctl)) {
       ok = false;
       break;
     }
@@ -585,7 +587,7 @@ __device__ __forceinline__ void softmax_wg(const FwdParams& p, uint32_t base, ui
   if (row < p.N) p.lse[static_cast<size_t>(bh) * p.N + row] = empty ? -INFINITY : (m_ref + lg2_approx(l)) * kLn2;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool FULL>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __grid_constant__ FwdParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -672,7 +674,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
     warpgroup_reg_alloc<C::HIGH_REGS>();
     const int sub = warp / 4;
     if (sub == 0 || has1)
-      softmax_wg<D, BF16>(p, base, tmem, sub, bh, row0, split, t0, sub ? nkv1 : nkv0, key_end, ctl);
+      softmax_wg<D, BF16, FULL>(p, base, tmem, sub, bh, row0, split, t0, sub ? nkv1 : nkv0, key_end, ctl);
   }
 
   tc_fence_before();
@@ -1227,13 +1229,16 @@ __global__ void __launch_bounds__(256) fa_merge_stream_kernel(const __grid_const
 template <int D, bool BF16>
 cudaError_t launch(const FwdParams& p, cudaStream_t stream) {
   using C = Cfg<D>;
-  auto kern = fa_fwd_f16_kernel<D, BF16>;
-  static std::atomic<uint64_t> attr_done{0};  // one bit per device ordinal (< 64)
+  // Two instantiations: every key tile full and unmasked (its masked path
+  // compiled out), or not.
+  const bool full = !p.causal && p.klen == nullptr && p.Nk % C::BN == 0;
+  auto kern = full ? fa_fwd_f16_kernel<D, BF16, true> : fa_fwd_f16_kernel<D, BF16, false>;
+  static std::atomic<uint64_t> attr_done[2] = {0, 0};  // one bit per device ordinal (< 64)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
-  if (!(attr_done.load() & bit)) {
+  if (!(attr_done[full].load() & bit)) {
     // The warpgroup register split is only valid if the CTA is launched with
     // exactly LAUNCH_REGS registers per thread; otherwise refuse to launch.
     cudaFuncAttributes fa_attr;
@@ -1242,7 +1247,7 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream) {
     if (fa_attr.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_done.fetch_or(bit);
+    attr_done[full].fetch_or(bit);
   }
   const long long all_qunits = static_cast<long long>(p.B) * p.H * ((p.N + 2 * C::BM - 1) / (2 * C::BM));
   if (p.st_ctas > 0 && !persist_eligible<D>(p)) return cudaErrorInvalidValue;
