@@ -404,7 +404,9 @@ __device__ __forceinline__ void store_acc_tile(uint32_t t_acc, uint32_t stage, i
 // Softmax warpgroup W (warps 4W .. 4W+3): queries [64W, 64W+64) of P^T and
 // dS^T; at the end dV (W = 0) or dK (W = 1)
 // --------------------------------------------------------------------------
-template <int D, bool BF16, int W>
+// FULL: no entry of any tile is masked (no causal mask, no key lengths, N a
+// multiple of 128): only the unmasked copy of the P loop is compiled.
+template <int D, bool BF16, int W, bool FULL>
 __device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint8_t* smem, uint32_t base, uint32_t tmem, int bh,
                                             int kv0, int nq, int key_end, const BCtl& ctl) {
   using C = BCfg<D>;
@@ -488,11 +490,15 @@ __device__ __forceinline__ void bwd_softmax(const BwdParams& p, uint8_t* smem, u
         if (q == 0 && W == 0 && t == 0) FA_TRACE(p, kBvSmPChunk0, i);
       }
     };
-    const bool diag = p.causal && i == 0;
-    if (diag || rest_masked)
-      p_phase(std::true_type{}, diag ? lim_diag : lim_rest);
-    else
+    if constexpr (FULL) {
       p_phase(std::false_type{}, 0);
+    } else {
+      const bool diag = p.causal && i == 0;
+      if (diag || rest_masked)
+        p_phase(std::true_type{}, diag ? lim_diag : lim_rest);
+      else
+        p_phase(std::false_type{}, 0);
+    }
     tmem_st_wait();
     tc_fence_before();
     __syncwarp();
@@ -604,7 +610,7 @@ __device__ __forceinline__ void bwd_dq(const BwdParams& p, uint32_t base, uint32
   if (t == 0) tma_store_wait_all();  // every reduce-add is complete before the CTA exits
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool FULL>
 __global__ void __launch_bounds__(BCfg<D>::THREADS, 1) fa_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   using C = BCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -693,10 +699,10 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1) fa_bwd_main_kernel(const 
     bwd_dq<D>(p, base, tmem, bh, q_first, nq, ctl);
   } else if (warp >= 4) {
     warpgroup_reg_alloc<C::SM_REGS>();
-    bwd_softmax<D, BF16, 1>(p, smem_raw, base, tmem, bh, kv0, nq, key_end, ctl);
+    bwd_softmax<D, BF16, 1, FULL>(p, smem_raw, base, tmem, bh, kv0, nq, key_end, ctl);
   } else {
     warpgroup_reg_alloc<C::SM_REGS>();
-    bwd_softmax<D, BF16, 0>(p, smem_raw, base, tmem, bh, kv0, nq, key_end, ctl);
+    bwd_softmax<D, BF16, 0, FULL>(p, smem_raw, base, tmem, bh, kv0, nq, key_end, ctl);
   }
 
   tc_fence_before();
@@ -780,13 +786,15 @@ __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const __grid_constant_
 template <int D, bool BF16>
 cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
   using C = BCfg<D>;
-  auto kern = fa_bwd_main_kernel<D, BF16>;
-  static std::atomic<uint64_t> attr_done{0};  // one bit per device ordinal (< 64)
+  // Two instantiations: no entry masked (only the unmasked P loop compiled), or not.
+  const bool full = !p.causal && p.klen == nullptr && p.N % C::BK == 0;
+  auto kern = full ? fa_bwd_main_kernel<D, BF16, true> : fa_bwd_main_kernel<D, BF16, false>;
+  static std::atomic<uint64_t> attr_done[2] = {0, 0};  // one bit per device ordinal (< 64)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
-  if (!(attr_done.load() & bit)) {
+  if (!(attr_done[full].load() & bit)) {
     // The warpgroup register split draws on the registers the CTA is launched
     // with: it is only valid at exactly LAUNCH_REGS per thread; refuse otherwise.
     cudaFuncAttributes fa_attr;
@@ -795,7 +803,7 @@ cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
     if (fa_attr.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_done.fetch_or(bit);
+    attr_done[full].fetch_or(bit);
   }
   const long long bh = static_cast<long long>(p.B) * p.H;
   const long long nt = (p.N + C::BK - 1) / C::BK;

@@ -194,7 +194,9 @@ drain:
 // --------------------------------------------------------------------------
 // Softmax + lazy correction + epilogue (warps 0-3)
 // --------------------------------------------------------------------------
-template <bool BF16>
+// FULL: no key of any tile is masked (no causal mask, no key lengths, a
+// multiple of 64 keys), so the masked path of the tile is compiled out.
+template <bool BF16, bool FULL>
 __device__ __forceinline__ void softmax256(const FwdParams& p, uint32_t base, uint32_t tmem, int bh, int row0,
                                            int split, int t0, int nkv, int key_end, const WaitCtl& ctl) {
   using C = C256;
@@ -237,7 +239,7 @@ __device__ __forceinline__ void softmax256(const FwdParams& p, uint32_t base, ui
       s[u] = __uint_as_float(sraw[0][u]);
       s[32 + u] = __uint_as_float(sraw[1][u]);
     }
-    const int valid = row_end - (t0 + j) * C::BN;  // keys of this tile this row may see
+    const int valid = FULL ? C::BN : row_end - (t0 + j) * C::BN;  // keys of this tile this row may see
     float mx = fmaxf(mx_lo, mx_hi);
     if (valid < C::BN) {
       // Masked keys become -inf and the max is taken over the rest (the
@@ -403,7 +405,7 @@ __device__ __forceinline__ void softmax256(const FwdParams& p, uint32_t base, ui
     p.lse[static_cast<size_t>(bh) * p.N + my_row] = empty ? -INFINITY : (m_ref + lg2_approx(l)) * kLn2_256;
 }
 
-template <bool BF16>
+template <bool BF16, bool FULL>
 __global__ void __launch_bounds__(C256::THREADS, 1) fa_fwd_d256_kernel(const __grid_constant__ FwdParams p) {
   using C = C256;
   extern __shared__ uint8_t smem_raw[];
@@ -470,7 +472,7 @@ __global__ void __launch_bounds__(C256::THREADS, 1) fa_fwd_d256_kernel(const __g
     mma256<BF16>(base, tmem, nkv, ctl);
     __syncwarp();
   } else {
-    softmax256<BF16>(p, base, tmem, bh, row0, split, t0, nkv, key_end, ctl);
+    softmax256<BF16, FULL>(p, base, tmem, bh, row0, split, t0, nkv, key_end, ctl);
   }
 
   tc_fence_before();
@@ -487,16 +489,19 @@ __global__ void __launch_bounds__(C256::THREADS, 1) fa_fwd_d256_kernel(const __g
 template <bool BF16>
 cudaError_t launch256(const FwdParams& p, cudaStream_t stream) {
   using C = C256;
-  auto kern = fa_fwd_d256_kernel<BF16>;
-  static std::atomic<uint64_t> attr_done{0};  // one bit per device ordinal (< 64)
+  // Two instantiations: every key tile full and unmasked (its masked path
+  // compiled out), or not.
+  const bool full = !p.causal && p.klen == nullptr && p.Nk % C::BN == 0;
+  auto kern = full ? fa_fwd_d256_kernel<BF16, true> : fa_fwd_d256_kernel<BF16, false>;
+  static std::atomic<uint64_t> attr_done[2] = {0, 0};  // one bit per device ordinal (< 64)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
-  if (!(attr_done.load() & bit)) {
+  if (!(attr_done[full].load() & bit)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_done.fetch_or(bit);
+    attr_done[full].fetch_or(bit);
   }
   const long long all_qunits = static_cast<long long>(p.B) * p.H * ((p.N + C::BM - 1) / C::BM);
   const long long qunits = p.qunit_count > 0 ? p.qunit_count : all_qunits;
