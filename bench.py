@@ -596,13 +596,16 @@ def main():
 def fwd_kernel_name(w, causal: bool = False, launches: int = 1, streamed: bool = False) -> str:
     """The forward kernel a workload's step spends its time in: at d = 128 one
     unsplit launch takes the persistent form when N is a multiple of 256
-    (512 with the causal mask) and at most 4096, and so does the streamed tail."""
+    (512 with the causal mask) and at most 4096, and so does the streamed
+    tail; at d = 64 the unmasked ones with the same N do."""
     t = "bf16" if w.dtype == "bf16" else "f16"
     if w.dtype == "f32":
         return f"fa_fwd_f32_kernel<{w.d}>"
     if w.d == 256:
         return f"fa_fwd_d256_kernel<{t}>"
     if w.d == 128 and (streamed or (launches == 1 and w.N % (512 if causal else 256) == 0 and w.N <= 4096)):
+        return f"fa_fwd_persist_kernel<{w.d},{t}>"
+    if w.d == 64 and not causal and launches == 1 and w.N % 256 == 0 and w.N <= 4096:
         return f"fa_fwd_persist_kernel<{w.d},{t}>"
     return f"fa_fwd_f16_kernel<{w.d},{t}>"
 

@@ -721,7 +721,6 @@ struct PCfg {
   static constexpr uint32_t STG_BYTES = C::Q_HALF_BYTES;  // 64 columns of a 128-row sub-tile
   static constexpr uint32_t SMEM_BYTES = OFF_STG + 2 * STG_BYTES + 1024;  // + slack to align the base
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(C::SOFTMAX_FREES_STAGES, "the persistent form frees K/V stages from the softmax warps");
 };
 
 template <int D>
@@ -940,9 +939,11 @@ __device__ __forceinline__ void persist_softmax(const FwdParams& p, uint32_t bas
         mbar_arrive(bar_addr<D>(base, C::B_KE + s));
       }
     }
-    // The unit's last P.V of this sub-tile (one commit per unit); its V stage is then free.
+    // The unit's last P.V of this sub-tile (one commit per unit); its V stage
+    // is then free (d = 64: commits behind the MMAs free the stages).
     if (ok) ok = __all_sync(0xffffffffu, wait_bar(b_od, k & 1, ctl, kWhereODone));
-    if (ok && lane == 0) mbar_arrive(bar_addr<D>(base, C::B_VE + (g + nkv_s - 1) % C::STAGES));
+    if constexpr (C::SOFTMAX_FREES_STAGES)
+      if (ok && lane == 0) mbar_arrive(bar_addr<D>(base, C::B_VE + (g + nkv_s - 1) % C::STAGES));
     // The whole warpgroup agrees before the epilogue, whose named barriers need all 128 threads.
     if (!named_bar_and(1 + sub, 128, ok)) break;
 
@@ -1036,11 +1037,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_persist_kernel(cons
 
   if (threadIdx.x == 0) {
     mbar_init(bar_addr<D>(base, C::B_Q), 1);
+    // Stage releases: one arrival per softmax warp of both sub-tiles (d = 128),
+    // or one commit per sub-tile's chain behind its MMAs (d = 64).
+    const uint32_t rel = C::SOFTMAX_FREES_STAGES ? 8u : 2u;
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar_addr<D>(base, C::B_KF + s), 1);
-      mbar_init(bar_addr<D>(base, C::B_KE + s), 8);  // one arrival per softmax warp of both sub-tiles
+      mbar_init(bar_addr<D>(base, C::B_KE + s), rel);
       mbar_init(bar_addr<D>(base, C::B_VF + s), 1);
-      mbar_init(bar_addr<D>(base, C::B_VE + s), 8);
+      mbar_init(bar_addr<D>(base, C::B_VE + s), rel);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_addr<D>(base, C::B_SF + i), 1);
@@ -1107,7 +1111,9 @@ bool persist_eligible(const FwdParams& p) {
   (void)p;
   return false;
 #else
-  if (D != 128) return false;
+  // d = 64: unmasked launches only (its stages are freed by commits, which
+  // the causal form's tiles used by one sub-tile only would not balance).
+  if (D != 128 && (D != 64 || p.causal || p.st_ctas > 0)) return false;
   if (p.st_ctas > 0) {
     const long long units = static_cast<long long>(p.B) * p.H * (p.N / (2 * Cfg<D>::BM));
     if (p.causal || p.o_part == nullptr || p.lse_part == nullptr || p.st_ctas > p.num_sms || p.st_ctas > 128 ||
@@ -1251,15 +1257,17 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream) {
   }
   const long long all_qunits = static_cast<long long>(p.B) * p.H * ((p.N + 2 * C::BM - 1) / (2 * C::BM));
   if (p.st_ctas > 0 && !persist_eligible<D>(p)) return cudaErrorInvalidValue;
-  if constexpr (D == 128) {
+  if constexpr (D == 128 || D == 64) {
     if (persist_eligible<D>(p)) {
       // Three instantiations: unmasked, causal, unmasked with the streamed
       // tail. Each carries only its own code: the tail's item walk and part
       // epilogue cost 2-5 % of the tile rate when present (measured on GB300).
       const int variant = p.st_ctas > 0 ? 2 : p.causal ? 1 : 0;
-      auto pk = variant == 2   ? fa_fwd_persist_kernel<D, BF16, true, false>
-                : variant == 1 ? fa_fwd_persist_kernel<D, BF16, false, true>
-                               : fa_fwd_persist_kernel<D, BF16, false, false>;
+      auto pk = fa_fwd_persist_kernel<D, BF16, false, false>;
+      if constexpr (D == 128) {
+        if (variant == 2) pk = fa_fwd_persist_kernel<D, BF16, true, false>;
+        if (variant == 1) pk = fa_fwd_persist_kernel<D, BF16, false, true>;
+      }
       static std::atomic<uint64_t> pattr[3] = {0, 0, 0};
       if (!(pattr[variant].load() & bit)) {
         cudaFuncAttributes pa;
@@ -1278,11 +1286,15 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream) {
       pk<<<dim3(static_cast<unsigned>(ctas)), dim3(C::THREADS), PCfg<D>::SMEM_BYTES, stream>>>(p);
       e = cudaGetLastError();
       if (e != cudaSuccess || p.st_ctas == 0) return e;
-      const long long blocks = (all_qunits - p.st_unit0) * (2 * C::BM / 8);  // 8 rows of a tail unit each
-      if (blocks <= 0 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-      // A programmatic dependent launch: the merge grid is set up while the
-      // persistent kernel finishes and waits (griddepcontrol.wait) for its writes.
-      return launch_pdl(fa_merge_stream_kernel<D, BF16>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
+      if constexpr (D == 128) {
+        const long long blocks = (all_qunits - p.st_unit0) * (2 * C::BM / 8);  // 8 rows of a tail unit each
+        if (blocks <= 0 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+        // A programmatic dependent launch: the merge grid is set up while the
+        // persistent kernel finishes and waits (griddepcontrol.wait) for its writes.
+        return launch_pdl(fa_merge_stream_kernel<D, BF16>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                          p);
+      }
+      return cudaErrorInvalidValue;
     }
   }
   const long long qunits = p.qunit_count > 0 ? p.qunit_count : all_qunits;

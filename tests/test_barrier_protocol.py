@@ -1123,6 +1123,100 @@ def test_forward_persistent_barrier_protocol(units):
         PersistModel(units, rng).run()
 
 
+class PersistCommitModel(PersistModel):
+    """The persistent form at d = 64 (unmasked units only): three K/V stages
+    freed by commits behind the MMAs instead of softmax arrivals, one commit
+    per sub-tile's S product (K) and P.V (V), so a stage's release barrier
+    counts two; the softmax warps release nothing."""
+
+    ST = 3
+
+    def __init__(self, units, rng):
+        PersistModel.__init__(self, units, rng)
+        for s in range(self.ST):
+            self.bars[f"KE{s}"] = Bar(2)
+            self.bars[f"VE{s}"] = Bar(2)
+
+    def mma(self):
+        g, gp = 0, [0, 0]
+        for k, (n0, n1) in enumerate(self.units):
+            assert n0 == n1, "the commit-freed form takes units with equal sub-tiles"
+            nkv = n0
+            yield ("wait", "Q", k)
+            for j in range(nkv + 1):
+                for sub in (0, 1):
+                    if j == 1 and k > 0:
+                        yield ("wait", f"OF{sub}", k - 1)
+                    if j > 0:
+                        gg = g + j - 1
+                        yield ("wait", f"VF{gg % self.ST}", gg // self.ST)
+                        yield ("wait", f"PF{sub}", gp[sub] + j - 1)
+                        self.issue(0, "PV", (sub, k, j - 1, gg))
+                        if j == nkv:
+                            self.commit(0, f"OD{sub}")
+                        self.commit(0, f"VE{gg % self.ST}")
+                        yield ("step",)
+                    if j < nkv:
+                        gg = g + j
+                        yield ("wait", f"KF{gg % self.ST}", gg // self.ST)
+                        self.issue(0, "S", (sub, k, j, gg))
+                        self.commit(0, f"SF{sub}")
+                        self.commit(0, f"KE{gg % self.ST}")
+                        yield ("step",)
+            g += nkv
+            gp[0] += n0
+            gp[1] += n1
+        self.commit(0, "DR")
+        yield ("wait", "DR", 0)
+
+    def softmax(self, sub, w):
+        g, gs = 0, 0
+        for k, (n0, n1) in enumerate(self.units):
+            n = n0
+            for j in range(n):
+                yield ("wait", f"SF{sub}", gs + j)
+                assert ("S", (sub, k, j, g + j)) in self.mma_done
+                self.bump(("p", sub, k), j)
+                self.bars[f"PF{sub}"].arrive()
+                if j == n - 1:
+                    self.bars["QE"].arrive()
+                yield ("step",)
+            yield ("wait", f"OD{sub}", k)
+            assert all(("PV", (sub, k, j, g + j)) in self.mma_done for j in range(n)), "epilogue before the last P.V"
+            self.o_read.add((sub, k))
+            self.bars[f"OF{sub}"].arrive()
+            yield ("step",)
+            g += n
+            gs += n
+
+
+@pytest.mark.parametrize("units", [
+    [(3, 3)], [(2, 2), (2, 2), (2, 2)], [(1, 1), (1, 1), (1, 1), (1, 1)], [(4, 4), (1, 1), (5, 5)], [(6, 6), (2, 2)],
+], ids=lambda u: "-".join(f"{a}.{b}" for a, b in u))
+def test_forward_persistent_d64_barrier_protocol(units):
+    rng = random.Random(hash(tuple(units)) ^ 0x64)
+    for _ in range(400):
+        PersistCommitModel(units, rng).run()
+
+
+def test_model_catches_a_commit_freed_stage_released_twice():
+    """Planted mistake: the softmax warps also release the stages (as at
+    d = 128) on top of the commits; a stage then completes its phase before
+    both chains have read it."""
+    class DoubleRelease(PersistCommitModel):
+        def softmax(self, sub, w):
+            g = 0
+            for req in PersistCommitModel.softmax(self, sub, w):
+                if req[0] == "wait" and req[1].startswith("SF") and w == 0:
+                    yield req
+                    self.bars[f"KE{req[2] % self.ST}"].arrive()
+                    continue
+                yield req
+    with pytest.raises(AssertionError):
+        for seed in range(300):
+            DoubleRelease([(3, 3), (2, 2), (4, 4)], random.Random(seed)).run()
+
+
 class PersistTwoWarpModel(PersistModel):
     """The persistent form with one MMA warp per sub-tile whose blocks
     alternate by turns, as in the one-unit kernel: sub-tile 0's block j >= 1
