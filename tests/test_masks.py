@@ -97,3 +97,15 @@ def test_padded_long_sequence_batch_split(causal, splits):
     if splits == 0:
         assert fa.fa_fwd_splitkv_num_splits(B, H, N, d) > 1
     check(q, k, v, "bf16", causal=causal, klen=klen, num_splits=splits)
+
+
+@pytest.mark.parametrize("B,H,N,dtype", [
+    (3, 52, 1024, "bf16"),   # 624 units: 312 heavy/light pairs, two or three per CTA
+    (2, 40, 2048, "f16"),    # 640 units of 8 Q blocks per head
+])
+def test_causal_persistent_several_pairs_per_cta(B, H, N, dtype):
+    """The persistent causal form (d = 128, N a multiple of 512): each CTA
+    walks several heavy/light pairs of Q blocks, with the barrier phases
+    carried across them; every output against the oracle."""
+    q, k, v = make_qkv(B, H, N, 128, dtype, sigma_qk=2.0, seed=42, wid=13300 + N)
+    check(q, k, v, dtype, causal=True)

@@ -25,28 +25,35 @@ def strict_lib():
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     L.fa_fwd.restype = i
+    L.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, vp]
+    L.fa_fwd_ex.restype = i
     return L
 
 
-@pytest.mark.parametrize("B,H,N,d,dtype,sig", [
-    (2, 16, 4096, 128, "bf16", 3.0),
-    (1, 8, 8192, 128, "f16", 1.0),
-    (4, 8, 1000, 64, "bf16", 1.0),
-    (3, 5, 777, 128, "f16", 2.0),
+@pytest.mark.parametrize("B,H,N,d,dtype,sig,causal", [
+    (2, 16, 4096, 128, "bf16", 3.0, False),   # the persistent form: 512 units on one CTA per SM
+    (2, 16, 4096, 128, "bf16", 3.0, True),    # its causal form: heavy/light pairs
+    (2, 16, 4096, 64, "f16", 1.0, False),     # its d = 64 form (stages freed by commits)
+    (1, 8, 8192, 128, "f16", 1.0, False),
+    (4, 8, 1000, 64, "bf16", 1.0, False),
+    (3, 5, 777, 128, "f16", 2.0, False),
 ])
-def test_default_order_equals_strict_order(strict_lib, B, H, N, d, dtype, sig):
+def test_default_order_equals_strict_order(strict_lib, B, H, N, d, dtype, sig, causal):
+    """The product build (S issued right behind the P.V that reads its
+    columns; the persistent form where it applies) against the strict-order
+    build (one CTA per unit, every P.V waited for): bit for bit."""
     q, k, v = (t.cuda() for t in make_qkv(B, H, N, d, dtype, sigma_qk=sig, seed=21, wid=9000 + N))
-    o1, l1 = fa.attention(q, k, v)
+    o1, l1 = fa.attention(q, k, v, causal=causal)
     o2, l2 = torch.empty_like(o1), torch.empty_like(l1)
     code = fa.FA_BF16 if dtype == "bf16" else fa.FA_F16
     stream = torch.cuda.current_stream().cuda_stream
     for _ in range(3):
-        rc = strict_lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o2.data_ptr(), l2.data_ptr(),
-                               B, H, N, d, 1.0 / d ** 0.5, code, stream)
+        rc = strict_lib.fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o2.data_ptr(), l2.data_ptr(),
+                                  B, H, N, d, 1.0 / d ** 0.5, code, int(causal), None, stream)
         assert rc == fa.FA_OK
         torch.cuda.synchronize()
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
-        o1, l1 = fa.attention(q, k, v)
+        o1, l1 = fa.attention(q, k, v, causal=causal)
 
 
 @pytest.mark.parametrize("B,H,N,d,dtype,sig", [

@@ -142,6 +142,21 @@ def test_fp32_output_small_shapes_strict_gate(d, dtype):
     assert np.all(lerr <= TOL[dtype]["lse_rel"] * np.maximum(1.0, np.abs(lse_ref)))
 
 
+@pytest.mark.parametrize("B,H,N,d,dtype", [
+    (4, 40, 1024, 64, "bf16"),    # 640 units on one CTA per SM: four or five per CTA
+    (3, 52, 1024, 64, "f16"),
+    (3, 52, 1024, 128, "f16"),
+])
+def test_persistent_several_units_per_cta(B, H, N, d, dtype):
+    """The persistent form (d = 64 and 128, N a multiple of 256): each CTA
+    walks several units with the barrier phases carried across them; every
+    output against the oracle, keys in rising-norm order with sigma 3 so
+    that rows rescale across units' boundaries too."""
+    q, k, v = make_qkv(B, H, N, d, dtype, sigma_qk=3.0, seed=12, wid=4100 + N + d + H)
+    k, v = rising_norm_order(k, v)
+    check(q, k, v, dtype)
+
+
 def test_non_default_scale():
     q, k, v = make_qkv(1, 2, 300, 128, "bf16", seed=3, wid=4000)
     check(q, k, v, "bf16", scale=0.3)
