@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -89,11 +90,19 @@ def sustained_leg(step, flops_per_step: float, stream, dev, barrier, seconds: fl
             "clocks": sampler.summary()}
 
 
+def code_of(text: str) -> str:
+    """A source file's code without its comments and blank lines: the traffic
+    recorded for a kernel stays valid across edits of its comments only."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_hash(kind: str = "fwd") -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[kind]:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(code_of(f.read()).encode())
     return h.hexdigest()[:16]
 
 

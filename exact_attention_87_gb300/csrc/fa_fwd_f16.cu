@@ -699,7 +699,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
 }
 
 // ==========================================================================
-// Persistent form (d = 128; no split, no key lengths, N a multiple of 256):
+// Persistent form (d = 128, unmasked or causal, and unmasked d = 64; no
+// key-range split, no key lengths, N a multiple of 256, at most 4096):
 // one CTA per SM walks the work units blockIdx.x, blockIdx.x + G, ... (G
 // CTAs), so a unit's Q and first K/V tiles load while the previous unit's
 // last tiles and epilogue run, instead of paying a CTA's start and end per
@@ -710,7 +711,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
 // has completed), and O_i has been read out by the epilogue (the next unit's
 // first P.V overwrites it). The epilogue stages O in 64-column halves through
 // a 16 KB buffer of each sub-tile, since the Q buffer already holds the next
-// unit's Q.
+// unit's Q. Separate instantiations for unmasked, causal and streamed-tail
+// launches carry only their own code (the kernels' speed depends on their
+// size); the unmasked ones compile the key mask out.
 // ==========================================================================
 template <int D>
 struct PCfg {
