@@ -123,6 +123,35 @@ def test_backward_deterministic(d):
         assert (dq.float() - ref[0].float()).abs().max().item() <= 1e-2 * ref[0].float().abs().max().item()
 
 
+@pytest.mark.parametrize("B,H,N,d,dtype", [(4, 20, 512, 128, "bf16"), (3, 16, 768, 64, "f16"), (2, 41, 256, 128, "f16")])
+def test_backward_more_key_tiles_than_sms(B, H, N, d, dtype):
+    """320, 288 and 164 key tiles: more CTAs than a 152-SM device holds at once
+    (one CTA per SM), so later waves start on SMs whose previous CTA left TMEM,
+    barriers and shared memory behind."""
+    check(B, H, N, d, dtype, 2.0, wid=8450 + N + d)
+
+
+@pytest.mark.parametrize("B,H,N,d", [(4, 20, 512, 128), (3, 16, 768, 64), (8, 32, 4096, 128)])
+def test_backward_full_tile_instantiation_matches_the_masked_one(B, H, N, d):
+    """With no mask and N a multiple of 128 the backward runs the instantiation
+    that compiles only the unmasked copy of the P loop; a key-length array of
+    all N selects the masked instantiation, in which nothing is masked. Both
+    compute each key tile's products in the same order: dK and dV must be
+    bit-identical, dQ (fp32 reduce-adds in a varying order) equal to fp32
+    rounding. The last shape is the benchmark's workload."""
+    q, k, v = (t.cuda() for t in make_qkv(B, H, N, d, "bf16", sigma_qk=3.0, seed=5, wid=8500 + d))
+    do = make_dout(B, H, N, d, "bf16", seed=5, wid=8500 + d).cuda()
+    o, lse = fa.attention(q, k, v)
+    a = fa.attention_backward(q, k, v, o, lse, do)
+    kl = torch.full((B,), N, dtype=torch.int32, device="cuda")
+    b = fa.attention_backward(q, k, v, o, lse, do, seqlens_k=kl)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    err = (a[0].float() - b[0].float()).abs().max().item()
+    assert err <= 1e-2 * b[0].float().abs().max().item()
+
+
 def test_backward_reuses_workspace_and_outputs():
     """A caller workspace and preallocated outputs holding garbage give the same result."""
     B, H, N, d = 1, 2, 300, 64
