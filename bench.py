@@ -39,9 +39,10 @@ COMMON_SOURCES = ["exact_attention_87_gb300/csrc/sm103_ptx.cuh", "exact_attentio
 KERNEL_SOURCES = {
     "fwd": ["exact_attention_87_gb300/csrc/fa_fwd_f16.cu"] + COMMON_SOURCES,
     "fwd_d256": ["exact_attention_87_gb300/csrc/fa_fwd_d256.cu"] + COMMON_SOURCES,
-    "bwd": ["exact_attention_87_gb300/csrc/fa_bwd_f16.cu"] + COMMON_SOURCES,
-    "bwd_d256": ["exact_attention_87_gb300/csrc/fa_bwd_f16.cu", "exact_attention_87_gb300/csrc/fa_bwd_d256.cu"]
+    "bwd": ["exact_attention_87_gb300/csrc/fa_bwd_f16.cu", "exact_attention_87_gb300/csrc/fa_bwd_order.cuh"]
     + COMMON_SOURCES,
+    "bwd_d256": ["exact_attention_87_gb300/csrc/fa_bwd_f16.cu", "exact_attention_87_gb300/csrc/fa_bwd_d256.cu",
+                 "exact_attention_87_gb300/csrc/fa_bwd_order.cuh"] + COMMON_SOURCES,
 }
 
 

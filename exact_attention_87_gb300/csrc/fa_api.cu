@@ -17,6 +17,9 @@
 #include "fa_testing.h"
 #endif
 #include "fa_internal.h"
+#ifdef FA_TESTING
+#include "fa_bwd_order.cuh"
+#endif
 
 // Device status word of this module: [0] flags (kStatusTimeout), [1] where the
 // first timeout happened. Kernels receive its address as a parameter.
@@ -887,6 +890,17 @@ int fa_testing_stream_piece(int tiles, int ctas, int n, int c, int q, int* out) 
   out[1] = pc.t0;
   out[2] = pc.t1;
   out[3] = pc.slot;
+  return 1;
+}
+
+int fa_testing_bwd_tile(int B, int H, int N, int d, int causal, int cta, int* out) {
+  if (!out || B < 1 || H < 1 || N < 1 || (d != 64 && d != 128 && d != 256)) return -1;
+  const long long nt = (static_cast<long long>(N) + 127) / 128;
+  const long long ctas = static_cast<long long>(B) * H * nt;
+  if (ctas >= (1ll << 31) || cta < 0 || cta >= ctas) return -1;
+  const fa::BwdTileOf t = fa::bwd_tile_of(cta, B * H, static_cast<int>(nt), N, d, causal != 0);
+  out[0] = t.bh;
+  out[1] = t.kt;
   return 1;
 }
 

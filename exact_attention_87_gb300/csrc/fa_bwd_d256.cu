@@ -60,6 +60,7 @@
 #include <atomic>
 #include <type_traits>
 
+#include "fa_bwd_order.cuh"
 #include "fa_device_common.cuh"
 
 namespace fa {
@@ -156,8 +157,9 @@ struct KeyTile {
 __device__ __forceinline__ KeyTile key_tile(const BwdParams& p) {
   KeyTile k;
   const int nt = (p.N + B256::BK - 1) / B256::BK;
-  k.bh = blockIdx.x / nt;
-  k.kv0 = (blockIdx.x % nt) * B256::BK;
+  const BwdTileOf tile = bwd_tile_of(static_cast<int>(blockIdx.x), p.B * p.H, nt, p.N, B256::D, p.causal != 0);
+  k.bh = tile.bh;
+  k.kv0 = tile.kt * B256::BK;
   k.key_end = p.klen != nullptr ? min(max(p.klen[k.bh / p.H], 0), p.N) : p.N;
   k.q_first = p.causal ? k.kv0 / B256::BQ : 0;
   k.nq = k.kv0 < k.key_end ? (p.N + B256::BQ - 1) / B256::BQ - k.q_first : 0;

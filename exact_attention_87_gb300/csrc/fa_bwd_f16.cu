@@ -62,6 +62,7 @@
 
 #include <cuda_fp16.h>
 
+#include "fa_bwd_order.cuh"
 #include "fa_device_common.cuh"
 
 namespace fa {
@@ -623,11 +624,12 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1) fa_bwd_main_kernel(const 
   }
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem_raw + C::OFF_MISC);
   const int warp = threadIdx.x >> 5;
-  // Consecutive CTAs take consecutive key tiles of one head, so that head's
-  // Q, dO and row statistics are read from L2 by all of them.
+  // This CTA's head and key tile (fa_bwd_order.cuh: a head's key tiles in a
+  // row; with the causal mask, longest first within windows of heads).
   const int nt = (p.N + C::BK - 1) / C::BK;
-  const int bh = blockIdx.x / nt;
-  const int kv0 = (blockIdx.x % nt) * C::BK;
+  const BwdTileOf tile = bwd_tile_of(static_cast<int>(blockIdx.x), p.B * p.H, nt, p.N, D, p.causal != 0);
+  const int bh = tile.bh;
+  const int kv0 = tile.kt * C::BK;
   int key_end = p.N;
   if (p.klen != nullptr) key_end = min(max(p.klen[bh / p.H], 0), p.N);
   // With the causal mask, Q tiles before the diagonal one (BQ == BK) see none

@@ -48,6 +48,8 @@ def lib():
         L.fa_testing_last_timeout_where.restype = ctypes.c_uint
         L.fa_testing_stream_piece.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]
         L.fa_testing_stream_piece.restype = i
+        L.fa_testing_bwd_tile.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]
+        L.fa_testing_bwd_tile.restype = i
         _lib = L
     return _lib
 
@@ -145,6 +147,13 @@ def device_status(stream=None) -> int:
 
 def last_timeout_where() -> int:
     return lib().fa_testing_last_timeout_where()
+
+
+def bwd_tile(B: int, H: int, N: int, d: int, causal: bool, cta: int):
+    """fa_testing_bwd_tile: (rc, (b*h, key tile)) of backward CTA `cta`."""
+    out = (ctypes.c_int * 2)()
+    rc = lib().fa_testing_bwd_tile(B, H, N, d, int(causal), cta, out)
+    return rc, (out[0], out[1])
 
 
 def stream_piece(tiles: int, ctas: int, n: int, c: int, q: int):

@@ -93,6 +93,17 @@ unsigned int fa_testing_last_timeout_where(void);
  */
 int fa_testing_stream_piece(int tiles, int ctas, int n, int c, int q, int *out);
 
+/*
+ * The key tile CTA `cta` of the backward's main kernels takes (host copy of
+ * the device arithmetic): out[0] = b*h, out[1] = key tile (128 keys each at
+ * every d). Without the causal mask a head's
+ * key tiles come in a row; with it, longest first within windows of heads
+ * whose Q, dO and fp32 dQ accumulator (8 N d bytes per head) fit 64 MiB.
+ * Requires B, H, N >= 1, d in {64, 128, 256}, 0 <= cta < B*H*ceil(N/128)
+ * < 2^31; returns 1, or -1 for arguments outside that (out untouched).
+ */
+int fa_testing_bwd_tile(int B, int H, int N, int d, int causal, int cta, int *out);
+
 #ifdef __cplusplus
 }
 #endif
