@@ -37,8 +37,10 @@ COMMON_SOURCES = ["exact_attention_87_gb300/csrc/sm103_ptx.cuh", "exact_attentio
                   "exact_attention_87_gb300/csrc/fa_internal.h"]
 # The source files of the kernel each timed path spends its time in.
 KERNEL_SOURCES = {
-    "fwd": ["exact_attention_87_gb300/csrc/fa_fwd_f16.cu"] + COMMON_SOURCES,
-    "fwd_d256": ["exact_attention_87_gb300/csrc/fa_fwd_d256.cu"] + COMMON_SOURCES,
+    "fwd": ["exact_attention_87_gb300/csrc/fa_fwd_f16.cu", "exact_attention_87_gb300/csrc/fa_fwd_order.cuh"]
+    + COMMON_SOURCES,
+    "fwd_d256": ["exact_attention_87_gb300/csrc/fa_fwd_d256.cu", "exact_attention_87_gb300/csrc/fa_fwd_order.cuh"]
+    + COMMON_SOURCES,
     "bwd": ["exact_attention_87_gb300/csrc/fa_bwd_f16.cu", "exact_attention_87_gb300/csrc/fa_bwd_order.cuh"]
     + COMMON_SOURCES,
     "bwd_d256": ["exact_attention_87_gb300/csrc/fa_bwd_f16.cu", "exact_attention_87_gb300/csrc/fa_bwd_d256.cu",

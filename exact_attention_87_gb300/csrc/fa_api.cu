@@ -19,6 +19,7 @@
 #include "fa_internal.h"
 #ifdef FA_TESTING
 #include "fa_bwd_order.cuh"
+#include "fa_fwd_order.cuh"
 #endif
 
 // Device status word of this module: [0] flags (kStatusTimeout), [1] where the
@@ -901,6 +902,18 @@ int fa_testing_bwd_tile(int B, int H, int N, int d, int causal, int cta, int* ou
   const fa::BwdTileOf t = fa::bwd_tile_of(cta, B * H, static_cast<int>(nt), N, d, causal != 0);
   out[0] = t.bh;
   out[1] = t.kt;
+  return 1;
+}
+
+int fa_testing_fwd_unit(int B, int H, int N, int d, int causal, int unit, int* out) {
+  if (!out || B < 1 || H < 1 || N < 1 || (d != 64 && d != 128 && d != 256)) return -1;
+  const long long rows = d == 256 ? 128 : 256;
+  const long long nqb = (static_cast<long long>(N) + rows - 1) / rows;
+  const long long units = static_cast<long long>(B) * H * nqb;
+  if (units >= (1ll << 31) || unit < 0 || unit >= units) return -1;
+  const fa::FwdUnitOf u = fa::fwd_unit_of(unit, B * H, static_cast<int>(nqb), N, d, causal != 0);
+  out[0] = u.bh;
+  out[1] = u.qb;
   return 1;
 }
 

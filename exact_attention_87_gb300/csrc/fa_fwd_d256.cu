@@ -27,6 +27,7 @@
 #include <atomic>
 
 #include "fa_device_common.cuh"
+#include "fa_fwd_order.cuh"
 
 namespace fa {
 namespace {
@@ -413,19 +414,19 @@ __global__ void __launch_bounds__(C256::THREADS, 1) fa_fwd_d256_kernel(const __g
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem_raw + (base - raw) + C::OFF_MISC);
   const int warp = threadIdx.x >> 5;
-  // Work unit: (batch*head, 128-row Q tile, key range); consecutive units
-  // share a head so its K/V stay in L2 while its Q tiles are processed.
+  // Work unit: (batch*head, 128-row Q tile, key range), in the order of
+  // fa_fwd_order.cuh: a head's Q tiles in a row; causal launches over every
+  // unit unsplit, longest first within windows of heads. Split launches keep
+  // the natural order, in which the units of the split-KV tail plan (the
+  // last ones) hold the last rows: its merge and partial buffers cover the
+  // rows from merge_row0 on.
   const int nqb = (p.N + C::BM - 1) / C::BM;
   const int split = blockIdx.x % p.num_splits;
   const int qunit = p.qunit0 + blockIdx.x / p.num_splits;
-  const int bh = qunit / nqb;
-  // Causal, one launch over every unit unsplit: Q tiles later in the sequence
-  // see more keys; they are launched first. Split launches keep the natural
-  // order, in which the units of the split-KV tail plan (the last ones) hold
-  // the last rows: its merge and partial buffers cover the rows from
-  // merge_row0 on.
   const bool heavy_first = p.causal && p.num_splits == 1 && p.qunit_count == 0;
-  const int qb = heavy_first ? nqb - 1 - qunit % nqb : qunit % nqb;
+  const FwdUnitOf unit = fwd_unit_of(qunit, p.B * p.H, nqb, p.Nk, 256, heavy_first);
+  const int bh = unit.bh;
+  const int qb = unit.qb;
   const int row0 = qb * C::BM;
   // Keys this unit may see: [0, key_end); causal limits the tile to its own last row.
   const int key_end = p.klen ? max(0, min(p.Nk, p.klen[bh / p.H])) : p.Nk;

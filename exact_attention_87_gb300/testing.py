@@ -50,6 +50,8 @@ def lib():
         L.fa_testing_stream_piece.restype = i
         L.fa_testing_bwd_tile.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]
         L.fa_testing_bwd_tile.restype = i
+        L.fa_testing_fwd_unit.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]
+        L.fa_testing_fwd_unit.restype = i
         _lib = L
     return _lib
 
@@ -153,6 +155,13 @@ def bwd_tile(B: int, H: int, N: int, d: int, causal: bool, cta: int):
     """fa_testing_bwd_tile: (rc, (b*h, key tile)) of backward CTA `cta`."""
     out = (ctypes.c_int * 2)()
     rc = lib().fa_testing_bwd_tile(B, H, N, d, int(causal), cta, out)
+    return rc, (out[0], out[1])
+
+
+def fwd_unit(B: int, H: int, N: int, d: int, causal: bool, unit: int):
+    """fa_testing_fwd_unit: (rc, (b*h, Q block)) of forward work unit `unit`."""
+    out = (ctypes.c_int * 2)()
+    rc = lib().fa_testing_fwd_unit(B, H, N, d, int(causal), unit, out)
     return rc, (out[0], out[1])
 
 

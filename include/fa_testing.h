@@ -104,6 +104,17 @@ int fa_testing_stream_piece(int tiles, int ctas, int n, int c, int q, int *out);
  */
 int fa_testing_bwd_tile(int B, int H, int N, int d, int causal, int cta, int *out);
 
+/*
+ * The work unit the one-CTA-per-unit forward kernels give unit number `unit`
+ * of an unsplit launch over every unit (host copy of the device arithmetic):
+ * out[0] = b*h, out[1] = Q block (256 rows at d = 64 / 128, 128 at d = 256).
+ * Unmasked, a head's Q blocks come in a row; causal, longest first within
+ * windows of heads whose K and V (4 N d bytes per head) fit 64 MiB.
+ * Requires B, H, N >= 1, d in {64, 128, 256}, 0 <= unit < B*H*(Q blocks)
+ * < 2^31; returns 1, or -1 for arguments outside that (out untouched).
+ */
+int fa_testing_fwd_unit(int B, int H, int N, int d, int causal, int unit, int *out);
+
 #ifdef __cplusplus
 }
 #endif

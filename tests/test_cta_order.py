@@ -1,4 +1,5 @@
-"""The order in which the backward's main kernels take key tiles (no GPU).
+"""The order in which the backward's main kernels take key tiles, and the
+one-CTA-per-unit forward kernels their work units (no GPU).
 
 Definition (include/fa_testing.h, fa_testing_bwd_tile): CTA c of the
 B*H*ceil(N/128) CTAs takes one (b*h, key tile). Without the causal mask a
@@ -75,3 +76,59 @@ def test_backward_tile_argument_errors():
     assert fat.bwd_tile(1, 1, 128, 128, 0, 1)[0] == -1      # one key tile: CTA 1 does not exist
     assert fat.bwd_tile(1, 1, 128, 128, 1, -1)[0] == -1
     assert fat.bwd_tile(65536, 65536, 4096, 128, 0, 0)[0] == -1   # 2^37 CTAs
+
+
+# ---------------------------------------------------------------------------
+# The forward's one-CTA-per-unit kernels (fa_testing_fwd_unit): unit u of an
+# unsplit launch over every unit takes one (b*h, Q block). Without the causal
+# mask a head's Q blocks come in a row (u = bh * nqb + qb). With it, Q block
+# qb sees qb + 1 blocks' worth of keys, and units are dealt out longest first
+# within windows of W heads, W = clamp(64 MiB // (4 N d), 1, B*H): window w
+# holds heads [w W, w W + g), g = min(W, B*H - w W), and its position j takes
+# Q block nqb - 1 - j // g of head w W + j % g.
+# ---------------------------------------------------------------------------
+def expected_fwd(B, H, N, d, causal):
+    rows = 128 if d == 256 else 256
+    nqb = -(-N // rows)
+    bhn = B * H
+    if not causal:
+        return [(bh, qb) for bh in range(bhn) for qb in range(nqb)]
+    W = max(1, min(bhn, (64 << 20) // (4 * N * d)))
+    order = []
+    for h0 in range(0, bhn, W):
+        g = min(W, bhn - h0)
+        for j in range(nqb):
+            order += [(h0 + x, nqb - 1 - j) for x in range(g)]
+    return order
+
+
+FWD_SHAPES = [
+    (8, 32, 4096, 128),   # 32 heads a window (the persistent kernel takes this shape; the order is the fallback's)
+    (1, 8, 16384, 128),   # 8 heads: all in one window
+    (8, 32, 4096, 64),    # 64
+    (4, 16, 4096, 256),   # 16 heads, 128-row Q tiles
+    (3, 7, 1000, 128),    # ragged N, all 21 heads in one window
+    (2, 3, 65536, 128),   # 2 heads a window, the last window 2
+    (1, 1, 1, 64),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("B,H,N,d", FWD_SHAPES)
+def test_forward_unit_order_matches_the_definition(B, H, N, d, causal):
+    want = expected_fwd(B, H, N, d, causal)
+    n = len(want)
+    idx = range(n) if n <= 4096 else sorted({*range(0, n, 89), *range(n - 300, n), *range(300)})
+    for u in idx:
+        rc, got = fat.fwd_unit(B, H, N, d, causal, u)
+        assert rc == 1 and got == want[u], (u, got, want[u])
+    rows = 128 if d == 256 else 256
+    assert sorted(want) == [(bh, qb) for bh in range(B * H) for qb in range(-(-N // rows))]
+
+
+def test_forward_unit_argument_errors():
+    assert fat.fwd_unit(0, 1, 256, 128, 0, 0)[0] == -1
+    assert fat.fwd_unit(1, 1, 256, 96, 0, 0)[0] == -1
+    assert fat.fwd_unit(1, 1, 256, 128, 1, 1)[0] == -1     # one 256-row block: unit 1 does not exist
+    assert fat.fwd_unit(1, 1, 256, 256, 1, 1)[0] == 1      # two 128-row tiles at d = 256
+    assert fat.fwd_unit(1, 1, 256, 128, 0, -1)[0] == -1

@@ -27,11 +27,13 @@ def L():
 
 
 def _qblock(u, nqb, causal, num_splits, qunit_count):
-    """The Q block of work unit u, restated from the kernels: under the causal
-    mask a launch over every unit unsplit takes the heavy (late) blocks
-    first; every split launch keeps the natural order."""
+    """The Q block of work unit u of a split launch, restated from the
+    kernels: every split launch keeps the natural order. (Only a causal
+    launch over every unit unsplit reorders its units, longest first within
+    windows of heads; test_cta_order.py checks that order.)"""
     heavy_first = causal and num_splits == 1 and qunit_count == 0
-    return nqb - 1 - u % nqb if heavy_first else u % nqb
+    assert not heavy_first, "the split launches checked here keep the natural order"
+    return u % nqb
 
 
 def _qrows(d):
