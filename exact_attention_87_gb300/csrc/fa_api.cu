@@ -905,13 +905,13 @@ int fa_testing_bwd_tile(int B, int H, int N, int d, int causal, int cta, int* ou
   return 1;
 }
 
-int fa_testing_fwd_unit(int B, int H, int N, int d, int causal, int unit, int* out) {
-  if (!out || B < 1 || H < 1 || N < 1 || (d != 64 && d != 128 && d != 256)) return -1;
+int fa_testing_fwd_unit(int B, int H, int N, int d, int causal, int num_sms, int unit, int* out) {
+  if (!out || B < 1 || H < 1 || N < 1 || num_sms < 0 || (d != 64 && d != 128 && d != 256)) return -1;
   const long long rows = d == 256 ? 128 : 256;
   const long long nqb = (static_cast<long long>(N) + rows - 1) / rows;
   const long long units = static_cast<long long>(B) * H * nqb;
   if (units >= (1ll << 31) || unit < 0 || unit >= units) return -1;
-  const fa::FwdUnitOf u = fa::fwd_unit_of(unit, B * H, static_cast<int>(nqb), N, d, causal != 0);
+  const fa::FwdUnitOf u = fa::fwd_unit_of(unit, B * H, static_cast<int>(nqb), N, d, causal != 0, num_sms);
   out[0] = u.bh;
   out[1] = u.qb;
   return 1;

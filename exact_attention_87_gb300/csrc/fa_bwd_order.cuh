@@ -36,10 +36,12 @@ __host__ __device__ inline BwdTileOf bwd_tile_of(int cta, int bhn, int nt, int N
     r.kt = cta - r.bh * nt;
     return r;
   }
-  long long w = kBwdWindowBytes / (8ll * N * d);
-  if (w < 1) w = 1;
-  if (w > bhn) w = bhn;
-  const int win = static_cast<int>(w);
+  // 32-bit division only (a 64-bit one is a long routine on the device)
+  const long long per_head = 8ll * N * d;
+  int win = per_head >= kBwdWindowBytes
+                ? 1
+                : static_cast<int>(static_cast<unsigned>(kBwdWindowBytes) / static_cast<unsigned>(per_head));
+  if (win > bhn) win = bhn;
   const int h0 = cta / (win * nt) * win;        // first head of this CTA's window
   const int g = bhn - h0 < win ? bhn - h0 : win;  // heads in the window
   const int c = cta - h0 * nt;                    // position within the window

@@ -607,7 +607,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_fwd_f16_kernel(const __
   const int split = blockIdx.x % p.num_splits;
   const int qunit = p.qunit0 + blockIdx.x / p.num_splits;
   const bool heavy_first = p.causal && p.num_splits == 1 && p.qunit_count == 0;
-  const FwdUnitOf unit = fwd_unit_of(qunit, p.B * p.H, nqb, p.Nk, D, heavy_first);
+  const FwdUnitOf unit = fwd_unit_of(qunit, p.B * p.H, nqb, p.Nk, D, heavy_first, p.num_sms);
   const int bh = unit.bh;
   const int qb = unit.qb;
   const int row0 = qb * 2 * C::BM;

@@ -50,7 +50,7 @@ def lib():
         L.fa_testing_stream_piece.restype = i
         L.fa_testing_bwd_tile.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]
         L.fa_testing_bwd_tile.restype = i
-        L.fa_testing_fwd_unit.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]
+        L.fa_testing_fwd_unit.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]
         L.fa_testing_fwd_unit.restype = i
         _lib = L
     return _lib
@@ -158,10 +158,10 @@ def bwd_tile(B: int, H: int, N: int, d: int, causal: bool, cta: int):
     return rc, (out[0], out[1])
 
 
-def fwd_unit(B: int, H: int, N: int, d: int, causal: bool, unit: int):
+def fwd_unit(B: int, H: int, N: int, d: int, causal: bool, unit: int, num_sms: int = 0):
     """fa_testing_fwd_unit: (rc, (b*h, Q block)) of forward work unit `unit`."""
     out = (ctypes.c_int * 2)()
-    rc = lib().fa_testing_fwd_unit(B, H, N, d, int(causal), unit, out)
+    rc = lib().fa_testing_fwd_unit(B, H, N, d, int(causal), num_sms, unit, out)
     return rc, (out[0], out[1])
 
 

@@ -109,11 +109,13 @@ int fa_testing_bwd_tile(int B, int H, int N, int d, int causal, int cta, int *ou
  * of an unsplit launch over every unit (host copy of the device arithmetic):
  * out[0] = b*h, out[1] = Q block (256 rows at d = 64 / 128, 128 at d = 256).
  * Unmasked, a head's Q blocks come in a row; causal, longest first within
- * windows of heads whose K and V (4 N d bytes per head) fit 64 MiB.
- * Requires B, H, N >= 1, d in {64, 128, 256}, 0 <= unit < B*H*(Q blocks)
- * < 2^31; returns 1, or -1 for arguments outside that (out untouched).
+ * windows of heads whose K and V (4 N d bytes per head) fit 64 MiB, or,
+ * when every unit fits on the device's num_sms SMs at once (num_sms > 0),
+ * longest first within each head. Requires B, H, N >= 1, d in {64, 128,
+ * 256}, num_sms >= 0, 0 <= unit < B*H*(Q blocks) < 2^31; returns 1, or -1
+ * for arguments outside that (out untouched).
  */
-int fa_testing_fwd_unit(int B, int H, int N, int d, int causal, int unit, int *out);
+int fa_testing_fwd_unit(int B, int H, int N, int d, int causal, int num_sms, int unit, int *out);
 
 #ifdef __cplusplus
 }

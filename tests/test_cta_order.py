@@ -85,14 +85,18 @@ def test_backward_tile_argument_errors():
 # qb sees qb + 1 blocks' worth of keys, and units are dealt out longest first
 # within windows of W heads, W = clamp(64 MiB // (4 N d), 1, B*H): window w
 # holds heads [w W, w W + g), g = min(W, B*H - w W), and its position j takes
-# Q block nqb - 1 - j // g of head w W + j % g.
+# Q block nqb - 1 - j // g of head w W + j % g; a launch whose units all fit
+# on the device's SMs at once (num_sms > 0, units <= num_sms) takes them
+# longest first within each head (u -> head u // nqb, block nqb - 1 - u % nqb).
 # ---------------------------------------------------------------------------
-def expected_fwd(B, H, N, d, causal):
+def expected_fwd(B, H, N, d, causal, num_sms=0):
     rows = 128 if d == 256 else 256
     nqb = -(-N // rows)
     bhn = B * H
     if not causal:
         return [(bh, qb) for bh in range(bhn) for qb in range(nqb)]
+    if 0 < num_sms and bhn * nqb <= num_sms:
+        return [(bh, nqb - 1 - qb) for bh in range(bhn) for qb in range(nqb)]
     W = max(1, min(bhn, (64 << 20) // (4 * N * d)))
     order = []
     for h0 in range(0, bhn, W):
@@ -113,14 +117,15 @@ FWD_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("num_sms", [0, 152])
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
-@pytest.mark.parametrize("B,H,N,d", FWD_SHAPES)
-def test_forward_unit_order_matches_the_definition(B, H, N, d, causal):
-    want = expected_fwd(B, H, N, d, causal)
+@pytest.mark.parametrize("B,H,N,d", FWD_SHAPES + [(1, 4, 512, 64), (2, 19, 1024, 128)])
+def test_forward_unit_order_matches_the_definition(B, H, N, d, causal, num_sms):
+    want = expected_fwd(B, H, N, d, causal, num_sms)
     n = len(want)
     idx = range(n) if n <= 4096 else sorted({*range(0, n, 89), *range(n - 300, n), *range(300)})
     for u in idx:
-        rc, got = fat.fwd_unit(B, H, N, d, causal, u)
+        rc, got = fat.fwd_unit(B, H, N, d, causal, u, num_sms)
         assert rc == 1 and got == want[u], (u, got, want[u])
     rows = 128 if d == 256 else 256
     assert sorted(want) == [(bh, qb) for bh in range(B * H) for qb in range(-(-N // rows))]
@@ -132,3 +137,4 @@ def test_forward_unit_argument_errors():
     assert fat.fwd_unit(1, 1, 256, 128, 1, 1)[0] == -1     # one 256-row block: unit 1 does not exist
     assert fat.fwd_unit(1, 1, 256, 256, 1, 1)[0] == 1      # two 128-row tiles at d = 256
     assert fat.fwd_unit(1, 1, 256, 128, 0, -1)[0] == -1
+    assert fat.fwd_unit(1, 1, 256, 128, 0, 0, -1)[0] == -1  # negative SM count
